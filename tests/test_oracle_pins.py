@@ -1,0 +1,319 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Each test targets a mistake the oracle could plausibly contain (a wrong sign,
+a transposed operand, a dropped term, a wrong bit order).  CPU only."""
+import math
+import os
+
+import numpy as np
+import pytest
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+# ------------------------------------------------------------- SplitMix64
+def test_splitmix64_published_outputs(oracle):
+    # First outputs of SplitMix64 seeded with 0 (Steele, Lea & Flood 2014; the
+    # values printed with the public reference implementation).
+    r = oracle.SplitMix64(0)
+    assert [r.next() for _ in range(3)] == [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4,
+                                            0x06C45D188009454F]
+
+
+def test_uniform_pm1_range(oracle):
+    r = oracle.SplitMix64(7)
+    u = np.array([r.uniform_pm1() for _ in range(20000)])
+    assert u.min() >= -1.0 and u.max() < 1.0
+    assert abs(u.mean()) < 0.02 and abs((u ** 2).mean() - 1 / 3) < 0.01
+
+
+# ------------------------------------------------------------- Hadamard
+@pytest.mark.parametrize("d", [1, 2, 4, 8, 16, 32, 128, 256])
+def test_hadamard_is_normalised_sylvester(oracle, d):
+    scipy_linalg = pytest.importorskip("scipy.linalg")
+    H = oracle.hadamard_matrix(d)
+    # Sylvester construction (scipy) scaled by 1/sqrt(d) -- "Orthogonal
+    # Invariance in Activation Space", 3.1: H_d is the normalised Hadamard matrix.
+    assert np.array_equal(H * math.sqrt(d), scipy_linalg.hadamard(d).astype(float))
+    assert np.allclose(H, H.T, atol=0)
+    assert np.abs(H @ H - np.eye(d)).max() < 1e-14     # self-inverse (3.1, item 3)
+
+
+def test_hadamard_kron_recursion(oracle):
+    # H_{2n} = H_2 (x) H_n, built independently of the popcount formula.
+    H = np.array([[1.0]])
+    h2 = np.array([[1.0, 1.0], [1.0, -1.0]]) / math.sqrt(2)
+    for _ in range(6):
+        H = np.kron(h2, H)
+    assert np.abs(H - oracle.hadamard_matrix(64)).max() < 1e-15
+
+
+@pytest.mark.parametrize("d", [4, 8, 16])
+def test_recursive_fwht_equals_dense_bruteforce(oracle, d):
+    # brute force over the whole basis: column j of the transform of e_j
+    I = np.eye(d)
+    F = np.stack([oracle.fwht_recursive(I[j]) for j in range(d)], axis=1)
+    assert np.abs(F - oracle.hadamard_matrix(d)).max() < 1e-15
+    x = np.random.default_rng(d).standard_normal((5, d))
+    assert np.abs(oracle.fwht_recursive(x) - x @ oracle.hadamard_matrix(d).T).max() < 1e-13
+
+
+# ------------------------------------------------------------- SO(4) blocks
+def test_quaternion_units_follow_hamilton_rules(oracle):
+    L = oracle.quat_left_matrix
+    one, i, j, k = (1, 0, 0, 0), (0, 1, 0, 0), (0, 0, 1, 0), (0, 0, 0, 1)
+    I4 = np.eye(4)
+    assert np.array_equal(L(one), I4)
+    for u in (i, j, k):
+        assert np.array_equal(L(u) @ L(u), -I4)          # i^2 = j^2 = k^2 = -1
+    assert np.array_equal(L(i) @ L(j), L(k))              # ij = k
+    assert np.array_equal(L(j) @ L(k), L(i))              # jk = i
+    assert np.array_equal(L(k) @ L(i), L(j))              # ki = j
+    assert np.array_equal(L(i) @ L(j) @ L(k), -I4)        # ijk = -1
+    # acting on a vector = quaternion product p*x: i * 1 = i
+    assert np.array_equal(L(i) @ np.array([1.0, 0, 0, 0]), np.array([0, 1.0, 0, 0]))
+
+
+def test_so4_blocks_gram_and_det(oracle):
+    # "Orthogonally mixed 3-bit KV cache", Mathematical statement: R_i^T R_i = I_4,
+    # det R_i = 1 (the MVP reports a Gram error of 8.9e-16).
+    _, quats = oracle.rotation_params(256, 42)
+    for p in quats:
+        R = oracle.quat_left_matrix(p)
+        assert np.abs(R.T @ R - np.eye(4)).max() < 1e-15
+        assert abs(np.linalg.det(R) - 1.0) < 1e-14
+    rng = np.random.default_rng(1)
+    p = rng.standard_normal(4) * 3
+    R = oracle.quat_left_matrix(p)
+    n2 = float(p @ p)
+    assert np.abs(R.T @ R - n2 * np.eye(4)).max() < 1e-12
+    assert abs(np.linalg.det(R) - n2 ** 2) < 1e-9 * n2 ** 2
+
+
+def test_rotation_params_shape_and_flags(oracle):
+    s, q = oracle.rotation_params(128, 42)
+    assert s.shape == (128,) and set(np.unique(s)) == {-1, 1}
+    assert q.shape == (32, 4)
+    assert np.abs(np.linalg.norm(q, axis=1) - 1).max() < 1e-15
+    s0, q0 = oracle.rotation_params(128, 42, use_sign=False, use_so4=False)
+    assert np.all(s0 == 1) and np.all(q0 == [1, 0, 0, 0])
+    s1, q1 = oracle.rotation_params(128, 43)
+    assert not np.array_equal(s, s1)
+    # the first d draws decide the signs: top bit set -> -1
+    r = oracle.SplitMix64(42)
+    assert [(-1 if r.next() >> 63 else 1) for _ in range(4)] == list(s[:4])
+
+
+def test_marsaglia_points_uniform_on_s3(oracle):
+    r = oracle.SplitMix64(5)
+    P = np.array([oracle.marsaglia_s3(r) for _ in range(20000)])
+    assert np.abs(np.linalg.norm(P, axis=1) - 1).max() < 1e-15
+    # uniform on S^3: every coordinate has mean 0 and second moment 1/4
+    assert np.abs(P.mean(0)).max() < 0.02
+    assert np.abs((P ** 2).mean(0) - 0.25).max() < 0.01
+
+
+# ------------------------------------------------------------- U and invariance
+@pytest.mark.parametrize("d,flags", [(4, 3), (8, 3), (128, 3), (128, 1), (256, 3), (256, 0)])
+def test_U_orthogonal(oracle, d, flags):
+    s, q = oracle.rotation_params(d, 42, bool(flags & 1), bool(flags & 2))
+    U = oracle.rotation_matrix(s, q)
+    assert np.abs(U.T @ U - np.eye(d)).max() < 1e-14     # MVP: inverse error 1.6e-15
+
+
+def test_U_order_is_B_H_D(oracle):
+    # columns: U e_j = B H (sigma_j e_j) -> the sign of column j is sigma_j times
+    # the column of B H; with B = I the first row of U is sigma/sqrt(d).
+    s, _ = oracle.rotation_params(16, 9)
+    U = oracle.rotation_matrix(s, np.tile([1.0, 0, 0, 0], (4, 1)))
+    assert np.allclose(U[0], s / 4.0, atol=0)
+    s2, q2 = oracle.rotation_params(16, 9)
+    U2 = oracle.rotation_matrix(s2, q2)
+    B = oracle.block_so4_matrix(q2)
+    assert np.abs(U2 - B @ U).max() < 1e-15            # B applied last
+
+
+def test_dot_product_invariance(oracle):
+    # (Uq)^T (Uk) = q^T k ("Orthogonally mixed 3-bit KV cache", Key formulas;
+    # the MVP reports 7.1e-15)
+    s, q = oracle.rotation_params(128, 42)
+    U = oracle.rotation_matrix(s, q)
+    rng = np.random.default_rng(0)
+    a, b = rng.standard_normal((2, 128))
+    assert abs((U @ a) @ (U @ b) - a @ b) < 1e-12
+
+
+def test_unquantised_rotated_attention_equals_plain(oracle):
+    # "Orthogonal Invariance in Activation Space", 2.3: rotating q, k and v by
+    # the same orthogonal matrix and v back by U^T leaves attention unchanged.
+    s, qq = oracle.rotation_params(128, 3)
+    U = oracle.rotation_matrix(s, qq)
+    rng = np.random.default_rng(2)
+    k = rng.standard_normal((300, 128)) * 4
+    v = rng.standard_normal((300, 128))
+    q = rng.standard_normal(128)
+    ref = oracle.attention_plain(q, k, v, 1 / math.sqrt(128))
+    got = oracle.attention_rotated(U, q, k @ U.T, v @ U.T, 1 / math.sqrt(128))
+    assert np.abs(got - ref).max() < 1e-13
+
+
+# ------------------------------------------------------------- scale types
+def test_e4m3_against_torch_float8(oracle):
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(3)
+    vals = np.concatenate([rng.uniform(0, 448, 5000), np.exp(rng.uniform(-14, 6, 5000)),
+                           [0.0, 2.0 ** -9, 2.0 ** -10, 2.0 ** -6, 448.0, 447.9, 0.3]])
+    mine = oracle.round_e4m3(vals)
+    ref = torch.tensor(vals, dtype=torch.float64).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(mine, ref)
+    # every finite positive code round-trips through encode/decode
+    b = np.arange(1, 127, dtype=np.uint8)
+    v = oracle.decode_e4m3(b)
+    assert np.array_equal(oracle.encode_e4m3(v), b)
+    assert np.array_equal(oracle.round_e4m3(v), v)
+    assert oracle.round_e4m3(1e6) == 448.0 and oracle.round_e4m3(464.1) == 448.0
+    assert oracle.decode_e4m3(0x7E) == 448.0 and oracle.decode_e4m3(1) == 2.0 ** -9
+
+
+def test_f16_saturates(oracle):
+    assert oracle.round_f16(1e9) == 65504.0
+    assert oracle.round_f16(65519.0) == 65504.0
+    assert oracle.round_f16(1.0 + 2 ** -11) == 1.0          # tie to even
+    assert oracle.round_f16(1.0 + 3 * 2 ** -11) == 1.0 + 2 ** -9
+
+
+def test_midpoint_distance(oracle):
+    q = 2.0 ** -10
+    assert oracle.scale_midpoint_distance(1.0 + q / 2, "f16") == 0.0
+    assert oracle.scale_midpoint_distance(1.0, "f16") == pytest.approx(q / 2)
+    assert oracle.scale_midpoint_distance(1.0 + 1 / 16, "e4m3") == 0.0
+    assert np.isinf(oracle.scale_midpoint_distance(3.0, "f32"))
+
+
+# ------------------------------------------------------------- quantiser
+@pytest.mark.parametrize("kind", ["f32", "f16", "e4m3"])
+@pytest.mark.parametrize("block", [32, 64])
+def test_quantiser_error_bound(oracle, kind, block):
+    # |x - s_q c| <= s_q / 2 wherever |x/s_q| <= 3.5, codes in [-3, 3]
+    rng = np.random.default_rng(block)
+    x = rng.standard_normal((400, 128)) * np.exp(rng.uniform(-3, 3, (400, 1)))
+    c, sq, s = oracle.quantize(x, block, 1e-6, kind)
+    assert c.min() >= -3 and c.max() <= 3
+    xb = x.reshape(400, -1, block)
+    err = np.abs(xb - sq[..., None] * c.reshape(xb.shape))
+    inside = np.abs(xb) <= 3.5 * sq[..., None]
+    assert np.all(err[inside] <= sq[..., None].repeat(block, -1)[inside] / 2 * (1 + 1e-12))
+    assert np.allclose(s, (np.abs(xb).max(-1) + 1e-6) / 3, rtol=1e-15)
+    if kind == "f32":
+        assert np.array_equal(c.reshape(xb.shape).max(-1).clip(0) + (-c.reshape(xb.shape)).max(-1).clip(0) > 0,
+                              np.ones(sq.shape, bool))
+        # the block's extreme element always lands on +-3 with an fp32 scale
+        amax = np.argmax(np.abs(xb), axis=-1)
+        cm = np.take_along_axis(c.reshape(xb.shape), amax[..., None], -1)[..., 0]
+        assert np.all(np.abs(cm) == 3)
+
+
+def test_quantiser_quadratic_error_scaling(oracle):
+    # with eps = 0, scaling x by 2^k scales the scales by 2^k and leaves the codes
+    # unchanged, so MSE/amplitude^2 is constant (the MVP's "quadratic error
+    # scaling": MSE/amp^2 varied by 5.4e-12)
+    x = np.random.default_rng(4).standard_normal((50, 128))
+    c0, s0, _ = oracle.quantize(x, 64, 0.0, "f32")
+    ratios = []
+    for k in range(-6, 7):
+        a = 2.0 ** k
+        c, s, _ = oracle.quantize(a * x, 64, 0.0, "f32")
+        assert np.array_equal(c, c0) and np.array_equal(s, s0 * a)
+        xh = (c.reshape(50, 2, 64) * s[..., None]).reshape(50, 128)
+        ratios.append(((xh - a * x) ** 2).mean() / a ** 2)
+    assert np.ptp(ratios) < 1e-15
+
+
+def test_quantiser_zero_and_tiny_blocks(oracle):
+    x = np.zeros((1, 64))
+    c, sq, _ = oracle.quantize(x, 32, 1e-6, "f32")
+    assert np.all(c == 0) and np.allclose(sq, np.float32(1e-6 / 3))
+    # an E4M3 scale that underflows to 0 gives zero codes
+    c, sq, _ = oracle.quantize(np.full((1, 32), 1e-4), 32, 0.0, "e4m3")
+    assert sq[0, 0] == 0.0 and np.all(c == 0)
+
+
+def test_quantiser_clip_fires_with_rounded_down_scale(oracle):
+    # an E4M3 scale rounded down makes |x/s_q| > 3 for the block maximum: the
+    # clip keeps the code at 3 (s = 2.0625*... rounds to 2.0)
+    x = np.zeros((1, 32))
+    x[0, 0] = 3 * 2.0624
+    c, sq, s = oracle.quantize(x, 32, 0.0, "e4m3")
+    assert sq[0, 0] == 2.0 and c[0, 0] == 3 and x[0, 0] / sq[0, 0] > 3
+
+
+# ------------------------------------------------------------- packing
+def _golden():
+    rows = []
+    for line in open(os.path.join(HERE, "golden", "pack3_worked_examples.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        name, d, codes, *hexb = line.split()
+        rows.append((name, int(d), [int(t) for t in codes.split(",")], bytes.fromhex("".join(hexb))))
+    return rows
+
+
+def test_pack_worked_examples(oracle):
+    for name, d, group, b in _golden():
+        codes = np.array(group * (d // 8), dtype=np.int8)[None]
+        assert oracle.pack_codes(codes)[0].tobytes() == b * (d // 8), name
+
+
+def test_unit_vector_writes_all_threes(oracle):
+    # end to end through U: k = +-e_0 with D = I, B = I -> every code is +-3
+    for sgn, name in ((1, "unit_e0"), (-1, "unit_minus_e0")):
+        s, q = oracle.rotation_params(128, 42, False, False)
+        U = oracle.rotation_matrix(s, q)
+        x = U @ (sgn * np.eye(128)[0])
+        c, sq, _ = oracle.quantize(x[None], 64, 1e-6, "f32")
+        assert np.all(c == 3 * sgn)
+        want = dict((r[0], r[3]) for r in _golden())[name]
+        assert oracle.pack_codes(c)[0].tobytes() == want * 16
+
+
+def test_pack_exhaustive_roundtrip(oracle):
+    # all 7^8 = 5,764,801 groups of eight codes in [-3, 3]
+    g = np.indices((7,) * 8).reshape(8, -1).T.astype(np.int8) - 3
+    b = oracle.pack_codes(g)
+    assert b.shape == (7 ** 8, 3)
+    assert np.array_equal(oracle.unpack_codes(b, 8), g)
+    # distinct groups give distinct byte strings
+    key = b[:, 0].astype(np.int64) | (b[:, 1].astype(np.int64) << 8) | (b[:, 2].astype(np.int64) << 16)
+    assert len(np.unique(key)) == 7 ** 8
+
+
+def test_pack_bit_positions_bruteforce(oracle):
+    # element j at bits 3j..3j+2: check bit by bit with Python integers
+    rng = np.random.default_rng(5)
+    for d in (8, 64, 128, 256):
+        c = rng.integers(-3, 4, (3, d)).astype(np.int8)
+        b = oracle.pack_codes(c)
+        for r in range(3):
+            acc = int.from_bytes(b[r].tobytes(), "little")
+            for j in range(d):
+                v = (acc >> (3 * j)) & 7
+                assert (v - 8 if v >= 4 else v) == c[r, j]
+
+
+# ------------------------------------------------------------- storage accounting
+def test_storage_accounting(oracle):
+    def bits(scale, m, d=128, P=64):
+        L = oracle.Layout(d, 1, m, scale, P, 1, 1, 1)
+        return 8 * L.record_bytes / (P * d)
+    # "Hardware-Fused Fast Hadamard Transforms ...": 3.125 effective bits with an
+    # FP8 header per 64 elements, 40 GB (fp16) -> 7.8 GB for a 70B model at 128K
+    assert bits("e4m3", 64) == 3.125
+    gib = 80 * 8 * 128 * 2 * 2 * 131072 / 2 ** 30          # layers*kvheads*d*K,V*2B*tokens
+    assert gib == 40.0 and gib * 3.125 / 16 == 7.8125
+    # the MVP's 1.45x with fp32 scales matches one scale per SO(4) block (m = 4)
+    assert round(16 / (3 + 32 / 4), 2) == 1.45
+    assert bits("f32", 64) == 3.5 and bits("f16", 64) == 3.25 and bits("f32", 32) == 4.0
+    # record sizes of the paged layout with 16-token pages, fp16 scales
+    assert oracle.Layout(128, 1, 64, "f16", 16, 1, 1, 1).record_bytes == 832
+    assert oracle.Layout(256, 1, 64, "f16", 16, 1, 1, 1).record_bytes == 1664
