@@ -1,0 +1,32 @@
+// Host-side declarations shared by the translation units of the library.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "kvq3_common.cuh"
+
+struct kvq3_rotation_s {
+  int32_t d;
+  uint32_t flags;
+  int8_t signs[kvq3::kMaxD];      // as used (all +1 without KVQ3_ROT_SIGN)
+  double quats64[kvq3::kMaxD];    // [d/4][4], unit length (identity without KVQ3_ROT_SO4)
+  kvq3::RotParams params;         // what the kernels receive
+};
+
+namespace kvq3 {
+
+// Validates a cache description for the cache kernels (d in {64,128,256},
+// block in {32,64}, bits 3, ...) and derives the geometry.
+kvq3_status make_geom(const kvq3_cache_desc* desc, CacheGeom* g);
+
+// Validates the device buffers of a cache against its geometry.
+kvq3_status check_cache(const CacheGeom& g, const kvq3_cache* cache, bool need_lens);
+
+// Number of streaming multiprocessors of the current device (cached).
+int sm_count();
+
+inline kvq3_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVQ3_OK : KVQ3_ERR_CUDA; }
+
+inline float inv_sqrt(int d) { return (float)(1.0 / __builtin_sqrt((double)d)); }
+
+}  // namespace kvq3

@@ -1,0 +1,264 @@
+/*
+ * kvq3.h -- C ABI of the orthogonally rotated 3-bit KV cache (GB300, sm_103a).
+ *
+ * Method.  Every key and value head vector is rotated by an orthogonal
+ * U = B . H_d . D and stored as signed 3-bit codes with one scale per block
+ * of m rotated coordinates; decode attention rotates the query by the same U,
+ * reads the packed cache directly (unpack, scale and dot product fused), runs
+ * an online softmax, multiplies by the dequantised values and rotates the
+ * output back with U^T.
+ *
+ * Sources (page title, then section):
+ *   [OMC] "Orthogonally mixed 3-bit KV cache" -- Mathematical statement
+ *         (H_d^T H_d = I, R_i in SO(4), B = diag(R_1..R_{d/4}), U = B H_d,
+ *         (Uq)^T(Uk) = q^T k, v' = Uv rotated back with U^T, the scale
+ *         s = (max_j|x_j| + eps)/(2^(b-1)-1) and the code
+ *         clip(round(x/s), -(2^(b-1)-1), 2^(b-1)-1) with b = 3); Key formulas
+ *         (Attn = softmax(QK^T/sqrt d) V); Implementation notes (write path:
+ *         k1 = U(k), v1 = U(v), one scale per block, "round to signed 3-bit
+ *         integers, and pack the codes into bytes", "store only packed codes
+ *         and scales"; read path: q1 = U(q), unpack and scale keys inside the
+ *         dot product, softmax, multiply by reconstructed values, y = U^T y1,
+ *         "full FP16 K/V tensors are never materialized"; SO(4) blocks from
+ *         normalised quaternions, fixed random rotations for a first version).
+ *   [OIQ] "Orthogonal Invariance in Activation Space: Fast Walsh-Hadamard
+ *         Transforms for KV Quantization" -- 3.1 (normalised FWHT, self
+ *         inverse), 3.2 (random sign flip D applied before the FWHT, generated
+ *         once and stored as a fixed parameter), 3.3 (store / retrieve /
+ *         attention pipeline), 3.4 (per-group scales, default g = 32),
+ *         4.2 (record = scale header followed by packed codes),
+ *         4.3 (dequantisation fused into the attention kernel).
+ *   [HFF] "Hardware-Fused Fast Hadamard Transforms Enable Lossless 3-Bit
+ *         KV-Cache Compression at 128K Context" -- 64-element sub-blocks with
+ *         an FP8 scale header, 3.125 effective bits per element.
+ *
+ * Readings fixed by this library where the pages are silent or disagree:
+ *   R1  H_d is the normalised Walsh-Hadamard matrix in natural (Sylvester)
+ *       order, H[i][j] = (-1)^popcount(i&j) / sqrt(d).
+ *   R2  U = B . H_d . D: sign flip first, then H_d, then the SO(4) blocks.
+ *   R3  R_i is the left-multiplication matrix of the unit quaternion
+ *       p_i = (a, b, c, e) (x -> p_i * x as a quaternion product):
+ *       [[a,-b,-c,-e],[b,a,-e,c],[c,e,a,-b],[e,-c,b,a]]; it acts on rotated
+ *       coordinates 4i..4i+3.
+ *   R4  Seed -> parameters: SplitMix64 (Steele, Lea & Flood 2014) seeded with
+ *       the seed.  Draws 0..d-1 give the signs (sign -1 when the top bit is
+ *       set); then for each block i a uniform point of S^3 by Marsaglia's 1972
+ *       method, with uniforms u = (next() >> 11) * 2^-53 * 2 - 1, pairs with
+ *       s = x^2 + y^2 outside (0, 1) rejected, all in IEEE fp64 without fused
+ *       multiply-add; the device uses the fp32 roundings of the quaternions.
+ *       Flags choose whether the drawn signs / quaternions are used
+ *       (otherwise +1 / identity); the draws are made either way.
+ *   R5  eps is taken as given (1e-6 by default) and kept in the formula.
+ *   R6  round = round half to even.
+ *   R7  The scale is rounded to its storage type first (fp32, or fp16 / OCP
+ *       FP8-E4M3 with round-to-nearest-even saturating to the largest finite
+ *       value) and the codes are computed with the stored scale s_q:
+ *       c = clip(round(x / s_q), -3, 3); c = 0 where s_q == 0.  Dequantisation
+ *       is exactly s_q * c.
+ *   R8  Codes are 3-bit two's complement (-3 = 0b101); 0b100 (-4) is never
+ *       written.
+ *   R9  Code string of a vector: element j at bits 3j..3j+2 of a
+ *       little-endian bit stream of 3d/8 bytes (bit k of the stream is bit
+ *       k%8 of byte k/8).  Blocks are consecutive rotated coordinates
+ *       [0,m), [m,2m), ...
+ *   R10 One scale per block and no per-vector scale ([OMC]); [OIQ] 4.2's
+ *       header count does not add up and is not followed.
+ *   R11 The query is rotated by the same U as the keys ([OMC] q1 = U(q)).
+ *   R12 Logits are scaled by sm_scale, 1/sqrt(d) by default ([OMC] Key
+ *       formulas).
+ *   R13 Decode attends to positions [0, seq_lens[b]); the caller appends the
+ *       current token with kvq3_write and advances seq_lens itself.
+ *   R14 Query head h reads kv head h / (Hq/Hkv) (consecutive grouping).
+ *   R15 The output is fp32 and unrotated; an empty sequence gives zeros.
+ *
+ * Cache layout (the "chunk record" of [OIQ] 4.2, one per page, kv head and
+ * K|V).  P = page_size tokens per page (a multiple of 16), nb = d/m blocks,
+ * sb = scale bytes (4, 2, 1), cb = 3d/8 code bytes:
+ *   record  = [ scales: P*nb entries, token-major (slot t, block j at t*nb+j),
+ *                       sb bytes each, little-endian ]
+ *             [ codes : P code strings of cb bytes (slot t at t*cb) ]
+ *             R = P*(nb*sb + cb) bytes
+ *   page    = for kv head 0..Hkv-1: K record, V record   (Hkv*2*R bytes)
+ *   pool    = num_pages pages
+ * Position pos of sequence b lives in slot pos % P of logical page pos / P.
+ * The physical page is page_table[b*max_pages_per_seq + pos/P] for a paged
+ * cache, or b*max_pages_per_seq + pos/P for a contiguous cache (no table).
+ * Every record and page size is a multiple of 16 bytes.
+ *
+ * Ownership.  The caller owns every buffer: pool, page table, lengths,
+ * inputs, outputs and the decode workspace (all device memory unless stated).
+ * The library's only allocation is the rotation handle itself (host memory,
+ * in kvq3_rotation_create*).  No entry point synchronises the device.
+ * Every device-side call is asynchronous on the given stream (a
+ * cudaStream_t passed as void*, NULL = legacy default stream) and runs on
+ * the device that is current for the calling thread.
+ *
+ * Errors.  Argument checks run on the host before any launch and return a
+ * kvq3_status; nothing is launched then.  Launch failures return
+ * KVQ3_ERR_CUDA.  Bad data found on the device (a position or page id out of
+ * range, a length above capacity, a stored code of -4, a wait that ran out)
+ * sets bits of the optional caller-provided device word *dev_status
+ * (atomicOr) and the kernel skips the affected unit; kernels never trap.
+ */
+#ifndef KVQ3_H_
+#define KVQ3_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVQ3_ABI_VERSION 1
+
+typedef enum {
+  KVQ3_OK = 0,
+  KVQ3_ERR_INVALID_ARG = 1,   /* a pointer, size or layout field is invalid */
+  KVQ3_ERR_UNSUPPORTED = 2,   /* valid, but not compiled in (d, m, bits, G) */
+  KVQ3_ERR_CUDA = 3,          /* a CUDA call or kernel launch failed */
+  KVQ3_ERR_WORKSPACE = 4      /* decode workspace missing or too small */
+} kvq3_status;
+
+typedef enum {
+  KVQ3_SCALE_F32 = 0,
+  KVQ3_SCALE_F16 = 1,
+  KVQ3_SCALE_E4M3 = 2
+} kvq3_scale_type;
+
+/* Rotation flags.  H_d is always applied. */
+enum { KVQ3_ROT_SIGN = 1u, KVQ3_ROT_SO4 = 2u };
+
+/* Bits of the device status word. */
+enum {
+  KVQ3_DEV_BAD_SEQ = 1,      /* sequence index outside [0, batch) */
+  KVQ3_DEV_BAD_POS = 2,      /* position outside [0, max_pages_per_seq*P) */
+  KVQ3_DEV_BAD_PAGE = 4,     /* page id outside [0, num_pages) */
+  KVQ3_DEV_BAD_LEN = 8,      /* seq_lens[b] outside [0, capacity] */
+  KVQ3_DEV_BAD_CODE = 16,    /* a stored code of -4 (never written) */
+  KVQ3_DEV_TIMEOUT = 32      /* an asynchronous copy did not arrive in time */
+};
+
+/* Opaque, immutable rotation U = B . H_d . D (host memory). */
+typedef struct kvq3_rotation_s *kvq3_rotation;
+
+/* Static description of a cache. */
+typedef struct {
+  int32_t head_dim;          /* d: 64, 128 or 256 for the cache kernels;
+                                any power of two 4..256 for kvq3_rotate */
+  int32_t num_kv_heads;      /* Hkv >= 1 */
+  int32_t block;             /* m: 32 or 64, divides d */
+  int32_t bits;              /* b: 3 */
+  int32_t scale_type;        /* kvq3_scale_type */
+  float eps;                 /* eps of the scale formula (1e-6) */
+  int32_t page_size;         /* P: tokens per page, a positive multiple of 16 */
+  int32_t batch;             /* number of sequences */
+  int32_t max_pages_per_seq; /* page-table row length (capacity / P) */
+  int32_t reserved;          /* 0 */
+  int64_t num_pages;         /* pages in the pool */
+} kvq3_cache_desc;
+
+/* Device buffers of a cache. */
+typedef struct {
+  void *pool;                /* num_pages * page_bytes, 16-byte aligned */
+  const int32_t *page_table; /* [batch][max_pages_per_seq] or NULL: contiguous */
+  const int32_t *seq_lens;   /* [batch] attended lengths (decode only) */
+} kvq3_cache;
+
+/* ABI version of the loaded library (KVQ3_ABI_VERSION). */
+int32_t kvq3_abi_version(void);
+
+/* Human-readable name of a status code (static string). */
+const char *kvq3_status_string(kvq3_status s);
+
+/* Creates the rotation of head dimension d (a power of two, 4 <= d <= 256)
+ * from a seed (reading R4; [OIQ] 3.2 "generated once ... fixed parameter";
+ * [OMC] Implementation notes "fixed random rotations ... normalized
+ * quaternion").  flags: KVQ3_ROT_SIGN | KVQ3_ROT_SO4.  *out receives a handle
+ * owned by the caller (free with kvq3_rotation_destroy).  Host only. */
+kvq3_status kvq3_rotation_create(int32_t d, uint64_t seed, uint32_t flags,
+                                 kvq3_rotation *out);
+
+/* Creates a rotation from explicit parameters (host arrays): signs[d] in
+ * {+1,-1}, quats[d/4][4] (a, b, c, e) -- each is normalised to unit length in
+ * fp64 before use; a zero quaternion is rejected.  Host only. */
+kvq3_status kvq3_rotation_create_from_params(int32_t d, const int8_t *signs,
+                                             const float *quats,
+                                             kvq3_rotation *out);
+
+/* Frees a rotation handle (NULL is accepted). */
+kvq3_status kvq3_rotation_destroy(kvq3_rotation rot);
+
+/* Copies the parameters the device uses into host arrays: signs[d] and
+ * quats[d/4][4] (fp32); *d_out (nullable) receives d. */
+kvq3_status kvq3_rotation_export(kvq3_rotation rot, int8_t *signs, float *quats,
+                                 int32_t *d_out);
+
+/* Byte sizes of a record, a page and the whole pool for a description. */
+kvq3_status kvq3_cache_sizes(const kvq3_cache_desc *desc, size_t *record_bytes,
+                             size_t *page_bytes, size_t *pool_bytes);
+
+/* y = U x (inverse = 0) or y = U^T x (inverse != 0) for n_vec vectors of
+ * dimension d ([OMC] k1 = U(k), q1 = U(q), y = U.T @ y1).
+ * x: device [n_vec][d], fp32 (x_is_fp16 = 0) or fp16 (x_is_fp16 = 1);
+ * y: device fp32 [n_vec][d].  fp32 arithmetic.  n_vec = 0 is a no-op. */
+kvq3_status kvq3_rotate(kvq3_rotation rot, const void *x, int32_t x_is_fp16,
+                        float *y, int64_t n_vec, int32_t inverse, void *stream);
+
+/* Write path ([OMC] Implementation notes: "On every new token, compute
+ * k1 = U(k) and v1 = U(v), partition them into quantization blocks, calculate
+ * one scale per block, round to signed 3-bit integers, and pack the codes
+ * into bytes.  Store only packed codes and scales."): for every token i and
+ * kv head, the K and V vectors are rotated, quantised (R7) and stored in the
+ * slot of (seq_idx[i], pos[i]).  Appends one token per sequence (decode) or a
+ * prefill chunk (many positions of one or more sequences).
+ * k, v: device fp16 [n_tok][Hkv][d]; seq_idx, pos: device int32 [n_tok].
+ * Tokens whose slot is invalid are skipped and flagged in *dev_status
+ * (nullable).  Two tokens with the same slot race (last writer unspecified). */
+kvq3_status kvq3_write(kvq3_rotation rot, const kvq3_cache_desc *desc,
+                       const kvq3_cache *cache, const void *k, const void *v,
+                       const int32_t *seq_idx, const int32_t *pos, int64_t n_tok,
+                       int32_t *dev_status, void *stream);
+
+/* Bytes of device workspace kvq3_decode_attn needs for num_q_heads query
+ * heads on the current device (0 < *bytes, a few MB). */
+kvq3_status kvq3_decode_workspace_size(const kvq3_cache_desc *desc,
+                                       int32_t num_q_heads, size_t *bytes);
+
+/* Read path ([OMC] Implementation notes: "At read time compute q1 = U(q),
+ * unpack and scale keys inside the attention dot-product kernel, calculate
+ * logits from q1 and reconstructed transformed keys, apply softmax, multiply
+ * by reconstructed transformed values, and rotate the output back with U.T";
+ * [OIQ] 4.3 fused dequantisation): one decode step of all sequences.
+ * q: device fp16 [batch][Hq][d]; out: device fp32 [batch][Hq][d];
+ * sm_scale <= 0 means 1/sqrt(d); Hq must be a multiple of Hkv with
+ * Hq/Hkv <= 16.  The attended length of sequence b is seq_lens[b]
+ * (device int32), 0 <= seq_lens[b] <= max_pages_per_seq*P.
+ * workspace: device, ws_bytes >= kvq3_decode_workspace_size (256-byte
+ * aligned); it holds split partials between the two kernels of one call, so
+ * calls that share a workspace must not overlap.  A sequence with a bad
+ * length is skipped (zero output, KVQ3_DEV_BAD_LEN); a bad page id masks that
+ * page (KVQ3_DEV_BAD_PAGE). */
+kvq3_status kvq3_decode_attn(kvq3_rotation rot, const kvq3_cache_desc *desc,
+                             const kvq3_cache *cache, const void *q,
+                             int32_t num_q_heads, float sm_scale, float *out,
+                             void *workspace, size_t ws_bytes,
+                             int32_t *dev_status, void *stream);
+
+/* Reads back positions t0..t0+nt-1 of sequence seq, kv head kv_head, K
+ * (which = 0) or V (which = 1) as fp32 out[nt][d]: s_q * c in the rotated
+ * domain (rot == NULL) or U^T (s_q * c) (rot != NULL) ([OIQ] 3.3 "Retrieve").
+ * codes_out (nullable): int32 [nt][d] raw codes.  Positions without a valid
+ * slot give zeros and set *dev_status bits; a stored -4 sets
+ * KVQ3_DEV_BAD_CODE and reads as 0.  A debugging and testing aid. */
+kvq3_status kvq3_dequant_debug(kvq3_rotation rot, const kvq3_cache_desc *desc,
+                               const kvq3_cache *cache, int32_t seq,
+                               int32_t kv_head, int32_t which, int64_t t0,
+                               int64_t nt, float *out, int32_t *codes_out,
+                               int32_t *dev_status, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ3_H_ */

@@ -1,0 +1,145 @@
+"""Shared set-up for the GPU parity tests: one cache description built twice,
+once for the library (device buffers) and once for the CPU oracle, fed with
+the same seeded inputs (kvq3_inputs).  Expected values come from the oracle
+only; the comparisons below parse the library's output bytes."""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+import kvq3_inputs as I
+from oracle import kvq3_oracle as O
+
+TOL_DECODE = 2e-3        # max|err| <= TOL_DECODE * rms(out)
+TOL_SCALE = 1e-6         # relative
+BOUNDARY = 1e-4          # |x/s_q| within this of k + 1/2: code may round either way
+MIDPOINT = 1e-6          # fp64 scale within this (relative) of a storage midpoint
+
+
+class Case:
+    def __init__(self, d=128, hkv=2, hq=8, block=64, scale="f16", page=16, lens=(37, 100),
+                 maxp=None, paged=False, flags=3, rot_seed=42, data=None, spare_pages=0):
+        import torch
+        import hadamard_rotated_bit_kvq3_gb300 as K
+        self.K, self.torch = K, torch
+        self.dev = torch.device("cuda:0")
+        self.d, self.hkv, self.hq, self.block, self.scale, self.page = d, hkv, hq, block, scale, page
+        self.lens = np.array(lens, np.int32)
+        self.B = len(lens)
+        need = [max(1, math.ceil(int(L) / page)) for L in lens]
+        self.maxp = maxp or max(need)
+        self.paged = paged
+        if paged:
+            self.table, n = I.page_table_np(rot_seed + 5, np.maximum(self.lens, 1), page, self.maxp)
+            self.num_pages = n + spare_pages
+        else:
+            self.table = None
+            self.num_pages = self.B * self.maxp + spare_pages
+        self.desc = K.CacheDesc(d, hkv, block, 3, K.SCALE_TYPES[scale], 1e-6, page, self.B, self.maxp,
+                                0, self.num_pages)
+        self.layout = O.Layout(d, hkv, block, scale, page, self.B, self.maxp, self.num_pages)
+        self.rot = K.Rotation(d, rot_seed, flags)
+        s, q = O.rotation_params(d, rot_seed, bool(flags & 1), bool(flags & 2))
+        self.U = O.rotation_matrix(s, q)
+        self.spec = data or I.DataSpec(d, hkv, 1234, 0.03, 20.0)
+        self.pool = torch.zeros(self.layout.pool_bytes, dtype=torch.uint8, device=self.dev)
+        self.pool_o = np.zeros(self.layout.pool_bytes, np.uint8)
+        self.table_t = None if self.table is None else torch.as_tensor(self.table, device=self.dev)
+        self.lens_t = torch.as_tensor(self.lens, device=self.dev)
+        self.cache = K.Cache(self.pool.data_ptr(),
+                             None if self.table_t is None else self.table_t.data_ptr(),
+                             self.lens_t.data_ptr())
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.dev)
+
+    # ------------------------------------------------------------ inputs
+    def tokens(self, upto=None):
+        """(k, v, seq_idx, pos) of every position [0, L_b) of every sequence."""
+        ks, vs, si, ps = [], [], [], []
+        for b in range(self.B):
+            n = int(self.lens[b]) if upto is None else min(int(self.lens[b]), upto)
+            if n == 0:
+                continue
+            ks.append(np.stack([I.kv_rows_np(self.spec, 0, b, h, 0, n) for h in range(self.hkv)], 1))
+            vs.append(np.stack([I.kv_rows_np(self.spec, 1, b, h, 0, n) for h in range(self.hkv)], 1))
+            si.append(np.full(n, b, np.int32))
+            ps.append(np.arange(n, dtype=np.int32))
+        return (np.concatenate(ks), np.concatenate(vs), np.concatenate(si), np.concatenate(ps))
+
+    def queries(self, step=0):
+        return I.q_np(self.spec, self.B, self.hq, step)
+
+    # ------------------------------------------------------------ runs
+    def gpu_write(self, k, v, si, ps):
+        t = self.torch
+        self.K.kvq3_write(self.rot.handle, self.desc, self.cache, t.as_tensor(k, device=self.dev),
+                          t.as_tensor(v, device=self.dev), t.as_tensor(si, device=self.dev),
+                          t.as_tensor(ps, device=self.dev), self.status)
+
+    def oracle_write(self, k, v, si, ps):
+        return O.write(self.pool_o, self.layout, self.U, k, v, si, ps, self.table)
+
+    def gpu_decode(self, q, sm_scale=0.0):
+        t = self.torch
+        out = t.full((self.B, self.hq, self.d), float("nan"), dtype=t.float32, device=self.dev)
+        ws = t.empty(self.K.kvq3_decode_workspace_size(self.desc, self.hq), dtype=t.uint8,
+                     device=self.dev)
+        self.K.kvq3_decode_attn(self.rot.handle, self.desc, self.cache, t.as_tensor(q, device=self.dev),
+                                out, ws, sm_scale, self.status)
+        t.cuda.synchronize()
+        return out.cpu().numpy().astype(np.float64)
+
+    def oracle_decode(self, q, sm_scale=0.0, lens=None):
+        return O.decode(self.pool_o, self.layout, self.U, q, self.lens if lens is None else lens,
+                        self.table, sm_scale)
+
+    def upload_oracle_pool(self):
+        self.pool.copy_(self.torch.as_tensor(self.pool_o, device=self.dev))
+
+    def device_status(self):
+        self.torch.cuda.synchronize()
+        return int(self.status.item())
+
+    # ------------------------------------------------------------ comparisons
+    def compare_written(self, k, v, si, ps):
+        """Compares the library's stored scales and codes with the oracle's
+        for every written token.  Returns counts of excluded boundary
+        elements and scale-midpoint blocks."""
+        gp = self.pool.cpu().numpy()
+        nb = self.d // self.block
+        excl_codes = excl_blocks = checked = 0
+        for which, src in ((0, k), (1, v)):
+            x = src.astype(np.float64).reshape(-1, self.d) @ self.U.T
+            c_o, sq_o, s_o = O.quantize(x, self.block, 1e-6, self.scale)
+            page, slot, st = O.locate(self.layout, self.table, np.repeat(si, self.hkv),
+                                      np.repeat(ps, self.hkv))
+            ok = st == 0
+            heads = np.tile(np.arange(self.hkv), len(si))
+            rec = page * self.layout.page_bytes + (heads * 2 + which) * self.layout.record_bytes
+            so = rec + slot * nb * self.layout.sb
+            co = rec + self.page * nb * self.layout.sb + slot * self.layout.code_bytes
+            idx_s = so[ok][:, None] + np.arange(nb * self.layout.sb)[None]
+            idx_c = co[ok][:, None] + np.arange(self.layout.code_bytes)[None]
+            sg = O.decode_scales(gp[idx_s], self.scale)
+            cg = O.unpack_codes(gp[idx_c], self.d)
+            sq_o, s_o, c_o, xo = sq_o[ok], s_o[ok], c_o[ok], x[ok]
+            mid = O.scale_midpoint_distance(s_o, self.scale) < MIDPOINT          # [n, nb]
+            good_blk = ~mid
+            assert np.all(np.abs(sg - sq_o)[good_blk] <= TOL_SCALE * sq_o[good_blk]), "scale mismatch"
+            r = np.abs(xo.reshape(-1, nb, self.block) / np.where(sq_o > 0, sq_o, 1)[..., None])
+            near = np.zeros(r.shape, bool)
+            for kk in range(3):
+                near |= np.abs(r - (kk + 0.5)) < BOUNDARY
+            near |= mid[..., None]
+            near = near.reshape(-1, self.d)
+            bad = (cg != c_o) & ~near
+            assert not bad.any(), f"{int(bad.sum())} codes differ outside rounding boundaries"
+            excl_codes += int(near.sum())
+            excl_blocks += int(mid.sum())
+            checked += cg.size
+        return dict(checked=checked, boundary_codes=excl_codes, midpoint_blocks=excl_blocks)
+
+
+def rel_err(got, ref):
+    rms = math.sqrt(float(np.mean(ref ** 2)))
+    return float(np.abs(got - ref).max()) / rms if rms > 0 else float(np.abs(got).max())

