@@ -228,14 +228,19 @@ struct DecodeSmem {
   static constexpr int kStageOff = ((kQInvOff + GPAD * 4) + 127) / 128 * 128;
 };
 
-template <int D, int BLOCK, int GPAD>
+// PSPLIT: the probabilities-times-value-scales P' enter PV as hi + lo fp16
+// halves too (PV n-tile = 4 heads x (hi, lo), like QK); otherwise one fp16
+// value per head (PV n-tile = 8 heads).  The split is needed when the value
+// scales are fp32 (p = 1 times an fp32 scale is not an fp16 value) and free
+// when G <= 4 (the 8-column tile has room).
+template <int D, int BLOCK, int GPAD, bool PSPLIT>
 __global__ void __launch_bounds__(128) decode_split_kernel(const __grid_constant__ DecodeParams p,
                                                            const __grid_constant__ RotParams rp) {
   constexpr int NB = D / BLOCK;
   constexpr int KS = D / 16;          // k-steps of QK^T == M-tiles of PV
   constexpr int KSB = BLOCK / 16;     // per block
   constexpr int NTQ = GPAD / 4;       // QK n-tiles: 4 heads x (hi, lo)
-  constexpr int NTP = (GPAD + 7) / 8; // PV n-tiles: 8 heads
+  constexpr int NTP = PSPLIT ? NTQ : (GPAD + 7) / 8;  // PV n-tiles
   constexpr int FQ = BLOCK / 4;       // key fields per lane per block
   constexpr int FV = BLOCK / 8;       // value fields per lane per block
   constexpr int CB = 3 * D / 8;
@@ -324,12 +329,25 @@ __global__ void __launch_bounds__(128) decode_split_kernel(const __grid_constant
       const int b = mt / KSB, mp = mt % KSB;
 #pragma unroll
       for (int tp = 0; tp < NTP; ++tp) {
+        if constexpr (PSPLIT) {
+          // columns 2j, 2j+1: head 4tp+j, hi and lo parts
+          const int h = 4 * tp + j;
 #pragma unroll
-        for (int reg = 0; reg < 4; ++reg) {
-          const int f = 2 * mp + (reg >> 1);
-          const int dim = b * BLOCK + r * FV + f;
-          const int h = 8 * tp + 2 * j + (reg & 1);
-          if (h < p.G) slot[h * D + dim] = acc[mt][tp][reg] * (1.0f / (float)(1 << v_off(f)));
+          for (int e = 0; e < 2; ++e) {
+            const int f = 2 * mp + e;
+            const int dim = b * BLOCK + r * FV + f;
+            if (h < p.G)
+              slot[h * D + dim] = (acc[mt][tp][2 * e] + acc[mt][tp][2 * e + 1]) *
+                                  (1.0f / (float)(1 << v_off(f)));
+          }
+        } else {
+#pragma unroll
+          for (int reg = 0; reg < 4; ++reg) {
+            const int f = 2 * mp + (reg >> 1);
+            const int dim = b * BLOCK + r * FV + f;
+            const int h = 8 * tp + 2 * j + (reg & 1);
+            if (h < p.G) slot[h * D + dim] = acc[mt][tp][reg] * (1.0f / (float)(1 << v_off(f)));
+          }
         }
       }
     }
@@ -495,7 +513,17 @@ __global__ void __launch_bounds__(128) decode_split_kernel(const __grid_constant
           m[tq] = mn;
           changed |= alpha[tq] != 1.0f;
         }
-        if (__any_sync(kFull, changed)) {
+        if constexpr (PSPLIT) {
+          // this lane's PV columns belong to its own QK head 4tp + j
+          if (__any_sync(kFull, changed)) {
+#pragma unroll
+            for (int tp = 0; tp < NTP; ++tp)
+#pragma unroll
+              for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc[mt][tp][c] *= alpha[tp];
+          }
+        } else if (__any_sync(kFull, changed)) {
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             float av[NTQ];
@@ -519,7 +547,9 @@ __global__ void __launch_bounds__(128) decode_split_kernel(const __grid_constant
         const int T0 = t0 + 2 * j;
         float x0[NTQ], x1[NTQ], x2[NTQ], x3[NTQ];
         {
-          const int srcA = 8 * j + (r & 3), srcB = 8 * j + 4 + (r & 3);
+          // B element (token T, column r) comes from the QK lane 4*(T%8) + head%4
+          const int hl = PSPLIT ? (r >> 1) : (r & 3);
+          const int srcA = 8 * j + hl, srcB = 8 * j + 4 + hl;
 #pragma unroll
           for (int tq = 0; tq < NTQ; ++tq) {
             x0[tq] = __shfl_sync(kFull, pr[tq], srcA);
@@ -536,6 +566,26 @@ __global__ void __launch_bounds__(128) decode_split_kernel(const __grid_constant
         const bool v0 = T0 < n_valid, v1 = T0 + 1 < n_valid, v2 = T0 + 8 < n_valid,
                    v3 = T0 + 9 < n_valid;
         uint32_t pb[NB][NTP][2];
+        if constexpr (PSPLIT) {
+#pragma unroll
+          for (int tp = 0; tp < NTP; ++tp) {
+            const bool hv = 4 * tp + (r >> 1) < p.G;
+            const bool lo_part = (r & 1) != 0;
+            auto part = [&](float v) {
+              const float hi = __half2float(__float2half_rn(v));
+              return lo_part ? v - hi : hi;
+            };
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+              const float y0 = hv && v0 ? x0[tp] * sv0[b] : 0.0f;
+              const float y1 = hv && v1 ? x1[tp] * sv1[b] : 0.0f;
+              const float y2 = hv && v2 ? x2[tp] * sv2[b] : 0.0f;
+              const float y3 = hv && v3 ? x3[tp] * sv3[b] : 0.0f;
+              pb[b][tp][0] = pack_half2(part(y0), part(y1));
+              pb[b][tp][1] = pack_half2(part(y2), part(y3));
+            }
+          }
+        } else {
 #pragma unroll
         for (int tp = 0; tp < NTP; ++tp) {
           const int hp = 8 * tp + r;
@@ -555,6 +605,7 @@ __global__ void __launch_bounds__(128) decode_split_kernel(const __grid_constant
             pb[b][tp][0] = pack_half2(hv && v0 ? y0 * sv0[b] : 0.0f, hv && v1 ? y1 * sv1[b] : 0.0f);
             pb[b][tp][1] = pack_half2(hv && v2 ? y2 * sv2[b] : 0.0f, hv && v3 ? y3 * sv3[b] : 0.0f);
           }
+        }
         }
         // ------------------------------------------------ o1^T += V^T P'^T
 #pragma unroll
@@ -653,6 +704,7 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const __grid_consta
 // ------------------------------------------------------------------ host
 struct DecodePlan {
   int gpad;
+  bool psplit;
   int warps_per_cta;
   int ctas;
   int stages;
@@ -661,16 +713,17 @@ struct DecodePlan {
   const void* kernel;
 };
 
-template <int D, int BLOCK, int GPAD>
+template <int D, int BLOCK, int GPAD, bool PSPLIT>
 const void* decode_kernel_ptr() {
-  return reinterpret_cast<const void*>(&decode_split_kernel<D, BLOCK, GPAD>);
+  return reinterpret_cast<const void*>(&decode_split_kernel<D, BLOCK, GPAD, PSPLIT>);
 }
 
 // Sizes the launch for the current device.
-template <int D, int BLOCK, int GPAD>
+template <int D, int BLOCK, int GPAD, bool PSPLIT>
 kvq3_status decode_plan_t(const CacheGeom& g, int G, DecodePlan* plan) {
   using SM = DecodeSmem<D, GPAD>;
   plan->gpad = GPAD;
+  plan->psplit = PSPLIT;
   plan->copy_bytes = (uint32_t)(2 * g.record_bytes);
   plan->stage_bytes = (plan->copy_bytes + 16 + 15) / 16 * 16;
   int stages = (int)(24576 / plan->stage_bytes);
@@ -687,7 +740,7 @@ kvq3_status decode_plan_t(const CacheGeom& g, int G, DecodePlan* plan) {
   plan->stages = stages;
   plan->warps_per_cta = wpc;
   plan->warp_smem = warp_smem;
-  const void* k = decode_kernel_ptr<D, BLOCK, GPAD>();
+  const void* k = decode_kernel_ptr<D, BLOCK, GPAD, PSPLIT>();
   plan->kernel = k;
   const int smem = wpc * (int)warp_smem;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
@@ -702,7 +755,7 @@ kvq3_status decode_plan_t(const CacheGeom& g, int G, DecodePlan* plan) {
   return KVQ3_OK;
 }
 
-template <int D, int BLOCK, int GPAD>
+template <int D, int BLOCK, int GPAD, bool PSPLIT>
 kvq3_status decode_run_t(const DecodePlan& plan, DecodeParams prm, const RotParams& rp, float* out,
                          cudaStream_t st) {
   prm.stages = plan.stages;
@@ -711,7 +764,7 @@ kvq3_status decode_run_t(const DecodePlan& plan, DecodeParams prm, const RotPara
   prm.total_warps = plan.ctas * plan.warps_per_cta;
   prm.warps_per_cta = plan.warps_per_cta;
   prm.warp_smem = plan.warp_smem;
-  decode_split_kernel<D, BLOCK, GPAD><<<plan.ctas, 32 * plan.warps_per_cta,
+  decode_split_kernel<D, BLOCK, GPAD, PSPLIT><<<plan.ctas, 32 * plan.warps_per_cta,
                                         plan.warps_per_cta * plan.warp_smem, st>>>(prm, rp);
   if (cudaGetLastError() != cudaSuccess) return KVQ3_ERR_CUDA;
   const int64_t items = (int64_t)prm.g.batch * prm.Hq;
@@ -730,28 +783,27 @@ kvq3_status decode_run_d64(const DecodePlan&, const DecodeParams&, const RotPara
 kvq3_status decode_run_d128(const DecodePlan&, const DecodeParams&, const RotParams&, float*, cudaStream_t);
 kvq3_status decode_run_d256(const DecodePlan&, const DecodeParams&, const RotParams&, float*, cudaStream_t);
 
+// Variant choice: P' split for G <= 4 (free) and for fp32 value scales.
+#define KVQ3_DECODE_PICK(D, BLK, FN, ...)                                                      \
+  {                                                                                           \
+    const bool f32 = g.scale_type == KVQ3_SCALE_F32;                                          \
+    if (gp == 4) return FN<D, BLK, 4, true>(__VA_ARGS__);                                     \
+    if (gp == 8) return f32 ? FN<D, BLK, 8, true>(__VA_ARGS__) : FN<D, BLK, 8, false>(__VA_ARGS__); \
+    return f32 ? FN<D, BLK, 16, true>(__VA_ARGS__) : FN<D, BLK, 16, false>(__VA_ARGS__);       \
+  }
+
 #define KVQ3_DECODE_INSTANCES(D)                                                              \
   kvq3_status decode_plan_d##D(const CacheGeom& g, int G, DecodePlan* plan) {                \
     const int gp = G <= 4 ? 4 : (G <= 8 ? 8 : 16);                                            \
-    if (g.block == 32) {                                                                      \
-      if (gp == 4) return decode_plan_t<D, 32, 4>(g, G, plan);                                \
-      if (gp == 8) return decode_plan_t<D, 32, 8>(g, G, plan);                                \
-      return decode_plan_t<D, 32, 16>(g, G, plan);                                            \
-    }                                                                                         \
-    if (gp == 4) return decode_plan_t<D, 64, 4>(g, G, plan);                                  \
-    if (gp == 8) return decode_plan_t<D, 64, 8>(g, G, plan);                                  \
-    return decode_plan_t<D, 64, 16>(g, G, plan);                                              \
+    if (g.block == 32) KVQ3_DECODE_PICK(D, 32, decode_plan_t, g, G, plan)                     \
+    KVQ3_DECODE_PICK(D, 64, decode_plan_t, g, G, plan)                                        \
   }                                                                                           \
   kvq3_status decode_run_d##D(const DecodePlan& plan, const DecodeParams& prm,                \
                               const RotParams& rp, float* out, cudaStream_t st) {             \
-    if (prm.g.block == 32) {                                                                  \
-      if (plan.gpad == 4) return decode_run_t<D, 32, 4>(plan, prm, rp, out, st);              \
-      if (plan.gpad == 8) return decode_run_t<D, 32, 8>(plan, prm, rp, out, st);              \
-      return decode_run_t<D, 32, 16>(plan, prm, rp, out, st);                                 \
-    }                                                                                         \
-    if (plan.gpad == 4) return decode_run_t<D, 64, 4>(plan, prm, rp, out, st);                \
-    if (plan.gpad == 8) return decode_run_t<D, 64, 8>(plan, prm, rp, out, st);                \
-    return decode_run_t<D, 64, 16>(plan, prm, rp, out, st);                                   \
+    const CacheGeom& g = prm.g;                                                               \
+    const int gp = plan.gpad;                                                                 \
+    if (g.block == 32) KVQ3_DECODE_PICK(D, 32, decode_run_t, plan, prm, rp, out, st)          \
+    KVQ3_DECODE_PICK(D, 64, decode_run_t, plan, prm, rp, out, st)                             \
   }
 
 }  // namespace kvq3

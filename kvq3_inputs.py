@@ -228,6 +228,17 @@ def normal_torch(seed: int, start: int, count: int, device):
     return z[off:off + count]
 
 
+def _round_fp16_torch(x):
+    """float64 -> float16 with a single round-to-nearest-even (as numpy's
+    conversion does).  A plain .to(float16) may pass through float32 and
+    round twice; here the value is first rounded to the fp16 grid in float64
+    (quantum 2^(e-10), subnormal quantum 2^-24), which the cast then keeps."""
+    torch = _torch()
+    _, E = torch.frexp(x)
+    quantum = torch.ldexp(torch.ones_like(x), torch.clamp(E - 1, min=-14) - 10)
+    return (torch.round(x / quantum) * quantum).to(torch.float16)
+
+
 def kv_rows_torch(spec: DataSpec, which: int, b: int, kv_head: int, pos0: int, n: int, device):
     """Same rows as :func:`kv_rows_np`, generated on ``device`` (fp16 [n][d])."""
     torch = _torch()
@@ -241,7 +252,7 @@ def kv_rows_torch(spec: DataSpec, which: int, b: int, kv_head: int, pos0: int, n
     if which == 0 and spec.key_decay:
         pos = torch.arange(pos0, pos0 + n, dtype=torch.float64, device=device)
         x *= (1.0 / torch.sqrt(1.0 + pos / 256.0))[:, None]
-    return x.to(torch.float16)
+    return _round_fp16_torch(x)
 
 
 # ---------------------------------------------------------------- workloads
