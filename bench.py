@@ -101,6 +101,9 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            t0 = time.time()
+            while not self.rows and time.time() - t0 < 5.0:   # first sample before timing
+                time.sleep(0.02)
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
@@ -406,8 +409,8 @@ def workload_desc(w: I.Workload) -> str:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.workloads()))
     ap.add_argument("--impl", default="kvq3", choices=["kvq3", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -431,6 +434,9 @@ def main():
     st = GpuWorkload(args.workload, dev, rank, args.batch)
     w = st.w
     stream = torch.cuda.current_stream()
+    clk = ClockSampler(local)
+    if not args.profile:
+        clk.__enter__()
     for _ in range(args.warmup):
         st.step()
     torch.cuda.synchronize()
@@ -448,18 +454,17 @@ def main():
            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        t_start.record(stream)
-        for i in range(args.steps):
-            ev[i][0].record(stream)
-            st.write(st.k_new, st.v_new, st.seq_new, st.pos_new)
-            ev[i][1].record(stream)
-            st.decode()
-            ev[i][2].record(stream)
-        t_end.record(stream)
-        torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        st.write(st.k_new, st.v_new, st.seq_new, st.pos_new)
+        ev[i][1].record(stream)
+        st.decode()
+        ev[i][2].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
     barrier(world)
     total_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
     ms_step = total_ms / args.steps
@@ -499,6 +504,7 @@ def main():
     b.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(a.elapsed_time(b), world) / args.steps
+    clk.__exit__(None, None, None)
     assert int(st.status.item()) == 0
 
     ab = algorithmic_bytes(w, st.lens)

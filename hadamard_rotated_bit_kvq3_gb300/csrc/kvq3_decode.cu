@@ -8,11 +8,28 @@ using namespace kvq3;
 
 namespace {
 
+#define KVQ3_BY_SCALE(D, FN, ...)                                  \
+  switch (g.scale_type) {                                          \
+    case KVQ3_SCALE_F32: return FN##_d##D##_f32(__VA_ARGS__);      \
+    case KVQ3_SCALE_F16: return FN##_d##D##_f16(__VA_ARGS__);      \
+    default: return FN##_d##D##_e4m3(__VA_ARGS__);                 \
+  }
+
 kvq3_status plan_for(const CacheGeom& g, int G, DecodePlan* plan) {
   switch (g.d) {
-    case 64: return decode_plan_d64(g, G, plan);
-    case 128: return decode_plan_d128(g, G, plan);
-    case 256: return decode_plan_d256(g, G, plan);
+    case 64: KVQ3_BY_SCALE(64, decode_plan, g, G, plan)
+    case 128: KVQ3_BY_SCALE(128, decode_plan, g, G, plan)
+    case 256: KVQ3_BY_SCALE(256, decode_plan, g, G, plan)
+  }
+  return KVQ3_ERR_UNSUPPORTED;
+}
+
+kvq3_status run_for(const CacheGeom& g, const DecodePlan& plan, const DecodeParams& prm,
+                    const RotParams& rp, float* out, cudaStream_t st) {
+  switch (g.d) {
+    case 64: KVQ3_BY_SCALE(64, decode_run, plan, prm, rp, out, st)
+    case 128: KVQ3_BY_SCALE(128, decode_run, plan, prm, rp, out, st)
+    case 256: KVQ3_BY_SCALE(256, decode_run, plan, prm, rp, out, st)
   }
   return KVQ3_ERR_UNSUPPORTED;
 }
@@ -72,13 +89,7 @@ kvq3_status kvq3_decode_attn(kvq3_rotation rot, const kvq3_cache_desc* desc,
   prm.inv_sqrt_d = inv_sqrt(g.d);
   prm.slot_floats = (uint32_t)(G * (g.d + 2));
   prm.wait_limit = 1u << 22;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  switch (g.d) {
-    case 64: return decode_run_d64(plan, prm, rot->params, out, st);
-    case 128: return decode_run_d128(plan, prm, rot->params, out, st);
-    case 256: return decode_run_d256(plan, prm, rot->params, out, st);
-  }
-  return KVQ3_ERR_UNSUPPORTED;
+  return run_for(g, plan, prm, rot->params, out, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -9,24 +9,29 @@
 // Activation Space", 4.3: dequantisation fused into the attention kernel.
 //
 // Design (one GPU, HBM-bound):
-//  * Work = the flattened list of (sequence, kv head, page) triples.  A
-//    persistent grid of warps splits it into equal contiguous ranges; a warp
-//    keeps an online-softmax state per (sequence, kv head) segment and writes
-//    one fp32 partial (o1[G][d] unnormalised, max, sum) per segment to the
-//    workspace, at slot (warp + unit), which is unique because ranges and
-//    units are both ordered.  A second kernel merges the partials of each
-//    (sequence, query head) with the log-sum-exp rule and applies U^T.
-//  * Each page's K and V records of one kv head are contiguous; one lane
-//    streams them with cp.async.bulk into a per-warp ring of shared-memory
-//    stages (mbarrier completion, L2 evict-first), several pages ahead.
+//  * Work = the flattened list of 64-token chunks of every (sequence, kv
+//    head) unit (a chunk is one page when pages hold >= 64 tokens, else
+//    64/P consecutive pages of the unit).  A persistent grid of 4-warp CTAs
+//    splits the list into equal contiguous ranges.
+//  * One thread per CTA streams each chunk's K and V records into a ring of
+//    shared-memory stages with cp.async.bulk (mbarrier completion, L2
+//    evict-first); the four warps share every stage, one 16-token step each,
+//    and release it through a second mbarrier.
+//  * Each warp keeps an online-softmax state per unit; at the end of a unit
+//    the four states merge (max, rescale, sum) into one fp32 partial
+//    (o1[G][d] unnormalised, max, sum) at workspace slot (cta + unit), unique
+//    because CTA ranges and units are both ordered.  A second kernel merges
+//    the partials of each (sequence, query head) with the log-sum-exp rule
+//    and applies U^T.
 //  * QK^T and PV run on tensor cores (mma.sync m16n8k16, fp16 in, fp32
 //    accumulate).  Codes in -3..3 become exact fp16 values by a mask/xor into
 //    the 0x6400 exponent pattern and one half2 subtraction; the field's bit
 //    offset inside the half leaves a power-of-two factor that is folded into
 //    q1 (keys) or into the output (values).  q1 is split into hi + lo fp16
-//    halves (two columns per head) so the logits keep ~fp32 accuracy;
-//    per-(token, block) scales multiply the per-block partial dot products
-//    (keys) or the probabilities (values).
+//    halves (two columns per head) so the logits keep ~fp32 accuracy; with
+//    fp32 value scales the probabilities are split the same way.  Per-(token,
+//    block) scales multiply the per-block partial dot products (keys) or the
+//    probabilities (values).
 #pragma once
 
 #include <float.h>
@@ -34,6 +39,10 @@
 #include "kvq3_internal.h"
 
 namespace kvq3 {
+
+constexpr int kChunk = 64;       // tokens per chunk (pages smaller than this are grouped)
+constexpr int kWarps = 4;        // consumer warps per CTA
+constexpr int kMaxStages = 8;
 
 struct DecodeParams {
   CacheGeom g;
@@ -47,25 +56,28 @@ struct DecodeParams {
   int32_t Hq;
   float qk_scale;         // sm_scale * log2(e)
   float inv_sqrt_d;
-  int32_t stages;         // ring depth per warp
-  uint32_t stage_bytes;   // bytes per stage (copy_bytes + padding)
-  uint32_t copy_bytes;    // K record + V record of one kv head
-  int32_t total_warps;
-  int32_t warps_per_cta;
+  int32_t stages;         // ring depth
+  uint32_t stage_bytes;   // bytes per stage
+  int32_t chunk_tokens;   // tokens per chunk: max(64, P)
+  int32_t pages_per_chunk;
+  int32_t ctas;
   uint32_t slot_floats;   // floats per partial slot: G*(D+2)
-  uint32_t warp_smem;     // dynamic shared memory per warp
   uint32_t wait_limit;    // bound on mbarrier polls
 };
 
 // ------------------------------------------------------------------ helpers
-__device__ __forceinline__ int64_t seq_pages(const DecodeParams& p, int b, bool flag) {
+__device__ __forceinline__ int64_t seq_len_checked(const DecodeParams& p, int b, bool flag) {
   const int64_t len = p.seq_lens[b];
   const int64_t cap = (int64_t)p.g.max_pages * p.g.page_size;
   if (len < 0 || len > cap) {
     if (flag) set_status(p.status, KVQ3_DEV_BAD_LEN);
     return 0;
   }
-  return (len + p.g.page_size - 1) / p.g.page_size;
+  return len;
+}
+
+__device__ __forceinline__ int64_t seq_chunks(const DecodeParams& p, int b, bool flag) {
+  return (seq_len_checked(p, b, flag) + p.chunk_tokens - 1) / p.chunk_tokens;
 }
 
 __device__ __forceinline__ int64_t warp_sum64(int64_t v) {
@@ -74,93 +86,139 @@ __device__ __forceinline__ int64_t warp_sum64(int64_t v) {
   return v;
 }
 
-// Total pages over all (sequence, kv head) units.
-__device__ __forceinline__ int64_t total_pages(const DecodeParams& p, bool flag) {
+// Total chunks over all (sequence, kv head) units.
+__device__ __forceinline__ int64_t total_chunks(const DecodeParams& p, bool flag) {
   const int lane = threadIdx.x & 31;
   int64_t acc = 0;
   for (int b0 = 0; b0 < p.g.batch; b0 += 32) {
     const int b = b0 + lane;
-    acc += warp_sum64(b < p.g.batch ? seq_pages(p, b, flag) : 0);
+    acc += warp_sum64(b < p.g.batch ? seq_chunks(p, b, flag) : 0);
   }
   return acc * p.g.hkv;
 }
 
-// Hkv * (pages of sequences 0..b-1).
-__device__ __forceinline__ int64_t pages_before(const DecodeParams& p, int b) {
+// Hkv * (chunks of sequences 0..b-1).
+__device__ __forceinline__ int64_t chunks_before(const DecodeParams& p, int b) {
   const int lane = threadIdx.x & 31;
   int64_t acc = 0;
   for (int b0 = 0; b0 < b; b0 += 32) {
     const int bb = b0 + lane;
-    acc += warp_sum64(bb < b ? seq_pages(p, bb, false) : 0);
+    acc += warp_sum64(bb < b ? seq_chunks(p, bb, false) : 0);
   }
   return acc * p.g.hkv;
 }
 
-// Position in the flattened page list: sequence b, kv head, logical page.
+// Position in the flattened chunk list: sequence b, kv head, chunk c of nc.
 struct Cursor {
   int b, kvh;
-  int64_t lp, np;
+  int64_t c, nc;
 };
 
-__device__ __forceinline__ Cursor cursor_at(const DecodeParams& p, int64_t pidx) {
+__device__ __forceinline__ Cursor cursor_at(const DecodeParams& p, int64_t idx) {
   const int lane = threadIdx.x & 31;
   int64_t acc = 0;
-  Cursor c{p.g.batch, 0, 0, 0};
+  Cursor cur{p.g.batch, 0, 0, 0};
   for (int b0 = 0; b0 < p.g.batch; b0 += 32) {
     const int b = b0 + lane;
-    const int64_t np = b < p.g.batch ? seq_pages(p, b, false) * p.g.hkv : 0;
-    int64_t incl = np;
+    const int64_t n = b < p.g.batch ? seq_chunks(p, b, false) * p.g.hkv : 0;
+    int64_t incl = n;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int64_t t = __shfl_up_sync(kFull, incl, o);
       if (lane >= o) incl += t;
     }
-    const int64_t excl = incl - np;
-    const unsigned hit = __ballot_sync(kFull, np > 0 && acc + excl <= pidx && pidx < acc + incl);
+    const int64_t excl = incl - n;
+    const unsigned hit = __ballot_sync(kFull, n > 0 && acc + excl <= idx && idx < acc + incl);
     if (hit) {
       const int src = __ffs(hit) - 1;
       const int64_t base = acc + __shfl_sync(kFull, excl, src);
-      const int64_t npb = __shfl_sync(kFull, np, src) / p.g.hkv;
-      const int64_t within = pidx - base;
-      c.b = b0 + src;
-      c.np = npb;
-      c.kvh = (int)(within / npb);
-      c.lp = within % npb;
-      return c;
+      const int64_t ncb = __shfl_sync(kFull, n, src) / p.g.hkv;
+      const int64_t within = idx - base;
+      cur.b = b0 + src;
+      cur.nc = ncb;
+      cur.kvh = (int)(within / ncb);
+      cur.c = within % ncb;
+      return cur;
     }
     acc += __shfl_sync(kFull, incl, 31);
   }
-  return c;
+  return cur;
 }
 
-__device__ __forceinline__ void cursor_next(const DecodeParams& p, Cursor& c) {
-  if (++c.lp < c.np) return;
-  c.lp = 0;
-  if (++c.kvh < p.g.hkv) return;
-  c.kvh = 0;
+__device__ __forceinline__ void cursor_next(const DecodeParams& p, Cursor& cur) {
+  if (++cur.c < cur.nc) return;
+  cur.c = 0;
+  if (++cur.kvh < p.g.hkv) return;
+  cur.kvh = 0;
   do {
-    ++c.b;
-    c.np = c.b < p.g.batch ? seq_pages(p, c.b, false) : 0;
-  } while (c.b < p.g.batch && c.np == 0);
+    ++cur.b;
+    cur.nc = cur.b < p.g.batch ? seq_chunks(p, cur.b, false) : 0;
+  } while (cur.b < p.g.batch && cur.nc == 0);
 }
 
-// Scales of one token's record: NB values of the runtime scale type.
-template <int NB>
-__device__ __forceinline__ void load_scales(const uint8_t* hdr, int tok, int type, float (&s)[NB]) {
-  if (type == KVQ3_SCALE_F32) {
-    const float* f = reinterpret_cast<const float*>(hdr) + tok * NB;
+// Scales of tokens t and t+1 of a record header: NB values of type SCALE per
+// token, token-major, read with one vector load.
+template <int NB, int SCALE>
+struct ScaleIO {
+  static constexpr int SB = SCALE == KVQ3_SCALE_F32 ? 4 : SCALE == KVQ3_SCALE_F16 ? 2 : 1;
+  static constexpr int BPT = NB * SB;
+
+  template <int N>
+  __device__ static __forceinline__ void raw(const uint8_t* p, uint32_t (&w)[(N + 3) / 4]) {
+    if constexpr (N == 1) w[0] = *p;
+    else if constexpr (N == 2) w[0] = *reinterpret_cast<const uint16_t*>(p);
+    else if constexpr (N == 4) w[0] = *reinterpret_cast<const uint32_t*>(p);
+    else if constexpr (N == 8) {
+      const uint2 v = *reinterpret_cast<const uint2*>(p);
+      w[0] = v.x; w[1] = v.y;
+    } else {
 #pragma unroll
-    for (int i = 0; i < NB; ++i) s[i] = f[i];
-  } else if (type == KVQ3_SCALE_F16) {
-    const __half* h = reinterpret_cast<const __half*>(hdr) + tok * NB;
-#pragma unroll
-    for (int i = 0; i < NB; ++i) s[i] = __half2float(h[i]);
-  } else {
-    const uint8_t* b = hdr + tok * NB;
-#pragma unroll
-    for (int i = 0; i < NB; ++i) s[i] = decode_scale(b[i], KVQ3_SCALE_E4M3);
+      for (int i = 0; i < N / 16; ++i) {
+        const uint4 v = reinterpret_cast<const uint4*>(p)[i];
+        w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+      }
+    }
   }
-}
+
+  __device__ static __forceinline__ float value(const uint32_t* w, int i) {
+    if constexpr (SCALE == KVQ3_SCALE_F32) return __uint_as_float(w[i]);
+    else if constexpr (SCALE == KVQ3_SCALE_F16) {
+      const uint32_t h = (w[i / 2] >> (16 * (i & 1))) & 0xffffu;
+      return __half2float(__ushort_as_half((unsigned short)h));
+    } else {
+      const uint32_t b = (w[i / 4] >> (8 * (i & 3))) & 0xffu;
+      const __half_raw hr = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)b, __NV_E4M3);
+      return __half2float(__half(hr));
+    }
+  }
+
+  // one token
+  __device__ static __forceinline__ void one(const uint8_t* hdr, int t, float (&s)[NB]) {
+    uint32_t w[(BPT + 3) / 4];
+    raw<BPT>(hdr + t * BPT, w);
+#pragma unroll
+    for (int i = 0; i < NB; ++i) s[i] = value(w, i);
+  }
+
+  // tokens t, t+1 (t even, so the pair is aligned to its size)
+  __device__ static __forceinline__ void two(const uint8_t* hdr, int t, float (&s0)[NB], float (&s1)[NB]) {
+    uint32_t w[(2 * BPT + 3) / 4];
+    raw<2 * BPT>(hdr + t * BPT, w);
+    if constexpr (BPT >= 4) {
+#pragma unroll
+      for (int i = 0; i < NB; ++i) {
+        s0[i] = value(w, i);
+        s1[i] = value(w + BPT / 4, i);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < NB; ++i) {
+        s0[i] = value(w, i);
+        s1[i] = value(w, NB + i);
+      }
+    }
+  }
+};
 
 // half2 subtraction on raw bits
 __device__ __forceinline__ uint32_t hsub2_bits(uint32_t a, uint32_t b) {
@@ -210,7 +268,7 @@ __device__ __forceinline__ void v_codes_to_half2(uint32_t c0, uint32_t c1, uint3
   }
 }
 
-// 3*F bits of a code string starting at bit `boff` (two aligned words).
+// Bits [boff, boff + 64) of a code string (two aligned words, funnel shift).
 __device__ __forceinline__ void load_bits(const uint8_t* str, int boff, uint32_t& lo, uint32_t& hi) {
   const uint32_t* w = reinterpret_cast<const uint32_t*>(str) + (boff >> 5);
   const int sh = boff & 31;
@@ -219,23 +277,39 @@ __device__ __forceinline__ void load_bits(const uint8_t* str, int boff, uint32_t
   hi = w1 >> sh;
 }
 
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // ------------------------------------------------------------------ kernel 1
 template <int D, int GPAD>
 struct DecodeSmem {
-  static constexpr int kBarBytes = 64;  // up to 8 mbarriers
-  static constexpr int kQOff = kBarBytes;
-  static constexpr int kQInvOff = kQOff + GPAD * D * 4;
+  static constexpr int kFullOff = 0;                              // kMaxStages mbarriers
+  static constexpr int kEmptyOff = kFullOff + 8 * kMaxStages;     // kMaxStages mbarriers
+  static constexpr int kMLOff = kEmptyOff + 8 * kMaxStages;       // [kWarps][2][GPAD] floats
+  static constexpr int kQOff = (kMLOff + kWarps * 2 * GPAD * 4 + 15) / 16 * 16;  // [GPAD][D]
+  static constexpr int kQInvOff = kQOff + GPAD * D * 4;           // [GPAD]
   static constexpr int kStageOff = ((kQInvOff + GPAD * 4) + 127) / 128 * 128;
 };
 
+// Resident CTAs per SM the register budget is sized for: the accumulators
+// (D/16 x 4 per PV n-tile) and the q1 fragments (D/8 per QK n-tile) grow
+// with D and the group padding.
+__host__ __device__ constexpr int decode_min_blocks(int D, int GPAD) {
+  return GPAD == 16 ? (D == 256 ? 1 : 2) : GPAD == 8 ? (D == 256 ? 2 : 3) : (D == 256 ? 3 : 4);
+}
+
 // PSPLIT: the probabilities-times-value-scales P' enter PV as hi + lo fp16
-// halves too (PV n-tile = 4 heads x (hi, lo), like QK); otherwise one fp16
-// value per head (PV n-tile = 8 heads).  The split is needed when the value
-// scales are fp32 (p = 1 times an fp32 scale is not an fp16 value) and free
-// when G <= 4 (the 8-column tile has room).
-template <int D, int BLOCK, int GPAD, bool PSPLIT>
-__global__ void __launch_bounds__(128) decode_split_kernel(const __grid_constant__ DecodeParams p,
-                                                           const __grid_constant__ RotParams rp) {
+// halves (PV n-tile = 4 heads x (hi, lo), like QK) -- needed when the value
+// scales are fp32, since p = 1 times an fp32 scale is not an fp16 value;
+// otherwise one fp16 value per head (PV n-tile = 8 heads).
+template <int D, int BLOCK, int GPAD, int SCALE, bool PSPLIT>
+__global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD)) decode_split_kernel(const __grid_constant__ DecodeParams p,
+                                                              const __grid_constant__ RotParams rp) {
   constexpr int NB = D / BLOCK;
   constexpr int KS = D / 16;          // k-steps of QK^T == M-tiles of PV
   constexpr int KSB = BLOCK / 16;     // per block
@@ -248,51 +322,71 @@ __global__ void __launch_bounds__(128) decode_split_kernel(const __grid_constant
   constexpr int LQ = D / EQ;
   constexpr int GPWQ = 32 / LQ;
   using SM = DecodeSmem<D, GPAD>;
+  using SIO = ScaleIO<NB, SCALE>;
 
   extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x & 31;
   const int wid = threadIdx.x >> 5;
   const int j = lane & 3, r = lane >> 2;
-  uint8_t* my = smem + (size_t)wid * p.warp_smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(my);
-  float* qs = reinterpret_cast<float*>(my + SM::kQOff);
-  float* qinv_s = reinterpret_cast<float*>(my + SM::kQInvOff);
-  uint8_t* stg = my + SM::kStageOff;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::kFullOff);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + SM::kEmptyOff);
+  float* ml_s = reinterpret_cast<float*>(smem + SM::kMLOff);
+  float* qs = reinterpret_cast<float*>(smem + SM::kQOff);
+  float* qinv_s = reinterpret_cast<float*>(smem + SM::kQInvOff);
+  uint8_t* stg = smem + SM::kStageOff;
   const int S = p.stages;
+  const CacheGeom& g = p.g;
 
-  const int64_t gw = (int64_t)blockIdx.x * p.warps_per_cta + wid;
-  const int64_t T = total_pages(p, gw == 0);
-  const int64_t W = p.total_warps;
-  const int64_t p0 = gw * T / W, p1 = (gw + 1) * T / W;
-  if (p0 >= p1) return;
+  const int64_t cta = blockIdx.x;
+  const int64_t T = total_chunks(p, cta == 0 && wid == 0);
+  const int64_t W = p.ctas;
+  const int64_t c0 = cta * T / W, c1 = (cta + 1) * T / W;
+  if (c0 >= c1) return;  // uniform over the CTA
+  const int64_t nch = c1 - c0;
 
-  if (lane == 0) {
-    for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kWarps);
+    }
     fence_mbar_init();
   }
-  __syncwarp();
+  __syncthreads();
   const uint64_t pol = policy_evict_first();
-  const int64_t npg = p1 - p0;
-  Cursor cp = cursor_at(p, p0);
-  Cursor cc = cp;
+  Cursor cp = cursor_at(p, c0);   // producer (thread 0)
+  Cursor cc = cp;                 // consumers
 
+  // bulk copies of the chunk's pages (each page: K record then V record)
   auto issue = [&](const Cursor& c, int stage) {
-    if (lane == 0) {
-      const int64_t page = page_of(p.g, p.page_table, c.b, c.lp);
-      uint8_t* dst = stg + (size_t)stage * p.stage_bytes;
-      if (page >= 0) {
-        mbar_expect_tx(&bars[stage], p.copy_bytes);
-        bulk_g2s(dst, p.pool + record_offset(p.g, page, c.kvh, 0), p.copy_bytes, &bars[stage], pol);
-      } else {
-        set_status(p.status, KVQ3_DEV_BAD_PAGE);
-        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&bars[stage]))
-                     : "memory");
-      }
+    uint8_t* dst = stg + (size_t)stage * p.stage_bytes;
+    const int64_t len = p.seq_lens[c.b];
+    const int64_t tok0 = c.c * p.chunk_tokens;
+    const int npg = (int)min((int64_t)p.pages_per_chunk, (len - tok0 + g.page_size - 1) / g.page_size);
+    const int64_t lp0 = tok0 / g.page_size;
+    uint32_t bytes = 0;
+    int64_t pages[kChunk / 16];
+    int bad = 0;
+    for (int i = 0; i < npg; ++i) {
+      pages[i] = page_of(g, p.page_table, c.b, lp0 + i);
+      if (pages[i] >= 0) bytes += (uint32_t)(2 * g.record_bytes);
+      else bad = 1;
+    }
+    if (bad) set_status(p.status, KVQ3_DEV_BAD_PAGE);
+    if (bytes) {
+      mbar_expect_tx(&full[stage], bytes);
+      for (int i = 0; i < npg; ++i)
+        if (pages[i] >= 0)
+          bulk_g2s(dst + (size_t)i * 2 * g.record_bytes, p.pool + record_offset(g, pages[i], c.kvh, 0),
+                   (uint32_t)(2 * g.record_bytes), &full[stage], pol);
+    } else {
+      mbar_arrive(&full[stage]);
     }
   };
-  for (int64_t i = 0; i < npg && i < S; ++i) {
-    issue(cp, (int)i);
-    cursor_next(p, cp);
+  if (threadIdx.x == 0) {
+    for (int64_t i = 0; i < nch && i < S; ++i) {
+      issue(cp, (int)i);
+      cursor_next(p, cp);
+    }
   }
 
   // per-lane query rotation parameters (dims rq*EQ ..)
@@ -308,8 +402,9 @@ __global__ void __launch_bounds__(128) decode_split_kernel(const __grid_constant
   float acc[KS][NTP][4];
   int cur_unit = -1;
 
+  // merge the four warps' states of a unit into workspace slot (cta + unit)
   auto flush = [&](int unit) {
-    float* slot = p.ws + (size_t)(gw + unit) * p.slot_floats;
+    float* slot = p.ws + (size_t)(cta + unit) * p.slot_floats;
     float* mS = slot + p.G * D;
     float* lS = mS + p.G;
 #pragma unroll
@@ -318,48 +413,98 @@ __global__ void __launch_bounds__(128) decode_split_kernel(const __grid_constant
       lt += __shfl_xor_sync(kFull, lt, 4);
       lt += __shfl_xor_sync(kFull, lt, 8);
       lt += __shfl_xor_sync(kFull, lt, 16);
-      const int h = 4 * tq + j;
-      if (r == 0 && h < p.G) {
-        mS[h] = m[tq];
-        lS[h] = lt;
+      if (r == 0) {
+        ml_s[(wid * 2 + 0) * GPAD + 4 * tq + j] = m[tq];
+        ml_s[(wid * 2 + 1) * GPAD + 4 * tq + j] = lt;
       }
     }
+    named_barrier(1, 128);
+    float cw[NTQ];  // this warp's weight for QK head 4tq + j
 #pragma unroll
-    for (int mt = 0; mt < KS; ++mt) {
-      const int b = mt / KSB, mp = mt % KSB;
+    for (int tq = 0; tq < NTQ; ++tq) {
+      const int h = 4 * tq + j;
+      float M = -INFINITY;
 #pragma unroll
-      for (int tp = 0; tp < NTP; ++tp) {
-        if constexpr (PSPLIT) {
-          // columns 2j, 2j+1: head 4tp+j, hi and lo parts
-          const int h = 4 * tp + j;
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ml_s[(w * 2) * GPAD + h]);
+      cw[tq] = M == -INFINITY ? 0.0f : ex2(m[tq] - M);
+      if (wid == 0 && r == 0 && h < p.G) {
+        float L = 0.0f;
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int f = 2 * mp + e;
-            const int dim = b * BLOCK + r * FV + f;
-            if (h < p.G)
-              slot[h * D + dim] = (acc[mt][tp][2 * e] + acc[mt][tp][2 * e + 1]) *
-                                  (1.0f / (float)(1 << v_off(f)));
+        for (int w = 0; w < kWarps; ++w) {
+          const float mw = ml_s[(w * 2) * GPAD + h];
+          L += (M == -INFINITY ? 0.0f : ex2(mw - M)) * ml_s[(w * 2 + 1) * GPAD + h];
+        }
+        mS[h] = M;
+        lS[h] = L;
+      }
+    }
+    // weights for the PV columns this lane holds
+    float cpv[NTP][2];
+#pragma unroll
+    for (int tp = 0; tp < NTP; ++tp) {
+      if constexpr (PSPLIT) {
+        cpv[tp][0] = cpv[tp][1] = cw[tp];
+      } else {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int hc = 8 * tp + 2 * j + e;
+          float v = 0.0f;
+#pragma unroll
+          for (int tq = 0; tq < NTQ; ++tq) {
+            const float t = __shfl_sync(kFull, cw[tq], hc & 3);
+            v = (tq == (hc >> 2)) ? t : v;
           }
-        } else {
-#pragma unroll
-          for (int reg = 0; reg < 4; ++reg) {
-            const int f = 2 * mp + (reg >> 1);
-            const int dim = b * BLOCK + r * FV + f;
-            const int h = 8 * tp + 2 * j + (reg & 1);
-            if (h < p.G) slot[h * D + dim] = acc[mt][tp][reg] * (1.0f / (float)(1 << v_off(f)));
-          }
+          cpv[tp][e] = v;
         }
       }
     }
+    // warp 0 stores its weighted state, then warps 1..3 add theirs
+    for (int pass = 0; pass < 2; ++pass) {
+      if ((pass == 0) == (wid == 0)) {
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          const int b = mt / KSB, mp = mt % KSB;
+#pragma unroll
+          for (int tp = 0; tp < NTP; ++tp) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {      // row r (e = 0) or r + 8 (e = 1)
+              const int f = 2 * mp + e;
+              const int dim = b * BLOCK + r * FV + f;
+              const float sc = 1.0f / (float)(1 << v_off(f));
+              if constexpr (PSPLIT) {
+                const int h = 4 * tp + j;
+                const float v = (acc[mt][tp][2 * e] + acc[mt][tp][2 * e + 1]) * sc * cpv[tp][0];
+                if (h < p.G) {
+                  if (pass == 0) slot[h * D + dim] = v;
+                  else atomicAdd(&slot[h * D + dim], v);
+                }
+              } else {
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                  const int h = 8 * tp + 2 * j + c;
+                  const float v = acc[mt][tp][2 * e + c] * sc * cpv[tp][c];
+                  if (h < p.G) {
+                    if (pass == 0) slot[h * D + dim] = v;
+                    else atomicAdd(&slot[h * D + dim], v);
+                  }
+                }
+              }
+            }
+          }
+        }
+      }
+      named_barrier(1, 128);
+    }
   };
 
+  // rotate the unit's G query heads once per CTA, then build each warp's
+  // B fragments: qs[g][dim] = (U q)[dim] * sm_scale*log2e * 2^e_g
   auto setup_unit = [&](int b, int kvh) {
-    // rotate the G query heads: qs[g][dim] = (U q)[dim] * sm_scale*log2e * 2^e_g
-    for (int g0 = 0; g0 < GPAD; g0 += GPWQ) {
-      const int g = g0 + gq;
-      const bool valid = g < p.G;
+    for (int g0 = wid * GPWQ; g0 < GPAD; g0 += kWarps * GPWQ) {
+      const int gg = g0 + gq;
+      const bool valid = gg < p.G;
       float x[EQ];
-      const __half* src = p.q + ((int64_t)b * p.Hq + (int64_t)kvh * p.G + g) * D + rq * EQ;
+      const __half* src = p.q + ((int64_t)b * p.Hq + (int64_t)kvh * p.G + gg) * D + rq * EQ;
 #pragma unroll
       for (int e = 0; e < EQ; ++e) x[e] = valid ? __half2float(src[e]) : 0.0f;
       rotate_forward<EQ, LQ>(x, rq, sgn_q, quat_q, p.inv_sqrt_d, so4);
@@ -375,13 +520,13 @@ __global__ void __launch_bounds__(128) decode_split_kernel(const __grid_constant
       if (amax > 0.0f) frexpf(amax, &ex);           // amax < 2^ex
       ex = max(-100, min(100, 8 - ex));               // scaled max in (2^7, 2^8]
       const float sc = ldexpf(1.0f, ex);
-      if (g < GPAD) {
+      if (gg < GPAD) {
 #pragma unroll
-        for (int e = 0; e < EQ; ++e) qs[g * D + rq * EQ + e] = x[e] * sc;
-        if (rq == 0) qinv_s[g] = ldexpf(1.0f, -ex);
+        for (int e = 0; e < EQ; ++e) qs[gg * D + rq * EQ + e] = x[e] * sc;
+        if (rq == 0) qinv_s[gg] = ldexpf(1.0f, -ex);
       }
     }
-    __syncwarp();
+    named_barrier(1, 128);
 #pragma unroll
     for (int tq = 0; tq < NTQ; ++tq) {
       const int head = 4 * tq + (r >> 1);
@@ -397,20 +542,13 @@ __global__ void __launch_bounds__(128) decode_split_kernel(const __grid_constant
           const float vlo = qs[head * D + dlo] * (1.0f / (float)(1 << kq_lo_off(k)));
           const float vhi = qs[head * D + dhi] * (1.0f / (float)(1 << kq_hi_off(k)));
           const __half hlo = __float2half_rn(vlo), hhi = __float2half_rn(vhi);
-          float olo, ohi;
-          if (part == 0) {
-            olo = __half2float(hlo);
-            ohi = __half2float(hhi);
-          } else {
-            olo = vlo - __half2float(hlo);
-            ohi = vhi - __half2float(hhi);
-          }
+          const float olo = part == 0 ? __half2float(hlo) : vlo - __half2float(hlo);
+          const float ohi = part == 0 ? __half2float(hhi) : vhi - __half2float(hhi);
           qf[tq][s][hf] = pack_half2(olo, ohi);
         }
       }
       qinv[tq] = qinv_s[4 * tq + j];
     }
-    __syncwarp();
 #pragma unroll
     for (int tq = 0; tq < NTQ; ++tq) {
       m[tq] = -INFINITY;
@@ -421,217 +559,228 @@ __global__ void __launch_bounds__(128) decode_split_kernel(const __grid_constant
 #pragma unroll
       for (int tp = 0; tp < NTP; ++tp)
 #pragma unroll
-        for (int reg = 0; reg < 4; ++reg) acc[mt][tp][reg] = 0.0f;
+        for (int c = 0; c < 4; ++c) acc[mt][tp][c] = 0.0f;
+    named_barrier(1, 128);  // qs is rewritten at the next unit
   };
 
-  const int stype = p.g.scale_type;
-  for (int64_t i = 0; i < npg; ++i) {
+  // one 16-token step at token offset t0 of a page whose records start at pg
+  auto step = [&](const uint8_t* pg, int t0, int n_valid) {
+    const uint8_t* kS = pg;
+    const uint8_t* kC = pg + g.scale_hdr_bytes;
+    const uint8_t* vS = pg + g.record_bytes;
+    const uint8_t* vC = vS + g.scale_hdr_bytes;
+    // ------------------------------------------------ S = K q1 (per block)
+    float accq[NB][NTQ][4];
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+#pragma unroll
+      for (int tq = 0; tq < NTQ; ++tq)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) accq[b][tq][c] = 0.0f;
+    const uint8_t* k0 = kC + (t0 + r) * CB;
+    const uint8_t* k8 = k0 + 8 * CB;
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      uint32_t h0[FQ / 2], h1[FQ / 2];
+      uint32_t lo, hi;
+      const int boff = 3 * (b * BLOCK + j * FQ);
+      load_bits(k0, boff, lo, hi);
+      k_codes_to_half2<FQ>(lo, hi, h0);
+      load_bits(k8, boff, lo, hi);
+      k_codes_to_half2<FQ>(lo, hi, h1);
+#pragma unroll
+      for (int sp = 0; sp < KSB; ++sp) {
+        const uint32_t a[4] = {h0[2 * sp], h1[2 * sp], h0[2 * sp + 1], h1[2 * sp + 1]};
+#pragma unroll
+        for (int tq = 0; tq < NTQ; ++tq)
+          mma_16816(accq[b][tq], a, qf[tq][b * KSB + sp][0], qf[tq][b * KSB + sp][1]);
+      }
+    }
+    float skr[NB], skr8[NB];
+    SIO::one(kS, t0 + r, skr);
+    SIO::one(kS, t0 + r + 8, skr8);
+    const bool vr = t0 + r < n_valid, vr8 = t0 + r + 8 < n_valid;
+    // ------------------------------------------------ online softmax
+    float pr[NTQ], pr8[NTQ], alpha[NTQ];
+    bool changed = false;
+#pragma unroll
+    for (int tq = 0; tq < NTQ; ++tq) {
+      float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        s0 = fmaf(skr[b], accq[b][tq][0] + accq[b][tq][1], s0);
+        s1 = fmaf(skr8[b], accq[b][tq][2] + accq[b][tq][3], s1);
+      }
+      s0 = vr ? s0 * qinv[tq] : -INFINITY;
+      s1 = vr8 ? s1 * qinv[tq] : -INFINITY;
+      float mx = fmaxf(s0, s1);
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+      const float mn = fmaxf(m[tq], mx);   // finite: every step has a valid token
+      alpha[tq] = ex2(m[tq] - mn);
+      pr[tq] = ex2(s0 - mn);
+      pr8[tq] = ex2(s1 - mn);
+      l[tq] = fmaf(l[tq], alpha[tq], pr[tq] + pr8[tq]);
+      m[tq] = mn;
+      changed |= alpha[tq] != 1.0f;
+    }
+    if (__any_sync(kFull, changed)) {
+      if constexpr (PSPLIT) {
+        // this lane's PV columns belong to its own QK head 4tp + j
+#pragma unroll
+        for (int tp = 0; tp < NTP; ++tp)
+#pragma unroll
+          for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[mt][tp][c] *= alpha[tp];
+      } else {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float av[NTQ];
+#pragma unroll
+          for (int tq = 0; tq < NTQ; ++tq) av[tq] = __shfl_sync(kFull, alpha[tq], (2 * j + e) & 3);
+#pragma unroll
+          for (int tp = 0; tp < NTP; ++tp) {
+            const int tsel = (8 * tp + 2 * j + e) >> 2;
+            float a = 1.0f;
+#pragma unroll
+            for (int tq = 0; tq < NTQ; ++tq) a = (tq == tsel) ? av[tq] : a;
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+              acc[mt][tp][e] *= a;
+              acc[mt][tp][2 + e] *= a;
+            }
+          }
+        }
+      }
+    }
+    // ------------------------------------------------ P' = p * s_v (B of PV)
+    const int T0 = t0 + 2 * j;
+    float x0[NTQ], x1[NTQ], x2[NTQ], x3[NTQ];
+    {
+      // B element (token T, column r) comes from QK lane 4*(T%8) + head%4
+      const int hl = PSPLIT ? (r >> 1) : (r & 3);
+      const int srcA = 8 * j + hl, srcB = 8 * j + 4 + hl;
+#pragma unroll
+      for (int tq = 0; tq < NTQ; ++tq) {
+        x0[tq] = __shfl_sync(kFull, pr[tq], srcA);
+        x1[tq] = __shfl_sync(kFull, pr[tq], srcB);
+        x2[tq] = __shfl_sync(kFull, pr8[tq], srcA);
+        x3[tq] = __shfl_sync(kFull, pr8[tq], srcB);
+      }
+    }
+    float sv0[NB], sv1[NB], sv2[NB], sv3[NB];
+    SIO::two(vS, T0, sv0, sv1);
+    SIO::two(vS, T0 + 8, sv2, sv3);
+    const bool v0 = T0 < n_valid, v1 = T0 + 1 < n_valid, v2 = T0 + 8 < n_valid,
+               v3 = T0 + 9 < n_valid;
+    uint32_t pb[NB][NTP][2];
+    if constexpr (PSPLIT) {
+#pragma unroll
+      for (int tp = 0; tp < NTP; ++tp) {
+        const bool hv = 4 * tp + (r >> 1) < p.G;
+        const bool lo_part = (r & 1) != 0;
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          const float y0 = hv && v0 ? x0[tp] * sv0[b] : 0.0f;
+          const float y1 = hv && v1 ? x1[tp] * sv1[b] : 0.0f;
+          const float y2 = hv && v2 ? x2[tp] * sv2[b] : 0.0f;
+          const float y3 = hv && v3 ? x3[tp] * sv3[b] : 0.0f;
+          const __half2 h01 = __floats2half2_rn(y0, y1), h23 = __floats2half2_rn(y2, y3);
+          if (lo_part) {
+            const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+            pb[b][tp][0] = pack_half2(y0 - f01.x, y1 - f01.y);
+            pb[b][tp][1] = pack_half2(y2 - f23.x, y3 - f23.y);
+          } else {
+            pb[b][tp][0] = *reinterpret_cast<const uint32_t*>(&h01);
+            pb[b][tp][1] = *reinterpret_cast<const uint32_t*>(&h23);
+          }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int tp = 0; tp < NTP; ++tp) {
+        const int hp = 8 * tp + r;
+        const int tsel = hp >> 2;
+        float y0 = 0.0f, y1 = 0.0f, y2 = 0.0f, y3 = 0.0f;
+#pragma unroll
+        for (int tq = 0; tq < NTQ; ++tq)
+          if (tq == tsel) {
+            y0 = x0[tq];
+            y1 = x1[tq];
+            y2 = x2[tq];
+            y3 = x3[tq];
+          }
+        const bool hv = hp < p.G;
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          pb[b][tp][0] = pack_half2(hv && v0 ? y0 * sv0[b] : 0.0f, hv && v1 ? y1 * sv1[b] : 0.0f);
+          pb[b][tp][1] = pack_half2(hv && v2 ? y2 * sv2[b] : 0.0f, hv && v3 ? y3 * sv3[b] : 0.0f);
+        }
+      }
+    }
+    // ------------------------------------------------ o1^T += V^T P'^T
+    const uint8_t* vt = vC + T0 * CB;
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      const int boff = 3 * (b * BLOCK + r * FV);
+      uint32_t c0v, c1v, c2v, c3v, dummy;
+      load_bits(vt, boff, c0v, dummy);
+      load_bits(vt + CB, boff, c1v, dummy);
+      load_bits(vt + 8 * CB, boff, c2v, dummy);
+      load_bits(vt + 9 * CB, boff, c3v, dummy);
+      uint32_t hv01[FV], hv89[FV];
+      v_codes_to_half2<FV>(c0v, c1v, hv01);
+      v_codes_to_half2<FV>(c2v, c3v, hv89);
+#pragma unroll
+      for (int mp = 0; mp < KSB; ++mp) {
+        const uint32_t a[4] = {hv01[2 * mp], hv01[2 * mp + 1], hv89[2 * mp], hv89[2 * mp + 1]};
+#pragma unroll
+        for (int tp = 0; tp < NTP; ++tp) mma_16816(acc[b * KSB + mp][tp], a, pb[b][tp][0], pb[b][tp][1]);
+      }
+    }
+  };
+
+  const int P = g.page_size;
+  for (int64_t i = 0; i < nch; ++i) {
     const int stage = (int)(i % S);
     const uint32_t parity = (uint32_t)((i / S) & 1);
-    const int unit = cc.b * p.g.hkv + cc.kvh;
+    const int unit = cc.b * g.hkv + cc.kvh;
     if (unit != cur_unit) {
       if (cur_unit >= 0) flush(cur_unit);
       setup_unit(cc.b, cc.kvh);
       cur_unit = unit;
     }
-    if (!mbar_wait(&bars[stage], parity, p.wait_limit)) {
+    if (!mbar_wait(&full[stage], parity, p.wait_limit)) {
       // a copy never arrived: flag it, wait (bounded) for the copies still in
-      // flight so no asynchronous write outlives this warp, and stop
+      // flight so no asynchronous write outlives this CTA, and stop
       if (lane == 0) set_status(p.status, KVQ3_DEV_TIMEOUT);
-      for (int64_t k = i + 1; k < npg && k < i + S; ++k)
-        mbar_wait(&bars[k % S], (uint32_t)((k / S) & 1), p.wait_limit);
+      for (int64_t k = i + 1; k < nch && k < i + S; ++k)
+        mbar_wait(&full[k % S], (uint32_t)((k / S) & 1), p.wait_limit);
       return;
     }
-    const int64_t page = page_of(p.g, p.page_table, cc.b, cc.lp);
-    if (page >= 0) {
-      const int64_t len = p.seq_lens[cc.b];
-      const int n_valid = (int)min((int64_t)p.g.page_size, len - cc.lp * p.g.page_size);
-      const uint8_t* st = stg + (size_t)stage * p.stage_bytes;
-      const uint8_t* kS = st;
-      const uint8_t* kC = st + p.g.scale_hdr_bytes;
-      const uint8_t* vS = st + p.g.record_bytes;
-      const uint8_t* vC = vS + p.g.scale_hdr_bytes;
-      for (int t0 = 0; t0 < n_valid; t0 += 16) {
-        // ------------------------------------------------ S = K q1 (per block)
-        float accq[NB][NTQ][4];
-#pragma unroll
-        for (int b = 0; b < NB; ++b)
-#pragma unroll
-          for (int tq = 0; tq < NTQ; ++tq)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) accq[b][tq][c] = 0.0f;
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-          uint32_t h0[FQ / 2], h1[FQ / 2];
-          uint32_t lo, hi;
-          const int boff = 3 * (b * BLOCK + j * FQ);
-          load_bits(kC + (t0 + r) * CB, boff, lo, hi);
-          k_codes_to_half2<FQ>(lo, hi, h0);
-          load_bits(kC + (t0 + r + 8) * CB, boff, lo, hi);
-          k_codes_to_half2<FQ>(lo, hi, h1);
-#pragma unroll
-          for (int sp = 0; sp < KSB; ++sp) {
-            const uint32_t a[4] = {h0[2 * sp], h1[2 * sp], h0[2 * sp + 1], h1[2 * sp + 1]};
-#pragma unroll
-            for (int tq = 0; tq < NTQ; ++tq)
-              mma_16816(accq[b][tq], a, qf[tq][b * KSB + sp][0], qf[tq][b * KSB + sp][1]);
-          }
-        }
-        float skr[NB], skr8[NB];
-        load_scales<NB>(kS, t0 + r, stype, skr);
-        load_scales<NB>(kS, t0 + r + 8, stype, skr8);
-        const bool vr = t0 + r < n_valid, vr8 = t0 + r + 8 < n_valid;
-        // ------------------------------------------------ online softmax
-        float pr[NTQ], pr8[NTQ];
-        bool changed = false;
-        float alpha[NTQ];
-#pragma unroll
-        for (int tq = 0; tq < NTQ; ++tq) {
-          float s0 = 0.0f, s1 = 0.0f;
-#pragma unroll
-          for (int b = 0; b < NB; ++b) {
-            s0 += skr[b] * (accq[b][tq][0] + accq[b][tq][1]);
-            s1 += skr8[b] * (accq[b][tq][2] + accq[b][tq][3]);
-          }
-          s0 = vr ? s0 * qinv[tq] : -INFINITY;
-          s1 = vr8 ? s1 * qinv[tq] : -INFINITY;
-          float mx = fmaxf(s0, s1);
-          mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
-          mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
-          mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
-          const float mn = fmaxf(m[tq], mx);
-          if (mn == -INFINITY) {
-            alpha[tq] = 1.0f;
-            pr[tq] = 0.0f;
-            pr8[tq] = 0.0f;
-          } else {
-            alpha[tq] = ex2(m[tq] - mn);
-            pr[tq] = ex2(s0 - mn);
-            pr8[tq] = ex2(s1 - mn);
-          }
-          l[tq] = l[tq] * alpha[tq] + pr[tq] + pr8[tq];
-          m[tq] = mn;
-          changed |= alpha[tq] != 1.0f;
-        }
-        if constexpr (PSPLIT) {
-          // this lane's PV columns belong to its own QK head 4tp + j
-          if (__any_sync(kFull, changed)) {
-#pragma unroll
-            for (int tp = 0; tp < NTP; ++tp)
-#pragma unroll
-              for (int mt = 0; mt < KS; ++mt)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) acc[mt][tp][c] *= alpha[tp];
-          }
-        } else if (__any_sync(kFull, changed)) {
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            float av[NTQ];
-#pragma unroll
-            for (int tq = 0; tq < NTQ; ++tq) av[tq] = __shfl_sync(kFull, alpha[tq], (2 * j + e) & 3);
-#pragma unroll
-            for (int tp = 0; tp < NTP; ++tp) {
-              const int tsel = (8 * tp + 2 * j + e) >> 2;
-              float a = 1.0f;
-#pragma unroll
-              for (int tq = 0; tq < NTQ; ++tq) a = (tq == tsel) ? av[tq] : a;
-#pragma unroll
-              for (int mt = 0; mt < KS; ++mt) {
-                acc[mt][tp][e] *= a;
-                acc[mt][tp][2 + e] *= a;
-              }
-            }
-          }
-        }
-        // ------------------------------------------------ P' = p * s_v (B of PV)
-        const int T0 = t0 + 2 * j;
-        float x0[NTQ], x1[NTQ], x2[NTQ], x3[NTQ];
-        {
-          // B element (token T, column r) comes from the QK lane 4*(T%8) + head%4
-          const int hl = PSPLIT ? (r >> 1) : (r & 3);
-          const int srcA = 8 * j + hl, srcB = 8 * j + 4 + hl;
-#pragma unroll
-          for (int tq = 0; tq < NTQ; ++tq) {
-            x0[tq] = __shfl_sync(kFull, pr[tq], srcA);
-            x1[tq] = __shfl_sync(kFull, pr[tq], srcB);
-            x2[tq] = __shfl_sync(kFull, pr8[tq], srcA);
-            x3[tq] = __shfl_sync(kFull, pr8[tq], srcB);
-          }
-        }
-        float sv0[NB], sv1[NB], sv2[NB], sv3[NB];
-        load_scales<NB>(vS, T0, stype, sv0);
-        load_scales<NB>(vS, T0 + 1, stype, sv1);
-        load_scales<NB>(vS, T0 + 8, stype, sv2);
-        load_scales<NB>(vS, T0 + 9, stype, sv3);
-        const bool v0 = T0 < n_valid, v1 = T0 + 1 < n_valid, v2 = T0 + 8 < n_valid,
-                   v3 = T0 + 9 < n_valid;
-        uint32_t pb[NB][NTP][2];
-        if constexpr (PSPLIT) {
-#pragma unroll
-          for (int tp = 0; tp < NTP; ++tp) {
-            const bool hv = 4 * tp + (r >> 1) < p.G;
-            const bool lo_part = (r & 1) != 0;
-            auto part = [&](float v) {
-              const float hi = __half2float(__float2half_rn(v));
-              return lo_part ? v - hi : hi;
-            };
-#pragma unroll
-            for (int b = 0; b < NB; ++b) {
-              const float y0 = hv && v0 ? x0[tp] * sv0[b] : 0.0f;
-              const float y1 = hv && v1 ? x1[tp] * sv1[b] : 0.0f;
-              const float y2 = hv && v2 ? x2[tp] * sv2[b] : 0.0f;
-              const float y3 = hv && v3 ? x3[tp] * sv3[b] : 0.0f;
-              pb[b][tp][0] = pack_half2(part(y0), part(y1));
-              pb[b][tp][1] = pack_half2(part(y2), part(y3));
-            }
-          }
-        } else {
-#pragma unroll
-        for (int tp = 0; tp < NTP; ++tp) {
-          const int hp = 8 * tp + r;
-          const int tsel = hp >> 2;
-          float y0 = 0.0f, y1 = 0.0f, y2 = 0.0f, y3 = 0.0f;
-#pragma unroll
-          for (int tq = 0; tq < NTQ; ++tq)
-            if (tq == tsel) {
-              y0 = x0[tq];
-              y1 = x1[tq];
-              y2 = x2[tq];
-              y3 = x3[tq];
-            }
-          const bool hv = hp < p.G;
-#pragma unroll
-          for (int b = 0; b < NB; ++b) {
-            pb[b][tp][0] = pack_half2(hv && v0 ? y0 * sv0[b] : 0.0f, hv && v1 ? y1 * sv1[b] : 0.0f);
-            pb[b][tp][1] = pack_half2(hv && v2 ? y2 * sv2[b] : 0.0f, hv && v3 ? y3 * sv3[b] : 0.0f);
-          }
-        }
-        }
-        // ------------------------------------------------ o1^T += V^T P'^T
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-          const int boff = 3 * (b * BLOCK + r * FV);
-          uint32_t c0, c1, c2, c3, dummy;
-          load_bits(vC + T0 * CB, boff, c0, dummy);
-          load_bits(vC + (T0 + 1) * CB, boff, c1, dummy);
-          load_bits(vC + (T0 + 8) * CB, boff, c2, dummy);
-          load_bits(vC + (T0 + 9) * CB, boff, c3, dummy);
-          uint32_t hv01[FV], hv89[FV];
-          v_codes_to_half2<FV>(c0, c1, hv01);
-          v_codes_to_half2<FV>(c2, c3, hv89);
-#pragma unroll
-          for (int mp = 0; mp < KSB; ++mp) {
-            const uint32_t a[4] = {hv01[2 * mp], hv01[2 * mp + 1], hv89[2 * mp], hv89[2 * mp + 1]};
-#pragma unroll
-            for (int tp = 0; tp < NTP; ++tp) mma_16816(acc[b * KSB + mp][tp], a, pb[b][tp][0], pb[b][tp][1]);
-          }
-        }
-      }
+    const int64_t len = p.seq_lens[cc.b];
+    const int64_t tok0 = cc.c * p.chunk_tokens;
+    const int n_chunk = (int)min((int64_t)p.chunk_tokens, len - tok0);
+    const uint8_t* st = stg + (size_t)stage * p.stage_bytes;
+    for (int s16 = wid; s16 * 16 < n_chunk; s16 += kWarps) {
+      const int t = s16 * 16;                       // token offset in the chunk
+      const int pi = t / P;                         // page within the chunk
+      if (page_of(g, p.page_table, cc.b, tok0 / P + pi) < 0) continue;  // masked page
+      step(st + (size_t)pi * 2 * g.record_bytes, t - pi * P, min(P, n_chunk - pi * P));
     }
     __syncwarp();
-    if (i + S < npg) {
-      fence_proxy_async();
-      issue(cp, stage);
+    if (lane == 0) mbar_arrive(&empty[stage]);
+    if (threadIdx.x == 0 && i + S < nch) {
+      // refill this stage once every warp has released it
+      if (mbar_wait(&empty[stage], parity, p.wait_limit)) {
+        fence_proxy_async();
+        issue(cp, stage);
+      } else {
+        set_status(p.status, KVQ3_DEV_TIMEOUT);
+        mbar_arrive(&full[stage]);  // keep the consumers' phases moving
+      }
       cursor_next(p, cp);
     }
     cursor_next(p, cc);
@@ -656,37 +805,37 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const __grid_consta
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int64_t items = (int64_t)p.g.batch * p.Hq;
-  const int64_t T = total_pages(p, false);
-  const int64_t W = p.total_warps;
+  const int64_t T = total_chunks(p, false);
+  const int64_t W = p.ctas;
   for (int64_t it = warp; it < items; it += nwarps) {
     const int b = (int)(it / p.Hq);
     const int h = (int)(it % p.Hq);
-    const int kvh = h / p.G, g = h % p.G;
-    const int64_t np = seq_pages(p, b, false);
+    const int kvh = h / p.G, gh = h % p.G;
+    const int64_t nc = seq_chunks(p, b, false);
     float o[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) o[e] = 0.0f;
-    if (np > 0) {
-      const int64_t pu = pages_before(p, b) + (int64_t)kvh * np;
+    if (nc > 0) {
+      const int64_t pu = chunks_before(p, b) + (int64_t)kvh * nc;
       const int unit = b * p.g.hkv + kvh;
+      // CTAs whose range meets [pu, pu + nc); CTAs with empty ranges wrote nothing
       const int64_t wlo = ((pu + 1) * W - 1) / T;
-      const int64_t whi = ((pu + np) * W - 1) / T;
+      const int64_t whi = ((pu + nc) * W - 1) / T;
       float M = -INFINITY;
-      // warps with an empty page range wrote nothing: skip them
       for (int64_t w = wlo; w <= whi; ++w) {
         if (w * T / W == (w + 1) * T / W) continue;
         const float* slot = p.ws + (size_t)(w + unit) * p.slot_floats;
-        M = fmaxf(M, slot[p.G * D + g]);
+        M = fmaxf(M, slot[p.G * D + gh]);
       }
       if (M != -INFINITY) {
         float lsum = 0.0f;
         for (int64_t w = wlo; w <= whi; ++w) {
           if (w * T / W == (w + 1) * T / W) continue;
           const float* slot = p.ws + (size_t)(w + unit) * p.slot_floats;
-          const float c = ex2(slot[p.G * D + g] - M);
-          lsum += c * slot[p.G * D + p.G + g];
+          const float c = ex2(slot[p.G * D + gh] - M);
+          lsum += c * slot[p.G * D + p.G + gh];
 #pragma unroll
-          for (int e = 0; e < E; ++e) o[e] += c * slot[g * D + rr * E + e];
+          for (int e = 0; e < E; ++e) o[e] += c * slot[gh * D + rr * E + e];
         }
         const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
 #pragma unroll
@@ -704,68 +853,50 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const __grid_consta
 // ------------------------------------------------------------------ host
 struct DecodePlan {
   int gpad;
-  bool psplit;
-  int warps_per_cta;
   int ctas;
   int stages;
-  uint32_t stage_bytes, copy_bytes, warp_smem;
+  int chunk_tokens, pages_per_chunk;
+  uint32_t stage_bytes, smem;
   size_t ws_bytes;
-  const void* kernel;
 };
 
-template <int D, int BLOCK, int GPAD, bool PSPLIT>
-const void* decode_kernel_ptr() {
-  return reinterpret_cast<const void*>(&decode_split_kernel<D, BLOCK, GPAD, PSPLIT>);
-}
-
-// Sizes the launch for the current device.
-template <int D, int BLOCK, int GPAD, bool PSPLIT>
+template <int D, int BLOCK, int GPAD, int SCALE, bool PSPLIT>
 kvq3_status decode_plan_t(const CacheGeom& g, int G, DecodePlan* plan) {
   using SM = DecodeSmem<D, GPAD>;
+  const void* k = reinterpret_cast<const void*>(&decode_split_kernel<D, BLOCK, GPAD, SCALE, PSPLIT>);
   plan->gpad = GPAD;
-  plan->psplit = PSPLIT;
-  plan->copy_bytes = (uint32_t)(2 * g.record_bytes);
-  plan->stage_bytes = (plan->copy_bytes + 16 + 15) / 16 * 16;
+  plan->chunk_tokens = g.page_size >= kChunk ? g.page_size : kChunk;
+  plan->pages_per_chunk = plan->chunk_tokens / g.page_size;
+  const size_t chunk_bytes = (size_t)plan->pages_per_chunk * 2 * g.record_bytes;
+  plan->stage_bytes = (uint32_t)((chunk_bytes + 16 + 127) / 128 * 128);  // +16: tail word reads
+  // aim for ~24 KB of stages per CTA (4 CTAs per SM), at least 2 stages
   int stages = (int)(24576 / plan->stage_bytes);
-  stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
-  int wpc = 4;
-  uint32_t warp_smem = 0;
-  for (;;) {
-    warp_smem = (uint32_t)((SM::kStageOff + (size_t)stages * plan->stage_bytes + 127) / 128 * 128);
-    if ((size_t)wpc * warp_smem <= 220 * 1024) break;
-    if (stages > 2) --stages;
-    else if (wpc > 1) wpc >>= 1;
-    else return KVQ3_ERR_UNSUPPORTED;  // pages too large for a two-stage ring
-  }
+  stages = stages < 2 ? 2 : (stages > 6 ? 6 : stages);
+  const size_t smem = SM::kStageOff + (size_t)stages * plan->stage_bytes;
+  if (smem > 220 * 1024) return KVQ3_ERR_UNSUPPORTED;  // pages too large for a two-stage ring
   plan->stages = stages;
-  plan->warps_per_cta = wpc;
-  plan->warp_smem = warp_smem;
-  const void* k = decode_kernel_ptr<D, BLOCK, GPAD, PSPLIT>();
-  plan->kernel = k;
-  const int smem = wpc * (int)warp_smem;
-  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+  plan->smem = (uint32_t)smem;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return KVQ3_ERR_CUDA;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, 32 * wpc, smem) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, 32 * kWarps, smem) != cudaSuccess)
     return KVQ3_ERR_CUDA;
   if (per_sm < 1) return KVQ3_ERR_UNSUPPORTED;
   plan->ctas = sm_count() * per_sm;
-  const size_t slots = (size_t)plan->ctas * wpc + (size_t)g.batch * g.hkv;
+  const size_t slots = (size_t)plan->ctas + (size_t)g.batch * g.hkv;
   plan->ws_bytes = slots * (size_t)G * (D + 2) * sizeof(float);
   return KVQ3_OK;
 }
 
-template <int D, int BLOCK, int GPAD, bool PSPLIT>
+template <int D, int BLOCK, int GPAD, int SCALE, bool PSPLIT>
 kvq3_status decode_run_t(const DecodePlan& plan, DecodeParams prm, const RotParams& rp, float* out,
                          cudaStream_t st) {
   prm.stages = plan.stages;
   prm.stage_bytes = plan.stage_bytes;
-  prm.copy_bytes = plan.copy_bytes;
-  prm.total_warps = plan.ctas * plan.warps_per_cta;
-  prm.warps_per_cta = plan.warps_per_cta;
-  prm.warp_smem = plan.warp_smem;
-  decode_split_kernel<D, BLOCK, GPAD, PSPLIT><<<plan.ctas, 32 * plan.warps_per_cta,
-                                        plan.warps_per_cta * plan.warp_smem, st>>>(prm, rp);
+  prm.chunk_tokens = plan.chunk_tokens;
+  prm.pages_per_chunk = plan.pages_per_chunk;
+  prm.ctas = plan.ctas;
+  decode_split_kernel<D, BLOCK, GPAD, SCALE, PSPLIT><<<plan.ctas, 32 * kWarps, plan.smem, st>>>(prm, rp);
   if (cudaGetLastError() != cudaSuccess) return KVQ3_ERR_CUDA;
   const int64_t items = (int64_t)prm.g.batch * prm.Hq;
   int64_t blocks = (items + 7) / 8;
@@ -775,35 +906,35 @@ kvq3_status decode_run_t(const DecodePlan& plan, DecodeParams prm, const RotPara
   return cudaGetLastError() == cudaSuccess ? KVQ3_OK : KVQ3_ERR_CUDA;
 }
 
-// Per-head-dim entry points (one translation unit each).
-kvq3_status decode_plan_d64(const CacheGeom& g, int G, DecodePlan* plan);
-kvq3_status decode_plan_d128(const CacheGeom& g, int G, DecodePlan* plan);
-kvq3_status decode_plan_d256(const CacheGeom& g, int G, DecodePlan* plan);
-kvq3_status decode_run_d64(const DecodePlan&, const DecodeParams&, const RotParams&, float*, cudaStream_t);
-kvq3_status decode_run_d128(const DecodePlan&, const DecodeParams&, const RotParams&, float*, cudaStream_t);
-kvq3_status decode_run_d256(const DecodePlan&, const DecodeParams&, const RotParams&, float*, cudaStream_t);
+// Per-(head dim, scale type) entry points, one translation unit each.
+#define KVQ3_DECODE_DECL(D, SN)                                                               \
+  kvq3_status decode_plan_d##D##_##SN(const CacheGeom& g, int G, DecodePlan* plan);          \
+  kvq3_status decode_run_d##D##_##SN(const DecodePlan&, const DecodeParams&, const RotParams&, \
+                                     float*, cudaStream_t);
+KVQ3_DECODE_DECL(64, f32) KVQ3_DECODE_DECL(64, f16) KVQ3_DECODE_DECL(64, e4m3)
+KVQ3_DECODE_DECL(128, f32) KVQ3_DECODE_DECL(128, f16) KVQ3_DECODE_DECL(128, e4m3)
+KVQ3_DECODE_DECL(256, f32) KVQ3_DECODE_DECL(256, f16) KVQ3_DECODE_DECL(256, e4m3)
 
-// Variant choice: P' split for G <= 4 (free) and for fp32 value scales.
-#define KVQ3_DECODE_PICK(D, BLK, FN, ...)                                                      \
+// P' split for fp32 value scales only.
+#define KVQ3_DECODE_PICK(D, BLK, SC, FN, ...)                                                 \
   {                                                                                           \
-    const bool f32 = g.scale_type == KVQ3_SCALE_F32;                                          \
-    if (gp == 4) return FN<D, BLK, 4, true>(__VA_ARGS__);                                     \
-    if (gp == 8) return f32 ? FN<D, BLK, 8, true>(__VA_ARGS__) : FN<D, BLK, 8, false>(__VA_ARGS__); \
-    return f32 ? FN<D, BLK, 16, true>(__VA_ARGS__) : FN<D, BLK, 16, false>(__VA_ARGS__);       \
+    constexpr bool SPLIT = (SC) == KVQ3_SCALE_F32;                                            \
+    if (gp == 4) return FN<D, BLK, 4, SC, SPLIT>(__VA_ARGS__);                                \
+    if (gp == 8) return FN<D, BLK, 8, SC, SPLIT>(__VA_ARGS__);                                \
+    return FN<D, BLK, 16, SC, SPLIT>(__VA_ARGS__);                                            \
   }
 
-#define KVQ3_DECODE_INSTANCES(D)                                                              \
-  kvq3_status decode_plan_d##D(const CacheGeom& g, int G, DecodePlan* plan) {                \
+#define KVQ3_DECODE_INSTANCES(D, SN, SC)                                                      \
+  kvq3_status decode_plan_d##D##_##SN(const CacheGeom& g, int G, DecodePlan* plan) {         \
     const int gp = G <= 4 ? 4 : (G <= 8 ? 8 : 16);                                            \
-    if (g.block == 32) KVQ3_DECODE_PICK(D, 32, decode_plan_t, g, G, plan)                     \
-    KVQ3_DECODE_PICK(D, 64, decode_plan_t, g, G, plan)                                        \
+    if (g.block == 32) KVQ3_DECODE_PICK(D, 32, SC, decode_plan_t, g, G, plan)                 \
+    KVQ3_DECODE_PICK(D, 64, SC, decode_plan_t, g, G, plan)                                    \
   }                                                                                           \
-  kvq3_status decode_run_d##D(const DecodePlan& plan, const DecodeParams& prm,                \
-                              const RotParams& rp, float* out, cudaStream_t st) {             \
-    const CacheGeom& g = prm.g;                                                               \
+  kvq3_status decode_run_d##D##_##SN(const DecodePlan& plan, const DecodeParams& prm,         \
+                                     const RotParams& rp, float* out, cudaStream_t st) {      \
     const int gp = plan.gpad;                                                                 \
-    if (g.block == 32) KVQ3_DECODE_PICK(D, 32, decode_run_t, plan, prm, rp, out, st)          \
-    KVQ3_DECODE_PICK(D, 64, decode_run_t, plan, prm, rp, out, st)                             \
+    if (prm.g.block == 32) KVQ3_DECODE_PICK(D, 32, SC, decode_run_t, plan, prm, rp, out, st)  \
+    KVQ3_DECODE_PICK(D, 64, SC, decode_run_t, plan, prm, rp, out, st)                         \
   }
 
 }  // namespace kvq3
