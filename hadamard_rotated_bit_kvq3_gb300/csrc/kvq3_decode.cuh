@@ -40,7 +40,7 @@
 
 namespace kvq3 {
 
-constexpr int kChunk = 64;       // tokens per chunk (pages smaller than this are grouped)
+constexpr int kChunk = 64;       // minimum tokens per chunk (smaller pages are grouped)
 constexpr int kWarps = 4;        // consumer warps per CTA
 constexpr int kMaxStages = 8;
 
@@ -156,70 +156,6 @@ __device__ __forceinline__ void cursor_next(const DecodeParams& p, Cursor& cur) 
   } while (cur.b < p.g.batch && cur.nc == 0);
 }
 
-// Scales of tokens t and t+1 of a record header: NB values of type SCALE per
-// token, token-major, read with one vector load.
-template <int NB, int SCALE>
-struct ScaleIO {
-  static constexpr int SB = SCALE == KVQ3_SCALE_F32 ? 4 : SCALE == KVQ3_SCALE_F16 ? 2 : 1;
-  static constexpr int BPT = NB * SB;
-
-  template <int N>
-  __device__ static __forceinline__ void raw(const uint8_t* p, uint32_t (&w)[(N + 3) / 4]) {
-    if constexpr (N == 1) w[0] = *p;
-    else if constexpr (N == 2) w[0] = *reinterpret_cast<const uint16_t*>(p);
-    else if constexpr (N == 4) w[0] = *reinterpret_cast<const uint32_t*>(p);
-    else if constexpr (N == 8) {
-      const uint2 v = *reinterpret_cast<const uint2*>(p);
-      w[0] = v.x; w[1] = v.y;
-    } else {
-#pragma unroll
-      for (int i = 0; i < N / 16; ++i) {
-        const uint4 v = reinterpret_cast<const uint4*>(p)[i];
-        w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
-      }
-    }
-  }
-
-  __device__ static __forceinline__ float value(const uint32_t* w, int i) {
-    if constexpr (SCALE == KVQ3_SCALE_F32) return __uint_as_float(w[i]);
-    else if constexpr (SCALE == KVQ3_SCALE_F16) {
-      const uint32_t h = (w[i / 2] >> (16 * (i & 1))) & 0xffffu;
-      return __half2float(__ushort_as_half((unsigned short)h));
-    } else {
-      const uint32_t b = (w[i / 4] >> (8 * (i & 3))) & 0xffu;
-      const __half_raw hr = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)b, __NV_E4M3);
-      return __half2float(__half(hr));
-    }
-  }
-
-  // one token
-  __device__ static __forceinline__ void one(const uint8_t* hdr, int t, float (&s)[NB]) {
-    uint32_t w[(BPT + 3) / 4];
-    raw<BPT>(hdr + t * BPT, w);
-#pragma unroll
-    for (int i = 0; i < NB; ++i) s[i] = value(w, i);
-  }
-
-  // tokens t, t+1 (t even, so the pair is aligned to its size)
-  __device__ static __forceinline__ void two(const uint8_t* hdr, int t, float (&s0)[NB], float (&s1)[NB]) {
-    uint32_t w[(2 * BPT + 3) / 4];
-    raw<2 * BPT>(hdr + t * BPT, w);
-    if constexpr (BPT >= 4) {
-#pragma unroll
-      for (int i = 0; i < NB; ++i) {
-        s0[i] = value(w, i);
-        s1[i] = value(w + BPT / 4, i);
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < NB; ++i) {
-        s0[i] = value(w, i);
-        s1[i] = value(w, NB + i);
-      }
-    }
-  }
-};
-
 // half2 subtraction on raw bits
 __device__ __forceinline__ uint32_t hsub2_bits(uint32_t a, uint32_t b) {
   __half2 x = *reinterpret_cast<__half2*>(&a);
@@ -286,6 +222,110 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 }
 
 // ------------------------------------------------------------------ kernel 1
+// Shared-memory loads at 32-bit addresses with immediate offsets.  volatile:
+// they must stay after the mbarrier wait that publishes the stage.
+template <int OFF>
+__device__ __forceinline__ uint32_t lds8(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u8 %0, [%1+%2];" : "=r"(v) : "r"(a), "n"(OFF));
+  return v;
+}
+template <int OFF>
+__device__ __forceinline__ uint32_t lds16(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u16 %0, [%1+%2];" : "=r"(v) : "r"(a), "n"(OFF));
+  return v;
+}
+template <int OFF>
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1+%2];" : "=r"(v) : "r"(a), "n"(OFF));
+  return v;
+}
+template <int OFF>
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0,%1}, [%2+%3];" : "=r"(v.x), "=r"(v.y) : "r"(a), "n"(OFF));
+  return v;
+}
+template <int OFF>
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4+%5];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a), "n"(OFF));
+  return v;
+}
+
+// N bytes (1..32, a power of two) at shared address a + OFF as 32-bit words.
+template <int N, int OFF>
+__device__ __forceinline__ void lds_bytes(uint32_t a, uint32_t (&w)[(N + 3) / 4]) {
+  if constexpr (N == 1) w[0] = lds8<OFF>(a);
+  else if constexpr (N == 2) w[0] = lds16<OFF>(a);
+  else if constexpr (N == 4) w[0] = lds32<OFF>(a);
+  else if constexpr (N == 8) {
+    const uint2 v = lds64<OFF>(a);
+    w[0] = v.x; w[1] = v.y;
+  } else if constexpr (N == 16) {
+    const uint4 v = lds128<OFF>(a);
+    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+  } else {
+    const uint4 v = lds128<OFF>(a), u = lds128<OFF + 16>(a);
+    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+    w[4] = u.x; w[5] = u.y; w[6] = u.z; w[7] = u.w;
+  }
+}
+
+// Decoded scales: NB values of type SCALE from raw words.
+template <int NB, int SCALE>
+struct ScaleDec {
+  static constexpr int SB = SCALE == KVQ3_SCALE_F32 ? 4 : SCALE == KVQ3_SCALE_F16 ? 2 : 1;
+  static constexpr int BPT = NB * SB;
+  __device__ static __forceinline__ float value(const uint32_t* w, int i) {
+    if constexpr (SCALE == KVQ3_SCALE_F32) return __uint_as_float(w[i]);
+    else if constexpr (SCALE == KVQ3_SCALE_F16) {
+      return __half2float(__ushort_as_half((unsigned short)((w[i / 2] >> (16 * (i & 1))) & 0xffffu)));
+    } else {
+      const __half_raw hr =
+          __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)((w[i / 4] >> (8 * (i & 3))) & 0xffu), __NV_E4M3);
+      return __half2float(__half(hr));
+    }
+  }
+  template <int OFF>
+  __device__ static __forceinline__ void one(uint32_t a, float (&s)[NB]) {
+    uint32_t w[(BPT + 3) / 4];
+    lds_bytes<BPT, OFF>(a, w);
+#pragma unroll
+    for (int i = 0; i < NB; ++i) s[i] = value(w, i);
+  }
+  // tokens at a and a + BPT (the pair is aligned to its size)
+  template <int OFF>
+  __device__ static __forceinline__ void two(uint32_t a, float (&s0)[NB], float (&s1)[NB]) {
+    uint32_t w[(2 * BPT + 3) / 4];
+    lds_bytes<2 * BPT, OFF>(a, w);
+    if constexpr (BPT >= 4) {
+#pragma unroll
+      for (int i = 0; i < NB; ++i) {
+        s0[i] = value(w, i);
+        s1[i] = value(w + BPT / 4, i);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < NB; ++i) {
+        s0[i] = value(w, i);
+        s1[i] = value(w, NB + i);
+      }
+    }
+  }
+};
+
+// What the producer thread publishes with each chunk (at the end of its stage).
+struct ChunkDesc {
+  int32_t unit, b, kvh, n_tok;
+  uint32_t page_ok;  // bit i: page i of the chunk has a valid id (else masked)
+  int32_t pad[3];
+};
+
 template <int D, int GPAD>
 struct DecodeSmem {
   static constexpr int kFullOff = 0;                              // kMaxStages mbarriers
@@ -308,8 +348,8 @@ __host__ __device__ constexpr int decode_min_blocks(int D, int GPAD) {
 // scales are fp32, since p = 1 times an fp32 scale is not an fp16 value;
 // otherwise one fp16 value per head (PV n-tile = 8 heads).
 template <int D, int BLOCK, int GPAD, int SCALE, bool PSPLIT>
-__global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD)) decode_split_kernel(const __grid_constant__ DecodeParams p,
-                                                              const __grid_constant__ RotParams rp) {
+__global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
+    decode_split_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ RotParams rp) {
   constexpr int NB = D / BLOCK;
   constexpr int KS = D / 16;          // k-steps of QK^T == M-tiles of PV
   constexpr int KSB = BLOCK / 16;     // per block
@@ -322,7 +362,8 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD)) decode_split_
   constexpr int LQ = D / EQ;
   constexpr int GPWQ = 32 / LQ;
   using SM = DecodeSmem<D, GPAD>;
-  using SIO = ScaleIO<NB, SCALE>;
+  using SDec = ScaleDec<NB, SCALE>;
+  constexpr int BPT = SDec::BPT;
 
   extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x & 31;
@@ -334,8 +375,11 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD)) decode_split_
   float* qs = reinterpret_cast<float*>(smem + SM::kQOff);
   float* qinv_s = reinterpret_cast<float*>(smem + SM::kQInvOff);
   uint8_t* stg = smem + SM::kStageOff;
+  const uint32_t stg_u32 = smem_u32(stg);
   const int S = p.stages;
   const CacheGeom& g = p.g;
+  const uint32_t REC = (uint32_t)g.record_bytes, HDR = (uint32_t)g.scale_hdr_bytes;
+  const uint32_t desc_off = p.stage_bytes - (uint32_t)sizeof(ChunkDesc);
 
   const int64_t cta = blockIdx.x;
   const int64_t T = total_chunks(p, cta == 0 && wid == 0);
@@ -352,40 +396,51 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD)) decode_split_
     fence_mbar_init();
   }
   __syncthreads();
-  const uint64_t pol = policy_evict_first();
-  Cursor cp = cursor_at(p, c0);   // producer (thread 0)
-  Cursor cc = cp;                 // consumers
 
-  // bulk copies of the chunk's pages (each page: K record then V record)
+  // ---- producer (thread 0): chunk descriptor + bulk copies of its pages
+  Cursor cp{};
+  uint64_t pol = 0;
   auto issue = [&](const Cursor& c, int stage) {
     uint8_t* dst = stg + (size_t)stage * p.stage_bytes;
     const int64_t len = p.seq_lens[c.b];
     const int64_t tok0 = c.c * p.chunk_tokens;
-    const int npg = (int)min((int64_t)p.pages_per_chunk, (len - tok0 + g.page_size - 1) / g.page_size);
+    const int n_tok = (int)min((int64_t)p.chunk_tokens, len - tok0);
+    const int npg = (n_tok + g.page_size - 1) / g.page_size;
     const int64_t lp0 = tok0 / g.page_size;
-    uint32_t bytes = 0;
-    int64_t pages[kChunk / 16];
-    int bad = 0;
+    uint32_t ok = 0, bytes = 0;
     for (int i = 0; i < npg; ++i) {
-      pages[i] = page_of(g, p.page_table, c.b, lp0 + i);
-      if (pages[i] >= 0) bytes += (uint32_t)(2 * g.record_bytes);
-      else bad = 1;
+      if (page_of(g, p.page_table, c.b, lp0 + i) >= 0) {
+        ok |= 1u << i;
+        bytes += 2 * REC;
+      }
     }
-    if (bad) set_status(p.status, KVQ3_DEV_BAD_PAGE);
+    if (ok != (1u << npg) - 1u) set_status(p.status, KVQ3_DEV_BAD_PAGE);
+    ChunkDesc* dsc = reinterpret_cast<ChunkDesc*>(dst + desc_off);
+    dsc->unit = c.b * g.hkv + c.kvh;
+    dsc->b = c.b;
+    dsc->kvh = c.kvh;
+    dsc->n_tok = n_tok;
+    dsc->page_ok = ok;
     if (bytes) {
       mbar_expect_tx(&full[stage], bytes);
       for (int i = 0; i < npg; ++i)
-        if (pages[i] >= 0)
-          bulk_g2s(dst + (size_t)i * 2 * g.record_bytes, p.pool + record_offset(g, pages[i], c.kvh, 0),
-                   (uint32_t)(2 * g.record_bytes), &full[stage], pol);
+        if ((ok >> i) & 1u)
+          bulk_g2s(dst + (size_t)i * 2 * REC,
+                   p.pool + record_offset(g, page_of(g, p.page_table, c.b, lp0 + i), c.kvh, 0), 2 * REC,
+                   &full[stage], pol);
     } else {
       mbar_arrive(&full[stage]);
     }
   };
-  if (threadIdx.x == 0) {
-    for (int64_t i = 0; i < nch && i < S; ++i) {
-      issue(cp, (int)i);
-      cursor_next(p, cp);
+  {
+    const Cursor c = cursor_at(p, c0);  // warp-collective
+    if (threadIdx.x == 0) {
+      pol = policy_evict_first();
+      cp = c;
+      for (int64_t i = 0; i < nch && i < S; ++i) {
+        issue(cp, (int)i);
+        cursor_next(p, cp);
+      }
     }
   }
 
@@ -395,6 +450,19 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD)) decode_split_
   float4 quat_q[EQ / 4];
   lane_quats<EQ>(rp, rq, quat_q);
   const bool so4 = (rp.flags & KVQ3_ROT_SO4) != 0;
+
+  // lane-constant code-string offsets: word byte offset and bit shift of this
+  // lane's key chunk (fields j*FQ.. of each block) and value chunk (fields
+  // r*FV.. of each block)
+  uint32_t kwo[NB], kshf[NB], vwo[NB], vshf[NB];
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    const int kb = 3 * (b * BLOCK + j * FQ), vb = 3 * (b * BLOCK + r * FV);
+    kwo[b] = (kb >> 5) * 4;
+    kshf[b] = kb & 31;
+    vwo[b] = (vb >> 5) * 4;
+    vshf[b] = vb & 31;
+  }
 
   uint32_t qf[NTQ][KS][2];
   float qinv[NTQ];
@@ -563,12 +631,9 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD)) decode_split_
     named_barrier(1, 128);  // qs is rewritten at the next unit
   };
 
-  // one 16-token step at token offset t0 of a page whose records start at pg
-  auto step = [&](const uint8_t* pg, int t0, int n_valid) {
-    const uint8_t* kS = pg;
-    const uint8_t* kC = pg + g.scale_hdr_bytes;
-    const uint8_t* vS = pg + g.record_bytes;
-    const uint8_t* vC = vS + g.scale_hdr_bytes;
+  // one 16-token step at token offset t0 of a page whose K record starts at
+  // shared address pg (V record at pg + REC); n_valid tokens of the page
+  auto step = [&](uint32_t pg, int t0, int n_valid) {
     // ------------------------------------------------ S = K q1 (per block)
     float accq[NB][NTQ][4];
 #pragma unroll
@@ -577,28 +642,33 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD)) decode_split_
       for (int tq = 0; tq < NTQ; ++tq)
 #pragma unroll
         for (int c = 0; c < 4; ++c) accq[b][tq][c] = 0.0f;
-    const uint8_t* k0 = kC + (t0 + r) * CB;
-    const uint8_t* k8 = k0 + 8 * CB;
+    const uint32_t kt = pg + HDR + (uint32_t)((t0 + r) * CB);   // token t0 + r
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
+      const uint32_t a = kt + kwo[b];
       uint32_t h0[FQ / 2], h1[FQ / 2];
-      uint32_t lo, hi;
-      const int boff = 3 * (b * BLOCK + j * FQ);
-      load_bits(k0, boff, lo, hi);
-      k_codes_to_half2<FQ>(lo, hi, h0);
-      load_bits(k8, boff, lo, hi);
-      k_codes_to_half2<FQ>(lo, hi, h1);
+      {
+        const uint32_t w0 = lds32<0>(a), w1 = lds32<4>(a);
+        k_codes_to_half2<FQ>(__funnelshift_r(w0, w1, kshf[b]), w1 >> kshf[b], h0);
+      }
+      {
+        const uint32_t w0 = lds32<8 * CB>(a), w1 = lds32<8 * CB + 4>(a);
+        k_codes_to_half2<FQ>(__funnelshift_r(w0, w1, kshf[b]), w1 >> kshf[b], h1);
+      }
 #pragma unroll
       for (int sp = 0; sp < KSB; ++sp) {
-        const uint32_t a[4] = {h0[2 * sp], h1[2 * sp], h0[2 * sp + 1], h1[2 * sp + 1]};
+        const uint32_t af[4] = {h0[2 * sp], h1[2 * sp], h0[2 * sp + 1], h1[2 * sp + 1]};
 #pragma unroll
         for (int tq = 0; tq < NTQ; ++tq)
-          mma_16816(accq[b][tq], a, qf[tq][b * KSB + sp][0], qf[tq][b * KSB + sp][1]);
+          mma_16816(accq[b][tq], af, qf[tq][b * KSB + sp][0], qf[tq][b * KSB + sp][1]);
       }
     }
     float skr[NB], skr8[NB];
-    SIO::one(kS, t0 + r, skr);
-    SIO::one(kS, t0 + r + 8, skr8);
+    {
+      const uint32_t a = pg + (uint32_t)((t0 + r) * BPT);
+      SDec::template one<0>(a, skr);
+      SDec::template one<8 * BPT>(a, skr8);
+    }
     const bool vr = t0 + r < n_valid, vr8 = t0 + r + 8 < n_valid;
     // ------------------------------------------------ online softmax
     float pr[NTQ], pr8[NTQ], alpha[NTQ];
@@ -671,16 +741,19 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD)) decode_split_
       }
     }
     float sv0[NB], sv1[NB], sv2[NB], sv3[NB];
-    SIO::two(vS, T0, sv0, sv1);
-    SIO::two(vS, T0 + 8, sv2, sv3);
+    {
+      const uint32_t a = pg + REC + (uint32_t)(T0 * BPT);
+      SDec::template two<0>(a, sv0, sv1);
+      SDec::template two<8 * BPT>(a, sv2, sv3);
+    }
     const bool v0 = T0 < n_valid, v1 = T0 + 1 < n_valid, v2 = T0 + 8 < n_valid,
                v3 = T0 + 9 < n_valid;
     uint32_t pb[NB][NTP][2];
     if constexpr (PSPLIT) {
+      const bool lo_part = (r & 1) != 0;
 #pragma unroll
       for (int tp = 0; tp < NTP; ++tp) {
         const bool hv = 4 * tp + (r >> 1) < p.G;
-        const bool lo_part = (r & 1) != 0;
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
           const float y0 = hv && v0 ? x0[tp] * sv0[b] : 0.0f;
@@ -688,14 +761,11 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD)) decode_split_
           const float y2 = hv && v2 ? x2[tp] * sv2[b] : 0.0f;
           const float y3 = hv && v3 ? x3[tp] * sv3[b] : 0.0f;
           const __half2 h01 = __floats2half2_rn(y0, y1), h23 = __floats2half2_rn(y2, y3);
-          if (lo_part) {
-            const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-            pb[b][tp][0] = pack_half2(y0 - f01.x, y1 - f01.y);
-            pb[b][tp][1] = pack_half2(y2 - f23.x, y3 - f23.y);
-          } else {
-            pb[b][tp][0] = *reinterpret_cast<const uint32_t*>(&h01);
-            pb[b][tp][1] = *reinterpret_cast<const uint32_t*>(&h23);
-          }
+          const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+          const uint32_t lo01 = pack_half2(y0 - f01.x, y1 - f01.y);
+          const uint32_t lo23 = pack_half2(y2 - f23.x, y3 - f23.y);
+          pb[b][tp][0] = lo_part ? lo01 : *reinterpret_cast<const uint32_t*>(&h01);
+          pb[b][tp][1] = lo_part ? lo23 : *reinterpret_cast<const uint32_t*>(&h23);
         }
       }
     } else {
@@ -705,13 +775,13 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD)) decode_split_
         const int tsel = hp >> 2;
         float y0 = 0.0f, y1 = 0.0f, y2 = 0.0f, y3 = 0.0f;
 #pragma unroll
-        for (int tq = 0; tq < NTQ; ++tq)
-          if (tq == tsel) {
-            y0 = x0[tq];
-            y1 = x1[tq];
-            y2 = x2[tq];
-            y3 = x3[tq];
-          }
+        for (int tq = 0; tq < NTQ; ++tq) {
+          const bool sel = tq == tsel;
+          y0 = sel ? x0[tq] : y0;
+          y1 = sel ? x1[tq] : y1;
+          y2 = sel ? x2[tq] : y2;
+          y3 = sel ? x3[tq] : y3;
+        }
         const bool hv = hp < p.G;
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
@@ -721,23 +791,23 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD)) decode_split_
       }
     }
     // ------------------------------------------------ o1^T += V^T P'^T
-    const uint8_t* vt = vC + T0 * CB;
+    const uint32_t vt = pg + REC + HDR + (uint32_t)(T0 * CB);
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
-      const int boff = 3 * (b * BLOCK + r * FV);
-      uint32_t c0v, c1v, c2v, c3v, dummy;
-      load_bits(vt, boff, c0v, dummy);
-      load_bits(vt + CB, boff, c1v, dummy);
-      load_bits(vt + 8 * CB, boff, c2v, dummy);
-      load_bits(vt + 9 * CB, boff, c3v, dummy);
+      const uint32_t a = vt + vwo[b];
+      const uint32_t sh = vshf[b];
+      const uint32_t c0v = __funnelshift_r(lds32<0>(a), lds32<4>(a), sh);
+      const uint32_t c1v = __funnelshift_r(lds32<CB>(a), lds32<CB + 4>(a), sh);
+      const uint32_t c2v = __funnelshift_r(lds32<8 * CB>(a), lds32<8 * CB + 4>(a), sh);
+      const uint32_t c3v = __funnelshift_r(lds32<9 * CB>(a), lds32<9 * CB + 4>(a), sh);
       uint32_t hv01[FV], hv89[FV];
       v_codes_to_half2<FV>(c0v, c1v, hv01);
       v_codes_to_half2<FV>(c2v, c3v, hv89);
 #pragma unroll
       for (int mp = 0; mp < KSB; ++mp) {
-        const uint32_t a[4] = {hv01[2 * mp], hv01[2 * mp + 1], hv89[2 * mp], hv89[2 * mp + 1]};
+        const uint32_t af[4] = {hv01[2 * mp], hv01[2 * mp + 1], hv89[2 * mp], hv89[2 * mp + 1]};
 #pragma unroll
-        for (int tp = 0; tp < NTP; ++tp) mma_16816(acc[b * KSB + mp][tp], a, pb[b][tp][0], pb[b][tp][1]);
+        for (int tp = 0; tp < NTP; ++tp) mma_16816(acc[b * KSB + mp][tp], af, pb[b][tp][0], pb[b][tp][1]);
       }
     }
   };
@@ -746,12 +816,6 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD)) decode_split_
   for (int64_t i = 0; i < nch; ++i) {
     const int stage = (int)(i % S);
     const uint32_t parity = (uint32_t)((i / S) & 1);
-    const int unit = cc.b * g.hkv + cc.kvh;
-    if (unit != cur_unit) {
-      if (cur_unit >= 0) flush(cur_unit);
-      setup_unit(cc.b, cc.kvh);
-      cur_unit = unit;
-    }
     if (!mbar_wait(&full[stage], parity, p.wait_limit)) {
       // a copy never arrived: flag it, wait (bounded) for the copies still in
       // flight so no asynchronous write outlives this CTA, and stop
@@ -760,15 +824,22 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD)) decode_split_
         mbar_wait(&full[k % S], (uint32_t)((k / S) & 1), p.wait_limit);
       return;
     }
-    const int64_t len = p.seq_lens[cc.b];
-    const int64_t tok0 = cc.c * p.chunk_tokens;
-    const int n_chunk = (int)min((int64_t)p.chunk_tokens, len - tok0);
-    const uint8_t* st = stg + (size_t)stage * p.stage_bytes;
-    for (int s16 = wid; s16 * 16 < n_chunk; s16 += kWarps) {
-      const int t = s16 * 16;                       // token offset in the chunk
-      const int pi = t / P;                         // page within the chunk
-      if (page_of(g, p.page_table, cc.b, tok0 / P + pi) < 0) continue;  // masked page
-      step(st + (size_t)pi * 2 * g.record_bytes, t - pi * P, min(P, n_chunk - pi * P));
+    const uint32_t st = stg_u32 + (uint32_t)stage * p.stage_bytes;
+    const uint4 dv = lds128<0>(st + desc_off);            // unit, b, kvh, n_tok
+    const uint32_t page_ok = lds32<16>(st + desc_off);
+    const int unit = (int)dv.x, n_tok = (int)dv.w;
+    if (unit != cur_unit) {
+      if (cur_unit >= 0) flush(cur_unit);
+      setup_unit((int)dv.y, (int)dv.z);
+      cur_unit = unit;
+    }
+    for (int t = wid * 16; t < n_tok; t += kWarps * 16) {
+      int pi = 0, tin = t;                              // page of the chunk, offset in it
+      while (tin >= P) {
+        tin -= P;
+        ++pi;
+      }
+      if ((page_ok >> pi) & 1u) step(st + (uint32_t)pi * 2 * REC, tin, min(P, n_tok - pi * P));
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
@@ -783,7 +854,6 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD)) decode_split_
       }
       cursor_next(p, cp);
     }
-    cursor_next(p, cc);
   }
   if (cur_unit >= 0) flush(cur_unit);
 }
@@ -865,10 +935,11 @@ kvq3_status decode_plan_t(const CacheGeom& g, int G, DecodePlan* plan) {
   using SM = DecodeSmem<D, GPAD>;
   const void* k = reinterpret_cast<const void*>(&decode_split_kernel<D, BLOCK, GPAD, SCALE, PSPLIT>);
   plan->gpad = GPAD;
-  plan->chunk_tokens = g.page_size >= kChunk ? g.page_size : kChunk;
-  plan->pages_per_chunk = plan->chunk_tokens / g.page_size;
+  plan->pages_per_chunk = (kChunk + g.page_size - 1) / g.page_size;
+  plan->chunk_tokens = plan->pages_per_chunk * g.page_size;
   const size_t chunk_bytes = (size_t)plan->pages_per_chunk * 2 * g.record_bytes;
-  plan->stage_bytes = (uint32_t)((chunk_bytes + 16 + 127) / 128 * 128);  // +16: tail word reads
+  // + 16: word reads past the last code string; + descriptor at the end
+  plan->stage_bytes = (uint32_t)((chunk_bytes + 16 + sizeof(ChunkDesc) + 127) / 128 * 128);
   // aim for ~24 KB of stages per CTA (4 CTAs per SM), at least 2 stages
   int stages = (int)(24576 / plan->stage_bytes);
   stages = stages < 2 ? 2 : (stages > 6 ? 6 : stages);
