@@ -36,11 +36,13 @@
 
 #include <float.h>
 
+#include <type_traits>
+
 #include "kvq3_internal.h"
 
 namespace kvq3 {
 
-constexpr int kChunk = 64;       // minimum tokens per chunk (smaller pages are grouped)
+constexpr int kChunk = 128;      // minimum tokens per chunk (smaller pages are grouped)
 constexpr int kWarps = 4;        // consumer warps per CTA
 constexpr int kMaxStages = 8;
 
@@ -156,6 +158,19 @@ __device__ __forceinline__ void cursor_next(const DecodeParams& p, Cursor& cur) 
   } while (cur.b < p.g.batch && cur.nc == 0);
 }
 
+// Compile-time loop: f(integral_constant<int, 0>) ... f(integral_constant<int, N-1>).
+template <int I, int N, typename F>
+__device__ __forceinline__ void static_for_impl(F&& f) {
+  if constexpr (I < N) {
+    f(std::integral_constant<int, I>{});
+    static_for_impl<I + 1, N>(f);
+  }
+}
+template <int N, typename F>
+__device__ __forceinline__ void static_for(F&& f) {
+  static_for_impl<0, N>(f);
+}
+
 // half2 subtraction on raw bits
 __device__ __forceinline__ uint32_t hsub2_bits(uint32_t a, uint32_t b) {
   __half2 x = *reinterpret_cast<__half2*>(&a);
@@ -172,16 +187,14 @@ __host__ __device__ constexpr int kq_lo_field(int k) { return 8 * (k / 4) + (k %
 __host__ __device__ constexpr int kq_lo_off(int k) { return (k & 1) ? 7 : 4; }
 __host__ __device__ constexpr int kq_hi_off(int k) { return (k & 1) ? 3 : 0; }
 
-template <int F>
-__device__ __forceinline__ void k_codes_to_half2(uint32_t lo, uint32_t hi, uint32_t (&h)[F / 2]) {
-#pragma unroll
-  for (int k = 0; k < F / 2; ++k) {
-    const int i = 8 * (k / 4) + (k & 2);  // first field of the window
-    const int o = 3 * i - 4;              // window start bit: field i lands at bit 4
-    const uint32_t w = o < 0 ? (lo << (-o)) : __funnelshift_r(lo, hi, o);
-    if (k & 1) h[k] = hsub2_bits((w & 0x00380380u) ^ 0x64206600u, 0x64206600u);
-    else h[k] = hsub2_bits((w & 0x00070070u) ^ 0x64046440u, 0x64046440u);
-  }
+// Pair k of a key chunk (lo, hi) as half2 (see above).
+template <int K>
+__device__ __forceinline__ uint32_t k_pair(uint32_t lo, uint32_t hi) {
+  constexpr int i = 8 * (K / 4) + (K & 2);  // first field of the window
+  constexpr int o = 3 * i - 4;              // window start bit: field i lands at bit 4
+  const uint32_t w = o < 0 ? (lo << (o < 0 ? -o : 0)) : __funnelshift_r(lo, hi, o < 0 ? 0 : o);
+  if constexpr (K & 1) return hsub2_bits((w & 0x00380380u) ^ 0x64206600u, 0x64206600u);
+  else return hsub2_bits((w & 0x00070070u) ^ 0x64046440u, 0x64046440u);
 }
 
 // Value codes: fields f = 0..F-1 (F = 8 or 4) of two tokens' 3F-bit chunks
@@ -190,18 +203,15 @@ __host__ __device__ constexpr int v_off(int f) {
   return f == 0 ? 0 : f == 1 ? 3 : f == 2 ? 6 : f == 3 ? 1 : f == 4 ? 4 : f == 5 ? 7 : f == 6 ? 2 : 5;
 }
 
+// Field f of two tokens' value chunks c0, c1 as half2 (token0, token1),
+// scaled by 2^voff(f).
 template <int F>
-__device__ __forceinline__ void v_codes_to_half2(uint32_t c0, uint32_t c1, uint32_t (&h)[F]) {
-  const uint32_t wa = __byte_perm(c0, c1, 0x5410);
-  const uint32_t wb = __byte_perm(c0, c1, 0x6521);
-  const uint32_t wc = __byte_perm(c0, c1, 0x7632);
-#pragma unroll
-  for (int f = 0; f < F; ++f) {
-    const uint32_t w = f < 3 ? wa : (f < 6 ? wb : wc);
-    const int o = v_off(f);
-    const uint32_t x = 0x64006400u | (0x00040004u << o);
-    h[f] = hsub2_bits((w & (0x00070007u << o)) ^ x, x);
-  }
+__device__ __forceinline__ uint32_t v_field(uint32_t c0, uint32_t c1) {
+  constexpr uint32_t sel = F < 3 ? 0x5410u : (F < 6 ? 0x6521u : 0x7632u);
+  constexpr int o = v_off(F);
+  constexpr uint32_t x = 0x64006400u | (0x00040004u << o);
+  const uint32_t w = __byte_perm(c0, c1, sel);
+  return hsub2_bits((w & (0x00070007u << o)) ^ x, x);
 }
 
 // Bits [boff, boff + 64) of a code string (two aligned words, funnel shift).
@@ -646,22 +656,21 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
       const uint32_t a = kt + kwo[b];
-      uint32_t h0[FQ / 2], h1[FQ / 2];
-      {
-        const uint32_t w0 = lds32<0>(a), w1 = lds32<4>(a);
-        k_codes_to_half2<FQ>(__funnelshift_r(w0, w1, kshf[b]), w1 >> kshf[b], h0);
-      }
-      {
-        const uint32_t w0 = lds32<8 * CB>(a), w1 = lds32<8 * CB + 4>(a);
-        k_codes_to_half2<FQ>(__funnelshift_r(w0, w1, kshf[b]), w1 >> kshf[b], h1);
-      }
-#pragma unroll
-      for (int sp = 0; sp < KSB; ++sp) {
-        const uint32_t af[4] = {h0[2 * sp], h1[2 * sp], h0[2 * sp + 1], h1[2 * sp + 1]};
+      const uint32_t x0 = lds32<0>(a), x1 = lds32<4>(a);
+      const uint32_t y0 = lds32<8 * CB>(a), y1 = lds32<8 * CB + 4>(a);
+      const uint32_t lo0 = __funnelshift_r(x0, x1, kshf[b]), hi0 = x1 >> kshf[b];   // token r
+      const uint32_t lo8 = __funnelshift_r(y0, y1, kshf[b]), hi8 = y1 >> kshf[b];   // token r + 8
+      static_for<KSB>([&](auto spc) {
+        constexpr int sp = decltype(spc)::value;
+        uint32_t af[4];
+        af[0] = k_pair<2 * sp>(lo0, hi0);
+        af[1] = k_pair<2 * sp>(lo8, hi8);
+        af[2] = k_pair<2 * sp + 1>(lo0, hi0);
+        af[3] = k_pair<2 * sp + 1>(lo8, hi8);
 #pragma unroll
         for (int tq = 0; tq < NTQ; ++tq)
           mma_16816(accq[b][tq], af, qf[tq][b * KSB + sp][0], qf[tq][b * KSB + sp][1]);
-      }
+      });
     }
     float skr[NB], skr8[NB];
     {
@@ -800,15 +809,16 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
       const uint32_t c1v = __funnelshift_r(lds32<CB>(a), lds32<CB + 4>(a), sh);
       const uint32_t c2v = __funnelshift_r(lds32<8 * CB>(a), lds32<8 * CB + 4>(a), sh);
       const uint32_t c3v = __funnelshift_r(lds32<9 * CB>(a), lds32<9 * CB + 4>(a), sh);
-      uint32_t hv01[FV], hv89[FV];
-      v_codes_to_half2<FV>(c0v, c1v, hv01);
-      v_codes_to_half2<FV>(c2v, c3v, hv89);
-#pragma unroll
-      for (int mp = 0; mp < KSB; ++mp) {
-        const uint32_t af[4] = {hv01[2 * mp], hv01[2 * mp + 1], hv89[2 * mp], hv89[2 * mp + 1]};
+      static_for<KSB>([&](auto mpc) {
+        constexpr int mp = decltype(mpc)::value;
+        uint32_t af[4];
+        af[0] = v_field<2 * mp>(c0v, c1v);
+        af[1] = v_field<2 * mp + 1>(c0v, c1v);
+        af[2] = v_field<2 * mp>(c2v, c3v);
+        af[3] = v_field<2 * mp + 1>(c2v, c3v);
 #pragma unroll
         for (int tp = 0; tp < NTP; ++tp) mma_16816(acc[b * KSB + mp][tp], af, pb[b][tp][0], pb[b][tp][1]);
-      }
+      });
     }
   };
 
