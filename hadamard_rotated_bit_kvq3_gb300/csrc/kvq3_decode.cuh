@@ -286,46 +286,54 @@ __device__ __forceinline__ void lds_bytes(uint32_t a, uint32_t (&w)[(N + 3) / 4]
   }
 }
 
-// Decoded scales: NB values of type SCALE from raw words.
+// Decoded scales: NB values of type SCALE from raw words (pairs converted
+// together: one half2 -> float2 for fp16, one fp8x2 -> half2 -> float2 for E4M3).
 template <int NB, int SCALE>
 struct ScaleDec {
   static constexpr int SB = SCALE == KVQ3_SCALE_F32 ? 4 : SCALE == KVQ3_SCALE_F16 ? 2 : 1;
   static constexpr int BPT = NB * SB;
-  __device__ static __forceinline__ float value(const uint32_t* w, int i) {
-    if constexpr (SCALE == KVQ3_SCALE_F32) return __uint_as_float(w[i]);
-    else if constexpr (SCALE == KVQ3_SCALE_F16) {
-      return __half2float(__ushort_as_half((unsigned short)((w[i / 2] >> (16 * (i & 1))) & 0xffffu)));
+  // values i = 0..n-1 starting at value index i0 of w
+  template <int N, int I0>
+  __device__ static __forceinline__ void decode(const uint32_t* w, float* s) {
+    if constexpr (SCALE == KVQ3_SCALE_F32) {
+#pragma unroll
+      for (int i = 0; i < N; ++i) s[i] = __uint_as_float(w[I0 + i]);
+    } else if constexpr (SCALE == KVQ3_SCALE_F16) {
+      if constexpr (N == 1) {
+        s[0] = __half2float(__ushort_as_half((unsigned short)(w[I0 / 2] >> (16 * (I0 & 1)))));
+      } else {
+#pragma unroll
+        for (int i = 0; i < N; i += 2) {
+          const uint32_t v = w[(I0 + i) / 2];
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&v));
+          s[i] = f.x;
+          s[i + 1] = f.y;
+        }
+      }
     } else {
-      const __half_raw hr =
-          __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)((w[i / 4] >> (8 * (i & 3))) & 0xffu), __NV_E4M3);
-      return __half2float(__half(hr));
+#pragma unroll
+      for (int i = 0; i < N; i += 2) {
+        const uint32_t v = w[(I0 + i) / 4] >> (8 * ((I0 + i) & 3));
+        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(v & 0xffffu), __NV_E4M3);
+        const float2 f = __half22float2(__half2(hr));
+        s[i] = f.x;
+        if (i + 1 < N) s[i + 1] = f.y;
+      }
     }
   }
   template <int OFF>
   __device__ static __forceinline__ void one(uint32_t a, float (&s)[NB]) {
     uint32_t w[(BPT + 3) / 4];
     lds_bytes<BPT, OFF>(a, w);
-#pragma unroll
-    for (int i = 0; i < NB; ++i) s[i] = value(w, i);
+    decode<NB, 0>(w, s);
   }
   // tokens at a and a + BPT (the pair is aligned to its size)
   template <int OFF>
   __device__ static __forceinline__ void two(uint32_t a, float (&s0)[NB], float (&s1)[NB]) {
     uint32_t w[(2 * BPT + 3) / 4];
     lds_bytes<2 * BPT, OFF>(a, w);
-    if constexpr (BPT >= 4) {
-#pragma unroll
-      for (int i = 0; i < NB; ++i) {
-        s0[i] = value(w, i);
-        s1[i] = value(w + BPT / 4, i);
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < NB; ++i) {
-        s0[i] = value(w, i);
-        s1[i] = value(w, NB + i);
-      }
-    }
+    decode<NB, 0>(w, s0);
+    decode<NB, NB>(w, s1);
   }
 };
 
@@ -333,13 +341,14 @@ struct ScaleDec {
 struct ChunkDesc {
   int32_t unit, b, kvh, n_tok;
   uint32_t page_ok;  // bit i: page i of the chunk has a valid id (else masked)
-  int32_t pad[3];
+  int32_t c;         // chunk index within its unit
+  int32_t pad[2];
 };
 
 template <int D, int GPAD>
 struct DecodeSmem {
   static constexpr int kFullOff = 0;                              // kMaxStages mbarriers
-  static constexpr int kEmptyOff = kFullOff + 8 * kMaxStages;     // kMaxStages mbarriers
+  static constexpr int kEmptyOff = kFullOff + 8 * kMaxStages;     // kMaxStages release counters
   static constexpr int kMLOff = kEmptyOff + 8 * kMaxStages;       // [kWarps][2][GPAD] floats
   static constexpr int kQOff = (kMLOff + kWarps * 2 * GPAD * 4 + 15) / 16 * 16;  // [GPAD][D]
   static constexpr int kQInvOff = kQOff + GPAD * D * 4;           // [GPAD]
@@ -380,7 +389,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
   const int wid = threadIdx.x >> 5;
   const int j = lane & 3, r = lane >> 2;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::kFullOff);
-  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + SM::kEmptyOff);
+  uint32_t* released = reinterpret_cast<uint32_t*>(smem + SM::kEmptyOff);
   float* ml_s = reinterpret_cast<float*>(smem + SM::kMLOff);
   float* qs = reinterpret_cast<float*>(smem + SM::kQOff);
   float* qinv_s = reinterpret_cast<float*>(smem + SM::kQInvOff);
@@ -401,15 +410,15 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kWarps);
+      released[s] = 0;
     }
     fence_mbar_init();
   }
   __syncthreads();
 
-  // ---- producer (thread 0): chunk descriptor + bulk copies of its pages
-  Cursor cp{};
-  uint64_t pol = 0;
+  // ---- producer: chunk descriptor + bulk copies of its pages (thread 0 fills
+  // the first stages; afterwards the last warp to release a stage refills it)
+  const uint64_t pol = policy_evict_first();
   auto issue = [&](const Cursor& c, int stage) {
     uint8_t* dst = stg + (size_t)stage * p.stage_bytes;
     const int64_t len = p.seq_lens[c.b];
@@ -431,6 +440,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
     dsc->kvh = c.kvh;
     dsc->n_tok = n_tok;
     dsc->page_ok = ok;
+    dsc->c = (int32_t)c.c;
     if (bytes) {
       mbar_expect_tx(&full[stage], bytes);
       for (int i = 0; i < npg; ++i)
@@ -443,10 +453,8 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
     }
   };
   {
-    const Cursor c = cursor_at(p, c0);  // warp-collective
+    Cursor cp = cursor_at(p, c0);  // warp-collective
     if (threadIdx.x == 0) {
-      pol = policy_evict_first();
-      cp = c;
       for (int64_t i = 0; i < nch && i < S; ++i) {
         issue(cp, (int)i);
         cursor_next(p, cp);
@@ -643,7 +651,8 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
 
   // one 16-token step at token offset t0 of a page whose K record starts at
   // shared address pg (V record at pg + REC); n_valid tokens of the page
-  auto step = [&](uint32_t pg, int t0, int n_valid) {
+  auto step = [&](uint32_t pg, int t0, auto full_c, int n_valid) {
+    constexpr bool FULL = decltype(full_c)::value;   // all 16 tokens valid
     // ------------------------------------------------ S = K q1 (per block)
     float accq[NB][NTQ][4];
 #pragma unroll
@@ -678,7 +687,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
       SDec::template one<0>(a, skr);
       SDec::template one<8 * BPT>(a, skr8);
     }
-    const bool vr = t0 + r < n_valid, vr8 = t0 + r + 8 < n_valid;
+    const bool vr = FULL || t0 + r < n_valid, vr8 = FULL || t0 + r + 8 < n_valid;
     // ------------------------------------------------ online softmax
     float pr[NTQ], pr8[NTQ], alpha[NTQ];
     bool changed = false;
@@ -755,8 +764,8 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
       SDec::template two<0>(a, sv0, sv1);
       SDec::template two<8 * BPT>(a, sv2, sv3);
     }
-    const bool v0 = T0 < n_valid, v1 = T0 + 1 < n_valid, v2 = T0 + 8 < n_valid,
-               v3 = T0 + 9 < n_valid;
+    const bool v0 = FULL || T0 < n_valid, v1 = FULL || T0 + 1 < n_valid,
+               v2 = FULL || T0 + 8 < n_valid, v3 = FULL || T0 + 9 < n_valid;
     uint32_t pb[NB][NTP][2];
     if constexpr (PSPLIT) {
       const bool lo_part = (r & 1) != 0;
@@ -836,8 +845,9 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
     }
     const uint32_t st = stg_u32 + (uint32_t)stage * p.stage_bytes;
     const uint4 dv = lds128<0>(st + desc_off);            // unit, b, kvh, n_tok
-    const uint32_t page_ok = lds32<16>(st + desc_off);
+    const uint2 dw = lds64<16>(st + desc_off);            // page_ok, c
     const int unit = (int)dv.x, n_tok = (int)dv.w;
+    const uint32_t page_ok = dw.x;
     if (unit != cur_unit) {
       if (cur_unit >= 0) flush(cur_unit);
       setup_unit((int)dv.y, (int)dv.z);
@@ -849,20 +859,30 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
         tin -= P;
         ++pi;
       }
-      if ((page_ok >> pi) & 1u) step(st + (uint32_t)pi * 2 * REC, tin, min(P, n_tok - pi * P));
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[stage]);
-    if (threadIdx.x == 0 && i + S < nch) {
-      // refill this stage once every warp has released it
-      if (mbar_wait(&empty[stage], parity, p.wait_limit)) {
-        fence_proxy_async();
-        issue(cp, stage);
-      } else {
-        set_status(p.status, KVQ3_DEV_TIMEOUT);
-        mbar_arrive(&full[stage]);  // keep the consumers' phases moving
+      if ((page_ok >> pi) & 1u) {
+        const uint32_t pg = st + (uint32_t)pi * 2 * REC;
+        const int nv = min(P, n_tok - pi * P);          // valid tokens of this page
+        if (nv - tin >= 16) step(pg, tin, std::true_type{}, nv);
+        else step(pg, tin, std::false_type{}, nv);
       }
-      cursor_next(p, cp);
+    }
+    // release the stage; the last warp to do so refills it with chunk i + S
+    __syncwarp();
+    uint32_t last = 0;
+    if (lane == 0) {
+      __threadfence_block();
+      last = atomicAdd(&released[stage], 1u) == kWarps - 1;
+      if (last) {
+        released[stage] = 0;
+        __threadfence_block();
+        if (i + S < nch) {
+          Cursor c{(int)dv.y, (int)dv.z, (int64_t)dw.y, 0};
+          c.nc = seq_chunks(p, c.b, false);
+          for (int k = 0; k < S; ++k) cursor_next(p, c);
+          fence_proxy_async();
+          issue(c, stage);
+        }
+      }
     }
   }
   if (cur_unit >= 0) flush(cur_unit);
@@ -950,9 +970,10 @@ kvq3_status decode_plan_t(const CacheGeom& g, int G, DecodePlan* plan) {
   const size_t chunk_bytes = (size_t)plan->pages_per_chunk * 2 * g.record_bytes;
   // + 16: word reads past the last code string; + descriptor at the end
   plan->stage_bytes = (uint32_t)((chunk_bytes + 16 + sizeof(ChunkDesc) + 127) / 128 * 128);
-  // aim for ~24 KB of stages per CTA (4 CTAs per SM), at least 2 stages
-  int stages = (int)(24576 / plan->stage_bytes);
-  stages = stages < 2 ? 2 : (stages > 6 ? 6 : stages);
+  // ~48 KB of stages per CTA: with four CTAs per SM that keeps well over
+  // 100 KB per SM in flight, enough to cover HBM latency; at least 2 stages
+  int stages = (int)(49152 / plan->stage_bytes);
+  stages = stages < 2 ? 2 : (stages > kMaxStages ? kMaxStages : stages);
   const size_t smem = SM::kStageOff + (size_t)stages * plan->stage_bytes;
   if (smem > 220 * 1024) return KVQ3_ERR_UNSUPPORTED;  // pages too large for a two-stage ring
   plan->stages = stages;
