@@ -16,7 +16,7 @@ __all__ = [
     "lib", "kvq3_abi_version", "kvq3_status_string", "kvq3_rotation_create",
     "kvq3_rotation_create_from_params", "kvq3_rotation_destroy", "kvq3_rotation_export",
     "kvq3_cache_sizes", "kvq3_rotate", "kvq3_write", "kvq3_decode_workspace_size",
-    "kvq3_decode_attn", "kvq3_dequant_debug", "Rotation",
+    "kvq3_decode_attn", "kvq3_decode_attn_noalloc", "kvq3_dequant_debug", "Rotation",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -67,6 +67,7 @@ _SIGS = {
     "kvq3_write": (ctypes.c_int, [_p, _D, _C, _p, _p, _p, _p, _i64, _p, _p]),
     "kvq3_decode_workspace_size": (ctypes.c_int, [_D, _i32, ctypes.POINTER(_sz)]),
     "kvq3_decode_attn": (ctypes.c_int, [_p, _D, _C, _p, _i32, _f32, _p, _p, _sz, _p, _p]),
+    "kvq3_decode_attn_noalloc": (ctypes.c_int, [_p, _D, _C, _p, _i32, _f32, _p, _p, _p]),
     "kvq3_dequant_debug": (ctypes.c_int, [_p, _D, _C, _i32, _i32, _i32, _i64, _i64, _p, _p, _p, _p]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -180,6 +181,16 @@ def kvq3_decode_attn(h, desc: CacheDesc, cache: Cache, q, out, workspace, sm_sca
                                 int(q.shape[1]), float(sm_scale), _ptr(out), _ptr(workspace),
                                 workspace.numel() * workspace.element_size(), _ptr(dev_status),
                                 _stream(stream)), "kvq3_decode_attn")
+
+
+def kvq3_decode_attn_noalloc(h, desc: CacheDesc, cache: Cache, q, out, sm_scale: float = 0.0,
+                             dev_status=None, stream=None) -> None:
+    """kvq3_decode_attn for callers that cannot allocate device memory: the
+    workspace is a fixed array inside the library (KVQ3_DECODE_NOALLOC_MAX_BYTES);
+    calls sharing it must not overlap on the GPU."""
+    _check(lib.kvq3_decode_attn_noalloc(h, ctypes.byref(desc), ctypes.byref(cache), _ptr(q),
+                                        int(q.shape[1]), float(sm_scale), _ptr(out), _ptr(dev_status),
+                                        _stream(stream)), "kvq3_decode_attn_noalloc")
 
 
 def kvq3_dequant_debug(h, desc: CacheDesc, cache: Cache, seq: int, kv_head: int, which: int,

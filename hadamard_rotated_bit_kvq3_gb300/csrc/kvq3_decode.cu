@@ -2,6 +2,8 @@
 #include <math.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "kvq3_decode.cuh"
 
 using namespace kvq3;
@@ -93,3 +95,50 @@ kvq3_status kvq3_decode_attn(kvq3_rotation rot, const kvq3_cache_desc* desc,
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ no-alloc
+// Workspace of kvq3_decode_attn_noalloc: a fixed array in the library's
+// device image, so the call itself never allocates.  Every GPU that loads the
+// library holds it until the process exits.
+namespace {
+
+constexpr size_t kNoAllocBytes = (size_t)8 << 20;  // 8 MiB: KVQ3_DECODE_NOALLOC_MAX_BYTES
+static_assert(kNoAllocBytes == KVQ3_DECODE_NOALLOC_MAX_BYTES, "header and library disagree");
+static __device__ __align__(256) unsigned char g_noalloc_ws[kNoAllocBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices];  // device address of g_noalloc_ws, per device
+
+// Device address of the array on the current device.  The name g_noalloc_ws
+// in host code is only a host-side stand-in, so the address is looked up
+// once per device (with that device current) and kept.
+kvq3_status noalloc_workspace(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KVQ3_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return KVQ3_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_ws) != cudaSuccess || p == nullptr) return KVQ3_ERR_CUDA;
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return KVQ3_OK;
+}
+
+}  // namespace
+
+extern "C" kvq3_status kvq3_decode_attn_noalloc(kvq3_rotation rot, const kvq3_cache_desc* desc,
+                                                const kvq3_cache* cache, const void* q,
+                                                int32_t num_q_heads, float sm_scale, float* out,
+                                                int32_t* dev_status, void* stream) {
+  size_t need = 0;
+  kvq3_status s = kvq3_decode_workspace_size(desc, num_q_heads, &need);
+  if (s != KVQ3_OK) return s;
+  if (need > kNoAllocBytes) return KVQ3_ERR_WORKSPACE;
+  void* ws = nullptr;
+  if ((s = noalloc_workspace(&ws)) != KVQ3_OK) return s;
+  return kvq3_decode_attn(rot, desc, cache, q, num_q_heads, sm_scale, out, ws, kNoAllocBytes,
+                          dev_status, stream);
+}

@@ -245,6 +245,32 @@ kvq3_status kvq3_decode_attn(kvq3_rotation rot, const kvq3_cache_desc *desc,
                              void *workspace, size_t ws_bytes,
                              int32_t *dev_status, void *stream);
 
+/* Largest decode workspace kvq3_decode_attn_noalloc can serve (bytes). */
+#define KVQ3_DECODE_NOALLOC_MAX_BYTES (8u << 20)
+
+/* kvq3_decode_attn without a caller-provided workspace (none of the pages
+ * has a counterpart: this is a deployment convenience).  For callers that
+ * cannot allocate device memory when they call -- for instance a serving loop
+ * whose memory is entirely reserved by its framework at start-up, or a plugin
+ * that is handed tensors but no allocator.  The call allocates nothing: the
+ * split partials go to a fixed 8 MiB array built into the library
+ * (KVQ3_DECODE_NOALLOC_MAX_BYTES), which every GPU that loads the library
+ * keeps until the process exits.  Arguments and results are those of
+ * kvq3_decode_attn.
+ *   - Returns KVQ3_ERR_WORKSPACE, with nothing launched, when the call would
+ *     need more than the array holds (kvq3_decode_workspace_size tells).
+ *   - The first call on a device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - All calls share the one array per device, and it keeps whatever the
+ *     last call left in it (nothing needs clearing: every partial the merge
+ *     reads is written earlier in the same call).  Calls that overlap on the
+ *     GPU -- on different streams, or from several host threads -- race on
+ *     it and give wrong results; serialise them. */
+kvq3_status kvq3_decode_attn_noalloc(kvq3_rotation rot, const kvq3_cache_desc *desc,
+                                     const kvq3_cache *cache, const void *q,
+                                     int32_t num_q_heads, float sm_scale, float *out,
+                                     int32_t *dev_status, void *stream);
+
 /* Reads back positions t0..t0+nt-1 of sequence seq, kv head kv_head, K
  * (which = 0) or V (which = 1) as fp32 out[nt][d]: s_q * c in the rotated
  * domain (rot == NULL) or U^T (s_q * c) (rot != NULL) ([OIQ] 3.3 "Retrieve").
