@@ -172,8 +172,11 @@ class GpuWorkload:
             for t0 in range(0, n, 65536):
                 m = min(65536, n - t0)
                 k, v = self.kv_rows(b, t0, m)
-                self.write(k, v, torch.full((m,), b, dtype=torch.int32, device=device),
-                           torch.arange(t0, t0 + m, dtype=torch.int32, device=device))
+                if w.d <= 128:
+                    K.kvq3_write_chunk(self.rot.handle, self.desc, self.cache, k, v, b, t0, self.status)
+                else:
+                    self.write(k, v, torch.full((m,), b, dtype=torch.int32, device=device),
+                               torch.arange(t0, t0 + m, dtype=torch.int32, device=device))
         # the decode step's own token: position L_b - 1 of every sequence
         rows = [self.kv_rows(b, int(self.lens[b]) - 1, 1) for b in range(w.batch)]
         self.k_new = torch.cat([r[0] for r in rows])
@@ -243,8 +246,8 @@ class PrefillWorkload:
         torch.cuda.synchronize()
 
     def step(self):
-        self.K.kvq3_write(self.rot.handle, self.desc, self.cache, self.k, self.v, self.seq, self.pos,
-                          self.status)
+        self.K.kvq3_write_chunk(self.rot.handle, self.desc, self.cache, self.k, self.v, 0, 0,
+                                self.status)
 
     def bytes(self):
         w = self.w
@@ -394,7 +397,7 @@ def run_prefill(args, world, rank, dev):
                        "l2": "inputs larger than L2"},
             "roofline": {"bound": "hbm", "achieved": gbs / world, "peak": peaks["hbm"], "unit": "GB/s",
                          "frac": gbs / world / peaks["hbm"], "traffic": None,
-                         "kernel": "write_kernel", "peak_source": peaks["src"]},
+                         "kernel": "write_chunk_kernel", "peak_source": peaks["src"]},
             "tokens_per_s": w.seq_len * world / (ms * 1e-3),
             "gpu_launches": args.steps, "clocks": clk.summary()}))
 

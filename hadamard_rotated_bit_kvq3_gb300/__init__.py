@@ -15,7 +15,7 @@ __all__ = [
     "KVQ3_OK", "KVQ3_ROT_SIGN", "KVQ3_ROT_SO4", "SCALE_TYPES", "CacheDesc", "Cache", "Kvq3Error",
     "lib", "kvq3_abi_version", "kvq3_status_string", "kvq3_rotation_create",
     "kvq3_rotation_create_from_params", "kvq3_rotation_destroy", "kvq3_rotation_export",
-    "kvq3_cache_sizes", "kvq3_rotate", "kvq3_write", "kvq3_decode_workspace_size",
+    "kvq3_cache_sizes", "kvq3_rotate", "kvq3_write", "kvq3_write_chunk", "kvq3_decode_workspace_size",
     "kvq3_decode_attn", "kvq3_decode_attn_noalloc", "kvq3_dequant_debug", "Rotation",
 ]
 
@@ -65,6 +65,7 @@ _SIGS = {
     "kvq3_cache_sizes": (ctypes.c_int, [_D, ctypes.POINTER(_sz), ctypes.POINTER(_sz), ctypes.POINTER(_sz)]),
     "kvq3_rotate": (ctypes.c_int, [_p, _p, _i32, _p, _i64, _i32, _p]),
     "kvq3_write": (ctypes.c_int, [_p, _D, _C, _p, _p, _p, _p, _i64, _p, _p]),
+    "kvq3_write_chunk": (ctypes.c_int, [_p, _D, _C, _p, _p, _i32, _i64, _i64, _p, _p]),
     "kvq3_decode_workspace_size": (ctypes.c_int, [_D, _i32, ctypes.POINTER(_sz)]),
     "kvq3_decode_attn": (ctypes.c_int, [_p, _D, _C, _p, _i32, _f32, _p, _p, _sz, _p, _p]),
     "kvq3_decode_attn_noalloc": (ctypes.c_int, [_p, _D, _C, _p, _i32, _f32, _p, _p, _p]),
@@ -165,6 +166,14 @@ def kvq3_write(h, desc: CacheDesc, cache: Cache, k, v, seq_idx, pos, dev_status=
     _check(lib.kvq3_write(h, ctypes.byref(desc), ctypes.byref(cache), _ptr(k), _ptr(v),
                           _ptr(seq_idx), _ptr(pos), int(k.shape[0]), _ptr(dev_status),
                           _stream(stream)), "kvq3_write")
+
+
+def kvq3_write_chunk(h, desc: CacheDesc, cache: Cache, k, v, seq: int, pos0: int, dev_status=None,
+                     stream=None) -> None:
+    """k, v: fp16 [n_tok][Hkv][d] for positions pos0.. of sequence seq (CUDA tensors)."""
+    _check(lib.kvq3_write_chunk(h, ctypes.byref(desc), ctypes.byref(cache), _ptr(k), _ptr(v), seq,
+                                pos0, int(k.shape[0]), _ptr(dev_status), _stream(stream)),
+           "kvq3_write_chunk")
 
 
 def kvq3_decode_workspace_size(desc: CacheDesc, num_q_heads: int) -> int:

@@ -1,0 +1,334 @@
+// Write path for a contiguous chunk of positions of one sequence (prefill):
+// rotate, quantise and pack every K and V vector of tokens pos0..pos0+n-1.
+//
+// "Orthogonally mixed 3-bit KV cache", Implementation notes (write path) and
+// Key formulas; "Orthogonal Invariance in Activation Space", 3.1-3.4.  Same
+// arithmetic and stored format as kvq3_write (include/kvq3.h R1-R9), laid out
+// for throughput:
+//  * one thread per vector (d = 64 or 128 values in registers), 128 vectors
+//    (consecutive tokens of one kv head, K or V) per CTA tile;
+//  * the tile's fp16 rows are staged through shared memory with cp.async
+//    (16-byte pieces, XOR-swizzled so both the coalesced fill and the
+//    row-per-thread read are bank-conflict free), double-buffered;
+//  * sign flip D as an XOR of fp16 sign bits with masks from the constant
+//    bank; the Walsh-Hadamard butterfly with packed f32x2 adds (element i
+//    and i + d/2 share a register pair, so every stage but the last is packed);
+//    SO(4) blocks with the quaternion pairs of blocks i and i + d/8 packed;
+//  * 1/sqrt(d) is folded into the block maximum and the reciprocal scale;
+//  * codes by one fused multiply-add against the 1.5*2^23 rounding constant
+//    (round half to even), packed in-thread into 32-bit words, stored with
+//    16-byte stores.
+#include <string.h>
+
+#include "kvq3_internal.h"
+
+using namespace kvq3;
+
+namespace {
+
+constexpr int kTile = 128;  // vectors per CTA tile = threads per CTA
+
+struct ChunkParams {
+  CacheGeom g;
+  uint8_t* pool;
+  const int32_t* page_table;
+  const __half* k;
+  const __half* v;
+  int32_t* status;
+  int64_t pos0, n_tok;
+  int32_t seq;
+  int32_t tiles_per_head;     // ceil(n_tok / kTile)
+  int64_t n_tiles;            // 2 * hkv * tiles_per_head
+  float inv_sqrt_d;
+  uint32_t sign_xor[kMaxD / 2];   // fp16-pair sign masks of the input order
+  float2 quat2[kMaxD / 8][4];     // quaternion coefficients of blocks (i, i + d/8)
+};
+
+typedef unsigned long long u64;
+__device__ __forceinline__ float2 f2add(float2 a, float2 b) {
+  u64 d, x = *reinterpret_cast<u64*>(&a), y = *reinterpret_cast<u64*>(&b);
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(x), "l"(y));
+  return *reinterpret_cast<float2*>(&d);
+}
+__device__ __forceinline__ float2 f2sub(float2 a, float2 b) {
+  u64 d, x = *reinterpret_cast<u64*>(&a), y = *reinterpret_cast<u64*>(&b);
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(x), "l"(y));
+  return *reinterpret_cast<float2*>(&d);
+}
+__device__ __forceinline__ float2 f2mul(float2 a, float2 b) {
+  u64 d, x = *reinterpret_cast<u64*>(&a), y = *reinterpret_cast<u64*>(&b);
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(x), "l"(y));
+  return *reinterpret_cast<float2*>(&d);
+}
+__device__ __forceinline__ float2 f2fma(float2 a, float2 b, float2 c) {
+  u64 d, x = *reinterpret_cast<u64*>(&a), y = *reinterpret_cast<u64*>(&b),
+         z = *reinterpret_cast<u64*>(&c);
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(x), "l"(y), "l"(z));
+  return *reinterpret_cast<float2*>(&d);
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  const int n = valid ? 16 : 0;  // 0 source bytes: the 16 bytes are zero-filled
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n)
+               : "memory");
+}
+
+template <int D, int BLOCK, int SCALE, bool SO4>
+__global__ void __launch_bounds__(kTile) write_chunk_kernel(const __grid_constant__ ChunkParams p) {
+  constexpr int H = D / 2;              // register pairs: x2[k] = (x[k], x[k + H])
+  constexpr int ROWB = 2 * D;           // bytes per input row
+  constexpr int PIECES = ROWB / 16;     // 16-byte pieces per row (8 or 16)
+  constexpr int NB = D / BLOCK;
+  constexpr int CB = 3 * D / 8;         // code bytes (24 or 48)
+  constexpr int SB = SCALE == KVQ3_SCALE_F32 ? 4 : SCALE == KVQ3_SCALE_F16 ? 2 : 1;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int t = threadIdx.x;
+  const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem);
+  const CacheGeom& g = p.g;
+
+  // stage the rows of tile `tile` into buffer `buf`
+  auto load_tile = [&](int64_t tile, int buf) {
+    const int which = (int)(tile / ((int64_t)g.hkv * p.tiles_per_head));
+    const int64_t rem = tile - (int64_t)which * g.hkv * p.tiles_per_head;
+    const int head = (int)(rem / p.tiles_per_head);
+    const int64_t tok0 = (rem - (int64_t)head * p.tiles_per_head) * kTile;
+    const __half* src = (which ? p.v : p.k) + head * D;
+    const uint32_t dst = sbase + (uint32_t)buf * kTile * ROWB;
+#pragma unroll
+    for (int i = 0; i < PIECES; ++i) {
+      const int idx = i * kTile + t;            // piece index in the tile
+      const int row = idx / PIECES, pc = idx % PIECES;
+      const int64_t tok = tok0 + row;
+      const bool valid = tok < p.n_tok;
+      const __half* s = src + (valid ? tok : 0) * (int64_t)g.hkv * D + pc * 8;
+      cp_async16(dst + row * ROWB + ((pc ^ (row & (PIECES - 1))) * 16), s, valid);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+
+  int64_t tile = blockIdx.x;
+  if (tile >= p.n_tiles) return;
+  load_tile(tile, 0);
+  for (int it = 0; tile < p.n_tiles; ++it, tile += gridDim.x) {
+    const int buf = it & 1;
+    const int64_t next = tile + gridDim.x;
+    if (next < p.n_tiles) load_tile(next, buf ^ 1);
+    else asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+    __syncthreads();
+
+    // ---- this thread's vector: row t of the tile
+    const int which = (int)(tile / ((int64_t)g.hkv * p.tiles_per_head));
+    const int64_t rem = tile - (int64_t)which * g.hkv * p.tiles_per_head;
+    const int head = (int)(rem / p.tiles_per_head);
+    const int64_t tok = (rem - (int64_t)head * p.tiles_per_head) * kTile + t;
+    float2 x2[H];
+    {
+      const uint32_t rowa = sbase + (uint32_t)buf * kTile * ROWB + t * ROWB;
+#pragma unroll
+      for (int pc = 0; pc < PIECES; ++pc) {
+        uint4 w;
+        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                     : "r"(rowa + ((pc ^ (t & (PIECES - 1))) * 16)));
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int e = pc * 8 + 2 * q;          // elements e, e+1
+          const uint32_t h = ww[q] ^ p.sign_xor[e / 2];
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+          if (e < H) {
+            x2[e].x = f.x;
+            x2[e + 1].x = f.y;
+          } else {
+            x2[e - H].y = f.x;
+            x2[e + 1 - H].y = f.y;
+          }
+        }
+      }
+    }
+    __syncthreads();  // the buffer is refilled two tiles later
+
+    // ---- Walsh-Hadamard butterfly: stages h < H packed, stage H inside pairs
+#pragma unroll
+    for (int h = 1; h < H; h <<= 1) {
+#pragma unroll
+      for (int i = 0; i < H; ++i) {
+        if ((i & h) == 0) {
+          const float2 a = x2[i], b = x2[i + h];
+          x2[i] = f2add(a, b);
+          x2[i + h] = f2sub(a, b);
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < H; ++i) {
+      const float a = x2[i].x, b = x2[i].y;
+      x2[i].x = a + b;
+      x2[i].y = a - b;
+    }
+    // ---- SO(4) blocks (coefficients carry 1/sqrt(d) when present)
+    if constexpr (SO4) {
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) {
+        const float2 a = p.quat2[i][0], b = p.quat2[i][1], c = p.quat2[i][2], e = p.quat2[i][3];
+        const float2 x0 = x2[4 * i], x1 = x2[4 * i + 1], xx2 = x2[4 * i + 2], x3 = x2[4 * i + 3];
+        const float2 nb = make_float2(-b.x, -b.y), nc = make_float2(-c.x, -c.y),
+                     ne = make_float2(-e.x, -e.y);
+        x2[4 * i] = f2fma(a, x0, f2fma(nb, x1, f2fma(nc, xx2, f2mul(ne, x3))));
+        x2[4 * i + 1] = f2fma(b, x0, f2fma(a, x1, f2fma(ne, xx2, f2mul(c, x3))));
+        x2[4 * i + 2] = f2fma(c, x0, f2fma(e, x1, f2fma(a, xx2, f2mul(nb, x3))));
+        x2[4 * i + 3] = f2fma(e, x0, f2fma(nc, x1, f2fma(b, xx2, f2mul(a, x3))));
+      }
+    }
+    // x2 now holds sqrt(d) * (U x) (or U x when SO4 folded 1/sqrt(d) in)
+    const float post = SO4 ? 1.0f : p.inv_sqrt_d;
+
+    // ---- scales and codes, block by block
+    const bool ok_tok = tok < p.n_tok;
+    const int64_t pos = p.pos0 + tok;
+    int64_t page = -1;
+    if (ok_tok) {
+      page = page_of(g, p.page_table, p.seq, pos / g.page_size);
+      if (page < 0) set_status(p.status, KVQ3_DEV_BAD_PAGE);
+    }
+    uint32_t words[CB / 4];
+#pragma unroll
+    for (int w = 0; w < CB / 4; ++w) words[w] = 0;
+    uint32_t sbits[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      float amax = 0.0f;
+#pragma unroll
+      for (int j = b * BLOCK; j < (b + 1) * BLOCK; ++j)
+        amax = fmaxf(amax, fabsf(j < H ? x2[j].x : x2[j - H].y));
+      const float s = __fdiv_rn(amax * post + g.eps, 3.0f);
+      uint32_t bits;
+      const float sq = round_scale(s, SCALE, bits);
+      sbits[b] = bits;
+      const float inv = sq > 0.0f ? __frcp_rn(sq) * post : 0.0f;
+#pragma unroll
+      for (int j = b * BLOCK; j < (b + 1) * BLOCK; ++j) {
+        const float xv = j < H ? x2[j].x : x2[j - H].y;
+        float tq = fmaf(xv, inv, 12582912.0f);            // 1.5 * 2^23 + rint(x / s_q)
+        if constexpr (SCALE != KVQ3_SCALE_F32) tq = fminf(fmaxf(tq, 12582909.0f), 12582915.0f);
+        const uint32_t c = __float_as_uint(tq) & 7u;      // 3-bit two's complement
+        const int bit = 3 * j;
+        words[bit / 32] |= c << (bit % 32);
+        if (bit % 32 > 29) words[bit / 32 + 1] |= c >> (32 - bit % 32);
+      }
+    }
+    if (page >= 0) {
+      const int slot = (int)(pos % g.page_size);
+      uint8_t* rec = p.pool + record_offset(g, page, head, which);
+      uint8_t* cp = rec + g.scale_hdr_bytes + (int64_t)slot * CB;
+      if constexpr (CB % 16 == 0) {   // d = 128: 48-byte strings, 16-byte aligned
+        uint4* cd = reinterpret_cast<uint4*>(cp);
+#pragma unroll
+        for (int w = 0; w < CB / 16; ++w)
+          cd[w] = make_uint4(words[4 * w], words[4 * w + 1], words[4 * w + 2], words[4 * w + 3]);
+      } else {                        // d = 64: 24-byte strings, 8-byte aligned
+        uint2* cd = reinterpret_cast<uint2*>(cp);
+#pragma unroll
+        for (int w = 0; w < CB / 8; ++w) cd[w] = make_uint2(words[2 * w], words[2 * w + 1]);
+      }
+      uint8_t* sp = rec + (int64_t)slot * NB * SB;
+      if constexpr (SB == 4) {
+#pragma unroll
+        for (int b = 0; b < NB; ++b) reinterpret_cast<uint32_t*>(sp)[b] = sbits[b];
+      } else if constexpr (SB == 2) {
+#pragma unroll
+        for (int b = 0; b < NB; ++b) reinterpret_cast<uint16_t*>(sp)[b] = (uint16_t)sbits[b];
+      } else {
+#pragma unroll
+        for (int b = 0; b < NB; ++b) sp[b] = (uint8_t)sbits[b];
+      }
+    }
+  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
+template <int D, int BLOCK, int SCALE, bool SO4>
+cudaError_t launch_chunk(const ChunkParams& p, cudaStream_t st) {
+  const size_t smem = 2 * (size_t)kTile * 2 * D;
+  auto k = write_chunk_kernel<D, BLOCK, SCALE, SO4>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kTile, smem);
+  if (e != cudaSuccess) return e;
+  int64_t grid = (int64_t)sm_count() * (per_sm > 0 ? per_sm : 1);
+  if (grid > p.n_tiles) grid = p.n_tiles;
+  k<<<(unsigned)grid, kTile, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+template <int D, int BLOCK>
+cudaError_t dispatch_chunk(const ChunkParams& p, int scale, bool so4, cudaStream_t st) {
+  if (scale == KVQ3_SCALE_F32)
+    return so4 ? launch_chunk<D, BLOCK, KVQ3_SCALE_F32, true>(p, st) : launch_chunk<D, BLOCK, KVQ3_SCALE_F32, false>(p, st);
+  if (scale == KVQ3_SCALE_F16)
+    return so4 ? launch_chunk<D, BLOCK, KVQ3_SCALE_F16, true>(p, st) : launch_chunk<D, BLOCK, KVQ3_SCALE_F16, false>(p, st);
+  return so4 ? launch_chunk<D, BLOCK, KVQ3_SCALE_E4M3, true>(p, st) : launch_chunk<D, BLOCK, KVQ3_SCALE_E4M3, false>(p, st);
+}
+
+}  // namespace
+
+extern "C" kvq3_status kvq3_write_chunk(kvq3_rotation rot, const kvq3_cache_desc* desc,
+                                        const kvq3_cache* cache, const void* k, const void* v,
+                                        int32_t seq, int64_t pos0, int64_t n_tok,
+                                        int32_t* dev_status, void* stream) {
+  CacheGeom g;
+  kvq3_status s = make_geom(desc, &g);
+  if (s != KVQ3_OK) return s;
+  if (!rot || rot->d != g.d || n_tok < 0) return KVQ3_ERR_INVALID_ARG;
+  if ((s = check_cache(g, cache, false)) != KVQ3_OK) return s;
+  if (n_tok == 0) return KVQ3_OK;
+  if (!k || !v || seq < 0 || seq >= g.batch || pos0 < 0 ||
+      pos0 + n_tok > (int64_t)g.max_pages * g.page_size)
+    return KVQ3_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) % 16 != 0)
+    return KVQ3_ERR_INVALID_ARG;
+  if (g.d > 128) {
+    // d = 256 does not fit one thread: the general path handles it
+    return KVQ3_ERR_UNSUPPORTED;
+  }
+  ChunkParams p;
+  memset(&p, 0, sizeof(p));
+  p.g = g;
+  p.pool = static_cast<uint8_t*>(cache->pool);
+  p.page_table = cache->page_table;
+  p.k = static_cast<const __half*>(k);
+  p.v = static_cast<const __half*>(v);
+  p.status = dev_status;
+  p.pos0 = pos0;
+  p.n_tok = n_tok;
+  p.seq = seq;
+  p.tiles_per_head = (int32_t)((n_tok + kTile - 1) / kTile);
+  p.n_tiles = 2 * (int64_t)g.hkv * p.tiles_per_head;
+  p.inv_sqrt_d = inv_sqrt(g.d);
+  const int d = g.d;
+  for (int e = 0; e < d / 2; ++e) {
+    uint32_t m = 0;
+    if (rot->signs[2 * e] < 0) m |= 0x8000u;
+    if (rot->signs[2 * e + 1] < 0) m |= 0x80000000u;
+    p.sign_xor[e] = m;
+  }
+  const bool so4 = (rot->flags & KVQ3_ROT_SO4) != 0;
+  const double isd = 1.0 / sqrt((double)d);
+  for (int i = 0; i < d / 8; ++i)
+    for (int c = 0; c < 4; ++c)
+      p.quat2[i][c] = make_float2((float)(rot->quats64[4 * i + c] * isd),
+                                  (float)(rot->quats64[4 * (i + d / 8) + c] * isd));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  const int key = g.d * 1000 + g.block;
+  switch (key) {
+    case 64032: e = dispatch_chunk<64, 32>(p, g.scale_type, so4, st); break;
+    case 64064: e = dispatch_chunk<64, 64>(p, g.scale_type, so4, st); break;
+    case 128032: e = dispatch_chunk<128, 32>(p, g.scale_type, so4, st); break;
+    case 128064: e = dispatch_chunk<128, 64>(p, g.scale_type, so4, st); break;
+    default: return KVQ3_ERR_UNSUPPORTED;
+  }
+  return cuda_status(e);
+}

@@ -220,6 +220,19 @@ kvq3_status kvq3_write(kvq3_rotation rot, const kvq3_cache_desc *desc,
                        const int32_t *seq_idx, const int32_t *pos, int64_t n_tok,
                        int32_t *dev_status, void *stream);
 
+/* Write path for a prefill chunk: positions pos0 .. pos0+n_tok-1 of sequence
+ * seq, with k, v: device fp16 [n_tok][Hkv][d] (row i is position pos0 + i).
+ * Same arithmetic and stored bytes as kvq3_write ([OMC] Implementation notes,
+ * write path), without per-token index arrays: one thread per vector, rows
+ * staged through shared memory, packed f32x2 butterfly.  d must be 64 or 128
+ * (KVQ3_ERR_UNSUPPORTED otherwise; kvq3_write covers d = 256).  The position
+ * range must lie inside the sequence's capacity (KVQ3_ERR_INVALID_ARG);
+ * invalid page ids are skipped and flagged in *dev_status. */
+kvq3_status kvq3_write_chunk(kvq3_rotation rot, const kvq3_cache_desc *desc,
+                             const kvq3_cache *cache, const void *k, const void *v,
+                             int32_t seq, int64_t pos0, int64_t n_tok,
+                             int32_t *dev_status, void *stream);
+
 /* Bytes of device workspace kvq3_decode_attn needs for num_q_heads query
  * heads on the current device (0 < *bytes, a few MB). */
 kvq3_status kvq3_decode_workspace_size(const kvq3_cache_desc *desc,

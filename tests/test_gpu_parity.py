@@ -236,3 +236,64 @@ def test_decode_split_count_invariance():
     q = c1.queries()
     a = c1.gpu_decode(q)
     assert rel_err(a, c1.oracle_decode(q)) <= TOL_DECODE
+
+
+# ------------------------------------------------------------------ write (prefill chunks)
+CHUNK_CASES = [
+    dict(d=128, block=32, scale="f32", page=64, lens=(700,), hkv=3, hq=3, flags=1, pos0=0),
+    dict(d=128, block=64, scale="f16", page=64, lens=(1000, 5), hkv=2, hq=8, flags=3, pos0=37),
+    dict(d=128, block=64, scale="e4m3", page=16, lens=(300,), hkv=2, hq=16, paged=True, flags=3, pos0=5),
+    dict(d=64, block=32, scale="f16", page=32, lens=(257,), hkv=2, hq=4, paged=True, flags=3, pos0=0),
+    dict(d=64, block=64, scale="f32", page=16, lens=(129,), hkv=1, hq=1, flags=0, pos0=16),
+    dict(d=128, block=32, scale="e4m3", page=48, lens=(400,), hkv=1, hq=2, flags=2, pos0=1),
+]
+
+
+@pytest.mark.parametrize("cfg", CHUNK_CASES, ids=lambda c: f"d{c['d']}-m{c['block']}-{c['scale']}-P{c['page']}-pos{c['pos0']}")
+def test_write_chunk_matches_oracle(cfg):
+    import torch
+    import hadamard_rotated_bit_kvq3_gb300 as K
+    cfg = dict(cfg)
+    pos0 = cfg.pop("pos0")
+    c = Case(**cfg)
+    n = int(c.lens[0]) - pos0
+    k = np.stack([__import__("kvq3_inputs").kv_rows_np(c.spec, 0, 0, h, pos0, n) for h in range(c.hkv)], 1)
+    v = np.stack([__import__("kvq3_inputs").kv_rows_np(c.spec, 1, 0, h, pos0, n) for h in range(c.hkv)], 1)
+    si = np.zeros(n, np.int32)
+    ps = np.arange(pos0, pos0 + n, dtype=np.int32)
+    K.kvq3_write_chunk(c.rot.handle, c.desc, c.cache, torch.as_tensor(k, device="cuda"),
+                       torch.as_tensor(v, device="cuda"), 0, pos0, c.status)
+    assert c.oracle_write(k, v, si, ps) == 0
+    assert c.device_status() == 0
+    stats = c.compare_written(k, v, si, ps)
+    print(stats)
+    if stats["boundary_codes"] == 0 and stats["midpoint_blocks"] == 0:
+        assert np.array_equal(c.pool.cpu().numpy(), c.pool_o)
+
+
+def test_write_chunk_equals_token_list_write():
+    # the chunk entry point and the token-list entry point store the same bytes
+    import torch
+    import hadamard_rotated_bit_kvq3_gb300 as K
+    c1 = Case(d=128, block=64, scale="f16", page=64, lens=(333,), hkv=4, hq=16)
+    c2 = Case(d=128, block=64, scale="f16", page=64, lens=(333,), hkv=4, hq=16)
+    k, v, si, ps = c1.tokens()
+    K.kvq3_write_chunk(c1.rot.handle, c1.desc, c1.cache, torch.as_tensor(k, device="cuda"),
+                       torch.as_tensor(v, device="cuda"), 0, 0, c1.status)
+    c2.gpu_write(k, v, si, ps)
+    torch.cuda.synchronize()
+    a, b = c1.pool.cpu().numpy(), c2.pool.cpu().numpy()
+    # both are fp32 computations of the same formula; allow only boundary flips
+    diff = np.nonzero(a != b)[0]
+    assert len(diff) <= 0.0005 * a.size
+
+
+def test_write_chunk_rejects_out_of_range():
+    import torch
+    import hadamard_rotated_bit_kvq3_gb300 as K
+    c = Case(d=128, block=64, scale="f16", page=64, lens=(100,), hkv=1, hq=1)
+    k = torch.zeros((10, 1, 128), dtype=torch.float16, device="cuda")
+    with pytest.raises(K.Kvq3Error):
+        K.kvq3_write_chunk(c.rot.handle, c.desc, c.cache, k, k, 0, c.maxp * 64 - 5, c.status)
+    with pytest.raises(K.Kvq3Error):
+        K.kvq3_write_chunk(c.rot.handle, c.desc, c.cache, k, k, 3, 0, c.status)
