@@ -73,6 +73,21 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool v
                : "memory");
 }
 
+// tile -> (K|V, kv head, first token); all counts fit 32 bits (checked on the host)
+struct TileId {
+  int which, head;
+  uint32_t tok0;
+};
+__device__ __forceinline__ TileId tile_id(const ChunkParams& p, uint32_t tile) {
+  const uint32_t per_which = (uint32_t)p.g.hkv * (uint32_t)p.tiles_per_head;
+  TileId id;
+  id.which = tile >= per_which;
+  const uint32_t rem = tile - (id.which ? per_which : 0u);
+  id.head = (int)(rem / (uint32_t)p.tiles_per_head);
+  id.tok0 = (rem - (uint32_t)id.head * (uint32_t)p.tiles_per_head) * kTile;
+  return id;
+}
+
 template <int D, int BLOCK, int SCALE, bool SO4>
 __global__ void __launch_bounds__(kTile) write_chunk_kernel(const __grid_constant__ ChunkParams p) {
   constexpr int H = D / 2;              // register pairs: x2[k] = (x[k], x[k + H])
@@ -87,41 +102,39 @@ __global__ void __launch_bounds__(kTile) write_chunk_kernel(const __grid_constan
   const CacheGeom& g = p.g;
 
   // stage the rows of tile `tile` into buffer `buf`
-  auto load_tile = [&](int64_t tile, int buf) {
-    const int which = (int)(tile / ((int64_t)g.hkv * p.tiles_per_head));
-    const int64_t rem = tile - (int64_t)which * g.hkv * p.tiles_per_head;
-    const int head = (int)(rem / p.tiles_per_head);
-    const int64_t tok0 = (rem - (int64_t)head * p.tiles_per_head) * kTile;
-    const __half* src = (which ? p.v : p.k) + head * D;
+  auto load_tile = [&](uint32_t tile, int buf) {
+    const TileId id = tile_id(p, tile);
+    const uint32_t tok0 = id.tok0;
+    const __half* src = (id.which ? p.v : p.k) + id.head * D;
     const uint32_t dst = sbase + (uint32_t)buf * kTile * ROWB;
 #pragma unroll
     for (int i = 0; i < PIECES; ++i) {
       const int idx = i * kTile + t;            // piece index in the tile
       const int row = idx / PIECES, pc = idx % PIECES;
-      const int64_t tok = tok0 + row;
-      const bool valid = tok < p.n_tok;
-      const __half* s = src + (valid ? tok : 0) * (int64_t)g.hkv * D + pc * 8;
+      const uint32_t tok = tok0 + row;
+      const bool valid = tok < (uint32_t)p.n_tok;
+      const __half* s = src + (size_t)(valid ? tok : 0u) * (uint32_t)(g.hkv * D) + pc * 8;
       cp_async16(dst + row * ROWB + ((pc ^ (row & (PIECES - 1))) * 16), s, valid);
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
   };
 
-  int64_t tile = blockIdx.x;
-  if (tile >= p.n_tiles) return;
+  const uint32_t n_tiles = (uint32_t)p.n_tiles;
+  uint32_t tile = blockIdx.x;
+  if (tile >= n_tiles) return;
   load_tile(tile, 0);
-  for (int it = 0; tile < p.n_tiles; ++it, tile += gridDim.x) {
+  for (int it = 0; tile < n_tiles; ++it, tile += gridDim.x) {
     const int buf = it & 1;
-    const int64_t next = tile + gridDim.x;
-    if (next < p.n_tiles) load_tile(next, buf ^ 1);
+    const uint32_t next = tile + gridDim.x;
+    if (next < n_tiles) load_tile(next, buf ^ 1);
     else asm volatile("cp.async.commit_group;" ::: "memory");
     asm volatile("cp.async.wait_group 1;" ::: "memory");
     __syncthreads();
 
     // ---- this thread's vector: row t of the tile
-    const int which = (int)(tile / ((int64_t)g.hkv * p.tiles_per_head));
-    const int64_t rem = tile - (int64_t)which * g.hkv * p.tiles_per_head;
-    const int head = (int)(rem / p.tiles_per_head);
-    const int64_t tok = (rem - (int64_t)head * p.tiles_per_head) * kTile + t;
+    const TileId id = tile_id(p, tile);
+    const int which = id.which, head = id.head;
+    const uint32_t tok = id.tok0 + t;
     float2 x2[H];
     {
       const uint32_t rowa = sbase + (uint32_t)buf * kTile * ROWB + t * ROWB;
@@ -185,11 +198,12 @@ __global__ void __launch_bounds__(kTile) write_chunk_kernel(const __grid_constan
     const float post = SO4 ? 1.0f : p.inv_sqrt_d;
 
     // ---- scales and codes, block by block
-    const bool ok_tok = tok < p.n_tok;
-    const int64_t pos = p.pos0 + tok;
+    const bool ok_tok = tok < (uint32_t)p.n_tok;
+    const uint32_t pos = (uint32_t)p.pos0 + tok;        // < capacity < 2^31
+    const uint32_t lp = pos / (uint32_t)g.page_size;
     int64_t page = -1;
     if (ok_tok) {
-      page = page_of(g, p.page_table, p.seq, pos / g.page_size);
+      page = page_of(g, p.page_table, p.seq, lp);
       if (page < 0) set_status(p.status, KVQ3_DEV_BAD_PAGE);
     }
     uint32_t words[CB / 4];
@@ -219,7 +233,7 @@ __global__ void __launch_bounds__(kTile) write_chunk_kernel(const __grid_constan
       }
     }
     if (page >= 0) {
-      const int slot = (int)(pos % g.page_size);
+      const int slot = (int)(pos - lp * (uint32_t)g.page_size);
       uint8_t* rec = p.pool + record_offset(g, page, head, which);
       uint8_t* cp = rec + g.scale_hdr_bytes + (int64_t)slot * CB;
       if constexpr (CB % 16 == 0) {   // d = 128: 48-byte strings, 16-byte aligned
@@ -287,6 +301,9 @@ extern "C" kvq3_status kvq3_write_chunk(kvq3_rotation rot, const kvq3_cache_desc
   if (!k || !v || seq < 0 || seq >= g.batch || pos0 < 0 ||
       pos0 + n_tok > (int64_t)g.max_pages * g.page_size)
     return KVQ3_ERR_INVALID_ARG;
+  // 32-bit position, token and tile arithmetic on the device
+  if (pos0 + n_tok >= ((int64_t)1 << 31) || n_tok * g.hkv * g.d >= ((int64_t)1 << 32))
+    return KVQ3_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) % 16 != 0)
     return KVQ3_ERR_INVALID_ARG;
   if (g.d > 128) {
