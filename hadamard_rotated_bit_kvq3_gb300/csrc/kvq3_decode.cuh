@@ -342,7 +342,8 @@ struct ChunkDesc {
   int32_t unit, b, kvh, n_tok;
   uint32_t page_ok;  // bit i: page i of the chunk has a valid id (else masked)
   int32_t c;         // chunk index within its unit
-  int32_t pad[2];
+  int32_t nc;        // chunks of the unit
+  int32_t len;       // attended length of the sequence
 };
 
 template <int D, int GPAD>
@@ -419,9 +420,8 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
   // ---- producer: chunk descriptor + bulk copies of its pages (thread 0 fills
   // the first stages; afterwards the last warp to release a stage refills it)
   const uint64_t pol = policy_evict_first();
-  auto issue = [&](const Cursor& c, int stage) {
+  auto issue = [&](const Cursor& c, int stage, int64_t len) {
     uint8_t* dst = stg + (size_t)stage * p.stage_bytes;
-    const int64_t len = p.seq_lens[c.b];
     const int64_t tok0 = c.c * p.chunk_tokens;
     const int n_tok = (int)min((int64_t)p.chunk_tokens, len - tok0);
     const int npg = (n_tok + g.page_size - 1) / g.page_size;
@@ -441,6 +441,8 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
     dsc->n_tok = n_tok;
     dsc->page_ok = ok;
     dsc->c = (int32_t)c.c;
+    dsc->nc = (int32_t)c.nc;
+    dsc->len = (int32_t)len;
     if (bytes) {
       mbar_expect_tx(&full[stage], bytes);
       for (int i = 0; i < npg; ++i)
@@ -456,7 +458,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
     Cursor cp = cursor_at(p, c0);  // warp-collective
     if (threadIdx.x == 0) {
       for (int64_t i = 0; i < nch && i < S; ++i) {
-        issue(cp, (int)i);
+        issue(cp, (int)i, seq_len_checked(p, cp.b, false));
         cursor_next(p, cp);
       }
     }
@@ -876,11 +878,15 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
         released[stage] = 0;
         __threadfence_block();
         if (i + S < nch) {
-          Cursor c{(int)dv.y, (int)dv.z, (int64_t)dw.y, 0};
-          c.nc = seq_chunks(p, c.b, false);
+          // chunk i + S: S chunks after this one; within the same sequence no
+          // global read is needed (the descriptor carries nc and the length)
+          const uint2 dx = lds64<24>(st + desc_off);      // nc, len
+          Cursor c{(int)dv.y, (int)dv.z, (int64_t)dw.y, (int64_t)dx.x};
+          const int b_now = c.b;
           for (int k = 0; k < S; ++k) cursor_next(p, c);
+          const int64_t len = c.b == b_now ? (int64_t)dx.y : seq_len_checked(p, c.b, false);
           fence_proxy_async();
-          issue(c, stage);
+          issue(c, stage, len);
         }
       }
     }
