@@ -42,7 +42,8 @@
 
 namespace kvq3 {
 
-constexpr int kChunk = 128;      // minimum tokens per chunk (smaller pages are grouped)
+constexpr int kChunk = 192;      // minimum tokens per chunk (smaller pages are grouped)
+constexpr int kMaxPagesPerChunk = kChunk / 16;
 constexpr int kWarps = 4;        // consumer warps per CTA
 constexpr int kMaxStages = 8;
 
@@ -422,13 +423,26 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
   const uint64_t pol = policy_evict_first();
   auto issue = [&](const Cursor& c, int stage, int64_t len) {
     uint8_t* dst = stg + (size_t)stage * p.stage_bytes;
-    const int64_t tok0 = c.c * p.chunk_tokens;
-    const int n_tok = (int)min((int64_t)p.chunk_tokens, len - tok0);
-    const int npg = (n_tok + g.page_size - 1) / g.page_size;
-    const int64_t lp0 = tok0 / g.page_size;
+    // chunk c.c covers logical pages c.c*ppc .. of sequence c.b (32-bit: a
+    // sequence holds fewer than 2^31 tokens)
+    const int ppc = p.pages_per_chunk;
+    const int tok0 = (int)c.c * p.chunk_tokens;
+    const int n_tok = min(p.chunk_tokens, (int)len - tok0);
+    const int npg = n_tok == p.chunk_tokens ? ppc : (n_tok + g.page_size - 1) / g.page_size;
+    const int lp0 = (int)c.c * ppc;
+    int64_t pages[kMaxPagesPerChunk];
+    if (p.page_table) {
+      const int32_t* row = p.page_table + (int64_t)c.b * g.max_pages + lp0;
+#pragma unroll
+      for (int i = 0; i < kMaxPagesPerChunk; ++i) pages[i] = i < npg ? row[i] : -1;
+    } else {
+#pragma unroll
+      for (int i = 0; i < kMaxPagesPerChunk; ++i) pages[i] = (int64_t)c.b * g.max_pages + lp0 + i;
+    }
     uint32_t ok = 0, bytes = 0;
-    for (int i = 0; i < npg; ++i) {
-      if (page_of(g, p.page_table, c.b, lp0 + i) >= 0) {
+#pragma unroll
+    for (int i = 0; i < kMaxPagesPerChunk; ++i) {
+      if (i < npg && pages[i] >= 0 && pages[i] < g.num_pages) {
         ok |= 1u << i;
         bytes += 2 * REC;
       }
@@ -445,11 +459,11 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
     dsc->len = (int32_t)len;
     if (bytes) {
       mbar_expect_tx(&full[stage], bytes);
-      for (int i = 0; i < npg; ++i)
+      const uint8_t* base = p.pool + (int64_t)(c.kvh * 2) * REC;
+#pragma unroll
+      for (int i = 0; i < kMaxPagesPerChunk; ++i)
         if ((ok >> i) & 1u)
-          bulk_g2s(dst + (size_t)i * 2 * REC,
-                   p.pool + record_offset(g, page_of(g, p.page_table, c.b, lp0 + i), c.kvh, 0), 2 * REC,
-                   &full[stage], pol);
+          bulk_g2s(dst + (size_t)i * 2 * REC, base + pages[i] * g.page_bytes, 2 * REC, &full[stage], pol);
     } else {
       mbar_arrive(&full[stage]);
     }
