@@ -180,39 +180,84 @@ __device__ __forceinline__ uint32_t hsub2_bits(uint32_t a, uint32_t b) {
   return *reinterpret_cast<uint32_t*>(&x);
 }
 
-// Key codes: a lane's F consecutive fields (F = 16 or 8) in (lo, hi) ->
-// F/2 half2 values.  Pair k holds field lf(k) = 8(k/4) + k%4 in its low half
-// scaled by 2^(4 or 7) and field lf(k)+4 in its high half scaled by 2^(0 or 3)
-// (odd k take the larger offsets).
-__host__ __device__ constexpr int kq_lo_field(int k) { return 8 * (k / 4) + (k % 4); }
-__host__ __device__ constexpr int kq_lo_off(int k) { return (k & 1) ? 7 : 4; }
-__host__ __device__ constexpr int kq_hi_off(int k) { return (k & 1) ? 3 : 0; }
+// ---- codes -> fp16, as subnormal halves.  A 3-bit field u placed at mantissa
+// bit k of a half with a zero exponent is the exact fp16 value u * 2^(k-24).
+// With the field's sign bit flipped, u = c + 4 (c the two's-complement code),
+// so the half is (c + 4) 2^(k-24): the power of two is folded into q1 (keys) or
+// the output (values), and the +4 offset is either removed per half (values)
+// or, for keys, becomes the per-block constant 4 * sum_d 2^k_d q1_d that seeds
+// the logit accumulators (so the key path is one mask per half2).
+//
+// Sign-bit patterns: bits 3i+2 of a code string after a right shift by o sit
+// at positions congruent to (2 - o) mod 3.
+constexpr uint32_t kSignRes0 = 0x49249249u;   // positions 0, 3, 6, ...
+constexpr uint32_t kSignRes2 = 0x24924924u;   // positions 2, 5, 8, ...
+constexpr uint32_t kSignV = 0x00924924u;      // the 8 sign bits of a 24-bit value chunk
 
-// Pair k of a key chunk (lo, hi) as half2 (see above).
-template <int K>
-__device__ __forceinline__ uint32_t k_pair(uint32_t lo, uint32_t hi) {
-  constexpr int i = 8 * (K / 4) + (K & 2);  // first field of the window
-  constexpr int o = 3 * i - 4;              // window start bit: field i lands at bit 4
-  const uint32_t w = o < 0 ? (lo << (o < 0 ? -o : 0)) : __funnelshift_r(lo, hi, o < 0 ? 0 : o);
-  if constexpr (K & 1) return hsub2_bits((w & 0x00380380u) ^ 0x64206600u, 0x64206600u);
-  else return hsub2_bits((w & 0x00070070u) ^ 0x64046440u, 0x64046440u);
+// Key pairs: a lane's FQ consecutive fields (FQ = 16 or 8; field 0 at bit 0 of
+// the 64-bit window lo:hi) -> FQ/2 half2 values.  Pair P cuts the window
+// (lo:hi) >> o(P) and keeps field fl(P) at mantissa bit kl(P) of the low half
+// and field fh(P) at bit kh(P) of the high half: 3 fl - o = kl and
+// 3 fh - o - 16 = kh.  The pairings use four shifted windows for 16 fields
+// (found by exhaustive search over window offsets) and two for 8.
+//                                                 P:  0   1  2   3   4   5   6   7
+__host__ __device__ constexpr int kp_o(int FQ, int P) {
+  return FQ == 16 ? (P == 0 ? -7 : P == 1 ? -4 : P == 2 ? 0 : P < 5 ? 14 : 23)
+                  : (P < 2 ? -4 : P == 2 ? 0 : 2);
+}
+__host__ __device__ constexpr int kp_fl(int FQ, int P) {
+  return FQ == 16 ? (P == 0 ? 0 : P == 1 ? 1 : P == 2 ? 2 : P == 3 ? 5 : P + 3) : P;
+}
+__host__ __device__ constexpr int kp_fh(int FQ, int P) {
+  return FQ == 16 ? (P == 0 ? 3 : P == 1 ? 4 : P == 2 ? 6 : P + 8) : P + 4;
+}
+__host__ __device__ constexpr int kp_kl(int FQ, int P) { return 3 * kp_fl(FQ, P) - kp_o(FQ, P); }
+__host__ __device__ constexpr int kp_kh(int FQ, int P) { return 3 * kp_fh(FQ, P) - kp_o(FQ, P) - 16; }
+__host__ __device__ constexpr bool kp_valid(int FQ) {
+  unsigned seen = 0;
+  for (int P = 0; P < FQ / 2; ++P) {
+    const int kl = kp_kl(FQ, P), kh = kp_kh(FQ, P), o = kp_o(FQ, P);
+    if (kl < 0 || kl > 7 || kh < 0 || kh > 7 || ((o % 3) + 3) % 3 == 1) return false;
+    seen |= (1u << kp_fl(FQ, P)) | (1u << kp_fh(FQ, P));
+  }
+  return seen == (FQ == 32 ? ~0u : (1u << FQ) - 1u);
+}
+static_assert(kp_valid(16) && kp_valid(8), "key pair table must cover every field once");
+
+// d = (a ^ s) & M in one LOP3 (M an immediate).
+template <uint32_t M>
+__device__ __forceinline__ uint32_t xor_and(uint32_t a, uint32_t s) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0x28;" : "=r"(d) : "r"(a), "r"(s), "n"(M));
+  return d;
+}
+
+// Pair P of a key chunk (lo, hi) as a subnormal half2 (c + 4) 2^(k - 24).
+// s0 / s2: the sign patterns kSignRes0 / kSignRes2 held in registers.
+template <int FQ, int P>
+__device__ __forceinline__ uint32_t k_pair(uint32_t lo, uint32_t hi, uint32_t s0, uint32_t s2) {
+  constexpr int o = kp_o(FQ, P);
+  uint32_t w;
+  if constexpr (o < 0) w = lo << (-o);
+  else if constexpr (o == 0) w = lo;
+  else w = __funnelshift_r(lo, hi, o);
+  constexpr uint32_t M = (7u << kp_kl(FQ, P)) | (7u << (16 + kp_kh(FQ, P)));
+  return xor_and<M>(w, ((o % 3) + 3) % 3 == 0 ? s2 : s0);
 }
 
 // Value codes: fields f = 0..F-1 (F = 8 or 4) of two tokens' 3F-bit chunks
-// c0, c1 -> half2 (token0, token1) of field f scaled by 2^voff(f).
+// (sign bits already flipped) -> half2 (token0, token1) of field f, equal to
+// c 2^(voff(f) - 24).
 __host__ __device__ constexpr int v_off(int f) {
   return f == 0 ? 0 : f == 1 ? 3 : f == 2 ? 6 : f == 3 ? 1 : f == 4 ? 4 : f == 5 ? 7 : f == 6 ? 2 : 5;
 }
 
-// Field f of two tokens' value chunks c0, c1 as half2 (token0, token1),
-// scaled by 2^voff(f).
 template <int F>
 __device__ __forceinline__ uint32_t v_field(uint32_t c0, uint32_t c1) {
   constexpr uint32_t sel = F < 3 ? 0x5410u : (F < 6 ? 0x6521u : 0x7632u);
   constexpr int o = v_off(F);
-  constexpr uint32_t x = 0x64006400u | (0x00040004u << o);
   const uint32_t w = __byte_perm(c0, c1, sel);
-  return hsub2_bits((w & (0x00070007u << o)) ^ x, x);
+  return hsub2_bits(w & (0x00070007u << o), 0x00040004u << o);
 }
 
 // Bits [boff, boff + 64) of a code string (two aligned words, funnel shift).
@@ -354,7 +399,8 @@ struct DecodeSmem {
   static constexpr int kMLOff = kEmptyOff + 8 * kMaxStages;       // [kWarps][2][GPAD] floats
   static constexpr int kQOff = (kMLOff + kWarps * 2 * GPAD * 4 + 15) / 16 * 16;  // [GPAD][D]
   static constexpr int kQInvOff = kQOff + GPAD * D * 4;           // [GPAD]
-  static constexpr int kStageOff = ((kQInvOff + GPAD * 4) + 127) / 128 * 128;
+  static constexpr int kKofsOff = kQInvOff + GPAD * 4;            // [D/32][GPAD] logit seeds
+  static constexpr int kStageOff = ((kKofsOff + (D / 32) * GPAD * 4) + 127) / 128 * 128;
 };
 
 // Resident CTAs per SM the register budget is sized for: the accumulators
@@ -498,8 +544,16 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
     vshf[b] = vb & 31;
   }
 
+  // sign-bit patterns of the key windows, kept in registers (one LOP3 per pair)
+  const uint32_t sgn0 = kSignRes0, sgn2 = kSignRes2;
+
   uint32_t qf[NTQ][KS][2];
   float qinv[NTQ];
+  // logit accumulator seeds (key offset, see setup_unit): registers when few,
+  // else shared memory [block][head]
+  constexpr bool KOFS_REG = NB * NTQ <= 4;
+  float kofs[KOFS_REG ? NB : 1][KOFS_REG ? NTQ : 1];
+  float* kofs_s = reinterpret_cast<float*>(smem + SM::kKofsOff);
   float m[NTQ], l[NTQ];
   float acc[KS][NTP][4];
   int cur_unit = -1;
@@ -572,7 +626,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
             for (int e = 0; e < 2; ++e) {      // row r (e = 0) or r + 8 (e = 1)
               const int f = 2 * mp + e;
               const int dim = b * BLOCK + r * FV + f;
-              const float sc = 1.0f / (float)(1 << v_off(f));
+              const float sc = (float)(1 << (24 - v_off(f)));   // value halves are c 2^(voff-24)
               if constexpr (PSPLIT) {
                 const int h = 4 * tp + j;
                 const float v = (acc[mt][tp][2 * e] + acc[mt][tp][2 * e + 1]) * sc * cpv[tp][0];
@@ -625,7 +679,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
       if (gg < GPAD) {
 #pragma unroll
         for (int e = 0; e < EQ; ++e) qs[gg * D + rq * EQ + e] = x[e] * sc;
-        if (rq == 0) qinv_s[gg] = ldexpf(1.0f, -ex);
+        if (rq == 0) qinv_s[gg] = ldexpf(1.0f, 24 - ex);   // 2^24: subnormal key halves
       }
     }
     named_barrier(1, 128);
@@ -633,21 +687,41 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
     for (int tq = 0; tq < NTQ; ++tq) {
       const int head = 4 * tq + (r >> 1);
       const int part = r & 1;
+      float csum[NB];
+#pragma unroll
+      for (int b = 0; b < NB; ++b) csum[b] = 0.0f;
 #pragma unroll
       for (int s = 0; s < KS; ++s) {
         const int b = s / KSB, sp = s % KSB;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
-          const int k = 2 * sp + hf;
-          const int dlo = b * BLOCK + j * FQ + kq_lo_field(k);
-          const int dhi = dlo + 4;
-          const float vlo = qs[head * D + dlo] * (1.0f / (float)(1 << kq_lo_off(k)));
-          const float vhi = qs[head * D + dhi] * (1.0f / (float)(1 << kq_hi_off(k)));
+          const int P = 2 * sp + hf;
+          const int dlo = b * BLOCK + j * FQ + kp_fl(FQ, P);
+          const int dhi = b * BLOCK + j * FQ + kp_fh(FQ, P);
+          const float vlo = qs[head * D + dlo] * (1.0f / (float)(1 << kp_kl(FQ, P)));
+          const float vhi = qs[head * D + dhi] * (1.0f / (float)(1 << kp_kh(FQ, P)));
           const __half hlo = __float2half_rn(vlo), hhi = __float2half_rn(vhi);
           const float olo = part == 0 ? __half2float(hlo) : vlo - __half2float(hlo);
           const float ohi = part == 0 ? __half2float(hhi) : vhi - __half2float(hhi);
           qf[tq][s][hf] = pack_half2(olo, ohi);
+          // sum_d 2^k_d q1_d of the fp16 values the MMA sees (this lane's part)
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&qf[tq][s][hf]));
+          csum[b] += f.x * (float)(1 << kp_kl(FQ, P)) + f.y * (float)(1 << kp_kh(FQ, P));
         }
+      }
+      // reduce over the lane's quad (fields) and the hi/lo parts: lanes 8h..8h+7
+      // then hold head 4tq + h; the logit lanes of head 4tq + j read lane 8j.
+      // The key halves are (c + 4) 2^(k-24): seed the accumulators with
+      // -4 * 2^-24 * sum_d 2^k_d q1_d so they sum c 2^(k-24) q1.
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        float t = csum[b];
+        t += __shfl_xor_sync(kFull, t, 1);
+        t += __shfl_xor_sync(kFull, t, 2);
+        t += __shfl_xor_sync(kFull, t, 4);
+        const float ko = -0x1p-22f * __shfl_sync(kFull, t, 8 * j);
+        if constexpr (KOFS_REG) kofs[b][tq] = ko;
+        else if (wid == 0 && r == 0) kofs_s[b * GPAD + 4 * tq + j] = ko;
       }
       qinv[tq] = qinv_s[4 * tq + j];
     }
@@ -676,7 +750,11 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
 #pragma unroll
       for (int tq = 0; tq < NTQ; ++tq)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) accq[b][tq][c] = 0.0f;
+      {
+        accq[b][tq][0] = accq[b][tq][2] = 0.0f;
+        accq[b][tq][1] = accq[b][tq][3] = KOFS_REG ? kofs[b % (KOFS_REG ? NB : 1)][tq % (KOFS_REG ? NTQ : 1)]
+                                                   : kofs_s[b * GPAD + 4 * tq + j];   // lo column
+      }
     const uint32_t kt = pg + HDR + (uint32_t)((t0 + r) * CB);   // token t0 + r
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
@@ -688,10 +766,10 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
       static_for<KSB>([&](auto spc) {
         constexpr int sp = decltype(spc)::value;
         uint32_t af[4];
-        af[0] = k_pair<2 * sp>(lo0, hi0);
-        af[1] = k_pair<2 * sp>(lo8, hi8);
-        af[2] = k_pair<2 * sp + 1>(lo0, hi0);
-        af[3] = k_pair<2 * sp + 1>(lo8, hi8);
+        af[0] = k_pair<FQ, 2 * sp>(lo0, hi0, sgn0, sgn2);
+        af[1] = k_pair<FQ, 2 * sp>(lo8, hi8, sgn0, sgn2);
+        af[2] = k_pair<FQ, 2 * sp + 1>(lo0, hi0, sgn0, sgn2);
+        af[3] = k_pair<FQ, 2 * sp + 1>(lo8, hi8, sgn0, sgn2);
 #pragma unroll
         for (int tq = 0; tq < NTQ; ++tq)
           mma_16816(accq[b][tq], af, qf[tq][b * KSB + sp][0], qf[tq][b * KSB + sp][1]);
@@ -830,10 +908,11 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
     for (int b = 0; b < NB; ++b) {
       const uint32_t a = vt + vwo[b];
       const uint32_t sh = vshf[b];
-      const uint32_t c0v = __funnelshift_r(lds32<0>(a), lds32<4>(a), sh);
-      const uint32_t c1v = __funnelshift_r(lds32<CB>(a), lds32<CB + 4>(a), sh);
-      const uint32_t c2v = __funnelshift_r(lds32<8 * CB>(a), lds32<8 * CB + 4>(a), sh);
-      const uint32_t c3v = __funnelshift_r(lds32<9 * CB>(a), lds32<9 * CB + 4>(a), sh);
+      // sign bits flipped: fields become c + 4
+      const uint32_t c0v = __funnelshift_r(lds32<0>(a), lds32<4>(a), sh) ^ kSignV;
+      const uint32_t c1v = __funnelshift_r(lds32<CB>(a), lds32<CB + 4>(a), sh) ^ kSignV;
+      const uint32_t c2v = __funnelshift_r(lds32<8 * CB>(a), lds32<8 * CB + 4>(a), sh) ^ kSignV;
+      const uint32_t c3v = __funnelshift_r(lds32<9 * CB>(a), lds32<9 * CB + 4>(a), sh) ^ kSignV;
       static_for<KSB>([&](auto mpc) {
         constexpr int mp = decltype(mpc)::value;
         uint32_t af[4];
