@@ -464,10 +464,11 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
   }
   __syncthreads();
 
-  // ---- producer: chunk descriptor + bulk copies of its pages (thread 0 fills
-  // the first stages; afterwards the last warp to release a stage refills it)
+  // ---- producer: chunk descriptor + bulk copies of its pages, issued by one
+  // whole warp (lane i copies page i of the chunk): warp 0 fills the first
+  // stages; afterwards the last warp to release a stage refills it
   const uint64_t pol = policy_evict_first();
-  auto issue = [&](const Cursor& c, int stage, int64_t len) {
+  auto issue = [&](const Cursor& c, int stage, int64_t len) {   // warp-collective
     uint8_t* dst = stg + (size_t)stage * p.stage_bytes;
     // chunk c.c covers logical pages c.c*ppc .. of sequence c.b (32-bit: a
     // sequence holds fewer than 2^31 tokens)
@@ -475,48 +476,35 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
     const int tok0 = (int)c.c * p.chunk_tokens;
     const int n_tok = min(p.chunk_tokens, (int)len - tok0);
     const int npg = n_tok == p.chunk_tokens ? ppc : (n_tok + g.page_size - 1) / g.page_size;
-    const int lp0 = (int)c.c * ppc;
-    int64_t pages[kMaxPagesPerChunk];
-    if (p.page_table) {
-      const int32_t* row = p.page_table + (int64_t)c.b * g.max_pages + lp0;
-#pragma unroll
-      for (int i = 0; i < kMaxPagesPerChunk; ++i) pages[i] = i < npg ? row[i] : -1;
-    } else {
-#pragma unroll
-      for (int i = 0; i < kMaxPagesPerChunk; ++i) pages[i] = (int64_t)c.b * g.max_pages + lp0 + i;
+    const int lp = (int)c.c * ppc + lane;
+    int64_t pg = -1;
+    if (lane < npg)
+      pg = p.page_table ? (int64_t)p.page_table[(int64_t)c.b * g.max_pages + lp]
+                        : (int64_t)c.b * g.max_pages + lp;
+    const bool ok = pg >= 0 && pg < g.num_pages;
+    const uint32_t okm = __ballot_sync(kFull, ok);
+    if (lane == 0) {
+      if (okm != (1u << npg) - 1u) set_status(p.status, KVQ3_DEV_BAD_PAGE);
+      ChunkDesc* dsc = reinterpret_cast<ChunkDesc*>(dst + desc_off);
+      dsc->unit = c.b * g.hkv + c.kvh;
+      dsc->b = c.b;
+      dsc->kvh = c.kvh;
+      dsc->n_tok = n_tok;
+      dsc->page_ok = okm;
+      dsc->c = (int32_t)c.c;
+      dsc->nc = (int32_t)c.nc;
+      dsc->len = (int32_t)len;
+      if (okm) mbar_expect_tx(&full[stage], (uint32_t)__popc(okm) * 2u * REC);
+      else mbar_arrive(&full[stage]);
     }
-    uint32_t ok = 0, bytes = 0;
-#pragma unroll
-    for (int i = 0; i < kMaxPagesPerChunk; ++i) {
-      if (i < npg && pages[i] >= 0 && pages[i] < g.num_pages) {
-        ok |= 1u << i;
-        bytes += 2 * REC;
-      }
-    }
-    if (ok != (1u << npg) - 1u) set_status(p.status, KVQ3_DEV_BAD_PAGE);
-    ChunkDesc* dsc = reinterpret_cast<ChunkDesc*>(dst + desc_off);
-    dsc->unit = c.b * g.hkv + c.kvh;
-    dsc->b = c.b;
-    dsc->kvh = c.kvh;
-    dsc->n_tok = n_tok;
-    dsc->page_ok = ok;
-    dsc->c = (int32_t)c.c;
-    dsc->nc = (int32_t)c.nc;
-    dsc->len = (int32_t)len;
-    if (bytes) {
-      mbar_expect_tx(&full[stage], bytes);
-      const uint8_t* base = p.pool + (int64_t)(c.kvh * 2) * REC;
-#pragma unroll
-      for (int i = 0; i < kMaxPagesPerChunk; ++i)
-        if ((ok >> i) & 1u)
-          bulk_g2s(dst + (size_t)i * 2 * REC, base + pages[i] * g.page_bytes, 2 * REC, &full[stage], pol);
-    } else {
-      mbar_arrive(&full[stage]);
-    }
+    __syncwarp();
+    if (ok)
+      bulk_g2s(dst + (size_t)lane * 2 * REC, p.pool + (int64_t)(c.kvh * 2) * REC + pg * g.page_bytes, 2 * REC,
+               &full[stage], pol);
   };
   {
     Cursor cp = cursor_at(p, c0);  // warp-collective
-    if (threadIdx.x == 0) {
+    if (wid == 0) {
       for (int64_t i = 0; i < nch && i < S; ++i) {
         issue(cp, (int)i, seq_len_checked(p, cp.b, false));
         cursor_next(p, cp);
@@ -970,18 +958,18 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
       if (last) {
         released[stage] = 0;
         __threadfence_block();
-        if (i + S < nch) {
-          // chunk i + S: S chunks after this one; within the same sequence no
-          // global read is needed (the descriptor carries nc and the length)
-          const uint2 dx = lds64<24>(st + desc_off);      // nc, len
-          Cursor c{(int)dv.y, (int)dv.z, (int64_t)dw.y, (int64_t)dx.x};
-          const int b_now = c.b;
-          for (int k = 0; k < S; ++k) cursor_next(p, c);
-          const int64_t len = c.b == b_now ? (int64_t)dx.y : seq_len_checked(p, c.b, false);
-          fence_proxy_async();
-          issue(c, stage, len);
-        }
       }
+    }
+    if (__shfl_sync(kFull, last, 0) && i + S < nch) {
+      // chunk i + S: S chunks after this one; within the same sequence no
+      // global read is needed (the descriptor carries nc and the length)
+      const uint2 dx = lds64<24>(st + desc_off);      // nc, len
+      Cursor c{(int)dv.y, (int)dv.z, (int64_t)dw.y, (int64_t)dx.x};
+      const int b_now = c.b;
+      for (int k = 0; k < S; ++k) cursor_next(p, c);
+      const int64_t len = c.b == b_now ? (int64_t)dx.y : seq_len_checked(p, c.b, false);
+      fence_proxy_async();
+      issue(c, stage, len);
     }
   }
   if (cur_unit >= 0) flush(cur_unit);
@@ -1069,15 +1057,18 @@ kvq3_status decode_plan_t(const CacheGeom& g, int G, DecodePlan* plan) {
   const size_t chunk_bytes = (size_t)plan->pages_per_chunk * 2 * g.record_bytes;
   // + 16: word reads past the last code string; + descriptor at the end
   plan->stage_bytes = (uint32_t)((chunk_bytes + 16 + sizeof(ChunkDesc) + 127) / 128 * 128);
-  // ~48 KB of stages per CTA: with four CTAs per SM that keeps well over
-  // 100 KB per SM in flight, enough to cover HBM latency; at least 2 stages
-  int stages = (int)(49152 / plan->stage_bytes);
+  // stages: the SM's 228 KB of shared memory split over the CTAs that the
+  // register budget lets reside (1 KB of it reserved per CTA); at least 2
+  const int mb = decode_min_blocks(D, GPAD);
+  const size_t per_cta = 228 * 1024 / mb - 1024 < 227 * 1024 ? 228 * 1024 / mb - 1024 : 227 * 1024;
+  int stages = per_cta > SM::kStageOff ? (int)((per_cta - SM::kStageOff) / plan->stage_bytes) : 0;
   stages = stages < 2 ? 2 : (stages > kMaxStages ? kMaxStages : stages);
   const size_t smem = SM::kStageOff + (size_t)stages * plan->stage_bytes;
-  if (smem > 220 * 1024) return KVQ3_ERR_UNSUPPORTED;  // pages too large for a two-stage ring
+  if (smem > 227 * 1024) return KVQ3_ERR_UNSUPPORTED;  // pages too large for a two-stage ring
   plan->stages = stages;
   plan->smem = (uint32_t)smem;
-  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+      cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
     return KVQ3_ERR_CUDA;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, 32 * kWarps, smem) != cudaSuccess)
