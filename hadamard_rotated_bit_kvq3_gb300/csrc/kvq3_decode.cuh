@@ -840,26 +840,28 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
         x3[tq] = __shfl_sync(kFull, pr8[tq], srcB);
       }
     }
-    float sv0[NB], sv1[NB], sv2[NB], sv3[NB];
-    {
-      const uint32_t a = pg + REC + (uint32_t)(T0 * BPT);
-      SDec::template two<0>(a, sv0, sv1);
-      SDec::template two<8 * BPT>(a, sv2, sv3);
-    }
     const bool v0 = FULL || T0 < n_valid, v1 = FULL || T0 + 1 < n_valid,
                v2 = FULL || T0 + 8 < n_valid, v3 = FULL || T0 + 9 < n_valid;
+    // Columns of padded heads (>= G) carry finite values (their q1 is zero)
+    // and are never stored, so only invalid tokens are masked (their scale
+    // bytes are stale stage contents).
     uint32_t pb[NB][NTP][2];
     if constexpr (PSPLIT) {
+      float sv0[NB], sv1[NB], sv2[NB], sv3[NB];
+      {
+        const uint32_t a = pg + REC + (uint32_t)(T0 * BPT);
+        SDec::template two<0>(a, sv0, sv1);
+        SDec::template two<8 * BPT>(a, sv2, sv3);
+      }
       const bool lo_part = (r & 1) != 0;
 #pragma unroll
       for (int tp = 0; tp < NTP; ++tp) {
-        const bool hv = 4 * tp + (r >> 1) < p.G;
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
-          const float y0 = hv && v0 ? x0[tp] * sv0[b] : 0.0f;
-          const float y1 = hv && v1 ? x1[tp] * sv1[b] : 0.0f;
-          const float y2 = hv && v2 ? x2[tp] * sv2[b] : 0.0f;
-          const float y3 = hv && v3 ? x3[tp] * sv3[b] : 0.0f;
+          const float y0 = v0 ? x0[tp] * sv0[b] : 0.0f;
+          const float y1 = v1 ? x1[tp] * sv1[b] : 0.0f;
+          const float y2 = v2 ? x2[tp] * sv2[b] : 0.0f;
+          const float y3 = v3 ? x3[tp] * sv3[b] : 0.0f;
           const __half2 h01 = __floats2half2_rn(y0, y1), h23 = __floats2half2_rn(y2, y3);
           const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
           const uint32_t lo01 = pack_half2(y0 - f01.x, y1 - f01.y);
@@ -869,24 +871,36 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
         }
       }
     } else {
+      // P' = fp16(p * s_v): one rounding of the fp32 product
+      float sv0[NB], sv1[NB], sv2[NB], sv3[NB];
+      {
+        const uint32_t a = pg + REC + (uint32_t)(T0 * BPT);
+        SDec::template two<0>(a, sv0, sv1);
+        SDec::template two<8 * BPT>(a, sv2, sv3);
+      }
 #pragma unroll
       for (int tp = 0; tp < NTP; ++tp) {
-        const int hp = 8 * tp + r;
-        const int tsel = hp >> 2;
-        float y0 = 0.0f, y1 = 0.0f, y2 = 0.0f, y3 = 0.0f;
+        float y0 = x0[0], y1 = x1[0], y2 = x2[0], y3 = x3[0];
+        if constexpr (NTQ > 1) {
+          const int tsel = (8 * tp + r) >> 2;   // < NTQ
 #pragma unroll
-        for (int tq = 0; tq < NTQ; ++tq) {
-          const bool sel = tq == tsel;
-          y0 = sel ? x0[tq] : y0;
-          y1 = sel ? x1[tq] : y1;
-          y2 = sel ? x2[tq] : y2;
-          y3 = sel ? x3[tq] : y3;
+          for (int tq = 1; tq < NTQ; ++tq) {
+            const bool sel = tq == tsel;
+            y0 = sel ? x0[tq] : y0;
+            y1 = sel ? x1[tq] : y1;
+            y2 = sel ? x2[tq] : y2;
+            y3 = sel ? x3[tq] : y3;
+          }
         }
-        const bool hv = hp < p.G;
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
-          pb[b][tp][0] = pack_half2(hv && v0 ? y0 * sv0[b] : 0.0f, hv && v1 ? y1 * sv1[b] : 0.0f);
-          pb[b][tp][1] = pack_half2(hv && v2 ? y2 * sv2[b] : 0.0f, hv && v3 ? y3 * sv3[b] : 0.0f);
+          if constexpr (FULL) {
+            pb[b][tp][0] = pack_half2(y0 * sv0[b], y1 * sv1[b]);
+            pb[b][tp][1] = pack_half2(y2 * sv2[b], y3 * sv3[b]);
+          } else {
+            pb[b][tp][0] = pack_half2(v0 ? y0 * sv0[b] : 0.0f, v1 ? y1 * sv1[b] : 0.0f);
+            pb[b][tp][1] = pack_half2(v2 ? y2 * sv2[b] : 0.0f, v3 ? y3 * sv3[b] : 0.0f);
+          }
         }
       }
     }
@@ -915,9 +929,9 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
   };
 
   const int P = g.page_size;
+  int stage = 0;          // i mod S
+  uint32_t parity = 0;    // (i / S) mod 2
   for (int64_t i = 0; i < nch; ++i) {
-    const int stage = (int)(i % S);
-    const uint32_t parity = (uint32_t)((i / S) & 1);
     if (!mbar_wait(&full[stage], parity, p.wait_limit)) {
       // a copy never arrived: flag it, wait (bounded) for the copies still in
       // flight so no asynchronous write outlives this CTA, and stop
@@ -970,6 +984,10 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
       const int64_t len = c.b == b_now ? (int64_t)dx.y : seq_len_checked(p, c.b, false);
       fence_proxy_async();
       issue(c, stage, len);
+    }
+    if (++stage == S) {
+      stage = 0;
+      parity ^= 1u;
     }
   }
   if (cur_unit >= 0) flush(cur_unit);

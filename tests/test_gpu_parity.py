@@ -184,6 +184,7 @@ def test_decode_end_to_end(cfg):
     c.oracle_write(k, v, si, ps)
     q = c.queries(1)
     e = rel_err(c.gpu_decode(q), c.oracle_decode(q))
+    print(f"max|err|/rms = {e:.3e}")
     assert c.device_status() == 0
     assert e <= TOL_DECODE
 
