@@ -286,9 +286,9 @@ def workloads():
     return {
         "tiny": Workload("tiny", 1, 4, 4, 128, 64, "f32", 3, 64, False, 1024, (),
                          DataSpec(128, 4, 1000, 0.03, 20.0)),
-        "llama8b": Workload("llama8b", 16, 8, 32, 128, 64, "f16", 3, 64, False, 32768, (),
+        "llama8b": Workload("llama8b", 16, 8, 32, 128, 64, "f16", 3, 128, False, 32768, (),
                             DataSpec(128, 8, 1001, 0.03, 20.0)),
-        "long70b": Workload("long70b", 8, 8, 64, 128, 64, "e4m3", 3, 64, False, 131072, (),
+        "long70b": Workload("long70b", 8, 8, 64, 128, 64, "e4m3", 3, 128, False, 131072, (),
                             DataSpec(128, 8, 1002, 0.03, 20.0, hi_heads=(2, 3, 4, 5),
                                      outlier_frac_hi=0.08)),
         "prefill": Workload("prefill", 1, 8, 8, 128, 32, "f32", 1, 64, False, 131072, (),
