@@ -519,18 +519,16 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
   lane_quats<EQ>(rp, rq, quat_q);
   const bool so4 = (rp.flags & KVQ3_ROT_SO4) != 0;
 
-  // lane-constant code-string offsets: word byte offset and bit shift of this
-  // lane's key chunk (fields j*FQ.. of each block) and value chunk (fields
-  // r*FV.. of each block)
-  uint32_t kwo[NB], kshf[NB], vwo[NB], vshf[NB];
-#pragma unroll
-  for (int b = 0; b < NB; ++b) {
-    const int kb = 3 * (b * BLOCK + j * FQ), vb = 3 * (b * BLOCK + r * FV);
-    kwo[b] = (kb >> 5) * 4;
-    kshf[b] = kb & 31;
-    vwo[b] = (vb >> 5) * 4;
-    vshf[b] = vb & 31;
-  }
+  // lane-constant offsets from a page's K record: this lane's key chunk
+  // (token r, fields j*FQ.. of each block), value chunk (token 2j, fields
+  // r*FV.. of each block) and their scales.  Block b's chunk lies 3*BLOCK/8
+  // bytes after block 0's, at the same bit shift (3*BLOCK is a multiple of 32).
+  const uint32_t kshf = (uint32_t)(3 * j * FQ) & 31u, vshf = (uint32_t)(3 * r * FV) & 31u;
+  const uint32_t k_lane = HDR + (uint32_t)(r * CB) + ((uint32_t)(3 * j * FQ) >> 5) * 4u;
+  const uint32_t v_lane = REC + HDR + (uint32_t)(2 * j * CB) + ((uint32_t)(3 * r * FV) >> 5) * 4u;
+  const uint32_t ks_lane = (uint32_t)(r * BPT), vs_lane = REC + (uint32_t)(2 * j * BPT);
+  static_assert((3 * BLOCK) % 32 == 0, "block chunks must start on a word boundary");
+  constexpr int KBB = 3 * BLOCK / 8;   // bytes per block of a code string
 
   // sign-bit patterns of the key windows, kept in registers (one LOP3 per pair)
   const uint32_t sgn0 = kSignRes0, sgn2 = kSignRes2;
@@ -743,14 +741,13 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
         accq[b][tq][1] = accq[b][tq][3] = KOFS_REG ? kofs[b % (KOFS_REG ? NB : 1)][tq % (KOFS_REG ? NTQ : 1)]
                                                    : kofs_s[b * GPAD + 4 * tq + j];   // lo column
       }
-    const uint32_t kt = pg + HDR + (uint32_t)((t0 + r) * CB);   // token t0 + r
-#pragma unroll
-    for (int b = 0; b < NB; ++b) {
-      const uint32_t a = kt + kwo[b];
-      const uint32_t x0 = lds32<0>(a), x1 = lds32<4>(a);
-      const uint32_t y0 = lds32<8 * CB>(a), y1 = lds32<8 * CB + 4>(a);
-      const uint32_t lo0 = __funnelshift_r(x0, x1, kshf[b]), hi0 = x1 >> kshf[b];   // token r
-      const uint32_t lo8 = __funnelshift_r(y0, y1, kshf[b]), hi8 = y1 >> kshf[b];   // token r + 8
+    const uint32_t kt = pg + (uint32_t)(t0 * CB) + k_lane;   // token t0 + r
+    static_for<NB>([&](auto bc) {
+      constexpr int b = decltype(bc)::value;
+      const uint32_t x0 = lds32<b * KBB>(kt), x1 = lds32<b * KBB + 4>(kt);
+      const uint32_t y0 = lds32<b * KBB + 8 * CB>(kt), y1 = lds32<b * KBB + 8 * CB + 4>(kt);
+      const uint32_t lo0 = __funnelshift_r(x0, x1, kshf), hi0 = x1 >> kshf;   // token r
+      const uint32_t lo8 = __funnelshift_r(y0, y1, kshf), hi8 = y1 >> kshf;   // token r + 8
       static_for<KSB>([&](auto spc) {
         constexpr int sp = decltype(spc)::value;
         uint32_t af[4];
@@ -762,10 +759,10 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
         for (int tq = 0; tq < NTQ; ++tq)
           mma_16816(accq[b][tq], af, qf[tq][b * KSB + sp][0], qf[tq][b * KSB + sp][1]);
       });
-    }
+    });
     float skr[NB], skr8[NB];
     {
-      const uint32_t a = pg + (uint32_t)((t0 + r) * BPT);
+      const uint32_t a = pg + (uint32_t)(t0 * BPT) + ks_lane;
       SDec::template one<0>(a, skr);
       SDec::template one<8 * BPT>(a, skr8);
     }
@@ -849,7 +846,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
     if constexpr (PSPLIT) {
       float sv0[NB], sv1[NB], sv2[NB], sv3[NB];
       {
-        const uint32_t a = pg + REC + (uint32_t)(T0 * BPT);
+        const uint32_t a = pg + (uint32_t)(t0 * BPT) + vs_lane;
         SDec::template two<0>(a, sv0, sv1);
         SDec::template two<8 * BPT>(a, sv2, sv3);
       }
@@ -874,7 +871,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
       // P' = fp16(p * s_v): one rounding of the fp32 product
       float sv0[NB], sv1[NB], sv2[NB], sv3[NB];
       {
-        const uint32_t a = pg + REC + (uint32_t)(T0 * BPT);
+        const uint32_t a = pg + (uint32_t)(t0 * BPT) + vs_lane;
         SDec::template two<0>(a, sv0, sv1);
         SDec::template two<8 * BPT>(a, sv2, sv3);
       }
@@ -905,16 +902,15 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
       }
     }
     // ------------------------------------------------ o1^T += V^T P'^T
-    const uint32_t vt = pg + REC + HDR + (uint32_t)(T0 * CB);
-#pragma unroll
-    for (int b = 0; b < NB; ++b) {
-      const uint32_t a = vt + vwo[b];
-      const uint32_t sh = vshf[b];
+    const uint32_t vt = pg + (uint32_t)(t0 * CB) + v_lane;   // token t0 + 2j
+    static_for<NB>([&](auto bc) {
+      constexpr int b = decltype(bc)::value;
+      constexpr int O = b * KBB;
       // sign bits flipped: fields become c + 4
-      const uint32_t c0v = __funnelshift_r(lds32<0>(a), lds32<4>(a), sh) ^ kSignV;
-      const uint32_t c1v = __funnelshift_r(lds32<CB>(a), lds32<CB + 4>(a), sh) ^ kSignV;
-      const uint32_t c2v = __funnelshift_r(lds32<8 * CB>(a), lds32<8 * CB + 4>(a), sh) ^ kSignV;
-      const uint32_t c3v = __funnelshift_r(lds32<9 * CB>(a), lds32<9 * CB + 4>(a), sh) ^ kSignV;
+      const uint32_t c0v = __funnelshift_r(lds32<O>(vt), lds32<O + 4>(vt), vshf) ^ kSignV;
+      const uint32_t c1v = __funnelshift_r(lds32<O + CB>(vt), lds32<O + CB + 4>(vt), vshf) ^ kSignV;
+      const uint32_t c2v = __funnelshift_r(lds32<O + 8 * CB>(vt), lds32<O + 8 * CB + 4>(vt), vshf) ^ kSignV;
+      const uint32_t c3v = __funnelshift_r(lds32<O + 9 * CB>(vt), lds32<O + 9 * CB + 4>(vt), vshf) ^ kSignV;
       static_for<KSB>([&](auto mpc) {
         constexpr int mp = decltype(mpc)::value;
         uint32_t af[4];
@@ -925,7 +921,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
 #pragma unroll
         for (int tp = 0; tp < NTP; ++tp) mma_16816(acc[b * KSB + mp][tp], af, pb[b][tp][0], pb[b][tp][1]);
       });
-    }
+    });
   };
 
   const int P = g.page_size;
