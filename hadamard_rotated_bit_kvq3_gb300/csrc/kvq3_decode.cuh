@@ -768,8 +768,11 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
     }
     const bool vr = FULL || t0 + r < n_valid, vr8 = FULL || t0 + r + 8 < n_valid;
     // ------------------------------------------------ online softmax
-    float pr[NTQ], pr8[NTQ], alpha[NTQ];
-    bool changed = false;
+    // The running max m of a head moves only when a score exceeds it: one vote
+    // finds that, and only then are the exact max (quad-column reduction) and
+    // the rescale computed; otherwise p = 2^(s - m) <= 1 as before.
+    float sc0[NTQ], sc1[NTQ], pr[NTQ], pr8[NTQ], alpha[NTQ];
+    bool over = false;
 #pragma unroll
     for (int tq = 0; tq < NTQ; ++tq) {
       float s0 = 0.0f, s1 = 0.0f;
@@ -778,21 +781,31 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
         s0 = fmaf(skr[b], accq[b][tq][0] + accq[b][tq][1], s0);
         s1 = fmaf(skr8[b], accq[b][tq][2] + accq[b][tq][3], s1);
       }
-      s0 = vr ? s0 * qinv[tq] : -INFINITY;
-      s1 = vr8 ? s1 * qinv[tq] : -INFINITY;
-      float mx = fmaxf(s0, s1);
-      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
-      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
-      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
-      const float mn = fmaxf(m[tq], mx);   // finite: every step has a valid token
-      alpha[tq] = ex2(m[tq] - mn);
-      pr[tq] = ex2(s0 - mn);
-      pr8[tq] = ex2(s1 - mn);
-      l[tq] = fmaf(l[tq], alpha[tq], pr[tq] + pr8[tq]);
-      m[tq] = mn;
-      changed |= alpha[tq] != 1.0f;
+      sc0[tq] = vr ? s0 * qinv[tq] : -INFINITY;
+      sc1[tq] = vr8 ? s1 * qinv[tq] : -INFINITY;
+      over |= sc0[tq] > m[tq] || sc1[tq] > m[tq];
     }
-    if (__any_sync(kFull, changed)) {
+    const bool changed = __any_sync(kFull, over);
+    if (changed) {
+#pragma unroll
+      for (int tq = 0; tq < NTQ; ++tq) {
+        float mx = fmaxf(sc0[tq], sc1[tq]);
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+        const float mn = fmaxf(m[tq], mx);   // finite: every step has a valid token
+        alpha[tq] = ex2(m[tq] - mn);
+        l[tq] *= alpha[tq];
+        m[tq] = mn;
+      }
+    }
+#pragma unroll
+    for (int tq = 0; tq < NTQ; ++tq) {
+      pr[tq] = ex2(sc0[tq] - m[tq]);
+      pr8[tq] = ex2(sc1[tq] - m[tq]);
+      l[tq] += pr[tq] + pr8[tq];
+    }
+    if (changed) {
       if constexpr (PSPLIT) {
         // this lane's PV columns belong to its own QK head 4tp + j
 #pragma unroll
