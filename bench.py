@@ -323,6 +323,12 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
+def whole_job_rate(units_per_rank: float, world: int, ms: float) -> float:
+    """Units per second of the whole job: every rank processes units_per_rank
+    units per step and ms is the slowest rank's time per step (max over ranks)."""
+    return units_per_rank * world / (ms * 1e-3)
+
+
 def barrier(world: int):
     if world > 1:
         import torch.distributed as dist
@@ -384,7 +390,7 @@ def run_prefill(args, world, rank, dev):
     ms = max_over_ranks(a.elapsed_time(b), world) / args.steps
     assert int(st.status.item()) == 0
     peaks = load_peaks()
-    gbs = st.bytes() * world / (ms * 1e-3) / 1e9
+    gbs = whole_job_rate(st.bytes(), world, ms) / 1e9
     if rank == 0:
         w = st.w
         print(json.dumps({
@@ -398,7 +404,7 @@ def run_prefill(args, world, rank, dev):
             "roofline": {"bound": "hbm", "achieved": gbs / world, "peak": peaks["hbm"], "unit": "GB/s",
                          "frac": gbs / world / peaks["hbm"], "traffic": None,
                          "kernel": "write_chunk_kernel", "peak_source": peaks["src"]},
-            "tokens_per_s": w.seq_len * world / (ms * 1e-3),
+            "tokens_per_s": whole_job_rate(w.seq_len, world, ms),
             "gpu_launches": args.steps, "clocks": clk.summary()}))
 
 
@@ -513,13 +519,12 @@ def main():
     ab = algorithmic_bytes(w, st.lens)
     peaks = load_peaks()
     dec_gbs = ab["decode"] / (dec_ms * 1e-3) / 1e9
-    tokens = w.batch * world
     if rank == 0:
         cpu = None
         if not args.no_cpu_baseline and world == 1:
             cpu = cpu_baseline(w, st.lens)
         line = {
-            "metric": "decode tokens/s (one layer, all heads)", "value": tokens / (ms_step * 1e-3),
+            "metric": "decode tokens/s (one layer, all heads)", "value": whole_job_rate(w.batch, world, ms_step),
             "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f16 mma / f32 accumulate (3-bit packed cache)", "data": "synthetic",
@@ -532,7 +537,7 @@ def main():
                          "frac": dec_gbs / peaks["hbm"], "traffic": recorded_traffic(args.workload),
                          "kernel": "kvq3_decode_attn (decode_split_kernel + decode_combine_kernel)",
                          "peak_source": peaks["src"]},
-            "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "e2e": {"value": whole_job_rate(w.batch, world, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": 3 * args.steps,
             "clocks": clk.summary(),
