@@ -9,14 +9,15 @@
 // Activation Space", 4.3: dequantisation fused into the attention kernel.
 //
 // Design (one GPU, HBM-bound):
-//  * Work = the flattened list of 64-token chunks of every (sequence, kv
-//    head) unit (a chunk is one page when pages hold >= 64 tokens, else
-//    64/P consecutive pages of the unit).  A persistent grid of 4-warp CTAs
-//    splits the list into equal contiguous ranges.
-//  * One thread per CTA streams each chunk's K and V records into a ring of
-//    shared-memory stages with cp.async.bulk (mbarrier completion, L2
-//    evict-first); the four warps share every stage, one 16-token step each,
-//    and release it through a second mbarrier.
+//  * Work = the flattened list of chunks of every (sequence, kv head) unit (a
+//    chunk is one page when pages hold >= kChunk tokens, else kChunk/P
+//    consecutive pages of the unit).  A persistent grid of 4-warp CTAs splits
+//    the list into equal contiguous ranges.
+//  * Each chunk's K and V records stream into a ring of shared-memory stages
+//    with cp.async.bulk (mbarrier completion, L2 evict-first), one warp
+//    issuing a chunk with lane i copying page i; the four warps share every
+//    stage, one 16-token step each, and the last warp to release a stage
+//    refills it with the chunk S places ahead.
 //  * Each warp keeps an online-softmax state per unit; at the end of a unit
 //    the four states merge (max, rescale, sum) into one fp32 partial
 //    (o1[G][d] unnormalised, max, sum) at workspace slot (cta + unit), unique
@@ -24,13 +25,16 @@
 //    the partials of each (sequence, query head) with the log-sum-exp rule
 //    and applies U^T.
 //  * QK^T and PV run on tensor cores (mma.sync m16n8k16, fp16 in, fp32
-//    accumulate).  Codes in -3..3 become exact fp16 values by a mask/xor into
-//    the 0x6400 exponent pattern and one half2 subtraction; the field's bit
-//    offset inside the half leaves a power-of-two factor that is folded into
-//    q1 (keys) or into the output (values).  q1 is split into hi + lo fp16
-//    halves (two columns per head) so the logits keep ~fp32 accuracy; with
-//    fp32 value scales the probabilities are split the same way.  Per-(token,
-//    block) scales multiply the per-block partial dot products (keys) or the
+//    accumulate).  A 3-bit field placed in the mantissa of a half with a
+//    zero exponent is an exact subnormal; with its sign bit flipped it reads
+//    (c + 4) 2^(k-24).  Keys take one LOP3 per pair of codes and the +4
+//    offset enters as a per-block constant seeded into the logit
+//    accumulator; values take a byte permute per three fields, a mask and
+//    one half2 subtraction.  The powers of two are folded into q1 (keys) or
+//    into the output (values).  q1 is split into hi + lo fp16 halves (two
+//    columns per head) so the logits keep ~fp32 accuracy; with fp32 value
+//    scales the probabilities are split the same way.  Per-(token, block)
+//    scales multiply the per-block partial dot products (keys) or the
 //    probabilities (values).
 #pragma once
 
