@@ -83,6 +83,9 @@ kvq3_status kvq3_decode_attn(kvq3_rotation rot, const kvq3_cache_desc* desc,
   prm.seq_lens = cache->seq_lens;
   prm.q = static_cast<const __half*>(q);
   prm.ws = static_cast<float*>(workspace);
+  prm.unit_cta = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) +
+                                            ((size_t)plan.ctas + (size_t)g.batch * g.hkv) * G * (g.d + 2) *
+                                                sizeof(float));
   prm.status = dev_status;
   prm.G = G;
   prm.Hq = num_q_heads;

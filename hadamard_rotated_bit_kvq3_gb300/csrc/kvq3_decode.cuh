@@ -58,6 +58,7 @@ struct DecodeParams {
   const int32_t* seq_lens;
   const __half* q;        // [B][Hq][D]
   float* ws;              // partial slots
+  int32_t* unit_cta;      // [units][2]: first and last CTA holding chunks of each unit
   int32_t* status;
   int32_t G;              // query heads per kv head
   int32_t Hq;
@@ -84,7 +85,9 @@ __device__ __forceinline__ int64_t seq_len_checked(const DecodeParams& p, int b,
 }
 
 __device__ __forceinline__ int64_t seq_chunks(const DecodeParams& p, int b, bool flag) {
-  return (seq_len_checked(p, b, flag) + p.chunk_tokens - 1) / p.chunk_tokens;
+  // lengths are int32, so the rounded-up sum stays below 2^32
+  return (int64_t)(((uint32_t)seq_len_checked(p, b, flag) + (uint32_t)(p.chunk_tokens - 1)) /
+                   (uint32_t)p.chunk_tokens);
 }
 
 __device__ __forceinline__ int64_t warp_sum64(int64_t v) {
@@ -100,17 +103,6 @@ __device__ __forceinline__ int64_t total_chunks(const DecodeParams& p, bool flag
   for (int b0 = 0; b0 < p.g.batch; b0 += 32) {
     const int b = b0 + lane;
     acc += warp_sum64(b < p.g.batch ? seq_chunks(p, b, flag) : 0);
-  }
-  return acc * p.g.hkv;
-}
-
-// Hkv * (chunks of sequences 0..b-1).
-__device__ __forceinline__ int64_t chunks_before(const DecodeParams& p, int b) {
-  const int lane = threadIdx.x & 31;
-  int64_t acc = 0;
-  for (int b0 = 0; b0 < b; b0 += 32) {
-    const int bb = b0 + lane;
-    acc += warp_sum64(bb < b ? seq_chunks(p, bb, false) : 0);
   }
   return acc * p.g.hkv;
 }
@@ -454,9 +446,11 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
 
   const int64_t cta = blockIdx.x;
   const int64_t T = total_chunks(p, cta == 0 && wid == 0);
-  const int64_t W = p.ctas;
+  // W = min(CTAs, chunks): every CTA below W gets a non-empty range, so the
+  // CTAs holding a unit's chunks are consecutive (the combine walks them)
+  const int64_t W = T < p.ctas ? T : p.ctas;
+  if (cta >= W) return;  // uniform over the CTA
   const int64_t c0 = cta * T / W, c1 = (cta + 1) * T / W;
-  if (c0 >= c1) return;  // uniform over the CTA
   const int64_t nch = c1 - c0;
 
   if (threadIdx.x == 0) {
@@ -547,9 +541,15 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
   float m[NTQ], l[NTQ];
   float acc[KS][NTP][4];
   int cur_unit = -1;
+  bool cur_first = false, cur_last = false;
 
-  // merge the four warps' states of a unit into workspace slot (cta + unit)
-  auto flush = [&](int unit) {
+  // merge the four warps' states of a unit into workspace slot (cta + unit);
+  // the CTA holding the unit's first (last) chunk records itself as such
+  auto flush = [&](int unit, bool first, bool last) {
+    if (threadIdx.x == 0) {
+      if (first) p.unit_cta[2 * unit] = (int32_t)cta;
+      if (last) p.unit_cta[2 * unit + 1] = (int32_t)cta;
+    }
     float* slot = p.ws + (size_t)(cta + unit) * p.slot_floats;
     float* mS = slot + p.G * D;
     float* lS = mS + p.G;
@@ -959,10 +959,12 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
     const int unit = (int)dv.x, n_tok = (int)dv.w;
     const uint32_t page_ok = dw.x;
     if (unit != cur_unit) {
-      if (cur_unit >= 0) flush(cur_unit);
+      if (cur_unit >= 0) flush(cur_unit, cur_first, cur_last);
       setup_unit((int)dv.y, (int)dv.z);
       cur_unit = unit;
+      cur_first = dw.y == 0;
     }
+    cur_last = (int)dw.y == (int)lds32<24>(st + desc_off) - 1;   // c == nc - 1
     for (int t = wid * 16; t < n_tok; t += kWarps * 16) {
       int pi = 0, tin = t;                              // page of the chunk, offset in it
       while (tin >= P) {
@@ -1003,7 +1005,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
       parity ^= 1u;
     }
   }
-  if (cur_unit >= 0) flush(cur_unit);
+  if (cur_unit >= 0) flush(cur_unit, cur_first, cur_last);
 }
 
 // ------------------------------------------------------------------ kernel 2
@@ -1020,35 +1022,31 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const __grid_consta
   float4 qt[E / 4];
   lane_quats<E>(rp, rr, qt);
   const bool so4 = (rp.flags & KVQ3_ROT_SO4) != 0;
-  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  const int64_t items = (int64_t)p.g.batch * p.Hq;
-  const int64_t T = total_chunks(p, false);
-  const int64_t W = p.ctas;
-  for (int64_t it = warp; it < items; it += nwarps) {
-    const int b = (int)(it / p.Hq);
-    const int h = (int)(it % p.Hq);
-    const int kvh = h / p.G, gh = h % p.G;
-    const int64_t nc = seq_chunks(p, b, false);
+  const int warp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int nwarps = (int)((gridDim.x * blockDim.x) >> 5);
+  const int items = p.g.batch * p.Hq;
+  for (int it = warp; it < items; it += nwarps) {
+    const int b = it / p.Hq;
+    const int h = it - b * p.Hq;
+    const int kvh = h / p.G, gh = h - kvh * p.G;
     float o[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) o[e] = 0.0f;
-    if (nc > 0) {
-      const int64_t pu = chunks_before(p, b) + (int64_t)kvh * nc;
+    if (seq_len_checked(p, b, false) > 0) {
       const int unit = b * p.g.hkv + kvh;
-      // CTAs whose range meets [pu, pu + nc); CTAs with empty ranges wrote nothing
-      const int64_t wlo = ((pu + 1) * W - 1) / T;
-      const int64_t whi = ((pu + nc) * W - 1) / T;
+      // the consecutive CTAs that hold the unit's chunks (clamped: a CTA that
+      // gave up on a copy may not have recorded itself; the status says so)
+      const int last_cta = p.ctas - 1;
+      const int wlo = min(max(p.unit_cta[2 * unit], 0), last_cta);
+      const int whi = min(max(p.unit_cta[2 * unit + 1], 0), last_cta);
       float M = -INFINITY;
-      for (int64_t w = wlo; w <= whi; ++w) {
-        if (w * T / W == (w + 1) * T / W) continue;
+      for (int w = wlo; w <= whi; ++w) {
         const float* slot = p.ws + (size_t)(w + unit) * p.slot_floats;
         M = fmaxf(M, slot[p.G * D + gh]);
       }
       if (M != -INFINITY) {
         float lsum = 0.0f;
-        for (int64_t w = wlo; w <= whi; ++w) {
-          if (w * T / W == (w + 1) * T / W) continue;
+        for (int w = wlo; w <= whi; ++w) {
           const float* slot = p.ws + (size_t)(w + unit) * p.slot_floats;
           const float c = ex2(slot[p.G * D + gh] - M);
           lsum += c * slot[p.G * D + p.G + gh];
@@ -1107,7 +1105,8 @@ kvq3_status decode_plan_t(const CacheGeom& g, int G, DecodePlan* plan) {
   if (per_sm < 1) return KVQ3_ERR_UNSUPPORTED;
   plan->ctas = sm_count() * per_sm;
   const size_t slots = (size_t)plan->ctas + (size_t)g.batch * g.hkv;
-  plan->ws_bytes = slots * (size_t)G * (D + 2) * sizeof(float);
+  // partial slots, then [units][2] int32 first/last CTA of each unit
+  plan->ws_bytes = slots * (size_t)G * (D + 2) * sizeof(float) + (size_t)g.batch * g.hkv * 2 * sizeof(int32_t);
   return KVQ3_OK;
 }
 
