@@ -49,36 +49,19 @@ __global__ void __launch_bounds__(256) write_kernel(
 
   for (int64_t base = warp * GPW; base < total; base += nwarps * GPW) {
     const int64_t item = base + grp;
-    bool ok = item < total;
+    const bool in_range = item < total;
     int which = 0, head = 0;
-    int64_t tok = 0, rec = 0;
-    int slot = 0;
-    if (ok) {
+    int64_t tok = 0;
+    if (in_range) {   // item = (which, token, head); below 2^31 (n_tok * Hkv is checked on the host)
       which = item >= per_which;
-      const int64_t rem = item - which * per_which;
-      tok = rem / g.hkv;
-      head = (int)(rem - tok * g.hkv);
-      const int s = seq_idx[tok];
-      const int64_t p = pos[tok];
-      int bad = 0;
-      int64_t page = -1;
-      if (s < 0 || s >= g.batch) bad = KVQ3_DEV_BAD_SEQ;
-      else if (p < 0 || p >= cap) bad = KVQ3_DEV_BAD_POS;
-      else {
-        page = page_of(g, page_table, s, p / g.page_size);
-        if (page < 0) bad = KVQ3_DEV_BAD_PAGE;
-      }
-      if (bad) {
-        if (r == 0) set_status(status, bad);
-        ok = false;
-      } else {
-        slot = (int)(p % g.page_size);
-        rec = record_offset(g, page, head, which);
-      }
+      const uint32_t rem = (uint32_t)(item - which * per_which);
+      tok = rem / (uint32_t)g.hkv;
+      head = (int)(rem - (uint32_t)tok * (uint32_t)g.hkv);
     }
-    // load E fp16 elements (one vector per lane group)
+    // the vector's load and quantisation do not wait for the position and
+    // page lookups: only the store does
     float x[E];
-    if (ok) {
+    if (in_range) {
       const __half* src = (which ? vin : kin) + (tok * g.hkv + head) * D + r * E;
       if constexpr (E == 8) {
         const uint4 u = *reinterpret_cast<const uint4*>(src);
@@ -105,6 +88,28 @@ __global__ void __launch_bounds__(256) write_kernel(
     } else {
 #pragma unroll
       for (int e = 0; e < E; ++e) x[e] = 0.0f;
+    }
+    bool ok = in_range;
+    int64_t rec = 0;
+    int slot = 0;
+    if (ok) {
+      const int s = seq_idx[tok];
+      const int64_t p = pos[tok];
+      int bad = 0;
+      int64_t page = -1;
+      if (s < 0 || s >= g.batch) bad = KVQ3_DEV_BAD_SEQ;
+      else if (p < 0 || p >= cap) bad = KVQ3_DEV_BAD_POS;
+      else {   // 0 <= p < max_pages * page_size; p is an int32 position
+        page = page_of(g, page_table, s, (int64_t)((uint32_t)p / (uint32_t)g.page_size));
+        if (page < 0) bad = KVQ3_DEV_BAD_PAGE;
+      }
+      if (bad) {
+        if (r == 0) set_status(status, bad);
+        ok = false;
+      } else {
+        slot = (int)((uint32_t)p % (uint32_t)g.page_size);
+        rec = record_offset(g, page, head, which);
+      }
     }
     rotate_forward<E, L>(x, r, sgn, q, inv_sqrt_d, so4);
 
@@ -272,6 +277,7 @@ kvq3_status kvq3_write(kvq3_rotation rot, const kvq3_cache_desc* desc, const kvq
   if (!rot || rot->d != g.d || n_tok < 0) return KVQ3_ERR_INVALID_ARG;
   if ((s = check_cache(g, cache, false)) != KVQ3_OK) return s;
   if (n_tok == 0) return KVQ3_OK;
+  if (n_tok >= ((int64_t)1 << 31) / (2 * g.hkv)) return KVQ3_ERR_UNSUPPORTED;  // 32-bit item index
   if (!k || !v || !seq_idx || !pos) return KVQ3_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) % 16 != 0)
     return KVQ3_ERR_INVALID_ARG;

@@ -15,12 +15,12 @@
  *         s = (max_j|x_j| + eps)/(2^(b-1)-1) and the code
  *         clip(round(x/s), -(2^(b-1)-1), 2^(b-1)-1) with b = 3); Key formulas
  *         (Attn = softmax(QK^T/sqrt d) V); Implementation notes (write path:
- *         k1 = U(k), v1 = U(v), one scale per block, "round to signed 3-bit
- *         integers, and pack the codes into bytes", "store only packed codes
- *         and scales"; read path: q1 = U(q), unpack and scale keys inside the
- *         dot product, softmax, multiply by reconstructed values, y = U^T y1,
- *         "full FP16 K/V tensors are never materialized"; SO(4) blocks from
- *         normalised quaternions, fixed random rotations for a first version).
+ *         k1 = U(k), v1 = U(v), one scale per block, signed 3-bit codes packed
+ *         into bytes, only codes and scales stored; read path: q1 = U(q),
+ *         keys unpacked and scaled inside the dot product, softmax, multiply
+ *         by reconstructed values, y = U^T y1, with no full-precision K/V ever
+ *         formed; SO(4) blocks from normalised quaternions, fixed random
+ *         rotations for a first version).
  *   [OIQ] "Orthogonal Invariance in Activation Space: Fast Walsh-Hadamard
  *         Transforms for KV Quantization" -- 3.1 (normalised FWHT, self
  *         inverse), 3.2 (random sign flip D applied before the FWHT, generated
@@ -172,9 +172,9 @@ int32_t kvq3_abi_version(void);
 const char *kvq3_status_string(kvq3_status s);
 
 /* Creates the rotation of head dimension d (a power of two, 4 <= d <= 256)
- * from a seed (reading R4; [OIQ] 3.2 "generated once ... fixed parameter";
- * [OMC] Implementation notes "fixed random rotations ... normalized
- * quaternion").  flags: KVQ3_ROT_SIGN | KVQ3_ROT_SO4.  *out receives a handle
+ * from a seed (reading R4; [OIQ] 3.2: the signs are drawn once and kept as a
+ * fixed parameter; [OMC] Implementation notes: fixed random rotations built
+ * from normalised quaternions).  flags: KVQ3_ROT_SIGN | KVQ3_ROT_SO4.  *out receives a handle
  * owned by the caller (free with kvq3_rotation_destroy).  Host only. */
 kvq3_status kvq3_rotation_create(int32_t d, uint64_t seed, uint32_t flags,
                                  kvq3_rotation *out);
@@ -205,16 +205,18 @@ kvq3_status kvq3_cache_sizes(const kvq3_cache_desc *desc, size_t *record_bytes,
 kvq3_status kvq3_rotate(kvq3_rotation rot, const void *x, int32_t x_is_fp16,
                         float *y, int64_t n_vec, int32_t inverse, void *stream);
 
-/* Write path ([OMC] Implementation notes: "On every new token, compute
- * k1 = U(k) and v1 = U(v), partition them into quantization blocks, calculate
- * one scale per block, round to signed 3-bit integers, and pack the codes
- * into bytes.  Store only packed codes and scales."): for every token i and
- * kv head, the K and V vectors are rotated, quantised (R7) and stored in the
- * slot of (seq_idx[i], pos[i]).  Appends one token per sequence (decode) or a
- * prefill chunk (many positions of one or more sequences).
- * k, v: device fp16 [n_tok][Hkv][d]; seq_idx, pos: device int32 [n_tok].
- * Tokens whose slot is invalid are skipped and flagged in *dev_status
- * (nullable).  Two tokens with the same slot race (last writer unspecified). */
+/* Write path ([OMC] Implementation notes: each new token's key and value are
+ * rotated by U, split into quantisation blocks with one scale each, rounded
+ * to signed 3-bit codes and packed; only codes and scales are kept): for
+ * every token i and kv head, the K and V vectors are rotated, quantised (R7)
+ * and stored in the slot of (seq_idx[i], pos[i]).  Appends one token per
+ * sequence (decode) or a prefill chunk (many positions of one or more
+ * sequences).
+ * k, v: device fp16 [n_tok][Hkv][d], 16-byte aligned; seq_idx, pos: device
+ * int32 [n_tok].  2 * n_tok * Hkv must stay below 2^31 (KVQ3_ERR_UNSUPPORTED
+ * otherwise).  Tokens whose slot is invalid are skipped and flagged in
+ * *dev_status (nullable).  Two tokens with the same slot race (last writer
+ * unspecified). */
 kvq3_status kvq3_write(kvq3_rotation rot, const kvq3_cache_desc *desc,
                        const kvq3_cache *cache, const void *k, const void *v,
                        const int32_t *seq_idx, const int32_t *pos, int64_t n_tok,
@@ -238,11 +240,11 @@ kvq3_status kvq3_write_chunk(kvq3_rotation rot, const kvq3_cache_desc *desc,
 kvq3_status kvq3_decode_workspace_size(const kvq3_cache_desc *desc,
                                        int32_t num_q_heads, size_t *bytes);
 
-/* Read path ([OMC] Implementation notes: "At read time compute q1 = U(q),
- * unpack and scale keys inside the attention dot-product kernel, calculate
- * logits from q1 and reconstructed transformed keys, apply softmax, multiply
- * by reconstructed transformed values, and rotate the output back with U.T";
- * [OIQ] 4.3 fused dequantisation): one decode step of all sequences.
+/* Read path ([OMC] Implementation notes: the query is rotated to q1 = U(q);
+ * keys are unpacked and scaled inside the attention dot product, logits come
+ * from q1 and the reconstructed rotated keys, then softmax, then the product
+ * with the reconstructed rotated values, and the output is rotated back with
+ * U^T; [OIQ] 4.3 fused dequantisation): one decode step of all sequences.
  * q: device fp16 [batch][Hq][d]; out: device fp32 [batch][Hq][d];
  * sm_scale <= 0 means 1/sqrt(d); Hq must be a multiple of Hkv with
  * Hq/Hkv <= 16.  The attended length of sequence b is seq_lens[b]

@@ -10,8 +10,8 @@ Sources (page titles with the section they come from):
   [OMC]  "Orthogonally mixed 3-bit KV cache" (synthcore idea 1973):
          Mathematical statement (U = B H_d, SO(4) blocks, the symmetric
          quantiser with eps), Key formulas, Implementation notes (write path,
-         read path, "pack the codes into bytes", "store only packed codes and
-         scales", q1 = U q, y = U^T y1).
+         read path, codes packed into bytes with only codes and scales kept,
+         q1 = U q, y = U^T y1).
   [OIQ]  "Orthogonal Invariance in Activation Space: Fast Walsh-Hadamard
          Transforms for KV Quantization": section 3.1 (normalised H_d,
          self-inverse), 3.2 (random sign flip D before the FWHT, generated once
@@ -297,7 +297,7 @@ def quantize(x: np.ndarray, block: int, eps: float, kind: str):
 def pack_codes(codes: np.ndarray) -> np.ndarray:
     """3-bit two's-complement codes [..., d] -> bytes [..., 3d/8]: element j at
     bits 3j..3j+2 of a little-endian bit stream (bit k of the stream is bit
-    k % 8 of byte k // 8) ([OMC] "pack the codes into bytes")."""
+    k % 8 of byte k // 8) ([OMC] Implementation notes: codes packed into bytes)."""
     d = codes.shape[-1]
     c = codes.astype(np.int64) & 7
     bits = np.stack([(c >> i) & 1 for i in range(3)], axis=-1)      # [..., d, 3]
