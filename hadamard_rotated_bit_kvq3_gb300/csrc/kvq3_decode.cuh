@@ -388,6 +388,10 @@ struct ChunkDesc {
   int32_t len;       // attended length of the sequence
 };
 
+// q1 fragments live in shared memory (one copy per CTA) for the variants
+// where they would take 32+ registers; elsewhere in registers.
+__host__ __device__ constexpr bool decode_qf_smem(int D, int GPAD) { return D == 256 || GPAD == 16; }
+
 template <int D, int GPAD>
 struct DecodeSmem {
   static constexpr int kFullOff = 0;                              // kMaxStages mbarriers
@@ -396,7 +400,9 @@ struct DecodeSmem {
   static constexpr int kQOff = (kMLOff + kWarps * 2 * GPAD * 4 + 15) / 16 * 16;  // [GPAD][D]
   static constexpr int kQInvOff = kQOff + GPAD * D * 4;           // [GPAD]
   static constexpr int kKofsOff = kQInvOff + GPAD * 4;            // [D/32][GPAD] logit seeds
-  static constexpr int kStageOff = ((kKofsOff + (D / 32) * GPAD * 4) + 127) / 128 * 128;
+  static constexpr int kQfOff = (kKofsOff + (D / 32) * GPAD * 4 + 15) / 16 * 16;  // [D/16][GPAD/4][32] uint2
+  static constexpr int kStageOff =
+      ((kQfOff + (decode_qf_smem(D, GPAD) ? (D / 16) * (GPAD / 4) * 256 : 0)) + 127) / 128 * 128;
 };
 
 // Resident CTAs per SM the register budget is sized for: the accumulators
@@ -531,7 +537,15 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
   // sign-bit patterns of the key windows, kept in registers (one LOP3 per pair)
   const uint32_t sgn0 = kSignRes0, sgn2 = kSignRes2;
 
-  uint32_t qf[NTQ][KS][2];
+  // q1 fragments (B operand of QK^T): in registers for d = 128 with up to 8
+  // heads per kv head (they are read by every MMA of the logit chain); in
+  // shared memory, one copy per CTA, where they would take 32+ registers of a
+  // larger variant: fragment (k-step s, n-tile tq) of lane l at
+  // kQfOff + ((s*NTQ + tq)*32 + l)*8
+  constexpr bool QF_SMEM = decode_qf_smem(D, GPAD);
+  uint32_t qf[QF_SMEM ? 1 : NTQ][QF_SMEM ? 1 : KS][2];
+  uint2* qf_s = reinterpret_cast<uint2*>(smem + SM::kQfOff);
+  const uint32_t qf_lane = smem_u32(qf_s) + (uint32_t)lane * 8u;
   float qinv[NTQ];
   // logit accumulator seeds (key offset, see setup_unit): registers when few,
   // else shared memory [block][head]
@@ -683,6 +697,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
 #pragma unroll
       for (int s = 0; s < KS; ++s) {
         const int b = s / KSB, sp = s % KSB;
+        uint32_t q2[2];
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           const int P = 2 * sp + hf;
@@ -693,10 +708,16 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
           const __half hlo = __float2half_rn(vlo), hhi = __float2half_rn(vhi);
           const float olo = part == 0 ? __half2float(hlo) : vlo - __half2float(hlo);
           const float ohi = part == 0 ? __half2float(hhi) : vhi - __half2float(hhi);
-          qf[tq][s][hf] = pack_half2(olo, ohi);
+          q2[hf] = pack_half2(olo, ohi);
           // sum_d 2^k_d q1_d of the fp16 values the MMA sees (this lane's part)
-          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&qf[tq][s][hf]));
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&q2[hf]));
           csum[b] += f.x * (float)(1 << kp_kl(FQ, P)) + f.y * (float)(1 << kp_kh(FQ, P));
+        }
+        if constexpr (QF_SMEM) {
+          if (wid == 0) qf_s[(s * NTQ + tq) * 32 + lane] = make_uint2(q2[0], q2[1]);
+        } else {
+          qf[tq % (QF_SMEM ? 1 : NTQ)][s % (QF_SMEM ? 1 : KS)][0] = q2[0];
+          qf[tq % (QF_SMEM ? 1 : NTQ)][s % (QF_SMEM ? 1 : KS)][1] = q2[1];
         }
       }
       // reduce over the lane's quad (fields) and the hi/lo parts: lanes 8h..8h+7
@@ -759,9 +780,16 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
         af[1] = k_pair<FQ, 2 * sp>(lo8, hi8, sgn0, sgn2);
         af[2] = k_pair<FQ, 2 * sp + 1>(lo0, hi0, sgn0, sgn2);
         af[3] = k_pair<FQ, 2 * sp + 1>(lo8, hi8, sgn0, sgn2);
-#pragma unroll
-        for (int tq = 0; tq < NTQ; ++tq)
-          mma_16816(accq[b][tq], af, qf[tq][b * KSB + sp][0], qf[tq][b * KSB + sp][1]);
+        static_for<NTQ>([&](auto tqc) {
+          constexpr int tq = decltype(tqc)::value;
+          if constexpr (QF_SMEM) {
+            const uint2 qv = lds64<((b * KSB + sp) * NTQ + tq) * 256>(qf_lane);
+            mma_16816(accq[b][tq], af, qv.x, qv.y);
+          } else {
+            constexpr int s1 = QF_SMEM ? 0 : b * KSB + sp, t1 = QF_SMEM ? 0 : tq;
+            mma_16816(accq[b][tq], af, qf[t1][s1][0], qf[t1][s1][1]);
+          }
+        });
       });
     });
     float skr[NB], skr8[NB];
