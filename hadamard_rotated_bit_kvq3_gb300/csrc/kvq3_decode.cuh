@@ -395,7 +395,7 @@ __host__ __device__ constexpr bool decode_qf_smem(int D, int GPAD) { return D ==
 template <int D, int GPAD>
 struct DecodeSmem {
   static constexpr int kFullOff = 0;                              // kMaxStages mbarriers
-  static constexpr int kEmptyOff = kFullOff + 8 * kMaxStages;     // kMaxStages release counters
+  static constexpr int kEmptyOff = kFullOff + 8 * kMaxStages;     // abort flag (+ spare)
   static constexpr int kMLOff = kEmptyOff + 8 * kMaxStages;       // [kWarps][2][GPAD] floats
   static constexpr int kQOff = (kMLOff + kWarps * 2 * GPAD * 4 + 15) / 16 * 16;  // [GPAD][D]
   static constexpr int kQInvOff = kQOff + GPAD * D * 4;           // [GPAD]
@@ -439,7 +439,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
   const int wid = threadIdx.x >> 5;
   const int j = lane & 3, r = lane >> 2;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::kFullOff);
-  uint32_t* released = reinterpret_cast<uint32_t*>(smem + SM::kEmptyOff);
+  volatile uint32_t* abort_s = reinterpret_cast<volatile uint32_t*>(smem + SM::kEmptyOff);  // a copy never arrived
   float* ml_s = reinterpret_cast<float*>(smem + SM::kMLOff);
   float* qs = reinterpret_cast<float*>(smem + SM::kQOff);
   float* qinv_s = reinterpret_cast<float*>(smem + SM::kQInvOff);
@@ -460,10 +460,8 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
   const int64_t nch = c1 - c0;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
-      released[s] = 0;
-    }
+    for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+    *abort_s = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -973,10 +971,14 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
   int stage = 0;          // i mod S
   uint32_t parity = 0;    // (i / S) mod 2
   for (int64_t i = 0; i < nch; ++i) {
-    if (!mbar_wait(&full[stage], parity, p.wait_limit)) {
+    if (!mbar_wait(&full[stage], parity, p.wait_limit) && lane == 0) *abort_s = 1;
+    // the four warps decide together whether to go on (every barrier below is
+    // then reached by all of them)
+    named_barrier(2, 32 * kWarps);
+    if (*abort_s) {
       // a copy never arrived: flag it, wait (bounded) for the copies still in
       // flight so no asynchronous write outlives this CTA, and stop
-      if (lane == 0) set_status(p.status, KVQ3_DEV_TIMEOUT);
+      if (threadIdx.x == 0) set_status(p.status, KVQ3_DEV_TIMEOUT);
       for (int64_t k = i + 1; k < nch && k < i + S; ++k)
         mbar_wait(&full[k % S], (uint32_t)((k / S) & 1), p.wait_limit);
       return;
@@ -1006,18 +1008,11 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
         else step(pg, tin, std::false_type{}, nv);
       }
     }
-    // release the stage; the last warp to do so refills it with chunk i + S
-    __syncwarp();
-    uint32_t last = 0;
-    if (lane == 0) {
-      __threadfence_block();
-      last = atomicAdd(&released[stage], 1u) == kWarps - 1;
-      if (last) {
-        released[stage] = 0;
-        __threadfence_block();
-      }
-    }
-    if (__shfl_sync(kFull, last, 0) && i + S < nch) {
+    // release the stage: the four warps meet here, so none runs more than a
+    // chunk ahead of the others and each sees the ring's full lookahead; warp
+    // i mod 4 then refills the stage with chunk i + S
+    named_barrier(2, 32 * kWarps);
+    if (((int)i & (kWarps - 1)) == wid && i + S < nch) {
       // chunk i + S: S chunks after this one; within the same sequence no
       // global read is needed (the descriptor carries nc and the length)
       const uint2 dx = lds64<24>(st + desc_off);      // nc, len
