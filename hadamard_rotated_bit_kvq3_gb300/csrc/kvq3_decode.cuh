@@ -970,18 +970,38 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
   const int P = g.page_size;
   int stage = 0;          // i mod S
   uint32_t parity = 0;    // (i / S) mod 2
+  int prev = S - 1;       // (i - 1) mod S
   for (int64_t i = 0; i < nch; ++i) {
     if (!mbar_wait(&full[stage], parity, p.wait_limit) && lane == 0) *abort_s = 1;
-    // the four warps decide together whether to go on (every barrier below is
-    // then reached by all of them)
+    // One barrier per chunk: the four warps have finished chunk i - 1 and
+    // waited for chunk i.  They decide together whether to go on (every
+    // barrier below is then reached by all of them), and the stage of chunk
+    // i - 1 is free: warp (i - 1) mod 4 refills it with chunk i - 1 + S.
+    // Keeping the warps within one chunk of each other gives every warp the
+    // ring's lookahead (a fast warp would otherwise wait on a refill that
+    // only the slowest warp can trigger).
     named_barrier(2, 32 * kWarps);
     if (*abort_s) {
       // a copy never arrived: flag it, wait (bounded) for the copies still in
-      // flight so no asynchronous write outlives this CTA, and stop
+      // flight (chunks up to i + S - 2) so no asynchronous write outlives this
+      // CTA, and stop
       if (threadIdx.x == 0) set_status(p.status, KVQ3_DEV_TIMEOUT);
-      for (int64_t k = i + 1; k < nch && k < i + S; ++k)
+      for (int64_t k = i + 1; k < nch && k < i + S - 1; ++k)
         mbar_wait(&full[k % S], (uint32_t)((k / S) & 1), p.wait_limit);
       return;
+    }
+    if (i > 0 && (((int)i - 1) & (kWarps - 1)) == wid && i - 1 + S < nch) {
+      // chunk i - 1 + S; within the same sequence no global read is needed
+      // (the descriptor carries nc and the length)
+      const uint32_t sp = stg_u32 + (uint32_t)prev * p.stage_bytes;
+      const uint4 pv = lds128<0>(sp + desc_off);      // unit, b, kvh, n_tok
+      const uint4 px = lds128<16>(sp + desc_off);     // page_ok, c, nc, len
+      Cursor c{(int)pv.y, (int)pv.z, (int64_t)px.y, (int64_t)px.z};
+      const int b_now = c.b;
+      for (int k = 0; k < S; ++k) cursor_next(p, c);
+      const int64_t len = c.b == b_now ? (int64_t)px.w : seq_len_checked(p, c.b, false);
+      fence_proxy_async();
+      issue(c, prev, len);
     }
     const uint32_t st = stg_u32 + (uint32_t)stage * p.stage_bytes;
     const uint4 dv = lds128<0>(st + desc_off);            // unit, b, kvh, n_tok
@@ -1008,21 +1028,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
         else step(pg, tin, std::false_type{}, nv);
       }
     }
-    // release the stage: the four warps meet here, so none runs more than a
-    // chunk ahead of the others and each sees the ring's full lookahead; warp
-    // i mod 4 then refills the stage with chunk i + S
-    named_barrier(2, 32 * kWarps);
-    if (((int)i & (kWarps - 1)) == wid && i + S < nch) {
-      // chunk i + S: S chunks after this one; within the same sequence no
-      // global read is needed (the descriptor carries nc and the length)
-      const uint2 dx = lds64<24>(st + desc_off);      // nc, len
-      Cursor c{(int)dv.y, (int)dv.z, (int64_t)dw.y, (int64_t)dx.x};
-      const int b_now = c.b;
-      for (int k = 0; k < S; ++k) cursor_next(p, c);
-      const int64_t len = c.b == b_now ? (int64_t)dx.y : seq_len_checked(p, c.b, false);
-      fence_proxy_async();
-      issue(c, stage, len);
-    }
+    prev = stage;
     if (++stage == S) {
       stage = 0;
       parity ^= 1u;
