@@ -188,7 +188,6 @@ __device__ __forceinline__ uint32_t hsub2_bits(uint32_t a, uint32_t b) {
 // at positions congruent to (2 - o) mod 3.
 constexpr uint32_t kSignRes0 = 0x49249249u;   // positions 0, 3, 6, ...
 constexpr uint32_t kSignRes2 = 0x24924924u;   // positions 2, 5, 8, ...
-constexpr uint32_t kSignV = 0x00924924u;      // the 8 sign bits of a 24-bit value chunk
 
 // Key pairs: a lane's FQ consecutive fields (FQ = 16 or 8; field 0 at bit 0 of
 // the 64-bit window lo:hi) -> FQ/2 half2 values.  Pair P cuts the window
@@ -242,18 +241,22 @@ __device__ __forceinline__ uint32_t k_pair(uint32_t lo, uint32_t hi, uint32_t s0
 }
 
 // Value codes: fields f = 0..F-1 (F = 8 or 4) of two tokens' 3F-bit chunks
-// (sign bits already flipped) -> half2 (token0, token1) of field f, equal to
-// c 2^(voff(f) - 24).
+// -> half2 (token0, token1) of field f, equal to c 2^(voff(f) - 24).
 __host__ __device__ constexpr int v_off(int f) {
   return f == 0 ? 0 : f == 1 ? 3 : f == 2 ? 6 : f == 3 ? 1 : f == 4 ? 4 : f == 5 ? 7 : f == 6 ? 2 : 5;
 }
 
+// The byte permute takes bytes g, g+1 of each token's chunk (g = 0, 1, 2 for
+// fields 0-2, 3-5, 6-7); the sign bits of that half sit at the positions of
+// kSignVg[g] (both halves), flipped in the same LOP3 that masks the field.
+constexpr uint32_t kSignVg0 = 0x49244924u, kSignVg1 = 0x92499249u, kSignVg2 = 0x24922492u;
+
 template <int F>
-__device__ __forceinline__ uint32_t v_field(uint32_t c0, uint32_t c1) {
+__device__ __forceinline__ uint32_t v_field(uint32_t c0, uint32_t c1, uint32_t s0, uint32_t s1, uint32_t s2) {
   constexpr uint32_t sel = F < 3 ? 0x5410u : (F < 6 ? 0x6521u : 0x7632u);
   constexpr int o = v_off(F);
   const uint32_t w = __byte_perm(c0, c1, sel);
-  return hsub2_bits(w & (0x00070007u << o), 0x00040004u << o);
+  return hsub2_bits(xor_and<(0x00070007u << o)>(w, F < 3 ? s0 : (F < 6 ? s1 : s2)), 0x00040004u << o);
 }
 
 // Bits [boff, boff + 64) of a code string (two aligned words, funnel shift).
@@ -534,6 +537,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
 
   // sign-bit patterns of the key windows, kept in registers (one LOP3 per pair)
   const uint32_t sgn0 = kSignRes0, sgn2 = kSignRes2;
+  const uint32_t vsg0 = kSignVg0, vsg1 = kSignVg1, vsg2 = kSignVg2;
 
   // q1 fragments (B operand of QK^T): in registers for d = 128 with up to 8
   // heads per kv head (they are read by every MMA of the logit chain); in
@@ -949,18 +953,18 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
     static_for<NB>([&](auto bc) {
       constexpr int b = decltype(bc)::value;
       constexpr int O = b * KBB;
-      // sign bits flipped: fields become c + 4
-      const uint32_t c0v = __funnelshift_r(lds32<O>(vt), lds32<O + 4>(vt), vshf) ^ kSignV;
-      const uint32_t c1v = __funnelshift_r(lds32<O + CB>(vt), lds32<O + CB + 4>(vt), vshf) ^ kSignV;
-      const uint32_t c2v = __funnelshift_r(lds32<O + 8 * CB>(vt), lds32<O + 8 * CB + 4>(vt), vshf) ^ kSignV;
-      const uint32_t c3v = __funnelshift_r(lds32<O + 9 * CB>(vt), lds32<O + 9 * CB + 4>(vt), vshf) ^ kSignV;
+      // this lane's value chunks of tokens T0, T0+1, T0+8, T0+9
+      const uint32_t c0v = __funnelshift_r(lds32<O>(vt), lds32<O + 4>(vt), vshf);
+      const uint32_t c1v = __funnelshift_r(lds32<O + CB>(vt), lds32<O + CB + 4>(vt), vshf);
+      const uint32_t c2v = __funnelshift_r(lds32<O + 8 * CB>(vt), lds32<O + 8 * CB + 4>(vt), vshf);
+      const uint32_t c3v = __funnelshift_r(lds32<O + 9 * CB>(vt), lds32<O + 9 * CB + 4>(vt), vshf);
       static_for<KSB>([&](auto mpc) {
         constexpr int mp = decltype(mpc)::value;
         uint32_t af[4];
-        af[0] = v_field<2 * mp>(c0v, c1v);
-        af[1] = v_field<2 * mp + 1>(c0v, c1v);
-        af[2] = v_field<2 * mp>(c2v, c3v);
-        af[3] = v_field<2 * mp + 1>(c2v, c3v);
+        af[0] = v_field<2 * mp>(c0v, c1v, vsg0, vsg1, vsg2);
+        af[1] = v_field<2 * mp + 1>(c0v, c1v, vsg0, vsg1, vsg2);
+        af[2] = v_field<2 * mp>(c2v, c3v, vsg0, vsg1, vsg2);
+        af[3] = v_field<2 * mp + 1>(c2v, c3v, vsg0, vsg1, vsg2);
 #pragma unroll
         for (int tp = 0; tp < NTP; ++tp) mma_16816(acc[b * KSB + mp][tp], af, pb[b][tp][0], pb[b][tp][1]);
       });
