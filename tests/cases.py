@@ -140,6 +140,99 @@ class Case:
         return dict(checked=checked, boundary_codes=excl_codes, midpoint_blocks=excl_blocks)
 
 
+def flip_bound(case, k, v, si, ps, q, sm_scale=0.0, differs=None):
+    """Upper bound, per (sequence, query head), on how far the decode output
+    may move when the cache holds any of the codes and scales that the write
+    bar allows besides the oracle's own: elements whose |x/s_q| lies within
+    BOUNDARY of a rounding boundary may be one code step off, and blocks whose
+    fp64 scale lies within MIDPOINT of a storage midpoint may hold the
+    neighbouring scale.  Computed from the oracle's data.  `differs`
+    (optional, from Case.written_differences) restricts the bound to the
+    elements and blocks that do differ in a given cache.
+
+    A value change dv at token t shifts the rotated output by w_t dv (w the
+    softmax weights).  A key change dk in coordinate i shifts logit t by
+    delta = sm |q1_i| dk; the output then moves by at most
+    sum_t w_t (e^|delta_t| - 1) (|v_t - o| + max_s |v_s - o|).  Both bound the
+    L2 change of the rotated output, hence every element after U^T."""
+    d, blk, nb = case.d, case.block, case.d // case.block
+    G = case.hq // case.hkv
+    sm = sm_scale if sm_scale > 0 else 1.0 / math.sqrt(d)
+    # relative spacing of neighbouring stored scales (upper bound)
+    ulp_rel = {"f32": 2.0 ** -23, "f16": 2.0 ** -10, "e4m3": 2.0 ** -3}[case.scale]
+    out = np.zeros((case.B, case.hq))
+    for b in range(case.B):
+        sel = np.nonzero(si == b)[0]
+        if sel.size == 0:
+            continue
+        sel = sel[np.argsort(ps[sel])]
+        for g in range(case.hkv):
+            deq, slack = [], []
+            for which, src in enumerate((k, v)):
+                x = src[sel, g].astype(np.float64) @ case.U.T
+                c, sq, s = O.quantize(x, blk, 1e-6, case.scale)
+                r = np.abs(x.reshape(-1, nb, blk) / np.where(sq > 0, sq, 1.0)[..., None])
+                mid = O.scale_midpoint_distance(s, case.scale) < MIDPOINT
+                # a neighbouring scale moves every x/s by up to 3.5 * ulp_rel:
+                # codes that close to a boundary may flip, and every value
+                # c * s_q moves by |c| * ulp_rel * s_q
+                reach = np.where(mid, BOUNDARY + 3.5 * ulp_rel, BOUNDARY)[..., None]
+                near = np.zeros(r.shape, bool)
+                for kk in range(3):
+                    near |= np.abs(r - (kk + 0.5)) < reach
+                if differs is not None:
+                    code_d, blk_d = differs[(b, g, which)]
+                    near &= code_d.reshape(r.shape)
+                    mid &= blk_d
+                step = np.where(near, 1.0 + ulp_rel, 0.0) * sq[..., None]
+                step += np.where(mid[..., None], np.abs(c.reshape(r.shape)) * ulp_rel, 0.0) * sq[..., None]
+                deq.append((c.reshape(-1, nb, blk) * sq[..., None]).reshape(-1, d))
+                slack.append(step.reshape(-1, d))
+            k_hat, v_hat = deq
+            dk, dv = slack
+            for gh in range(G):
+                h = g * G + gh
+                q1 = case.U @ q[b, h].astype(np.float64)
+                z = sm * (k_hat @ q1)
+                w = np.exp(z - z.max())
+                w /= w.sum()
+                o = w @ v_hat
+                bound_v = float(w @ dv.sum(axis=1))
+                delta = sm * (dk @ np.abs(q1))
+                dist = np.linalg.norm(v_hat - o, axis=1)
+                bound_k = float((w * np.expm1(delta)) @ (dist + dist.max()))
+                out[b, h] = bound_v + bound_k
+    return out
+
+
+def written_differences(case, k, v, si, ps):
+    """Where the library's stored codes and scales differ from the oracle's,
+    per (sequence, kv head, K|V), in position order: (code mask [n][d], block
+    mask [n][d/m]).  Every difference must be one the write bar allows
+    (compare_written checks that first)."""
+    case.compare_written(k, v, si, ps)
+    gp = case.pool.cpu().numpy()
+    nb = case.d // case.block
+    out = {}
+    for b in range(case.B):
+        sel = np.nonzero(si == b)[0]
+        if sel.size == 0:
+            continue
+        sel = sel[np.argsort(ps[sel])]
+        page, slot, st = O.locate(case.layout, case.table, si[sel], ps[sel])
+        for g in range(case.hkv):
+            for which, src in ((0, k), (1, v)):
+                x = src[sel, g].astype(np.float64) @ case.U.T
+                c_o, sq_o, _ = O.quantize(x, case.block, 1e-6, case.scale)
+                rec = page * case.layout.page_bytes + (g * 2 + which) * case.layout.record_bytes
+                so = rec + slot * nb * case.layout.sb
+                co = rec + case.page * nb * case.layout.sb + slot * case.layout.code_bytes
+                sg = O.decode_scales(gp[so[:, None] + np.arange(nb * case.layout.sb)[None]], case.scale)
+                cg = O.unpack_codes(gp[co[:, None] + np.arange(case.layout.code_bytes)[None]], case.d)
+                out[(b, g, which)] = (cg != c_o, sg != sq_o)
+    return out
+
+
 def rel_err(got, ref):
     rms = math.sqrt(float(np.mean(ref ** 2)))
     return float(np.abs(got - ref).max()) / rms if rms > 0 else float(np.abs(got).max())

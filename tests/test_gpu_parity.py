@@ -11,7 +11,7 @@ import math
 import numpy as np
 import pytest
 
-from cases import TOL_DECODE, Case, rel_err
+from cases import TOL_DECODE, Case, flip_bound, rel_err, written_differences
 
 pytestmark = pytest.mark.gpu
 
@@ -183,10 +183,20 @@ def test_decode_end_to_end(cfg):
     c.gpu_write(k, v, si, ps)
     c.oracle_write(k, v, si, ps)
     q = c.queries(1)
-    e = rel_err(c.gpu_decode(q), c.oracle_decode(q))
-    print(f"max|err|/rms = {e:.3e}")
+    got, ref = c.gpu_decode(q), c.oracle_decode(q)
     assert c.device_status() == 0
-    assert e <= TOL_DECODE
+    # The GPU write may legitimately hold another code at an element within
+    # BOUNDARY of a rounding boundary (or another scale at a midpoint): the
+    # write bar allows it.  Each (sequence, head) therefore gets the decode
+    # bar plus the oracle-side bound of what the elements that do differ
+    # (all checked against the write bar first) can move.
+    rms = math.sqrt(float(np.mean(ref ** 2)))
+    slack = flip_bound(c, k, v, si, ps, q, differs=written_differences(c, k, v, si, ps))
+    err = np.abs(got - ref).max(axis=-1)
+    e = rel_err(got, ref)
+    print(f"max|err|/rms = {e:.3e}; heads with boundary slack: {int((slack > 0).sum())}; "
+          f"worst (err - slack)/rms = {float((err - slack).max()) / rms:.3e}")
+    assert np.all(err <= TOL_DECODE * rms + slack)
 
 
 def test_decode_custom_scale_and_empty_sequences():
