@@ -498,6 +498,32 @@ def decode(pool: np.ndarray, layout: Layout, U: np.ndarray, q: np.ndarray,
     return out
 
 
+def prefill(pool: np.ndarray, layout: Layout, U: np.ndarray, q: np.ndarray, seq: int, pos0: int,
+            page_table=None, sm_scale: float = 0.0) -> np.ndarray:
+    """Chunked-prefill attention over the packed cache: query token i of
+    q [n][Hq][d] sits at position pos0 + i of sequence ``seq`` and attends
+    causally to positions [0, pos0 + i] -- exactly one decode step of the
+    sequence truncated after its own position (the reading taken for the
+    pages' prefill-phase attention: [OMC] read path, Key formulas with a
+    causal mask).  Query head h reads kv head h // (Hq/Hkv).  Returns fp64
+    [n][Hq][d]."""
+    n, Hq, d = q.shape
+    G = Hq // layout.num_kv_heads
+    if sm_scale <= 0:
+        sm_scale = 1.0 / math.sqrt(d)
+    out = np.zeros((n, Hq, d))
+    L = pos0 + n
+    for g in range(layout.num_kv_heads):
+        kh = read_rotated(pool, layout, seq, g, 0, 0, L, page_table)[0]
+        vh = read_rotated(pool, layout, seq, g, 1, 0, L, page_table)[0]
+        for i in range(n):
+            m = pos0 + i + 1
+            for gh in range(G):
+                h = g * G + gh
+                out[i, h] = attention_rotated(U, q[i, h], kh[:m], vh[:m], sm_scale)
+    return out
+
+
 def attention_plain(q: np.ndarray, k: np.ndarray, v: np.ndarray, sm_scale: float) -> np.ndarray:
     """softmax(k q * sm_scale) v for one query head in fp64 ([OMC] Key
     formulas, Attn(Q, K, V)); the reference that rotated attention must equal

@@ -185,3 +185,48 @@ def test_rotation_reduces_error_on_outlier_data(oracle):
         bmax[name] = np.abs(y).reshape(-1, 2, 64).max(-1).mean()
     assert errs["rotated"] < 0.85 * errs["none"] and errs["hadamard"] < 0.85 * errs["none"]
     assert bmax["hadamard"] < bmax["none"] / 2 and bmax["rotated"] < bmax["none"] / 2
+
+
+# ---------------------------------------------------------------- prefill pins
+def test_prefill_first_position_attends_to_itself(oracle):
+    # query at position 0 sees one key: weight 1, so o = U^T v_hat_0
+    U, L, pool, table = _setup(oracle, paged=True)
+    rng = np.random.default_rng(21)
+    _fill(oracle, L, pool, U, table, [30, 50], rng)
+    q = rng.standard_normal((5, 4, 128)).astype(np.float16)
+    out = oracle.prefill(pool, L, U, q, 1, 0, table)
+    for h in range(4):
+        vh = oracle.read_rotated(pool, L, 1, h // 2, 1, 0, 1, table)[0][0]
+        assert np.abs(out[0, h] - U.T @ vh).max() < 1e-12
+
+
+def test_prefill_zero_queries_average_their_prefix(oracle):
+    # q = 0: uniform weights over positions [0, pos0 + i] (the causal prefix)
+    U, L, pool, _ = _setup(oracle)
+    rng = np.random.default_rng(22)
+    _fill(oracle, L, pool, U, None, [40, 64], rng)
+    pos0, n = 17, 23
+    q = np.zeros((n, 4, 128), np.float16)
+    out = oracle.prefill(pool, L, U, q, 0, pos0)
+    for i in (0, 5, n - 1):
+        for h in (0, 3):
+            vh = oracle.read_rotated(pool, L, 0, h // 2, 1, 0, pos0 + i + 1)[0]
+            assert np.abs(out[i, h] - U.T @ vh.mean(0)).max() < 1e-12
+
+
+def test_prefill_is_causal(oracle):
+    # rewriting the key and value at position p changes the outputs of the
+    # queries at positions >= p and of none before it
+    U, L, pool, _ = _setup(oracle, B=1, maxp=4)
+    rng = np.random.default_rng(23)
+    _fill(oracle, L, pool, U, None, [60], rng)
+    pos0, n, p = 10, 40, 31
+    q = rng.standard_normal((n, 4, 128)).astype(np.float16)
+    before = oracle.prefill(pool, L, U, q, 0, pos0)
+    k = (rng.standard_normal((1, 2, 128)) * 4).astype(np.float16)
+    v = (rng.standard_normal((1, 2, 128)) * 4).astype(np.float16)
+    oracle.write(pool, L, U, k, v, np.array([0]), np.array([p]))
+    after = oracle.prefill(pool, L, U, q, 0, pos0)
+    moved = np.abs(after - before).max(axis=(1, 2))
+    assert np.all(moved[:p - pos0] == 0.0)
+    assert np.all(moved[p - pos0:] > 1e-6)
