@@ -16,7 +16,8 @@ __all__ = [
     "lib", "kvq3_abi_version", "kvq3_status_string", "kvq3_rotation_create",
     "kvq3_rotation_create_from_params", "kvq3_rotation_destroy", "kvq3_rotation_export",
     "kvq3_cache_sizes", "kvq3_rotate", "kvq3_write", "kvq3_write_chunk", "kvq3_decode_workspace_size",
-    "kvq3_decode_attn", "kvq3_decode_attn_noalloc", "kvq3_dequant_debug", "Rotation",
+    "kvq3_decode_attn", "kvq3_decode_attn_noalloc", "kvq3_prefill_workspace_size", "kvq3_prefill_attn",
+    "kvq3_dequant_debug", "Rotation",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -69,6 +70,8 @@ _SIGS = {
     "kvq3_decode_workspace_size": (ctypes.c_int, [_D, _i32, ctypes.POINTER(_sz)]),
     "kvq3_decode_attn": (ctypes.c_int, [_p, _D, _C, _p, _i32, _f32, _p, _p, _sz, _p, _p]),
     "kvq3_decode_attn_noalloc": (ctypes.c_int, [_p, _D, _C, _p, _i32, _f32, _p, _p, _p]),
+    "kvq3_prefill_workspace_size": (ctypes.c_int, [_D, _i32, _i64, ctypes.POINTER(_sz)]),
+    "kvq3_prefill_attn": (ctypes.c_int, [_p, _D, _C, _i32, _i64, _i64, _p, _i32, _f32, _p, _p, _sz, _p, _p]),
     "kvq3_dequant_debug": (ctypes.c_int, [_p, _D, _C, _i32, _i32, _i32, _i64, _i64, _p, _p, _p, _p]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -200,6 +203,24 @@ def kvq3_decode_attn_noalloc(h, desc: CacheDesc, cache: Cache, q, out, sm_scale:
     _check(lib.kvq3_decode_attn_noalloc(h, ctypes.byref(desc), ctypes.byref(cache), _ptr(q),
                                         int(q.shape[1]), float(sm_scale), _ptr(out), _ptr(dev_status),
                                         _stream(stream)), "kvq3_decode_attn_noalloc")
+
+
+def kvq3_prefill_workspace_size(desc: CacheDesc, num_q_heads: int, n_q: int) -> int:
+    n = _sz()
+    _check(lib.kvq3_prefill_workspace_size(ctypes.byref(desc), num_q_heads, n_q, ctypes.byref(n)),
+           "kvq3_prefill_workspace_size")
+    return n.value
+
+
+def kvq3_prefill_attn(h, desc: CacheDesc, cache: Cache, seq: int, pos0: int, q, out, workspace,
+                      sm_scale: float = 0.0, dev_status=None, stream=None) -> None:
+    """q: fp16 [n_q][Hq][d] at positions pos0.. of sequence seq; out: fp32 [n_q][Hq][d];
+    workspace: uint8 CUDA tensor (kvq3_prefill_workspace_size bytes)."""
+    _check(lib.kvq3_prefill_attn(h, ctypes.byref(desc), ctypes.byref(cache), seq, pos0,
+                                 int(q.shape[0]), _ptr(q), int(q.shape[1]), float(sm_scale),
+                                 _ptr(out), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _ptr(dev_status),
+                                 _stream(stream)), "kvq3_prefill_attn")
 
 
 def kvq3_dequant_debug(h, desc: CacheDesc, cache: Cache, seq: int, kv_head: int, which: int,

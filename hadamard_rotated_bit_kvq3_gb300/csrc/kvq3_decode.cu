@@ -36,15 +36,123 @@ kvq3_status run_for(const CacheGeom& g, const DecodePlan& plan, const DecodePara
   return KVQ3_ERR_UNSUPPORTED;
 }
 
+kvq3_status prefill_plan_for(const CacheGeom& g, int G, DecodePlan* plan) {
+  switch (g.d) {
+    case 64: KVQ3_BY_SCALE(64, prefill_plan, g, G, plan)
+    case 128: KVQ3_BY_SCALE(128, prefill_plan, g, G, plan)
+    case 256: KVQ3_BY_SCALE(256, prefill_plan, g, G, plan)
+  }
+  return KVQ3_ERR_UNSUPPORTED;
+}
+
+kvq3_status prefill_run_for(const CacheGeom& g, const DecodePlan& plan, const DecodeParams& prm,
+                            const RotParams& rp, float* out, cudaStream_t st) {
+  switch (g.d) {
+    case 64: KVQ3_BY_SCALE(64, prefill_run, plan, prm, rp, out, st)
+    case 128: KVQ3_BY_SCALE(128, prefill_run, plan, prm, rp, out, st)
+    case 256: KVQ3_BY_SCALE(256, prefill_run, plan, prm, rp, out, st)
+  }
+  return KVQ3_ERR_UNSUPPORTED;
+}
+
 kvq3_status check_heads(const CacheGeom& g, int32_t hq) {
   if (hq < 1 || hq % g.hkv != 0) return KVQ3_ERR_INVALID_ARG;
   if (hq / g.hkv > 16) return KVQ3_ERR_UNSUPPORTED;
   return KVQ3_OK;
 }
 
+// Prefill geometry: the G query heads of a kv head form hb blocks of hpb
+// <= 8 heads; n_q query tokens form ceil(n_q / qt) blocks of qt = 8 / hpb
+// tokens; a tile (token block, head block) is a unit of gcols = qt * hpb
+// logit columns per kv head.  *vg is the cache geometry with the tiles as
+// its batch.
+kvq3_status prefill_geom(const kvq3_cache_desc* desc, int32_t hq, int64_t n_q, CacheGeom* vg,
+                         int* qt, int* gcols, int* hb = nullptr, int* hpb = nullptr) {
+  kvq3_status s = make_geom(desc, vg);
+  if (s != KVQ3_OK) return s;
+  if ((s = check_heads(*vg, hq)) != KVQ3_OK) return s;
+  if (n_q < 0 || n_q >= ((int64_t)1 << 31)) return KVQ3_ERR_INVALID_ARG;
+  const int G = hq / vg->hkv;
+  const int nhb = (G + 7) / 8, per = (G + nhb - 1) / nhb;
+  *qt = 8 / per;
+  *gcols = *qt * per;
+  if (hb) *hb = nhb;
+  if (hpb) *hpb = per;
+  const int64_t tiles = (n_q + *qt - 1) / *qt * nhb;
+  if (tiles * vg->hkv >= ((int64_t)1 << 31)) return KVQ3_ERR_UNSUPPORTED;
+  vg->batch = (int32_t)(tiles > 0 ? tiles : 1);
+  return KVQ3_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+kvq3_status kvq3_prefill_workspace_size(const kvq3_cache_desc* desc, int32_t num_q_heads,
+                                        int64_t n_q, size_t* bytes) {
+  CacheGeom vg;
+  int qt = 0, gcols = 0;
+  kvq3_status s = prefill_geom(desc, num_q_heads, n_q, &vg, &qt, &gcols);
+  if (s != KVQ3_OK) return s;
+  if (!bytes) return KVQ3_ERR_INVALID_ARG;
+  DecodePlan plan;
+  if ((s = prefill_plan_for(vg, gcols, &plan)) != KVQ3_OK) return s;
+  *bytes = plan.ws_bytes;
+  return KVQ3_OK;
+}
+
+kvq3_status kvq3_prefill_attn(kvq3_rotation rot, const kvq3_cache_desc* desc,
+                              const kvq3_cache* cache, int32_t seq, int64_t pos0, int64_t n_q,
+                              const void* q, int32_t num_q_heads, float sm_scale, float* out,
+                              void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  CacheGeom vg;
+  int qt = 0, gcols = 0, hb = 0, hpb = 0;
+  kvq3_status s = prefill_geom(desc, num_q_heads, n_q, &vg, &qt, &gcols, &hb, &hpb);
+  if (s != KVQ3_OK) return s;
+  if (!rot || rot->d != vg.d || !cache) return KVQ3_ERR_INVALID_ARG;
+  if (seq < 0 || seq >= desc->batch || pos0 < 0 ||
+      pos0 + n_q > (int64_t)vg.max_pages * vg.page_size || pos0 + n_q >= ((int64_t)1 << 31))
+    return KVQ3_ERR_INVALID_ARG;
+  if (n_q == 0) return KVQ3_OK;
+  if (!q || !out) return KVQ3_ERR_INVALID_ARG;
+  {
+    CacheGeom g;   // the real geometry for the cache checks (lengths unused)
+    make_geom(desc, &g);
+    if ((s = check_cache(g, cache, false)) != KVQ3_OK) return s;
+  }
+  if (!(sm_scale <= 0.0f || isfinite(sm_scale))) return KVQ3_ERR_INVALID_ARG;
+  DecodePlan plan;
+  if ((s = prefill_plan_for(vg, gcols, &plan)) != KVQ3_OK) return s;
+  if (!workspace || ws_bytes < plan.ws_bytes || reinterpret_cast<uintptr_t>(workspace) % 256)
+    return KVQ3_ERR_WORKSPACE;
+  DecodeParams prm;
+  memset(&prm, 0, sizeof(prm));
+  prm.g = vg;
+  prm.pool = static_cast<const uint8_t*>(cache->pool);
+  prm.page_table = cache->page_table;
+  prm.seq_lens = nullptr;
+  prm.q = static_cast<const __half*>(q);
+  prm.ws = static_cast<float*>(workspace);
+  prm.unit_cta = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) +
+                                            ((size_t)plan.ctas + (size_t)vg.batch * vg.hkv) * gcols *
+                                                (vg.d + 2) * sizeof(float));
+  prm.status = dev_status;
+  prm.G = gcols;
+  prm.Hq = num_q_heads;
+  const double sc = sm_scale > 0.0f ? (double)sm_scale : 1.0 / sqrt((double)vg.d);
+  prm.qk_scale = (float)(sc * 1.4426950408889634);  // log2(e): softmax in base 2
+  prm.inv_sqrt_d = inv_sqrt(vg.d);
+  prm.slot_floats = (uint32_t)(gcols * (vg.d + 2));
+  prm.wait_limit = 1u << 22;
+  prm.pf_n = (int32_t)n_q;
+  prm.pf_qt = qt;
+  prm.pf_hb = hb;
+  prm.pf_hpb = hpb;
+  prm.pf_gkv = num_q_heads / vg.hkv;
+  prm.pf_seq = seq;
+  prm.pf_pos0 = pos0;
+  return prefill_run_for(vg, plan, prm, rot->params, out, static_cast<cudaStream_t>(stream));
+}
 
 kvq3_status kvq3_decode_workspace_size(const kvq3_cache_desc* desc, int32_t num_q_heads,
                                        size_t* bytes) {

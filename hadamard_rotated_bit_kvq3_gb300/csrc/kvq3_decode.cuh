@@ -71,10 +71,27 @@ struct DecodeParams {
   int32_t ctas;
   uint32_t slot_floats;   // floats per partial slot: G*(D+2)
   uint32_t wait_limit;    // bound on mbarrier polls
+  // Chunked prefill (pf_n > 0): the "sequences" are tiles of sequence
+  // pf_seq: tile b holds query tokens tb*pf_qt .. (tb = b / pf_hb) and the
+  // head block hb = b % pf_hb of pf_hpb query heads of each kv head; column
+  // c of a unit is query token tb*pf_qt + c / pf_hpb and query head
+  // hb*pf_hpb + c % pf_hpb of the kv head (when < pf_gkv).  Query token i sits
+  // at position pf_pos0 + i and attends to positions [0, pf_pos0 + i].
+  int32_t pf_n;           // query tokens (0: decode)
+  int32_t pf_qt;          // query tokens per tile
+  int32_t pf_hb;          // head blocks per kv head
+  int32_t pf_hpb;         // query heads per head block
+  int32_t pf_gkv;         // query heads per kv head
+  int32_t pf_seq;         // the sequence
+  int64_t pf_pos0;        // position of query token 0
 };
 
 // ------------------------------------------------------------------ helpers
 __device__ __forceinline__ int64_t seq_len_checked(const DecodeParams& p, int b, bool flag) {
+  if (p.pf_n > 0) {   // query tile b attends up to its last token (checked on the host)
+    const int64_t last = min((int64_t)(b / p.pf_hb + 1) * p.pf_qt, (int64_t)p.pf_n);
+    return p.pf_pos0 + last;
+  }
   const int64_t len = p.seq_lens[b];
   const int64_t cap = (int64_t)p.g.max_pages * p.g.page_size;
   if (len < 0 || len > cap) {
@@ -419,7 +436,7 @@ __host__ __device__ constexpr int decode_min_blocks(int D, int GPAD) {
 // halves (PV n-tile = 4 heads x (hi, lo), like QK) -- needed when the value
 // scales are fp32, since p = 1 times an fp32 scale is not an fp16 value;
 // otherwise one fp16 value per head (PV n-tile = 8 heads).
-template <int D, int BLOCK, int GPAD, int SCALE, bool PSPLIT>
+template <int D, int BLOCK, int GPAD, int SCALE, bool PSPLIT, bool PF = false>
 __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
     decode_split_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ RotParams rp) {
   constexpr int NB = D / BLOCK;
@@ -483,9 +500,9 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
     const int npg = n_tok == p.chunk_tokens ? ppc : (n_tok + g.page_size - 1) / g.page_size;
     const int lp = (int)c.c * ppc + lane;
     int64_t pg = -1;
+    const int64_t row = p.pf_n > 0 ? p.pf_seq : c.b;   // prefill tiles all read one sequence
     if (lane < npg)
-      pg = p.page_table ? (int64_t)p.page_table[(int64_t)c.b * g.max_pages + lp]
-                        : (int64_t)c.b * g.max_pages + lp;
+      pg = p.page_table ? (int64_t)p.page_table[row * g.max_pages + lp] : row * g.max_pages + lp;
     const bool ok = pg >= 0 && pg < g.num_pages;
     const uint32_t okm = __ballot_sync(kFull, ok);
     if (lane == 0) {
@@ -549,6 +566,8 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
   uint2* qf_s = reinterpret_cast<uint2*>(smem + SM::kQfOff);
   const uint32_t qf_lane = smem_u32(qf_s) + (uint32_t)lane * 8u;
   float qinv[NTQ];
+  int64_t lim[PF ? NTQ : 1];   // prefill: causal limit of each logit column
+  int64_t step_tok = 0;        // prefill: position of the current step's token t0
   // logit accumulator seeds (key offset, see setup_unit): registers when few,
   // else shared memory [block][head]
   constexpr bool KOFS_REG = NB * NTQ <= 4;
@@ -662,11 +681,30 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
   // rotate the unit's G query heads once per CTA, then build each warp's
   // B fragments: qs[g][dim] = (U q)[dim] * sm_scale*log2e * 2^e_g
   auto setup_unit = [&](int b, int kvh) {
+    if constexpr (PF) {
+      // causal limit of this lane's logit columns 4tq + j: position of its
+      // query token (columns past the last token keep no limit: their q is 0)
+#pragma unroll
+      for (int tq = 0; tq < NTQ; ++tq) {
+        const int col = 4 * tq + j;
+        const int tok = (b / p.pf_hb) * p.pf_qt + col / p.pf_hpb;
+        lim[tq] = (col < p.G && tok < p.pf_n) ? p.pf_pos0 + tok : INT64_MAX;
+      }
+    }
     for (int g0 = wid * GPWQ; g0 < GPAD; g0 += kWarps * GPWQ) {
       const int gg = g0 + gq;
-      const bool valid = gg < p.G;
+      bool valid = gg < p.G;
+      int64_t qrow;   // row of q [..][Hq][D]
+      if constexpr (PF) {
+        const int tok = (b / p.pf_hb) * p.pf_qt + gg / p.pf_hpb;
+        const int hd = (b % p.pf_hb) * p.pf_hpb + gg % p.pf_hpb;   // head within the kv group
+        valid = valid && tok < p.pf_n && hd < p.pf_gkv;
+        qrow = (int64_t)tok * p.Hq + (int64_t)kvh * p.pf_gkv + hd;
+      } else {
+        qrow = (int64_t)b * p.Hq + (int64_t)kvh * p.G + gg;
+      }
       float x[EQ];
-      const __half* src = p.q + ((int64_t)b * p.Hq + (int64_t)kvh * p.G + gg) * D + rq * EQ;
+      const __half* src = p.q + (valid ? qrow : 0) * D + rq * EQ;
 #pragma unroll
       for (int e = 0; e < EQ; ++e) x[e] = valid ? __half2float(src[e]) : 0.0f;
       rotate_forward<EQ, LQ>(x, rq, sgn_q, quat_q, p.inv_sqrt_d, so4);
@@ -817,6 +855,11 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
       }
       sc0[tq] = vr ? s0 * qinv[tq] : -INFINITY;
       sc1[tq] = vr8 ? s1 * qinv[tq] : -INFINITY;
+      if constexpr (PF) {   // causal mask: rows are tokens t0 + r and t0 + r + 8
+        const int64_t t = step_tok + r;
+        if (t > lim[tq % (PF ? NTQ : 1)]) sc0[tq] = -INFINITY;
+        if (t + 8 > lim[tq % (PF ? NTQ : 1)]) sc1[tq] = -INFINITY;
+      }
       over |= sc0[tq] > m[tq] || sc1[tq] > m[tq];
     }
     const bool changed = __any_sync(kFull, over);
@@ -827,16 +870,18 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
         mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
         mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
         mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
-        const float mn = fmaxf(m[tq], mx);   // finite: every step has a valid token
-        alpha[tq] = ex2(m[tq] - mn);
+        const float mn = fmaxf(m[tq], mx);   // decode: finite, every step has a valid token
+        // prefill: a column may have seen no token yet (all masked): keep 1
+        alpha[tq] = (PF && mn == -INFINITY) ? 1.0f : ex2(m[tq] - mn);
         l[tq] *= alpha[tq];
         m[tq] = mn;
       }
     }
 #pragma unroll
     for (int tq = 0; tq < NTQ; ++tq) {
-      pr[tq] = ex2(sc0[tq] - m[tq]);
-      pr8[tq] = ex2(sc1[tq] - m[tq]);
+      const float mref = (PF && m[tq] == -INFINITY) ? 0.0f : m[tq];   // all masked: p = 0
+      pr[tq] = ex2(sc0[tq] - mref);
+      pr8[tq] = ex2(sc1[tq] - mref);
       l[tq] += pr[tq] + pr8[tq];
     }
     if (changed) {
@@ -1028,6 +1073,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
       if ((page_ok >> pi) & 1u) {
         const uint32_t pg = st + (uint32_t)pi * 2 * REC;
         const int nv = min(P, n_tok - pi * P);          // valid tokens of this page
+        if constexpr (PF) step_tok = (int64_t)dw.y * p.chunk_tokens + t;
         if (nv - tin >= 16) step(pg, tin, std::true_type{}, nv);
         else step(pg, tin, std::false_type{}, nv);
       }
@@ -1057,11 +1103,24 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const __grid_consta
   const bool so4 = (rp.flags & KVQ3_ROT_SO4) != 0;
   const int warp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int nwarps = (int)((gridDim.x * blockDim.x) >> 5);
-  const int items = p.g.batch * p.Hq;
+  // output row it = (sequence or query token) * Hq + query head
+  const int items = (p.pf_n > 0 ? p.pf_n : p.g.batch) * p.Hq;
   for (int it = warp; it < items; it += nwarps) {
-    const int b = it / p.Hq;
-    const int h = it - b * p.Hq;
-    const int kvh = h / p.G, gh = h - kvh * p.G;
+    int b, h, kvh, gh;   // unit sequence (prefill: query tile), head, kv head, column
+    if (p.pf_n > 0) {
+      const int i = it / p.Hq;
+      h = it - i * p.Hq;
+      kvh = h / p.pf_gkv;
+      const int hd = h - kvh * p.pf_gkv, hb = hd / p.pf_hpb;
+      const int tb = i / p.pf_qt;
+      b = tb * p.pf_hb + hb;
+      gh = (i - tb * p.pf_qt) * p.pf_hpb + (hd - hb * p.pf_hpb);
+    } else {
+      b = it / p.Hq;
+      h = it - b * p.Hq;
+      kvh = h / p.G;
+      gh = h - kvh * p.G;
+    }
     float o[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) o[e] = 0.0f;
@@ -1094,7 +1153,7 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const __grid_consta
     rotate_inverse<E, L>(o, rr, sgn, qt, p.inv_sqrt_d, so4);
     if (grp == 0) {
 #pragma unroll
-      for (int e = 0; e < E; ++e) out[((int64_t)b * p.Hq + h) * D + rr * E + e] = o[e];
+      for (int e = 0; e < E; ++e) out[(int64_t)it * D + rr * E + e] = o[e];
     }
   }
 }
@@ -1109,10 +1168,10 @@ struct DecodePlan {
   size_t ws_bytes;
 };
 
-template <int D, int BLOCK, int GPAD, int SCALE, bool PSPLIT>
+template <int D, int BLOCK, int GPAD, int SCALE, bool PSPLIT, bool PF = false>
 kvq3_status decode_plan_t(const CacheGeom& g, int G, DecodePlan* plan) {
   using SM = DecodeSmem<D, GPAD>;
-  const void* k = reinterpret_cast<const void*>(&decode_split_kernel<D, BLOCK, GPAD, SCALE, PSPLIT>);
+  const void* k = reinterpret_cast<const void*>(&decode_split_kernel<D, BLOCK, GPAD, SCALE, PSPLIT, PF>);
   plan->gpad = GPAD;
   plan->pages_per_chunk = (kChunk + g.page_size - 1) / g.page_size;
   plan->chunk_tokens = plan->pages_per_chunk * g.page_size;
@@ -1143,7 +1202,7 @@ kvq3_status decode_plan_t(const CacheGeom& g, int G, DecodePlan* plan) {
   return KVQ3_OK;
 }
 
-template <int D, int BLOCK, int GPAD, int SCALE, bool PSPLIT>
+template <int D, int BLOCK, int GPAD, int SCALE, bool PSPLIT, bool PF = false>
 kvq3_status decode_run_t(const DecodePlan& plan, DecodeParams prm, const RotParams& rp, float* out,
                          cudaStream_t st) {
   prm.stages = plan.stages;
@@ -1151,9 +1210,9 @@ kvq3_status decode_run_t(const DecodePlan& plan, DecodeParams prm, const RotPara
   prm.chunk_tokens = plan.chunk_tokens;
   prm.pages_per_chunk = plan.pages_per_chunk;
   prm.ctas = plan.ctas;
-  decode_split_kernel<D, BLOCK, GPAD, SCALE, PSPLIT><<<plan.ctas, 32 * kWarps, plan.smem, st>>>(prm, rp);
+  decode_split_kernel<D, BLOCK, GPAD, SCALE, PSPLIT, PF><<<plan.ctas, 32 * kWarps, plan.smem, st>>>(prm, rp);
   if (cudaGetLastError() != cudaSuccess) return KVQ3_ERR_CUDA;
-  const int64_t items = (int64_t)prm.g.batch * prm.Hq;
+  const int64_t items = (int64_t)(prm.pf_n > 0 ? prm.pf_n : prm.g.batch) * prm.Hq;
   int64_t blocks = (items + 7) / 8;
   const int64_t cap = (int64_t)sm_count() * 8;
   if (blocks > cap) blocks = cap > 0 ? cap : 1;
@@ -1165,7 +1224,10 @@ kvq3_status decode_run_t(const DecodePlan& plan, DecodeParams prm, const RotPara
 #define KVQ3_DECODE_DECL(D, SN)                                                               \
   kvq3_status decode_plan_d##D##_##SN(const CacheGeom& g, int G, DecodePlan* plan);          \
   kvq3_status decode_run_d##D##_##SN(const DecodePlan&, const DecodeParams&, const RotParams&, \
-                                     float*, cudaStream_t);
+                                     float*, cudaStream_t);                                   \
+  kvq3_status prefill_plan_d##D##_##SN(const CacheGeom& g, int G, DecodePlan* plan);         \
+  kvq3_status prefill_run_d##D##_##SN(const DecodePlan&, const DecodeParams&, const RotParams&, \
+                                      float*, cudaStream_t);
 KVQ3_DECODE_DECL(64, f32) KVQ3_DECODE_DECL(64, f16) KVQ3_DECODE_DECL(64, e4m3)
 KVQ3_DECODE_DECL(128, f32) KVQ3_DECODE_DECL(128, f16) KVQ3_DECODE_DECL(128, e4m3)
 KVQ3_DECODE_DECL(256, f32) KVQ3_DECODE_DECL(256, f16) KVQ3_DECODE_DECL(256, e4m3)
@@ -1190,6 +1252,18 @@ KVQ3_DECODE_DECL(256, f32) KVQ3_DECODE_DECL(256, f16) KVQ3_DECODE_DECL(256, e4m3
     const int gp = plan.gpad;                                                                 \
     if (prm.g.block == 32) KVQ3_DECODE_PICK(D, 32, SC, decode_run_t, plan, prm, rp, out, st)  \
     KVQ3_DECODE_PICK(D, 64, SC, decode_run_t, plan, prm, rp, out, st)                         \
+  }                                                                                           \
+  /* chunked prefill: 8 logit columns = query tokens x a block of query heads of a kv head, \
+     with P' split into hi + lo halves (the many outputs of a prefill chunk leave the  \
+     single fp16 rounding of P' too close to the tolerance) */                         \
+  kvq3_status prefill_plan_d##D##_##SN(const CacheGeom& g, int G, DecodePlan* plan) {        \
+    if (g.block == 32) return decode_plan_t<D, 32, 8, SC, true, true>(g, G, plan);            \
+    return decode_plan_t<D, 64, 8, SC, true, true>(g, G, plan);                               \
+  }                                                                                           \
+  kvq3_status prefill_run_d##D##_##SN(const DecodePlan& plan, const DecodeParams& prm,        \
+                                      const RotParams& rp, float* out, cudaStream_t st) {     \
+    if (prm.g.block == 32) return decode_run_t<D, 32, 8, SC, true, true>(plan, prm, rp, out, st); \
+    return decode_run_t<D, 64, 8, SC, true, true>(plan, prm, rp, out, st);                    \
   }
 
 }  // namespace kvq3

@@ -286,6 +286,29 @@ kvq3_status kvq3_decode_attn_noalloc(kvq3_rotation rot, const kvq3_cache_desc *d
                                      int32_t num_q_heads, float sm_scale, float *out,
                                      int32_t *dev_status, void *stream);
 
+/* Chunked-prefill attention over the packed cache ([OMC] read path and Key
+ * formulas with a causal mask; the pages quantise keys and values during the
+ * prefill phase as well as decode, and the same fused read applies): query
+ * token i, at position pos0 + i of sequence seq, attends to positions
+ * [0, pos0 + i] of that sequence -- one decode step of the sequence cut
+ * after its own position.  The positions must already be in the cache (e.g.
+ * written by kvq3_write_chunk); seq_lens is not read.
+ * q: device fp16 [n_q][Hq][d]; out: device fp32 [n_q][Hq][d]; sm_scale <= 0
+ * means 1/sqrt(d); Hq a multiple of Hkv with Hq/Hkv <= 16.  Internally the
+ * queries form tiles of up to 8 (query token, head) pairs per kv head.
+ * workspace:
+ * device, ws_bytes >= kvq3_prefill_workspace_size(desc, Hq, n_q), 256-byte
+ * aligned; calls sharing it must not overlap.  n_q = 0 is a no-op;
+ * KVQ3_ERR_INVALID_ARG when seq is out of range or pos0 + n_q exceeds the
+ * sequence capacity max_pages_per_seq * P. */
+kvq3_status kvq3_prefill_workspace_size(const kvq3_cache_desc *desc, int32_t num_q_heads,
+                                        int64_t n_q, size_t *bytes);
+kvq3_status kvq3_prefill_attn(kvq3_rotation rot, const kvq3_cache_desc *desc,
+                              const kvq3_cache *cache, int32_t seq, int64_t pos0,
+                              int64_t n_q, const void *q, int32_t num_q_heads,
+                              float sm_scale, float *out, void *workspace, size_t ws_bytes,
+                              int32_t *dev_status, void *stream);
+
 /* Reads back positions t0..t0+nt-1 of sequence seq, kv head kv_head, K
  * (which = 0) or V (which = 1) as fp32 out[nt][d]: s_q * c in the rotated
  * domain (rot == NULL) or U^T (s_q * c) (rot != NULL) ([OIQ] 3.3 "Retrieve").

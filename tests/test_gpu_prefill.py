@@ -1,0 +1,97 @@
+"""Chunked-prefill attention over the packed cache: GPU (kvq3_prefill_attn)
+against the oracle (oracle.prefill) on the same oracle-written cache.
+
+Query token i of the chunk sits at position pos0 + i and attends causally to
+positions [0, pos0 + i]; the library tiles 16/G query tokens x G heads per kv
+head, so the cases cover every group size's tiling, ragged last tiles, a chunk
+at the start of a sequence and one in the middle, paged and contiguous caches.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import kvq3_inputs as I
+from cases import TOL_DECODE, Case, rel_err
+from oracle import kvq3_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+PREFILL_CASES = [
+    # (case kwargs, sequence, pos0, n_q)
+    (dict(d=128, block=64, scale="f16", page=64, lens=(300,), hkv=2, hq=8), 0, 200, 100),     # G=4, 25 tiles
+    (dict(d=128, block=64, scale="f16", page=16, lens=(90, 257), hkv=2, hq=8, paged=True), 1, 0, 257),
+    (dict(d=128, block=64, scale="e4m3", page=64, lens=(520,), hkv=2, hq=16), 0, 450, 70),    # G=8
+    (dict(d=128, block=64, scale="f32", page=64, lens=(200,), hkv=4, hq=4), 0, 150, 50),      # G=1, qt=16
+    (dict(d=128, block=64, scale="f16", page=16, lens=(130,), hkv=1, hq=16, flags=1), 0, 100, 30),   # G=16
+    (dict(d=64, block=32, scale="f16", page=16, lens=(150,), hkv=2, hq=12), 0, 60, 90),       # G=6, qt=2
+    (dict(d=256, block=64, scale="f16", page=16, lens=(300, 180), hkv=2, hq=8, paged=True), 1, 100, 80),
+]
+
+
+def _ids(c):
+    kw, seq, pos0, n = c
+    return (f"d{kw['d']}-m{kw['block']}-{kw['scale']}-G{kw['hq'] // kw['hkv']}-"
+            f"{'paged' if kw.get('paged') else 'contig'}-pos{pos0}-n{n}")
+
+
+def _run(c: Case, seq: int, pos0: int, q: np.ndarray, sm_scale: float = 0.0):
+    t = c.torch
+    qd = t.as_tensor(q, device=c.dev)
+    out = t.full((q.shape[0], c.hq, c.d), float("nan"), dtype=t.float32, device=c.dev)
+    ws = t.empty(c.K.kvq3_prefill_workspace_size(c.desc, c.hq, q.shape[0]), dtype=t.uint8, device=c.dev)
+    c.K.kvq3_prefill_attn(c.rot.handle, c.desc, c.cache, seq, pos0, qd, out, ws, sm_scale, c.status)
+    t.cuda.synchronize()
+    return out.cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("cfg", PREFILL_CASES, ids=_ids)
+def test_prefill_matches_oracle(cfg):
+    kw, seq, pos0, n = cfg
+    c = Case(**kw)
+    k, v, si, ps = c.tokens()
+    c.oracle_write(k, v, si, ps)
+    c.upload_oracle_pool()
+    q = I.q_np(c.spec, n, c.hq, 7)            # [n][Hq][d]: one row per query token
+    got = _run(c, seq, pos0, q)
+    ref = O.prefill(c.pool_o, c.layout, c.U, q, seq, pos0, c.table)
+    assert c.device_status() == 0
+    e = rel_err(got, ref)
+    print(f"max|err|/rms = {e:.3e}")
+    assert e <= TOL_DECODE
+
+
+def test_prefill_single_query_equals_decode():
+    # one query at the last position is a decode step of the whole sequence
+    c = Case(d=128, block=64, scale="f16", page=64, lens=(333,), hkv=2, hq=8)
+    k, v, si, ps = c.tokens()
+    c.oracle_write(k, v, si, ps)
+    c.upload_oracle_pool()
+    q = c.queries(3)                          # [1][Hq][d]
+    got_p = _run(c, 0, 332, q)
+    got_d = c.gpu_decode(q)
+    assert c.device_status() == 0
+    assert rel_err(got_p, got_d) <= TOL_DECODE
+
+
+def test_prefill_custom_scale_and_bounds():
+    c = Case(d=128, block=64, scale="f16", page=64, lens=(128,), hkv=2, hq=8)
+    k, v, si, ps = c.tokens()
+    c.oracle_write(k, v, si, ps)
+    c.upload_oracle_pool()
+    q = I.q_np(c.spec, 40, c.hq, 9)
+    for sm in (0.02, 0.3):
+        got = _run(c, 0, 88, q, sm)
+        ref = O.prefill(c.pool_o, c.layout, c.U, q, 0, 88, c.table, sm)
+        assert rel_err(got, ref) <= TOL_DECODE
+    t = c.torch
+    qd = t.as_tensor(q, device=c.dev)
+    out = t.empty((40, c.hq, c.d), dtype=t.float32, device=c.dev)
+    ws = t.empty(c.K.kvq3_prefill_workspace_size(c.desc, c.hq, 40), dtype=t.uint8, device=c.dev)
+    # past the sequence capacity, or a sequence that does not exist
+    for seq, pos0 in ((0, 100), (1, 0), (-1, 0)):
+        with pytest.raises(c.K.Kvq3Error):
+            c.K.kvq3_prefill_attn(c.rot.handle, c.desc, c.cache, seq, pos0, qd, out, ws)
+    # a workspace one byte short
+    with pytest.raises(c.K.Kvq3Error):
+        c.K.kvq3_prefill_attn(c.rot.handle, c.desc, c.cache, 0, 0, qd, out, ws[:-1])
