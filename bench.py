@@ -408,6 +408,98 @@ def run_prefill(args, world, rank, dev):
             "gpu_launches": args.steps, "clocks": clk.summary()}))
 
 
+class PrefillAttnWorkload:
+    """Chunked-prefill attention: one sequence whose cache holds seq_len
+    tokens (written once with kvq3_write_chunk); one step runs
+    kvq3_prefill_attn for its last `chunk` positions (queries resident)."""
+
+    def __init__(self, device, w: I.Workload):
+        import torch
+        import hadamard_rotated_bit_kvq3_gb300 as K
+        self.K, self.torch, self.w, self.dev = K, torch, w, device
+        n, P = w.seq_len, w.page_size
+        self.maxp = (n + P - 1) // P
+        self.desc = K.CacheDesc(w.d, w.num_kv_heads, w.block, 3, K.SCALE_TYPES[w.scale], w.eps, P, 1,
+                                self.maxp, 0, self.maxp)
+        _, _, pool_bytes = K.kvq3_cache_sizes(self.desc)
+        self.pool = torch.zeros(pool_bytes, dtype=torch.uint8, device=device)
+        self.lens_t = torch.tensor([n], dtype=torch.int32, device=device)
+        self.cache = K.Cache(self.pool.data_ptr(), None, self.lens_t.data_ptr())
+        self.rot = K.Rotation(w.d, w.rot_seed, w.rot_flags)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        for t0 in range(0, n, 8192):
+            m = min(8192, n - t0)
+            k = torch.stack([I.kv_rows_torch(w.data, 0, 0, h, t0, m, device) for h in range(w.num_kv_heads)], 1)
+            v = torch.stack([I.kv_rows_torch(w.data, 1, 0, h, t0, m, device) for h in range(w.num_kv_heads)], 1)
+            K.kvq3_write_chunk(self.rot.handle, self.desc, self.cache, k.contiguous(), v.contiguous(), 0, t0,
+                               self.status)
+        self.pos0 = n - w.chunk
+        self.q = torch.as_tensor(I.q_np(w.data, w.chunk, w.num_q_heads, 0), device=device)
+        self.out = torch.empty((w.chunk, w.num_q_heads, w.d), dtype=torch.float32, device=device)
+        self.ws = torch.empty(K.kvq3_prefill_workspace_size(self.desc, w.num_q_heads, w.chunk),
+                              dtype=torch.uint8, device=device)
+        torch.cuda.synchronize()
+
+    def step(self):
+        self.K.kvq3_prefill_attn(self.rot.handle, self.desc, self.cache, 0, self.pos0, self.q, self.out,
+                                 self.ws, 0.0, self.status)
+
+    def flops(self) -> float:
+        """QK^T and PV multiply-adds of the causal chunk: 4 d flops per (query
+        head, attended key)."""
+        w = self.w
+        keys = sum(self.pos0 + i + 1 for i in range(w.chunk))
+        return 4.0 * w.d * w.num_q_heads * keys
+
+
+def run_prefill_attn(args, world, rank, dev):
+    import torch
+    w = I.workloads()[args.workload]
+    st = PrefillAttnWorkload(dev, w)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        st.step()
+    torch.cuda.synchronize()
+    assert int(st.status.item()) == 0
+    if args.profile:
+        for _ in range(args.steps):
+            st.step()
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": w.name, "status": int(st.status.item())}))
+        return
+    barrier(world)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index or 0) as clk:
+        a.record(stream)
+        for _ in range(args.steps):
+            st.step()
+        b.record(stream)
+        torch.cuda.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b), world) / args.steps
+    assert int(st.status.item()) == 0
+    pk = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    peak = float(pk.get("bf16_tflops", 1900.0))
+    tflops = st.flops() / (ms * 1e-3) / 1e12
+    if rank == 0:
+        print(json.dumps({
+            "metric": "prefill-attention query tokens/s (one layer, all heads)",
+            "value": whole_job_rate(w.chunk, world, ms), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16 mma / f32 accumulate (3-bit packed cache)",
+            "data": "synthetic",
+            "config": {"workload": f"{w.name}: chunk of {w.chunk} queries at positions {w.seq_len - w.chunk}.."
+                                   f"{w.seq_len - 1} of a {w.seq_len}-token cache, Hkv{w.num_kv_heads} "
+                                   f"Hq{w.num_q_heads} d{w.d} m{w.block} {w.scale} scales, contiguous "
+                                   f"P{w.page_size}, causal", "l2": "cache 3.4 MB per kv head"},
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tflops / peak, "traffic": None,
+                         "kernel": "kvq3_prefill_attn (decode_split_kernel<..., prefill> + combine)",
+                         "peak_source": "measured bf16 (fp16 mma has the same nominal rate)"
+                         if pk else "fallback"},
+            "gpu_launches": 2 * args.steps, "clocks": clk.summary()}))
+
+
 def workload_desc(w: I.Workload) -> str:
     lens = f"N={w.seq_len}" if not w.len_range else f"N~U[{w.len_range[0]},{w.len_range[1]}]"
     return (f"{w.name}: B{w.batch} Hkv{w.num_kv_heads} Hq{w.num_q_heads} d{w.d} {lens} m{w.block} "
@@ -437,6 +529,9 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = I.workloads()[args.workload]
+    if w.chunk > 0:
+        run_prefill_attn(args, world, rank, dev)
+        return
     if not w.decode:
         run_prefill(args, world, rank, dev)
         return

@@ -275,6 +275,7 @@ class Workload:
     rot_seed: int = 42
     decode: bool = True
     eps: float = 1e-6
+    chunk: int = 0        # prefill-attention workloads: query tokens of the chunk
 
     @property
     def group(self) -> int:
@@ -293,6 +294,8 @@ def workloads():
                                      outlier_frac_hi=0.08)),
         "prefill": Workload("prefill", 1, 8, 8, 128, 32, "f32", 1, 64, False, 131072, (),
                             DataSpec(128, 8, 1003, 0.03, 20.0), decode=False),
+        "prefill_attn": Workload("prefill_attn", 1, 8, 32, 128, 64, "f16", 3, 128, False, 32768, (),
+                                 DataSpec(128, 8, 1005, 0.03, 20.0), decode=False, chunk=2048),
         "ragged": Workload("ragged", 64, 4, 16, 256, 64, "f16", 3, 16, True, 0, (1024, 65536),
                            DataSpec(256, 4, 1004, 0.05, 30.0)),
     }
