@@ -453,8 +453,12 @@ class PrefillAttnWorkload:
 
 
 def run_prefill_attn(args, world, rank, dev):
+    import dataclasses
+
     import torch
     w = I.workloads()[args.workload]
+    if args.tokens:   # a shorter context (profiling): the chunk is at most a quarter of it
+        w = dataclasses.replace(w, seq_len=args.tokens, chunk=min(w.chunk, max(1, args.tokens // 4)))
     st = PrefillAttnWorkload(dev, w)
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):

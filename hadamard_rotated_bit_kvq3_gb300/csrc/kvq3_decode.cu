@@ -125,6 +125,14 @@ kvq3_status kvq3_prefill_attn(kvq3_rotation rot, const kvq3_cache_desc* desc,
   if ((s = prefill_plan_for(vg, gcols, &plan)) != KVQ3_OK) return s;
   if (!workspace || ws_bytes < plan.ws_bytes || reinterpret_cast<uintptr_t>(workspace) % 256)
     return KVQ3_ERR_WORKSPACE;
+  const double qks = (sm_scale > 0.0f ? (double)sm_scale : 1.0 / sqrt((double)vg.d)) * 1.4426950408889634;
+  if (vg.d == 128) {
+    // shared dequantised tiles: each K/V tile is unpacked once for 64 query rows
+    CacheGeom g;
+    make_geom(desc, &g);
+    return prefill_tiles(g, cache, seq, pos0, n_q, q, num_q_heads, (float)qks, out, dev_status,
+                         rot->params, static_cast<cudaStream_t>(stream));
+  }
   DecodeParams prm;
   memset(&prm, 0, sizeof(prm));
   prm.g = vg;

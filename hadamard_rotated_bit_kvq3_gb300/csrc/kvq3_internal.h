@@ -25,6 +25,11 @@ kvq3_status check_cache(const CacheGeom& g, const kvq3_cache* cache, bool need_l
 // Number of streaming multiprocessors of the current device (cached).
 int sm_count();
 
+// Tile-kernel path of kvq3_prefill_attn (d = 128; arguments already checked).
+kvq3_status prefill_tiles(const CacheGeom& g, const kvq3_cache* cache, int32_t seq, int64_t pos0,
+                          int64_t n_q, const void* q, int32_t hq, float qk_scale, float* out,
+                          int32_t* dev_status, const RotParams& rp, cudaStream_t st);
+
 inline kvq3_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVQ3_OK : KVQ3_ERR_CUDA; }
 
 inline float inv_sqrt(int d) { return (float)(1.0 / __builtin_sqrt((double)d)); }
