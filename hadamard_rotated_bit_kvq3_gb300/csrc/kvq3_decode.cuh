@@ -10,14 +10,16 @@
 //
 // Design (one GPU, HBM-bound):
 //  * Work = the flattened list of chunks of every (sequence, kv head) unit (a
-//    chunk is one page when pages hold >= kChunk tokens, else kChunk/P
-//    consecutive pages of the unit).  A persistent grid of 4-warp CTAs splits
-//    the list into equal contiguous ranges.
+//    chunk is up to ceil(kChunk/P) consecutive pages of the unit: fewer when
+//    two stages of them would not fit in a resident CTA's share of shared
+//    memory).  A persistent grid of 4-warp CTAs splits the list into equal
+//    contiguous ranges.
 //  * Each chunk's K and V records stream into a ring of shared-memory stages
 //    with cp.async.bulk (mbarrier completion, L2 evict-first), one warp
 //    issuing a chunk with lane i copying page i; the four warps share every
-//    stage, one 16-token step each, and the last warp to release a stage
-//    refills it with the chunk S places ahead.
+//    stage, one 16-token step each, meet at one barrier per chunk, and one
+//    of them then refills the stage just released with the chunk S places
+//    ahead.
 //  * Each warp keeps an online-softmax state per unit; at the end of a unit
 //    the four states merge (max, rescale, sum) into one fp32 partial
 //    (o1[G][d] unnormalised, max, sum) at workspace slot (cta + unit), unique
@@ -399,6 +401,16 @@ struct ScaleDec {
   }
 };
 
+// Per-step values handed between the parts of a decode step.
+template <int NTQ>
+struct StepLogits {
+  float s0[NTQ], s1[NTQ];   // rows r and r + 8
+};
+template <int NB, int NTP>
+struct StepP {
+  uint32_t b[NB][NTP][2];   // P' fragments (B operand of PV)
+};
+
 // What the producer thread publishes with each chunk (at the end of its stage).
 struct ChunkDesc {
   int32_t unit, b, kvh, n_tok;
@@ -567,7 +579,6 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
   const uint32_t qf_lane = smem_u32(qf_s) + (uint32_t)lane * 8u;
   float qinv[NTQ];
   int64_t lim[PF ? NTQ : 1];   // prefill: causal limit of each logit column
-  int64_t step_tok = 0;        // prefill: position of the current step's token t0
   // logit accumulator seeds (key offset, see setup_unit): registers when few,
   // else shared memory [block][head]
   constexpr bool KOFS_REG = NB * NTQ <= 4;
@@ -790,11 +801,18 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
     named_barrier(1, 128);  // qs is rewritten at the next unit
   };
 
-  // one 16-token step at token offset t0 of a page whose K record starts at
-  // shared address pg (V record at pg + REC); n_valid tokens of the page
-  auto step = [&](uint32_t pg, int t0, auto full_c, int n_valid) {
-    constexpr bool FULL = decltype(full_c)::value;   // all 16 tokens valid
-    // ------------------------------------------------ S = K q1 (per block)
+  // A 16-token step at token offset t0 of a page whose K record starts at
+  // shared address pg (V record at pg + REC), n_valid tokens of the page,
+  // comes in four parts: the logits, the running-max update, P' and PV.
+  // FULL: all 16 tokens valid.  tok (prefill): position of token t0.
+  // ------------------------------------------------ S = K q1 (per block)
+  // sc0 / sc1: logits of tokens t0 + r and t0 + r + 8, column 4tq + j
+  using SL = StepLogits<NTQ>;
+  using SP = StepP<NB, NTP>;
+  auto logits = [&](uint32_t pg, int t0, auto full_c, int n_valid, int64_t tok, SL& sl) {
+    constexpr bool FULL = decltype(full_c)::value;
+    float* sc0 = sl.s0;
+    float* sc1 = sl.s1;
     float accq[NB][NTQ][4];
 #pragma unroll
     for (int b = 0; b < NB; ++b)
@@ -839,12 +857,6 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
       SDec::template one<8 * BPT>(a, skr8);
     }
     const bool vr = FULL || t0 + r < n_valid, vr8 = FULL || t0 + r + 8 < n_valid;
-    // ------------------------------------------------ online softmax
-    // The running max m of a head moves only when a score exceeds it: one vote
-    // finds that, and only then are the exact max (quad-column reduction) and
-    // the rescale computed; otherwise p = 2^(s - m) <= 1 as before.
-    float sc0[NTQ], sc1[NTQ], pr[NTQ], pr8[NTQ], alpha[NTQ];
-    bool over = false;
 #pragma unroll
     for (int tq = 0; tq < NTQ; ++tq) {
       float s0 = 0.0f, s1 = 0.0f;
@@ -856,14 +868,26 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
       sc0[tq] = vr ? s0 * qinv[tq] : -INFINITY;
       sc1[tq] = vr8 ? s1 * qinv[tq] : -INFINITY;
       if constexpr (PF) {   // causal mask: rows are tokens t0 + r and t0 + r + 8
-        const int64_t t = step_tok + r;
+        const int64_t t = tok + r;
         if (t > lim[tq % (PF ? NTQ : 1)]) sc0[tq] = -INFINITY;
         if (t + 8 > lim[tq % (PF ? NTQ : 1)]) sc1[tq] = -INFINITY;
       }
-      over |= sc0[tq] > m[tq] || sc1[tq] > m[tq];
     }
-    const bool changed = __any_sync(kFull, over);
-    if (changed) {
+  };
+
+  // ------------------------------------------------ online softmax
+  // The running max m of a head moves only when a score exceeds it: one vote
+  // finds that, and only then are the exact max (quad-column reduction) and
+  // the rescale of l and of the accumulators computed; otherwise
+  // p = 2^(s - m) <= 1 as before.
+  auto update = [&](const SL& sl) {
+    const float* sc0 = sl.s0;
+    const float* sc1 = sl.s1;
+    bool over = false;
+#pragma unroll
+    for (int tq = 0; tq < NTQ; ++tq) over |= sc0[tq] > m[tq] || sc1[tq] > m[tq];
+    if (__any_sync(kFull, over)) {
+      float alpha[NTQ];
 #pragma unroll
       for (int tq = 0; tq < NTQ; ++tq) {
         float mx = fmaxf(sc0[tq], sc1[tq]);
@@ -876,15 +900,6 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
         l[tq] *= alpha[tq];
         m[tq] = mn;
       }
-    }
-#pragma unroll
-    for (int tq = 0; tq < NTQ; ++tq) {
-      const float mref = (PF && m[tq] == -INFINITY) ? 0.0f : m[tq];   // all masked: p = 0
-      pr[tq] = ex2(sc0[tq] - mref);
-      pr8[tq] = ex2(sc1[tq] - mref);
-      l[tq] += pr[tq] + pr8[tq];
-    }
-    if (changed) {
       if constexpr (PSPLIT) {
         // this lane's PV columns belong to its own QK head 4tp + j
 #pragma unroll
@@ -914,7 +929,23 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
         }
       }
     }
-    // ------------------------------------------------ P' = p * s_v (B of PV)
+  };
+
+  // ------------------------------------------------ P' = p * s_v (B of PV)
+  // p = 2^(s - m) of the step's logits; l += p
+  auto pprime = [&](uint32_t pg, int t0, auto full_c, int n_valid, const SL& sl, SP& sp) {
+    constexpr bool FULL = decltype(full_c)::value;
+    const float* sc0 = sl.s0;
+    const float* sc1 = sl.s1;
+    auto& pb = sp.b;
+    float pr[NTQ], pr8[NTQ];
+#pragma unroll
+    for (int tq = 0; tq < NTQ; ++tq) {
+      const float mref = (PF && m[tq] == -INFINITY) ? 0.0f : m[tq];   // all masked: p = 0
+      pr[tq] = ex2(sc0[tq] - mref);
+      pr8[tq] = ex2(sc1[tq] - mref);
+      l[tq] += pr[tq] + pr8[tq];
+    }
     const int T0 = t0 + 2 * j;
     float x0[NTQ], x1[NTQ], x2[NTQ], x3[NTQ];
     {
@@ -934,7 +965,6 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
     // Columns of padded heads (>= G) carry finite values (their q1 is zero)
     // and are never stored, so only invalid tokens are masked (their scale
     // bytes are stale stage contents).
-    uint32_t pb[NB][NTP][2];
     if constexpr (PSPLIT) {
       float sv0[NB], sv1[NB], sv2[NB], sv3[NB];
       {
@@ -993,7 +1023,11 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
         }
       }
     }
-    // ------------------------------------------------ o1^T += V^T P'^T
+  };
+
+  // ------------------------------------------------ o1^T += V^T P'^T
+  auto pv = [&](uint32_t pg, int t0, const SP& sp) {
+    const auto& pb = sp.b;
     const uint32_t vt = pg + (uint32_t)(t0 * CB) + v_lane;   // token t0 + 2j
     static_for<NB>([&](auto bc) {
       constexpr int b = decltype(bc)::value;
@@ -1064,18 +1098,66 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
       cur_first = dw.y == 0;
     }
     cur_last = (int)dw.y == (int)lds32<24>(st + desc_off) - 1;   // c == nc - 1
-    for (int t = wid * 16; t < n_tok; t += kWarps * 16) {
-      int pi = 0, tin = t;                              // page of the chunk, offset in it
+    if (!PF && n_tok == p.chunk_tokens && page_ok == (1u << p.pages_per_chunk) - 1u &&
+        p.chunk_tokens % (16 * kWarps) == 0) {
+      // A whole chunk: the warp's steps t = 16 wid + 64 k, software-pipelined
+      // so that P' and PV of step k and the logits of step k + 1 form one
+      // branch-free stretch (the running-max update follows PV of step k).
+      const int nsw = p.chunk_tokens / (16 * kWarps);
+      int pi = 0, tin = wid * 16;                       // page of the chunk, offset in it
       while (tin >= P) {
         tin -= P;
         ++pi;
       }
-      if ((page_ok >> pi) & 1u) {
-        const uint32_t pg = st + (uint32_t)pi * 2 * REC;
-        const int nv = min(P, n_tok - pi * P);          // valid tokens of this page
-        if constexpr (PF) step_tok = (int64_t)dw.y * p.chunk_tokens + t;
-        if (nv - tin >= 16) step(pg, tin, std::true_type{}, nv);
-        else step(pg, tin, std::false_type{}, nv);
+      uint32_t pg = st + (uint32_t)pi * 2 * REC;
+      int t0 = tin;
+      SL sa;
+      logits(pg, t0, std::true_type{}, P, 0, sa);
+      update(sa);
+      for (int k = 1; k < nsw; ++k) {
+        tin += 16 * kWarps;
+        while (tin >= P) {
+          tin -= P;
+          ++pi;
+        }
+        const uint32_t pgn = st + (uint32_t)pi * 2 * REC;
+        SP pb;
+        pprime(pg, t0, std::true_type{}, P, sa, pb);
+        SL sb;
+        logits(pgn, tin, std::true_type{}, P, 0, sb);
+        pv(pg, t0, pb);
+        update(sb);
+        pg = pgn;
+        t0 = tin;
+        sa = sb;
+      }
+      SP pb;
+      pprime(pg, t0, std::true_type{}, P, sa, pb);
+      pv(pg, t0, pb);
+    } else {
+      for (int t = wid * 16; t < n_tok; t += kWarps * 16) {
+        int pi = 0, tin = t;                            // page of the chunk, offset in it
+        while (tin >= P) {
+          tin -= P;
+          ++pi;
+        }
+        if ((page_ok >> pi) & 1u) {
+          const uint32_t pg = st + (uint32_t)pi * 2 * REC;
+          const int nv = min(P, n_tok - pi * P);        // valid tokens of this page
+          const int64_t tok = (int64_t)dw.y * p.chunk_tokens + t;
+          SL sc;
+          SP pb;
+          if (nv - tin >= 16) {
+            logits(pg, tin, std::true_type{}, nv, tok, sc);
+            update(sc);
+            pprime(pg, tin, std::true_type{}, nv, sc, pb);
+          } else {
+            logits(pg, tin, std::false_type{}, nv, tok, sc);
+            update(sc);
+            pprime(pg, tin, std::false_type{}, nv, sc, pb);
+          }
+          pv(pg, tin, pb);
+        }
       }
     }
     prev = stage;
@@ -1173,15 +1255,31 @@ kvq3_status decode_plan_t(const CacheGeom& g, int G, DecodePlan* plan) {
   using SM = DecodeSmem<D, GPAD>;
   const void* k = reinterpret_cast<const void*>(&decode_split_kernel<D, BLOCK, GPAD, SCALE, PSPLIT, PF>);
   plan->gpad = GPAD;
-  plan->pages_per_chunk = (kChunk + g.page_size - 1) / g.page_size;
-  plan->chunk_tokens = plan->pages_per_chunk * g.page_size;
-  const size_t chunk_bytes = (size_t)plan->pages_per_chunk * 2 * g.record_bytes;
-  // + 16: word reads past the last code string; + descriptor at the end
-  plan->stage_bytes = (uint32_t)((chunk_bytes + 16 + sizeof(ChunkDesc) + 127) / 128 * 128);
-  // stages: the SM's 228 KB of shared memory split over the CTAs that the
-  // register budget lets reside (1 KB of it reserved per CTA); at least 2
+  // the SM's 228 KB of shared memory split over the CTAs that the register
+  // budget lets reside (1 KB of it reserved per CTA)
   const int mb = decode_min_blocks(D, GPAD);
   const size_t per_cta = 228 * 1024 / mb - 1024 < 227 * 1024 ? 228 * 1024 / mb - 1024 : 227 * 1024;
+  // + 16: word reads past the last code string; + descriptor at the end
+  auto stage_of = [&](int ppc) {
+    return (uint32_t)(((size_t)ppc * 2 * g.record_bytes + 16 + sizeof(ChunkDesc) + 127) / 128 * 128);
+  };
+  // Chunk: the pages of kChunk tokens, fewer where two stages of them would
+  // not fit in a CTA's share (one CTA fewer per SM costs more than a shorter
+  // chunk), preferring a whole number of 64-token rounds (4 warps x 16
+  // tokens) so that no warp idles at the chunk barrier.
+  {
+    const int most = (kChunk + g.page_size - 1) / g.page_size;
+    int fit = 0, even = 0;
+    for (int n = most; n >= 1 && even == 0; --n) {
+      if (SM::kStageOff + 2 * (size_t)stage_of(n) > per_cta) continue;
+      if (fit == 0) fit = n;
+      if ((n * g.page_size) % (16 * kWarps) == 0) even = n;
+    }
+    plan->pages_per_chunk = even ? even : (fit ? fit : 1);
+  }
+  plan->chunk_tokens = plan->pages_per_chunk * g.page_size;
+  plan->stage_bytes = stage_of(plan->pages_per_chunk);
+  // stages: as many as fit in the CTA's share; at least 2
   int stages = per_cta > SM::kStageOff ? (int)((per_cta - SM::kStageOff) / plan->stage_bytes) : 0;
   stages = stages < 2 ? 2 : (stages > kMaxStages ? kMaxStages : stages);
   const size_t smem = SM::kStageOff + (size_t)stages * plan->stage_bytes;
