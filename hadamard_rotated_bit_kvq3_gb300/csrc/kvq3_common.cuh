@@ -221,6 +221,15 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
 
 // Bounded wait for phase `parity` of an mbarrier.  Returns false when the
 // bound ran out (the caller flags KVQ3_DEV_TIMEOUT and winds down).
+// Programmatic dependent launch (griddepcontrol): a grid launched with
+// programmatic stream serialisation may start before the preceding grid ends;
+// griddep_wait blocks until that grid has completed and its writes are
+// visible, griddep_launch_dependents lets the following grid start.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t max_iter) {
   const uint32_t a = smem_u32(bar);
   for (uint32_t it = 0; it < max_iter; ++it) {

@@ -466,6 +466,8 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
   using SDec = ScaleDec<NB, SCALE>;
   constexpr int BPT = SDec::BPT;
 
+  // the combine kernel may launch now: it waits for this grid before reading
+  griddep_launch_dependents();
   extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x & 31;
   const int wid = threadIdx.x >> 5;
@@ -1183,6 +1185,9 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const __grid_consta
   float4 qt[E / 4];
   lane_quats<E>(rp, rr, qt);
   const bool so4 = (rp.flags & KVQ3_ROT_SO4) != 0;
+  // launched as a programmatic dependent of the split kernel: everything above
+  // overlaps its tail; its partials are complete and visible after this
+  griddep_wait();
   const int warp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int nwarps = (int)((gridDim.x * blockDim.x) >> 5);
   // output row it = (sequence or query token) * Hq + query head
@@ -1314,7 +1319,19 @@ kvq3_status decode_run_t(const DecodePlan& plan, DecodeParams prm, const RotPara
   int64_t blocks = (items + 7) / 8;
   const int64_t cap = (int64_t)sm_count() * 8;
   if (blocks > cap) blocks = cap > 0 ? cap : 1;
-  decode_combine_kernel<D><<<(unsigned)blocks, 256, 0, st>>>(prm, rp, out);
+  // programmatic dependent launch: the combine's launch and set-up overlap
+  // the split kernel's last CTAs (it waits on the grid before its reads)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, prm, rp, out) != cudaSuccess) return KVQ3_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? KVQ3_OK : KVQ3_ERR_CUDA;
 }
 
