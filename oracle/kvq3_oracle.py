@@ -1,4 +1,5 @@
-"""Plain, slow, fp64 CPU oracle of the orthogonally rotated 3-bit KV cache.
+"""Plain, slow, fp64 CPU oracle of the orthogonally rotated 3-bit KV cache
+(and its 2- and 4-bit variants).
 
 TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the benchmark's
 CPU-baseline leg may import this module.  The library (CUDA kernels and C ABI)
@@ -35,6 +36,10 @@ header of the library as well):
     c = clip(round_half_even(x/s_q), -3, 3), and c = 0 where s_q = 0.
   * Codes are 3-bit two's complement in a little-endian bit stream: element j
     of a vector at bits 3j..3j+2 of its 3d/8-byte code string.
+  * Other bit widths b = 2 and 4 ([OIQ] 3.3, 4.2 and 5.1 evaluate them; the
+    quantiser of [OMC] Key formulas is written for any b): divisor and clip
+    bound 2^(b-1) - 1, b-bit two's-complement codes in the same bit stream
+    (element j at bits b*j..b*j+b-1), code strings of b*d/8 bytes.
   * Cache layout: see :class:`Layout`.
   * Attention: logits = (q1 . k1_hat) * sm_scale with sm_scale = 1/sqrt(d),
     softmax over positions [0, seq_len), output U^T y1 in fp32; an empty
@@ -277,40 +282,59 @@ def decode_scales(buf: np.ndarray, kind: str) -> np.ndarray:
 # ---------------------------------------------------------------------------
 # Quantiser and packing
 # ---------------------------------------------------------------------------
-def quantize(x: np.ndarray, block: int, eps: float, kind: str):
-    """Blockwise symmetric 3-bit quantiser ([OMC] Key formulas, b = 3):
-    per block of ``block`` consecutive coordinates, s = (max|x| + eps)/(2^2-1),
+BIT_WIDTHS = (2, 3, 4)
+
+
+def qmax(bits: int) -> int:
+    """Largest code magnitude of the b-bit symmetric quantiser, 2^(b-1) - 1
+    ([OMC] Key formulas; the method fixes b = 3, [OIQ] 3.3 and 5.1 use b = 2,
+    3 and 4): 1, 3 or 7."""
+    if bits not in BIT_WIDTHS:
+        raise ValueError(f"bit width {bits} not in {BIT_WIDTHS}")
+    return (1 << (bits - 1)) - 1
+
+
+def quantize(x: np.ndarray, block: int, eps: float, kind: str, bits: int = 3):
+    """Blockwise symmetric b-bit quantiser ([OMC] Key formulas): per block of
+    ``block`` consecutive coordinates, s = (max|x| + eps)/(2^(b-1) - 1),
     stored as s_q = round(s) in the scale type, codes
-    c = clip(round_half_even(x/s_q), -3, 3) (c = 0 where s_q = 0).
+    c = clip(round_half_even(x/s_q), -(2^(b-1) - 1), 2^(b-1) - 1)
+    (c = 0 where s_q = 0).
     x: fp64 [n][d].  Returns (codes int8 [n][d], s_q fp64 [n][d/block],
     s fp64 [n][d/block])."""
     n, d = x.shape
+    qm = qmax(bits)
     xb = x.reshape(n, d // block, block)
-    s = (np.abs(xb).max(axis=-1, initial=0.0) + eps) / 3.0
+    s = (np.abs(xb).max(axis=-1, initial=0.0) + eps) / float(qm)
     sq = round_scale(s, kind)
     with np.errstate(divide="ignore", invalid="ignore"):
         r = np.where(sq[..., None] > 0, xb / sq[..., None], 0.0)
-    c = np.clip(np.rint(r), -3, 3).astype(np.int8)
+    c = np.clip(np.rint(r), -qm, qm).astype(np.int8)
     return c.reshape(n, d), sq, s
 
 
-def pack_codes(codes: np.ndarray) -> np.ndarray:
-    """3-bit two's-complement codes [..., d] -> bytes [..., 3d/8]: element j at
-    bits 3j..3j+2 of a little-endian bit stream (bit k of the stream is bit
-    k % 8 of byte k // 8) ([OMC] Implementation notes: codes packed into bytes)."""
+def pack_codes(codes: np.ndarray, bits: int = 3) -> np.ndarray:
+    """b-bit two's-complement codes [..., d] -> bytes [..., b*d/8]: element j
+    at bits b*j..b*j+b-1 of a little-endian bit stream (bit k of the stream is
+    bit k % 8 of byte k // 8) ([OMC] Implementation notes: codes packed into
+    bytes; [OIQ] 4.2: INT3/INT4 packed values after the scale header)."""
+    qmax(bits)
     d = codes.shape[-1]
-    c = codes.astype(np.int64) & 7
-    bits = np.stack([(c >> i) & 1 for i in range(3)], axis=-1)      # [..., d, 3]
-    bits = bits.reshape(codes.shape[:-1] + (3 * d,)).astype(np.uint8)
-    return np.packbits(bits, axis=-1, bitorder="little")
+    c = codes.astype(np.int64) & ((1 << bits) - 1)
+    bs = np.stack([(c >> i) & 1 for i in range(bits)], axis=-1)      # [..., d, b]
+    bs = bs.reshape(codes.shape[:-1] + (bits * d,)).astype(np.uint8)
+    return np.packbits(bs, axis=-1, bitorder="little")
 
 
-def unpack_codes(buf: np.ndarray, d: int) -> np.ndarray:
-    """Inverse of :func:`pack_codes` (the unused 3-bit value 4 reads as -4)."""
-    bits = np.unpackbits(np.asarray(buf, dtype=np.uint8), axis=-1, bitorder="little")
-    bits = bits.reshape(buf.shape[:-1] + (d, 3)).astype(np.int64)
-    v = bits[..., 0] + 2 * bits[..., 1] + 4 * bits[..., 2]
-    return np.where(v >= 4, v - 8, v).astype(np.int8)
+def unpack_codes(buf: np.ndarray, d: int, bits: int = 3) -> np.ndarray:
+    """Inverse of :func:`pack_codes` (the value -2^(b-1), which the quantiser
+    never writes, reads as itself)."""
+    qmax(bits)
+    bs = np.unpackbits(np.asarray(buf, dtype=np.uint8), axis=-1, bitorder="little")
+    bs = bs.reshape(buf.shape[:-1] + (d, bits)).astype(np.int64)
+    v = sum(bs[..., i] << i for i in range(bits))
+    half = 1 << (bits - 1)
+    return np.where(v >= half, v - 2 * half, v).astype(np.int8)
 
 
 # ---------------------------------------------------------------------------
@@ -324,8 +348,9 @@ class Layout:
     holds, for kv heads 0..Hkv-1 in order, a K record then a V record.  A
     record is its scale header -- P*(d/block) scales, token-major
     (slot t, block j at index t*(d/block)+j), each in the scale type,
-    little-endian -- followed by P code strings of 3d/8 bytes (slot t at
-    t*3d/8).  Token position ``pos`` of sequence ``b`` lives in slot pos % P of
+    little-endian -- followed by P code strings of b*d/8 bytes (slot t at
+    t*b*d/8; b = ``bits``, 3 unless stated).  Token position ``pos`` of
+    sequence ``b`` lives in slot pos % P of
     logical page pos // P; the physical page is page_table[b][pos // P], or
     b*max_pages_per_seq + pos // P for a contiguous cache (no page table)."""
     d: int
@@ -336,6 +361,7 @@ class Layout:
     batch: int
     max_pages_per_seq: int
     num_pages: int
+    bits: int = 3
 
     @property
     def nb(self) -> int:
@@ -347,7 +373,7 @@ class Layout:
 
     @property
     def code_bytes(self) -> int:
-        return 3 * self.d // 8
+        return self.bits * self.d // 8
 
     @property
     def record_bytes(self) -> int:
@@ -422,8 +448,8 @@ def write(pool: np.ndarray, layout: Layout, U: np.ndarray, k: np.ndarray, v: np.
     ok = np.nonzero(st == 0)[0]
     for which, src in ((0, k), (1, v)):
         x = src[ok].astype(np.float64).reshape(len(ok) * H, layout.d) @ U.T
-        codes, sq, _ = quantize(x, layout.block, eps, layout.scale)
-        packed = pack_codes(codes)                              # [n*H, cb]
+        codes, sq, _ = quantize(x, layout.block, eps, layout.scale, layout.bits)
+        packed = pack_codes(codes, layout.bits)                 # [n*H, cb]
         hdr = encode_scales(sq, layout.scale)                   # [n*H, nb*sb]
         heads = np.tile(np.arange(H), len(ok))
         pg = np.repeat(page[ok], H)
@@ -449,7 +475,7 @@ def read_rotated(pool: np.ndarray, layout: Layout, b: int, kv_head: int, which: 
     so = rec + slot * layout.nb * layout.sb
     co = rec + layout.page_size * layout.nb * layout.sb + slot * layout.code_bytes
     sc = decode_scales(pool[_gather_index(so, layout.nb * layout.sb)], layout.scale)
-    cs = unpack_codes(pool[_gather_index(co, layout.code_bytes)], layout.d)
+    cs = unpack_codes(pool[_gather_index(co, layout.code_bytes)], layout.d, layout.bits)
     xh = (cs.reshape(nt, layout.nb, layout.block) * sc[..., None]).reshape(nt, layout.d)
     return xh, cs, sc
 

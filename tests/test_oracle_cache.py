@@ -8,11 +8,11 @@ import pytest
 import kvq3_inputs as I
 
 
-def _setup(oracle, d=128, H=2, block=64, scale="f16", P=16, B=2, maxp=4, paged=False, seed=42):
+def _setup(oracle, d=128, H=2, block=64, scale="f16", P=16, B=2, maxp=4, paged=False, seed=42, bits=3):
     s, q = oracle.rotation_params(d, seed)
     U = oracle.rotation_matrix(s, q)
     num_pages = B * maxp + (3 if paged else 0)
-    L = oracle.Layout(d, H, block, scale, P, B, maxp, num_pages)
+    L = oracle.Layout(d, H, block, scale, P, B, maxp, num_pages, bits)
     pool = np.zeros(L.pool_bytes, np.uint8)
     table = None
     if paged:
@@ -23,8 +23,9 @@ def _setup(oracle, d=128, H=2, block=64, scale="f16", P=16, B=2, maxp=4, paged=F
 
 @pytest.mark.parametrize("paged", [False, True])
 @pytest.mark.parametrize("scale", ["f32", "f16", "e4m3"])
-def test_write_read_roundtrip(oracle, paged, scale):
-    U, L, pool, table = _setup(oracle, scale=scale, paged=paged)
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_write_read_roundtrip(oracle, paged, scale, bits):
+    U, L, pool, table = _setup(oracle, scale=scale, paged=paged, bits=bits)
     rng = np.random.default_rng(0)
     n = 40
     k = (rng.standard_normal((n, 2, 128)) * 3).astype(np.float16)
@@ -39,7 +40,7 @@ def test_write_read_roundtrip(oracle, paged, scale):
             for which, src in ((0, k), (1, v)):
                 xh, c, sc = oracle.read_rotated(pool, L, b, h, which, p0, 20, table)
                 x = src[sel, h].astype(np.float64) @ U.T
-                c2, sq2, _ = oracle.quantize(x, 64, 1e-6, scale)
+                c2, sq2, _ = oracle.quantize(x, 64, 1e-6, scale, bits)
                 assert np.array_equal(c, c2) and np.array_equal(sc, sq2)
 
 
@@ -70,6 +71,25 @@ def test_layout_byte_positions(oracle):
     assert not np.any(pool[~touched])
 
 
+@pytest.mark.parametrize("bits", [2, 4])
+def test_layout_byte_positions_b24(oracle, bits):
+    # the b-bit code string of slot 1 sits b*d/8 bytes after slot 0's; one
+    # token at position 17 of sequence 1, kv head 1, V record, P = 16 (page 5)
+    U, L, pool, _ = _setup(oracle, scale="f32", P=16, bits=bits)
+    cb = bits * 128 // 8
+    assert L.code_bytes == cb and L.record_bytes == 16 * (2 * 4 + cb)
+    k = np.zeros((1, 2, 128), np.float16)
+    v = np.zeros((1, 2, 128), np.float16)
+    v[0, 1, 0] = 1.0
+    oracle.write(pool, L, U, k, v, np.array([1]), np.array([17]))
+    rec = 5 * L.page_bytes + (1 * 2 + 1) * L.record_bytes
+    codes = rec + 16 * 2 * 4 + 1 * cb
+    c, _, _ = oracle.quantize((U @ np.eye(128)[0])[None], 64, 1e-6, "f32", bits)
+    assert np.abs(c).max() == (1 << (bits - 1)) - 1
+    assert pool[codes:codes + cb].tobytes() == oracle.pack_codes(c, bits)[0].tobytes()
+    assert not pool[codes + cb:codes + 2 * cb].any() and not pool[codes - cb:codes].any()
+
+
 def test_write_status_bits(oracle):
     U, L, pool, table = _setup(oracle, paged=True)
     k = np.ones((5, 2, 128), np.float16)
@@ -89,9 +109,10 @@ def _fill(oracle, L, pool, U, table, lens, rng, kscale=3.0):
         oracle.write(pool, L, U, k, v, np.full(n, b), np.arange(n), table)
 
 
-def test_decode_single_token_returns_value(oracle):
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_decode_single_token_returns_value(oracle, bits):
     # N = 1: softmax weight 1, so o = U^T v_hat
-    U, L, pool, _ = _setup(oracle)
+    U, L, pool, _ = _setup(oracle, bits=bits)
     rng = np.random.default_rng(1)
     _fill(oracle, L, pool, U, None, [1, 1], rng)
     q = rng.standard_normal((2, 4, 128)).astype(np.float16)
@@ -185,6 +206,24 @@ def test_rotation_reduces_error_on_outlier_data(oracle):
         bmax[name] = np.abs(y).reshape(-1, 2, 64).max(-1).mean()
     assert errs["rotated"] < 0.85 * errs["none"] and errs["hadamard"] < 0.85 * errs["none"]
     assert bmax["hadamard"] < bmax["none"] / 2 and bmax["rotated"] < bmax["none"] / 2
+
+
+def test_error_falls_with_bit_width(oracle):
+    # "Orthogonal Invariance in Activation Space", 5.3: error falls from 2 to 3
+    # to 4 bits.  For the quantiser each extra bit roughly halves the step
+    # (divisors 1, 3, 7), so the MSE of the rotated outlier data falls by about
+    # (7/3)^2 and (3/1)^2 -- diagnostic on the seeded distribution.
+    spec = I.DataSpec(128, 1, 78, 0.03, 20.0)
+    x = I.kv_rows_np(spec, 0, 0, 0, 0, 512).astype(np.float64)
+    s, q = oracle.rotation_params(128, 42)
+    U = oracle.rotation_matrix(s, q)
+    y = x @ U.T
+    mse = {}
+    for bits in (2, 3, 4):
+        c, sq, _ = oracle.quantize(y, 64, 1e-6, "f32", bits)
+        yh = (c.reshape(-1, 2, 64) * sq[..., None]).reshape(y.shape)
+        mse[bits] = np.mean((yh @ U - x) ** 2)
+    assert mse[4] < mse[3] / 3 and mse[3] < mse[2] / 3
 
 
 # ---------------------------------------------------------------- prefill pins

@@ -317,3 +317,110 @@ def test_storage_accounting(oracle):
     # record sizes of the paged layout with 16-token pages, fp16 scales
     assert oracle.Layout(128, 1, 64, "f16", 16, 1, 1, 1).record_bytes == 832
     assert oracle.Layout(256, 1, 64, "f16", 16, 1, 1, 1).record_bytes == 1664
+
+
+# ------------------------------------------------------------- bit widths 2 and 4
+def _golden24():
+    rows = []
+    for line in open(os.path.join(HERE, "golden", "pack24_worked_examples.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        name, bits, d, codes, *hexb = line.split()
+        rows.append((name, int(bits), int(d), [int(t) for t in codes.split(",")], bytes.fromhex("".join(hexb))))
+    return rows
+
+
+def test_pack24_worked_examples(oracle):
+    rows = _golden24()
+    assert {r[1] for r in rows} == {2, 4}
+    for name, bits, d, group, b in rows:
+        codes = np.array(group * (d // 8), dtype=np.int8)[None]
+        assert oracle.pack_codes(codes, bits)[0].tobytes() == b * (d // 8), name
+        assert np.array_equal(oracle.unpack_codes(np.frombuffer(b * (d // 8), np.uint8)[None], d, bits), codes), name
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_unit_vector_writes_all_qmax(oracle, bits):
+    golden = dict((r[0], r[4]) for r in _golden24())
+    for sgn, name in ((1, f"unit_e0_{bits}"), (-1, f"unit_minus_e0_{bits}")):
+        s, q = oracle.rotation_params(128, 42, False, False)
+        U = oracle.rotation_matrix(s, q)
+        c, sq, _ = oracle.quantize((U @ (sgn * np.eye(128)[0]))[None], 64, 1e-6, "f32", bits)
+        assert np.all(c == sgn * ((1 << (bits - 1)) - 1))
+        assert oracle.pack_codes(c, bits)[0].tobytes() == golden[name] * 16
+
+
+def test_quantiser_b24_hand_examples(oracle):
+    # b = 4: block maximum 7 with eps = 0 gives s = 7/7 = 1; 3.5 rounds half to even (4)
+    x = np.zeros((1, 32))
+    x[0, :5] = [7.0, 3.5, -1.0, 0.0, -2.5]
+    c, sq, s = oracle.quantize(x, 32, 0.0, "f32", 4)
+    assert s[0, 0] == 1.0 and sq[0, 0] == 1.0
+    assert list(c[0, :5]) == [7, 4, -1, 0, -2]
+    # b = 2: divisor 1, so s is the block maximum itself: 2 -> x/s = 1, .25, -.75, .5, .2
+    x = np.zeros((1, 32))
+    x[0, :5] = [2.0, 0.5, -1.5, 1.0, 0.4]
+    c, sq, s = oracle.quantize(x, 32, 0.0, "f32", 2)
+    assert s[0, 0] == 2.0 and list(c[0, :5]) == [1, 0, -1, 0, 0]
+    with pytest.raises(ValueError):
+        oracle.quantize(x, 32, 0.0, "f32", 5)
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("kind", ["f32", "f16", "e4m3"])
+def test_quantiser_error_bound_b24(oracle, bits, kind):
+    # |x - s_q c| <= s_q / 2 wherever |x/s_q| <= qmax + 1/2, codes in [-qmax, qmax]
+    qm = (1 << (bits - 1)) - 1
+    rng = np.random.default_rng(bits)
+    x = rng.standard_normal((300, 128)) * np.exp(rng.uniform(-3, 3, (300, 1)))
+    c, sq, s = oracle.quantize(x, 64, 1e-6, kind, bits)
+    assert c.min() >= -qm and c.max() <= qm
+    xb = x.reshape(300, -1, 64)
+    assert np.allclose(s, (np.abs(xb).max(-1) + 1e-6) / qm, rtol=1e-15)
+    err = np.abs(xb - sq[..., None] * c.reshape(xb.shape))
+    inside = np.abs(xb) <= (qm + 0.5) * sq[..., None]
+    assert np.all(err[inside] <= sq[..., None].repeat(64, -1)[inside] / 2 * (1 + 1e-12))
+    if kind == "f32":   # the block's extreme element lands on +-qmax
+        amax = np.argmax(np.abs(xb), axis=-1)
+        cm = np.take_along_axis(c.reshape(xb.shape), amax[..., None], -1)[..., 0]
+        assert np.all(np.abs(cm) == qm)
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_pack_b24_exhaustive_roundtrip(oracle, bits):
+    # every b-bit value (including -2^(b-1), which the quantiser never writes)
+    # in every position of an 8-element group
+    n = 1 << bits
+    vals = np.arange(n) - n // 2
+    g = np.indices((n,) * (8 if bits == 2 else 4)).reshape(8 if bits == 2 else 4, -1).T
+    g = np.concatenate([g, g], axis=1)[:, :8] if bits == 4 else g
+    g = vals[g].astype(np.int8)
+    b = oracle.pack_codes(g, bits)
+    assert b.shape == (len(g), bits)
+    assert np.array_equal(oracle.unpack_codes(b, 8, bits), g)
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_pack_b24_bit_positions_bruteforce(oracle, bits):
+    qm = (1 << (bits - 1)) - 1
+    rng = np.random.default_rng(50 + bits)
+    for d in (8, 64, 128, 256):
+        c = rng.integers(-qm, qm + 1, (3, d)).astype(np.int8)
+        b = oracle.pack_codes(c, bits)
+        assert b.shape == (3, bits * d // 8)
+        for r in range(3):
+            acc = int.from_bytes(b[r].tobytes(), "little")
+            for j in range(d):
+                v = (acc >> (bits * j)) & ((1 << bits) - 1)
+                assert (v - (1 << bits) if v >= (1 << (bits - 1)) else v) == c[r, j]
+
+
+def test_storage_accounting_b24(oracle):
+    # "Orthogonal Invariance in Activation Space", 3.3: d*b bits of codes per
+    # vector; 4.2: 48 bytes of data for d = 128 at b = 3 (so 64 at b = 4, 32 at b = 2)
+    for bits, cb in ((2, 32), (3, 48), (4, 64)):
+        L = oracle.Layout(128, 1, 64, "f16", 16, 1, 1, 1, bits)
+        assert L.code_bytes == cb
+        assert L.record_bytes == 16 * (2 * 2 + cb)
+        assert 8 * L.record_bytes / (16 * 128) == bits + 0.25
