@@ -30,6 +30,7 @@ struct RotParams {
 // Cache geometry derived on the host from kvq3_cache_desc.
 struct CacheGeom {
   int32_t d, hkv, block, nb, sb, cb, page_size, batch, max_pages;
+  int32_t bits;             // code width b: 2, 3 or 4
   int32_t scale_type;
   float eps;
   int64_t num_pages;

@@ -10,11 +10,17 @@ using namespace kvq3;
 
 namespace {
 
+#define KVQ3_BY_BITS(D, SN, FN, ...)                               \
+  switch (g.bits) {                                                \
+    case 2: return FN##_d##D##_##SN##_b2(__VA_ARGS__);             \
+    case 4: return FN##_d##D##_##SN##_b4(__VA_ARGS__);             \
+    default: return FN##_d##D##_##SN##_b3(__VA_ARGS__);            \
+  }
 #define KVQ3_BY_SCALE(D, FN, ...)                                  \
   switch (g.scale_type) {                                          \
-    case KVQ3_SCALE_F32: return FN##_d##D##_f32(__VA_ARGS__);      \
-    case KVQ3_SCALE_F16: return FN##_d##D##_f16(__VA_ARGS__);      \
-    default: return FN##_d##D##_e4m3(__VA_ARGS__);                 \
+    case KVQ3_SCALE_F32: KVQ3_BY_BITS(D, f32, FN, __VA_ARGS__)     \
+    case KVQ3_SCALE_F16: KVQ3_BY_BITS(D, f16, FN, __VA_ARGS__)     \
+    default: KVQ3_BY_BITS(D, e4m3, FN, __VA_ARGS__)                \
   }
 
 kvq3_status plan_for(const CacheGeom& g, int G, DecodePlan* plan) {
@@ -126,7 +132,7 @@ kvq3_status kvq3_prefill_attn(kvq3_rotation rot, const kvq3_cache_desc* desc,
   if (!workspace || ws_bytes < plan.ws_bytes || reinterpret_cast<uintptr_t>(workspace) % 256)
     return KVQ3_ERR_WORKSPACE;
   const double qks = (sm_scale > 0.0f ? (double)sm_scale : 1.0 / sqrt((double)vg.d)) * 1.4426950408889634;
-  if (vg.d == 128) {
+  if (vg.d == 128 && vg.bits == 3) {
     // shared dequantised tiles: each K/V tile is unpacked once for 64 query rows
     CacheGeom g;
     make_geom(desc, &g);

@@ -195,48 +195,76 @@ __device__ __forceinline__ uint32_t hsub2_bits(uint32_t a, uint32_t b) {
   return *reinterpret_cast<uint32_t*>(&x);
 }
 
-// ---- codes -> fp16, as subnormal halves.  A 3-bit field u placed at mantissa
-// bit k of a half with a zero exponent is the exact fp16 value u * 2^(k-24).
-// With the field's sign bit flipped, u = c + 4 (c the two's-complement code),
-// so the half is (c + 4) 2^(k-24): the power of two is folded into q1 (keys) or
-// the output (values), and the +4 offset is either removed per half (values)
-// or, for keys, becomes the per-block constant 4 * sum_d 2^k_d q1_d that seeds
-// the logit accumulators (so the key path is one mask per half2).
-//
-// Sign-bit patterns: bits 3i+2 of a code string after a right shift by o sit
-// at positions congruent to (2 - o) mod 3.
-constexpr uint32_t kSignRes0 = 0x49249249u;   // positions 0, 3, 6, ...
-constexpr uint32_t kSignRes2 = 0x24924924u;   // positions 2, 5, 8, ...
+// ---- codes -> fp16, as subnormal halves.  A b-bit field u placed at
+// mantissa bit k of a half with a zero exponent is the exact fp16 value
+// u * 2^(k-24).  With the field's sign bit flipped, u = c + 2^(b-1) (c the
+// two's-complement code), so the half is (c + 2^(b-1)) 2^(k-24): the power of
+// two is folded into q1 (keys) or the output (values), and the offset is
+// either removed per half (values) or, for keys, becomes the per-block
+// constant 2^(b-1) * sum_d 2^k_d q1_d that seeds the logit accumulators (so
+// the key path is one mask per half2).
 
 // Key pairs: a lane's FQ consecutive fields (FQ = 16 or 8; field 0 at bit 0 of
-// the 64-bit window lo:hi) -> FQ/2 half2 values.  Pair P cuts the window
-// (lo:hi) >> o(P) and keeps field fl(P) at mantissa bit kl(P) of the low half
-// and field fh(P) at bit kh(P) of the high half: 3 fl - o = kl and
-// 3 fh - o - 16 = kh.  The pairings use four shifted windows for 16 fields
+// the 64-bit window lo:hi) -> FQ/2 half2 values, each holding field fl(P) at
+// mantissa bit kl(P) of the low half and field fh(P) at bit kh(P) of the high
+// half (a b-bit field at bit k of a half with a zero exponent needs
+// k + b <= 10).
+//
+// 3-bit fields: pair P cuts the window (lo:hi) >> o(P), so 3 fl - o = kl and
+// 3 fh - o - 16 = kh; the pairings use four shifted windows for 16 fields
 // (found by exhaustive search over window offsets) and two for 8.
-//                                                 P:  0   1  2   3   4   5   6   7
-__host__ __device__ constexpr int kp_o(int FQ, int P) {
+//                                                  P:  0   1  2   3   4   5   6   7
+__host__ __device__ constexpr int kp3_o(int FQ, int P) {
   return FQ == 16 ? (P == 0 ? -7 : P == 1 ? -4 : P == 2 ? 0 : P < 5 ? 14 : 23)
                   : (P < 2 ? -4 : P == 2 ? 0 : 2);
 }
-__host__ __device__ constexpr int kp_fl(int FQ, int P) {
+__host__ __device__ constexpr int kp3_fl(int FQ, int P) {
   return FQ == 16 ? (P == 0 ? 0 : P == 1 ? 1 : P == 2 ? 2 : P == 3 ? 5 : P + 3) : P;
 }
-__host__ __device__ constexpr int kp_fh(int FQ, int P) {
+__host__ __device__ constexpr int kp3_fh(int FQ, int P) {
   return FQ == 16 ? (P == 0 ? 3 : P == 1 ? 4 : P == 2 ? 6 : P + 8) : P + 4;
 }
-__host__ __device__ constexpr int kp_kl(int FQ, int P) { return 3 * kp_fl(FQ, P) - kp_o(FQ, P); }
-__host__ __device__ constexpr int kp_kh(int FQ, int P) { return 3 * kp_fh(FQ, P) - kp_o(FQ, P) - 16; }
-__host__ __device__ constexpr bool kp_valid(int FQ) {
+// 4-bit fields: word w = P/4 of the window holds fields 8w..8w+7 at nibbles;
+// pair P = (8w + a, 8w + a + 4), a = P % 4, from the word shifted right by 8
+// when a >= 2: both halves at bit 4 (a % 2).
+// 2-bit fields: byte pair g = P/4 holds fields 8g..8g+7; a byte permute puts
+// byte 2g in the low half and byte 2g+1 in the high half: pair P =
+// (8g + a, 8g + a + 4) at bit 2a of each half.
+__host__ __device__ constexpr int kp_fl(int NBIT, int FQ, int P) {
+  return NBIT == 3 ? kp3_fl(FQ, P) : 8 * (P / 4) + P % 4;
+}
+__host__ __device__ constexpr int kp_fh(int NBIT, int FQ, int P) {
+  return NBIT == 3 ? kp3_fh(FQ, P) : 8 * (P / 4) + P % 4 + 4;
+}
+__host__ __device__ constexpr int kp_kl(int NBIT, int FQ, int P) {
+  return NBIT == 3 ? 3 * kp3_fl(FQ, P) - kp3_o(FQ, P) : NBIT == 4 ? 4 * (P % 2) : 2 * (P % 4);
+}
+__host__ __device__ constexpr int kp_kh(int NBIT, int FQ, int P) {
+  return NBIT == 3 ? 3 * kp3_fh(FQ, P) - kp3_o(FQ, P) - 16 : kp_kl(NBIT, FQ, P);
+}
+__host__ __device__ constexpr bool kp_valid(int NBIT, int FQ) {
   unsigned seen = 0;
   for (int P = 0; P < FQ / 2; ++P) {
-    const int kl = kp_kl(FQ, P), kh = kp_kh(FQ, P), o = kp_o(FQ, P);
-    if (kl < 0 || kl > 7 || kh < 0 || kh > 7 || ((o % 3) + 3) % 3 == 1) return false;
-    seen |= (1u << kp_fl(FQ, P)) | (1u << kp_fh(FQ, P));
+    const int kl = kp_kl(NBIT, FQ, P), kh = kp_kh(NBIT, FQ, P);
+    if (kl < 0 || kl + NBIT > 10 || kh < 0 || kh + NBIT > 10) return false;
+    if (NBIT == 3 && ((kp3_o(FQ, P) % 3) + 3) % 3 == 1) return false;
+    seen |= (1u << kp_fl(NBIT, FQ, P)) | (1u << kp_fh(NBIT, FQ, P));
   }
-  return seen == (FQ == 32 ? ~0u : (1u << FQ) - 1u);
+  return seen == (1u << FQ) - 1u;
 }
-static_assert(kp_valid(16) && kp_valid(8), "key pair table must cover every field once");
+static_assert(kp_valid(3, 16) && kp_valid(3, 8) && kp_valid(4, 16) && kp_valid(4, 8) &&
+                  kp_valid(2, 16) && kp_valid(2, 8),
+              "key pair tables must cover every field once");
+
+// Sign bits of the fields, flipped so that a field reads c + 2^(b-1):
+// 3-bit: bits 3i+2 of a code string after a right shift by o sit at
+// positions congruent to (2 - o) mod 3; 4-bit: bit 3 of every nibble;
+// 2-bit: bit 1 of every bit pair (the shifts and byte permutes above keep
+// nibbles and bit pairs aligned).
+constexpr uint32_t kSignRes0 = 0x49249249u;   // positions 0, 3, 6, ...
+constexpr uint32_t kSignRes2 = 0x24924924u;   // positions 2, 5, 8, ...
+constexpr uint32_t kSign4 = 0x88888888u;
+constexpr uint32_t kSign2 = 0xAAAAAAAAu;
 
 // d = (a ^ s) & M in one LOP3 (M an immediate).
 template <uint32_t M>
@@ -246,36 +274,59 @@ __device__ __forceinline__ uint32_t xor_and(uint32_t a, uint32_t s) {
   return d;
 }
 
-// Pair P of a key chunk (lo, hi) as a subnormal half2 (c + 4) 2^(k - 24).
-// s0 / s2: the sign patterns kSignRes0 / kSignRes2 held in registers.
-template <int FQ, int P>
+// Pair P of a key chunk (lo, hi) as a subnormal half2 (c + 2^(b-1)) 2^(k - 24).
+// s0 / s2: the sign patterns (3-bit: kSignRes0 / kSignRes2; else both the
+// width's pattern) held in registers.
+template <int NBIT, int FQ, int P>
 __device__ __forceinline__ uint32_t k_pair(uint32_t lo, uint32_t hi, uint32_t s0, uint32_t s2) {
-  constexpr int o = kp_o(FQ, P);
-  uint32_t w;
-  if constexpr (o < 0) w = lo << (-o);
-  else if constexpr (o == 0) w = lo;
-  else w = __funnelshift_r(lo, hi, o);
-  constexpr uint32_t M = (7u << kp_kl(FQ, P)) | (7u << (16 + kp_kh(FQ, P)));
-  return xor_and<M>(w, ((o % 3) + 3) % 3 == 0 ? s2 : s0);
+  constexpr int kl = kp_kl(NBIT, FQ, P), kh = kp_kh(NBIT, FQ, P);
+  constexpr uint32_t F = (1u << NBIT) - 1u;
+  constexpr uint32_t M = (F << kl) | (F << (16 + kh));
+  if constexpr (NBIT == 3) {
+    constexpr int o = kp3_o(FQ, P);
+    uint32_t w;
+    if constexpr (o < 0) w = lo << (-o);
+    else if constexpr (o == 0) w = lo;
+    else w = __funnelshift_r(lo, hi, o);
+    return xor_and<M>(w, ((o % 3) + 3) % 3 == 0 ? s2 : s0);
+  } else if constexpr (NBIT == 4) {
+    const uint32_t w = (P < 4 ? lo : hi) >> ((P % 4) >= 2 ? 8 : 0);
+    return xor_and<M>(w, s0);
+  } else {
+    constexpr uint32_t sel = (P / 4) == 0 ? 0x1100u : 0x3322u;
+    return xor_and<M>(__byte_perm(lo, 0u, sel), s0);
+  }
 }
 
-// Value codes: fields f = 0..F-1 (F = 8 or 4) of two tokens' 3F-bit chunks
-// -> half2 (token0, token1) of field f, equal to c 2^(voff(f) - 24).
-__host__ __device__ constexpr int v_off(int f) {
-  return f == 0 ? 0 : f == 1 ? 3 : f == 2 ? 6 : f == 3 ? 1 : f == 4 ? 4 : f == 5 ? 7 : f == 6 ? 2 : 5;
+// Value codes: fields f = 0..F-1 (F = 8 or 4) of two tokens' chunks -> half2
+// (token0, token1) of field f, equal to c 2^(voff(f) - 24).
+//   3-bit: the byte permute takes bytes g, g+1 of each token's chunk (g = 0,
+//     1, 2 for fields 0-2, 3-5, 6-7); the sign bits of that half sit at the
+//     positions of kSignVg[g] (both halves).
+//   4-bit: byte f/2 of each chunk, field at bit 4 (f % 2).
+//   2-bit: byte f/4 of each chunk, field at bit 2 (f % 4).
+__host__ __device__ constexpr int v_off(int NBIT, int f) {
+  return NBIT == 4 ? 4 * (f % 2)
+       : NBIT == 2 ? 2 * (f % 4)
+       : (f == 0 ? 0 : f == 1 ? 3 : f == 2 ? 6 : f == 3 ? 1 : f == 4 ? 4 : f == 5 ? 7 : f == 6 ? 2 : 5);
 }
-
-// The byte permute takes bytes g, g+1 of each token's chunk (g = 0, 1, 2 for
-// fields 0-2, 3-5, 6-7); the sign bits of that half sit at the positions of
-// kSignVg[g] (both halves), flipped in the same LOP3 that masks the field.
 constexpr uint32_t kSignVg0 = 0x49244924u, kSignVg1 = 0x92499249u, kSignVg2 = 0x24922492u;
 
-template <int F>
+template <int NBIT, int F>
 __device__ __forceinline__ uint32_t v_field(uint32_t c0, uint32_t c1, uint32_t s0, uint32_t s1, uint32_t s2) {
-  constexpr uint32_t sel = F < 3 ? 0x5410u : (F < 6 ? 0x6521u : 0x7632u);
-  constexpr int o = v_off(F);
-  const uint32_t w = __byte_perm(c0, c1, sel);
-  return hsub2_bits(xor_and<(0x00070007u << o)>(w, F < 3 ? s0 : (F < 6 ? s1 : s2)), 0x00040004u << o);
+  constexpr int o = v_off(NBIT, F);
+  constexpr uint32_t FM = (1u << NBIT) - 1u;
+  constexpr uint32_t M = (FM << o) | (FM << (16 + o));
+  constexpr uint32_t OFS = (1u << (NBIT - 1)) * 0x00010001u << o;   // 2^(b-1) in both halves
+  if constexpr (NBIT == 3) {
+    constexpr uint32_t sel = F < 3 ? 0x5410u : (F < 6 ? 0x6521u : 0x7632u);
+    const uint32_t w = __byte_perm(c0, c1, sel);
+    return hsub2_bits(xor_and<M>(w, F < 3 ? s0 : (F < 6 ? s1 : s2)), OFS);
+  } else {
+    constexpr uint32_t g = NBIT == 4 ? F / 2 : F / 4;
+    constexpr uint32_t sel = g | (g << 4) | ((4 + g) << 8) | ((4 + g) << 12);
+    return hsub2_bits(xor_and<M>(__byte_perm(c0, c1, sel), s0), OFS);
+  }
 }
 
 // Bits [boff, boff + 64) of a code string (two aligned words, funnel shift).
@@ -448,7 +499,7 @@ __host__ __device__ constexpr int decode_min_blocks(int D, int GPAD) {
 // halves (PV n-tile = 4 heads x (hi, lo), like QK) -- needed when the value
 // scales are fp32, since p = 1 times an fp32 scale is not an fp16 value;
 // otherwise one fp16 value per head (PV n-tile = 8 heads).
-template <int D, int BLOCK, int GPAD, int SCALE, bool PSPLIT, bool PF = false>
+template <int D, int BLOCK, int GPAD, int SCALE, int NBIT, bool PSPLIT, bool PF = false>
 __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
     decode_split_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ RotParams rp) {
   constexpr int NB = D / BLOCK;
@@ -458,7 +509,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
   constexpr int NTP = PSPLIT ? NTQ : (GPAD + 7) / 8;  // PV n-tiles
   constexpr int FQ = BLOCK / 4;       // key fields per lane per block
   constexpr int FV = BLOCK / 8;       // value fields per lane per block
-  constexpr int CB = 3 * D / 8;
+  constexpr int CB = NBIT * D / 8;    // code bytes per token
   constexpr int EQ = D >= 128 ? D / 32 : 4;  // query rotation layout
   constexpr int LQ = D / EQ;
   constexpr int GPWQ = 32 / LQ;
@@ -559,16 +610,18 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
   // (token r, fields j*FQ.. of each block), value chunk (token 2j, fields
   // r*FV.. of each block) and their scales.  Block b's chunk lies 3*BLOCK/8
   // bytes after block 0's, at the same bit shift (3*BLOCK is a multiple of 32).
-  const uint32_t kshf = (uint32_t)(3 * j * FQ) & 31u, vshf = (uint32_t)(3 * r * FV) & 31u;
-  const uint32_t k_lane = HDR + (uint32_t)(r * CB) + ((uint32_t)(3 * j * FQ) >> 5) * 4u;
-  const uint32_t v_lane = REC + HDR + (uint32_t)(2 * j * CB) + ((uint32_t)(3 * r * FV) >> 5) * 4u;
+  const uint32_t kshf = (uint32_t)(NBIT * j * FQ) & 31u, vshf = (uint32_t)(NBIT * r * FV) & 31u;
+  const uint32_t k_lane = HDR + (uint32_t)(r * CB) + ((uint32_t)(NBIT * j * FQ) >> 5) * 4u;
+  const uint32_t v_lane = REC + HDR + (uint32_t)(2 * j * CB) + ((uint32_t)(NBIT * r * FV) >> 5) * 4u;
   const uint32_t ks_lane = (uint32_t)(r * BPT), vs_lane = REC + (uint32_t)(2 * j * BPT);
-  static_assert((3 * BLOCK) % 32 == 0, "block chunks must start on a word boundary");
-  constexpr int KBB = 3 * BLOCK / 8;   // bytes per block of a code string
+  static_assert((NBIT * BLOCK) % 32 == 0, "block chunks must start on a word boundary");
+  constexpr int KBB = NBIT * BLOCK / 8;   // bytes per block of a code string
+  constexpr int KBITS = NBIT * FQ, VBITS = NBIT * FV;   // bits of a lane's key / value chunk
 
   // sign-bit patterns of the key windows, kept in registers (one LOP3 per pair)
-  const uint32_t sgn0 = kSignRes0, sgn2 = kSignRes2;
-  const uint32_t vsg0 = kSignVg0, vsg1 = kSignVg1, vsg2 = kSignVg2;
+  constexpr uint32_t kSignB = NBIT == 4 ? kSign4 : kSign2;
+  const uint32_t sgn0 = NBIT == 3 ? kSignRes0 : kSignB, sgn2 = NBIT == 3 ? kSignRes2 : kSignB;
+  const uint32_t vsg0 = NBIT == 3 ? kSignVg0 : kSignB, vsg1 = kSignVg1, vsg2 = kSignVg2;
 
   // q1 fragments (B operand of QK^T): in registers for d = 128 with up to 8
   // heads per kv head (they are read by every MMA of the logit chain); in
@@ -664,7 +717,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
             for (int e = 0; e < 2; ++e) {      // row r (e = 0) or r + 8 (e = 1)
               const int f = 2 * mp + e;
               const int dim = b * BLOCK + r * FV + f;
-              const float sc = (float)(1 << (24 - v_off(f)));   // value halves are c 2^(voff-24)
+              const float sc = (float)(1 << (24 - v_off(NBIT, f)));   // value halves are c 2^(voff-24)
               if constexpr (PSPLIT) {
                 const int h = 4 * tp + j;
                 const float v = (acc[mt][tp][2 * e] + acc[mt][tp][2 * e + 1]) * sc * cpv[tp][0];
@@ -754,17 +807,17 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           const int P = 2 * sp + hf;
-          const int dlo = b * BLOCK + j * FQ + kp_fl(FQ, P);
-          const int dhi = b * BLOCK + j * FQ + kp_fh(FQ, P);
-          const float vlo = qs[head * D + dlo] * (1.0f / (float)(1 << kp_kl(FQ, P)));
-          const float vhi = qs[head * D + dhi] * (1.0f / (float)(1 << kp_kh(FQ, P)));
+          const int dlo = b * BLOCK + j * FQ + kp_fl(NBIT, FQ, P);
+          const int dhi = b * BLOCK + j * FQ + kp_fh(NBIT, FQ, P);
+          const float vlo = qs[head * D + dlo] * (1.0f / (float)(1 << kp_kl(NBIT, FQ, P)));
+          const float vhi = qs[head * D + dhi] * (1.0f / (float)(1 << kp_kh(NBIT, FQ, P)));
           const __half hlo = __float2half_rn(vlo), hhi = __float2half_rn(vhi);
           const float olo = part == 0 ? __half2float(hlo) : vlo - __half2float(hlo);
           const float ohi = part == 0 ? __half2float(hhi) : vhi - __half2float(hhi);
           q2[hf] = pack_half2(olo, ohi);
           // sum_d 2^k_d q1_d of the fp16 values the MMA sees (this lane's part)
           const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&q2[hf]));
-          csum[b] += f.x * (float)(1 << kp_kl(FQ, P)) + f.y * (float)(1 << kp_kh(FQ, P));
+          csum[b] += f.x * (float)(1 << kp_kl(NBIT, FQ, P)) + f.y * (float)(1 << kp_kh(NBIT, FQ, P));
         }
         if constexpr (QF_SMEM) {
           if (wid == 0) qf_s[(s * NTQ + tq) * 32 + lane] = make_uint2(q2[0], q2[1]);
@@ -783,7 +836,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
         t += __shfl_xor_sync(kFull, t, 1);
         t += __shfl_xor_sync(kFull, t, 2);
         t += __shfl_xor_sync(kFull, t, 4);
-        const float ko = -0x1p-22f * __shfl_sync(kFull, t, 8 * j);
+        const float ko = -(float)(1 << (NBIT - 1)) * 0x1p-24f * __shfl_sync(kFull, t, 8 * j);
         if constexpr (KOFS_REG) kofs[b][tq] = ko;
         else if (wid == 0 && r == 0) kofs_s[b * GPAD + 4 * tq + j] = ko;
       }
@@ -819,9 +872,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
 #pragma unroll
     for (int b = 0; b < NB; ++b)
 #pragma unroll
-      for (int tq = 0; tq < NTQ; ++tq)
-#pragma unroll
-      {
+      for (int tq = 0; tq < NTQ; ++tq) {
         accq[b][tq][0] = accq[b][tq][2] = 0.0f;
         accq[b][tq][1] = accq[b][tq][3] = KOFS_REG ? kofs[b % (KOFS_REG ? NB : 1)][tq % (KOFS_REG ? NTQ : 1)]
                                                    : kofs_s[b * GPAD + 4 * tq + j];   // lo column
@@ -829,17 +880,33 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
     const uint32_t kt = pg + (uint32_t)(t0 * CB) + k_lane;   // token t0 + r
     static_for<NB>([&](auto bc) {
       constexpr int b = decltype(bc)::value;
-      const uint32_t x0 = lds32<b * KBB>(kt), x1 = lds32<b * KBB + 4>(kt);
-      const uint32_t y0 = lds32<b * KBB + 8 * CB>(kt), y1 = lds32<b * KBB + 8 * CB + 4>(kt);
-      const uint32_t lo0 = __funnelshift_r(x0, x1, kshf), hi0 = x1 >> kshf;   // token r
-      const uint32_t lo8 = __funnelshift_r(y0, y1, kshf), hi8 = y1 >> kshf;   // token r + 8
+      // this lane's key chunks of tokens r and r + 8 as 64-bit windows lo:hi
+      uint32_t lo0, hi0 = 0, lo8, hi8 = 0;
+      if constexpr (KBITS % 32 == 0) {          // whole words (kshf = 0)
+        lo0 = lds32<b * KBB>(kt);
+        lo8 = lds32<b * KBB + 8 * CB>(kt);
+        if constexpr (KBITS > 32) {
+          hi0 = lds32<b * KBB + 4>(kt);
+          hi8 = lds32<b * KBB + 8 * CB + 4>(kt);
+        }
+      } else if constexpr (32 % KBITS == 0) {   // within one word
+        lo0 = lds32<b * KBB>(kt) >> kshf;
+        lo8 = lds32<b * KBB + 8 * CB>(kt) >> kshf;
+      } else {
+        const uint32_t x0 = lds32<b * KBB>(kt), x1 = lds32<b * KBB + 4>(kt);
+        const uint32_t y0 = lds32<b * KBB + 8 * CB>(kt), y1 = lds32<b * KBB + 8 * CB + 4>(kt);
+        lo0 = __funnelshift_r(x0, x1, kshf);
+        hi0 = x1 >> kshf;
+        lo8 = __funnelshift_r(y0, y1, kshf);
+        hi8 = y1 >> kshf;
+      }
       static_for<KSB>([&](auto spc) {
         constexpr int sp = decltype(spc)::value;
         uint32_t af[4];
-        af[0] = k_pair<FQ, 2 * sp>(lo0, hi0, sgn0, sgn2);
-        af[1] = k_pair<FQ, 2 * sp>(lo8, hi8, sgn0, sgn2);
-        af[2] = k_pair<FQ, 2 * sp + 1>(lo0, hi0, sgn0, sgn2);
-        af[3] = k_pair<FQ, 2 * sp + 1>(lo8, hi8, sgn0, sgn2);
+        af[0] = k_pair<NBIT, FQ, 2 * sp>(lo0, hi0, sgn0, sgn2);
+        af[1] = k_pair<NBIT, FQ, 2 * sp>(lo8, hi8, sgn0, sgn2);
+        af[2] = k_pair<NBIT, FQ, 2 * sp + 1>(lo0, hi0, sgn0, sgn2);
+        af[3] = k_pair<NBIT, FQ, 2 * sp + 1>(lo8, hi8, sgn0, sgn2);
         static_for<NTQ>([&](auto tqc) {
           constexpr int tq = decltype(tqc)::value;
           if constexpr (QF_SMEM) {
@@ -1034,18 +1101,26 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
     static_for<NB>([&](auto bc) {
       constexpr int b = decltype(bc)::value;
       constexpr int O = b * KBB;
-      // this lane's value chunks of tokens T0, T0+1, T0+8, T0+9
-      const uint32_t c0v = __funnelshift_r(lds32<O>(vt), lds32<O + 4>(vt), vshf);
-      const uint32_t c1v = __funnelshift_r(lds32<O + CB>(vt), lds32<O + CB + 4>(vt), vshf);
-      const uint32_t c2v = __funnelshift_r(lds32<O + 8 * CB>(vt), lds32<O + 8 * CB + 4>(vt), vshf);
-      const uint32_t c3v = __funnelshift_r(lds32<O + 9 * CB>(vt), lds32<O + 9 * CB + 4>(vt), vshf);
+      // this lane's value chunks of tokens T0, T0+1, T0+8, T0+9 (at bit 0)
+      uint32_t c0v, c1v, c2v, c3v;
+      if constexpr (32 % VBITS == 0) {   // a chunk never crosses a word
+        c0v = lds32<O>(vt) >> vshf;
+        c1v = lds32<O + CB>(vt) >> vshf;
+        c2v = lds32<O + 8 * CB>(vt) >> vshf;
+        c3v = lds32<O + 9 * CB>(vt) >> vshf;
+      } else {
+        c0v = __funnelshift_r(lds32<O>(vt), lds32<O + 4>(vt), vshf);
+        c1v = __funnelshift_r(lds32<O + CB>(vt), lds32<O + CB + 4>(vt), vshf);
+        c2v = __funnelshift_r(lds32<O + 8 * CB>(vt), lds32<O + 8 * CB + 4>(vt), vshf);
+        c3v = __funnelshift_r(lds32<O + 9 * CB>(vt), lds32<O + 9 * CB + 4>(vt), vshf);
+      }
       static_for<KSB>([&](auto mpc) {
         constexpr int mp = decltype(mpc)::value;
         uint32_t af[4];
-        af[0] = v_field<2 * mp>(c0v, c1v, vsg0, vsg1, vsg2);
-        af[1] = v_field<2 * mp + 1>(c0v, c1v, vsg0, vsg1, vsg2);
-        af[2] = v_field<2 * mp>(c2v, c3v, vsg0, vsg1, vsg2);
-        af[3] = v_field<2 * mp + 1>(c2v, c3v, vsg0, vsg1, vsg2);
+        af[0] = v_field<NBIT, 2 * mp>(c0v, c1v, vsg0, vsg1, vsg2);
+        af[1] = v_field<NBIT, 2 * mp + 1>(c0v, c1v, vsg0, vsg1, vsg2);
+        af[2] = v_field<NBIT, 2 * mp>(c2v, c3v, vsg0, vsg1, vsg2);
+        af[3] = v_field<NBIT, 2 * mp + 1>(c2v, c3v, vsg0, vsg1, vsg2);
 #pragma unroll
         for (int tp = 0; tp < NTP; ++tp) mma_16816(acc[b * KSB + mp][tp], af, pb[b][tp][0], pb[b][tp][1]);
       });
@@ -1255,10 +1330,10 @@ struct DecodePlan {
   size_t ws_bytes;
 };
 
-template <int D, int BLOCK, int GPAD, int SCALE, bool PSPLIT, bool PF = false>
+template <int D, int BLOCK, int GPAD, int SCALE, int NBIT, bool PSPLIT, bool PF = false>
 kvq3_status decode_plan_t(const CacheGeom& g, int G, DecodePlan* plan) {
   using SM = DecodeSmem<D, GPAD>;
-  const void* k = reinterpret_cast<const void*>(&decode_split_kernel<D, BLOCK, GPAD, SCALE, PSPLIT, PF>);
+  const void* k = reinterpret_cast<const void*>(&decode_split_kernel<D, BLOCK, GPAD, SCALE, NBIT, PSPLIT, PF>);
   plan->gpad = GPAD;
   // the SM's 228 KB of shared memory split over the CTAs that the register
   // budget lets reside (1 KB of it reserved per CTA)
@@ -1305,7 +1380,7 @@ kvq3_status decode_plan_t(const CacheGeom& g, int G, DecodePlan* plan) {
   return KVQ3_OK;
 }
 
-template <int D, int BLOCK, int GPAD, int SCALE, bool PSPLIT, bool PF = false>
+template <int D, int BLOCK, int GPAD, int SCALE, int NBIT, bool PSPLIT, bool PF = false>
 kvq3_status decode_run_t(const DecodePlan& plan, DecodeParams prm, const RotParams& rp, float* out,
                          cudaStream_t st) {
   prm.stages = plan.stages;
@@ -1313,7 +1388,7 @@ kvq3_status decode_run_t(const DecodePlan& plan, DecodeParams prm, const RotPara
   prm.chunk_tokens = plan.chunk_tokens;
   prm.pages_per_chunk = plan.pages_per_chunk;
   prm.ctas = plan.ctas;
-  decode_split_kernel<D, BLOCK, GPAD, SCALE, PSPLIT, PF><<<plan.ctas, 32 * kWarps, plan.smem, st>>>(prm, rp);
+  decode_split_kernel<D, BLOCK, GPAD, SCALE, NBIT, PSPLIT, PF><<<plan.ctas, 32 * kWarps, plan.smem, st>>>(prm, rp);
   if (cudaGetLastError() != cudaSuccess) return KVQ3_ERR_CUDA;
   const int64_t items = (int64_t)(prm.pf_n > 0 ? prm.pf_n : prm.g.batch) * prm.Hq;
   int64_t blocks = (items + 7) / 8;
@@ -1335,50 +1410,54 @@ kvq3_status decode_run_t(const DecodePlan& plan, DecodeParams prm, const RotPara
   return cudaGetLastError() == cudaSuccess ? KVQ3_OK : KVQ3_ERR_CUDA;
 }
 
-// Per-(head dim, scale type) entry points, one translation unit each.
-#define KVQ3_DECODE_DECL(D, SN)                                                               \
-  kvq3_status decode_plan_d##D##_##SN(const CacheGeom& g, int G, DecodePlan* plan);          \
-  kvq3_status decode_run_d##D##_##SN(const DecodePlan&, const DecodeParams&, const RotParams&, \
-                                     float*, cudaStream_t);                                   \
-  kvq3_status prefill_plan_d##D##_##SN(const CacheGeom& g, int G, DecodePlan* plan);         \
-  kvq3_status prefill_run_d##D##_##SN(const DecodePlan&, const DecodeParams&, const RotParams&, \
-                                      float*, cudaStream_t);
+// Per-(head dim, scale type, code width) entry points, one translation unit each.
+#define KVQ3_DECODE_DECL1(D, SN, NB)                                                          \
+  kvq3_status decode_plan_d##D##_##SN##_b##NB(const CacheGeom& g, int G, DecodePlan* plan);  \
+  kvq3_status decode_run_d##D##_##SN##_b##NB(const DecodePlan&, const DecodeParams&,          \
+                                             const RotParams&, float*, cudaStream_t);         \
+  kvq3_status prefill_plan_d##D##_##SN##_b##NB(const CacheGeom& g, int G, DecodePlan* plan); \
+  kvq3_status prefill_run_d##D##_##SN##_b##NB(const DecodePlan&, const DecodeParams&,         \
+                                              const RotParams&, float*, cudaStream_t);
+#define KVQ3_DECODE_DECL(D, SN) KVQ3_DECODE_DECL1(D, SN, 2) KVQ3_DECODE_DECL1(D, SN, 3) KVQ3_DECODE_DECL1(D, SN, 4)
 KVQ3_DECODE_DECL(64, f32) KVQ3_DECODE_DECL(64, f16) KVQ3_DECODE_DECL(64, e4m3)
 KVQ3_DECODE_DECL(128, f32) KVQ3_DECODE_DECL(128, f16) KVQ3_DECODE_DECL(128, e4m3)
 KVQ3_DECODE_DECL(256, f32) KVQ3_DECODE_DECL(256, f16) KVQ3_DECODE_DECL(256, e4m3)
 
-// P' split for fp32 value scales only.
-#define KVQ3_DECODE_PICK(D, BLK, SC, FN, ...)                                                 \
+// P' split into hi + lo halves for fp32 value scales (p times an fp32 scale is
+// not an fp16 value) and for up to 4 heads per kv head, where the split
+// columns fit the same 8-column PV tile (no extra MMAs) and remove the fp16
+// rounding of P' from the error.
+#define KVQ3_DECODE_PICK(D, BLK, SC, NB, FN, ...)                                             \
   {                                                                                           \
     constexpr bool SPLIT = (SC) == KVQ3_SCALE_F32;                                            \
-    if (gp == 4) return FN<D, BLK, 4, SC, SPLIT>(__VA_ARGS__);                                \
-    if (gp == 8) return FN<D, BLK, 8, SC, SPLIT>(__VA_ARGS__);                                \
-    return FN<D, BLK, 16, SC, SPLIT>(__VA_ARGS__);                                            \
+    if (gp == 4) return FN<D, BLK, 4, SC, NB, true>(__VA_ARGS__);                             \
+    if (gp == 8) return FN<D, BLK, 8, SC, NB, SPLIT>(__VA_ARGS__);                            \
+    return FN<D, BLK, 16, SC, NB, SPLIT>(__VA_ARGS__);                                        \
   }
 
-#define KVQ3_DECODE_INSTANCES(D, SN, SC)                                                      \
-  kvq3_status decode_plan_d##D##_##SN(const CacheGeom& g, int G, DecodePlan* plan) {         \
+#define KVQ3_DECODE_INSTANCES(D, SN, SC, NB)                                                  \
+  kvq3_status decode_plan_d##D##_##SN##_b##NB(const CacheGeom& g, int G, DecodePlan* plan) { \
     const int gp = G <= 4 ? 4 : (G <= 8 ? 8 : 16);                                            \
-    if (g.block == 32) KVQ3_DECODE_PICK(D, 32, SC, decode_plan_t, g, G, plan)                 \
-    KVQ3_DECODE_PICK(D, 64, SC, decode_plan_t, g, G, plan)                                    \
+    if (g.block == 32) KVQ3_DECODE_PICK(D, 32, SC, NB, decode_plan_t, g, G, plan)             \
+    KVQ3_DECODE_PICK(D, 64, SC, NB, decode_plan_t, g, G, plan)                                \
   }                                                                                           \
-  kvq3_status decode_run_d##D##_##SN(const DecodePlan& plan, const DecodeParams& prm,         \
-                                     const RotParams& rp, float* out, cudaStream_t st) {      \
+  kvq3_status decode_run_d##D##_##SN##_b##NB(const DecodePlan& plan, const DecodeParams& prm, \
+                                             const RotParams& rp, float* out, cudaStream_t st) { \
     const int gp = plan.gpad;                                                                 \
-    if (prm.g.block == 32) KVQ3_DECODE_PICK(D, 32, SC, decode_run_t, plan, prm, rp, out, st)  \
-    KVQ3_DECODE_PICK(D, 64, SC, decode_run_t, plan, prm, rp, out, st)                         \
+    if (prm.g.block == 32) KVQ3_DECODE_PICK(D, 32, SC, NB, decode_run_t, plan, prm, rp, out, st) \
+    KVQ3_DECODE_PICK(D, 64, SC, NB, decode_run_t, plan, prm, rp, out, st)                     \
   }                                                                                           \
   /* chunked prefill: 8 logit columns = query tokens x a block of query heads of a kv head, \
      with P' split into hi + lo halves (the many outputs of a prefill chunk leave the  \
      single fp16 rounding of P' too close to the tolerance) */                         \
-  kvq3_status prefill_plan_d##D##_##SN(const CacheGeom& g, int G, DecodePlan* plan) {        \
-    if (g.block == 32) return decode_plan_t<D, 32, 8, SC, true, true>(g, G, plan);            \
-    return decode_plan_t<D, 64, 8, SC, true, true>(g, G, plan);                               \
+  kvq3_status prefill_plan_d##D##_##SN##_b##NB(const CacheGeom& g, int G, DecodePlan* plan) { \
+    if (g.block == 32) return decode_plan_t<D, 32, 8, SC, NB, true, true>(g, G, plan);        \
+    return decode_plan_t<D, 64, 8, SC, NB, true, true>(g, G, plan);                           \
   }                                                                                           \
-  kvq3_status prefill_run_d##D##_##SN(const DecodePlan& plan, const DecodeParams& prm,        \
-                                      const RotParams& rp, float* out, cudaStream_t st) {     \
-    if (prm.g.block == 32) return decode_run_t<D, 32, 8, SC, true, true>(plan, prm, rp, out, st); \
-    return decode_run_t<D, 64, 8, SC, true, true>(plan, prm, rp, out, st);                    \
+  kvq3_status prefill_run_d##D##_##SN##_b##NB(const DecodePlan& plan, const DecodeParams& prm, \
+                                              const RotParams& rp, float* out, cudaStream_t st) { \
+    if (prm.g.block == 32) return decode_run_t<D, 32, 8, SC, NB, true, true>(plan, prm, rp, out, st); \
+    return decode_run_t<D, 64, 8, SC, NB, true, true>(plan, prm, rp, out, st);                \
   }
 
 }  // namespace kvq3

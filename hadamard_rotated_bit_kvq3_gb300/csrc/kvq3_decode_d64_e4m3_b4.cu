@@ -1,0 +1,9 @@
+// Decode-attention kernels for head dimension 64, e4m3 scales and 4-bit codes
+// (both block sizes, all GQA group paddings, the chunked-prefill variant); one
+// translation unit per (head dimension, scale type, code width) for a
+// parallel build.
+#include "kvq3_decode.cuh"
+
+namespace kvq3 {
+KVQ3_DECODE_INSTANCES(64, e4m3, KVQ3_SCALE_E4M3, 4)
+}  // namespace kvq3

@@ -84,14 +84,15 @@ kvq3_status make_geom(const kvq3_cache_desc* desc, CacheGeom* g) {
       !(desc->eps >= 0.0f) || !isfinite(desc->eps) || desc->block < 1 || d % desc->block != 0 ||
       desc->scale_type < KVQ3_SCALE_F32 || desc->scale_type > KVQ3_SCALE_E4M3)
     return KVQ3_ERR_INVALID_ARG;
-  if (desc->bits != 3) return KVQ3_ERR_UNSUPPORTED;
+  if (desc->bits < 2 || desc->bits > 4) return KVQ3_ERR_UNSUPPORTED;
   if (d < 64 || (desc->block != 32 && desc->block != 64)) return KVQ3_ERR_UNSUPPORTED;
   g->d = d;
   g->hkv = desc->num_kv_heads;
   g->block = desc->block;
   g->nb = d / desc->block;
   g->sb = desc->scale_type == KVQ3_SCALE_F32 ? 4 : desc->scale_type == KVQ3_SCALE_F16 ? 2 : 1;
-  g->cb = 3 * d / 8;
+  g->bits = desc->bits;
+  g->cb = desc->bits * d / 8;
   g->page_size = desc->page_size;
   g->batch = desc->batch;
   g->max_pages = desc->max_pages_per_seq;

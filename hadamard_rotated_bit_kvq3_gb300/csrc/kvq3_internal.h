@@ -16,7 +16,7 @@ struct kvq3_rotation_s {
 namespace kvq3 {
 
 // Validates a cache description for the cache kernels (d in {64,128,256},
-// block in {32,64}, bits 3, ...) and derives the geometry.
+// block in {32,64}, bits in {2,3,4}, ...) and derives the geometry.
 kvq3_status make_geom(const kvq3_cache_desc* desc, CacheGeom* g);
 
 // Validates the device buffers of a cache against its geometry.

@@ -4,7 +4,9 @@
 // token compute k1 = U(k), v1 = U(v), split into quantisation blocks, one
 // scale per block, round to signed 3-bit integers, pack the codes into bytes,
 // store only packed codes and scales.  Key formulas: s = (max|x| + eps)/3,
-// x_hat = s * clip(round(x/s), -3, 3).  "Orthogonal Invariance in Activation
+// x_hat = s * clip(round(x/s), -3, 3) -- for b-bit codes (b = 2, 3, 4;
+// "Orthogonal Invariance in Activation Space", 3.3, 4.2, 5.1) the divisor and
+// the clip bound are 2^(b-1) - 1.  "Orthogonal Invariance in Activation
 // Space", 3.3 "Retrieve" for the read-back.
 //
 // One group of L = D/E lanes handles one (token, kv head, K|V) vector, E
@@ -12,8 +14,8 @@
 // the sign flip, the Walsh-Hadamard butterfly (log2 E register stages, log2 L
 // shuffle stages), 1/sqrt(d), the SO(4) 4x4 products in registers, the block
 // maximum by an xor-shuffle reduction, the scale rounded to its storage type,
-// the codes, and the 3-bit words of the code string assembled by shuffles
-// and stored by the first 3D/32 lanes of the group.
+// the codes, and the 32-bit words of the code string assembled by shuffles
+// and stored by the first NBIT*D/32 lanes of the group.
 #include <string.h>
 
 #include "kvq3_internal.h"
@@ -22,7 +24,7 @@ using namespace kvq3;
 
 namespace {
 
-template <int D, int E, int BLOCK>
+template <int D, int E, int BLOCK, int NBIT>
 __global__ void __launch_bounds__(256) write_kernel(
     const __grid_constant__ RotParams rp, const __grid_constant__ CacheGeom g,
     uint8_t* __restrict__ pool, const int32_t* __restrict__ page_table,
@@ -32,8 +34,9 @@ __global__ void __launch_bounds__(256) write_kernel(
   constexpr int L = D / E;            // lanes per vector
   constexpr int GPW = 32 / L;         // vectors per warp
   constexpr int LPB = BLOCK / E;      // lanes per quantisation block
-  constexpr int BITS = 3 * E;         // code bits per lane
-  constexpr int WORDS = 3 * D / 32;   // 32-bit words of a code string
+  constexpr int BITS = NBIT * E;      // code bits per lane
+  constexpr int WORDS = NBIT * D / 32;  // 32-bit words of a code string
+  constexpr int QMAX = (1 << (NBIT - 1)) - 1;
   static_assert(E <= BLOCK && BITS <= 32 && WORDS <= L, "lane layout");
   const int lane = threadIdx.x & 31;
   const int r = lane % L, grp = lane / L;
@@ -119,15 +122,15 @@ __global__ void __launch_bounds__(256) write_kernel(
     for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(x[e]));
 #pragma unroll
     for (int m = 1; m < LPB; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, m));
-    const float s = __fdiv_rn(amax + g.eps, 3.0f);
+    const float s = __fdiv_rn(amax + g.eps, (float)QMAX);
     uint32_t sbits;
     const float sq = round_scale(s, g.scale_type, sbits);
     const float inv = sq > 0.0f ? __frcp_rn(sq) : 0.0f;
     uint32_t bits = 0;
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-      const float c = fminf(fmaxf(rintf(x[e] * inv), -3.0f), 3.0f);
-      bits |= ((uint32_t)(int)c & 7u) << (3 * e);
+      const float c = fminf(fmaxf(rintf(x[e] * inv), -(float)QMAX), (float)QMAX);
+      bits |= ((uint32_t)(int)c & ((1u << NBIT) - 1u)) << (NBIT * e);
     }
     // word w of the code string collects bits [32w, 32w+32) from the lanes
     // whose [BITS*r, BITS*r + BITS) ranges overlap it
@@ -157,10 +160,10 @@ __global__ void __launch_bounds__(256) write_kernel(
   }
 }
 
-template <int D, int BLOCK>
-cudaError_t launch_write(const RotParams& rp, const CacheGeom& g, const kvq3_cache* c,
-                         const __half* k, const __half* v, const int32_t* si, const int32_t* pos,
-                         int64_t n_tok, int32_t* st, cudaStream_t stream) {
+template <int D, int BLOCK, int NBIT>
+cudaError_t launch_write_b(const RotParams& rp, const CacheGeom& g, const kvq3_cache* c,
+                           const __half* k, const __half* v, const int32_t* si, const int32_t* pos,
+                           int64_t n_tok, int32_t* st, cudaStream_t stream) {
   constexpr int E = D >= 128 ? D / 32 : 4;
   constexpr int GPW = 32 / (D / E);
   const int64_t items = 2 * n_tok * g.hkv;
@@ -168,10 +171,19 @@ cudaError_t launch_write(const RotParams& rp, const CacheGeom& g, const kvq3_cac
   int64_t blocks = (warps + 7) / 8;
   const int64_t cap = (int64_t)sm_count() * 8;
   if (blocks > cap) blocks = cap > 0 ? cap : 1;
-  write_kernel<D, E, BLOCK><<<(unsigned)blocks, 256, 0, stream>>>(
+  write_kernel<D, E, BLOCK, NBIT><<<(unsigned)blocks, 256, 0, stream>>>(
       rp, g, static_cast<uint8_t*>(c->pool), c->page_table, k, v, si, pos, n_tok, st,
       inv_sqrt(D));
   return cudaGetLastError();
+}
+
+template <int D, int BLOCK>
+cudaError_t launch_write(const RotParams& rp, const CacheGeom& g, const kvq3_cache* c,
+                         const __half* k, const __half* v, const int32_t* si, const int32_t* pos,
+                         int64_t n_tok, int32_t* st, cudaStream_t stream) {
+  if (g.bits == 2) return launch_write_b<D, BLOCK, 2>(rp, g, c, k, v, si, pos, n_tok, st, stream);
+  if (g.bits == 4) return launch_write_b<D, BLOCK, 4>(rp, g, c, k, v, si, pos, n_tok, st, stream);
+  return launch_write_b<D, BLOCK, 3>(rp, g, c, k, v, si, pos, n_tok, st, stream);
 }
 
 // ------------------------------------------------------------ read-back
@@ -219,14 +231,15 @@ __global__ void __launch_bounds__(256) dequant_kernel(
         uint32_t sbits = 0;
         for (int i = 0; i < g.sb; ++i) sbits |= (uint32_t)sp[i] << (8 * i);
         const float sq = decode_scale(sbits, g.scale_type);
+        const int nbit = g.bits, half = 1 << (nbit - 1);
 #pragma unroll
         for (int e = 0; e < E; ++e) {
-          const int bit = 3 * (r * E + e);
+          const int bit = nbit * (r * E + e);
           const uint32_t two = (uint32_t)codes[bit / 8] |
                                ((bit / 8 + 1 < g.cb) ? (uint32_t)codes[bit / 8 + 1] << 8 : 0u);
-          const int f = (int)((two >> (bit % 8)) & 7u);
-          int cv = f >= 4 ? f - 8 : f;
-          if (cv == -4) {
+          const int f = (int)((two >> (bit % 8)) & ((1u << nbit) - 1u));
+          int cv = f >= half ? f - 2 * half : f;
+          if (cv == -half) {   // the value the quantiser never writes
             bad |= KVQ3_DEV_BAD_CODE;
             cv = 0;
           }

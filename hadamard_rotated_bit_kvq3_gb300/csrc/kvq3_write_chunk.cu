@@ -16,8 +16,9 @@
 //    SO(4) blocks with the quaternion pairs of blocks i and i + d/8 packed;
 //  * 1/sqrt(d) is folded into the block maximum and the reciprocal scale;
 //  * codes by one fused multiply-add against the 1.5*2^23 rounding constant
-//    (round half to even), packed in-thread into 32-bit words, stored with
-//    16-byte stores.
+//    (round half to even), packed in-thread into 32-bit words (b-bit codes,
+//    b = 2, 3, 4: divisor and clip bound 2^(b-1) - 1), stored with 16-byte
+//    stores.
 #include <string.h>
 
 #include "kvq3_internal.h"
@@ -88,13 +89,14 @@ __device__ __forceinline__ TileId tile_id(const ChunkParams& p, uint32_t tile) {
   return id;
 }
 
-template <int D, int BLOCK, int SCALE, bool SO4>
+template <int D, int BLOCK, int SCALE, bool SO4, int NBIT>
 __global__ void __launch_bounds__(kTile) write_chunk_kernel(const __grid_constant__ ChunkParams p) {
   constexpr int H = D / 2;              // register pairs: x2[k] = (x[k], x[k + H])
   constexpr int ROWB = 2 * D;           // bytes per input row
   constexpr int PIECES = ROWB / 16;     // 16-byte pieces per row (8 or 16)
   constexpr int NB = D / BLOCK;
-  constexpr int CB = 3 * D / 8;         // code bytes (24 or 48)
+  constexpr int CB = NBIT * D / 8;      // code bytes (16 .. 64)
+  constexpr int QMAX = (1 << (NBIT - 1)) - 1;
   constexpr int SB = SCALE == KVQ3_SCALE_F32 ? 4 : SCALE == KVQ3_SCALE_F16 ? 2 : 1;
   extern __shared__ __align__(128) uint8_t smem[];
   const int t = threadIdx.x;
@@ -216,7 +218,7 @@ __global__ void __launch_bounds__(kTile) write_chunk_kernel(const __grid_constan
 #pragma unroll
       for (int j = b * BLOCK; j < (b + 1) * BLOCK; ++j)
         amax = fmaxf(amax, fabsf(j < H ? x2[j].x : x2[j - H].y));
-      const float s = __fdiv_rn(amax * post + g.eps, 3.0f);
+      const float s = __fdiv_rn(amax * post + g.eps, (float)QMAX);
       uint32_t bits;
       const float sq = round_scale(s, SCALE, bits);
       sbits[b] = bits;
@@ -225,18 +227,19 @@ __global__ void __launch_bounds__(kTile) write_chunk_kernel(const __grid_constan
       for (int j = b * BLOCK; j < (b + 1) * BLOCK; ++j) {
         const float xv = j < H ? x2[j].x : x2[j - H].y;
         float tq = fmaf(xv, inv, 12582912.0f);            // 1.5 * 2^23 + rint(x / s_q)
-        if constexpr (SCALE != KVQ3_SCALE_F32) tq = fminf(fmaxf(tq, 12582909.0f), 12582915.0f);
-        const uint32_t c = __float_as_uint(tq) & 7u;      // 3-bit two's complement
-        const int bit = 3 * j;
+        if constexpr (SCALE != KVQ3_SCALE_F32)   // clip to [-QMAX, QMAX]
+          tq = fminf(fmaxf(tq, 12582912.0f - QMAX), 12582912.0f + QMAX);
+        const uint32_t c = __float_as_uint(tq) & ((1u << NBIT) - 1u);   // b-bit two's complement
+        const int bit = NBIT * j;
         words[bit / 32] |= c << (bit % 32);
-        if (bit % 32 > 29) words[bit / 32 + 1] |= c >> (32 - bit % 32);
+        if (bit % 32 > 32 - NBIT) words[bit / 32 + 1] |= c >> (32 - bit % 32);
       }
     }
     if (page >= 0) {
       const int slot = (int)(pos - lp * (uint32_t)g.page_size);
       uint8_t* rec = p.pool + record_offset(g, page, head, which);
       uint8_t* cp = rec + g.scale_hdr_bytes + (int64_t)slot * CB;
-      if constexpr (CB % 16 == 0) {   // d = 128: 48-byte strings, 16-byte aligned
+      if constexpr (CB % 16 == 0) {   // 16-byte multiples (all but 3-bit d = 64), 16-byte aligned
         uint4* cd = reinterpret_cast<uint4*>(cp);
 #pragma unroll
         for (int w = 0; w < CB / 16; ++w)
@@ -262,10 +265,10 @@ __global__ void __launch_bounds__(kTile) write_chunk_kernel(const __grid_constan
   asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
-template <int D, int BLOCK, int SCALE, bool SO4>
-cudaError_t launch_chunk(const ChunkParams& p, cudaStream_t st) {
+template <int D, int BLOCK, int SCALE, bool SO4, int NBIT>
+cudaError_t launch_chunk_b(const ChunkParams& p, cudaStream_t st) {
   const size_t smem = 2 * (size_t)kTile * 2 * D;
-  auto k = write_chunk_kernel<D, BLOCK, SCALE, SO4>;
+  auto k = write_chunk_kernel<D, BLOCK, SCALE, SO4, NBIT>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
@@ -275,6 +278,13 @@ cudaError_t launch_chunk(const ChunkParams& p, cudaStream_t st) {
   if (grid > p.n_tiles) grid = p.n_tiles;
   k<<<(unsigned)grid, kTile, smem, st>>>(p);
   return cudaGetLastError();
+}
+
+template <int D, int BLOCK, int SCALE, bool SO4>
+cudaError_t launch_chunk(const ChunkParams& p, cudaStream_t st) {
+  if (p.g.bits == 2) return launch_chunk_b<D, BLOCK, SCALE, SO4, 2>(p, st);
+  if (p.g.bits == 4) return launch_chunk_b<D, BLOCK, SCALE, SO4, 4>(p, st);
+  return launch_chunk_b<D, BLOCK, SCALE, SO4, 3>(p, st);
 }
 
 template <int D, int BLOCK>

@@ -19,12 +19,13 @@ MIDPOINT = 1e-6          # fp64 scale within this (relative) of a storage midpoi
 
 class Case:
     def __init__(self, d=128, hkv=2, hq=8, block=64, scale="f16", page=16, lens=(37, 100),
-                 maxp=None, paged=False, flags=3, rot_seed=42, data=None, spare_pages=0):
+                 maxp=None, paged=False, flags=3, rot_seed=42, data=None, spare_pages=0, bits=3):
         import torch
         import hadamard_rotated_bit_kvq3_gb300 as K
         self.K, self.torch = K, torch
         self.dev = torch.device("cuda:0")
         self.d, self.hkv, self.hq, self.block, self.scale, self.page = d, hkv, hq, block, scale, page
+        self.bits = bits
         self.lens = np.array(lens, np.int32)
         self.B = len(lens)
         need = [max(1, math.ceil(int(L) / page)) for L in lens]
@@ -36,9 +37,9 @@ class Case:
         else:
             self.table = None
             self.num_pages = self.B * self.maxp + spare_pages
-        self.desc = K.CacheDesc(d, hkv, block, 3, K.SCALE_TYPES[scale], 1e-6, page, self.B, self.maxp,
+        self.desc = K.CacheDesc(d, hkv, block, bits, K.SCALE_TYPES[scale], 1e-6, page, self.B, self.maxp,
                                 0, self.num_pages)
-        self.layout = O.Layout(d, hkv, block, scale, page, self.B, self.maxp, self.num_pages)
+        self.layout = O.Layout(d, hkv, block, scale, page, self.B, self.maxp, self.num_pages, bits)
         self.rot = K.Rotation(d, rot_seed, flags)
         s, q = O.rotation_params(d, rot_seed, bool(flags & 1), bool(flags & 2))
         self.U = O.rotation_matrix(s, q)
@@ -110,7 +111,7 @@ class Case:
         excl_codes = excl_blocks = checked = 0
         for which, src in ((0, k), (1, v)):
             x = src.astype(np.float64).reshape(-1, self.d) @ self.U.T
-            c_o, sq_o, s_o = O.quantize(x, self.block, 1e-6, self.scale)
+            c_o, sq_o, s_o = O.quantize(x, self.block, 1e-6, self.scale, self.bits)
             page, slot, st = O.locate(self.layout, self.table, np.repeat(si, self.hkv),
                                       np.repeat(ps, self.hkv))
             ok = st == 0
@@ -121,14 +122,14 @@ class Case:
             idx_s = so[ok][:, None] + np.arange(nb * self.layout.sb)[None]
             idx_c = co[ok][:, None] + np.arange(self.layout.code_bytes)[None]
             sg = O.decode_scales(gp[idx_s], self.scale)
-            cg = O.unpack_codes(gp[idx_c], self.d)
+            cg = O.unpack_codes(gp[idx_c], self.d, self.bits)
             sq_o, s_o, c_o, xo = sq_o[ok], s_o[ok], c_o[ok], x[ok]
             mid = O.scale_midpoint_distance(s_o, self.scale) < MIDPOINT          # [n, nb]
             good_blk = ~mid
             assert np.all(np.abs(sg - sq_o)[good_blk] <= TOL_SCALE * sq_o[good_blk]), "scale mismatch"
             r = np.abs(xo.reshape(-1, nb, self.block) / np.where(sq_o > 0, sq_o, 1)[..., None])
             near = np.zeros(r.shape, bool)
-            for kk in range(3):
+            for kk in range(O.qmax(self.bits)):
                 near |= np.abs(r - (kk + 0.5)) < BOUNDARY
             near |= mid[..., None]
             near = near.reshape(-1, self.d)
@@ -170,15 +171,16 @@ def flip_bound(case, k, v, si, ps, q, sm_scale=0.0, differs=None):
             deq, slack = [], []
             for which, src in enumerate((k, v)):
                 x = src[sel, g].astype(np.float64) @ case.U.T
-                c, sq, s = O.quantize(x, blk, 1e-6, case.scale)
+                qm = O.qmax(case.bits)
+                c, sq, s = O.quantize(x, blk, 1e-6, case.scale, case.bits)
                 r = np.abs(x.reshape(-1, nb, blk) / np.where(sq > 0, sq, 1.0)[..., None])
                 mid = O.scale_midpoint_distance(s, case.scale) < MIDPOINT
-                # a neighbouring scale moves every x/s by up to 3.5 * ulp_rel:
+                # a neighbouring scale moves every x/s by up to (qmax + 1/2) * ulp_rel:
                 # codes that close to a boundary may flip, and every value
                 # c * s_q moves by |c| * ulp_rel * s_q
-                reach = np.where(mid, BOUNDARY + 3.5 * ulp_rel, BOUNDARY)[..., None]
+                reach = np.where(mid, BOUNDARY + (qm + 0.5) * ulp_rel, BOUNDARY)[..., None]
                 near = np.zeros(r.shape, bool)
-                for kk in range(3):
+                for kk in range(qm):
                     near |= np.abs(r - (kk + 0.5)) < reach
                 if differs is not None:
                     code_d, blk_d = differs[(b, g, which)]
@@ -223,12 +225,12 @@ def written_differences(case, k, v, si, ps):
         for g in range(case.hkv):
             for which, src in ((0, k), (1, v)):
                 x = src[sel, g].astype(np.float64) @ case.U.T
-                c_o, sq_o, _ = O.quantize(x, case.block, 1e-6, case.scale)
+                c_o, sq_o, _ = O.quantize(x, case.block, 1e-6, case.scale, case.bits)
                 rec = page * case.layout.page_bytes + (g * 2 + which) * case.layout.record_bytes
                 so = rec + slot * nb * case.layout.sb
                 co = rec + case.page * nb * case.layout.sb + slot * case.layout.code_bytes
                 sg = O.decode_scales(gp[so[:, None] + np.arange(nb * case.layout.sb)[None]], case.scale)
-                cg = O.unpack_codes(gp[co[:, None] + np.arange(case.layout.code_bytes)[None]], case.d)
+                cg = O.unpack_codes(gp[co[:, None] + np.arange(case.layout.code_bytes)[None]], case.d, case.bits)
                 out[(b, g, which)] = (cg != c_o, sg != sq_o)
     return out
 

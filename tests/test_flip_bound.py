@@ -13,18 +13,19 @@ import math
 import types
 
 import numpy as np
+import pytest
 
 import kvq3_inputs as I
 from cases import BOUNDARY, flip_bound
 from oracle import kvq3_oracle as O
 
 
-def _case(d=128, hkv=1, hq=4, block=64, scale="f16", page=64, lens=(400,), seed=7):
+def _case(d=128, hkv=1, hq=4, block=64, scale="f16", page=64, lens=(400,), seed=7, bits=3):
     s, qt = O.rotation_params(d, 42, True, True)
-    c = types.SimpleNamespace(d=d, hkv=hkv, hq=hq, block=block, scale=scale, page=page,
+    c = types.SimpleNamespace(d=d, hkv=hkv, hq=hq, block=block, scale=scale, page=page, bits=bits,
                               lens=np.array(lens, np.int32), B=len(lens), U=O.rotation_matrix(s, qt))
     maxp = max(math.ceil(L / page) for L in lens)
-    c.layout = O.Layout(d, hkv, block, scale, page, c.B, maxp, c.B * maxp)
+    c.layout = O.Layout(d, hkv, block, scale, page, c.B, maxp, c.B * maxp, bits)
     # narrow outlier-free data: many coordinates land near rounding boundaries
     c.spec = I.DataSpec(d, hkv, seed, 0.0, 1.0)
     return c
@@ -47,14 +48,15 @@ def _flip_near_boundary(c, pool, k, v, si, ps, widen, every=1, differs=None):
     many were moved; records the moved elements in `differs` as
     Case.written_differences would."""
     nb, blk = c.d // c.block, c.block
+    qm = O.qmax(c.bits)
     moved = 0
     for which, src in ((0, k), (1, v)):
         for g in range(c.hkv):
             x = src[:, g].astype(np.float64) @ c.U.T
-            codes, sq, _ = O.quantize(x, blk, 1e-6, c.scale)
+            codes, sq, _ = O.quantize(x, blk, 1e-6, c.scale, c.bits)
             r = x.reshape(-1, nb, blk) / np.where(sq > 0, sq, 1.0)[..., None]
             frac = np.abs(r) - np.floor(np.abs(r))
-            near = (np.abs(frac - 0.5) < widen) & (np.abs(r) < 3.0)
+            near = (np.abs(frac - 0.5) < widen) & (np.abs(r) < qm)
             idx = np.flatnonzero(near)
             near = np.zeros(near.shape, bool)
             near.flat[idx[::every]] = True
@@ -65,17 +67,18 @@ def _flip_near_boundary(c, pool, k, v, si, ps, widen, every=1, differs=None):
             alt = codes.reshape(-1, nb, blk).astype(np.int64)
             # the other neighbour of the boundary
             other = np.where(np.rint(r) == np.floor(r), np.floor(r) + 1, np.floor(r))
-            alt = np.where(near, np.clip(other, -3, 3), alt).reshape(-1, c.d)
+            alt = np.where(near, np.clip(other, -qm, qm), alt).reshape(-1, c.d)
             moved += int(near.sum())
             page, slot, st = O.locate(c.layout, None, si, ps)
             for t in np.nonzero(near.reshape(-1, c.d).any(axis=1))[0]:
                 off = c.layout.code_offset(page[t], g, which, slot[t])
-                pool[off:off + c.layout.code_bytes] = O.pack_codes(alt[t][None].astype(np.int8))[0]
+                pool[off:off + c.layout.code_bytes] = O.pack_codes(alt[t][None].astype(np.int8), c.bits)[0]
     return moved
 
 
-def test_flip_bound_covers_alternative_codes():
-    c = _case()
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_flip_bound_covers_alternative_codes(bits):
+    c = _case(bits=bits)
     k, v, si, ps = _tokens(c)
     pool = np.zeros(c.layout.pool_bytes, np.uint8)
     O.write(pool, c.layout, c.U, k, v, si, ps, None)
@@ -102,7 +105,7 @@ def test_flip_bound_is_zero_without_boundary_elements():
     near_any = False
     for src in (k, v):
         x = src[:, 0].astype(np.float64) @ c.U.T
-        _, sq, _ = O.quantize(x, c.block, 1e-6, c.scale)
+        _, sq, _ = O.quantize(x, c.block, 1e-6, c.scale, c.bits)
         r = np.abs(x.reshape(-1, nb, c.block) / sq[..., None])
         near_any |= bool((np.abs(r - np.floor(r) - 0.5) < BOUNDARY).any())
     assert (bound.max() > 0) == near_any

@@ -72,10 +72,11 @@ def test_rotation_from_params_normalises(K):
 @pytest.mark.parametrize("d,block,scale,page", [(128, 64, "f16", 16), (256, 64, "f16", 16),
                                                 (128, 32, "f32", 64), (128, 64, "e4m3", 64),
                                                 (64, 32, "e4m3", 32)])
-def test_cache_sizes_match_oracle_layout(K, oracle, d, block, scale, page):
-    desc = K.CacheDesc(d, 3, block, 3, K.SCALE_TYPES[scale], 1e-6, page, 2, 5, 0, 11)
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_cache_sizes_match_oracle_layout(K, oracle, d, block, scale, page, bits):
+    desc = K.CacheDesc(d, 3, block, bits, K.SCALE_TYPES[scale], 1e-6, page, 2, 5, 0, 11)
     rb, pb, tb = K.kvq3_cache_sizes(desc)
-    L = oracle.Layout(d, 3, block, scale, page, 2, 5, 11)
+    L = oracle.Layout(d, 3, block, scale, page, 2, 5, 11, bits)
     assert (rb, pb, tb) == (L.record_bytes, L.page_bytes, L.pool_bytes)
     assert rb % 16 == 0
 
@@ -88,7 +89,7 @@ def test_invalid_descriptions_rejected_on_host(K):
         return K.CacheDesc(**base)
     assert K.kvq3_cache_sizes(desc())[0] == 832
     for kw, want in [(dict(head_dim=96), 1), (dict(block=48), 1), (dict(page_size=8), 1),
-                     (dict(bits=4), 2), (dict(block=16), 2), (dict(scale_type=7), 1),
+                     (dict(bits=5), 2), (dict(bits=1), 2), (dict(block=16), 2), (dict(scale_type=7), 1),
                      (dict(num_kv_heads=0), 1), (dict(eps=float("nan")), 1), (dict(head_dim=32, block=32), 2)]:
         with pytest.raises(K.Kvq3Error) as e:
             K.kvq3_cache_sizes(desc(**kw))
