@@ -43,12 +43,23 @@ def algorithmic_bytes(w: I.Workload, lens) -> dict:
     input and packed output of the write."""
     nb = w.d // w.block
     sb = {"f32": 4, "f16": 2, "e4m3": 1}[w.scale]
-    per_tok_head = 2 * (3 * w.d // 8 + nb * sb)
+    per_tok_head = 2 * (w.bits * w.d // 8 + nb * sb)
     kv = int(sum(int(L) for L in lens)) * w.num_kv_heads * per_tok_head
     qo = w.batch * w.num_q_heads * w.d * (2 + 4)
     write_in = w.batch * w.num_kv_heads * 2 * w.d * 2
     write_out = w.batch * w.num_kv_heads * per_tok_head
     return dict(decode=kv + qo, write=write_in + write_out, per_token_head=per_tok_head)
+
+
+# code width override (--bits): 0 keeps each workload's own
+BITS_OVERRIDE = 0
+
+
+def workload(name: str) -> I.Workload:
+    """The named workload, with the code width of --bits when given."""
+    import dataclasses
+    w = I.workloads()[name]
+    return dataclasses.replace(w, bits=BITS_OVERRIDE) if BITS_OVERRIDE else w
 
 
 def workload_lens(w: I.Workload) -> np.ndarray:
@@ -73,10 +84,12 @@ def load_peaks() -> dict:
     return dict(hbm=6800.0, src="fallback")
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(name: str, bits: int = 3):
     """DRAM bytes per decode launch from the committed ncu summary, if it was
-    taken on the current kernel sources."""
-    p = os.path.join(ROOT, "profiles", f"decode_{workload}_traffic.json")
+    taken on the current kernel sources (3-bit codes)."""
+    p = os.path.join(ROOT, "profiles", f"decode_{name}_traffic.json")
+    if bits != 3:
+        return None
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
@@ -141,7 +154,7 @@ class GpuWorkload:
         import torch
         import hadamard_rotated_bit_kvq3_gb300 as K
         self.K, self.torch = K, torch
-        self.w = w = I.workloads()[name]
+        self.w = w = workload(name)
         if batch:
             self.w = w = dataclasses.replace(w, batch=batch)
         self.dev = device
@@ -154,7 +167,7 @@ class GpuWorkload:
         else:
             self.table_np, self.table = None, None
             self.num_pages = w.batch * self.maxp
-        self.desc = K.CacheDesc(w.d, w.num_kv_heads, w.block, 3, K.SCALE_TYPES[w.scale], w.eps, P,
+        self.desc = K.CacheDesc(w.d, w.num_kv_heads, w.block, w.bits, K.SCALE_TYPES[w.scale], w.eps, P,
                                 w.batch, self.maxp, 0, self.num_pages)
         _, _, pool_bytes = K.kvq3_cache_sizes(self.desc)
         self.pool = torch.zeros(pool_bytes, dtype=torch.uint8, device=device)
@@ -216,7 +229,7 @@ class PrefillWorkload:
         import torch
         import hadamard_rotated_bit_kvq3_gb300 as K
         self.K, self.torch = K, torch
-        self.w = w = I.workloads()["prefill"]
+        self.w = w = workload("prefill")
         if tokens:
             self.w = w = dataclasses.replace(w, seq_len=tokens)
         self.dev = device
@@ -224,7 +237,7 @@ class PrefillWorkload:
         self.maxp = n // P
         self.num_pages = self.maxp
         self.table_np = None
-        self.desc = K.CacheDesc(w.d, w.num_kv_heads, w.block, 3, K.SCALE_TYPES[w.scale], w.eps, P, 1,
+        self.desc = K.CacheDesc(w.d, w.num_kv_heads, w.block, w.bits, K.SCALE_TYPES[w.scale], w.eps, P, 1,
                                 self.maxp, 0, self.num_pages)
         _, _, pool_bytes = K.kvq3_cache_sizes(self.desc)
         self.pool = torch.zeros(pool_bytes, dtype=torch.uint8, device=device)
@@ -251,7 +264,7 @@ class PrefillWorkload:
 
     def bytes(self):
         w = self.w
-        rec_tok = 3 * w.d // 8 + (w.d // w.block) * 4
+        rec_tok = w.bits * w.d // 8 + (w.d // w.block) * 4
         n = w.seq_len * w.num_kv_heads * 2
         return n * w.d * 2 + n * rec_tok
 
@@ -266,7 +279,7 @@ def oracle_sample(w: I.Workload, lens, unit: int):
     L = int(lens[b])
     P = w.page_size
     maxp = int(math.ceil(L / P))
-    lay = O.Layout(w.d, 1, w.block, w.scale, P, 1, maxp, maxp)
+    lay = O.Layout(w.d, 1, w.block, w.scale, P, 1, maxp, maxp, w.bits)
     signs, quats = O.rotation_params(w.d, w.rot_seed, bool(w.rot_flags & 1), bool(w.rot_flags & 2))
     U = O.rotation_matrix(signs, quats)
     pool = np.zeros(lay.pool_bytes, np.uint8)
@@ -336,7 +349,7 @@ def barrier(world: int):
 
 
 def run_reference(args, world, rank):
-    w = I.workloads()[args.workload]
+    w = workload(args.workload)
     lens = workload_lens(w)
     if rank != 0:
         return
@@ -422,7 +435,7 @@ class PrefillAttnWorkload:
         self.K, self.torch, self.w, self.dev = K, torch, w, device
         n, P = w.seq_len, w.page_size
         self.maxp = (n + P - 1) // P
-        self.desc = K.CacheDesc(w.d, w.num_kv_heads, w.block, 3, K.SCALE_TYPES[w.scale], w.eps, P, 1,
+        self.desc = K.CacheDesc(w.d, w.num_kv_heads, w.block, w.bits, K.SCALE_TYPES[w.scale], w.eps, P, 1,
                                 self.maxp, 0, self.maxp)
         _, _, pool_bytes = K.kvq3_cache_sizes(self.desc)
         self.pool = torch.zeros(pool_bytes, dtype=torch.uint8, device=device)
@@ -459,7 +472,7 @@ def run_prefill_attn(args, world, rank, dev):
     import dataclasses
 
     import torch
-    w = I.workloads()[args.workload]
+    w = workload(args.workload)
     if args.tokens:   # a shorter context (profiling): the chunk is at most a quarter of it
         w = dataclasses.replace(w, seq_len=args.tokens, chunk=min(w.chunk, max(1, args.tokens // 4)))
     st = PrefillAttnWorkload(dev, w)
@@ -510,7 +523,7 @@ def run_prefill_attn(args, world, rank, dev):
 def workload_desc(w: I.Workload) -> str:
     lens = f"N={w.seq_len}" if not w.len_range else f"N~U[{w.len_range[0]},{w.len_range[1]}]"
     return (f"{w.name}: B{w.batch} Hkv{w.num_kv_heads} Hq{w.num_q_heads} d{w.d} {lens} m{w.block} "
-            f"{w.scale} scales, {'paged' if w.paged else 'contiguous'} P{w.page_size}, "
+            f"{w.scale} scales, {w.bits}-bit codes, {'paged' if w.paged else 'contiguous'} P{w.page_size}, "
             f"rot flags {w.rot_flags}; step = kvq3_write(1 token/seq) + kvq3_decode_attn")
 
 
@@ -525,7 +538,11 @@ def main():
     ap.add_argument("--batch", type=int, default=0, help="override the batch (smaller profiling cases)")
     ap.add_argument("--tokens", type=int, default=0, help="override the prefill token count")
     ap.add_argument("--profile", action="store_true", help="plain steps only, for ncu captures")
+    ap.add_argument("--bits", type=int, default=0, choices=[0, 2, 3, 4],
+                    help="code width of the cache (0: the workload's own, 3)")
     args = ap.parse_args()
+    global BITS_OVERRIDE
+    BITS_OVERRIDE = args.bits
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
@@ -535,7 +552,7 @@ def main():
     import torch
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = I.workloads()[args.workload]
+    w = workload(args.workload)
     if w.chunk > 0:
         run_prefill_attn(args, world, rank, dev)
         return
@@ -640,7 +657,7 @@ def main():
                        "bytes": ab["decode"]},
             "write": {"ms": wr_ms, "gbs": ab["write"] / (wr_ms * 1e-3) / 1e9, "bytes": ab["write"]},
             "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": peaks["hbm"], "unit": "GB/s",
-                         "frac": dec_gbs / peaks["hbm"], "traffic": recorded_traffic(args.workload),
+                         "frac": dec_gbs / peaks["hbm"], "traffic": recorded_traffic(args.workload, w.bits),
                          "kernel": "kvq3_decode_attn (decode_split_kernel + decode_combine_kernel)",
                          "peak_source": peaks["src"]},
             "e2e": {"value": whole_job_rate(w.batch, world, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,

@@ -61,6 +61,12 @@
  *       little-endian bit stream of 3d/8 bytes (bit k of the stream is bit
  *       k%8 of byte k/8).  Blocks are consecutive rotated coordinates
  *       [0,m), [m,2m), ...
+ *   R16 Other code widths b = 2 and 4 ([OIQ] 3.3 stores d*b bits per
+ *       vector, 4.2 packs INT3/INT4 values, 5.1 evaluates b = 4, 3, 2; [OMC]
+ *       writes its quantiser for any b): divisor and clip bound
+ *       2^(b-1) - 1 (1, 3, 7) in R7, b-bit two's complement in R8 (-2^(b-1)
+ *       is never written), element j at bits b*j..b*j+b-1 of a b*d/8-byte
+ *       string in R9.
  *   R10 One scale per block and no per-vector scale ([OMC]); [OIQ] 4.2's
  *       header count does not add up and is not followed.
  *   R11 The query is rotated by the same U as the keys ([OMC] q1 = U(q)).
@@ -73,7 +79,7 @@
  *
  * Cache layout (the "chunk record" of [OIQ] 4.2, one per page, kv head and
  * K|V).  P = page_size tokens per page (a multiple of 16), nb = d/m blocks,
- * sb = scale bytes (4, 2, 1), cb = 3d/8 code bytes:
+ * sb = scale bytes (4, 2, 1), cb = b*d/8 code bytes (3d/8 at b = 3):
  *   record  = [ scales: P*nb entries, token-major (slot t, block j at t*nb+j),
  *                       sb bytes each, little-endian ]
  *             [ codes : P code strings of cb bytes (slot t at t*cb) ]
@@ -135,7 +141,7 @@ enum {
   KVQ3_DEV_BAD_POS = 2,      /* position outside [0, max_pages_per_seq*P) */
   KVQ3_DEV_BAD_PAGE = 4,     /* page id outside [0, num_pages) */
   KVQ3_DEV_BAD_LEN = 8,      /* seq_lens[b] outside [0, capacity] */
-  KVQ3_DEV_BAD_CODE = 16,    /* a stored code of -4 (never written) */
+  KVQ3_DEV_BAD_CODE = 16,    /* a stored code of -2^(b-1), e.g. -4 at b = 3 (never written) */
   KVQ3_DEV_TIMEOUT = 32      /* an asynchronous copy did not arrive in time */
 };
 
@@ -148,7 +154,7 @@ typedef struct {
                                 any power of two 4..256 for kvq3_rotate */
   int32_t num_kv_heads;      /* Hkv >= 1 */
   int32_t block;             /* m: 32 or 64, divides d */
-  int32_t bits;              /* b: 3 */
+  int32_t bits;              /* b: code width, 2, 3 or 4 (R16) */
   int32_t scale_type;        /* kvq3_scale_type */
   float eps;                 /* eps of the scale formula (1e-6) */
   int32_t page_size;         /* P: tokens per page, a positive multiple of 16 */
@@ -313,8 +319,8 @@ kvq3_status kvq3_prefill_attn(kvq3_rotation rot, const kvq3_cache_desc *desc,
  * (which = 0) or V (which = 1) as fp32 out[nt][d]: s_q * c in the rotated
  * domain (rot == NULL) or U^T (s_q * c) (rot != NULL) ([OIQ] 3.3 "Retrieve").
  * codes_out (nullable): int32 [nt][d] raw codes.  Positions without a valid
- * slot give zeros and set *dev_status bits; a stored -4 sets
- * KVQ3_DEV_BAD_CODE and reads as 0.  A debugging and testing aid. */
+ * slot give zeros and set *dev_status bits; a stored -2^(b-1) (-4 at b = 3)
+ * sets KVQ3_DEV_BAD_CODE and reads as 0.  A debugging and testing aid. */
 kvq3_status kvq3_dequant_debug(kvq3_rotation rot, const kvq3_cache_desc *desc,
                                const kvq3_cache *cache, int32_t seq,
                                int32_t kv_head, int32_t which, int64_t t0,

@@ -276,6 +276,7 @@ class Workload:
     decode: bool = True
     eps: float = 1e-6
     chunk: int = 0        # prefill-attention workloads: query tokens of the chunk
+    bits: int = 3         # code width b (2, 3 or 4)
 
     @property
     def group(self) -> int:
