@@ -61,7 +61,7 @@
  *       little-endian bit stream of 3d/8 bytes (bit k of the stream is bit
  *       k%8 of byte k/8).  Blocks are consecutive rotated coordinates
  *       [0,m), [m,2m), ...
- *   R16 Other code widths b = 2 and 4 ([OIQ] 3.3 stores d*b bits per
+ *   R17 Other code widths b = 2 and 4 ([OIQ] 3.3 stores d*b bits per
  *       vector, 4.2 packs INT3/INT4 values, 5.1 evaluates b = 4, 3, 2; [OMC]
  *       writes its quantiser for any b): divisor and clip bound
  *       2^(b-1) - 1 (1, 3, 7) in R7, b-bit two's complement in R8 (-2^(b-1)
@@ -154,7 +154,7 @@ typedef struct {
                                 any power of two 4..256 for kvq3_rotate */
   int32_t num_kv_heads;      /* Hkv >= 1 */
   int32_t block;             /* m: 32 or 64, divides d */
-  int32_t bits;              /* b: code width, 2, 3 or 4 (R16) */
+  int32_t bits;              /* b: code width, 2, 3 or 4 (R17) */
   int32_t scale_type;        /* kvq3_scale_type */
   float eps;                 /* eps of the scale formula (1e-6) */
   int32_t page_size;         /* P: tokens per page, a positive multiple of 16 */
