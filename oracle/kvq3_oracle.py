@@ -36,6 +36,12 @@ header of the library as well):
     c = clip(round_half_even(x/s_q), -3, 3), and c = 0 where s_q = 0.
   * Codes are 3-bit two's complement in a little-endian bit stream: element j
     of a vector at bits 3j..3j+2 of its 3d/8-byte code string.
+  * The asymmetric variant of [HFF] (scale kind "e4m3zp"): per block an E4M3
+    scale s = (max - min + eps)/(2^b - 1) and an E4M3 zero point z = min,
+    stored as two bytes, and unsigned codes u = clip(round((x - z_q)/s_q), 0,
+    2^b - 1); x_hat = s_q u + z_q.  The page's "FP8 scale and zero-point
+    header" is taken as one byte each (3.25 bits per element at m = 64); its
+    3.125-bit figure fits a single header byte and is not followed.
   * Other bit widths b = 2 and 4 ([OIQ] 3.3, 4.2 and 5.1 evaluate them; the
     quantiser of [OMC] Key formulas is written for any b): divisor and clip
     bound 2^(b-1) - 1, b-bit two's-complement codes in the same bit stream
@@ -53,7 +59,9 @@ from dataclasses import dataclass
 import numpy as np
 
 MASK64 = (1 << 64) - 1
-SCALE_BYTES = {"f32": 4, "f16": 2, "e4m3": 1}
+# "e4m3zp": the asymmetric variant of [HFF] -- an E4M3 scale byte and an
+# E4M3 zero-point byte per block, unsigned codes (see quantize_asym)
+SCALE_BYTES = {"f32": 4, "f16": 2, "e4m3": 1, "e4m3zp": 2}
 
 # Device-status bits (the library's dev_status word uses the same meaning).
 ST_BAD_SEQ = 1
@@ -192,6 +200,18 @@ def round_e4m3(s):
     return np.minimum(np.where(s == 0, 0.0, q), 448.0)
 
 
+def round_e4m3_signed(v):
+    """E4M3 rounding of signed values: the sign, then round_e4m3 of |v|."""
+    v = np.asarray(v, dtype=np.float64)
+    return np.sign(v) * round_e4m3(np.abs(v))
+
+
+def encode_e4m3_signed(q):
+    """Bytes of exactly representable E4M3 values of either sign (sign bit 0x80)."""
+    q = np.asarray(q, dtype=np.float64)
+    return (encode_e4m3(np.abs(q)) | np.where(q < 0, 0x80, 0)).astype(np.uint8)
+
+
 def encode_e4m3(q):
     """Bytes of exactly representable non-negative E4M3 values."""
     q = np.asarray(q, dtype=np.float64)
@@ -258,8 +278,13 @@ def scale_midpoint_distance(s, kind: str):
 
 
 def encode_scales(q: np.ndarray, kind: str) -> np.ndarray:
-    """Stored scale values (..., n) -> little-endian bytes (..., n*sb)."""
+    """Stored scale values (..., n) -> little-endian bytes (..., n*sb).  For
+    "e4m3zp" q is (..., n, 2): (scale, zero point) of each block, stored as
+    the scale byte then the zero-point byte."""
     q = np.asarray(q, dtype=np.float64)
+    if kind == "e4m3zp":
+        b = np.stack([encode_e4m3(q[..., 0]), encode_e4m3_signed(q[..., 1])], axis=-1)
+        return b.reshape(q.shape[:-2] + (-1,))
     if kind == "f32":
         b = q.astype("<f4").view(np.uint8)
     elif kind == "f16":
@@ -270,8 +295,11 @@ def encode_scales(q: np.ndarray, kind: str) -> np.ndarray:
 
 
 def decode_scales(buf: np.ndarray, kind: str) -> np.ndarray:
-    """Scale bytes (uint8, ..., n*sb) -> fp64 values (..., n)."""
+    """Scale bytes (uint8, ..., n*sb) -> fp64 values (..., n); for "e4m3zp"
+    (..., n, 2) pairs (scale, zero point)."""
     buf = np.ascontiguousarray(buf)
+    if kind == "e4m3zp":
+        return decode_e4m3(buf.reshape(buf.shape[:-1] + (-1, 2)))
     if kind == "f32":
         return buf.view("<f4").astype(np.float64)
     if kind == "f16":
@@ -313,6 +341,29 @@ def quantize(x: np.ndarray, block: int, eps: float, kind: str, bits: int = 3):
     return c.reshape(n, d), sq, s
 
 
+def quantize_asym(x: np.ndarray, block: int, eps: float, bits: int = 3):
+    """The asymmetric variant of [HFF] ("3-bit unsigned integers paired with
+    a shared FP8 scale and zero-point header", per 64-element sub-block):
+    per block, z = min x and s = (max x - min x + eps)/(2^b - 1), both
+    stored in E4M3 (round half to even, saturating; z keeps its sign), and
+    unsigned codes u = clip(round_half_even((x - z_q)/s_q), 0, 2^b - 1)
+    (u = 0 where s_q = 0).  Dequantisation: x_hat = s_q u + z_q.
+    x: fp64 [n][d].  Returns (codes uint8 [n][d], (s_q, z_q) fp64
+    [n][d/block][2], s fp64 [n][d/block])."""
+    qmax(bits)
+    n, d = x.shape
+    top = (1 << bits) - 1
+    xb = x.reshape(n, d // block, block)
+    lo, hi = xb.min(axis=-1), xb.max(axis=-1)
+    s = (hi - lo + eps) / float(top)
+    sq = round_e4m3(s)
+    zq = round_e4m3_signed(lo)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = np.where(sq[..., None] > 0, (xb - zq[..., None]) / sq[..., None], 0.0)
+    u = np.clip(np.rint(r), 0, top).astype(np.uint8)
+    return u.reshape(n, d), np.stack([sq, zq], axis=-1), s
+
+
 def pack_codes(codes: np.ndarray, bits: int = 3) -> np.ndarray:
     """b-bit two's-complement codes [..., d] -> bytes [..., b*d/8]: element j
     at bits b*j..b*j+b-1 of a little-endian bit stream (bit k of the stream is
@@ -326,13 +377,16 @@ def pack_codes(codes: np.ndarray, bits: int = 3) -> np.ndarray:
     return np.packbits(bs, axis=-1, bitorder="little")
 
 
-def unpack_codes(buf: np.ndarray, d: int, bits: int = 3) -> np.ndarray:
+def unpack_codes(buf: np.ndarray, d: int, bits: int = 3, signed: bool = True) -> np.ndarray:
     """Inverse of :func:`pack_codes` (the value -2^(b-1), which the quantiser
-    never writes, reads as itself)."""
+    never writes, reads as itself); signed=False reads the unsigned codes of
+    the asymmetric variant."""
     qmax(bits)
     bs = np.unpackbits(np.asarray(buf, dtype=np.uint8), axis=-1, bitorder="little")
     bs = bs.reshape(buf.shape[:-1] + (d, bits)).astype(np.int64)
     v = sum(bs[..., i] << i for i in range(bits))
+    if not signed:
+        return v.astype(np.uint8)
     half = 1 << (bits - 1)
     return np.where(v >= half, v - 2 * half, v).astype(np.int8)
 
@@ -448,7 +502,10 @@ def write(pool: np.ndarray, layout: Layout, U: np.ndarray, k: np.ndarray, v: np.
     ok = np.nonzero(st == 0)[0]
     for which, src in ((0, k), (1, v)):
         x = src[ok].astype(np.float64).reshape(len(ok) * H, layout.d) @ U.T
-        codes, sq, _ = quantize(x, layout.block, eps, layout.scale, layout.bits)
+        if layout.scale == "e4m3zp":
+            codes, sq, _ = quantize_asym(x, layout.block, eps, layout.bits)
+        else:
+            codes, sq, _ = quantize(x, layout.block, eps, layout.scale, layout.bits)
         packed = pack_codes(codes, layout.bits)                 # [n*H, cb]
         hdr = encode_scales(sq, layout.scale)                   # [n*H, nb*sb]
         heads = np.tile(np.arange(H), len(ok))
@@ -465,8 +522,10 @@ def write(pool: np.ndarray, layout: Layout, U: np.ndarray, k: np.ndarray, v: np.
 def read_rotated(pool: np.ndarray, layout: Layout, b: int, kv_head: int, which: int,
                  t0: int, nt: int, page_table=None):
     """Stored codes and scales of positions t0..t0+nt-1 of sequence b,
-    dequantised in the rotated domain: x_hat = s_q * c ([OMC] Key formulas).
-    Returns (x_hat fp64 [nt][d], codes int8 [nt][d], scales fp64 [nt][d/m])."""
+    dequantised in the rotated domain: x_hat = s_q * c ([OMC] Key formulas),
+    or s_q * u + z_q for the asymmetric variant ("e4m3zp").
+    Returns (x_hat fp64 [nt][d], codes int8 [nt][d] (uint8 for "e4m3zp"),
+    scales fp64 [nt][d/m] ([nt][d/m][2] (scale, zero point) for "e4m3zp"))."""
     pos = np.arange(t0, t0 + nt)
     page, slot, st = locate(layout, page_table, np.full(nt, b), pos)
     if np.any(st):
@@ -475,6 +534,11 @@ def read_rotated(pool: np.ndarray, layout: Layout, b: int, kv_head: int, which: 
     so = rec + slot * layout.nb * layout.sb
     co = rec + layout.page_size * layout.nb * layout.sb + slot * layout.code_bytes
     sc = decode_scales(pool[_gather_index(so, layout.nb * layout.sb)], layout.scale)
+    if layout.scale == "e4m3zp":     # x_hat = s_q u + z_q
+        cs = unpack_codes(pool[_gather_index(co, layout.code_bytes)], layout.d, layout.bits, signed=False)
+        cb = cs.reshape(nt, layout.nb, layout.block).astype(np.float64)
+        xh = (cb * sc[..., 0:1] + sc[..., 1:2]).reshape(nt, layout.d)
+        return xh, cs, sc
     cs = unpack_codes(pool[_gather_index(co, layout.code_bytes)], layout.d, layout.bits)
     xh = (cs.reshape(nt, layout.nb, layout.block) * sc[..., None]).reshape(nt, layout.d)
     return xh, cs, sc

@@ -71,6 +71,39 @@ def test_layout_byte_positions(oracle):
     assert not np.any(pool[~touched])
 
 
+@pytest.mark.parametrize("paged", [False, True])
+def test_write_read_roundtrip_asym(oracle, paged):
+    U, L, pool, table = _setup(oracle, scale="e4m3zp", paged=paged)
+    rng = np.random.default_rng(2)
+    n = 30
+    k = (rng.standard_normal((n, 2, 128)) * 3 + 1).astype(np.float16)
+    v = rng.standard_normal((n, 2, 128)).astype(np.float16)
+    seq = np.repeat([0, 1], n // 2)
+    pos = np.concatenate([np.arange(15), np.arange(15) + 9])
+    assert oracle.write(pool, L, U, k, v, seq, pos, table) == 0
+    for b in (0, 1):
+        sel = seq == b
+        for h in (0, 1):
+            for which, src in ((0, k), (1, v)):
+                xh, u, sz = oracle.read_rotated(pool, L, b, h, which, int(pos[sel][0]), 15, table)
+                x = src[sel, h].astype(np.float64) @ U.T
+                u2, sz2, _ = oracle.quantize_asym(x, 64, 1e-6)
+                assert np.array_equal(u, u2) and np.array_equal(sz, sz2)
+                assert np.allclose(xh, (u2.reshape(15, 2, 64) * sz2[..., 0:1] + sz2[..., 1:2]).reshape(15, 128))
+
+
+def test_decode_single_token_returns_value_asym(oracle):
+    U, L, pool, _ = _setup(oracle, scale="e4m3zp")
+    rng = np.random.default_rng(4)
+    _fill(oracle, L, pool, U, None, [1, 1], rng)
+    q = rng.standard_normal((2, 4, 128)).astype(np.float16)
+    out = oracle.decode(pool, L, U, q, np.array([1, 1]))
+    for b in range(2):
+        for h in range(4):
+            vh = oracle.read_rotated(pool, L, b, h // 2, 1, 0, 1)[0][0]
+            assert np.abs(out[b, h] - U.T @ vh).max() < 1e-12
+
+
 @pytest.mark.parametrize("bits", [2, 4])
 def test_layout_byte_positions_b24(oracle, bits):
     # the b-bit code string of slot 1 sits b*d/8 bytes after slot 0's; one

@@ -424,3 +424,69 @@ def test_storage_accounting_b24(oracle):
         assert L.code_bytes == cb
         assert L.record_bytes == 16 * (2 * 2 + cb)
         assert 8 * L.record_bytes / (16 * 128) == bits + 0.25
+
+
+# ------------------------------------------------------------- asymmetric variant ("e4m3zp")
+def test_asym_hand_example(oracle):
+    # "Hardware-Fused Fast Hadamard Transforms ...": unsigned 3-bit codes with
+    # an FP8 scale and zero point per block.  min -1, max 2.5 (eps = 0):
+    # s = 3.5/7 = 0.5 and z = -1, both exact in E4M3; u = (x + 1)/0.5, half to even
+    x = np.zeros((1, 32))
+    x[0, :5] = [-1.0, 2.5, 0.0, 0.25, 1.0]
+    u, sz, s = oracle.quantize_asym(x, 32, 0.0)
+    assert s[0, 0] == 0.5 and tuple(sz[0, 0]) == (0.5, -1.0)
+    assert list(u[0, :5]) == [0, 7, 2, 2, 4] and np.all(u[0, 5:] == 2)
+    # bytes: scale 0.5 = 0x30, zero point -1 = 0xB8 (sign | exponent 7 << 3)
+    assert oracle.encode_scales(sz, "e4m3zp").tobytes() == bytes([0x30, 0xB8])
+    # unsigned codes use the same little-endian stream: u = 0,7,2,2,4,2,2,2 sets
+    # bits 3-5, 7 | 10, 14 | 16, 19, 22 -> B8 44 49
+    assert oracle.pack_codes(u[:, :8], 3)[0].tobytes() == bytes([0xB8, 0x44, 0x49])
+    assert np.array_equal(oracle.unpack_codes(oracle.pack_codes(u, 3), 32, 3, signed=False), u)
+
+
+def test_e4m3_signed_round_trip(oracle):
+    b = np.array([v for v in range(256) if (v & 0x7F) != 0x7F], np.uint8)
+    vals = oracle.decode_e4m3(b)
+    assert np.array_equal(oracle.encode_e4m3_signed(vals)[vals != 0], b[vals != 0])
+    assert np.array_equal(oracle.round_e4m3_signed(vals), vals)
+    assert oracle.round_e4m3_signed(-3.3) == -oracle.round_e4m3(3.3)
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_asym_error_bound(oracle, bits):
+    # |x - (s_q u + z_q)| <= s_q/2 wherever (x - z_q)/s_q lies in [-1/2, 2^b - 1/2]
+    top = (1 << bits) - 1
+    rng = np.random.default_rng(60 + bits)
+    x = rng.standard_normal((300, 128)) * np.exp(rng.uniform(-3, 3, (300, 1))) + rng.uniform(-1, 1, (300, 1))
+    u, sz, s = oracle.quantize_asym(x, 64, 1e-6, bits)
+    assert u.min() >= 0 and u.max() <= top
+    xb = x.reshape(300, -1, 64)
+    assert np.allclose(s, (xb.max(-1) - xb.min(-1) + 1e-6) / top, rtol=1e-15)
+    sq, zq = sz[..., 0:1], sz[..., 1:2]
+    xh = u.reshape(xb.shape) * sq + zq
+    r = (xb - zq) / sq
+    inside = (r >= -0.5) & (r <= top + 0.5)
+    err = np.abs(xb - xh)
+    assert np.all(err[inside] <= np.broadcast_to(sq, xb.shape)[inside] / 2 * (1 + 1e-12))
+    assert inside.mean() > 0.95
+
+
+def test_asym_storage_and_error_against_symmetric(oracle):
+    # 2 header bytes per 64-element block: 3.25 bits per element (the page's
+    # 3.125 counts one header byte); on the rotated outlier data the
+    # asymmetric codes (8 levels over [min, max]) give a lower error than the
+    # symmetric E4M3 ones (7 levels over [-max|x|, max|x|])
+    L = oracle.Layout(128, 1, 64, "e4m3zp", 16, 1, 1, 1)
+    assert L.record_bytes == 16 * (2 * 2 + 48) and 8 * L.record_bytes / (16 * 128) == 3.25
+    import kvq3_inputs as I
+    spec = I.DataSpec(128, 1, 79, 0.03, 20.0)
+    x = I.kv_rows_np(spec, 0, 0, 0, 0, 512).astype(np.float64)
+    s, q = oracle.rotation_params(128, 42)
+    U = oracle.rotation_matrix(s, q)
+    y = x @ U.T
+    c, sq, _ = oracle.quantize(y, 64, 1e-6, "e4m3")
+    ys = (c.reshape(-1, 2, 64) * sq[..., None]).reshape(y.shape)
+    u, sz, _ = oracle.quantize_asym(y, 64, 1e-6)
+    ya = (u.reshape(-1, 2, 64) * sz[..., 0:1] + sz[..., 1:2]).reshape(y.shape)
+    mse_s, mse_a = np.mean((ys - y) ** 2), np.mean((ya - y) ** 2)
+    assert mse_a < 0.8 * mse_s
