@@ -42,7 +42,7 @@ def algorithmic_bytes(w: I.Workload, lens) -> dict:
     attended token (read once), q (fp16) and out (fp32) of the decode; fp16
     input and packed output of the write."""
     nb = w.d // w.block
-    sb = {"f32": 4, "f16": 2, "e4m3": 1}[w.scale]
+    sb = {"f32": 4, "f16": 2, "e4m3": 1, "e4m3zp": 2}[w.scale]
     per_tok_head = 2 * (w.bits * w.d // 8 + nb * sb)
     kv = int(sum(int(L) for L in lens)) * w.num_kv_heads * per_tok_head
     qo = w.batch * w.num_q_heads * w.d * (2 + 4)
@@ -51,15 +51,21 @@ def algorithmic_bytes(w: I.Workload, lens) -> dict:
     return dict(decode=kv + qo, write=write_in + write_out, per_token_head=per_tok_head)
 
 
-# code width override (--bits): 0 keeps each workload's own
+# code width and scale format overrides (--bits, --scale): 0 / "" keep each workload's own
 BITS_OVERRIDE = 0
+SCALE_OVERRIDE = ""
 
 
 def workload(name: str) -> I.Workload:
-    """The named workload, with the code width of --bits when given."""
+    """The named workload, with the code width of --bits and the scale
+    format of --scale when given."""
     import dataclasses
     w = I.workloads()[name]
-    return dataclasses.replace(w, bits=BITS_OVERRIDE) if BITS_OVERRIDE else w
+    if BITS_OVERRIDE:
+        w = dataclasses.replace(w, bits=BITS_OVERRIDE)
+    if SCALE_OVERRIDE:
+        w = dataclasses.replace(w, scale=SCALE_OVERRIDE)
+    return w
 
 
 def workload_lens(w: I.Workload) -> np.ndarray:
@@ -264,7 +270,7 @@ class PrefillWorkload:
 
     def bytes(self):
         w = self.w
-        rec_tok = w.bits * w.d // 8 + (w.d // w.block) * 4
+        rec_tok = w.bits * w.d // 8 + (w.d // w.block) * {"f32": 4, "f16": 2, "e4m3": 1, "e4m3zp": 2}[w.scale]
         n = w.seq_len * w.num_kv_heads * 2
         return n * w.d * 2 + n * rec_tok
 
@@ -540,9 +546,12 @@ def main():
     ap.add_argument("--profile", action="store_true", help="plain steps only, for ncu captures")
     ap.add_argument("--bits", type=int, default=0, choices=[0, 2, 3, 4],
                     help="code width of the cache (0: the workload's own, 3)")
+    ap.add_argument("--scale", default="", choices=["", "f32", "f16", "e4m3", "e4m3zp"],
+                    help="scale format (e4m3zp: the asymmetric variant, E4M3 scale and zero point)")
     args = ap.parse_args()
-    global BITS_OVERRIDE
+    global BITS_OVERRIDE, SCALE_OVERRIDE
     BITS_OVERRIDE = args.bits
+    SCALE_OVERRIDE = args.scale
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup(args)
     if args.impl == "reference":

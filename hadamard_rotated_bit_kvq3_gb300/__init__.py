@@ -26,7 +26,7 @@ LIB_PATH = os.path.join(_HERE, "libkvq3.so")
 KVQ3_OK = 0
 KVQ3_ROT_SIGN = 1
 KVQ3_ROT_SO4 = 2
-SCALE_TYPES = {"f32": 0, "f16": 1, "e4m3": 2}
+SCALE_TYPES = {"f32": 0, "f16": 1, "e4m3": 2, "e4m3zp": 3}
 DEV_BITS = {"bad_seq": 1, "bad_pos": 2, "bad_page": 4, "bad_len": 8, "bad_code": 16, "timeout": 32}
 
 if not os.path.exists(LIB_PATH):

@@ -20,6 +20,7 @@ namespace {
   switch (g.scale_type) {                                          \
     case KVQ3_SCALE_F32: KVQ3_BY_BITS(D, f32, FN, __VA_ARGS__)     \
     case KVQ3_SCALE_F16: KVQ3_BY_BITS(D, f16, FN, __VA_ARGS__)     \
+    case KVQ3_SCALE_E4M3_ZP: return FN##_d##D##_e4m3zp_b3(__VA_ARGS__); \
     default: KVQ3_BY_BITS(D, e4m3, FN, __VA_ARGS__)                \
   }
 
@@ -132,7 +133,7 @@ kvq3_status kvq3_prefill_attn(kvq3_rotation rot, const kvq3_cache_desc* desc,
   if (!workspace || ws_bytes < plan.ws_bytes || reinterpret_cast<uintptr_t>(workspace) % 256)
     return KVQ3_ERR_WORKSPACE;
   const double qks = (sm_scale > 0.0f ? (double)sm_scale : 1.0 / sqrt((double)vg.d)) * 1.4426950408889634;
-  if (vg.d == 128 && vg.bits == 3) {
+  if (vg.d == 128 && vg.bits == 3 && vg.scale_type != KVQ3_SCALE_E4M3_ZP) {
     // shared dequantised tiles: each K/V tile is unpacked once for 64 query rows
     CacheGeom g;
     make_geom(desc, &g);

@@ -312,13 +312,19 @@ __host__ __device__ constexpr int v_off(int NBIT, int f) {
 }
 constexpr uint32_t kSignVg0 = 0x49244924u, kSignVg1 = 0x92499249u, kSignVg2 = 0x24922492u;
 
-template <int NBIT, int F>
+// UNS: unsigned codes (the asymmetric variant): the field is the code itself,
+// with no sign flip (s0..s2 are 0) and no offset to remove.
+template <int NBIT, int F, bool UNS = false>
 __device__ __forceinline__ uint32_t v_field(uint32_t c0, uint32_t c1, uint32_t s0, uint32_t s1, uint32_t s2) {
   constexpr int o = v_off(NBIT, F);
   constexpr uint32_t FM = (1u << NBIT) - 1u;
   constexpr uint32_t M = (FM << o) | (FM << (16 + o));
   constexpr uint32_t OFS = (1u << (NBIT - 1)) * 0x00010001u << o;   // 2^(b-1) in both halves
-  if constexpr (NBIT == 3) {
+  if constexpr (UNS) {
+    constexpr uint32_t sel = NBIT == 3 ? (F < 3 ? 0x5410u : (F < 6 ? 0x6521u : 0x7632u))
+                                       : ((NBIT == 4 ? F / 2 : F / 4) * 0x1111u + 0x4400u);
+    return __byte_perm(c0, c1, sel) & M;
+  } else if constexpr (NBIT == 3) {
     constexpr uint32_t sel = F < 3 ? 0x5410u : (F < 6 ? 0x6521u : 0x7632u);
     const uint32_t w = __byte_perm(c0, c1, sel);
     return hsub2_bits(xor_and<M>(w, F < 3 ? s0 : (F < 6 ? s1 : s2)), OFS);
@@ -405,7 +411,8 @@ __device__ __forceinline__ void lds_bytes(uint32_t a, uint32_t (&w)[(N + 3) / 4]
 // together: one half2 -> float2 for fp16, one fp8x2 -> half2 -> float2 for E4M3).
 template <int NB, int SCALE>
 struct ScaleDec {
-  static constexpr int SB = SCALE == KVQ3_SCALE_F32 ? 4 : SCALE == KVQ3_SCALE_F16 ? 2 : 1;
+  static constexpr int SB = SCALE == KVQ3_SCALE_F32 ? 4
+                          : (SCALE == KVQ3_SCALE_F16 || SCALE == KVQ3_SCALE_E4M3_ZP) ? 2 : 1;
   static constexpr int BPT = NB * SB;
   // values i = 0..n-1 starting at value index i0 of w
   template <int N, int I0>
@@ -449,6 +456,33 @@ struct ScaleDec {
     lds_bytes<2 * BPT, OFF>(a, w);
     decode<NB, 0>(w, s0);
     decode<NB, NB>(w, s1);
+  }
+  // Asymmetric variant: (scale, zero point) E4M3 byte pairs of blocks
+  // I0 .. I0+N-1, one fp8x2 conversion per block.
+  template <int N, int I0>
+  __device__ static __forceinline__ void decode_sz(const uint32_t* w, float* s, float* z) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      const uint32_t v = w[(I0 + i) / 2] >> (16 * ((I0 + i) & 1));
+      const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(v & 0xffffu), __NV_E4M3);
+      const float2 f = __half22float2(__half2(hr));
+      s[i] = f.x;
+      z[i] = f.y;
+    }
+  }
+  template <int OFF>
+  __device__ static __forceinline__ void one_sz(uint32_t a, float (&s)[NB], float (&z)[NB]) {
+    uint32_t w[(BPT + 3) / 4];
+    lds_bytes<BPT, OFF>(a, w);
+    decode_sz<NB, 0>(w, s, z);
+  }
+  template <int OFF>
+  __device__ static __forceinline__ void two_sz(uint32_t a, float (&s0)[NB], float (&s1)[NB], float (&z0)[NB],
+                                                float (&z1)[NB]) {
+    uint32_t w[(2 * BPT + 3) / 4];
+    lds_bytes<2 * BPT, OFF>(a, w);
+    decode_sz<NB, 0>(w, s0, z0);
+    decode_sz<NB, NB>(w, s1, z1);
   }
 };
 
@@ -510,6 +544,10 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
   constexpr int FQ = BLOCK / 4;       // key fields per lane per block
   constexpr int FV = BLOCK / 8;       // value fields per lane per block
   constexpr int CB = NBIT * D / 8;    // code bytes per token
+  // Asymmetric variant: unsigned codes, x_hat = s u + z per (token, block):
+  // logits gain z_k * sum_{d in block} q1_d, outputs sum_t p_t z_v
+  constexpr bool ASYM = SCALE == KVQ3_SCALE_E4M3_ZP;
+  static_assert(!ASYM || PSPLIT, "the asymmetric variant splits P'");
   constexpr int EQ = D >= 128 ? D / 32 : 4;  // query rotation layout
   constexpr int LQ = D / EQ;
   constexpr int GPWQ = 32 / LQ;
@@ -620,7 +658,9 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
 
   // sign-bit patterns of the key windows, kept in registers (one LOP3 per pair)
   constexpr uint32_t kSignB = NBIT == 4 ? kSign4 : kSign2;
-  const uint32_t sgn0 = NBIT == 3 ? kSignRes0 : kSignB, sgn2 = NBIT == 3 ? kSignRes2 : kSignB;
+  // unsigned codes (ASYM) flip no sign bit: (x ^ 0) & M
+  const uint32_t sgn0 = ASYM ? 0u : NBIT == 3 ? kSignRes0 : kSignB;
+  const uint32_t sgn2 = ASYM ? 0u : NBIT == 3 ? kSignRes2 : kSignB;
   const uint32_t vsg0 = NBIT == 3 ? kSignVg0 : kSignB, vsg1 = kSignVg1, vsg2 = kSignVg2;
 
   // q1 fragments (B operand of QK^T): in registers for d = 128 with up to 8
@@ -641,6 +681,8 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
   float* kofs_s = reinterpret_cast<float*>(smem + SM::kKofsOff);
   float m[NTQ], l[NTQ];
   float acc[KS][NTP][4];
+  // ASYM: sum_t p_t z_v[t, block] of this lane's P' column (head 4tp + r/2)
+  float zacc[ASYM ? NTP : 1][ASYM ? NB : 1];
   int cur_unit = -1;
   bool cur_first = false, cur_last = false;
 
@@ -705,6 +747,20 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
         }
       }
     }
+    // ASYM: the zero-point sums of head 4tp + j: column 2j's lanes 8j..8j+3
+    // hold its tokens (the hi column; the lo column holds the same sums)
+    float zh[ASYM ? NTP : 1][ASYM ? NB : 1];
+    if constexpr (ASYM) {
+#pragma unroll
+      for (int tp = 0; tp < NTP; ++tp)
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          float z = zacc[tp][b];
+          z += __shfl_xor_sync(kFull, z, 1);
+          z += __shfl_xor_sync(kFull, z, 2);
+          zh[tp][b] = __shfl_sync(kFull, z, 8 * j);
+        }
+    }
     // warp 0 stores its weighted state, then warps 1..3 add theirs
     for (int pass = 0; pass < 2; ++pass) {
       if ((pass == 0) == (wid == 0)) {
@@ -720,7 +776,9 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
               const float sc = (float)(1 << (24 - v_off(NBIT, f)));   // value halves are c 2^(voff-24)
               if constexpr (PSPLIT) {
                 const int h = 4 * tp + j;
-                const float v = (acc[mt][tp][2 * e] + acc[mt][tp][2 * e + 1]) * sc * cpv[tp][0];
+                float v = (acc[mt][tp][2 * e] + acc[mt][tp][2 * e + 1]) * sc;
+                if constexpr (ASYM) v += zh[tp % (ASYM ? NTP : 1)][b % (ASYM ? NB : 1)];
+                v *= cpv[tp][0];
                 if (h < p.G) {
                   if (pass == 0) slot[h * D + dim] = v;
                   else atomicAdd(&slot[h * D + dim], v);
@@ -836,7 +894,8 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
         t += __shfl_xor_sync(kFull, t, 1);
         t += __shfl_xor_sync(kFull, t, 2);
         t += __shfl_xor_sync(kFull, t, 4);
-        const float ko = -(float)(1 << (NBIT - 1)) * 0x1p-24f * __shfl_sync(kFull, t, 8 * j);
+        // ASYM: no offset; the zero-point term needs 2^-24 sum_d q1_d instead
+        const float ko = (ASYM ? 1.0f : -(float)(1 << (NBIT - 1))) * 0x1p-24f * __shfl_sync(kFull, t, 8 * j);
         if constexpr (KOFS_REG) kofs[b][tq] = ko;
         else if (wid == 0 && r == 0) kofs_s[b * GPAD + 4 * tq + j] = ko;
       }
@@ -853,6 +912,10 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
       for (int tp = 0; tp < NTP; ++tp)
 #pragma unroll
         for (int c = 0; c < 4; ++c) acc[mt][tp][c] = 0.0f;
+#pragma unroll
+    for (int tp = 0; tp < (ASYM ? NTP : 1); ++tp)
+#pragma unroll
+      for (int b = 0; b < (ASYM ? NB : 1); ++b) zacc[tp][b] = 0.0f;
     named_barrier(1, 128);  // qs is rewritten at the next unit
   };
 
@@ -874,8 +937,10 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
 #pragma unroll
       for (int tq = 0; tq < NTQ; ++tq) {
         accq[b][tq][0] = accq[b][tq][2] = 0.0f;
-        accq[b][tq][1] = accq[b][tq][3] = KOFS_REG ? kofs[b % (KOFS_REG ? NB : 1)][tq % (KOFS_REG ? NTQ : 1)]
-                                                   : kofs_s[b * GPAD + 4 * tq + j];   // lo column
+        accq[b][tq][1] = accq[b][tq][3] =
+            ASYM ? 0.0f
+                 : KOFS_REG ? kofs[b % (KOFS_REG ? NB : 1)][tq % (KOFS_REG ? NTQ : 1)]
+                            : kofs_s[b * GPAD + 4 * tq + j];   // lo column
       }
     const uint32_t kt = pg + (uint32_t)(t0 * CB) + k_lane;   // token t0 + r
     static_for<NB>([&](auto bc) {
@@ -919,11 +984,16 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
         });
       });
     });
-    float skr[NB], skr8[NB];
+    float skr[NB], skr8[NB], zkr[NB], zkr8[NB];
     {
       const uint32_t a = pg + (uint32_t)(t0 * BPT) + ks_lane;
-      SDec::template one<0>(a, skr);
-      SDec::template one<8 * BPT>(a, skr8);
+      if constexpr (ASYM) {
+        SDec::template one_sz<0>(a, skr, zkr);
+        SDec::template one_sz<8 * BPT>(a, skr8, zkr8);
+      } else {
+        SDec::template one<0>(a, skr);
+        SDec::template one<8 * BPT>(a, skr8);
+      }
     }
     const bool vr = FULL || t0 + r < n_valid, vr8 = FULL || t0 + r + 8 < n_valid;
 #pragma unroll
@@ -931,6 +1001,12 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
       float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
+        if constexpr (ASYM) {   // + z_k * 2^-24 sum_{d in block} q1_d
+          const float qz = KOFS_REG ? kofs[b % (KOFS_REG ? NB : 1)][tq % (KOFS_REG ? NTQ : 1)]
+                                    : kofs_s[b * GPAD + 4 * tq + j];
+          s0 = fmaf(zkr[b], qz, s0);
+          s1 = fmaf(zkr8[b], qz, s1);
+        }
         s0 = fmaf(skr[b], accq[b][tq][0] + accq[b][tq][1], s0);
         s1 = fmaf(skr8[b], accq[b][tq][2] + accq[b][tq][3], s1);
       }
@@ -977,6 +1053,14 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
           for (int mt = 0; mt < KS; ++mt)
 #pragma unroll
             for (int c = 0; c < 4; ++c) acc[mt][tp][c] *= alpha[tp];
+        if constexpr (ASYM) {   // zacc belongs to head 4tp + r/2: lane r/2 holds its alpha
+#pragma unroll
+          for (int tp = 0; tp < NTP; ++tp) {
+            const float az = __shfl_sync(kFull, alpha[tp], r >> 1);
+#pragma unroll
+            for (int b = 0; b < NB; ++b) zacc[tp % (ASYM ? NTP : 1)][b % (ASYM ? NB : 1)] *= az;
+          }
+        }
       } else {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
@@ -1038,8 +1122,26 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
       float sv0[NB], sv1[NB], sv2[NB], sv3[NB];
       {
         const uint32_t a = pg + (uint32_t)(t0 * BPT) + vs_lane;
-        SDec::template two<0>(a, sv0, sv1);
-        SDec::template two<8 * BPT>(a, sv2, sv3);
+        if constexpr (ASYM) {
+          float zv0[NB], zv1[NB], zv2[NB], zv3[NB];
+          SDec::template two_sz<0>(a, sv0, sv1, zv0, zv1);
+          SDec::template two_sz<8 * BPT>(a, sv2, sv3, zv2, zv3);
+          // sum_t p_t z_v[t, block] for this lane's column (invalid tokens: 0,
+          // their scale bytes are stale stage contents)
+#pragma unroll
+          for (int tp = 0; tp < NTP; ++tp)
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+              float zs = v0 ? x0[tp] * zv0[b] : 0.0f;
+              zs = v1 ? fmaf(x1[tp], zv1[b], zs) : zs;
+              zs = v2 ? fmaf(x2[tp], zv2[b], zs) : zs;
+              zs = v3 ? fmaf(x3[tp], zv3[b], zs) : zs;
+              zacc[tp % (ASYM ? NTP : 1)][b % (ASYM ? NB : 1)] += zs;
+            }
+        } else {
+          SDec::template two<0>(a, sv0, sv1);
+          SDec::template two<8 * BPT>(a, sv2, sv3);
+        }
       }
       const bool lo_part = (r & 1) != 0;
 #pragma unroll
@@ -1117,10 +1219,10 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
       static_for<KSB>([&](auto mpc) {
         constexpr int mp = decltype(mpc)::value;
         uint32_t af[4];
-        af[0] = v_field<NBIT, 2 * mp>(c0v, c1v, vsg0, vsg1, vsg2);
-        af[1] = v_field<NBIT, 2 * mp + 1>(c0v, c1v, vsg0, vsg1, vsg2);
-        af[2] = v_field<NBIT, 2 * mp>(c2v, c3v, vsg0, vsg1, vsg2);
-        af[3] = v_field<NBIT, 2 * mp + 1>(c2v, c3v, vsg0, vsg1, vsg2);
+        af[0] = v_field<NBIT, 2 * mp, ASYM>(c0v, c1v, vsg0, vsg1, vsg2);
+        af[1] = v_field<NBIT, 2 * mp + 1, ASYM>(c0v, c1v, vsg0, vsg1, vsg2);
+        af[2] = v_field<NBIT, 2 * mp, ASYM>(c2v, c3v, vsg0, vsg1, vsg2);
+        af[3] = v_field<NBIT, 2 * mp + 1, ASYM>(c2v, c3v, vsg0, vsg1, vsg2);
 #pragma unroll
         for (int tp = 0; tp < NTP; ++tp) mma_16816(acc[b * KSB + mp][tp], af, pb[b][tp][0], pb[b][tp][1]);
       });
@@ -1422,6 +1524,7 @@ kvq3_status decode_run_t(const DecodePlan& plan, DecodeParams prm, const RotPara
 KVQ3_DECODE_DECL(64, f32) KVQ3_DECODE_DECL(64, f16) KVQ3_DECODE_DECL(64, e4m3)
 KVQ3_DECODE_DECL(128, f32) KVQ3_DECODE_DECL(128, f16) KVQ3_DECODE_DECL(128, e4m3)
 KVQ3_DECODE_DECL(256, f32) KVQ3_DECODE_DECL(256, f16) KVQ3_DECODE_DECL(256, e4m3)
+KVQ3_DECODE_DECL1(64, e4m3zp, 3) KVQ3_DECODE_DECL1(128, e4m3zp, 3) KVQ3_DECODE_DECL1(256, e4m3zp, 3)
 
 // P' split into hi + lo halves for fp32 value scales (p times an fp32 scale is
 // not an fp16 value) and for up to 4 heads per kv head, where the split
@@ -1429,7 +1532,7 @@ KVQ3_DECODE_DECL(256, f32) KVQ3_DECODE_DECL(256, f16) KVQ3_DECODE_DECL(256, e4m3
 // rounding of P' from the error.
 #define KVQ3_DECODE_PICK(D, BLK, SC, NB, FN, ...)                                             \
   {                                                                                           \
-    constexpr bool SPLIT = (SC) == KVQ3_SCALE_F32;                                            \
+    constexpr bool SPLIT = (SC) == KVQ3_SCALE_F32 || (SC) == KVQ3_SCALE_E4M3_ZP;              \
     if (gp == 4) return FN<D, BLK, 4, SC, NB, true>(__VA_ARGS__);                             \
     if (gp == 8) return FN<D, BLK, 8, SC, NB, SPLIT>(__VA_ARGS__);                            \
     return FN<D, BLK, 16, SC, NB, SPLIT>(__VA_ARGS__);                                        \

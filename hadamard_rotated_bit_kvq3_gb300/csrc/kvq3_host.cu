@@ -82,15 +82,19 @@ kvq3_status make_geom(const kvq3_cache_desc* desc, CacheGeom* g) {
       desc->max_pages_per_seq < 1 || desc->num_pages < 1 || desc->page_size < 16 ||
       desc->page_size % 16 != 0 || desc->page_size > 4096 || desc->reserved != 0 ||
       !(desc->eps >= 0.0f) || !isfinite(desc->eps) || desc->block < 1 || d % desc->block != 0 ||
-      desc->scale_type < KVQ3_SCALE_F32 || desc->scale_type > KVQ3_SCALE_E4M3)
+      desc->scale_type < KVQ3_SCALE_F32 || desc->scale_type > KVQ3_SCALE_E4M3_ZP)
     return KVQ3_ERR_INVALID_ARG;
   if (desc->bits < 2 || desc->bits > 4) return KVQ3_ERR_UNSUPPORTED;
+  if (desc->scale_type == KVQ3_SCALE_E4M3_ZP && desc->bits != 3) return KVQ3_ERR_UNSUPPORTED;
   if (d < 64 || (desc->block != 32 && desc->block != 64)) return KVQ3_ERR_UNSUPPORTED;
   g->d = d;
   g->hkv = desc->num_kv_heads;
   g->block = desc->block;
   g->nb = d / desc->block;
-  g->sb = desc->scale_type == KVQ3_SCALE_F32 ? 4 : desc->scale_type == KVQ3_SCALE_F16 ? 2 : 1;
+  // bytes per block of the scale header: the asymmetric variant stores
+  // (scale, zero point) as two E4M3 bytes
+  g->sb = desc->scale_type == KVQ3_SCALE_F32 ? 4
+        : desc->scale_type == KVQ3_SCALE_F16 || desc->scale_type == KVQ3_SCALE_E4M3_ZP ? 2 : 1;
   g->bits = desc->bits;
   g->cb = desc->bits * d / 8;
   g->page_size = desc->page_size;

@@ -116,21 +116,48 @@ __global__ void __launch_bounds__(256) write_kernel(
     }
     rotate_forward<E, L>(x, r, sgn, q, inv_sqrt_d, so4);
 
-    // block maximum: this lane's E elements lie in one block of LPB lanes
-    float amax = 0.0f;
+    // this lane's E elements lie in one block of LPB lanes
+    uint32_t sbits, bits = 0;
+    if (g.scale_type != KVQ3_SCALE_E4M3_ZP) {
+      // block maximum -> symmetric scale, two's-complement codes
+      float amax = 0.0f;
 #pragma unroll
-    for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(x[e]));
+      for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(x[e]));
 #pragma unroll
-    for (int m = 1; m < LPB; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, m));
-    const float s = __fdiv_rn(amax + g.eps, (float)QMAX);
-    uint32_t sbits;
-    const float sq = round_scale(s, g.scale_type, sbits);
-    const float inv = sq > 0.0f ? __frcp_rn(sq) : 0.0f;
-    uint32_t bits = 0;
+      for (int m = 1; m < LPB; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, m));
+      const float s = __fdiv_rn(amax + g.eps, (float)QMAX);
+      const float sq = round_scale(s, g.scale_type, sbits);
+      const float inv = sq > 0.0f ? __frcp_rn(sq) : 0.0f;
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-      const float c = fminf(fmaxf(rintf(x[e] * inv), -(float)QMAX), (float)QMAX);
-      bits |= ((uint32_t)(int)c & ((1u << NBIT) - 1u)) << (NBIT * e);
+      for (int e = 0; e < E; ++e) {
+        const float c = fminf(fmaxf(rintf(x[e] * inv), -(float)QMAX), (float)QMAX);
+        bits |= ((uint32_t)(int)c & ((1u << NBIT) - 1u)) << (NBIT * e);
+      }
+    } else {
+      // asymmetric variant: block minimum and maximum -> E4M3 scale
+      // (max - min + eps)/(2^b - 1) and E4M3 zero point min, unsigned codes
+      constexpr float UMAX = (float)((1 << NBIT) - 1);
+      float mx = -INFINITY, mn = INFINITY;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        mx = fmaxf(mx, x[e]);
+        mn = fminf(mn, x[e]);
+      }
+#pragma unroll
+      for (int m = 1; m < LPB; m <<= 1) {
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, m));
+        mn = fminf(mn, __shfl_xor_sync(kFull, mn, m));
+      }
+      uint32_t sb8, zb8;
+      const float sq = round_scale(__fdiv_rn((mx - mn) + g.eps, UMAX), KVQ3_SCALE_E4M3, sb8);
+      const float zq = round_scale(mn, KVQ3_SCALE_E4M3, zb8);
+      sbits = sb8 | (zb8 << 8);       // scale byte, then zero-point byte
+      const float inv = sq > 0.0f ? __frcp_rn(sq) : 0.0f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const float u = fminf(fmaxf(rintf((x[e] - zq) * inv), 0.0f), UMAX);
+        bits |= (uint32_t)u << (NBIT * e);
+      }
     }
     // word w of the code string collects bits [32w, 32w+32) from the lanes
     // whose [BITS*r, BITS*r + BITS) ranges overlap it
@@ -230,7 +257,9 @@ __global__ void __launch_bounds__(256) dequant_kernel(
         const uint8_t* sp = rec + ((int64_t)slot * g.nb + blk) * g.sb;
         uint32_t sbits = 0;
         for (int i = 0; i < g.sb; ++i) sbits |= (uint32_t)sp[i] << (8 * i);
-        const float sq = decode_scale(sbits, g.scale_type);
+        const bool asym = g.scale_type == KVQ3_SCALE_E4M3_ZP;   // x_hat = s_q u + z_q
+        const float sq = decode_scale(sbits & (asym ? 0xffu : ~0u), g.scale_type);
+        const float zq = asym ? decode_scale(sbits >> 8, KVQ3_SCALE_E4M3) : 0.0f;
         const int nbit = g.bits, half = 1 << (nbit - 1);
 #pragma unroll
         for (int e = 0; e < E; ++e) {
@@ -238,6 +267,11 @@ __global__ void __launch_bounds__(256) dequant_kernel(
           const uint32_t two = (uint32_t)codes[bit / 8] |
                                ((bit / 8 + 1 < g.cb) ? (uint32_t)codes[bit / 8 + 1] << 8 : 0u);
           const int f = (int)((two >> (bit % 8)) & ((1u << nbit) - 1u));
+          if (asym) {
+            c[e] = f;
+            x[e] = fmaf(sq, (float)f, zq);
+            continue;
+          }
           int cv = f >= half ? f - 2 * half : f;
           if (cv == -half) {   // the value the quantiser never writes
             bad |= KVQ3_DEV_BAD_CODE;

@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(kTile) write_chunk_kernel(const __grid_constan
   constexpr int NB = D / BLOCK;
   constexpr int CB = NBIT * D / 8;      // code bytes (16 .. 64)
   constexpr int QMAX = (1 << (NBIT - 1)) - 1;
-  constexpr int SB = SCALE == KVQ3_SCALE_F32 ? 4 : SCALE == KVQ3_SCALE_F16 ? 2 : 1;
+  constexpr int SB = SCALE == KVQ3_SCALE_F32 ? 4 : (SCALE == KVQ3_SCALE_F16 || SCALE == KVQ3_SCALE_E4M3_ZP) ? 2 : 1;
   extern __shared__ __align__(128) uint8_t smem[];
   const int t = threadIdx.x;
   const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem);
@@ -214,6 +214,35 @@ __global__ void __launch_bounds__(kTile) write_chunk_kernel(const __grid_constan
     uint32_t sbits[NB];
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
+      if constexpr (SCALE == KVQ3_SCALE_E4M3_ZP) {
+        // asymmetric variant: E4M3 scale (max - min + eps)/(2^b - 1) and E4M3
+        // zero point min; unsigned codes round((x - z_q)/s_q) clipped to [0, 2^b - 1]
+        constexpr float UMAX = (float)((1 << NBIT) - 1);
+        float mx = -INFINITY, mn = INFINITY;
+#pragma unroll
+        for (int j = b * BLOCK; j < (b + 1) * BLOCK; ++j) {
+          const float xv = j < H ? x2[j].x : x2[j - H].y;
+          mx = fmaxf(mx, xv);
+          mn = fminf(mn, xv);
+        }
+        uint32_t sb8, zb8;
+        const float sq = round_scale(__fdiv_rn((mx - mn) * post + g.eps, UMAX), KVQ3_SCALE_E4M3, sb8);
+        const float zq = round_scale(mn * post, KVQ3_SCALE_E4M3, zb8);
+        sbits[b] = sb8 | (zb8 << 8);
+        const float r = sq > 0.0f ? __frcp_rn(sq) : 0.0f;
+        const float inv = r * post, zoff = -zq * r;
+#pragma unroll
+        for (int j = b * BLOCK; j < (b + 1) * BLOCK; ++j) {
+          const float xv = j < H ? x2[j].x : x2[j - H].y;
+          float tq = fmaf(xv, inv, zoff) + 12582912.0f;      // 1.5 * 2^23 + rint((x - z_q) / s_q)
+          tq = fminf(fmaxf(tq, 12582912.0f), 12582912.0f + UMAX);
+          const uint32_t c = __float_as_uint(tq) & ((1u << NBIT) - 1u);
+          const int bit = NBIT * j;
+          words[bit / 32] |= c << (bit % 32);
+          if (bit % 32 > 32 - NBIT) words[bit / 32 + 1] |= c >> (32 - bit % 32);
+        }
+        continue;
+      }
       float amax = 0.0f;
 #pragma unroll
       for (int j = b * BLOCK; j < (b + 1) * BLOCK; ++j)
@@ -250,7 +279,10 @@ __global__ void __launch_bounds__(kTile) write_chunk_kernel(const __grid_constan
         for (int w = 0; w < CB / 8; ++w) cd[w] = make_uint2(words[2 * w], words[2 * w + 1]);
       }
       uint8_t* sp = rec + (int64_t)slot * NB * SB;
-      if constexpr (SB == 4) {
+      if constexpr (SCALE == KVQ3_SCALE_E4M3_ZP) {   // (scale, zero point) byte pairs
+#pragma unroll
+        for (int b = 0; b < NB; ++b) reinterpret_cast<uint16_t*>(sp)[b] = (uint16_t)sbits[b];
+      } else if constexpr (SB == 4) {
 #pragma unroll
         for (int b = 0; b < NB; ++b) reinterpret_cast<uint32_t*>(sp)[b] = sbits[b];
       } else if constexpr (SB == 2) {
@@ -282,6 +314,7 @@ cudaError_t launch_chunk_b(const ChunkParams& p, cudaStream_t st) {
 
 template <int D, int BLOCK, int SCALE, bool SO4>
 cudaError_t launch_chunk(const ChunkParams& p, cudaStream_t st) {
+  if constexpr (SCALE == KVQ3_SCALE_E4M3_ZP) return launch_chunk_b<D, BLOCK, SCALE, SO4, 3>(p, st);   // 3-bit only
   if (p.g.bits == 2) return launch_chunk_b<D, BLOCK, SCALE, SO4, 2>(p, st);
   if (p.g.bits == 4) return launch_chunk_b<D, BLOCK, SCALE, SO4, 4>(p, st);
   return launch_chunk_b<D, BLOCK, SCALE, SO4, 3>(p, st);
@@ -293,6 +326,8 @@ cudaError_t dispatch_chunk(const ChunkParams& p, int scale, bool so4, cudaStream
     return so4 ? launch_chunk<D, BLOCK, KVQ3_SCALE_F32, true>(p, st) : launch_chunk<D, BLOCK, KVQ3_SCALE_F32, false>(p, st);
   if (scale == KVQ3_SCALE_F16)
     return so4 ? launch_chunk<D, BLOCK, KVQ3_SCALE_F16, true>(p, st) : launch_chunk<D, BLOCK, KVQ3_SCALE_F16, false>(p, st);
+  if (scale == KVQ3_SCALE_E4M3_ZP)
+    return so4 ? launch_chunk<D, BLOCK, KVQ3_SCALE_E4M3_ZP, true>(p, st) : launch_chunk<D, BLOCK, KVQ3_SCALE_E4M3_ZP, false>(p, st);
   return so4 ? launch_chunk<D, BLOCK, KVQ3_SCALE_E4M3, true>(p, st) : launch_chunk<D, BLOCK, KVQ3_SCALE_E4M3, false>(p, st);
 }
 

@@ -61,6 +61,15 @@
  *       little-endian bit stream of 3d/8 bytes (bit k of the stream is bit
  *       k%8 of byte k/8).  Blocks are consecutive rotated coordinates
  *       [0,m), [m,2m), ...
+ *   R18 The asymmetric variant of [HFF] ("3-bit unsigned integers paired
+ *       with a shared FP8 scale and zero-point header" per 64-element
+ *       sub-block), scale type KVQ3_SCALE_E4M3_ZP: per block z = min x and
+ *       s = (max x - min x + eps)/7, each stored as one E4M3 byte (RNE,
+ *       saturating; scale byte first), unsigned codes
+ *       u = clip(round((x - z_q)/s_q), 0, 7) (u = 0 where s_q == 0) in the
+ *       R9 bit stream, x_hat = s_q*u + z_q.  Two header bytes per block
+ *       (3.25 bits per element at m = 64): the page's 3.125-bit figure would
+ *       leave one byte for both and is not followed.  3-bit codes only.
  *   R17 Other code widths b = 2 and 4 ([OIQ] 3.3 stores d*b bits per
  *       vector, 4.2 packs INT3/INT4 values, 5.1 evaluates b = 4, 3, 2; [OMC]
  *       writes its quantiser for any b): divisor and clip bound
@@ -129,7 +138,9 @@ typedef enum {
 typedef enum {
   KVQ3_SCALE_F32 = 0,
   KVQ3_SCALE_F16 = 1,
-  KVQ3_SCALE_E4M3 = 2
+  KVQ3_SCALE_E4M3 = 2,
+  KVQ3_SCALE_E4M3_ZP = 3      /* asymmetric variant (R18): E4M3 scale and E4M3
+                                 zero point per block, unsigned codes; b = 3 */
 } kvq3_scale_type;
 
 /* Rotation flags.  H_d is always applied. */

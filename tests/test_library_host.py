@@ -81,6 +81,16 @@ def test_cache_sizes_match_oracle_layout(K, oracle, d, block, scale, page, bits)
     assert rb % 16 == 0
 
 
+@pytest.mark.parametrize("d,block,page", [(128, 64, 16), (256, 64, 16), (64, 32, 32)])
+def test_cache_sizes_match_oracle_layout_asym(K, oracle, d, block, page):
+    # the asymmetric variant: (scale, zero point) byte pairs, 3-bit codes
+    desc = K.CacheDesc(d, 2, block, 3, K.SCALE_TYPES["e4m3zp"], 1e-6, page, 2, 5, 0, 11)
+    rb, pb, tb = K.kvq3_cache_sizes(desc)
+    L = oracle.Layout(d, 2, block, "e4m3zp", page, 2, 5, 11)
+    assert (rb, pb, tb) == (L.record_bytes, L.page_bytes, L.pool_bytes)
+    assert rb == page * (2 * (d // block) + 3 * d // 8)
+
+
 def test_invalid_descriptions_rejected_on_host(K):
     def desc(**kw):
         base = dict(head_dim=128, num_kv_heads=2, block=64, bits=3, scale_type=1, eps=1e-6,
@@ -90,6 +100,7 @@ def test_invalid_descriptions_rejected_on_host(K):
     assert K.kvq3_cache_sizes(desc())[0] == 832
     for kw, want in [(dict(head_dim=96), 1), (dict(block=48), 1), (dict(page_size=8), 1),
                      (dict(bits=5), 2), (dict(bits=1), 2), (dict(block=16), 2), (dict(scale_type=7), 1),
+                     (dict(scale_type=3, bits=2), 2), (dict(scale_type=3, bits=4), 2), (dict(scale_type=4), 1),
                      (dict(num_kv_heads=0), 1), (dict(eps=float("nan")), 1), (dict(head_dim=32, block=32), 2)]:
         with pytest.raises(K.Kvq3Error) as e:
             K.kvq3_cache_sizes(desc(**kw))
