@@ -61,9 +61,9 @@
  *       little-endian bit stream of 3d/8 bytes (bit k of the stream is bit
  *       k%8 of byte k/8).  Blocks are consecutive rotated coordinates
  *       [0,m), [m,2m), ...
- *   R18 The asymmetric variant of [HFF] ("3-bit unsigned integers paired
- *       with a shared FP8 scale and zero-point header" per 64-element
- *       sub-block), scale type KVQ3_SCALE_E4M3_ZP: per block z = min x and
+ *   R18 The asymmetric variant of [HFF] (per 64-element sub-block: unsigned
+ *       3-bit codes and an FP8 header with a scale and a zero point), scale
+ *       type KVQ3_SCALE_E4M3_ZP: per block z = min x and
  *       s = (max x - min x + eps)/7, each stored as one E4M3 byte (RNE,
  *       saturating; scale byte first), unsigned codes
  *       u = clip(round((x - z_q)/s_q), 0, 7) (u = 0 where s_q == 0) in the

@@ -342,8 +342,8 @@ def quantize(x: np.ndarray, block: int, eps: float, kind: str, bits: int = 3):
 
 
 def quantize_asym(x: np.ndarray, block: int, eps: float, bits: int = 3):
-    """The asymmetric variant of [HFF] ("3-bit unsigned integers paired with
-    a shared FP8 scale and zero-point header", per 64-element sub-block):
+    """The asymmetric variant of [HFF] (each 64-element sub-block keeps
+    unsigned 3-bit codes and an FP8 header with a scale and a zero point):
     per block, z = min x and s = (max x - min x + eps)/(2^b - 1), both
     stored in E4M3 (round half to even, saturating; z keeps its sign), and
     unsigned codes u = clip(round_half_even((x - z_q)/s_q), 0, 2^b - 1)

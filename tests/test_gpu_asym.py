@@ -1,8 +1,8 @@
 """The asymmetric variant (scale type "e4m3zp") on the GPU against the oracle.
 
-"Hardware-Fused Fast Hadamard Transforms ...": each 64-element sub-block is
-stored as 3-bit unsigned integers with an FP8 scale and zero point; the
-library's reading: z = min, s = (max - min + eps)/7, both E4M3, unsigned
+"Hardware-Fused Fast Hadamard Transforms ...": per 64-element sub-block,
+unsigned 3-bit codes plus an FP8 scale and an FP8 zero point; the library's
+reading: z = min, s = (max - min + eps)/7, both E4M3, unsigned
 codes u = clip(round((x - z_q)/s_q), 0, 7), x_hat = s_q u + z_q.
 
 Bars as for the symmetric codes: codes bit-exact except elements whose
