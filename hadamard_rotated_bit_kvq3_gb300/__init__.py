@@ -17,7 +17,7 @@ __all__ = [
     "kvq3_rotation_create_from_params", "kvq3_rotation_destroy", "kvq3_rotation_export",
     "kvq3_cache_sizes", "kvq3_rotate", "kvq3_write", "kvq3_write_chunk", "kvq3_decode_workspace_size",
     "kvq3_decode_attn", "kvq3_decode_attn_noalloc", "kvq3_prefill_workspace_size", "kvq3_prefill_attn",
-    "kvq3_dequant_debug", "Rotation",
+    "kvq3_dequant_debug", "kvq3_calib_sse", "kvq3_calibrate_workspace_size", "kvq3_calibrate_so4", "Rotation",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -73,6 +73,9 @@ _SIGS = {
     "kvq3_prefill_workspace_size": (ctypes.c_int, [_D, _i32, _i64, ctypes.POINTER(_sz)]),
     "kvq3_prefill_attn": (ctypes.c_int, [_p, _D, _C, _i32, _i64, _i64, _p, _i32, _f32, _p, _p, _sz, _p, _p]),
     "kvq3_dequant_debug": (ctypes.c_int, [_p, _D, _C, _i32, _i32, _i32, _i64, _i64, _p, _p, _p, _p]),
+    "kvq3_calib_sse": (ctypes.c_int, [_p, _D, _p, _i32, _p, _i64, _p, _p]),
+    "kvq3_calibrate_workspace_size": (ctypes.c_int, [_D, _i32, ctypes.POINTER(_sz)]),
+    "kvq3_calibrate_so4": (ctypes.c_int, [_p, _D, _p, _i64, _i32, _i32, _f32, _u64, _p, _sz, _p, _p, _p]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -221,6 +224,36 @@ def kvq3_prefill_attn(h, desc: CacheDesc, cache: Cache, seq: int, pos0: int, q, 
                                  _ptr(out), _ptr(workspace),
                                  workspace.numel() * workspace.element_size(), _ptr(dev_status),
                                  _stream(stream)), "kvq3_prefill_attn")
+
+
+def kvq3_calib_sse(h, desc: CacheDesc, quats, x, sse, stream=None) -> None:
+    """quats: fp32 CUDA [P][d/4][4] candidate quaternion sets; x: fp16 CUDA
+    [n][d] sample vectors; sse: fp64 CUDA [P][d/m] (overwritten)."""
+    _check(lib.kvq3_calib_sse(h, ctypes.byref(desc), _ptr(quats), int(quats.shape[0]), _ptr(x),
+                              int(x.shape[0]), _ptr(sse), _stream(stream)), "kvq3_calib_sse")
+
+
+def kvq3_calibrate_workspace_size(desc: CacheDesc, num_candidates: int) -> int:
+    n = _sz()
+    _check(lib.kvq3_calibrate_workspace_size(ctypes.byref(desc), num_candidates, ctypes.byref(n)),
+           "kvq3_calibrate_workspace_size")
+    return n.value
+
+
+def kvq3_calibrate_so4(h, desc: CacheDesc, x, rounds: int, num_candidates: int, step: float, seed: int,
+                       workspace, stream=None):
+    """Returns (quats float32 [d/4][4], sse float64 [d/m]) as numpy arrays; x:
+    fp16 CUDA [n][d]; workspace: uint8 CUDA tensor of
+    kvq3_calibrate_workspace_size bytes.  Synchronises the stream."""
+    import numpy as np
+    d = desc.head_dim
+    q = np.zeros((d // 4, 4), np.float32)
+    e = np.zeros(d // desc.block, np.float64)
+    _check(lib.kvq3_calibrate_so4(h, ctypes.byref(desc), _ptr(x), int(x.shape[0]), rounds, num_candidates,
+                                  float(step), seed & ((1 << 64) - 1), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), q.ctypes.data_as(_p),
+                                  e.ctypes.data_as(_p), _stream(stream)), "kvq3_calibrate_so4")
+    return q, e
 
 
 def kvq3_dequant_debug(h, desc: CacheDesc, cache: Cache, seq: int, kv_head: int, which: int,

@@ -70,6 +70,12 @@
  *       R9 bit stream, x_hat = s_q*u + z_q.  Two header bytes per block
  *       (3.25 bits per element at m = 64): the page's 3.125-bit figure would
  *       leave one byte for both and is not followed.  3-bit codes only.
+ *   R19 SO(4) calibration (kvq3_calibrate_so4): the page asks for the
+ *       quaternions that minimise the post-quantisation reconstruction MSE
+ *       on sample vectors and names no search; taken as a random local
+ *       search that keeps, per quantisation block, the best of the current
+ *       set and perturbed copies, one quaternion per block (the general
+ *       two-quaternion SO(4) is not used).
  *   R17 Other code widths b = 2 and 4 ([OIQ] 3.3 stores d*b bits per
  *       vector, 4.2 packs INT3/INT4 values, 5.1 evaluates b = 4, 3, 2; [OMC]
  *       writes its quantiser for any b): divisor and clip bound
@@ -337,6 +343,48 @@ kvq3_status kvq3_dequant_debug(kvq3_rotation rot, const kvq3_cache_desc *desc,
                                int32_t kv_head, int32_t which, int64_t t0,
                                int64_t nt, float *out, int32_t *codes_out,
                                int32_t *dev_status, void *stream);
+
+/* ---- SO(4) calibration ([OMC] Implementation notes: calibrate the fixed
+ * random rotations on representative sequences by minimising the
+ * reconstruction MSE after quantisation, each SO(4) block a normalised
+ * quaternion).  Offline tools, not on the decode path.
+ *
+ * kvq3_calib_sse: for num_candidates (P) quaternion sets, the squared
+ * reconstruction error of the sample under each, per quantisation block:
+ * sse[p][j] = sum over the n vectors and the coordinates i of block j of
+ * (y_i - y_hat_i)^2, y = B_p H D x (the rotation's signs, candidate p's
+ * quaternions, SO(4) blocks always applied) and y_hat its quantised value
+ * under desc's block size, code width, scale format and eps (the write
+ * path's arithmetic, fp32).  Since U is orthogonal, sum_j sse[p][j] is the
+ * error of U^T y_hat against x.
+ * quats: device fp32 [P][d/4][4], 16-byte aligned; x: device fp16 [n][d],
+ * 16-byte aligned; sse: device fp64 [P][d/block], overwritten.  Only d,
+ * block, bits, scale_type and eps of desc are used (the rest must still be
+ * valid).  1 <= P <= 65535; n = 0 gives zeros. */
+kvq3_status kvq3_calib_sse(kvq3_rotation rot, const kvq3_cache_desc *desc, const float *quats,
+                           int32_t num_candidates, const void *x, int64_t n, double *sse,
+                           void *stream);
+
+/* Device workspace bytes of kvq3_calibrate_so4 with num_candidates (>= 2). */
+kvq3_status kvq3_calibrate_workspace_size(const kvq3_cache_desc *desc, int32_t num_candidates,
+                                          size_t *bytes);
+
+/* Random local search over the quaternions of rot (reading R19): each of
+ * `rounds` rounds evaluates the current set and num_candidates - 1 copies in
+ * which every quaternion moves by sigma * (uniform [-1,1)^4, SplitMix64
+ * seeded with `seed`) and is renormalised, with sigma = step * (1 - t/rounds)
+ * in round t, in one kvq3_calib_sse launch; every quantisation block keeps
+ * the candidate with the lowest error (ties: the current set), which is
+ * possible because block j of y depends only on its own m/4 quaternions.
+ * So no block's error ever rises.  quats_out: host fp32 [d/4][4] (the rotation
+ * itself is not changed: kvq3_rotation_create_from_params makes the
+ * calibrated one); sse_out (nullable): host fp64 [d/block], the final error.
+ * workspace: device, >= kvq3_calibrate_workspace_size bytes, 256-byte
+ * aligned.  Synchronises the stream once per round (host decisions). */
+kvq3_status kvq3_calibrate_so4(kvq3_rotation rot, const kvq3_cache_desc *desc, const void *x,
+                               int64_t n, int32_t rounds, int32_t num_candidates, float step,
+                               uint64_t seed, void *workspace, size_t ws_bytes, float *quats_out,
+                               double *sse_out, void *stream);
 
 #ifdef __cplusplus
 }

@@ -364,6 +364,28 @@ def quantize_asym(x: np.ndarray, block: int, eps: float, bits: int = 3):
     return u.reshape(n, d), np.stack([sq, zq], axis=-1), s
 
 
+def calib_sse(x: np.ndarray, signs: np.ndarray, quats: np.ndarray, block: int, kind: str,
+              bits: int = 3, eps: float = 1e-6) -> np.ndarray:
+    """Objective of the SO(4) calibration ([OMC] Implementation notes:
+    reconstruction MSE after quantisation, SO(4) blocks as normalised
+    quaternions): per quantisation block j, the sum over the sample vectors
+    x (fp64 [n][d]) and the coordinates of block j of (y - y_hat)^2, with
+    y = B H D x for these signs and quaternions (SO(4) blocks applied) and
+    y_hat its quantised value (symmetric codes, or the asymmetric variant for
+    kind "e4m3zp").  Returns fp64 [d/block]."""
+    U = rotation_matrix(np.asarray(signs), np.asarray(quats, dtype=np.float64))
+    y = np.asarray(x, dtype=np.float64) @ U.T
+    n, d = y.shape
+    eps = float(np.float32(eps))
+    if kind == "e4m3zp":
+        u, sz, _ = quantize_asym(y, block, eps, bits)
+        yh = (u.reshape(n, d // block, block) * sz[..., 0:1] + sz[..., 1:2]).reshape(n, d)
+    else:
+        c, sq, _ = quantize(y, block, eps, kind, bits)
+        yh = (c.reshape(n, d // block, block) * sq[..., None]).reshape(n, d)
+    return ((y - yh) ** 2).reshape(n, d // block, block).sum(axis=(0, 2))
+
+
 def pack_codes(codes: np.ndarray, bits: int = 3) -> np.ndarray:
     """b-bit two's-complement codes [..., d] -> bytes [..., b*d/8]: element j
     at bits b*j..b*j+b-1 of a little-endian bit stream (bit k of the stream is
