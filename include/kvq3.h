@@ -131,7 +131,7 @@
 extern "C" {
 #endif
 
-#define KVQ3_ABI_VERSION 1
+#define KVQ3_ABI_VERSION 2   /* 2: code widths 2-4, the asymmetric scale type, calibration */
 
 typedef enum {
   KVQ3_OK = 0,

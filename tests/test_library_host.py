@@ -36,7 +36,7 @@ def test_every_declared_symbol_is_exported(K):
 
 
 def test_abi_and_status_strings(K):
-    assert K.kvq3_abi_version() == 1
+    assert K.kvq3_abi_version() == 2
     assert K.kvq3_status_string(0) == "ok"
     assert "workspace" in K.kvq3_status_string(4)
 
