@@ -26,7 +26,7 @@ def _oracle_unit(oracle, w, lens, b, kvh, table_row=None):
     L = int(lens[b])
     P = w.page_size
     maxp = int(math.ceil(L / P))
-    lay = oracle.Layout(w.d, 1, w.block, w.scale, P, 1, maxp, maxp)
+    lay = oracle.Layout(w.d, 1, w.block, w.scale, P, 1, maxp, maxp, w.bits)
     s, q = oracle.rotation_params(w.d, w.rot_seed, bool(w.rot_flags & 1), bool(w.rot_flags & 2))
     U = oracle.rotation_matrix(s, q)
     k = I.kv_rows_np(w.data, 0, b, kvh, 0, L)
@@ -41,12 +41,23 @@ def _check_codes(oracle, w, st, gp, lay_full, b, kvh, U, src, which, t0, nt):
     against the oracle's quantisation of the same input rows."""
     _, cg, sg = oracle.read_rotated(gp, lay_full, b, kvh, which, t0, nt, st.table_np)
     x = src[t0:t0 + nt].astype(np.float64) @ U.T
-    c, sq, s = oracle.quantize(x, w.block, w.eps, w.scale)
-    mid = oracle.scale_midpoint_distance(s, w.scale) < MIDPOINT
-    assert np.all(np.abs(sg - sq)[~mid] <= 1e-6 * sq[~mid])
-    r = np.abs(x.reshape(nt, -1, w.block) / np.where(sq > 0, sq, 1)[..., None])
+    if w.scale == "e4m3zp":   # asymmetric variant: (scale, zero point) pairs, unsigned codes
+        c, sz, s = oracle.quantize_asym(x, w.block, w.eps, w.bits)
+        lo = x.reshape(nt, -1, w.block).min(-1)
+        mid = (oracle.scale_midpoint_distance(s, "e4m3") < MIDPOINT) | \
+              (oracle.scale_midpoint_distance(np.abs(lo), "e4m3") < MIDPOINT)
+        assert np.array_equal(sg[~mid], sz[~mid])
+        sq, zq = sz[..., 0], sz[..., 1]
+        r = (x.reshape(nt, -1, w.block) - zq[..., None]) / np.where(sq > 0, sq, 1)[..., None]
+        top = (1 << w.bits) - 1
+    else:
+        c, sq, s = oracle.quantize(x, w.block, w.eps, w.scale, w.bits)
+        mid = oracle.scale_midpoint_distance(s, w.scale) < MIDPOINT
+        assert np.all(np.abs(sg - sq)[~mid] <= 1e-6 * sq[~mid])
+        r = np.abs(x.reshape(nt, -1, w.block) / np.where(sq > 0, sq, 1)[..., None])
+        top = oracle.qmax(w.bits)
     near = np.zeros(r.shape, bool)
-    for kk in range(3):
+    for kk in range(top):
         near |= np.abs(r - (kk + 0.5)) < BOUNDARY
     near = (near | mid[..., None]).reshape(nt, w.d)
     assert not np.any((cg != c) & ~near)
@@ -67,7 +78,7 @@ def test_fullsize_decode_step(oracle, name, samples):
     out = st.out.cpu().numpy().astype(np.float64)
     w = st.w
     lay_full = oracle.Layout(w.d, w.num_kv_heads, w.block, w.scale, w.page_size, w.batch, st.maxp,
-                             st.num_pages)
+                             st.num_pages, w.bits)
     q = I.q_np(w.data, w.batch, w.num_q_heads)
     gp = st.pool.cpu().numpy()
     got, ref = [], []
@@ -89,6 +100,19 @@ def test_fullsize_decode_step(oracle, name, samples):
     err = float(np.abs(got - ref).max())
     print(f"{name}: max|err|/rms = {err / rms:.3e}")
     assert err <= TOL_DECODE * rms
+
+
+@pytest.mark.parametrize("bits,scale", [(2, ""), (4, ""), (0, "e4m3zp")], ids=["b2", "b4", "asym"])
+def test_fullsize_decode_step_other_formats(oracle, bits, scale):
+    # the llama8b workload at the other code widths and in the asymmetric
+    # variant, as bench.py --bits / --scale runs it
+    import bench
+    saved = bench.BITS_OVERRIDE, bench.SCALE_OVERRIDE
+    bench.BITS_OVERRIDE, bench.SCALE_OVERRIDE = bits, scale
+    try:
+        test_fullsize_decode_step(oracle, "llama8b", [(0, 0), (15, 7)])
+    finally:
+        bench.BITS_OVERRIDE, bench.SCALE_OVERRIDE = saved
 
 
 def test_fullsize_prefill_write(oracle):
