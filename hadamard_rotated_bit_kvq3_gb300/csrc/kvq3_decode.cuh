@@ -27,17 +27,20 @@
 //    the partials of each (sequence, query head) with the log-sum-exp rule
 //    and applies U^T.
 //  * QK^T and PV run on tensor cores (mma.sync m16n8k16, fp16 in, fp32
-//    accumulate).  A 3-bit field placed in the mantissa of a half with a
-//    zero exponent is an exact subnormal; with its sign bit flipped it reads
-//    (c + 4) 2^(k-24).  Keys take one LOP3 per pair of codes and the +4
-//    offset enters as a per-block constant seeded into the logit
-//    accumulator; values take a byte permute per three fields, a mask and
-//    one half2 subtraction.  The powers of two are folded into q1 (keys) or
-//    into the output (values).  q1 is split into hi + lo fp16 halves (two
-//    columns per head) so the logits keep ~fp32 accuracy; with fp32 value
-//    scales the probabilities are split the same way.  Per-(token, block)
-//    scales multiply the per-block partial dot products (keys) or the
-//    probabilities (values).
+//    accumulate).  A b-bit field (b = 2, 3, 4) placed in the mantissa of a
+//    half with a zero exponent is an exact subnormal; with its sign bit
+//    flipped it reads (c + 2^(b-1)) 2^(k-24).  Keys take one LOP3 per pair of
+//    codes and the offset enters as a per-block constant seeded into the
+//    logit accumulator; values take a byte permute per 2-4 fields, a mask
+//    and one half2 subtraction.  The powers of two are folded into q1 (keys)
+//    or into the output (values).  The asymmetric variant's unsigned codes
+//    need neither the flip nor the offset; its zero points add z_k * sum q1
+//    per block to the logits and sum p z_v per block to the outputs.  q1 is
+//    split into hi + lo fp16 halves (two columns per head) so the logits
+//    keep ~fp32 accuracy; the probabilities are split the same way with fp32
+//    value scales, at up to 4 heads per kv head and in the asymmetric
+//    variant.  Per-(token, block) scales multiply the per-block partial dot
+//    products (keys) or the probabilities (values).
 #pragma once
 
 #include <float.h>
@@ -886,8 +889,10 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
       }
       // reduce over the lane's quad (fields) and the hi/lo parts: lanes 8h..8h+7
       // then hold head 4tq + h; the logit lanes of head 4tq + j read lane 8j.
-      // The key halves are (c + 4) 2^(k-24): seed the accumulators with
-      // -4 * 2^-24 * sum_d 2^k_d q1_d so they sum c 2^(k-24) q1.
+      // The key halves are (c + 2^(b-1)) 2^(k-24): seed the accumulators with
+      // -2^(b-1) * 2^-24 * sum_d 2^k_d q1_d so they sum c 2^(k-24) q1.  The
+      // asymmetric variant seeds nothing and keeps 2^-24 * sum_d q1_d (the
+      // same sum) for its zero-point term.
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
         float t = csum[b];
@@ -1143,7 +1148,9 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
           SDec::template two<8 * BPT>(a, sv2, sv3);
         }
       }
-      const bool lo_part = (r & 1) != 0;
+      // hi column (r even): fp16(y); lo column (r odd): fp16(y - fp16(y)),
+      // the difference exact in fp32 -- one rounding of y - m * fp16(y)
+      const float m_lo = (r & 1) ? 1.0f : 0.0f;
 #pragma unroll
       for (int tp = 0; tp < NTP; ++tp) {
 #pragma unroll
@@ -1152,12 +1159,10 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
           const float y1 = v1 ? x1[tp] * sv1[b] : 0.0f;
           const float y2 = v2 ? x2[tp] * sv2[b] : 0.0f;
           const float y3 = v3 ? x3[tp] * sv3[b] : 0.0f;
-          const __half2 h01 = __floats2half2_rn(y0, y1), h23 = __floats2half2_rn(y2, y3);
-          const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-          const uint32_t lo01 = pack_half2(y0 - f01.x, y1 - f01.y);
-          const uint32_t lo23 = pack_half2(y2 - f23.x, y3 - f23.y);
-          pb[b][tp][0] = lo_part ? lo01 : *reinterpret_cast<const uint32_t*>(&h01);
-          pb[b][tp][1] = lo_part ? lo23 : *reinterpret_cast<const uint32_t*>(&h23);
+          const float2 f01 = __half22float2(__floats2half2_rn(y0, y1));
+          const float2 f23 = __half22float2(__floats2half2_rn(y2, y3));
+          pb[b][tp][0] = pack_half2(fmaf(-m_lo, f01.x, y0), fmaf(-m_lo, f01.y, y1));
+          pb[b][tp][1] = pack_half2(fmaf(-m_lo, f23.x, y2), fmaf(-m_lo, f23.y, y3));
         }
       }
     } else {
