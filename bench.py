@@ -512,11 +512,11 @@ def run_prefill_attn(args, world, rank, dev):
             "metric": "prefill-attention query tokens/s (one layer, all heads)",
             "value": whole_job_rate(w.chunk, world, ms), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f16 mma / f32 accumulate (3-bit packed cache)",
+            "scaling": "weak", "vs_baseline": None, "dtype": f"f16 mma / f32 accumulate ({w.bits}-bit packed cache)",
             "data": "synthetic",
             "config": {"workload": f"{w.name}: chunk of {w.chunk} queries at positions {w.seq_len - w.chunk}.."
                                    f"{w.seq_len - 1} of a {w.seq_len}-token cache, Hkv{w.num_kv_heads} "
-                                   f"Hq{w.num_q_heads} d{w.d} m{w.block} {w.scale} scales, contiguous "
+                                   f"Hq{w.num_q_heads} d{w.d} m{w.block} {w.scale} scales, {w.bits}-bit codes, contiguous "
                                    f"P{w.page_size}, causal", "l2": "cache 3.4 MB per kv head"},
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                          "frac": tflops / peak, "traffic": None,
@@ -659,7 +659,7 @@ def main():
             "metric": "decode tokens/s (one layer, all heads)", "value": whole_job_rate(w.batch, world, ms_step),
             "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f16 mma / f32 accumulate (3-bit packed cache)", "data": "synthetic",
+            "dtype": f"f16 mma / f32 accumulate ({w.bits}-bit packed cache)", "data": "synthetic",
             "config": {"workload": workload_desc(w), "l2": "inputs larger than L2 (packed cache "
                        f"{ab['decode'] / 1e6:.0f} MB per step)", "parallelism": f"replicas x{world} (dp over sequences)"},
             "decode": {"ms": dec_ms, "hbm_gbs": dec_gbs, "frac_of_peak": dec_gbs / peaks["hbm"],
