@@ -156,8 +156,9 @@ def test_decode_single_token_returns_value(oracle, bits):
             assert np.abs(out[b, h] - U.T @ vh).max() < 1e-12
 
 
-def test_decode_zero_query_is_mean(oracle):
-    U, L, pool, table = _setup(oracle, paged=True)
+@pytest.mark.parametrize("scale,bits", [("f16", 3), ("f16", 2), ("f32", 4), ("e4m3zp", 3)])
+def test_decode_zero_query_is_mean(oracle, scale, bits):
+    U, L, pool, table = _setup(oracle, paged=True, scale=scale, bits=bits)
     rng = np.random.default_rng(2)
     _fill(oracle, L, pool, U, table, [37, 64], rng)
     q = np.zeros((2, 2, 128), np.float16)
@@ -185,8 +186,9 @@ def test_decode_gqa_mapping_and_empty(oracle):
     assert np.all(out[1] == 0)
 
 
-def test_decode_equal_keys_uniform(oracle):
-    U, L, pool, _ = _setup(oracle)
+@pytest.mark.parametrize("scale,bits", [("f16", 3), ("f16", 2), ("f32", 4), ("e4m3zp", 3)])
+def test_decode_equal_keys_uniform(oracle, scale, bits):
+    U, L, pool, _ = _setup(oracle, scale=scale, bits=bits)
     rng = np.random.default_rng(4)
     n = 33
     k = np.tile(rng.standard_normal((1, 2, 128)), (n, 1, 1)).astype(np.float16)
@@ -272,9 +274,10 @@ def test_prefill_first_position_attends_to_itself(oracle):
         assert np.abs(out[0, h] - U.T @ vh).max() < 1e-12
 
 
-def test_prefill_zero_queries_average_their_prefix(oracle):
+@pytest.mark.parametrize("scale,bits", [("f16", 3), ("f16", 2), ("f32", 4), ("e4m3zp", 3)])
+def test_prefill_zero_queries_average_their_prefix(oracle, scale, bits):
     # q = 0: uniform weights over positions [0, pos0 + i] (the causal prefix)
-    U, L, pool, _ = _setup(oracle)
+    U, L, pool, _ = _setup(oracle, scale=scale, bits=bits)
     rng = np.random.default_rng(22)
     _fill(oracle, L, pool, U, None, [40, 64], rng)
     pos0, n = 17, 23
@@ -286,10 +289,11 @@ def test_prefill_zero_queries_average_their_prefix(oracle):
             assert np.abs(out[i, h] - U.T @ vh.mean(0)).max() < 1e-12
 
 
-def test_prefill_is_causal(oracle):
+@pytest.mark.parametrize("scale,bits", [("f16", 3), ("f16", 2), ("f32", 4), ("e4m3zp", 3)])
+def test_prefill_is_causal(oracle, scale, bits):
     # rewriting the key and value at position p changes the outputs of the
     # queries at positions >= p and of none before it
-    U, L, pool, _ = _setup(oracle, B=1, maxp=4)
+    U, L, pool, _ = _setup(oracle, B=1, maxp=4, scale=scale, bits=bits)
     rng = np.random.default_rng(23)
     _fill(oracle, L, pool, U, None, [60], rng)
     pos0, n, p = 10, 40, 31
