@@ -106,6 +106,8 @@ class Case:
         """Compares the library's stored scales and codes with the oracle's
         for every written token.  Returns counts of excluded boundary
         elements and scale-midpoint blocks."""
+        if self.scale == "e4m3zp":
+            return self._compare_written_asym(k, v, si, ps)
         gp = self.pool.cpu().numpy()
         nb = self.d // self.block
         excl_codes = excl_blocks = checked = 0
@@ -141,6 +143,53 @@ class Case:
         return dict(checked=checked, boundary_codes=excl_codes, midpoint_blocks=excl_blocks)
 
 
+def _asym_sets(case, x):
+    """Asymmetric variant: oracle codes, (scale, zero point), fp64 scale,
+    (x - z_q)/s_q and the blocks whose scale or zero point sits within
+    MIDPOINT of an E4M3 rounding midpoint."""
+    nb, blk = case.d // case.block, case.block
+    u, sz, s = O.quantize_asym(x, blk, 1e-6, case.bits)
+    lo = x.reshape(-1, nb, blk).min(-1)
+    mid_s = O.scale_midpoint_distance(s, "e4m3") < MIDPOINT
+    mid_z = O.scale_midpoint_distance(np.abs(lo), "e4m3") < MIDPOINT
+    sq, zq = sz[..., 0], sz[..., 1]
+    r = (x.reshape(-1, nb, blk) - zq[..., None]) / np.where(sq > 0, sq, 1)[..., None]
+    return u, sz, r, mid_s, mid_z
+
+
+def _compare_written_asym(self, k, v, si, ps):
+    gp = self.pool.cpu().numpy()
+    lay, nb = self.layout, self.d // self.block
+    top = (1 << self.bits) - 1
+    checked = excluded = mids = 0
+    for which, src in ((0, k), (1, v)):
+        x = src.astype(np.float64).reshape(-1, self.d) @ self.U.T
+        u_o, sz_o, r, mid_s, mid_z = _asym_sets(self, x)
+        page, slot, st = O.locate(lay, self.table, np.repeat(si, self.hkv), np.repeat(ps, self.hkv))
+        ok = st == 0
+        heads = np.tile(np.arange(self.hkv), len(si))
+        rec = page * lay.page_bytes + (heads * 2 + which) * lay.record_bytes
+        so = rec + slot * nb * lay.sb
+        co = rec + self.page * nb * lay.sb + slot * lay.code_bytes
+        sz_g = O.decode_scales(gp[so[ok][:, None] + np.arange(nb * lay.sb)[None]], "e4m3zp")
+        u_g = O.unpack_codes(gp[co[ok][:, None] + np.arange(lay.code_bytes)[None]], self.d, self.bits, signed=False)
+        mid = (mid_s | mid_z)[ok]
+        assert np.array_equal(sz_g[~mid], sz_o[ok][~mid]), "scale / zero point mismatch"
+        near = np.zeros(r[ok].shape, bool)
+        for kk in range(top):
+            near |= np.abs(r[ok] - (kk + 0.5)) < BOUNDARY
+        near = (near | mid[..., None]).reshape(-1, self.d)
+        bad = (u_g != u_o[ok]) & ~near
+        assert not bad.any(), f"{int(bad.sum())} codes differ outside rounding boundaries"
+        checked += u_g.size
+        excluded += int(near.sum())
+        mids += int(mid.sum())
+    return dict(checked=checked, boundary_codes=excluded, midpoint_blocks=mids)
+
+
+Case._compare_written_asym = _compare_written_asym
+
+
 def flip_bound(case, k, v, si, ps, q, sm_scale=0.0, differs=None):
     """Upper bound, per (sequence, query head), on how far the decode output
     may move when the cache holds any of the codes and scales that the write
@@ -160,7 +209,7 @@ def flip_bound(case, k, v, si, ps, q, sm_scale=0.0, differs=None):
     G = case.hq // case.hkv
     sm = sm_scale if sm_scale > 0 else 1.0 / math.sqrt(d)
     # relative spacing of neighbouring stored scales (upper bound)
-    ulp_rel = {"f32": 2.0 ** -23, "f16": 2.0 ** -10, "e4m3": 2.0 ** -3}[case.scale]
+    ulp_rel = {"f32": 2.0 ** -23, "f16": 2.0 ** -10, "e4m3": 2.0 ** -3, "e4m3zp": 2.0 ** -3}[case.scale]
     out = np.zeros((case.B, case.hq))
     for b in range(case.B):
         sel = np.nonzero(si == b)[0]
@@ -171,6 +220,33 @@ def flip_bound(case, k, v, si, ps, q, sm_scale=0.0, differs=None):
             deq, slack = [], []
             for which, src in enumerate((k, v)):
                 x = src[sel, g].astype(np.float64) @ case.U.T
+                if case.scale == "e4m3zp":
+                    # asymmetric variant: a code within reach of a boundary of
+                    # (x - z_q)/s_q may be one step s_q off; a neighbouring
+                    # scale moves every value s_q u by u * ulp * s_q and shifts
+                    # (x - z_q)/s_q by up to (2^b - 1/2) * ulp, a neighbouring
+                    # zero point moves every value by ulp * |z_q| and shifts
+                    # (x - z_q)/s_q by that over s_q
+                    top = (1 << case.bits) - 1
+                    u, sz, r, mid_s, mid_z = _asym_sets(case, x)
+                    sq, zq = sz[..., 0], sz[..., 1]
+                    reach = BOUNDARY + np.where(mid_s, (top + 0.5) * ulp_rel, 0.0) + \
+                        np.where(mid_z, ulp_rel * np.abs(zq) / np.where(sq > 0, sq, 1), 0.0)
+                    near = np.zeros(r.shape, bool)
+                    for kk in range(top):
+                        near |= np.abs(r - (kk + 0.5)) < reach[..., None]
+                    mid = mid_s | mid_z
+                    if differs is not None:
+                        code_d, blk_d = differs[(b, g, which)]
+                        near &= code_d.reshape(r.shape)
+                        mid &= blk_d
+                        mid_s, mid_z = mid_s & blk_d, mid_z & blk_d
+                    step = np.where(near, 1.0 + ulp_rel, 0.0) * sq[..., None]
+                    step += np.where(mid_s[..., None], u.reshape(r.shape) * ulp_rel, 0.0) * sq[..., None]
+                    step += np.where(mid_z[..., None], ulp_rel * np.abs(zq)[..., None], 0.0)
+                    deq.append((u.reshape(r.shape) * sq[..., None] + zq[..., None]).reshape(-1, d))
+                    slack.append(step.reshape(-1, d))
+                    continue
                 qm = O.qmax(case.bits)
                 c, sq, s = O.quantize(x, blk, 1e-6, case.scale, case.bits)
                 r = np.abs(x.reshape(-1, nb, blk) / np.where(sq > 0, sq, 1.0)[..., None])
@@ -225,6 +301,16 @@ def written_differences(case, k, v, si, ps):
         for g in range(case.hkv):
             for which, src in ((0, k), (1, v)):
                 x = src[sel, g].astype(np.float64) @ case.U.T
+                if case.scale == "e4m3zp":
+                    u_o, sz_o, _ = O.quantize_asym(x, case.block, 1e-6, case.bits)
+                    rec = page * case.layout.page_bytes + (g * 2 + which) * case.layout.record_bytes
+                    so = rec + slot * nb * case.layout.sb
+                    co = rec + case.page * nb * case.layout.sb + slot * case.layout.code_bytes
+                    sz_g = O.decode_scales(gp[so[:, None] + np.arange(nb * case.layout.sb)[None]], "e4m3zp")
+                    u_g = O.unpack_codes(gp[co[:, None] + np.arange(case.layout.code_bytes)[None]], case.d,
+                                         case.bits, signed=False)
+                    out[(b, g, which)] = (u_g != u_o, (sz_g != sz_o).any(-1))
+                    continue
                 c_o, sq_o, _ = O.quantize(x, case.block, 1e-6, case.scale, case.bits)
                 rec = page * case.layout.page_bytes + (g * 2 + which) * case.layout.record_bytes
                 so = rec + slot * nb * case.layout.sb

@@ -129,3 +129,53 @@ def test_flip_bound_restricted_to_the_elements_that_differ():
     assert moved > 0
     assert np.all(delta <= some * (1 + 1e-9) + 1e-12)
     assert np.all(some <= band * (1 + 1e-12))
+
+
+def _flip_near_boundary_asym(c, pool, k, v, si, ps, widen, every=1, differs=None):
+    """As _flip_near_boundary for the asymmetric variant: unsigned codes,
+    boundaries of (x - z_q)/s_q."""
+    nb, blk = c.d // c.block, c.block
+    top = (1 << c.bits) - 1
+    moved = 0
+    for which, src in ((0, k), (1, v)):
+        for g in range(c.hkv):
+            x = src[:, g].astype(np.float64) @ c.U.T
+            u, sz, _ = O.quantize_asym(x, blk, 1e-6, c.bits)
+            sq, zq = sz[..., 0], sz[..., 1]
+            r = (x.reshape(-1, nb, blk) - zq[..., None]) / np.where(sq > 0, sq, 1.0)[..., None]
+            frac = r - np.floor(r)
+            near = (np.abs(frac - 0.5) < widen) & (r > 0) & (r < top)
+            idx = np.flatnonzero(near)
+            near = np.zeros(near.shape, bool)
+            near.flat[idx[::every]] = True
+            if differs is not None:
+                differs[(0, g, which)] = (near.reshape(-1, c.d), np.zeros(sq.shape, bool))
+            if not near.any():
+                continue
+            other = np.where(np.rint(r) == np.floor(r), np.floor(r) + 1, np.floor(r))
+            alt = np.where(near, np.clip(other, 0, top), u.reshape(-1, nb, blk)).reshape(-1, c.d)
+            moved += int(near.sum())
+            page, slot, st = O.locate(c.layout, None, si, ps)
+            for t in np.nonzero(near.reshape(-1, c.d).any(axis=1))[0]:
+                off = c.layout.code_offset(page[t], g, which, slot[t])
+                pool[off:off + c.layout.code_bytes] = O.pack_codes(alt[t][None].astype(np.int64), c.bits)[0]
+    return moved
+
+
+def test_flip_bound_covers_alternative_codes_asym():
+    c = _case(scale="e4m3zp")
+    k, v, si, ps = _tokens(c)
+    pool = np.zeros(c.layout.pool_bytes, np.uint8)
+    O.write(pool, c.layout, c.U, k, v, si, ps, None)
+    q = I.q_np(c.spec, c.B, c.hq, 0)
+    ref = O.decode(pool, c.layout, c.U, q, c.lens, None, 0.0)
+    flipped, differs = pool.copy(), {}
+    moved = _flip_near_boundary_asym(c, flipped, k, v, si, ps, BOUNDARY, differs=differs)
+    got = O.decode(flipped, c.layout, c.U, q, c.lens, None, 0.0)
+    delta = np.abs(got - ref).max(axis=-1)
+    some = flip_bound(c, k, v, si, ps, q, differs=differs)
+    band = flip_bound(c, k, v, si, ps, q)
+    assert moved > 0, "the case must contain boundary elements"
+    assert np.all(delta <= some * (1 + 1e-9) + 1e-12)
+    assert np.all(some <= band * (1 + 1e-12))
+    assert float(some.max()) < 1e4 * max(float(delta.max()), 1e-12)

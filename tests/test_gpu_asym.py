@@ -14,7 +14,7 @@ import numpy as np
 import pytest
 
 import kvq3_inputs as I
-from cases import BOUNDARY, MIDPOINT, TOL_DECODE, Case, rel_err
+from cases import BOUNDARY, MIDPOINT, TOL_DECODE, Case, flip_bound, rel_err, written_differences
 from oracle import kvq3_oracle as O
 
 pytestmark = pytest.mark.gpu
@@ -188,3 +188,23 @@ def test_asym_rejects_other_widths():
         with pytest.raises(K.Kvq3Error) as e:
             K.kvq3_cache_sizes(d)
         assert e.value.status == 2
+
+
+@pytest.mark.parametrize("cfg", DECODE_CASES[1:4], ids=_did)
+def test_decode_end_to_end_asym(cfg):
+    # GPU write + GPU decode against oracle write + oracle decode; elements the
+    # write bar lets differ widen each head's bar by the oracle-side bound of
+    # what they can move (cases.flip_bound)
+    import math
+    c = Case(scale="e4m3zp", **cfg)
+    k, v, si, ps = c.tokens()
+    c.gpu_write(k, v, si, ps)
+    c.oracle_write(k, v, si, ps)
+    q = c.queries(1)
+    got, ref = c.gpu_decode(q), c.oracle_decode(q)
+    assert c.device_status() == 0
+    rms = math.sqrt(float(np.mean(ref ** 2)))
+    slack = flip_bound(c, k, v, si, ps, q, differs=written_differences(c, k, v, si, ps))
+    err = np.abs(got - ref).max(axis=-1)
+    print(f"max|err|/rms = {rel_err(got, ref):.3e}; heads with slack: {int((slack > 0).sum())}")
+    assert np.all(err <= TOL_DECODE * rms + slack)
