@@ -117,3 +117,35 @@ def test_invalid_descriptions_rejected_on_host(K):
     st = K.lib.kvq3_decode_attn(K.kvq3_rotation_create(128, 1), ctypes.byref(d), ctypes.byref(c),
                                 ctypes.c_void_p(256), 3, 0.0, ctypes.c_void_p(256), None, 0, None, None)
     assert st == 1
+
+
+def test_calibration_arguments_checked_on_host(K):
+    # workspace: candidate quaternions (rounded up to 256 bytes) + fp64 errors
+    d = K.CacheDesc(128, 1, 64, 3, K.SCALE_TYPES["f16"], 1e-6, 16, 1, 1, 0, 1)
+    assert K.kvq3_calibrate_workspace_size(d, 64) == (64 * 128 * 4 + 255) // 256 * 256 + 64 * 2 * 8
+    assert K.kvq3_calibrate_workspace_size(d, 3) == (3 * 128 * 4 + 255) // 256 * 256 + 3 * 2 * 8
+    for p in (1, 0, 70000):
+        with pytest.raises(K.Kvq3Error) as e:
+            K.kvq3_calibrate_workspace_size(d, p)
+        assert e.value.status == 1
+    rot = K.kvq3_rotation_create(128, 1)
+    sse = ctypes.c_void_p(256)
+    # candidates out of range, a null or misaligned candidate array, a misaligned sample
+    for p, quats, x in ((0, 256, 256), (1, 0, 256), (1, 264, 256), (1, 256, 258)):
+        st = K.lib.kvq3_calib_sse(rot, ctypes.byref(d), ctypes.c_void_p(quats), p, ctypes.c_void_p(x), 16, sse, None)
+        assert st == 1, (p, quats, x)
+    # a rotation of another dimension
+    st = K.lib.kvq3_calib_sse(K.kvq3_rotation_create(64, 1), ctypes.byref(d), ctypes.c_void_p(256), 1,
+                              ctypes.c_void_p(256), 16, sse, None)
+    assert st == 1
+    # the search: a short, missing or misaligned workspace; bad step or rounds
+    q = (ctypes.c_float * 128)()
+    need = K.kvq3_calibrate_workspace_size(d, 4)
+    for ws, nbytes in ((256, need - 8), (0, need), (264, need)):
+        st = K.lib.kvq3_calibrate_so4(rot, ctypes.byref(d), ctypes.c_void_p(256), 16, 1, 4, 0.5, 1,
+                                      ctypes.c_void_p(ws), nbytes, q, None, None)
+        assert st == 4, (ws, nbytes)
+    for rounds, step in ((-1, 0.5), (1, -0.5), (1, float("nan"))):
+        st = K.lib.kvq3_calibrate_so4(rot, ctypes.byref(d), ctypes.c_void_p(256), 16, rounds, 4, step, 1,
+                                      ctypes.c_void_p(256), need, q, None, None)
+        assert st == 1, (rounds, step)
