@@ -354,13 +354,81 @@ def barrier(world: int):
         dist.barrier()
 
 
+def oracle_write_sample(w: I.Workload, n_tok: int):
+    """Oracle leg of the write-path workload: a closure writing the first
+    n_tok positions (all kv heads, K and V) into a fresh oracle pool."""
+    from oracle import kvq3_oracle as O
+    P = w.page_size
+    maxp = int(math.ceil(n_tok / P))
+    lay = O.Layout(w.d, w.num_kv_heads, w.block, w.scale, P, 1, maxp, maxp, w.bits)
+    signs, quats = O.rotation_params(w.d, w.rot_seed, bool(w.rot_flags & 1), bool(w.rot_flags & 2))
+    U = O.rotation_matrix(signs, quats)
+    k = np.stack([I.kv_rows_np(w.data, 0, 0, h, 0, n_tok) for h in range(w.num_kv_heads)], 1)
+    v = np.stack([I.kv_rows_np(w.data, 1, 0, h, 0, n_tok) for h in range(w.num_kv_heads)], 1)
+    pool = np.zeros(lay.pool_bytes, np.uint8)
+
+    def run():
+        O.write(pool, lay, U, k, v, np.zeros(n_tok, np.int32), np.arange(n_tok), None, w.eps)
+    return run
+
+
+def oracle_prefill_sample(w: I.Workload, n_q: int):
+    """Oracle leg of the prefill-attention workload: the cache of the whole
+    context written once (untimed); a closure answering the last n_q queries
+    of the chunk (all query heads)."""
+    from oracle import kvq3_oracle as O
+    n, P = w.seq_len, w.page_size
+    maxp = int(math.ceil(n / P))
+    lay = O.Layout(w.d, w.num_kv_heads, w.block, w.scale, P, 1, maxp, maxp, w.bits)
+    signs, quats = O.rotation_params(w.d, w.rot_seed, bool(w.rot_flags & 1), bool(w.rot_flags & 2))
+    U = O.rotation_matrix(signs, quats)
+    pool = np.zeros(lay.pool_bytes, np.uint8)
+    step = 4096
+    for t0 in range(0, n, step):
+        m = min(step, n - t0)
+        k = np.stack([I.kv_rows_np(w.data, 0, 0, h, t0, m) for h in range(w.num_kv_heads)], 1)
+        v = np.stack([I.kv_rows_np(w.data, 1, 0, h, t0, m) for h in range(w.num_kv_heads)], 1)
+        O.write(pool, lay, U, k, v, np.zeros(m, np.int32), np.arange(t0, t0 + m), None, w.eps)
+    q = I.q_np(w.data, n_q, w.num_q_heads, 3)
+
+    def run():
+        return O.prefill(pool, lay, U, q, 0, n - n_q)
+    return run
+
+
 def run_reference(args, world, rank):
+    """The reference arm: the CPU oracle, timed as it stands on a bounded
+    sample of the workload (rank 0 only; about 120 s of timed work at most),
+    scaled to the workload's metric."""
     w = workload(args.workload)
     lens = workload_lens(w)
     if rank != 0:
         return
-    units = w.batch * w.num_kv_heads
-    run = oracle_sample(w, lens, 0)
+    if w.chunk > 0:            # prefill attention: query tokens/s
+        n_q = 2
+        run = oracle_prefill_sample(w, n_q)
+        metric, unit = "prefill-attention query tokens/s (one layer, all heads)", "tokens/s"
+        what = (f"each step: oracle prefill attention of the last {n_q} queries of the chunk (all "
+                f"{w.num_q_heads} heads) over the {w.seq_len}-token cache")
+        to_value = lambda per: n_q / per                                   # noqa: E731
+        to_step_s = lambda per: per * w.chunk / n_q                        # noqa: E731
+    elif not w.decode:         # write path: GB/s of fp16 in + packed out
+        n_tok = 256
+        run = oracle_write_sample(w, n_tok)
+        sb = {"f32": 4, "f16": 2, "e4m3": 1, "e4m3zp": 2}[w.scale]
+        nbytes = n_tok * w.num_kv_heads * 2 * (2 * w.d + w.bits * w.d // 8 + (w.d // w.block) * sb)
+        metric, unit = "write-path GB/s (fp16 in + packed out)", "GB/s"
+        what = f"each step: oracle write of {n_tok} tokens x {w.num_kv_heads} kv heads, K and V"
+        to_value = lambda per: nbytes / per / 1e9                          # noqa: E731
+        to_step_s = lambda per: per * w.seq_len / n_tok                    # noqa: E731
+    else:                      # decode: tokens/s of the whole batch
+        units = w.batch * w.num_kv_heads
+        run = oracle_sample(w, lens, 0)
+        metric, unit = "decode tokens/s (one layer, all heads)", "tokens/s"
+        what = (f"each step: oracle write 1 token + decode {w.group} query heads of one (sequence, "
+                f"kv head) unit over {int(lens[0])} tokens; scaled by {units} units")
+        to_step_s = lambda per: per * units * float(np.mean(lens)) / int(lens[0])   # noqa: E731
+        to_value = lambda per: w.batch / to_step_s(per)                    # noqa: E731
     for _ in range(min(args.warmup, 3)):
         run()
     # bounded: the timed samples stop after ~120 s of CPU work (at least one)
@@ -369,20 +437,17 @@ def run_reference(args, world, rank):
     while done < args.steps and (done == 0 or time.perf_counter() - t0 < 120.0):
         run()
         done += 1
-    per_unit = (time.perf_counter() - t0) / done
-    step_s = per_unit * units * float(np.mean(lens)) / int(lens[0])
-    value = w.batch / step_s
+    per = (time.perf_counter() - t0) / done
+    value = to_value(per)
     line = {
-        "impl": "reference", "metric": "decode tokens/s (one layer, all heads)", "value": value,
-        "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "impl": "reference", "metric": metric, "value": value,
+        "unit": unit, "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": to_step_s(per) * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
         "config": {"workload": workload_desc(w)},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-                         "sample": f"each step: oracle write 1 token + decode {w.group} query heads of "
-                                   f"one (sequence, kv head) unit over {int(lens[0])} tokens; "
-                                   f"scaled by {units} units; {done} steps timed (120 s cap)"},
-        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": f"{what}; {done} steps timed (120 s cap)"},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
 
