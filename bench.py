@@ -354,6 +354,21 @@ def barrier(world: int):
         dist.barrier()
 
 
+def timed_cpu_baseline(run, to_value, unit: str, what: str, budget_s: float = 15.0) -> dict:
+    """The oracle as it stands, timed on a bounded sample (about budget_s of
+    CPU work after one untimed run)."""
+    t0 = time.perf_counter()
+    run()
+    per = time.perf_counter() - t0
+    n = max(1, min(16, int(budget_s / max(per, 1e-3))))
+    t0 = time.perf_counter()
+    for _ in range(n):
+        run()
+    per = (time.perf_counter() - t0) / n
+    return {"value": to_value(per), "unit": unit, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{what}; x{n} runs"}
+
+
 def oracle_write_sample(w: I.Workload, n_tok: int):
     """Oracle leg of the write-path workload: a closure writing the first
     n_tok positions (all kv heads, K and V) into a fresh oracle pool."""
@@ -480,19 +495,27 @@ def run_prefill(args, world, rank, dev):
     gbs = whole_job_rate(st.bytes(), world, ms) / 1e9
     if rank == 0:
         w = st.w
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            n_tok = 256
+            sb = {"f32": 4, "f16": 2, "e4m3": 1, "e4m3zp": 2}[w.scale]
+            nbytes = n_tok * w.num_kv_heads * 2 * (2 * w.d + w.bits * w.d // 8 + (w.d // w.block) * sb)
+            cpu = timed_cpu_baseline(oracle_write_sample(w, n_tok), lambda per: nbytes / per / 1e9, "GB/s",
+                                     f"oracle write of {n_tok} tokens x {w.num_kv_heads} kv heads, K and V")
         print(json.dumps({
             "metric": "write-path GB/s (fp16 in + packed out)", "value": gbs, "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
             "config": {"workload": f"prefill: {w.seq_len} tokens x Hkv{w.num_kv_heads} x d{w.d}, K+V fp16, "
-                                   f"sign flip + FWHT, m{w.block} f32 scales",
+                                   f"sign flip + FWHT, m{w.block} {w.scale} scales, {w.bits}-bit codes",
                        "l2": "inputs larger than L2"},
             "roofline": {"bound": "hbm", "achieved": gbs / world, "peak": peaks["hbm"], "unit": "GB/s",
                          "frac": gbs / world / peaks["hbm"], "traffic": None,
                          "kernel": "write_chunk_kernel", "peak_source": peaks["src"]},
             "tokens_per_s": whole_job_rate(w.seq_len, world, ms),
-            "gpu_launches": args.steps, "clocks": clk.summary()}))
+            "gpu_launches": args.steps, "clocks": clk.summary(),
+            **({"cpu_baseline": cpu} if cpu else {})}))
 
 
 class PrefillAttnWorkload:
@@ -572,7 +595,15 @@ def run_prefill_attn(args, world, rank, dev):
         os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
     peak = float(pk.get("bf16_tflops", 1900.0))
     tflops = st.flops() / (ms * 1e-3) / 1e12
+    # d = 128 with 3-bit symmetric codes runs the tile kernel (one launch);
+    # the other formats the decode kernel's prefill variant and the combine
+    tile = w.d == 128 and w.bits == 3 and w.scale != "e4m3zp"
     if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            cpu = timed_cpu_baseline(oracle_prefill_sample(w, 1), lambda per: 1.0 / per, "tokens/s",
+                                     f"oracle prefill attention of the chunk's last query (all {w.num_q_heads} "
+                                     f"heads) over the {w.seq_len}-token cache (cache written once, untimed)")
         print(json.dumps({
             "metric": "prefill-attention query tokens/s (one layer, all heads)",
             "value": whole_job_rate(w.chunk, world, ms), "unit": "tokens/s", "n_gpus": world,
@@ -585,10 +616,12 @@ def run_prefill_attn(args, world, rank, dev):
                                    f"P{w.page_size}, causal", "l2": "cache 3.4 MB per kv head"},
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                          "frac": tflops / peak, "traffic": None,
-                         "kernel": "kvq3_prefill_attn (decode_split_kernel<..., prefill> + combine)",
+                         "kernel": "kvq3_prefill_attn (" + ("prefill_tile_kernel" if tile else
+                                   "decode_split_kernel<..., prefill> + decode_combine_kernel") + ")",
                          "peak_source": "measured bf16 (fp16 mma has the same nominal rate)"
                          if pk else "fallback"},
-            "gpu_launches": 2 * args.steps, "clocks": clk.summary()}))
+            "gpu_launches": (1 if tile else 2) * args.steps, "clocks": clk.summary(),
+            **({"cpu_baseline": cpu} if cpu else {})}))
 
 
 def workload_desc(w: I.Workload) -> str:
