@@ -490,3 +490,23 @@ def test_asym_storage_and_error_against_symmetric(oracle):
     ya = (u.reshape(-1, 2, 64) * sz[..., 0:1] + sz[..., 1:2]).reshape(y.shape)
     mse_s, mse_a = np.mean((ys - y) ** 2), np.mean((ya - y) ** 2)
     assert mse_a < 0.8 * mse_s
+
+
+def test_asym_edge_cases(oracle):
+    # a constant block: s = eps/7 underflows E4M3 to 0, so every code is 0 and
+    # x_hat = z_q = E4M3(c) (2.3 -> 2.25: the E4M3 grid near 2 is 0.25)
+    x = np.full((1, 32), 2.3)
+    u, sz, s = oracle.quantize_asym(x, 32, 1e-6)
+    assert sz[0, 0, 0] == 0.0 and sz[0, 0, 1] == 2.25 and np.all(u == 0)
+    # an all-positive block: z = min = 1, s = (8 - 1)/7 = 1 (eps = 0), codes x - 1
+    x = np.array([[1.0, 8.0, 4.0, 2.0] + [5.0] * 28])
+    u, sz, _ = oracle.quantize_asym(x, 32, 0.0)
+    assert tuple(sz[0, 0]) == (1.0, 1.0) and list(u[0, :4]) == [0, 7, 3, 1] and np.all(u[0, 4:] == 4)
+    # a zero point beyond E4M3's range saturates to -448: the block minimum
+    # then lies below z_q and its code clips to 0
+    x = np.zeros((1, 32))
+    x[0, 0] = -1000.0
+    u, sz, s = oracle.quantize_asym(x, 32, 0.0)
+    assert sz[0, 0, 1] == -448.0 and u[0, 0] == 0
+    assert sz[0, 0, 0] == oracle.round_e4m3(1000.0 / 7)                 # 142.857.. -> 144
+    assert np.all(u[0, 1:] == np.clip(np.rint(448.0 / sz[0, 0, 0]), 0, 7))
