@@ -86,7 +86,8 @@
  *       header count does not add up and is not followed.
  *   R11 The query is rotated by the same U as the keys ([OMC] q1 = U(q)).
  *   R12 Logits are scaled by sm_scale, 1/sqrt(d) by default ([OMC] Key
- *       formulas).
+ *       formulas; the page's Implementation notes sketch writes the logits
+ *       without the scale, and the formula is taken over the sketch).
  *   R13 Decode attends to positions [0, seq_lens[b]); the caller appends the
  *       current token with kvq3_write and advances seq_lens itself.
  *   R14 Query head h reads kv head h / (Hq/Hkv) (consecutive grouping).
@@ -247,9 +248,13 @@ kvq3_status kvq3_write(kvq3_rotation rot, const kvq3_cache_desc *desc,
 
 /* Write path for a prefill chunk: positions pos0 .. pos0+n_tok-1 of sequence
  * seq, with k, v: device fp16 [n_tok][Hkv][d] (row i is position pos0 + i).
- * Same arithmetic and stored bytes as kvq3_write ([OMC] Implementation notes,
- * write path), without per-token index arrays: one thread per vector, rows
- * staged through shared memory, packed f32x2 butterfly.  d must be 64 or 128
+ * The same formula as kvq3_write ([OMC] Implementation notes, write path),
+ * without per-token index arrays: one thread per vector, rows staged through
+ * shared memory, packed f32x2 butterfly.  Both are fp32 computations with
+ * different summation orders, so the stored bytes agree except where an
+ * element's |x/s_q| lies within about 1e-6 relative of a rounding boundary
+ * (or a block's scale at a rounding midpoint of its storage type), where
+ * either neighbour may be stored.  d must be 64 or 128
  * (KVQ3_ERR_UNSUPPORTED otherwise; kvq3_write covers d = 256).  The position
  * range must lie inside the sequence's capacity (KVQ3_ERR_INVALID_ARG);
  * invalid page ids are skipped and flagged in *dev_status. */
@@ -299,6 +304,10 @@ kvq3_status kvq3_decode_attn(kvq3_rotation rot, const kvq3_cache_desc *desc,
  *     need more than the array holds (kvq3_decode_workspace_size tells).
  *   - The first call on a device looks up the array's device address with
  *     that device current; make that first call before any stream capture.
+ *     The address is kept for the life of the process: after a
+ *     cudaDeviceReset (or any other teardown of the device's primary
+ *     context) the module may load elsewhere, so do not call this entry
+ *     point again on that device after such a reset.
  *   - All calls share the one array per device, and it keeps whatever the
  *     last call left in it (nothing needs clearing: every partial the merge
  *     reads is written earlier in the same call).  Calls that overlap on the

@@ -306,3 +306,76 @@ def test_prefill_is_causal(oracle, scale, bits):
     moved = np.abs(after - before).max(axis=(1, 2))
     assert np.all(moved[:p - pos0] == 0.0)
     assert np.all(moved[p - pos0:] > 1e-6)
+
+
+# ---------------------------------------------------------------- softmax scale
+def _two_token_cache(oracle, d=128):
+    """A cache whose dequantised rotated keys and values are known in closed
+    form.  With the rotation flags off, U = H_d.  Key 0 = e_0 and key 1 = -e_0
+    rotate to +-(1/sqrt d) 1, whose blocks all quantise to +-3 (the worked
+    example of the packing pins) with the fp32 scale s_q = fl32((1/sqrt d +
+    eps)/3); so k_hat_0 = -k_hat_1 = 3 s_q 1.  Value t = e_(t+1) rotates to
+    +-(1/sqrt d) entries, all codes +-3 with the same s_q, so
+    U^T v_hat_t = 3 s_q sqrt(d) e_(t+1)."""
+    signs, quats = oracle.rotation_params(d, 42, False, False)
+    U = oracle.rotation_matrix(signs, quats)
+    L = oracle.Layout(d, 1, 64, "f32", 16, 1, 1, 1)
+    pool = np.zeros(L.pool_bytes, np.uint8)
+    k = np.zeros((2, 1, d), np.float16)
+    v = np.zeros((2, 1, d), np.float16)
+    k[0, 0, 0], k[1, 0, 0] = 1.0, -1.0
+    v[0, 0, 1], v[1, 0, 2] = 1.0, 1.0
+    assert oracle.write(pool, L, U, k, v, np.zeros(2, np.int32), np.arange(2)) == 0
+    s_q = float(np.float32((1.0 / math.sqrt(d) + 1e-6) / 3.0))
+    return U, L, pool, s_q
+
+
+@pytest.mark.parametrize("alpha", [0.5, 3.0, -2.0])
+def test_default_softmax_scale_is_one_over_sqrt_d(oracle, alpha):
+    # Orthogonally mixed 3-bit KV cache, Key formulas: softmax(Q K^T / sqrt d).
+    # Query q = alpha e_0 rotates to q1 = (alpha/sqrt d) 1, so the two logits
+    # are +-(q1 . 3 s_q 1) = +-3 alpha s_q sqrt d and, after the 1/sqrt(d)
+    # scale, +-z with z = 3 alpha s_q.  Token 0 then weighs
+    # w0 = 1/(1 + e^(-2z)) and the output is 3 s_q sqrt(d) (w0 e_1 + w1 e_2).
+    # Dropping the scale (z sqrt d) or using 1/d (z / sqrt d) moves w0 by
+    # 0.02-0.4 at these alphas.
+    d = 128
+    U, L, pool, s_q = _two_token_cache(oracle, d)
+    q = np.zeros((1, 1, d), np.float16)
+    q[0, 0, 0] = alpha
+    z = 3.0 * alpha * s_q
+    w0 = 1.0 / (1.0 + math.exp(-2.0 * z))
+    mag = 3.0 * s_q * math.sqrt(d)
+    want = np.zeros(d)
+    want[1], want[2] = w0 * mag, (1.0 - w0) * mag
+    got = oracle.decode(pool, L, U, q, np.array([2]))[0, 0]
+    assert np.abs(got - want).max() < 1e-12
+    # the wrong scales are told apart by far more than the tolerance
+    for wrong in (1.0, 1.0 / d):
+        zw = 3.0 * alpha * s_q * math.sqrt(d) * wrong
+        w0w = 1.0 / (1.0 + math.exp(-2.0 * zw))
+        assert abs(w0w - w0) * mag > 1e-3
+    # an explicit sm_scale replaces the default
+    got2 = oracle.decode(pool, L, U, q, np.array([2]), sm_scale=1.0)[0, 0]
+    z2 = 3.0 * alpha * s_q * math.sqrt(d)
+    w02 = 1.0 / (1.0 + math.exp(-2.0 * z2))
+    assert abs(got2[1] - w02 * mag) < 1e-12 and abs(got2[2] - (1.0 - w02) * mag) < 1e-12
+
+
+def test_prefill_default_softmax_scale(oracle):
+    # The prefill chunk's second query (position 1) sees both tokens with the
+    # same 1/sqrt(d)-scaled logistic weights; its first query (position 0)
+    # sees token 0 alone.
+    d = 128
+    U, L, pool, s_q = _two_token_cache(oracle, d)
+    q = np.zeros((2, 1, d), np.float16)
+    q[0, 0, 0], q[1, 0, 0] = 1.5, 1.5
+    out = oracle.prefill(pool, L, U, q, 0, 0)
+    mag = 3.0 * s_q * math.sqrt(d)
+    first = np.zeros(d)
+    first[1] = mag
+    assert np.abs(out[0, 0] - first).max() < 1e-12
+    w0 = 1.0 / (1.0 + math.exp(-2.0 * 3.0 * 1.5 * s_q))
+    second = np.zeros(d)
+    second[1], second[2] = w0 * mag, (1.0 - w0) * mag
+    assert np.abs(out[1, 0] - second).max() < 1e-12
