@@ -91,6 +91,44 @@ kvq3_status prefill_geom(const kvq3_cache_desc* desc, int32_t hq, int64_t n_q, C
   return KVQ3_OK;
 }
 
+kvq3_status decode_attn_impl(kvq3_rotation rot, const kvq3_cache_desc* desc, const kvq3_cache* cache,
+                             const void* q, int32_t num_q_heads, float sm_scale, float* out,
+                             void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream,
+                             uint32_t wait_polls) {
+  CacheGeom g;
+  kvq3_status s = make_geom(desc, &g);
+  if (s != KVQ3_OK) return s;
+  if (!rot || rot->d != g.d || !q || !out) return KVQ3_ERR_INVALID_ARG;
+  if ((s = check_cache(g, cache, true)) != KVQ3_OK) return s;
+  if ((s = check_heads(g, num_q_heads)) != KVQ3_OK) return s;
+  if (!(sm_scale <= 0.0f || isfinite(sm_scale))) return KVQ3_ERR_INVALID_ARG;
+  const int G = num_q_heads / g.hkv;
+  DecodePlan plan;
+  if ((s = plan_for(g, G, &plan)) != KVQ3_OK) return s;
+  if (!workspace || ws_bytes < plan.ws_bytes || reinterpret_cast<uintptr_t>(workspace) % 256)
+    return KVQ3_ERR_WORKSPACE;
+  DecodeParams prm;
+  memset(&prm, 0, sizeof(prm));
+  prm.g = g;
+  prm.pool = static_cast<const uint8_t*>(cache->pool);
+  prm.page_table = cache->page_table;
+  prm.seq_lens = cache->seq_lens;
+  prm.q = static_cast<const __half*>(q);
+  prm.ws = static_cast<float*>(workspace);
+  prm.unit_cta = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) +
+                                            ((size_t)plan.ctas + (size_t)g.batch * g.hkv) * G * (g.d + 2) *
+                                                sizeof(float));
+  prm.status = dev_status;
+  prm.G = G;
+  prm.Hq = num_q_heads;
+  const double sc = sm_scale > 0.0f ? (double)sm_scale : 1.0 / sqrt((double)g.d);
+  prm.qk_scale = (float)(sc * 1.4426950408889634);  // log2(e): softmax in base 2
+  prm.inv_sqrt_d = inv_sqrt(g.d);
+  prm.slot_floats = (uint32_t)(G * (g.d + 2));
+  prm.wait_limit = wait_polls;
+  return run_for(g, plan, prm, rot->params, out, static_cast<cudaStream_t>(stream));
+}
+
 }  // namespace
 
 extern "C" {
@@ -158,7 +196,7 @@ kvq3_status kvq3_prefill_attn(kvq3_rotation rot, const kvq3_cache_desc* desc,
   prm.qk_scale = (float)(sc * 1.4426950408889634);  // log2(e): softmax in base 2
   prm.inv_sqrt_d = inv_sqrt(vg.d);
   prm.slot_floats = (uint32_t)(gcols * (vg.d + 2));
-  prm.wait_limit = 1u << 22;
+  prm.wait_limit = kWaitPolls;
   prm.pf_n = (int32_t)n_q;
   prm.pf_qt = qt;
   prm.pf_hb = hb;
@@ -186,38 +224,21 @@ kvq3_status kvq3_decode_attn(kvq3_rotation rot, const kvq3_cache_desc* desc,
                              const kvq3_cache* cache, const void* q, int32_t num_q_heads,
                              float sm_scale, float* out, void* workspace, size_t ws_bytes,
                              int32_t* dev_status, void* stream) {
-  CacheGeom g;
-  kvq3_status s = make_geom(desc, &g);
-  if (s != KVQ3_OK) return s;
-  if (!rot || rot->d != g.d || !q || !out) return KVQ3_ERR_INVALID_ARG;
-  if ((s = check_cache(g, cache, true)) != KVQ3_OK) return s;
-  if ((s = check_heads(g, num_q_heads)) != KVQ3_OK) return s;
-  if (!(sm_scale <= 0.0f || isfinite(sm_scale))) return KVQ3_ERR_INVALID_ARG;
-  const int G = num_q_heads / g.hkv;
-  DecodePlan plan;
-  if ((s = plan_for(g, G, &plan)) != KVQ3_OK) return s;
-  if (!workspace || ws_bytes < plan.ws_bytes || reinterpret_cast<uintptr_t>(workspace) % 256)
-    return KVQ3_ERR_WORKSPACE;
-  DecodeParams prm;
-  memset(&prm, 0, sizeof(prm));
-  prm.g = g;
-  prm.pool = static_cast<const uint8_t*>(cache->pool);
-  prm.page_table = cache->page_table;
-  prm.seq_lens = cache->seq_lens;
-  prm.q = static_cast<const __half*>(q);
-  prm.ws = static_cast<float*>(workspace);
-  prm.unit_cta = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) +
-                                            ((size_t)plan.ctas + (size_t)g.batch * g.hkv) * G * (g.d + 2) *
-                                                sizeof(float));
-  prm.status = dev_status;
-  prm.G = G;
-  prm.Hq = num_q_heads;
-  const double sc = sm_scale > 0.0f ? (double)sm_scale : 1.0 / sqrt((double)g.d);
-  prm.qk_scale = (float)(sc * 1.4426950408889634);  // log2(e): softmax in base 2
-  prm.inv_sqrt_d = inv_sqrt(g.d);
-  prm.slot_floats = (uint32_t)(G * (g.d + 2));
-  prm.wait_limit = 1u << 22;
-  return run_for(g, plan, prm, rot->params, out, static_cast<cudaStream_t>(stream));
+  return decode_attn_impl(rot, desc, cache, q, num_q_heads, sm_scale, out, workspace, ws_bytes,
+                          dev_status, stream, kWaitPolls);
+}
+
+// Test hook, not part of the public header: kvq3_decode_attn with the bound
+// on each stage wait set to `polls` mbarrier polls.  With polls = 0 no wait
+// can succeed, so every CTA takes its time-out path (flag KVQ3_DEV_TIMEOUT,
+// drain its copies in flight, return) while every copy still targets valid
+// memory: the time-out path runs without any fault or hang.
+kvq3_status kvq3_test_decode_attn_polls(kvq3_rotation rot, const kvq3_cache_desc* desc,
+                                        const kvq3_cache* cache, const void* q, int32_t num_q_heads,
+                                        float sm_scale, float* out, void* workspace, size_t ws_bytes,
+                                        int32_t* dev_status, void* stream, uint32_t polls) {
+  return decode_attn_impl(rot, desc, cache, q, num_q_heads, sm_scale, out, workspace, ws_bytes,
+                          dev_status, stream, polls);
 }
 
 }  // extern "C"

@@ -55,6 +55,11 @@ constexpr int kChunk = 192;      // minimum tokens per chunk (smaller pages are 
 constexpr int kMaxPagesPerChunk = kChunk / 16;
 constexpr int kWarps = 4;        // consumer warps per CTA
 constexpr int kMaxStages = 8;
+// Bound on the polls of the drain after a timed-out copy (the normal waits
+// take DecodeParams::wait_limit).
+constexpr uint32_t kDrainPolls = 1u << 22;
+// Default bound on the polls of a stage wait.
+constexpr uint32_t kWaitPolls = 1u << 22;
 
 struct DecodeParams {
   CacheGeom g;
@@ -1249,12 +1254,16 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
     // only the slowest warp can trigger).
     named_barrier(2, 32 * kWarps);
     if (*abort_s) {
-      // a copy never arrived: flag it, wait (bounded) for the copies still in
-      // flight (chunks up to i + S - 2) so no asynchronous write outlives this
-      // CTA, and stop
+      // A copy did not arrive within the bound: flag it, wait for every copy
+      // this CTA still has in flight so that no asynchronous write outlives
+      // it, and stop.  In flight: chunk i itself (the one that ran out) up to
+      // the last chunk issued, S - 1 from the prologue at i = 0, else i + S - 2
+      // (the refill of iteration i - 1).  The drain has its own bound,
+      // independent of the caller's wait limit.
       if (threadIdx.x == 0) set_status(p.status, KVQ3_DEV_TIMEOUT);
-      for (int64_t k = i + 1; k < nch && k < i + S - 1; ++k)
-        mbar_wait(&full[k % S], (uint32_t)((k / S) & 1), p.wait_limit);
+      const int64_t last = i == 0 ? (int64_t)S - 1 : i + S - 2;
+      for (int64_t k = i; k < nch && k <= last; ++k)
+        mbar_wait(&full[k % S], (uint32_t)((k / S) & 1), kDrainPolls);
       return;
     }
     if (i > 0 && (((int)i - 1) & (kWarps - 1)) == wid && i - 1 + S < nch) {

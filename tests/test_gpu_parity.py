@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 
 from cases import TOL_DECODE, Case, flip_bound, rel_err, written_differences
+from oracle import kvq3_oracle as O
 
 pytestmark = pytest.mark.gpu
 
@@ -85,9 +86,24 @@ def test_write_single_token_appends_and_scatter():
     si = np.array([3, 0, 2, 1], np.int32)
     ps = np.array([499, 0, 63, 64], np.int32)
     c.gpu_write(k, v, si, ps)
-    c.oracle_write(k, v, si, ps)
-    c.compare_written(k, v, si, ps)
-    assert np.array_equal(c.pool.cpu().numpy(), c.pool_o) or True
+    assert c.oracle_write(k, v, si, ps) == 0
+    assert c.device_status() == 0
+    stats = c.compare_written(k, v, si, ps)
+    # slots nobody wrote stay zero on both sides; with nothing excluded by the
+    # write bar the whole pool is byte-identical
+    if stats["boundary_codes"] == 0 and stats["midpoint_blocks"] == 0:
+        assert np.array_equal(c.pool.cpu().numpy(), c.pool_o)
+    else:
+        written = np.zeros(c.layout.pool_bytes, bool)
+        page, slot, _ = O.locate(c.layout, c.table, si, ps)
+        for pg, sl in zip(page, slot):
+            for rec in range(2 * c.hkv):
+                base = pg * c.layout.page_bytes + rec * c.layout.record_bytes
+                nb_sb = c.layout.nb * c.layout.sb
+                written[base + sl * nb_sb: base + (sl + 1) * nb_sb] = True
+                co = base + c.page * nb_sb + sl * c.layout.code_bytes
+                written[co: co + c.layout.code_bytes] = True
+        assert np.array_equal(c.pool.cpu().numpy()[~written], c.pool_o[~written])
 
 
 def test_write_bad_slots_flag_and_skip():
@@ -237,16 +253,43 @@ def test_decode_bad_length_and_bad_page():
     assert np.all(np.isfinite(got))
 
 
-def test_decode_split_count_invariance():
-    # the same sequences decoded alone (many warps per sequence) and inside a
-    # large batch (few warps per sequence) give the same result
+def test_decode_split_count_invariance(oracle):
+    # The same sequence decoded alone and inside a large batch.  Alone, its
+    # 12 chunks of 256 tokens go to 12 CTAs (a 12-way split merged by the
+    # combine kernel); in the batch, 640 units of 2 chunks share the CTAs, so
+    # sequence 0's unit lies within one CTA or straddles two.  Both runs must
+    # match the oracle (which does not split at all) and each other.
+    import hadamard_rotated_bit_kvq3_gb300 as K
     c1 = Case(d=128, block=64, scale="f16", page=64, lens=(3000,), hkv=1, hq=4)
     k, v, si, ps = c1.tokens()
     c1.oracle_write(k, v, si, ps)
     c1.upload_oracle_pool()
     q = c1.queries()
     a = c1.gpu_decode(q)
-    assert rel_err(a, c1.oracle_decode(q)) <= TOL_DECODE
+    ref = c1.oracle_decode(q)
+    assert c1.device_status() == 0
+    assert rel_err(a, ref) <= TOL_DECODE
+    # sequence 0 again (same seeds, so the same keys, values and queries),
+    # now with 639 more sequences of 512 tokens after it
+    lens = (3000,) + (512,) * 639
+    c2 = Case(d=128, block=64, scale="f16", page=64, lens=lens, hkv=1, hq=4)
+    k2, v2, si2, ps2 = c2.tokens()
+    c2.oracle_write(k2, v2, si2, ps2)
+    c2.upload_oracle_pool()
+    q2 = c2.queries()
+    assert np.array_equal(q2[0], q[0])
+    ws_alone = K.kvq3_decode_workspace_size(c1.desc, 4)
+    ws_batch = K.kvq3_decode_workspace_size(c2.desc, 4)
+    assert ws_batch > ws_alone
+    b2 = c2.gpu_decode(q2)
+    assert c2.device_status() == 0
+    assert rel_err(b2[0], ref[0]) <= TOL_DECODE
+    assert rel_err(b2[0], a[0]) <= TOL_DECODE
+    # a sample of the other sequences against the oracle as well
+    heads = [(b, h) for b in (1, 317, 639) for h in range(4)]
+    ref2 = oracle.decode(c2.pool_o, c2.layout, c2.U, q2, c2.lens, heads=heads)
+    for b in (1, 317, 639):
+        assert rel_err(b2[b], ref2[b]) <= TOL_DECODE
 
 
 # ------------------------------------------------------------------ write (prefill chunks)
@@ -293,10 +336,18 @@ def test_write_chunk_equals_token_list_write():
                        torch.as_tensor(v, device="cuda"), 0, 0, c1.status)
     c2.gpu_write(k, v, si, ps)
     torch.cuda.synchronize()
+    assert c1.device_status() == 0 and c2.device_status() == 0
+    # Both entry points meet the same write bar against the oracle: codes
+    # bit-exact except within 1e-4 of a rounding boundary, scales exact except
+    # at a storage midpoint.  Their two fp32 butterflies may round such a
+    # boundary element differently, so byte equality between them holds
+    # wherever the oracle's bar leaves no choice.
+    s1 = c1.compare_written(k, v, si, ps)
+    s2 = c2.compare_written(k, v, si, ps)
     a, b = c1.pool.cpu().numpy(), c2.pool.cpu().numpy()
-    # both are fp32 computations of the same formula; allow only boundary flips
-    diff = np.nonzero(a != b)[0]
-    assert len(diff) <= 0.0005 * a.size
+    if s1["boundary_codes"] == 0 and s1["midpoint_blocks"] == 0 and \
+            s2["boundary_codes"] == 0 and s2["midpoint_blocks"] == 0:
+        assert np.array_equal(a, b)
 
 
 def test_write_chunk_rejects_out_of_range():
@@ -308,3 +359,39 @@ def test_write_chunk_rejects_out_of_range():
         K.kvq3_write_chunk(c.rot.handle, c.desc, c.cache, k, k, 0, c.maxp * 64 - 5, c.status)
     with pytest.raises(K.Kvq3Error):
         K.kvq3_write_chunk(c.rot.handle, c.desc, c.cache, k, k, 3, 0, c.status)
+
+
+# ------------------------------------------------------------------ margin at large groups
+# At G = 8 and 16 the probabilities-times-value-scales enter PV as one fp16
+# rounding (no hi + lo split).  Several data seeds per case, isolated and end
+# to end, to see how close the worst case sits to the bar.
+SEED_CASES = [
+    dict(d=128, block=64, scale="e4m3", page=64, lens=(1500, 400), hkv=2, hq=16),     # G=8, E4M3
+    dict(d=128, block=64, scale="f16", page=64, lens=(1500, 400), hkv=2, hq=32),      # G=16
+    dict(d=256, block=64, scale="f16", page=16, lens=(900, 33), hkv=1, hq=8, paged=True),   # G=8, d256
+]
+
+
+@pytest.mark.parametrize("seed", [11, 12, 13, 14])
+@pytest.mark.parametrize("cfg", SEED_CASES, ids=_ids)
+def test_decode_large_group_over_seeds(cfg, seed):
+    import kvq3_inputs as I
+    cfg = dict(cfg, data=I.DataSpec(cfg["d"], cfg["hkv"], seed, 0.03, 20.0))
+    c = Case(**cfg)
+    k, v, si, ps = c.tokens()
+    c.oracle_write(k, v, si, ps)
+    c.upload_oracle_pool()
+    q = c.queries(seed)
+    e_iso = rel_err(c.gpu_decode(q), c.oracle_decode(q))
+    assert c.device_status() == 0
+    c.pool.zero_()
+    c.gpu_write(k, v, si, ps)
+    got, ref = c.gpu_decode(q), c.oracle_decode(q)
+    assert c.device_status() == 0
+    rms = math.sqrt(float(np.mean(ref ** 2)))
+    slack = flip_bound(c, k, v, si, ps, q, differs=written_differences(c, k, v, si, ps))
+    err = np.abs(got - ref).max(axis=-1)
+    print(f"seed {seed}: isolated {e_iso:.3e}, end to end {rel_err(got, ref):.3e} "
+          f"(worst (err - slack)/rms {float((err - slack).max()) / rms:.3e})")
+    assert e_iso <= TOL_DECODE
+    assert np.all(err <= TOL_DECODE * rms + slack)
