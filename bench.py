@@ -1,14 +1,22 @@
 """Benchmark of the rotated 3-bit KV cache on GB300.
 
-One step = one decode step of one layer for every sequence of the workload:
-kvq3_write appends the current token's K and V (one per sequence, position
-N-1) and kvq3_decode_attn attends over the N cached tokens.  The default
-workload is the Llama-3-8B-shaped layer (batch 16, 32 query heads over 8 kv
-heads, d = 128, 32,768-token contiguous cache, blocks of 64 with fp16
-scales).  Inputs are seeded synthetic data (kvq3_inputs).
+Decode workloads: one step = one decode step of one layer for every sequence
+of the workload -- kvq3_write appends the current token's K and V (one per
+sequence, position N-1) and kvq3_decode_attn attends over the N cached
+tokens.  The write-path workload: one step rotates, quantises and packs the
+whole prefill (131,072 tokens x 8 kv heads, K and V) with kvq3_write_chunk.
+Inputs are seeded synthetic data (kvq3_inputs).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-  python bench.py --impl reference ...   (the CPU oracle, bounded sample)
+The default run measures every single-GPU workload in one process and prints
+one JSON line.  Its headline is the largest decode workload, ragged (batch 64,
+lengths drawn from [1,024, 65,536], d = 256, paged); the 70B-shaped 128K
+decode (long70b), the Llama-3-8B-shaped decode (llama8b) and the prefill
+write path (prefill) ride along under "configs", each with its own roofline,
+end-to-end figure and CPU-oracle baseline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W]
+  python bench.py --workload NAME ...     (one workload only; --profile for ncu)
+  python bench.py --impl reference ...    (the CPU oracle, bounded sample)
 
 Multi-GPU: every rank serves its own batch of sequences (data parallel over
 (sequence, kv head) units, no exchange on the data path): weak scaling.
@@ -32,9 +40,6 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 import kvq3_inputs as I  # noqa: E402
-
-DEFAULT_WORKLOAD = "llama8b"
-
 
 # ---------------------------------------------------------------------- helpers
 def algorithmic_bytes(w: I.Workload, lens) -> dict:
@@ -88,18 +93,6 @@ def load_peaks() -> dict:
         d = json.load(open(p))
         return dict(hbm=float(d["hbm_gbs"]), src="measured")
     return dict(hbm=6800.0, src="fallback")
-
-
-def recorded_traffic(name: str, bits: int = 3):
-    """DRAM bytes per decode launch from the committed ncu summary, if it was
-    taken on the current kernel sources (3-bit codes)."""
-    p = os.path.join(ROOT, "profiles", f"decode_{name}_traffic.json")
-    if bits != 3:
-        return None
-    if not os.path.exists(p):
-        return None
-    d = json.load(open(p))
-    return d["dram_bytes_per_launch"] if d.get("source_hash") == source_hash() else None
 
 
 class ClockSampler:
@@ -314,7 +307,7 @@ def cpu_baseline(w: I.Workload, lens, budget_s: float = 15.0) -> dict:
         run()
     per_unit = (time.perf_counter() - t0) / n
     step_s = per_unit * units * float(np.mean(lens)) / int(lens[0])
-    return {"value": w.batch / step_s, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+    return {"value": w.batch / step_s, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
             "sample": f"unit (b=0, kv head 0): write 1 token + decode {w.group} heads over "
                       f"{int(lens[0])} tokens, x{n} runs; scaled to {units} units"}
 
@@ -365,7 +358,7 @@ def timed_cpu_baseline(run, to_value, unit: str, what: str, budget_s: float = 15
     for _ in range(n):
         run()
     per = (time.perf_counter() - t0) / n
-    return {"value": to_value(per), "unit": unit, "cores": os.cpu_count(), "kind": "oracle",
+    return {"value": to_value(per), "unit": unit, "cores": blas_threads(), "kind": "oracle",
             "sample": f"{what}; x{n} runs"}
 
 
@@ -411,39 +404,383 @@ def oracle_prefill_sample(w: I.Workload, n_q: int):
     return run
 
 
+DECODE_METRIC = "decode tokens/s (one layer, all heads)"
+WRITE_METRIC = "write-path GB/s (fp16 in + packed out)"
+PREFILL_ATTN_METRIC = "prefill-attention query tokens/s (one layer, all heads)"
+PRIMARY = "ragged"                                 # the largest single-GPU decode workload
+EXTRAS = ("long70b", "llama8b", "prefill")         # measured in the same run, under "configs"
+NOMINAL_HBM_GBS = 8000.0                           # the HBM peak the method's target is quoted against
+
+
+def sbytes(w: I.Workload) -> int:
+    return {"f32": 4, "f16": 2, "e4m3": 1, "e4m3zp": 2}[w.scale]
+
+
+def blas_threads() -> int:
+    """Threads numpy's BLAS may use (the oracle's matrix products); its other
+    steps run on one Python thread."""
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        v = os.environ.get(var)
+        if v and v.isdigit():
+            return int(v)
+    return os.cpu_count() or 1
+
+
+def workload_config(w: I.Workload, lens, world: int) -> dict:
+    """The "config" object of a workload's JSON record (the same for both arms)."""
+    if w.decode:
+        ab = algorithmic_bytes(w, lens)
+        return {"workload": workload_desc(w),
+                "l2": f"inputs larger than L2 (packed cache {ab['decode'] / 1e6:.0f} MB per step)",
+                "parallelism": f"replicas x{world} (dp over sequences)"}
+    if w.chunk > 0:
+        return {"workload": f"{w.name}: chunk of {w.chunk} queries at positions {w.seq_len - w.chunk}.."
+                            f"{w.seq_len - 1} of a {w.seq_len}-token cache, Hkv{w.num_kv_heads} "
+                            f"Hq{w.num_q_heads} d{w.d} m{w.block} {w.scale} scales, {w.bits}-bit codes, contiguous "
+                            f"P{w.page_size}, causal", "l2": "cache 3.4 MB per kv head",
+                "parallelism": f"replicas x{world}"}
+    return {"workload": f"prefill: {w.seq_len} tokens x Hkv{w.num_kv_heads} x d{w.d}, K+V fp16, "
+                        f"sign flip + FWHT, m{w.block} {w.scale} scales, {w.bits}-bit codes",
+            "l2": "inputs larger than L2 (537 MB fp16 in, 134 MB packed out per step)",
+            "parallelism": f"replicas x{world}"}
+
+
+def recorded_traffic_of(kernel: str, name: str):
+    """DRAM bytes per launch from the committed ncu summary of `kernel` on
+    workload `name`, if it was taken on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", f"{kernel}_{name}_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    return d["dram_bytes_per_launch"] if d.get("source_hash") == source_hash() else None
+
+
+def _median(xs):
+    return statistics.median(xs) if xs else float("nan")
+
+
+def time_decode(st, steps: int, warmup: int, world: int, stream) -> dict:
+    """Device-timed steps of a decode workload, inputs resident: per step an
+    event before the write, between write and decode and after the decode;
+    the whole region between barriers (max over ranks)."""
+    import torch
+    for _ in range(warmup):
+        st.step()
+    torch.cuda.synchronize()
+    assert int(st.status.item()) == 0, f"device status {int(st.status.item())}"
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(steps):
+        ev[i][0].record(stream)
+        st.write(st.k_new, st.v_new, st.seq_new, st.pos_new)
+        ev[i][1].record(stream)
+        st.decode()
+        ev[i][2].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
+    dec = [e[1].elapsed_time(e[2]) for e in ev]
+    wr = [e[0].elapsed_time(e[1]) for e in ev]
+    step = [e[0].elapsed_time(e[2]) for e in ev]
+    assert int(st.status.item()) == 0
+    return dict(ms_step=total_ms / steps, ms_step_median=_median(step), dec_median=_median(dec),
+                dec_mean=statistics.mean(dec), wr_median=_median(wr), wr_mean=statistics.mean(wr))
+
+
+def time_decode_e2e(st, steps: int, warmup: int, world: int, stream, dev) -> dict:
+    """The same step through pinned host buffers with the copies inside the
+    timed region: the step's inputs (new k, v, the queries, positions,
+    sequence ids) sit in one pinned host buffer and go over in one copy; the
+    output comes back."""
+    import torch
+    srcs = (st.k_new, st.v_new, st.q, st.pos_new, st.seq_new)
+    offs, total = [], 0
+    for t in srcs:
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    inp_h = torch.empty(total, dtype=torch.uint8).pin_memory()
+    inp_d = torch.empty(total, dtype=torch.uint8, device=dev)
+    views_d = []
+    for t, o in zip(srcs, offs):
+        nb = t.numel() * t.element_size()
+        inp_h[o:o + nb].copy_(t.cpu().contiguous().view(-1).view(torch.uint8))
+        views_d.append(inp_d[o:o + nb].view(t.dtype).view(t.shape))
+    k_d, v_d, q_d, pos_d, seq_d = views_d
+    out_h = torch.empty(st.out.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in srcs)
+    d2h = out_h.numel() * out_h.element_size()
+
+    def e2e_step():
+        inp_d.copy_(inp_h, non_blocking=True)
+        st.write(k_d, v_d, seq_d, pos_d)
+        st.decode(q_d, st.out)
+        out_h.copy_(st.out, non_blocking=True)
+
+    for _ in range(warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    assert int(st.status.item()) == 0
+    return dict(ms=max_over_ranks(a.elapsed_time(b), world) / steps, h2d=h2d, d2h=d2h)
+
+
+def decode_record(name: str, args, world: int, rank: int, dev, peaks: dict, cpu: bool) -> dict:
+    """Builds, times and tears down one decode workload; returns its record."""
+    import torch
+    st = GpuWorkload(name, dev, rank, args.batch)
+    w = st.w
+    stream = torch.cuda.current_stream()
+    t = time_decode(st, args.steps, args.warmup, world, stream)
+    e = time_decode_e2e(st, args.steps, args.warmup, world, stream, dev)
+    ab = algorithmic_bytes(w, st.lens)
+    gbs = ab["decode"] / (t["dec_median"] * 1e-3) / 1e9
+    rec = {
+        "metric": DECODE_METRIC, "value": whole_job_rate(w.batch, world, t["ms_step"]), "unit": "tokens/s",
+        "ms_per_step": t["ms_step"], "ms_per_step_median": t["ms_step_median"],
+        "dtype": f"f16 mma / f32 accumulate ({w.bits}-bit packed cache)",
+        "config": workload_config(w, st.lens, world),
+        "decode": {"ms_median": t["dec_median"], "ms_mean": t["dec_mean"], "hbm_gbs": gbs,
+                   "frac_of_peak": gbs / peaks["hbm"], "frac_of_nominal": gbs / NOMINAL_HBM_GBS,
+                   "bytes": ab["decode"], "bytes_per_token_head": ab["per_token_head"]},
+        "write": {"ms_median": t["wr_median"], "gbs": ab["write"] / (t["wr_median"] * 1e-3) / 1e9,
+                  "bytes": ab["write"]},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm"], "frac_of_nominal": gbs / NOMINAL_HBM_GBS,
+                     "traffic": recorded_traffic_of("decode", name) if w.bits == 3 and not args.batch else None,
+                     "kernel": "kvq3_decode_attn (decode_split_kernel + decode_combine_kernel)",
+                     "timing": "median over steps of CUDA events around the kvq3_decode_attn call",
+                     "peak_source": peaks["src"]},
+        "e2e": {"value": whole_job_rate(w.batch, world, e["ms"]), "unit": "tokens/s",
+                "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"]},
+        "gpu_launches": 3 * args.steps,
+    }
+    if cpu:
+        rec["cpu_baseline"] = cpu_baseline(w, st.lens)
+    del st
+    torch.cuda.empty_cache()
+    return rec
+
+
+def prefill_record(args, world: int, rank: int, dev, peaks: dict, cpu: bool) -> dict:
+    """The write-path workload: device-timed steps (inputs resident), then
+    the same step with the fp16 input copied from pinned host memory and the
+    packed cache read back inside the timed region."""
+    import torch
+    st = PrefillWorkload(dev, args.tokens)
+    w = st.w
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        st.step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        st.step()
+        ev[i][1].record(stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    assert int(st.status.item()) == 0
+    ms = max_over_ranks(a.elapsed_time(b), world) / args.steps
+    med = _median([x.elapsed_time(y) for x, y in ev])
+    nbytes = st.bytes()
+    gbs_med = nbytes / (med * 1e-3) / 1e9
+    # end to end: fp16 K, V from pinned host memory, packed pool back
+    k_h = st.k.cpu().pin_memory()
+    v_h = st.v.cpu().pin_memory()
+    pool_h = torch.empty(st.pool.shape, dtype=torch.uint8).pin_memory()
+
+    def e2e_step():
+        st.k.copy_(k_h, non_blocking=True)
+        st.v.copy_(v_h, non_blocking=True)
+        st.step()
+        pool_h.copy_(st.pool, non_blocking=True)
+
+    for _ in range(min(args.warmup, 3)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    a.record(stream)
+    n_e2e = max(3, min(args.steps, 20))
+    for _ in range(n_e2e):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(a.elapsed_time(b), world) / n_e2e
+    rec = {
+        "metric": WRITE_METRIC, "value": whole_job_rate(nbytes, world, ms) / 1e9, "unit": "GB/s",
+        "ms_per_step": ms, "ms_per_step_median": med, "dtype": "f32",
+        "config": workload_config(w, None, world),
+        "roofline": {"bound": "hbm", "achieved": gbs_med, "peak": peaks["hbm"], "unit": "GB/s",
+                     "frac": gbs_med / peaks["hbm"], "frac_of_nominal": gbs_med / NOMINAL_HBM_GBS,
+                     "traffic": recorded_traffic_of("write_chunk", "prefill") if not args.tokens else None,
+                     "kernel": "write_chunk_kernel", "bytes": nbytes,
+                     "timing": "median over steps of CUDA events around the kvq3_write_chunk call",
+                     "peak_source": peaks["src"]},
+        "tokens_per_s": whole_job_rate(w.seq_len, world, ms),
+        "e2e": {"value": whole_job_rate(nbytes, world, e2e_ms) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": (k_h.numel() + v_h.numel()) * 2, "d2h_bytes_per_step": pool_h.numel(),
+                "steps": n_e2e},
+        "gpu_launches": args.steps,
+    }
+    if cpu:
+        n_tok = 256
+        nb = n_tok * w.num_kv_heads * 2 * (2 * w.d + w.bits * w.d // 8 + (w.d // w.block) * sbytes(w))
+        rec["cpu_baseline"] = timed_cpu_baseline(
+            oracle_write_sample(w, n_tok), lambda per: nb / per / 1e9, "GB/s",
+            f"oracle write of {n_tok} tokens x {w.num_kv_heads} kv heads, K and V")
+    del st
+    torch.cuda.empty_cache()
+    return rec
+
+
+def single_thread_oracle(names=("tiny", "llama8b")) -> dict:
+    """The oracle's decode step timed with every BLAS pool at one thread, in
+    a child process (the thread count of a BLAS library is fixed when it
+    loads)."""
+    out = {}
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    for n in names:
+        try:
+            p = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-leg", n], env=env,
+                               capture_output=True, text=True, timeout=300)
+            out[n] = json.loads(p.stdout.strip().splitlines()[-1]) if p.returncode == 0 else \
+                {"error": p.stderr.strip()[-300:]}
+        except (subprocess.TimeoutExpired, ValueError, IndexError) as e:
+            out[n] = {"error": str(e)[:300]}
+    return out
+
+
+def run_suite(args, world, rank, dev):
+    """The default run (every workload, one JSON line), or one named
+    workload."""
+    import torch
+    peaks = load_peaks()
+    cpu = not args.no_cpu_baseline and world == 1 and rank == 0
+    names = [args.workload] if args.workload else [PRIMARY, *EXTRAS]
+    if args.profile:
+        for name in names:
+            profile_steps(name, args, rank, dev)
+        return
+    records = {}
+    with ClockSampler(dev.index or 0) as clk:
+        for name in names:
+            if name == "prefill":
+                records[name] = prefill_record(args, world, rank, dev, peaks, False)
+            else:
+                records[name] = decode_record(name, args, world, rank, dev, peaks, False)
+            torch.cuda.synchronize()
+    clocks = clk.summary()
+    if rank != 0:
+        return
+    if cpu:   # after the GPU work: the oracle legs run on the host alone
+        for name in names:
+            w = workload(name)
+            if name == "prefill":
+                n_tok = 256
+                nb = n_tok * w.num_kv_heads * 2 * (2 * w.d + w.bits * w.d // 8 + (w.d // w.block) * sbytes(w))
+                records[name]["cpu_baseline"] = timed_cpu_baseline(
+                    oracle_write_sample(w, n_tok), lambda per, nb=nb: nb / per / 1e9, "GB/s",
+                    f"oracle write of {n_tok} tokens x {w.num_kv_heads} kv heads, K and V",
+                    budget_s=10.0 if name != names[0] else 15.0)
+            else:
+                if args.batch:
+                    import dataclasses
+                    w = dataclasses.replace(w, batch=args.batch)
+                records[name]["cpu_baseline"] = cpu_baseline(
+                    w, workload_lens(w), budget_s=10.0 if name != names[0] else 15.0)
+    head = records[names[0]]
+    line = {"metric": head["metric"], "value": head["value"], "unit": head["unit"], "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": head["dtype"],
+            "data": "synthetic", "config": head["config"]}
+    for key in ("ms_per_step_median", "decode", "write", "roofline", "e2e", "gpu_launches", "cpu_baseline",
+                "tokens_per_s"):
+        if key in head:
+            line[key] = head[key]
+    line["clocks"] = clocks
+    if len(names) > 1:
+        line["configs"] = {n: records[n] for n in names[1:]}
+        line["gpu_launches_all"] = sum(r["gpu_launches"] for r in records.values())
+    if cpu and not args.workload:
+        line["cpu_baseline_single_thread"] = single_thread_oracle()
+    print(json.dumps(line))
+
+
+def profile_steps(name, args, rank, dev):
+    """Plain steps only, for ncu captures (kernel order per decode step:
+    write, decode split, decode combine)."""
+    import torch
+    if name == "prefill":
+        st = PrefillWorkload(dev, args.tokens)
+    else:
+        st = GpuWorkload(name, dev, rank, args.batch)
+    for _ in range(args.warmup + args.steps):
+        st.step()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": name, "status": int(st.status.item())}))
+    del st
+    torch.cuda.empty_cache()
+
+
+def oracle_leg(name: str) -> None:
+    """One oracle timing (for single_thread_oracle): prints a cpu_baseline
+    record of workload `name` (decode step)."""
+    w = workload(name)
+    rec = cpu_baseline(w, workload_lens(w), budget_s=8.0)
+    rec["cores"] = blas_threads()
+    print(json.dumps(rec))
+
+
 def run_reference(args, world, rank):
     """The reference arm: the CPU oracle, timed as it stands on a bounded
-    sample of the workload (rank 0 only; about 120 s of timed work at most),
-    scaled to the workload's metric."""
-    w = workload(args.workload)
+    sample of the workload (rank 0 only; about 120 s of timed work at most).
+    Each timed step runs one sample (one (sequence, kv head) unit, or a slice
+    of the write or of the prefill chunk); ms_per_step is that measured time,
+    and value scales it to the whole workload by the factor in "sample"."""
+    w = workload(args.workload or PRIMARY)
     lens = workload_lens(w)
     if rank != 0:
         return
     if w.chunk > 0:            # prefill attention: query tokens/s
         n_q = 2
         run = oracle_prefill_sample(w, n_q)
-        metric, unit = "prefill-attention query tokens/s (one layer, all heads)", "tokens/s"
-        what = (f"each step: oracle prefill attention of the last {n_q} queries of the chunk (all "
+        metric, unit = PREFILL_ATTN_METRIC, "tokens/s"
+        what = (f"oracle prefill attention of the last {n_q} queries of the chunk (all "
                 f"{w.num_q_heads} heads) over the {w.seq_len}-token cache")
+        scale = w.chunk / n_q
         to_value = lambda per: n_q / per                                   # noqa: E731
-        to_step_s = lambda per: per * w.chunk / n_q                        # noqa: E731
     elif not w.decode:         # write path: GB/s of fp16 in + packed out
         n_tok = 256
         run = oracle_write_sample(w, n_tok)
-        sb = {"f32": 4, "f16": 2, "e4m3": 1, "e4m3zp": 2}[w.scale]
-        nbytes = n_tok * w.num_kv_heads * 2 * (2 * w.d + w.bits * w.d // 8 + (w.d // w.block) * sb)
-        metric, unit = "write-path GB/s (fp16 in + packed out)", "GB/s"
-        what = f"each step: oracle write of {n_tok} tokens x {w.num_kv_heads} kv heads, K and V"
+        nbytes = n_tok * w.num_kv_heads * 2 * (2 * w.d + w.bits * w.d // 8 + (w.d // w.block) * sbytes(w))
+        metric, unit = WRITE_METRIC, "GB/s"
+        what = f"oracle write of {n_tok} tokens x {w.num_kv_heads} kv heads, K and V"
+        scale = w.seq_len / n_tok
         to_value = lambda per: nbytes / per / 1e9                          # noqa: E731
-        to_step_s = lambda per: per * w.seq_len / n_tok                    # noqa: E731
     else:                      # decode: tokens/s of the whole batch
         units = w.batch * w.num_kv_heads
         run = oracle_sample(w, lens, 0)
-        metric, unit = "decode tokens/s (one layer, all heads)", "tokens/s"
-        what = (f"each step: oracle write 1 token + decode {w.group} query heads of one (sequence, "
-                f"kv head) unit over {int(lens[0])} tokens; scaled by {units} units")
-        to_step_s = lambda per: per * units * float(np.mean(lens)) / int(lens[0])   # noqa: E731
-        to_value = lambda per: w.batch / to_step_s(per)                    # noqa: E731
+        metric, unit = DECODE_METRIC, "tokens/s"
+        what = (f"oracle write of 1 token + decode of the {w.group} query heads of one (sequence, kv head) "
+                f"unit over {int(lens[0])} tokens")
+        scale = units * float(np.mean(lens)) / int(lens[0])
+        to_value = lambda per: w.batch / (per * scale)                     # noqa: E731
     for _ in range(min(args.warmup, 3)):
         run()
     # bounded: the timed samples stop after ~120 s of CPU work (at least one)
@@ -454,68 +791,19 @@ def run_reference(args, world, rank):
         done += 1
     per = (time.perf_counter() - t0) / done
     value = to_value(per)
+    sample = (f"each step: {what}; the workload is {scale:.4g} such samples (value = the sample rate "
+              f"scaled by that factor); {done} of {args.steps} steps timed (120 s cap)")
     line = {
         "impl": "reference", "metric": metric, "value": value,
-        "unit": unit, "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": to_step_s(per) * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f64", "data": "synthetic",
-        "config": {"workload": workload_desc(w)},
-        "cpu_baseline": {"value": value, "unit": unit, "cores": os.cpu_count(), "kind": "oracle",
-                         "sample": f"{what}; {done} steps timed (120 s cap)"},
+        "unit": unit, "n_gpus": args.gpus, "steps": done, "warmup": min(args.warmup, 3),
+        "ms_per_step": per * 1e3, "sample_scale": scale, "ms_per_workload_step": per * scale * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic", "config": workload_config(w, lens, world),
+        "cpu_baseline": {"value": value, "unit": unit, "cores": blas_threads(), "kind": "oracle",
+                         "sample": sample},
         "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
-
-
-def run_prefill(args, world, rank, dev):
-    """Write-path throughput: one step writes the whole prefill workload."""
-    import torch
-    st = PrefillWorkload(dev, args.tokens)
-    stream = torch.cuda.current_stream()
-    for _ in range(args.warmup):
-        st.step()
-    torch.cuda.synchronize()
-    if args.profile:
-        for _ in range(args.steps):
-            st.step()
-        torch.cuda.synchronize()
-        print(json.dumps({"profile": "prefill", "tokens": st.w.seq_len, "status": int(st.status.item())}))
-        return
-    barrier(world)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(dev.index or 0) as clk:
-        a.record(stream)
-        for _ in range(args.steps):
-            st.step()
-        b.record(stream)
-        torch.cuda.synchronize()
-    ms = max_over_ranks(a.elapsed_time(b), world) / args.steps
-    assert int(st.status.item()) == 0
-    peaks = load_peaks()
-    gbs = whole_job_rate(st.bytes(), world, ms) / 1e9
-    if rank == 0:
-        w = st.w
-        cpu = None
-        if not args.no_cpu_baseline and world == 1:
-            n_tok = 256
-            sb = {"f32": 4, "f16": 2, "e4m3": 1, "e4m3zp": 2}[w.scale]
-            nbytes = n_tok * w.num_kv_heads * 2 * (2 * w.d + w.bits * w.d // 8 + (w.d // w.block) * sb)
-            cpu = timed_cpu_baseline(oracle_write_sample(w, n_tok), lambda per: nbytes / per / 1e9, "GB/s",
-                                     f"oracle write of {n_tok} tokens x {w.num_kv_heads} kv heads, K and V")
-        print(json.dumps({
-            "metric": "write-path GB/s (fp16 in + packed out)", "value": gbs, "unit": "GB/s",
-            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic",
-            "config": {"workload": f"prefill: {w.seq_len} tokens x Hkv{w.num_kv_heads} x d{w.d}, K+V fp16, "
-                                   f"sign flip + FWHT, m{w.block} {w.scale} scales, {w.bits}-bit codes",
-                       "l2": "inputs larger than L2"},
-            "roofline": {"bound": "hbm", "achieved": gbs / world, "peak": peaks["hbm"], "unit": "GB/s",
-                         "frac": gbs / world / peaks["hbm"], "traffic": None,
-                         "kernel": "write_chunk_kernel", "peak_source": peaks["src"]},
-            "tokens_per_s": whole_job_rate(w.seq_len, world, ms),
-            "gpu_launches": args.steps, "clocks": clk.summary(),
-            **({"cpu_baseline": cpu} if cpu else {})}))
 
 
 class PrefillAttnWorkload:
@@ -610,10 +898,7 @@ def run_prefill_attn(args, world, rank, dev):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": f"f16 mma / f32 accumulate ({w.bits}-bit packed cache)",
             "data": "synthetic",
-            "config": {"workload": f"{w.name}: chunk of {w.chunk} queries at positions {w.seq_len - w.chunk}.."
-                                   f"{w.seq_len - 1} of a {w.seq_len}-token cache, Hkv{w.num_kv_heads} "
-                                   f"Hq{w.num_q_heads} d{w.d} m{w.block} {w.scale} scales, {w.bits}-bit codes, contiguous "
-                                   f"P{w.page_size}, causal", "l2": "cache 3.4 MB per kv head"},
+            "config": workload_config(w, None, world),
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                          "frac": tflops / peak, "traffic": None,
                          "kernel": "kvq3_prefill_attn (" + ("prefill_tile_kernel" if tile else
@@ -634,9 +919,10 @@ def workload_desc(w: I.Workload) -> str:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.workloads()))
+    ap.add_argument("--workload", default="", choices=[""] + sorted(I.workloads()),
+                    help="one workload only (default: all, ragged first)")
     ap.add_argument("--impl", default="kvq3", choices=["kvq3", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0, help="override the batch (smaller profiling cases)")
@@ -646,10 +932,14 @@ def main():
                     help="code width of the cache (0: the workload's own, 3)")
     ap.add_argument("--scale", default="", choices=["", "f32", "f16", "e4m3", "e4m3zp"],
                     help="scale format (e4m3zp: the asymmetric variant, E4M3 scale and zero point)")
+    ap.add_argument("--oracle-leg", default="", help=argparse.SUPPRESS)
     args = ap.parse_args()
     global BITS_OVERRIDE, SCALE_OVERRIDE
     BITS_OVERRIDE = args.bits
     SCALE_OVERRIDE = args.scale
+    if args.oracle_leg:
+        oracle_leg(args.oracle_leg)
+        return
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
@@ -659,122 +949,10 @@ def main():
     import torch
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = workload(args.workload)
-    if w.chunk > 0:
+    if args.workload and workload(args.workload).chunk > 0:
         run_prefill_attn(args, world, rank, dev)
-        return
-    if not w.decode:
-        run_prefill(args, world, rank, dev)
-        return
-    st = GpuWorkload(args.workload, dev, rank, args.batch)
-    w = st.w
-    stream = torch.cuda.current_stream()
-    clk = ClockSampler(local)
-    if not args.profile:
-        clk.__enter__()
-    for _ in range(args.warmup):
-        st.step()
-    torch.cuda.synchronize()
-    assert int(st.status.item()) == 0, f"device status {int(st.status.item())}"
-    if args.profile:
-        # plain steps only (kernel order per step: write, decode split, decode combine)
-        for _ in range(args.steps):
-            st.step()
-        torch.cuda.synchronize()
-        print(json.dumps({"profile": w.name, "batch": w.batch, "status": int(st.status.item())}))
-        return
-
-    # ---- device-timed steps (inputs resident; cache > L2 so every step streams it from HBM)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    barrier(world)
-    torch.cuda.synchronize()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for i in range(args.steps):
-        ev[i][0].record(stream)
-        st.write(st.k_new, st.v_new, st.seq_new, st.pos_new)
-        ev[i][1].record(stream)
-        st.decode()
-        ev[i][2].record(stream)
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    total_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
-    ms_step = total_ms / args.steps
-    dec_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
-    wr_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
-
-    # ---- end to end through host buffers (pinned), copies inside the timed region:
-    # the step's inputs (new k, v, the queries, positions, sequence ids) sit in
-    # one pinned host buffer and go over in one copy; the output comes back
-    srcs = (st.k_new, st.v_new, st.q, st.pos_new, st.seq_new)
-    offs, total = [], 0
-    for t in srcs:
-        offs.append(total)
-        total += (t.numel() * t.element_size() + 255) // 256 * 256
-    inp_h = torch.empty(total, dtype=torch.uint8).pin_memory()
-    inp_d = torch.empty(total, dtype=torch.uint8, device=dev)
-    views_d = []
-    for t, o in zip(srcs, offs):
-        nb = t.numel() * t.element_size()
-        inp_h[o:o + nb].copy_(t.cpu().contiguous().view(-1).view(torch.uint8))
-        views_d.append(inp_d[o:o + nb].view(t.dtype).view(t.shape))
-    k_d, v_d, q_d, pos_d, seq_d = views_d
-    out_h = torch.empty(st.out.shape, dtype=torch.float32).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in srcs)
-    d2h = out_h.numel() * out_h.element_size()
-
-    def e2e_step():
-        inp_d.copy_(inp_h, non_blocking=True)
-        st.write(k_d, v_d, seq_d, pos_d)
-        st.decode(q_d, st.out)
-        out_h.copy_(st.out, non_blocking=True)
-
-    for _ in range(args.warmup):
-        e2e_step()
-    torch.cuda.synchronize()
-    barrier(world)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    b.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(a.elapsed_time(b), world) / args.steps
-    clk.__exit__(None, None, None)
-    assert int(st.status.item()) == 0
-
-    ab = algorithmic_bytes(w, st.lens)
-    peaks = load_peaks()
-    dec_gbs = ab["decode"] / (dec_ms * 1e-3) / 1e9
-    if rank == 0:
-        cpu = None
-        if not args.no_cpu_baseline and world == 1:
-            cpu = cpu_baseline(w, st.lens)
-        line = {
-            "metric": "decode tokens/s (one layer, all heads)", "value": whole_job_rate(w.batch, world, ms_step),
-            "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": f"f16 mma / f32 accumulate ({w.bits}-bit packed cache)", "data": "synthetic",
-            "config": {"workload": workload_desc(w), "l2": "inputs larger than L2 (packed cache "
-                       f"{ab['decode'] / 1e6:.0f} MB per step)", "parallelism": f"replicas x{world} (dp over sequences)"},
-            "decode": {"ms": dec_ms, "hbm_gbs": dec_gbs, "frac_of_peak": dec_gbs / peaks["hbm"],
-                       "bytes": ab["decode"]},
-            "write": {"ms": wr_ms, "gbs": ab["write"] / (wr_ms * 1e-3) / 1e9, "bytes": ab["write"]},
-            "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": peaks["hbm"], "unit": "GB/s",
-                         "frac": dec_gbs / peaks["hbm"], "traffic": recorded_traffic(args.workload, w.bits),
-                         "kernel": "kvq3_decode_attn (decode_split_kernel + decode_combine_kernel)",
-                         "peak_source": peaks["src"]},
-            "e2e": {"value": whole_job_rate(w.batch, world, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
-            "gpu_launches": 3 * args.steps,
-            "clocks": clk.summary(),
-        }
-        if cpu is not None:
-            line["cpu_baseline"] = cpu
-        print(json.dumps(line))
+    else:
+        run_suite(args, world, rank, dev)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
