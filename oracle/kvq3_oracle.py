@@ -129,6 +129,20 @@ def rotation_params(d: int, seed: int, use_sign: bool = True, use_so4: bool = Tr
     return signs, quats
 
 
+def rotation_params_pair(d: int, seed: int, use_sign: bool = True):
+    """(signs, quats, quats_r) of the two-quaternion rotation: the draws of
+    :func:`rotation_params` (signs, then the left quaternion p_i of every
+    block), followed by one more point of S^3 per block, the right quaternion
+    q_i of R_i = L(p_i) R(conj q_i)."""
+    rng = SplitMix64(seed)
+    signs = np.array([-1 if (rng.next() >> 63) else 1 for _ in range(d)], dtype=np.int8)
+    quats = np.array([marsaglia_s3(rng) for _ in range(d // 4)], dtype=np.float64).reshape(d // 4, 4)
+    quats_r = np.array([marsaglia_s3(rng) for _ in range(d // 4)], dtype=np.float64).reshape(d // 4, 4)
+    if not use_sign:
+        signs[:] = 1
+    return signs, quats, quats_r
+
+
 # ---------------------------------------------------------------------------
 # The orthogonal transform U = B . H_d . D
 # ---------------------------------------------------------------------------
@@ -169,19 +183,44 @@ def quat_left_matrix(p) -> np.ndarray:
                      [e, -c, b, a]], dtype=np.float64)
 
 
-def block_so4_matrix(quats: np.ndarray) -> np.ndarray:
-    """B = diag(R_1, ..., R_{d/4}), R_i acting on coordinates 4i..4i+3."""
+def quat_right_matrix(q) -> np.ndarray:
+    """Matrix of x -> x (x) q (Hamilton product with q on the right) for
+    q = (a, b, c, e).  Orthogonal with det |q|^4."""
+    a, b, c, e = (float(t) for t in q)
+    return np.array([[a, -b, -c, -e],
+                     [b, a, e, -c],
+                     [c, -e, a, b],
+                     [e, c, -b, a]], dtype=np.float64)
+
+
+def quat_conj(q) -> np.ndarray:
+    a, b, c, e = (float(t) for t in q)
+    return np.array([a, -b, -c, -e], dtype=np.float64)
+
+
+def so4_pair_matrix(p, q) -> np.ndarray:
+    """The general element of SO(4) as a pair of unit quaternions:
+    x -> p (x) x (x) conj(q), i.e. L(p) R(conj q) (every rotation of R^4 has
+    this form, and (p, q) and (-p, -q) give the same one).  The block form
+    R_i in SO(4) of [OMC] Mathematical statement; q = 1 gives L(p)."""
+    return quat_left_matrix(p) @ quat_right_matrix(quat_conj(q))
+
+
+def block_so4_matrix(quats: np.ndarray, quats_r=None) -> np.ndarray:
+    """B = diag(R_1, ..., R_{d/4}), R_i acting on coordinates 4i..4i+3:
+    R_i = L(p_i), or L(p_i) R(conj q_i) when right quaternions are given."""
     n = len(quats)
     B = np.zeros((4 * n, 4 * n))
     for i, p in enumerate(quats):
-        B[4 * i:4 * i + 4, 4 * i:4 * i + 4] = quat_left_matrix(p)
+        R = quat_left_matrix(p) if quats_r is None else so4_pair_matrix(p, quats_r[i])
+        B[4 * i:4 * i + 4, 4 * i:4 * i + 4] = R
     return B
 
 
-def rotation_matrix(signs: np.ndarray, quats: np.ndarray) -> np.ndarray:
+def rotation_matrix(signs: np.ndarray, quats: np.ndarray, quats_r=None) -> np.ndarray:
     """Dense U = B . H_d . D ([OMC] U = B H_d; [OIQ] 3.2 puts D before H)."""
     d = len(signs)
-    return block_so4_matrix(quats) @ hadamard_matrix(d) @ np.diag(signs.astype(np.float64))
+    return block_so4_matrix(quats, quats_r) @ hadamard_matrix(d) @ np.diag(signs.astype(np.float64))
 
 
 # ---------------------------------------------------------------------------
@@ -365,15 +404,17 @@ def quantize_asym(x: np.ndarray, block: int, eps: float, bits: int = 3):
 
 
 def calib_sse(x: np.ndarray, signs: np.ndarray, quats: np.ndarray, block: int, kind: str,
-              bits: int = 3, eps: float = 1e-6) -> np.ndarray:
+              bits: int = 3, eps: float = 1e-6, quats_r=None) -> np.ndarray:
     """Objective of the SO(4) calibration ([OMC] Implementation notes:
     reconstruction MSE after quantisation, SO(4) blocks as normalised
     quaternions): per quantisation block j, the sum over the sample vectors
     x (fp64 [n][d]) and the coordinates of block j of (y - y_hat)^2, with
     y = B H D x for these signs and quaternions (SO(4) blocks applied) and
     y_hat its quantised value (symmetric codes, or the asymmetric variant for
-    kind "e4m3zp").  Returns fp64 [d/block]."""
-    U = rotation_matrix(np.asarray(signs), np.asarray(quats, dtype=np.float64))
+    kind "e4m3zp").  With quats_r, the blocks are the two-quaternion
+    R_i = L(p_i) R(conj q_i).  Returns fp64 [d/block]."""
+    U = rotation_matrix(np.asarray(signs), np.asarray(quats, dtype=np.float64),
+                        None if quats_r is None else np.asarray(quats_r, dtype=np.float64))
     y = np.asarray(x, dtype=np.float64) @ U.T
     n, d = y.shape
     eps = float(np.float32(eps))

@@ -71,3 +71,34 @@ def test_sse_identity_quaternions_is_hadamard_error(oracle):
     c, sq, _ = oracle.quantize(y, 64, float(np.float32(1e-6)), "f16")
     want = ((y - (c.reshape(-1, 2, 64) * sq[..., None]).reshape(y.shape)) ** 2).reshape(-1, 2, 64).sum(axis=(0, 2))
     assert np.allclose(oracle.calib_sse(x, signs, ident, 64, "f16"), want, rtol=1e-12)
+
+
+def test_sse_pair_equals_cache_round_trip_error(oracle):
+    # the two-quaternion blocks R_i = L(p_i) R(conj q_i): the objective still
+    # equals the error of the oracle's write -> packed bytes -> read-back -> U^T
+    x = _sample()
+    signs, quats, quats_r = oracle.rotation_params_pair(128, 42)
+    U = oracle.rotation_matrix(signs, quats, quats_r)
+    sse = oracle.calib_sse(x.astype(np.float64), signs, quats, 64, "f16", 3, quats_r=quats_r)
+    n = x.shape[0]
+    L = oracle.Layout(128, 1, 64, "f16", 16, 1, n // 16, n // 16, 3)
+    pool = np.zeros(L.pool_bytes, np.uint8)
+    oracle.write(pool, L, U, x[:, None], x[:, None], np.zeros(n, np.int32), np.arange(n))
+    yh = oracle.read_rotated(pool, L, 0, 0, 0, 0, n)[0]
+    err = float(((x.astype(np.float64) - yh @ U) ** 2).sum())
+    assert abs(sse.sum() - err) <= 1e-9 * err
+    # identity right quaternions give the one-quaternion objective exactly
+    ident = np.tile([1.0, 0.0, 0.0, 0.0], (32, 1))
+    assert np.array_equal(oracle.calib_sse(x.astype(np.float64), signs, quats, 64, "f16", 3, quats_r=ident),
+                          oracle.calib_sse(x.astype(np.float64), signs, quats, 64, "f16", 3))
+
+
+def test_sse_pair_separates_over_quantisation_blocks(oracle):
+    # moving the right quaternions inside quantisation block 0 changes sse[0] only
+    x = _sample().astype(np.float64)
+    signs, quats, quats_r = oracle.rotation_params_pair(128, 42)
+    base = oracle.calib_sse(x, signs, quats, 64, "f16", quats_r=quats_r)
+    r2 = quats_r.copy()
+    r2[0:16] = np.roll(r2[0:16], 1, axis=1)
+    moved = oracle.calib_sse(x, signs, quats, 64, "f16", quats_r=r2)
+    assert moved[1] == base[1] and moved[0] != base[0]

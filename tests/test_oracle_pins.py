@@ -90,6 +90,77 @@ def test_so4_blocks_gram_and_det(oracle):
     assert abs(np.linalg.det(R) - n2 ** 2) < 1e-9 * n2 ** 2
 
 
+def test_right_multiplication_follows_hamilton_rules(oracle):
+    # x -> x (x) u, basis products by Hamilton's rules: i j = k, j i = -k,
+    # i k = -j, k j = -i; right multiplications compose in reverse order:
+    # (x u) v = x (u v), so R(v) R(u) = R(u v)
+    R, L = oracle.quat_right_matrix, oracle.quat_left_matrix
+    e = np.eye(4)
+    one, i, j, k = (1, 0, 0, 0), (0, 1, 0, 0), (0, 0, 1, 0), (0, 0, 0, 1)
+    assert np.array_equal(R(one), e)
+    assert np.array_equal(R(j) @ e[1], e[3])        # i j = k
+    assert np.array_equal(R(i) @ e[2], -e[3])       # j i = -k
+    assert np.array_equal(R(k) @ e[1], -e[2])       # i k = -j
+    assert np.array_equal(R(j) @ e[3], -e[1])       # k j = -i
+    assert np.array_equal(R(j) @ R(i), R(k))        # (x i) j = x (i j) = x k
+    for u in (i, j, k):
+        assert np.array_equal(R(u) @ R(u), -e)       # x u u = -x
+
+
+def test_so4_pair_blocks(oracle):
+    # The general rotation of R^4 as x -> p x conj(q) (Orthogonally mixed
+    # 3-bit KV cache, Mathematical statement: R_i in SO(4)):
+    rng = np.random.default_rng(11)
+    L, R = oracle.quat_left_matrix, oracle.quat_right_matrix
+    for _ in range(20):
+        p = rng.standard_normal(4)
+        q = rng.standard_normal(4)
+        p /= np.linalg.norm(p)
+        q /= np.linalg.norm(q)
+        M = oracle.so4_pair_matrix(p, q)
+        # orthogonal, det 1
+        assert np.abs(M.T @ M - np.eye(4)).max() < 1e-15
+        assert abs(np.linalg.det(M) - 1.0) < 1e-14
+        # left and right multiplications commute (associativity of the product)
+        assert np.abs(L(p) @ R(q) - R(q) @ L(p)).max() < 1e-15
+        # (p, q) and (-p, -q) are the same rotation (the double cover)
+        assert np.abs(oracle.so4_pair_matrix(-p, -q) - M).max() < 1e-15
+        # q = 1 is the one-quaternion block L(p)
+        assert np.array_equal(oracle.so4_pair_matrix(p, (1.0, 0, 0, 0)), L(p))
+    # a simple rotation by theta in the (e0, e1) plane that fixes e2 and e3:
+    # p = (cos t/2, sin t/2, 0, 0), q = conj(p).  No single left
+    # multiplication gives it (p' x = x forces p' = 1), so the pair form
+    # reaches rotations the one-quaternion blocks cannot.
+    t = 0.7
+    p = np.array([np.cos(t / 2), np.sin(t / 2), 0.0, 0.0])
+    q = np.array([np.cos(t / 2), -np.sin(t / 2), 0.0, 0.0])
+    want = np.eye(4)
+    want[:2, :2] = [[np.cos(t), -np.sin(t)], [np.sin(t), np.cos(t)]]
+    assert np.abs(oracle.so4_pair_matrix(p, q) - want).max() < 1e-15
+
+
+def test_rotation_params_pair(oracle):
+    # the pair rotation keeps the one-quaternion draws (signs, then the left
+    # quaternions) and draws one more point of S^3 per block afterwards
+    s, q = oracle.rotation_params(128, 42)
+    s2, p2, r2 = oracle.rotation_params_pair(128, 42)
+    assert np.array_equal(s, s2) and np.array_equal(q, p2)
+    assert r2.shape == (32, 4) and np.abs(np.linalg.norm(r2, axis=1) - 1).max() < 1e-15
+    rng = oracle.SplitMix64(42)
+    for _ in range(128):
+        rng.next()
+    for _ in range(32):
+        oracle.marsaglia_s3(rng)
+    assert np.array_equal(np.array(oracle.marsaglia_s3(rng)), r2[0])
+    U = oracle.rotation_matrix(s2, p2, r2)
+    assert np.abs(U.T @ U - np.eye(128)).max() < 1e-14
+    # block i of U is R_i = L(p_i) R(conj q_i) applied after H D
+    HD = oracle.hadamard_matrix(128) @ np.diag(s2.astype(np.float64))
+    B = U @ HD.T
+    assert np.abs(B[4:8, 4:8] - oracle.so4_pair_matrix(p2[1], r2[1])).max() < 1e-14
+    assert np.abs(B[4:8, 8:12]).max() < 1e-14
+
+
 def test_rotation_params_shape_and_flags(oracle):
     s, q = oracle.rotation_params(128, 42)
     assert s.shape == (128,) and set(np.unique(s)) == {-1, 1}
