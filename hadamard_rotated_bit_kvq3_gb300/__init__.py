@@ -14,7 +14,9 @@ import os
 __all__ = [
     "KVQ3_OK", "KVQ3_ROT_SIGN", "KVQ3_ROT_SO4", "SCALE_TYPES", "CacheDesc", "Cache", "Kvq3Error",
     "lib", "kvq3_abi_version", "kvq3_status_string", "kvq3_rotation_create",
-    "kvq3_rotation_create_from_params", "kvq3_rotation_destroy", "kvq3_rotation_export",
+    "kvq3_rotation_create_from_params", "kvq3_rotation_create_from_params_pair", "kvq3_rotation_destroy",
+    "kvq3_rotation_export", "kvq3_rotation_export_pair", "KVQ3_ROT_SO4_PAIR", "kvq3_calib_sse_pair",
+    "kvq3_calibrate_so4_pair",
     "kvq3_cache_sizes", "kvq3_rotate", "kvq3_write", "kvq3_write_chunk", "kvq3_decode_workspace_size",
     "kvq3_decode_attn", "kvq3_decode_attn_noalloc", "kvq3_prefill_workspace_size", "kvq3_prefill_attn",
     "kvq3_dequant_debug", "kvq3_calib_sse", "kvq3_calibrate_workspace_size", "kvq3_calibrate_so4", "Rotation",
@@ -26,6 +28,7 @@ LIB_PATH = os.path.join(_HERE, "libkvq3.so")
 KVQ3_OK = 0
 KVQ3_ROT_SIGN = 1
 KVQ3_ROT_SO4 = 2
+KVQ3_ROT_SO4_PAIR = 4
 SCALE_TYPES = {"f32": 0, "f16": 1, "e4m3": 2, "e4m3zp": 3}
 DEV_BITS = {"bad_seq": 1, "bad_pos": 2, "bad_page": 4, "bad_len": 8, "bad_code": 16, "timeout": 32}
 
@@ -61,8 +64,10 @@ _SIGS = {
     "kvq3_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "kvq3_rotation_create": (ctypes.c_int, [_i32, _u64, _u32, ctypes.POINTER(_p)]),
     "kvq3_rotation_create_from_params": (ctypes.c_int, [_i32, _p, _p, ctypes.POINTER(_p)]),
+    "kvq3_rotation_create_from_params_pair": (ctypes.c_int, [_i32, _p, _p, _p, ctypes.POINTER(_p)]),
     "kvq3_rotation_destroy": (ctypes.c_int, [_p]),
     "kvq3_rotation_export": (ctypes.c_int, [_p, _p, _p, _p]),
+    "kvq3_rotation_export_pair": (ctypes.c_int, [_p, _p, _p, _p, _p]),
     "kvq3_cache_sizes": (ctypes.c_int, [_D, ctypes.POINTER(_sz), ctypes.POINTER(_sz), ctypes.POINTER(_sz)]),
     "kvq3_rotate": (ctypes.c_int, [_p, _p, _i32, _p, _i64, _i32, _p]),
     "kvq3_write": (ctypes.c_int, [_p, _D, _C, _p, _p, _p, _p, _i64, _p, _p]),
@@ -74,6 +79,9 @@ _SIGS = {
     "kvq3_prefill_attn": (ctypes.c_int, [_p, _D, _C, _i32, _i64, _i64, _p, _i32, _f32, _p, _p, _sz, _p, _p]),
     "kvq3_dequant_debug": (ctypes.c_int, [_p, _D, _C, _i32, _i32, _i32, _i64, _i64, _p, _p, _p, _p]),
     "kvq3_calib_sse": (ctypes.c_int, [_p, _D, _p, _i32, _p, _i64, _p, _p]),
+    "kvq3_calib_sse_pair": (ctypes.c_int, [_p, _D, _p, _p, _i32, _p, _i64, _p, _p]),
+    "kvq3_calibrate_so4_pair": (ctypes.c_int, [_p, _D, _p, _i64, _i32, _i32, _f32, _u64, _p, _sz, _p, _p, _p,
+                                               _p]),
     "kvq3_calibrate_workspace_size": (ctypes.c_int, [_D, _i32, ctypes.POINTER(_sz)]),
     "kvq3_calibrate_so4": (ctypes.c_int, [_p, _D, _p, _i64, _i32, _i32, _f32, _u64, _p, _sz, _p, _p, _p]),
 }
@@ -135,6 +143,19 @@ def kvq3_rotation_create_from_params(d: int, signs, quats):
     return h
 
 
+def kvq3_rotation_create_from_params_pair(d: int, signs, quats, quats_r):
+    """Two-quaternion blocks: signs int8 [d]; quats, quats_r float32 [d/4][4] (numpy)."""
+    import numpy as np
+    s = np.ascontiguousarray(signs, dtype=np.int8)
+    q = np.ascontiguousarray(quats, dtype=np.float32)
+    r = np.ascontiguousarray(quats_r, dtype=np.float32)
+    h = ctypes.c_void_p()
+    _check(lib.kvq3_rotation_create_from_params_pair(d, s.ctypes.data_as(_p), q.ctypes.data_as(_p),
+                                                     r.ctypes.data_as(_p), ctypes.byref(h)),
+           "kvq3_rotation_create_from_params_pair")
+    return h
+
+
 def kvq3_rotation_destroy(h) -> None:
     _check(lib.kvq3_rotation_destroy(h), "kvq3_rotation_destroy")
 
@@ -149,6 +170,19 @@ def kvq3_rotation_export(h):
     _check(lib.kvq3_rotation_export(h, s.ctypes.data_as(_p), q.ctypes.data_as(_p), None),
            "kvq3_rotation_export")
     return s, q
+
+
+def kvq3_rotation_export_pair(h):
+    """(signs int8 [d], quats float32 [d/4][4], quats_r float32 [d/4][4])."""
+    import numpy as np
+    d = ctypes.c_int32()
+    _check(lib.kvq3_rotation_export_pair(h, None, None, None, ctypes.byref(d)), "kvq3_rotation_export_pair")
+    s = np.zeros(d.value, np.int8)
+    q = np.zeros((d.value // 4, 4), np.float32)
+    r = np.zeros((d.value // 4, 4), np.float32)
+    _check(lib.kvq3_rotation_export_pair(h, s.ctypes.data_as(_p), q.ctypes.data_as(_p), r.ctypes.data_as(_p),
+                                         None), "kvq3_rotation_export_pair")
+    return s, q, r
 
 
 def kvq3_cache_sizes(desc: CacheDesc):
@@ -233,6 +267,13 @@ def kvq3_calib_sse(h, desc: CacheDesc, quats, x, sse, stream=None) -> None:
                               int(x.shape[0]), _ptr(sse), _stream(stream)), "kvq3_calib_sse")
 
 
+def kvq3_calib_sse_pair(h, desc: CacheDesc, quats, quats_r, x, sse, stream=None) -> None:
+    """quats, quats_r: fp32 CUDA [P][d/4][4] candidate two-quaternion blocks;
+    x: fp16 CUDA [n][d]; sse: fp64 CUDA [P][d/m] (overwritten)."""
+    _check(lib.kvq3_calib_sse_pair(h, ctypes.byref(desc), _ptr(quats), _ptr(quats_r), int(quats.shape[0]),
+                                   _ptr(x), int(x.shape[0]), _ptr(sse), _stream(stream)), "kvq3_calib_sse_pair")
+
+
 def kvq3_calibrate_workspace_size(desc: CacheDesc, num_candidates: int) -> int:
     n = _sz()
     _check(lib.kvq3_calibrate_workspace_size(ctypes.byref(desc), num_candidates, ctypes.byref(n)),
@@ -254,6 +295,23 @@ def kvq3_calibrate_so4(h, desc: CacheDesc, x, rounds: int, num_candidates: int, 
                                   workspace.numel() * workspace.element_size(), q.ctypes.data_as(_p),
                                   e.ctypes.data_as(_p), _stream(stream)), "kvq3_calibrate_so4")
     return q, e
+
+
+def kvq3_calibrate_so4_pair(h, desc: CacheDesc, x, rounds: int, num_candidates: int, step: float, seed: int,
+                            workspace, stream=None):
+    """Returns (quats, quats_r float32 [d/4][4], sse float64 [d/m]) as numpy
+    arrays: the search over two-quaternion blocks.  Synchronises the stream."""
+    import numpy as np
+    d = desc.head_dim
+    q = np.zeros((d // 4, 4), np.float32)
+    r = np.zeros((d // 4, 4), np.float32)
+    e = np.zeros(d // desc.block, np.float64)
+    _check(lib.kvq3_calibrate_so4_pair(h, ctypes.byref(desc), _ptr(x), int(x.shape[0]), rounds, num_candidates,
+                                       float(step), seed & ((1 << 64) - 1), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), q.ctypes.data_as(_p),
+                                       r.ctypes.data_as(_p), e.ctypes.data_as(_p), _stream(stream)),
+           "kvq3_calibrate_so4_pair")
+    return q, r, e
 
 
 def kvq3_dequant_debug(h, desc: CacheDesc, cache: Cache, seq: int, kv_head: int, which: int,

@@ -17,12 +17,14 @@ namespace kvq3 {
 constexpr int kMaxD = 256;
 constexpr unsigned kFull = 0xffffffffu;
 
-// Rotation parameters as kernels receive them (by value, ~1 KB of kernel
-// parameter space): sign bit j set <=> sigma_j = -1; quaternion i acts on
-// rotated coordinates 4i..4i+3 (reading R3).
+// Rotation parameters as kernels receive them (by value, ~2 KB of kernel
+// parameter space): sign bit j set <=> sigma_j = -1; block i acts on rotated
+// coordinates 4i..4i+3 as x -> p_i x (reading R3), or as x -> p_i x conj(q_i)
+// with KVQ3_ROT_SO4_PAIR (reading R20; q_i = 1 otherwise).
 struct RotParams {
   uint32_t sign_bits[kMaxD / 32];
-  float4 quat[kMaxD / 4];
+  float4 quat[kMaxD / 4];     // p_i
+  float4 quat_r[kMaxD / 4];   // q_i
   int32_t d;
   uint32_t flags;
 };
@@ -85,12 +87,30 @@ __device__ __forceinline__ void quat_apply_t(const float4 p, float& x0, float& x
   quat_apply(make_float4(p.x, -p.y, -p.z, -p.w), x0, x1, x2, x3);
 }
 
+// y = x * q: the quaternion product with q on the right (reading R20).
+__device__ __forceinline__ void quat_apply_right(const float4 q, float& x0, float& x1, float& x2,
+                                                 float& x3) {
+  const float y0 = x0 * q.x - x1 * q.y - x2 * q.z - x3 * q.w;
+  const float y1 = x0 * q.y + x1 * q.x + x2 * q.w - x3 * q.z;
+  const float y2 = x0 * q.z - x1 * q.w + x2 * q.x + x3 * q.y;
+  const float y3 = x0 * q.w + x1 * q.z - x2 * q.y + x3 * q.x;
+  x0 = y0; x1 = y1; x2 = y2; x3 = y3;
+}
+
+// y = x * conj(q) (the right half of a two-quaternion block; its inverse is
+// quat_apply_right with q).
+__device__ __forceinline__ void quat_apply_right_conj(const float4 q, float& x0, float& x1,
+                                                      float& x2, float& x3) {
+  quat_apply_right(make_float4(q.x, -q.y, -q.z, -q.w), x0, x1, x2, x3);
+}
+
 // Forward U = B H D on the E elements this lane holds (dims r*E .. r*E+E-1).
-// sgn: E sign bits of this lane; q: the E/4 quaternions of this lane.
+// sgn: E sign bits of this lane; q, qr: the E/4 left and right quaternions of
+// this lane; pair: two-quaternion blocks (reading R20).
 template <int E, int L>
 __device__ __forceinline__ void rotate_forward(float (&x)[E], int r, uint32_t sgn,
-                                               const float4 (&q)[E / 4], float inv_sqrt_d,
-                                               bool so4) {
+                                               const float4 (&q)[E / 4], const float4 (&qr)[E / 4],
+                                               float inv_sqrt_d, bool so4, bool pair) {
 #pragma unroll
   for (int e = 0; e < E; ++e)
     if ((sgn >> e) & 1u) x[e] = -x[e];
@@ -99,18 +119,24 @@ __device__ __forceinline__ void rotate_forward(float (&x)[E], int r, uint32_t sg
   for (int e = 0; e < E; ++e) x[e] *= inv_sqrt_d;
   if (so4) {
 #pragma unroll
-    for (int i = 0; i < E / 4; ++i) quat_apply(q[i], x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+    for (int i = 0; i < E / 4; ++i) {
+      quat_apply(q[i], x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+      if (pair) quat_apply_right_conj(qr[i], x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+    }
   }
 }
 
 // Inverse U^T = D H B^T.
 template <int E, int L>
 __device__ __forceinline__ void rotate_inverse(float (&x)[E], int r, uint32_t sgn,
-                                               const float4 (&q)[E / 4], float inv_sqrt_d,
-                                               bool so4) {
+                                               const float4 (&q)[E / 4], const float4 (&qr)[E / 4],
+                                               float inv_sqrt_d, bool so4, bool pair) {
   if (so4) {
 #pragma unroll
-    for (int i = 0; i < E / 4; ++i) quat_apply_t(q[i], x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+    for (int i = 0; i < E / 4; ++i) {
+      if (pair) quat_apply_right(qr[i], x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+      quat_apply_t(q[i], x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+    }
   }
   fwht_group<E, L>(x, r);
 #pragma unroll
@@ -132,6 +158,18 @@ template <int E>
 __device__ __forceinline__ void lane_quats(const RotParams& rp, int r, float4 (&q)[E / 4]) {
 #pragma unroll
   for (int i = 0; i < E / 4; ++i) q[i] = rp.quat[r * (E / 4) + i];
+}
+
+template <int E>
+__device__ __forceinline__ void lane_quats_r(const RotParams& rp, int r, float4 (&q)[E / 4]) {
+#pragma unroll
+  for (int i = 0; i < E / 4; ++i) q[i] = rp.quat_r[r * (E / 4) + i];
+}
+
+// Flags of a rotation as the kernels test them.
+__device__ __forceinline__ bool rot_so4(const RotParams& rp) { return (rp.flags & KVQ3_ROT_SO4) != 0; }
+__device__ __forceinline__ bool rot_pair(const RotParams& rp) {
+  return (rp.flags & (KVQ3_ROT_SO4 | KVQ3_ROT_SO4_PAIR)) == (KVQ3_ROT_SO4 | KVQ3_ROT_SO4_PAIR);
 }
 
 // ---------------------------------------------------------------- scales

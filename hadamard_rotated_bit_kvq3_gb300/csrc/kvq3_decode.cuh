@@ -648,9 +648,6 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
   // per-lane query rotation parameters (dims rq*EQ ..)
   const int rq = lane % LQ, gq = lane / LQ;
   const uint32_t sgn_q = lane_signs<EQ>(rp, rq);
-  float4 quat_q[EQ / 4];
-  lane_quats<EQ>(rp, rq, quat_q);
-  const bool so4 = (rp.flags & KVQ3_ROT_SO4) != 0;
 
   // lane-constant offsets from a page's K record: this lane's key chunk
   // (token r, fields j*FQ.. of each block), value chunk (token 2j, fields
@@ -839,7 +836,14 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
       const __half* src = p.q + (valid ? qrow : 0) * D + rq * EQ;
 #pragma unroll
       for (int e = 0; e < EQ; ++e) x[e] = valid ? __half2float(src[e]) : 0.0f;
-      rotate_forward<EQ, LQ>(x, rq, sgn_q, quat_q, p.inv_sqrt_d, so4);
+      {
+        // this lane's quaternions, read from the parameter space here rather
+        // than held in registers across the kernel
+        float4 quat_q[EQ / 4], quat_r[EQ / 4];
+        lane_quats<EQ>(rp, rq, quat_q);
+        lane_quats_r<EQ>(rp, rq, quat_r);
+        rotate_forward<EQ, LQ>(x, rq, sgn_q, quat_q, quat_r, p.inv_sqrt_d, rot_so4(rp), rot_pair(rp));
+      }
       float amax = 0.0f;
 #pragma unroll
       for (int e = 0; e < EQ; ++e) {
@@ -1373,9 +1377,10 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const __grid_consta
   const int lane = threadIdx.x & 31;
   const int rr = lane % L, grp = lane / L;
   const uint32_t sgn = lane_signs<E>(rp, rr);
-  float4 qt[E / 4];
+  float4 qt[E / 4], qtr[E / 4];
   lane_quats<E>(rp, rr, qt);
-  const bool so4 = (rp.flags & KVQ3_ROT_SO4) != 0;
+  lane_quats_r<E>(rp, rr, qtr);
+  const bool so4 = rot_so4(rp), pair = rot_pair(rp);
   // launched as a programmatic dependent of the split kernel: everything above
   // overlaps its tail; its partials are complete and visible after this
   griddep_wait();
@@ -1428,7 +1433,7 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const __grid_consta
         for (int e = 0; e < E; ++e) o[e] *= inv;
       }
     }
-    rotate_inverse<E, L>(o, rr, sgn, qt, p.inv_sqrt_d, so4);
+    rotate_inverse<E, L>(o, rr, sgn, qt, qtr, p.inv_sqrt_d, so4, pair);
     if (grp == 0) {
 #pragma unroll
       for (int e = 0; e < E; ++e) out[(int64_t)it * D + rr * E + e] = o[e];

@@ -59,9 +59,24 @@ void fill_params(kvq3_rotation_s* r) {
   p.flags = r->flags;
   for (int j = 0; j < r->d; ++j)
     if (r->signs[j] < 0) p.sign_bits[j / 32] |= 1u << (j % 32);
-  for (int i = 0; i < r->d / 4; ++i)
+  for (int i = 0; i < r->d / 4; ++i) {
     p.quat[i] = make_float4((float)r->quats64[4 * i], (float)r->quats64[4 * i + 1],
                             (float)r->quats64[4 * i + 2], (float)r->quats64[4 * i + 3]);
+    p.quat_r[i] = make_float4((float)r->quats_r64[4 * i], (float)r->quats_r64[4 * i + 1],
+                              (float)r->quats_r64[4 * i + 2], (float)r->quats_r64[4 * i + 3]);
+  }
+}
+
+// Normalises n quaternions into out (fp64); false for a zero or non-finite one.
+bool normalise_quats(const float* q, int n, double* out) {
+  for (int i = 0; i < n; ++i) {
+    double n2 = 0.0;
+    for (int c = 0; c < 4; ++c) n2 += (double)q[4 * i + c] * (double)q[4 * i + c];
+    if (!(n2 > 0.0) || !isfinite(n2)) return false;
+    const double inv = 1.0 / sqrt(n2);
+    for (int c = 0; c < 4; ++c) out[4 * i + c] = (double)q[4 * i + c] * inv;
+  }
+  return true;
 }
 
 }  // namespace
@@ -138,9 +153,10 @@ __global__ void __launch_bounds__(256) rotate_kernel(const __grid_constant__ Rot
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const uint32_t sgn = lane_signs<E>(rp, r);
-  float4 q[E / 4];
+  float4 q[E / 4], qr[E / 4];
   lane_quats<E>(rp, r, q);
-  const bool so4 = (rp.flags & KVQ3_ROT_SO4) != 0;
+  lane_quats_r<E>(rp, r, qr);
+  const bool so4 = rot_so4(rp), pair = rot_pair(rp);
   for (int64_t base = warp * GPW; base < n; base += nwarps * GPW) {
     const int64_t vi = base + grp;
     const bool ok = vi < n;
@@ -155,8 +171,8 @@ __global__ void __launch_bounds__(256) rotate_kernel(const __grid_constant__ Rot
       }
       v[e] = t;
     }
-    if (inverse) rotate_inverse<E, L>(v, r, sgn, q, inv_sqrt_d, so4);
-    else rotate_forward<E, L>(v, r, sgn, q, inv_sqrt_d, so4);
+    if (inverse) rotate_inverse<E, L>(v, r, sgn, q, qr, inv_sqrt_d, so4, pair);
+    else rotate_forward<E, L>(v, r, sgn, q, qr, inv_sqrt_d, so4, pair);
     if (ok) {
 #pragma unroll
       for (int e = 0; e < E; ++e) y[vi * D + r * E + e] = v[e];
@@ -197,8 +213,10 @@ const char* kvq3_status_string(kvq3_status s) {
 }
 
 kvq3_status kvq3_rotation_create(int32_t d, uint64_t seed, uint32_t flags, kvq3_rotation* out) {
-  if (!out || !pow2_in(d, 4, kMaxD) || (flags & ~(uint32_t)(KVQ3_ROT_SIGN | KVQ3_ROT_SO4)))
+  if (!out || !pow2_in(d, 4, kMaxD) ||
+      (flags & ~(uint32_t)(KVQ3_ROT_SIGN | KVQ3_ROT_SO4 | KVQ3_ROT_SO4_PAIR)))
     return KVQ3_ERR_INVALID_ARG;
+  if ((flags & KVQ3_ROT_SO4_PAIR) && !(flags & KVQ3_ROT_SO4)) return KVQ3_ERR_INVALID_ARG;
   kvq3_rotation_s* r = static_cast<kvq3_rotation_s*>(calloc(1, sizeof(kvq3_rotation_s)));
   if (!r) return KVQ3_ERR_INVALID_ARG;
   r->d = d;
@@ -213,6 +231,12 @@ kvq3_status kvq3_rotation_create(int32_t d, uint64_t seed, uint32_t flags, kvq3_
     marsaglia_s3(rng, p);
     for (int c = 0; c < 4; ++c)
       r->quats64[4 * i + c] = (flags & KVQ3_ROT_SO4) ? p[c] : (c == 0 ? 1.0 : 0.0);
+  }
+  // reading R20: the right quaternions are drawn after every left one
+  for (int i = 0; i < d / 4; ++i) {
+    double q[4] = {1.0, 0.0, 0.0, 0.0};
+    if (flags & KVQ3_ROT_SO4_PAIR) marsaglia_s3(rng, q);
+    for (int c = 0; c < 4; ++c) r->quats_r64[4 * i + c] = q[c];
   }
   fill_params(r);
   *out = r;
@@ -229,15 +253,29 @@ kvq3_status kvq3_rotation_create_from_params(int32_t d, const int8_t* signs, con
   r->d = d;
   r->flags = KVQ3_ROT_SIGN | KVQ3_ROT_SO4;
   for (int j = 0; j < d; ++j) r->signs[j] = signs[j];
-  for (int i = 0; i < d / 4; ++i) {
-    double n2 = 0.0;
-    for (int c = 0; c < 4; ++c) n2 += (double)quats[4 * i + c] * (double)quats[4 * i + c];
-    if (!(n2 > 0.0) || !isfinite(n2)) {
-      free(r);
-      return KVQ3_ERR_INVALID_ARG;
-    }
-    const double inv = 1.0 / sqrt(n2);
-    for (int c = 0; c < 4; ++c) r->quats64[4 * i + c] = (double)quats[4 * i + c] * inv;
+  if (!normalise_quats(quats, d / 4, r->quats64)) {
+    free(r);
+    return KVQ3_ERR_INVALID_ARG;
+  }
+  for (int i = 0; i < d / 4; ++i) r->quats_r64[4 * i] = 1.0;
+  fill_params(r);
+  *out = r;
+  return KVQ3_OK;
+}
+
+kvq3_status kvq3_rotation_create_from_params_pair(int32_t d, const int8_t* signs, const float* quats,
+                                                  const float* quats_r, kvq3_rotation* out) {
+  if (!out || !signs || !quats || !quats_r || !pow2_in(d, 4, kMaxD)) return KVQ3_ERR_INVALID_ARG;
+  for (int j = 0; j < d; ++j)
+    if (signs[j] != 1 && signs[j] != -1) return KVQ3_ERR_INVALID_ARG;
+  kvq3_rotation_s* r = static_cast<kvq3_rotation_s*>(calloc(1, sizeof(kvq3_rotation_s)));
+  if (!r) return KVQ3_ERR_INVALID_ARG;
+  r->d = d;
+  r->flags = KVQ3_ROT_SIGN | KVQ3_ROT_SO4 | KVQ3_ROT_SO4_PAIR;
+  for (int j = 0; j < d; ++j) r->signs[j] = signs[j];
+  if (!normalise_quats(quats, d / 4, r->quats64) || !normalise_quats(quats_r, d / 4, r->quats_r64)) {
+    free(r);
+    return KVQ3_ERR_INVALID_ARG;
   }
   fill_params(r);
   *out = r;
@@ -260,6 +298,20 @@ kvq3_status kvq3_rotation_export(kvq3_rotation rot, int8_t* signs, float* quats,
       quats[4 * i + 1] = rot->params.quat[i].y;
       quats[4 * i + 2] = rot->params.quat[i].z;
       quats[4 * i + 3] = rot->params.quat[i].w;
+    }
+  return KVQ3_OK;
+}
+
+kvq3_status kvq3_rotation_export_pair(kvq3_rotation rot, int8_t* signs, float* quats, float* quats_r,
+                                      int32_t* d_out) {
+  const kvq3_status s = kvq3_rotation_export(rot, signs, quats, d_out);
+  if (s != KVQ3_OK) return s;
+  if (quats_r)
+    for (int i = 0; i < rot->d / 4; ++i) {
+      quats_r[4 * i] = rot->params.quat_r[i].x;
+      quats_r[4 * i + 1] = rot->params.quat_r[i].y;
+      quats_r[4 * i + 2] = rot->params.quat_r[i].z;
+      quats_r[4 * i + 3] = rot->params.quat_r[i].w;
     }
   return KVQ3_OK;
 }

@@ -9,7 +9,8 @@ struct kvq3_rotation_s {
   int32_t d;
   uint32_t flags;
   int8_t signs[kvq3::kMaxD];      // as used (all +1 without KVQ3_ROT_SIGN)
-  double quats64[kvq3::kMaxD];    // [d/4][4], unit length (identity without KVQ3_ROT_SO4)
+  double quats64[kvq3::kMaxD];    // [d/4][4] p_i, unit length (identity without KVQ3_ROT_SO4)
+  double quats_r64[kvq3::kMaxD];  // [d/4][4] q_i, unit length (identity without KVQ3_ROT_SO4_PAIR)
   kvq3::RotParams params;         // what the kernels receive
 };
 
@@ -33,5 +34,28 @@ kvq3_status prefill_tiles(const CacheGeom& g, const kvq3_cache* cache, int32_t s
 inline kvq3_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVQ3_OK : KVQ3_ERR_CUDA; }
 
 inline float inv_sqrt(int d) { return (float)(1.0 / __builtin_sqrt((double)d)); }
+
+// Block i of B as a row-major 4x4 matrix in fp64: L(p_i), or L(p_i) R(conj q_i)
+// for two-quaternion blocks (readings R3, R20); the identity without SO(4).
+inline void so4_block_matrix(const kvq3_rotation_s* r, int i, double M[16]) {
+  const double* p = &r->quats64[4 * i];
+  const double* q = &r->quats_r64[4 * i];
+  const double a = p[0], b = p[1], c = p[2], e = p[3];
+  const double Lp[16] = {a, -b, -c, -e, b, a, -e, c, c, e, a, -b, e, -c, b, a};
+  // x -> x * conj(q): the right-multiplication matrix of conj(q)
+  const double w = q[0], x = -q[1], y = -q[2], z = -q[3];
+  const double Rq[16] = {w, -x, -y, -z, x, w, z, -y, y, -z, w, x, z, y, -x, w};
+  const bool pair = (r->flags & KVQ3_ROT_SO4_PAIR) != 0;
+  for (int row = 0; row < 4; ++row)
+    for (int col = 0; col < 4; ++col) {
+      double v = 0.0;
+      if (pair) {
+        for (int k = 0; k < 4; ++k) v += Lp[4 * row + k] * Rq[4 * k + col];
+      } else {
+        v = Lp[4 * row + col];
+      }
+      M[4 * row + col] = v;
+    }
+}
 
 }  // namespace kvq3

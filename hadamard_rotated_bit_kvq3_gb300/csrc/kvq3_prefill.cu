@@ -110,9 +110,10 @@ __global__ void __launch_bounds__(kThreadsP, 2) prefill_tile_kernel(const __grid
   // ---- q1 = U q of this CTA's rows into shared memory (warp per row)
   {
     const uint32_t sgn = lane_signs<4>(rp, lane);
-    float4 qt[1];
+    float4 qt[1], qtr[1];
     lane_quats<4>(rp, lane, qt);
-    const bool so4 = (rp.flags & KVQ3_ROT_SO4) != 0;
+    lane_quats_r<4>(rp, lane, qtr);
+    const bool so4 = rot_so4(rp), pair = rot_pair(rp);
     for (int row = wid; row < kRowsP; row += kWarpsP) {
       float x[4] = {0.0f, 0.0f, 0.0f, 0.0f};
       if (row < nrows) {
@@ -121,7 +122,7 @@ __global__ void __launch_bounds__(kThreadsP, 2) prefill_tile_kernel(const __grid
 #pragma unroll
         for (int e = 0; e < 4; ++e) x[e] = __half2float(src[e]);
       }
-      rotate_forward<4, 32>(x, lane, sgn, qt, p.inv_sqrt_d, so4);
+      rotate_forward<4, 32>(x, lane, sgn, qt, qtr, p.inv_sqrt_d, so4, pair);
       float amax = 0.0f;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -396,14 +397,15 @@ __global__ void __launch_bounds__(kThreadsP, 2) prefill_tile_kernel(const __grid
   __syncthreads();
   {
     const uint32_t sgn = lane_signs<4>(rp, lane);
-    float4 qt[1];
+    float4 qt[1], qtr[1];
     lane_quats<4>(rp, lane, qt);
-    const bool so4 = (rp.flags & KVQ3_ROT_SO4) != 0;
+    lane_quats_r<4>(rp, lane, qtr);
+    const bool so4 = rot_so4(rp), pair = rot_pair(rp);
     for (int row = wid; row < nrows; row += kWarpsP) {
       float x[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) x[e] = rows_s[row * kD + lane * 4 + e];
-      rotate_inverse<4, 32>(x, lane, sgn, qt, p.inv_sqrt_d, so4);
+      rotate_inverse<4, 32>(x, lane, sgn, qt, qtr, p.inv_sqrt_d, so4, pair);
       const int tok = t0 + row / p.G, h = kvh * p.G + row % p.G;
       float4* dst = reinterpret_cast<float4*>(p.out + ((int64_t)tok * p.Hq + h) * kD + lane * 4);
       *dst = make_float4(x[0], x[1], x[2], x[3]);

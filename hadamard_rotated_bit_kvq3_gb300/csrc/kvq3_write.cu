@@ -44,8 +44,10 @@ __global__ void __launch_bounds__(256) write_kernel(
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const uint32_t sgn = lane_signs<E>(rp, r);
   float4 q[E / 4];
+  float4 qr[E / 4];
   lane_quats<E>(rp, r, q);
-  const bool so4 = (rp.flags & KVQ3_ROT_SO4) != 0;
+  lane_quats_r<E>(rp, r, qr);
+  const bool so4 = rot_so4(rp), pair = rot_pair(rp);
   const int64_t per_which = n_tok * g.hkv;
   const int64_t total = 2 * per_which;
   const int64_t cap = (int64_t)g.max_pages * g.page_size;
@@ -114,7 +116,7 @@ __global__ void __launch_bounds__(256) write_kernel(
         rec = record_offset(g, page, head, which);
       }
     }
-    rotate_forward<E, L>(x, r, sgn, q, inv_sqrt_d, so4);
+    rotate_forward<E, L>(x, r, sgn, q, qr, inv_sqrt_d, so4, pair);
 
     // this lane's E elements lie in one block of LPB lanes
     uint32_t sbits, bits = 0;
@@ -229,8 +231,10 @@ __global__ void __launch_bounds__(256) dequant_kernel(
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const uint32_t sgn = lane_signs<E>(rp, r);
   float4 q[E / 4];
+  float4 qr[E / 4];
   lane_quats<E>(rp, r, q);
-  const bool so4 = (rp.flags & KVQ3_ROT_SO4) != 0;
+  lane_quats_r<E>(rp, r, qr);
+  const bool so4 = rot_so4(rp), pair = rot_pair(rp);
   const int64_t cap = (int64_t)g.max_pages * g.page_size;
   for (int64_t base = warp * GPW; base < nt; base += nwarps * GPW) {
     const int64_t t = base + grp;
@@ -283,7 +287,7 @@ __global__ void __launch_bounds__(256) dequant_kernel(
       }
       if (bad) set_status(status, bad);
     }
-    if (use_rot) rotate_inverse<E, L>(x, r, sgn, q, inv_sqrt_d, so4);
+    if (use_rot) rotate_inverse<E, L>(x, r, sgn, q, qr, inv_sqrt_d, so4, pair);
     if (ok) {
 #pragma unroll
       for (int e = 0; e < E; ++e) {

@@ -13,7 +13,8 @@
 //  * sign flip D as an XOR of fp16 sign bits with masks from the constant
 //    bank; the Walsh-Hadamard butterfly with packed f32x2 adds (element i
 //    and i + d/2 share a register pair, so every stage but the last is packed);
-//    SO(4) blocks with the quaternion pairs of blocks i and i + d/8 packed;
+//    SO(4) blocks as 4x4 matrices (one- or two-quaternion blocks alike),
+//    blocks i and i + d/8 packed;
 //  * 1/sqrt(d) is folded into the block maximum and the reciprocal scale;
 //  * codes by one fused multiply-add against the 1.5*2^23 rounding constant
 //    (round half to even), packed in-thread into 32-bit words (b-bit codes,
@@ -28,6 +29,7 @@ using namespace kvq3;
 namespace {
 
 constexpr int kTile = 128;  // vectors per CTA tile = threads per CTA
+constexpr int kChunkMaxD = 128;  // head dimensions this path serves: 64, 128
 
 struct ChunkParams {
   CacheGeom g;
@@ -42,7 +44,7 @@ struct ChunkParams {
   int64_t n_tiles;            // 2 * hkv * tiles_per_head
   float inv_sqrt_d;
   uint32_t sign_xor[kMaxD / 2];   // fp16-pair sign masks of the input order
-  float2 quat2[kMaxD / 8][4];     // quaternion coefficients of blocks (i, i + d/8)
+  float2 mat2[kChunkMaxD / 8][16];  // SO(4) block matrices of blocks (i, i + d/8), row-major
 };
 
 typedef unsigned long long u64;
@@ -182,18 +184,16 @@ __global__ void __launch_bounds__(kTile) write_chunk_kernel(const __grid_constan
       x2[i].x = a + b;
       x2[i].y = a - b;
     }
-    // ---- SO(4) blocks (coefficients carry 1/sqrt(d) when present)
+    // ---- SO(4) blocks (matrix entries carry 1/sqrt(d) when present)
     if constexpr (SO4) {
 #pragma unroll
       for (int i = 0; i < D / 8; ++i) {
-        const float2 a = p.quat2[i][0], b = p.quat2[i][1], c = p.quat2[i][2], e = p.quat2[i][3];
         const float2 x0 = x2[4 * i], x1 = x2[4 * i + 1], xx2 = x2[4 * i + 2], x3 = x2[4 * i + 3];
-        const float2 nb = make_float2(-b.x, -b.y), nc = make_float2(-c.x, -c.y),
-                     ne = make_float2(-e.x, -e.y);
-        x2[4 * i] = f2fma(a, x0, f2fma(nb, x1, f2fma(nc, xx2, f2mul(ne, x3))));
-        x2[4 * i + 1] = f2fma(b, x0, f2fma(a, x1, f2fma(ne, xx2, f2mul(c, x3))));
-        x2[4 * i + 2] = f2fma(c, x0, f2fma(e, x1, f2fma(a, xx2, f2mul(nb, x3))));
-        x2[4 * i + 3] = f2fma(e, x0, f2fma(nc, x1, f2fma(b, xx2, f2mul(a, x3))));
+#pragma unroll
+        for (int row = 0; row < 4; ++row) {
+          const float2* m = &p.mat2[i][4 * row];
+          x2[4 * i + row] = f2fma(m[0], x0, f2fma(m[1], x1, f2fma(m[2], xx2, f2mul(m[3], x3))));
+        }
       }
     }
     // x2 now holds sqrt(d) * (U x) (or U x when SO4 folded 1/sqrt(d) in)
@@ -378,10 +378,13 @@ extern "C" kvq3_status kvq3_write_chunk(kvq3_rotation rot, const kvq3_cache_desc
   }
   const bool so4 = (rot->flags & KVQ3_ROT_SO4) != 0;
   const double isd = 1.0 / sqrt((double)d);
-  for (int i = 0; i < d / 8; ++i)
-    for (int c = 0; c < 4; ++c)
-      p.quat2[i][c] = make_float2((float)(rot->quats64[4 * i + c] * isd),
-                                  (float)(rot->quats64[4 * (i + d / 8) + c] * isd));
+  if (d > kChunkMaxD) return KVQ3_ERR_UNSUPPORTED;
+  for (int i = 0; i < d / 8; ++i) {
+    double Ma[16], Mb[16];
+    so4_block_matrix(rot, i, Ma);
+    so4_block_matrix(rot, i + d / 8, Mb);
+    for (int c = 0; c < 16; ++c) p.mat2[i][c] = make_float2((float)(Ma[c] * isd), (float)(Mb[c] * isd));
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   const int key = g.d * 1000 + g.block;

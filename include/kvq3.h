@@ -39,7 +39,14 @@
  *   R3  R_i is the left-multiplication matrix of the unit quaternion
  *       p_i = (a, b, c, e) (x -> p_i * x as a quaternion product):
  *       [[a,-b,-c,-e],[b,a,-e,c],[c,e,a,-b],[e,-c,b,a]]; it acts on rotated
- *       coordinates 4i..4i+3.
+ *       coordinates 4i..4i+3.  With KVQ3_ROT_SO4_PAIR, R20 instead.
+ *   R20 The general element of SO(4) ([OMC] Mathematical statement: R_i in
+ *       SO(4)) as a pair of unit quaternions: R_i x = p_i * x * conj(q_i),
+ *       i.e. L(p_i) R(conj q_i) with R(q) the right-multiplication matrix
+ *       x -> x * q = [[a,-b,-c,-e],[b,a,e,-c],[c,-e,a,b],[e,c,-b,a]].  From a
+ *       seed, q_i is one more Marsaglia point per block drawn after all the
+ *       p_i (R4), so the signs and p_i are those of the one-quaternion
+ *       rotation with the same seed.
  *   R4  Seed -> parameters: SplitMix64 (Steele, Lea & Flood 2014) seeded with
  *       the seed.  Draws 0..d-1 give the signs (sign -1 when the top bit is
  *       set); then for each block i a uniform point of S^3 by Marsaglia's 1972
@@ -74,8 +81,8 @@
  *       quaternions that minimise the post-quantisation reconstruction MSE
  *       on sample vectors and names no search; taken as a random local
  *       search that keeps, per quantisation block, the best of the current
- *       set and perturbed copies, one quaternion per block (the general
- *       two-quaternion SO(4) is not used).
+ *       set and perturbed copies: one quaternion per block
+ *       (kvq3_calibrate_so4) or the pair of R20 (kvq3_calibrate_so4_pair).
  *   R17 Other code widths b = 2 and 4 ([OIQ] 3.3 stores d*b bits per
  *       vector, 4.2 packs INT3/INT4 values, 5.1 evaluates b = 4, 3, 2; [OMC]
  *       writes its quantiser for any b): divisor and clip bound
@@ -132,7 +139,8 @@
 extern "C" {
 #endif
 
-#define KVQ3_ABI_VERSION 2   /* 2: code widths 2-4, the asymmetric scale type, calibration */
+#define KVQ3_ABI_VERSION 3   /* 2: code widths 2-4, the asymmetric scale type, calibration;
+                                3: two-quaternion SO(4) blocks (KVQ3_ROT_SO4_PAIR) */
 
 typedef enum {
   KVQ3_OK = 0,
@@ -150,8 +158,10 @@ typedef enum {
                                  zero point per block, unsigned codes; b = 3 */
 } kvq3_scale_type;
 
-/* Rotation flags.  H_d is always applied. */
-enum { KVQ3_ROT_SIGN = 1u, KVQ3_ROT_SO4 = 2u };
+/* Rotation flags.  H_d is always applied.  KVQ3_ROT_SO4_PAIR (with
+ * KVQ3_ROT_SO4) makes every SO(4) block the general two-quaternion rotation
+ * of R20. */
+enum { KVQ3_ROT_SIGN = 1u, KVQ3_ROT_SO4 = 2u, KVQ3_ROT_SO4_PAIR = 4u };
 
 /* Bits of the device status word. */
 enum {
@@ -210,6 +220,14 @@ kvq3_status kvq3_rotation_create_from_params(int32_t d, const int8_t *signs,
                                              const float *quats,
                                              kvq3_rotation *out);
 
+/* Creates a two-quaternion rotation (R20) from explicit parameters (host
+ * arrays): signs[d], quats[d/4][4] (p_i) and quats_r[d/4][4] (q_i), each
+ * quaternion normalised in fp64 (a zero one is rejected).  Flags of the
+ * handle: KVQ3_ROT_SIGN | KVQ3_ROT_SO4 | KVQ3_ROT_SO4_PAIR.  Host only. */
+kvq3_status kvq3_rotation_create_from_params_pair(int32_t d, const int8_t *signs,
+                                                  const float *quats, const float *quats_r,
+                                                  kvq3_rotation *out);
+
 /* Frees a rotation handle (NULL is accepted). */
 kvq3_status kvq3_rotation_destroy(kvq3_rotation rot);
 
@@ -217,6 +235,11 @@ kvq3_status kvq3_rotation_destroy(kvq3_rotation rot);
  * quats[d/4][4] (fp32); *d_out (nullable) receives d. */
 kvq3_status kvq3_rotation_export(kvq3_rotation rot, int8_t *signs, float *quats,
                                  int32_t *d_out);
+
+/* As kvq3_rotation_export, plus quats_r[d/4][4] (nullable), the right
+ * quaternions q_i the device uses ((1,0,0,0) for a one-quaternion rotation). */
+kvq3_status kvq3_rotation_export_pair(kvq3_rotation rot, int8_t *signs, float *quats,
+                                      float *quats_r, int32_t *d_out);
 
 /* Byte sizes of a record, a page and the whole pool for a description. */
 kvq3_status kvq3_cache_sizes(const kvq3_cache_desc *desc, size_t *record_bytes,
@@ -374,7 +397,15 @@ kvq3_status kvq3_calib_sse(kvq3_rotation rot, const kvq3_cache_desc *desc, const
                            int32_t num_candidates, const void *x, int64_t n, double *sse,
                            void *stream);
 
-/* Device workspace bytes of kvq3_calibrate_so4 with num_candidates (>= 2). */
+/* kvq3_calib_sse for candidate two-quaternion blocks (R20): candidate p's
+ * quaternion pair of block i is (quats[p][i], quats_r[p][i]); both device
+ * fp32 [P][d/4][4], 16-byte aligned.  Otherwise as kvq3_calib_sse. */
+kvq3_status kvq3_calib_sse_pair(kvq3_rotation rot, const kvq3_cache_desc *desc, const float *quats,
+                                const float *quats_r, int32_t num_candidates, const void *x, int64_t n,
+                                double *sse, void *stream);
+
+/* Device workspace bytes of kvq3_calibrate_so4 and kvq3_calibrate_so4_pair
+ * with num_candidates (>= 2). */
 kvq3_status kvq3_calibrate_workspace_size(const kvq3_cache_desc *desc, int32_t num_candidates,
                                           size_t *bytes);
 
@@ -394,6 +425,18 @@ kvq3_status kvq3_calibrate_so4(kvq3_rotation rot, const kvq3_cache_desc *desc, c
                                int64_t n, int32_t rounds, int32_t num_candidates, float step,
                                uint64_t seed, void *workspace, size_t ws_bytes, float *quats_out,
                                double *sse_out, void *stream);
+
+/* The search of kvq3_calibrate_so4 over two-quaternion blocks (R20): every
+ * round perturbs both quaternions of every block (each by its own
+ * sigma * uniform [-1,1)^4 step, renormalised) and every quantisation block
+ * keeps its best pair.  The start is rot's pairs (q_i = 1 for a
+ * one-quaternion rotation).  quats_out, quats_r_out: host fp32 [d/4][4];
+ * sse_out (nullable) as in kvq3_calibrate_so4.  Synchronises the stream once
+ * per round. */
+kvq3_status kvq3_calibrate_so4_pair(kvq3_rotation rot, const kvq3_cache_desc *desc, const void *x,
+                                    int64_t n, int32_t rounds, int32_t num_candidates, float step,
+                                    uint64_t seed, void *workspace, size_t ws_bytes, float *quats_out,
+                                    float *quats_r_out, double *sse_out, void *stream);
 
 #ifdef __cplusplus
 }

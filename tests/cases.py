@@ -41,8 +41,12 @@ class Case:
                                 0, self.num_pages)
         self.layout = O.Layout(d, hkv, block, scale, page, self.B, self.maxp, self.num_pages, bits)
         self.rot = K.Rotation(d, rot_seed, flags)
-        s, q = O.rotation_params(d, rot_seed, bool(flags & 1), bool(flags & 2))
-        self.U = O.rotation_matrix(s, q)
+        if flags & 4:   # two-quaternion SO(4) blocks
+            s, q, qr = O.rotation_params_pair(d, rot_seed, bool(flags & 1))
+            self.U = O.rotation_matrix(s, q, qr)
+        else:
+            s, q = O.rotation_params(d, rot_seed, bool(flags & 1), bool(flags & 2))
+            self.U = O.rotation_matrix(s, q)
         self.spec = data or I.DataSpec(d, hkv, 1234, 0.03, 20.0)
         self.pool = torch.zeros(self.layout.pool_bytes, dtype=torch.uint8, device=self.dev)
         self.pool_o = np.zeros(self.layout.pool_bytes, np.uint8)

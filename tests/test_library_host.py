@@ -36,7 +36,7 @@ def test_every_declared_symbol_is_exported(K):
 
 
 def test_abi_and_status_strings(K):
-    assert K.kvq3_abi_version() == 2
+    assert K.kvq3_abi_version() == 3
     assert K.kvq3_status_string(0) == "ok"
     assert "workspace" in K.kvq3_status_string(4)
 
@@ -67,6 +67,46 @@ def test_rotation_from_params_normalises(K):
         K.kvq3_rotation_create_from_params(8, signs, np.zeros((2, 4), np.float32))
     with pytest.raises(K.Kvq3Error):
         K.kvq3_rotation_create(12, 1)                      # not a power of two
+
+
+@pytest.mark.parametrize("d", [4, 64, 128, 256])
+@pytest.mark.parametrize("flags", [6, 7])
+def test_pair_rotation_params_match_oracle(K, oracle, d, flags):
+    # reading R20: the signs and left quaternions of the one-quaternion
+    # rotation with the same seed, then one right quaternion per block
+    h = K.kvq3_rotation_create(d, 42, flags)
+    try:
+        s, q, r = K.kvq3_rotation_export_pair(h)
+    finally:
+        K.kvq3_rotation_destroy(h)
+    so, qo, ro = oracle.rotation_params_pair(d, 42, bool(flags & 1))
+    assert np.array_equal(s, so)
+    assert np.array_equal(q, qo.astype(np.float32))
+    assert np.array_equal(r, ro.astype(np.float32))
+    # one-quaternion rotations export identity right quaternions
+    h = K.kvq3_rotation_create(d, 42, 3)
+    try:
+        _, _, r1 = K.kvq3_rotation_export_pair(h)
+    finally:
+        K.kvq3_rotation_destroy(h)
+    assert np.all(r1 == np.array([1, 0, 0, 0], np.float32))
+
+
+def test_pair_rotation_flags_and_params(K):
+    with pytest.raises(K.Kvq3Error):
+        K.kvq3_rotation_create(128, 1, 4)                  # the pair needs the SO(4) blocks
+    with pytest.raises(K.Kvq3Error):
+        K.kvq3_rotation_create(128, 1, 8)                  # unknown flag
+    signs = np.ones(8, np.int8)
+    quats = np.array([[2, 0, 0, 0], [0, 0, 3, 4]], np.float32)
+    quats_r = np.array([[0, 5, 0, 0], [1, 1, 1, 1]], np.float32)
+    h = K.kvq3_rotation_create_from_params_pair(8, signs, quats, quats_r)
+    s, q, r = K.kvq3_rotation_export_pair(h)
+    K.kvq3_rotation_destroy(h)
+    assert np.allclose(q, [[1, 0, 0, 0], [0, 0, 0.6, 0.8]], atol=1e-7)
+    assert np.allclose(r, [[0, 1, 0, 0], [0.5, 0.5, 0.5, 0.5]], atol=1e-7)
+    with pytest.raises(K.Kvq3Error):
+        K.kvq3_rotation_create_from_params_pair(8, signs, quats, np.zeros((2, 4), np.float32))
 
 
 @pytest.mark.parametrize("d,block,scale,page", [(128, 64, "f16", 16), (256, 64, "f16", 16),
@@ -122,8 +162,9 @@ def test_invalid_descriptions_rejected_on_host(K):
 def test_calibration_arguments_checked_on_host(K):
     # workspace: candidate quaternions (rounded up to 256 bytes) + fp64 errors
     d = K.CacheDesc(128, 1, 64, 3, K.SCALE_TYPES["f16"], 1e-6, 16, 1, 1, 0, 1)
-    assert K.kvq3_calibrate_workspace_size(d, 64) == (64 * 128 * 4 + 255) // 256 * 256 + 64 * 2 * 8
-    assert K.kvq3_calibrate_workspace_size(d, 3) == (3 * 128 * 4 + 255) // 256 * 256 + 3 * 2 * 8
+    # (left and right quaternions of the two-quaternion search, each rounded)
+    assert K.kvq3_calibrate_workspace_size(d, 64) == 2 * ((64 * 128 * 4 + 255) // 256 * 256) + 64 * 2 * 8
+    assert K.kvq3_calibrate_workspace_size(d, 3) == 2 * ((3 * 128 * 4 + 255) // 256 * 256) + 3 * 2 * 8
     for p in (1, 0, 70000):
         with pytest.raises(K.Kvq3Error) as e:
             K.kvq3_calibrate_workspace_size(d, p)
@@ -149,3 +190,14 @@ def test_calibration_arguments_checked_on_host(K):
         st = K.lib.kvq3_calibrate_so4(rot, ctypes.byref(d), ctypes.c_void_p(256), 16, rounds, 4, step, 1,
                                       ctypes.c_void_p(256), need, q, None, None)
         assert st == 1, (rounds, step)
+    # the two-quaternion search takes the same checks, and needs quats_r_out
+    st = K.lib.kvq3_calibrate_so4_pair(rot, ctypes.byref(d), ctypes.c_void_p(256), 16, 1, 4, 0.5, 1,
+                                       ctypes.c_void_p(256), need - 8, q, q, None, None)
+    assert st == 4
+    st = K.lib.kvq3_calibrate_so4_pair(rot, ctypes.byref(d), ctypes.c_void_p(256), 16, 1, 4, 0.5, 1,
+                                       ctypes.c_void_p(256), need, q, None, None, None)
+    assert st == 1
+    for quats, quats_r in ((256, 0), (256, 264), (0, 256)):
+        st = K.lib.kvq3_calib_sse_pair(rot, ctypes.byref(d), ctypes.c_void_p(quats), ctypes.c_void_p(quats_r), 1,
+                                       ctypes.c_void_p(256), 16, sse, None)
+        assert st == 1, (quats, quats_r)
