@@ -56,9 +56,11 @@ def algorithmic_bytes(w: I.Workload, lens) -> dict:
     return dict(decode=kv + qo, write=write_in + write_out, per_token_head=per_tok_head)
 
 
-# code width and scale format overrides (--bits, --scale): 0 / "" keep each workload's own
+# code width, scale format and page size overrides (--bits, --scale, --page): 0 / "" keep each
+# workload's own
 BITS_OVERRIDE = 0
 SCALE_OVERRIDE = ""
+PAGE_OVERRIDE = 0
 
 
 def workload(name: str) -> I.Workload:
@@ -70,6 +72,8 @@ def workload(name: str) -> I.Workload:
         w = dataclasses.replace(w, bits=BITS_OVERRIDE)
     if SCALE_OVERRIDE:
         w = dataclasses.replace(w, scale=SCALE_OVERRIDE)
+    if PAGE_OVERRIDE and w.decode and not w.paged:
+        w = dataclasses.replace(w, page_size=PAGE_OVERRIDE)
     return w
 
 
@@ -460,31 +464,37 @@ def _median(xs):
 
 
 def time_decode(st, steps: int, warmup: int, world: int, stream) -> dict:
-    """Device-timed steps of a decode workload, inputs resident: per step an
-    event before the write, between write and decode and after the decode;
-    the whole region between barriers (max over ranks)."""
+    """Device-timed steps of a decode workload, inputs resident: first K steps
+    with nothing between the calls (the step time, between barriers, max over
+    ranks; the decode may then start under the token write), then K steps
+    with an event before the write, between write and decode and after the
+    decode (the per-call times)."""
     import torch
     for _ in range(warmup):
         st.step()
     torch.cuda.synchronize()
     assert int(st.status.item()) == 0, f"device status {int(st.status.item())}"
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     barrier(world)
     torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
+    for _ in range(steps):
+        st.write(st.k_new, st.v_new, st.seq_new, st.pos_new)
+        st.decode()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for i in range(steps):
         ev[i][0].record(stream)
         st.write(st.k_new, st.v_new, st.seq_new, st.pos_new)
         ev[i][1].record(stream)
         st.decode()
         ev[i][2].record(stream)
-    t_end.record(stream)
     torch.cuda.synchronize()
-    barrier(world)
-    total_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
     dec = [e[1].elapsed_time(e[2]) for e in ev]
     wr = [e[0].elapsed_time(e[1]) for e in ev]
     step = [e[0].elapsed_time(e[2]) for e in ev]
@@ -932,11 +942,14 @@ def main():
                     help="code width of the cache (0: the workload's own, 3)")
     ap.add_argument("--scale", default="", choices=["", "f32", "f16", "e4m3", "e4m3zp"],
                     help="scale format (e4m3zp: the asymmetric variant, E4M3 scale and zero point)")
+    ap.add_argument("--page", type=int, default=0,
+                    help="tokens per page of the contiguous decode caches (0: the workload's own, 128)")
     ap.add_argument("--oracle-leg", default="", help=argparse.SUPPRESS)
     args = ap.parse_args()
-    global BITS_OVERRIDE, SCALE_OVERRIDE
+    global BITS_OVERRIDE, SCALE_OVERRIDE, PAGE_OVERRIDE
     BITS_OVERRIDE = args.bits
     SCALE_OVERRIDE = args.scale
+    PAGE_OVERRIDE = args.page
     if args.oracle_leg:
         oracle_leg(args.oracle_leg)
         return

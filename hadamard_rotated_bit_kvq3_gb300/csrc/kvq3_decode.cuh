@@ -563,6 +563,10 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
   using SDec = ScaleDec<NB, SCALE>;
   constexpr int BPT = SDec::BPT;
 
+  // Launched as a programmatic dependent of the preceding kernel (the token
+  // write, typically): everything up to here overlaps it, and nothing is
+  // read before its writes are complete and visible.
+  griddep_wait();
   // the combine kernel may launch now: it waits for this grid before reading
   griddep_launch_dependents();
   extern __shared__ __align__(128) uint8_t smem[];
@@ -1509,24 +1513,30 @@ kvq3_status decode_run_t(const DecodePlan& plan, DecodeParams prm, const RotPara
   prm.chunk_tokens = plan.chunk_tokens;
   prm.pages_per_chunk = plan.pages_per_chunk;
   prm.ctas = plan.ctas;
-  decode_split_kernel<D, BLOCK, GPAD, SCALE, NBIT, PSPLIT, PF><<<plan.ctas, 32 * kWarps, plan.smem, st>>>(prm, rp);
-  if (cudaGetLastError() != cudaSuccess) return KVQ3_ERR_CUDA;
+  // Both kernels are programmatic dependents of what precedes them on the
+  // stream: the split kernel's launch overlaps the preceding kernel (the
+  // token write) and the combine's the split kernel's last CTAs; each waits
+  // on the preceding grid before its first read.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)plan.ctas);
+  cfg.blockDim = dim3(32 * kWarps);
+  cfg.dynamicSmemBytes = plan.smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, decode_split_kernel<D, BLOCK, GPAD, SCALE, NBIT, PSPLIT, PF>, prm, rp) !=
+      cudaSuccess)
+    return KVQ3_ERR_CUDA;
   const int64_t items = (int64_t)(prm.pf_n > 0 ? prm.pf_n : prm.g.batch) * prm.Hq;
   int64_t blocks = (items + 7) / 8;
   const int64_t cap = (int64_t)sm_count() * 8;
   if (blocks > cap) blocks = cap > 0 ? cap : 1;
-  // programmatic dependent launch: the combine's launch and set-up overlap
-  // the split kernel's last CTAs (it waits on the grid before its reads)
-  cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)blocks);
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, prm, rp, out) != cudaSuccess) return KVQ3_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? KVQ3_OK : KVQ3_ERR_CUDA;
 }

@@ -38,6 +38,9 @@ __global__ void __launch_bounds__(256) write_kernel(
   constexpr int WORDS = NBIT * D / 32;  // 32-bit words of a code string
   constexpr int QMAX = (1 << (NBIT - 1)) - 1;
   static_assert(E <= BLOCK && BITS <= 32 && WORDS <= L, "lane layout");
+  // a kernel launched after this one as a programmatic dependent (the decode)
+  // may start now; it waits for this grid's writes before it reads anything
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int r = lane % L, grp = lane / L;
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;

@@ -100,6 +100,9 @@ __global__ void __launch_bounds__(kTile) write_chunk_kernel(const __grid_constan
   constexpr int CB = NBIT * D / 8;      // code bytes (16 .. 64)
   constexpr int QMAX = (1 << (NBIT - 1)) - 1;
   constexpr int SB = SCALE == KVQ3_SCALE_F32 ? 4 : (SCALE == KVQ3_SCALE_F16 || SCALE == KVQ3_SCALE_E4M3_ZP) ? 2 : 1;
+  // a kernel launched after this one as a programmatic dependent may start
+  // now; it waits for this grid's writes before it reads anything
+  griddep_launch_dependents();
   extern __shared__ __align__(128) uint8_t smem[];
   const int t = threadIdx.x;
   const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem);

@@ -11,6 +11,9 @@ import numpy as np
 import kvq3_inputs as I
 from oracle import kvq3_oracle as O
 
+CANARY = 256             # guard bytes after every device buffer a kernel writes
+CANARY_BYTE = 0xA5
+
 TOL_DECODE = 2e-3        # max|err| <= TOL_DECODE * rms(out)
 TOL_SCALE = 1e-6         # relative
 BOUNDARY = 1e-4          # |x/s_q| within this of k + 1/2: code may round either way
@@ -48,7 +51,10 @@ class Case:
             s, q = O.rotation_params(d, rot_seed, bool(flags & 1), bool(flags & 2))
             self.U = O.rotation_matrix(s, q)
         self.spec = data or I.DataSpec(d, hkv, 1234, 0.03, 20.0)
-        self.pool = torch.zeros(self.layout.pool_bytes, dtype=torch.uint8, device=self.dev)
+        # the pool, then CANARY guard bytes that no kernel may touch
+        self._pool_full = torch.zeros(self.layout.pool_bytes + CANARY, dtype=torch.uint8, device=self.dev)
+        self._pool_full[self.layout.pool_bytes:] = CANARY_BYTE
+        self.pool = self._pool_full[:self.layout.pool_bytes]
         self.pool_o = np.zeros(self.layout.pool_bytes, np.uint8)
         self.table_t = None if self.table is None else torch.as_tensor(self.table, device=self.dev)
         self.lens_t = torch.as_tensor(self.lens, device=self.dev)
@@ -84,15 +90,37 @@ class Case:
     def oracle_write(self, k, v, si, ps):
         return O.write(self.pool_o, self.layout, self.U, k, v, si, ps, self.table)
 
+    def guarded(self, nbytes):
+        """A uint8 device buffer of nbytes followed by CANARY guard bytes:
+        (full, view); check_guard(full, nbytes) after the kernels ran."""
+        t = self.torch
+        full = t.empty(nbytes + CANARY, dtype=t.uint8, device=self.dev)
+        full[nbytes:] = CANARY_BYTE
+        return full, full[:nbytes]
+
+    @staticmethod
+    def check_guard(full, nbytes, what):
+        tail = full[nbytes:].cpu().numpy()
+        assert np.all(tail == CANARY_BYTE), f"{what}: a kernel wrote past the end of the buffer"
+
     def gpu_decode(self, q, sm_scale=0.0):
         t = self.torch
-        out = t.full((self.B, self.hq, self.d), float("nan"), dtype=t.float32, device=self.dev)
-        ws = t.empty(self.K.kvq3_decode_workspace_size(self.desc, self.hq), dtype=t.uint8,
-                     device=self.dev)
+        n_out = self.B * self.hq * self.d * 4
+        out_full, out_b = self.guarded(n_out)
+        out = out_b.view(t.float32).view(self.B, self.hq, self.d)
+        out.fill_(float("nan"))
+        n_ws = self.K.kvq3_decode_workspace_size(self.desc, self.hq)
+        ws_full, ws = self.guarded(n_ws)
         self.K.kvq3_decode_attn(self.rot.handle, self.desc, self.cache, t.as_tensor(q, device=self.dev),
                                 out, ws, sm_scale, self.status)
         t.cuda.synchronize()
+        self.check_guard(out_full, n_out, "decode output")
+        self.check_guard(ws_full, n_ws, "decode workspace")
+        self.check_pool_guard()
         return out.cpu().numpy().astype(np.float64)
+
+    def check_pool_guard(self):
+        self.check_guard(self._pool_full, self.layout.pool_bytes, "cache pool")
 
     def oracle_decode(self, q, sm_scale=0.0, lens=None):
         return O.decode(self.pool_o, self.layout, self.U, q, self.lens if lens is None else lens,
@@ -103,6 +131,7 @@ class Case:
 
     def device_status(self):
         self.torch.cuda.synchronize()
+        self.check_pool_guard()
         return int(self.status.item())
 
     # ------------------------------------------------------------ comparisons

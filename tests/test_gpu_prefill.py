@@ -38,10 +38,16 @@ def _ids(c):
 def _run(c: Case, seq: int, pos0: int, q: np.ndarray, sm_scale: float = 0.0):
     t = c.torch
     qd = t.as_tensor(q, device=c.dev)
-    out = t.full((q.shape[0], c.hq, c.d), float("nan"), dtype=t.float32, device=c.dev)
-    ws = t.empty(c.K.kvq3_prefill_workspace_size(c.desc, c.hq, q.shape[0]), dtype=t.uint8, device=c.dev)
+    n_out = q.shape[0] * c.hq * c.d * 4
+    out_full, out_b = c.guarded(n_out)
+    out = out_b.view(t.float32).view(q.shape[0], c.hq, c.d)
+    out.fill_(float("nan"))
+    n_ws = c.K.kvq3_prefill_workspace_size(c.desc, c.hq, q.shape[0])
+    ws_full, ws = c.guarded(n_ws)
     c.K.kvq3_prefill_attn(c.rot.handle, c.desc, c.cache, seq, pos0, qd, out, ws, sm_scale, c.status)
     t.cuda.synchronize()
+    c.check_guard(out_full, n_out, "prefill output")
+    c.check_guard(ws_full, n_ws, "prefill workspace")
     return out.cpu().numpy().astype(np.float64)
 
 
