@@ -23,14 +23,17 @@ __all__ = [
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libkvq3.so")
+# KVQ3_LIBRARY selects another build of the library (e.g. libkvq3_checked.so,
+# the build with in-kernel bounds checks); the default is the in-tree build
+LIB_PATH = os.environ.get("KVQ3_LIBRARY") or os.path.join(_HERE, "libkvq3.so")
 
 KVQ3_OK = 0
 KVQ3_ROT_SIGN = 1
 KVQ3_ROT_SO4 = 2
 KVQ3_ROT_SO4_PAIR = 4
 SCALE_TYPES = {"f32": 0, "f16": 1, "e4m3": 2, "e4m3zp": 3}
-DEV_BITS = {"bad_seq": 1, "bad_pos": 2, "bad_page": 4, "bad_len": 8, "bad_code": 16, "timeout": 32}
+DEV_BITS = {"bad_seq": 1, "bad_pos": 2, "bad_page": 4, "bad_len": 8, "bad_code": 16, "timeout": 32,
+            "check": 64}
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(

@@ -16,6 +16,9 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libkvq3.so")
 BUILD = os.path.join(ROOT, "_build")
+# the checked build: every kernel with its bounds checks (KVQ3_CHECKED) on
+LIB_CHECKED = os.path.join(HERE, "libkvq3_checked.so")
+BUILD_CHECKED = os.path.join(ROOT, "_build", "checked")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-ffp-contract=off",
@@ -40,15 +43,20 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, extra=()) -> str:
-    """Compiles (when stale) and links libkvq3.so; returns its path."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, extra=(), checked: bool = False) -> str:
+    """Compiles (when stale) and links libkvq3.so -- or, with checked=True,
+    libkvq3_checked.so, whose kernels carry the bounds checks that report
+    KVQ3_DEV_CHECK -- and returns its path."""
+    lib_path, build_dir = (LIB_CHECKED, BUILD_CHECKED) if checked else (LIB, BUILD)
+    if checked:
+        extra = (*extra, "-DKVQ3_CHECKED")
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
     headers.append(os.path.join(ROOT, "include", "kvq3.h"))
     objs, jobs = [], []
     for src in sources():
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if _stale(obj, [src] + headers):
             jobs.append([cc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj])
@@ -63,10 +71,10 @@ def build(verbose: bool = False, extra=()) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 4))) as ex:
         list(ex.map(run, jobs))
-    if jobs or _stale(LIB, objs):
-        run([cc, *ARCH, "-shared", "-o", LIB, *objs])
-    return LIB
+    if jobs or _stale(lib_path, objs):
+        run([cc, *ARCH, "-shared", "-o", lib_path, *objs])
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(verbose="-v" in sys.argv))
+    print(build(verbose="-v" in sys.argv, checked="--checked" in sys.argv))

@@ -218,6 +218,24 @@ __device__ __forceinline__ void set_status(int32_t* st, int bits) {
   if (st) atomicOr(st, bits);
 }
 
+// Bounds checks of a checked build (compiled with -DKVQ3_CHECKED): a check
+// that fails sets KVQ3_DEV_CHECK in the status word and its caller skips the
+// access.  In the normal build every check is the constant true.
+#ifdef KVQ3_CHECKED
+__device__ __forceinline__ bool checked(int32_t* st, bool ok) {
+  if (!ok) set_status(st, KVQ3_DEV_CHECK);
+  return ok;
+}
+#define KVQ3_CHECK(st, cond) ::kvq3::checked((st), (cond))
+#else
+#define KVQ3_CHECK(st, cond) true
+#endif
+
+// [base, base + n) lies inside [0, size)
+__device__ __forceinline__ bool in_range(int64_t base, int64_t n, int64_t size) {
+  return base >= 0 && n >= 0 && base <= size - n;
+}
+
 // ---------------------------------------------------------------- PTX
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

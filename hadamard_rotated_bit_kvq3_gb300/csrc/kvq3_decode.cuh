@@ -80,6 +80,8 @@ struct DecodeParams {
   int32_t pages_per_chunk;
   int32_t ctas;
   uint32_t slot_floats;   // floats per partial slot: G*(D+2)
+  uint32_t smem_bytes;    // dynamic shared memory of a CTA (checked builds)
+  int64_t slots;          // partial slots of the workspace (checked builds)
   uint32_t wait_limit;    // bound on mbarrier polls
   // Chunked prefill (pf_n > 0): the "sequences" are tiles of sequence
   // pf_seq: tile b holds query tokens tb*pf_qt .. (tb = b / pf_hb) and the
@@ -635,7 +637,10 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
       else mbar_arrive(&full[stage]);
     }
     __syncwarp();
-    if (ok)
+    if (ok && KVQ3_CHECK(p.status, in_range(SM::kStageOff + (int64_t)stage * p.stage_bytes + (int64_t)lane * 2 * REC,
+                                            2 * REC, p.smem_bytes) &&
+                                   in_range(pg * g.page_bytes + (int64_t)(c.kvh * 2) * REC, 2 * REC,
+                                            g.num_pages * g.page_bytes)))
       bulk_g2s(dst + (size_t)lane * 2 * REC, p.pool + (int64_t)(c.kvh * 2) * REC + pg * g.page_bytes, 2 * REC,
                &full[stage], pol);
   };
@@ -698,7 +703,11 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
   // merge the four warps' states of a unit into workspace slot (cta + unit);
   // the CTA holding the unit's first (last) chunk records itself as such
   auto flush = [&](int unit, bool first, bool last) {
-    if (threadIdx.x == 0) {
+    // checked builds: the slot and the unit range entry lie in the workspace
+    // (the merge below still runs, every warp reaching its barriers)
+    const bool slot_ok =
+        KVQ3_CHECK(p.status, cta + unit < p.slots && unit >= 0 && unit < (int64_t)g.batch * g.hkv);
+    if (threadIdx.x == 0 && slot_ok) {
       if (first) p.unit_cta[2 * unit] = (int32_t)cta;
       if (last) p.unit_cta[2 * unit + 1] = (int32_t)cta;
     }
@@ -732,8 +741,10 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
           const float mw = ml_s[(w * 2) * GPAD + h];
           L += (M == -INFINITY ? 0.0f : ex2(mw - M)) * ml_s[(w * 2 + 1) * GPAD + h];
         }
-        mS[h] = M;
-        lS[h] = L;
+        if (slot_ok) {
+          mS[h] = M;
+          lS[h] = L;
+        }
       }
     }
     // weights for the PV columns this lane holds
@@ -788,7 +799,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
                 float v = (acc[mt][tp][2 * e] + acc[mt][tp][2 * e + 1]) * sc;
                 if constexpr (ASYM) v += zh[tp % (ASYM ? NTP : 1)][b % (ASYM ? NB : 1)];
                 v *= cpv[tp][0];
-                if (h < p.G) {
+                if (h < p.G && slot_ok) {
                   if (pass == 0) slot[h * D + dim] = v;
                   else atomicAdd(&slot[h * D + dim], v);
                 }
@@ -797,7 +808,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
                 for (int c = 0; c < 2; ++c) {
                   const int h = 8 * tp + 2 * j + c;
                   const float v = acc[mt][tp][2 * e + c] * sc * cpv[tp][c];
-                  if (h < p.G) {
+                  if (h < p.G && slot_ok) {
                     if (pass == 0) slot[h * D + dim] = v;
                     else atomicAdd(&slot[h * D + dim], v);
                   }
@@ -1300,7 +1311,9 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
     }
     cur_last = (int)dw.y == (int)lds32<24>(st + desc_off) - 1;   // c == nc - 1
     if (!PF && n_tok == p.chunk_tokens && page_ok == (1u << p.pages_per_chunk) - 1u &&
-        p.chunk_tokens % (16 * kWarps) == 0) {
+        p.chunk_tokens % (16 * kWarps) == 0 &&
+        KVQ3_CHECK(p.status, in_range(SM::kStageOff + (int64_t)stage * p.stage_bytes,
+                                      (int64_t)p.pages_per_chunk * 2 * REC + 16, p.smem_bytes))) {
       // A whole chunk: the warp's steps t = 16 wid + 64 k, software-pipelined
       // so that P' and PV of step k and the logits of step k + 1 form one
       // branch-free stretch (the running-max update follows PV of step k).
@@ -1342,7 +1355,10 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, GPAD))
           tin -= P;
           ++pi;
         }
-        if ((page_ok >> pi) & 1u) {
+        if (((page_ok >> pi) & 1u) &&
+            KVQ3_CHECK(p.status, pi < p.pages_per_chunk && tin + 16 <= P &&
+                                     in_range(SM::kStageOff + (int64_t)stage * p.stage_bytes + (int64_t)(pi + 1) * 2 * REC,
+                                              0, p.smem_bytes))) {
           const uint32_t pg = st + (uint32_t)pi * 2 * REC;
           const int nv = min(P, n_tok - pi * P);        // valid tokens of this page
           const int64_t tok = (int64_t)dw.y * p.chunk_tokens + t;
@@ -1417,8 +1433,9 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const __grid_consta
       // gave up on a copy may not have recorded itself; the status says so)
       const int last_cta = p.ctas - 1;
       const int wlo = min(max(p.unit_cta[2 * unit], 0), last_cta);
-      const int whi = min(max(p.unit_cta[2 * unit + 1], 0), last_cta);
+      int whi = min(max(p.unit_cta[2 * unit + 1], 0), last_cta);
       float M = -INFINITY;
+      if (!KVQ3_CHECK(p.status, whi + unit < p.slots)) whi = wlo - 1;   // checked builds: no slot past the end
       for (int w = wlo; w <= whi; ++w) {
         const float* slot = p.ws + (size_t)(w + unit) * p.slot_floats;
         M = fmaxf(M, slot[p.G * D + gh]);
@@ -1513,6 +1530,8 @@ kvq3_status decode_run_t(const DecodePlan& plan, DecodeParams prm, const RotPara
   prm.chunk_tokens = plan.chunk_tokens;
   prm.pages_per_chunk = plan.pages_per_chunk;
   prm.ctas = plan.ctas;
+  prm.smem_bytes = plan.smem;
+  prm.slots = (int64_t)plan.ctas + (int64_t)prm.g.batch * prm.g.hkv;
   // Both kernels are programmatic dependents of what precedes them on the
   // stream: the split kernel's launch overlaps the preceding kernel (the
   // token write) and the combine's the split kernel's last CTAs; each waits

@@ -177,7 +177,8 @@ __global__ void __launch_bounds__(256) write_kernel(
       const int sh = BITS * src - 32 * r;
       if (in && sh > -BITS && sh < 32) word |= sh >= 0 ? (v << sh) : (v >> (-sh));
     }
-    if (ok) {
+    if (ok && KVQ3_CHECK(status, ::kvq3::in_range(rec, g.record_bytes, g.num_pages * g.page_bytes) &&
+                                     slot >= 0 && slot < g.page_size)) {
       uint8_t* base_p = pool + rec;
       if (r < WORDS)
         *reinterpret_cast<uint32_t*>(base_p + g.scale_hdr_bytes + (int64_t)slot * g.cb + 4 * r) = word;
@@ -256,6 +257,9 @@ __global__ void __launch_bounds__(256) dequant_kernel(
       if (seq < 0 || seq >= g.batch) bad = KVQ3_DEV_BAD_SEQ;
       else if (p < 0 || p >= cap) bad = KVQ3_DEV_BAD_POS;
       else if ((page = page_of(g, page_table, seq, p / g.page_size)) < 0) bad = KVQ3_DEV_BAD_PAGE;
+      if (!bad && !KVQ3_CHECK(status, ::kvq3::in_range(record_offset(g, page, kvh, which), g.record_bytes,
+                                               g.num_pages * g.page_bytes)))
+        bad = KVQ3_DEV_CHECK;
       if (!bad) {
         const int slot = (int)(p % g.page_size);
         const uint8_t* rec = pool + record_offset(g, page, kvh, which);

@@ -267,7 +267,9 @@ __global__ void __launch_bounds__(kTile) write_chunk_kernel(const __grid_constan
         if (bit % 32 > 32 - NBIT) words[bit / 32 + 1] |= c >> (32 - bit % 32);
       }
     }
-    if (page >= 0) {
+    if (page >= 0 && KVQ3_CHECK(p.status, in_range(record_offset(g, page, head, which), g.record_bytes,
+                                                  g.num_pages * g.page_bytes) &&
+                                         pos - lp * (uint32_t)g.page_size < (uint32_t)g.page_size)) {
       const int slot = (int)(pos - lp * (uint32_t)g.page_size);
       uint8_t* rec = p.pool + record_offset(g, page, head, which);
       uint8_t* cp = rec + g.scale_hdr_bytes + (int64_t)slot * CB;

@@ -170,7 +170,10 @@ enum {
   KVQ3_DEV_BAD_PAGE = 4,     /* page id outside [0, num_pages) */
   KVQ3_DEV_BAD_LEN = 8,      /* seq_lens[b] outside [0, capacity] */
   KVQ3_DEV_BAD_CODE = 16,    /* a stored code of -2^(b-1), e.g. -4 at b = 3 (never written) */
-  KVQ3_DEV_TIMEOUT = 32      /* an asynchronous copy did not arrive in time */
+  KVQ3_DEV_TIMEOUT = 32,     /* an asynchronous copy did not arrive in time */
+  KVQ3_DEV_CHECK = 64        /* a bounds check of a checked build failed (the
+                                library compiled with KVQ3_CHECKED); the
+                                access was skipped */
 };
 
 /* Opaque, immutable rotation U = B . H_d . D (host memory). */

@@ -395,3 +395,25 @@ def test_decode_large_group_over_seeds(cfg, seed):
           f"(worst (err - slack)/rms {float((err - slack).max()) / rms:.3e})")
     assert e_iso <= TOL_DECODE
     assert np.all(err <= TOL_DECODE * rms + slack)
+
+
+# ------------------------------------------------------------------ tiny cases
+@pytest.mark.parametrize("n", [1, 2, 3])
+@pytest.mark.parametrize("d,scale", [(64, "f32"), (128, "f16"), (256, "e4m3")])
+def test_tiny_one_page(d, scale, n):
+    # one page, 1-3 tokens: write against the oracle byte for byte (when no
+    # element sits at a rounding boundary) and decode against the oracle
+    c = Case(d=d, block=64 if d >= 128 else 32, scale=scale, page=16, lens=(n,), hkv=1, hq=2)
+    k, v, si, ps = c.tokens()
+    c.gpu_write(k, v, si, ps)
+    assert c.oracle_write(k, v, si, ps) == 0
+    assert c.device_status() == 0
+    stats = c.compare_written(k, v, si, ps)
+    # fp16 / E4M3 scales are exact away from a midpoint; an fp32 scale may sit
+    # an ulp from the oracle's (the 1e-6 bar), so only its codes are bytewise
+    if stats["boundary_codes"] == 0 and stats["midpoint_blocks"] == 0 and scale != "f32":
+        assert np.array_equal(c.pool.cpu().numpy(), c.pool_o)
+    q = c.queries()
+    got, ref = c.gpu_decode(q), c.oracle_decode(q)
+    assert c.device_status() == 0
+    assert rel_err(got, ref) <= TOL_DECODE
