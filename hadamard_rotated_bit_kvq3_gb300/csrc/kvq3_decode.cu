@@ -146,10 +146,11 @@ kvq3_status kvq3_prefill_workspace_size(const kvq3_cache_desc* desc, int32_t num
   return KVQ3_OK;
 }
 
-kvq3_status kvq3_prefill_attn(kvq3_rotation rot, const kvq3_cache_desc* desc,
-                              const kvq3_cache* cache, int32_t seq, int64_t pos0, int64_t n_q,
-                              const void* q, int32_t num_q_heads, float sm_scale, float* out,
-                              void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream) {
+static kvq3_status prefill_attn_impl(kvq3_rotation rot, const kvq3_cache_desc* desc,
+                                     const kvq3_cache* cache, int32_t seq, int64_t pos0, int64_t n_q,
+                                     const void* q, int32_t num_q_heads, float sm_scale, float* out,
+                                     void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream,
+                                     uint32_t wait_limit) {
   CacheGeom vg;
   int qt = 0, gcols = 0, hb = 0, hpb = 0;
   kvq3_status s = prefill_geom(desc, num_q_heads, n_q, &vg, &qt, &gcols, &hb, &hpb);
@@ -172,9 +173,13 @@ kvq3_status kvq3_prefill_attn(kvq3_rotation rot, const kvq3_cache_desc* desc,
     return KVQ3_ERR_WORKSPACE;
   const double qks = (sm_scale > 0.0f ? (double)sm_scale : 1.0 / sqrt((double)vg.d)) * 1.4426950408889634;
   if (vg.d == 128 && vg.bits == 3 && vg.scale_type != KVQ3_SCALE_E4M3_ZP) {
-    // shared dequantised tiles: each K/V tile is unpacked once for 64 query rows
+    // shared dequantised tiles: each K/V tile is unpacked once for 128 query
+    // rows on the tcgen05 path (blocks of 64), for 64 on the mma.sync one
     CacheGeom g;
     make_geom(desc, &g);
+    if (prefill_tc_supported(g, num_q_heads))
+      return prefill_tc(g, cache, seq, pos0, n_q, q, num_q_heads, (float)qks, out, dev_status, rot->params,
+                        wait_limit, static_cast<cudaStream_t>(stream));
     return prefill_tiles(g, cache, seq, pos0, n_q, q, num_q_heads, (float)qks, out, dev_status,
                          rot->params, static_cast<cudaStream_t>(stream));
   }
@@ -196,7 +201,7 @@ kvq3_status kvq3_prefill_attn(kvq3_rotation rot, const kvq3_cache_desc* desc,
   prm.qk_scale = (float)(sc * 1.4426950408889634);  // log2(e): softmax in base 2
   prm.inv_sqrt_d = inv_sqrt(vg.d);
   prm.slot_floats = (uint32_t)(gcols * (vg.d + 2));
-  prm.wait_limit = kWaitPolls;
+  prm.wait_limit = wait_limit;
   prm.pf_n = (int32_t)n_q;
   prm.pf_qt = qt;
   prm.pf_hb = hb;
@@ -205,6 +210,14 @@ kvq3_status kvq3_prefill_attn(kvq3_rotation rot, const kvq3_cache_desc* desc,
   prm.pf_seq = seq;
   prm.pf_pos0 = pos0;
   return prefill_run_for(vg, plan, prm, rot->params, out, static_cast<cudaStream_t>(stream));
+}
+
+kvq3_status kvq3_prefill_attn(kvq3_rotation rot, const kvq3_cache_desc* desc,
+                              const kvq3_cache* cache, int32_t seq, int64_t pos0, int64_t n_q,
+                              const void* q, int32_t num_q_heads, float sm_scale, float* out,
+                              void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  return prefill_attn_impl(rot, desc, cache, seq, pos0, n_q, q, num_q_heads, sm_scale, out, workspace,
+                           ws_bytes, dev_status, stream, kWaitPolls);
 }
 
 kvq3_status kvq3_decode_workspace_size(const kvq3_cache_desc* desc, int32_t num_q_heads,
@@ -239,6 +252,20 @@ kvq3_status kvq3_test_decode_attn_polls(kvq3_rotation rot, const kvq3_cache_desc
                                         int32_t* dev_status, void* stream, uint32_t polls) {
   return decode_attn_impl(rot, desc, cache, q, num_q_heads, sm_scale, out, workspace, ws_bytes,
                           dev_status, stream, polls);
+}
+
+// Test hook, not part of the public header: kvq3_prefill_attn with the bound
+// on each mbarrier wait set to `polls` polls (the tcgen05 path and the decode
+// kernel's prefill variant; the mma.sync tile kernel has no waits).  With
+// polls = 0 every CTA takes its time-out path: it flags KVQ3_DEV_TIMEOUT,
+// drains the copies and MMAs it issued, frees its tensor memory and returns.
+kvq3_status kvq3_test_prefill_attn_polls(kvq3_rotation rot, const kvq3_cache_desc* desc,
+                                         const kvq3_cache* cache, int32_t seq, int64_t pos0, int64_t n_q,
+                                         const void* q, int32_t num_q_heads, float sm_scale, float* out,
+                                         void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream,
+                                         uint32_t polls) {
+  return prefill_attn_impl(rot, desc, cache, seq, pos0, n_q, q, num_q_heads, sm_scale, out, workspace,
+                           ws_bytes, dev_status, stream, polls);
 }
 
 }  // extern "C"

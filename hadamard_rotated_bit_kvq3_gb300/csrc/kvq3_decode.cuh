@@ -55,11 +55,6 @@ constexpr int kChunk = 192;      // minimum tokens per chunk (smaller pages are 
 constexpr int kMaxPagesPerChunk = kChunk / 16;
 constexpr int kWarps = 4;        // consumer warps per CTA
 constexpr int kMaxStages = 8;
-// Bound on the polls of the drain after a timed-out copy (the normal waits
-// take DecodeParams::wait_limit).
-constexpr uint32_t kDrainPolls = 1u << 22;
-// Default bound on the polls of a stage wait.
-constexpr uint32_t kWaitPolls = 1u << 22;
 
 struct DecodeParams {
   CacheGeom g;

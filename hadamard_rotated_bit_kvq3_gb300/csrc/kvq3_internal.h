@@ -26,6 +26,19 @@ kvq3_status check_cache(const CacheGeom& g, const kvq3_cache* cache, bool need_l
 // Number of streaming multiprocessors of the current device (cached).
 int sm_count();
 
+// Bound on the polls of a drain after a timed-out wait (the normal waits take
+// the kernel's wait limit).
+constexpr uint32_t kDrainPolls = 1u << 22;
+// Default bound on the polls of an mbarrier wait.
+constexpr uint32_t kWaitPolls = 1u << 22;
+
+// tcgen05 path of kvq3_prefill_attn: d = 128, 3-bit symmetric codes, blocks
+// of 64, at most 128 query heads per kv head (arguments already checked).
+bool prefill_tc_supported(const CacheGeom& g, int32_t hq);
+kvq3_status prefill_tc(const CacheGeom& g, const kvq3_cache* cache, int32_t seq, int64_t pos0, int64_t n_q,
+                       const void* q, int32_t hq, float qk_scale, float* out, int32_t* dev_status,
+                       const RotParams& rp, uint32_t wait_limit, cudaStream_t st);
+
 // Tile-kernel path of kvq3_prefill_attn (d = 128; arguments already checked).
 kvq3_status prefill_tiles(const CacheGeom& g, const kvq3_cache* cache, int32_t seq, int64_t pos0,
                           int64_t n_q, const void* q, int32_t hq, float qk_scale, float* out,

@@ -26,6 +26,13 @@ PREFILL_CASES = [
     (dict(d=128, block=64, scale="f16", page=16, lens=(130,), hkv=1, hq=16, flags=1), 0, 100, 30),   # G=16
     (dict(d=64, block=32, scale="f16", page=16, lens=(150,), hkv=2, hq=12), 0, 60, 90),       # G=6, qt=2
     (dict(d=256, block=64, scale="f16", page=16, lens=(300, 180), hkv=2, hq=8, paged=True), 1, 100, 80),
+    # d = 128, blocks of 64: the tcgen05 kernel (128 rows = 128/G tokens x G heads a CTA, 64-key tiles)
+    (dict(d=128, block=64, scale="f16", page=64, lens=(400,), hkv=2, hq=6), 0, 100, 250),      # G=3: 126-row CTAs
+    (dict(d=128, block=64, scale="f16", page=48, lens=(700, 90), hkv=2, hq=8, paged=True), 0, 300, 400),  # tiles straddle pages
+    (dict(d=128, block=64, scale="f16", page=128, lens=(3000,), hkv=1, hq=4), 0, 2400, 600),   # 47 tiles, stage ring wraps
+    (dict(d=128, block=64, scale="e4m3", page=32, lens=(500,), hkv=4, hq=8, paged=True), 0, 499, 1),   # one query
+    (dict(d=128, block=64, scale="f32", page=16, lens=(260,), hkv=1, hq=12), 0, 0, 260),      # G=12: 120-row CTAs, from 0
+    (dict(d=128, block=64, scale="e4m3", page=64, lens=(1100,), hkv=2, hq=4, flags=7), 0, 1000, 100),  # SO(4) pairs
 ]
 
 
@@ -101,3 +108,36 @@ def test_prefill_custom_scale_and_bounds():
     # a workspace one byte short
     with pytest.raises(c.K.Kvq3Error):
         c.K.kvq3_prefill_attn(c.rot.handle, c.desc, c.cache, 0, 0, qd, out, ws[:-1])
+
+
+def test_prefill_bad_page_flags_and_masks():
+    # an out-of-range page id in the table: its keys are left out (masked),
+    # KVQ3_DEV_BAD_PAGE is flagged, and every output stays finite
+    c = Case(d=128, block=64, scale="f16", page=32, lens=(400,), hkv=2, hq=8, paged=True)
+    k, v, si, ps = c.tokens()
+    c.oracle_write(k, v, si, ps)
+    c.upload_oracle_pool()
+    table = c.table.copy()
+    table[0, 3] = c.num_pages + 7              # positions 96..127
+    c.table_t.copy_(c.torch.as_tensor(table, device=c.dev))
+    q = I.q_np(c.spec, 150, c.hq, 9)
+    got = _run(c, 0, 250, q)
+    assert c.device_status() & 4
+    assert np.isfinite(got).all()
+    # the masked prefill equals attention over the other positions: compare
+    # with the oracle on a cache where those keys can never win (a reference
+    # computed from the oracle's dequantised rows without positions 96..127)
+    from oracle import kvq3_oracle as Ox
+    U = c.U
+    ref = np.zeros_like(got)
+    keep = np.r_[0:96, 128:400]
+    for g in range(c.hkv):
+        kh = Ox.read_rotated(c.pool_o, c.layout, 0, g, 0, 0, 400, c.table)[0]
+        vh = Ox.read_rotated(c.pool_o, c.layout, 0, g, 1, 0, 400, c.table)[0]
+        for i in range(150):
+            m = 250 + i + 1
+            idx = keep[keep < m]
+            for gh in range(c.hq // c.hkv):
+                h = g * (c.hq // c.hkv) + gh
+                ref[i, h] = Ox.attention_rotated(U, q[i, h], kh[idx], vh[idx], 1.0 / np.sqrt(c.d))
+    assert rel_err(got, ref) <= TOL_DECODE
