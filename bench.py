@@ -893,9 +893,11 @@ def run_prefill_attn(args, world, rank, dev):
         os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
     peak = float(pk.get("bf16_tflops", 1900.0))
     tflops = st.flops() / (ms * 1e-3) / 1e12
-    # d = 128 with 3-bit symmetric codes runs the tile kernel (one launch);
-    # the other formats the decode kernel's prefill variant and the combine
+    # d = 128 with 3-bit symmetric codes runs a tile kernel (one launch): the
+    # tcgen05 one with blocks of 64, the mma.sync one with blocks of 32; the
+    # other formats the decode kernel's prefill variant and the combine
     tile = w.d == 128 and w.bits == 3 and w.scale != "e4m3zp"
+    tile_kernel = "prefill_tc_kernel" if w.block == 64 else "prefill_tile_kernel"
     if rank == 0:
         cpu = None
         if not args.no_cpu_baseline and world == 1:
@@ -911,7 +913,7 @@ def run_prefill_attn(args, world, rank, dev):
             "config": workload_config(w, None, world),
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                          "frac": tflops / peak, "traffic": None,
-                         "kernel": "kvq3_prefill_attn (" + ("prefill_tile_kernel" if tile else
+                         "kernel": "kvq3_prefill_attn (" + (tile_kernel if tile else
                                    "decode_split_kernel<..., prefill> + decode_combine_kernel") + ")",
                          "peak_source": "measured bf16 (fp16 mma has the same nominal rate)"
                          if pk else "fallback"},

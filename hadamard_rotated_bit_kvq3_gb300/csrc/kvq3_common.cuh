@@ -317,6 +317,30 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Packed pairs of fp32 (sm_100 family f32x2 arithmetic): one instruction for two lanes' worth.
+typedef unsigned long long u64;
+__device__ __forceinline__ float2 f2add(float2 a, float2 b) {
+  u64 d, x = *reinterpret_cast<u64*>(&a), y = *reinterpret_cast<u64*>(&b);
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(x), "l"(y));
+  return *reinterpret_cast<float2*>(&d);
+}
+__device__ __forceinline__ float2 f2sub(float2 a, float2 b) {
+  u64 d, x = *reinterpret_cast<u64*>(&a), y = *reinterpret_cast<u64*>(&b);
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(x), "l"(y));
+  return *reinterpret_cast<float2*>(&d);
+}
+__device__ __forceinline__ float2 f2mul(float2 a, float2 b) {
+  u64 d, x = *reinterpret_cast<u64*>(&a), y = *reinterpret_cast<u64*>(&b);
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(x), "l"(y));
+  return *reinterpret_cast<float2*>(&d);
+}
+__device__ __forceinline__ float2 f2fma(float2 a, float2 b, float2 c) {
+  u64 d, x = *reinterpret_cast<u64*>(&a), y = *reinterpret_cast<u64*>(&b),
+         z = *reinterpret_cast<u64*>(&c);
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(x), "l"(y), "l"(z));
+  return *reinterpret_cast<float2*>(&d);
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);

@@ -27,15 +27,19 @@
 // the product; E4M3 scales have s_lo = 0 and skip the third MMA).  Dequantised
 // values must lie in the fp16 range, as for every kernel of this library.
 //
-// Roles (9 warps):
-//  * warps 0-3, softmax: thread = row.  tcgen05.ld of S, scales, mask, online
-//    softmax, p_hi / p_lo written back over S with tcgen05.st (the A operand
-//    of PV), rare rescales of O in place;
-//  * warps 4-7, dequantisation: thread = (key, half of the dimensions).  Thread
-//    0 issues the bulk copies of packed codes and scales into a ring of raw
-//    stages; all unpack a tile into the MMA layouts in shared memory: integer
-//    key codes K-major, values c*s_hi and c*s_lo MN-major;
-//  * warp 8, lane 0: issues QK^T of tile t, then PV of tile t - 1.
+// Roles (14 warps):
+//  * warps 6-13, softmax: warps w and w + 4 share the 32 rows of TMEM lane
+//    quarter w % 4 (thread = row), each taking 32 of a tile's 64 keys; they trade
+//    row maxima through shared memory at a 64-thread named barrier that also
+//    carries their decision to go on.  tcgen05.ld of S, key scales, mask,
+//    online softmax, p_hi / p_lo written back over S with tcgen05.st (the A
+//    operand of PV), rare rescales of O in place;
+//  * warps 2-5, dequantisation: thread = (key, half of the dimensions); a tile
+//    is unpacked into the MMA layouts in shared memory: integer key codes
+//    K-major, values c*s_hi and c*s_lo MN-major;
+//  * warp 0, lane 0: issues QK^T of tile t, then PV of tile t - 1;
+//  * warp 1, lane 0: issues the bulk copies of packed codes and scales into a
+//    ring of raw stages, up to kStages tiles ahead.
 // TMEM: q1 hi / lo (128 columns), two S/P buffers (128 each), O (128).
 // Every hand-off is an mbarrier; every wait is bounded (a time-out sets
 // KVQ3_DEV_TIMEOUT and the CTA winds down: MMAs and copies in flight are
@@ -54,10 +58,15 @@ constexpr int kKeys = 64;             // keys per tile
 constexpr int kD = 128;               // head dimension
 constexpr int kCB = 3 * kD / 8;       // code bytes per vector (48)
 constexpr int kStages = 4;            // raw stages in flight
-constexpr int kThreads = 9 * 32;
-constexpr int kMmaThread = 8 * 32;
+constexpr int kThreads = 14 * 32;
+constexpr int kMmaWarp = 0;           // the two one-thread roles take the lowest warps,
+constexpr int kMmaThread = 0;         // which the schedulers favour
+constexpr int kProducer = 32;
+constexpr int kDequant0 = 2 * 32;     // warps 2-5
+constexpr int kSoftmax0 = 6;          // warps 6-13
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColQ = 0, kColSP = 128, kColO = 384;   // TMEM column map
+constexpr int kSP = 3;                // S/P buffers in TMEM
+constexpr uint32_t kColSP = 0, kColO = 384;   // TMEM: S/P buffer j at 128 j, O
 constexpr float kRescale = 8.0f;      // log2 of the largest p between rescales
 
 // shared memory (bytes)
@@ -67,15 +76,18 @@ constexpr int kOffV = kOffK + 2 * kTile;                       // [2][hi, lo] va
 constexpr int kRawK = 0, kRawV = kKeys * kCB;                  // raw stage: codes K, V
 constexpr int kRawKs = 2 * kKeys * kCB, kRawVs = kRawKs + kKeys * 2 * 4;   // scales K, V (<= 8 B a key)
 constexpr int kRawBytes = kRawVs + kKeys * 2 * 4;              // 7168
-constexpr int kOffRaw = kOffV + 4 * kTile;
-constexpr int kOffKs = kOffRaw + kStages * kRawBytes;          // [2][2 blocks][64] fp32 key scales
+constexpr int kOffQ = kOffV + 4 * kTile;                       // q1 hi, lo: K-major A of QK^T
+constexpr int kOffRaw = kOffQ + 4 * kTile;
+constexpr int kOffKs = kOffRaw + kStages * kRawBytes;          // [kStages][64 keys][2 blocks] fp32 key scales
+constexpr int kOffRed = kOffKs + kStages * kKeys * 2 * 4;      // [2][2][128] fp32 row maxima / sums traded
 constexpr int kPitch = kD + 1;                                 // row staging pitch (floats)
-constexpr int kOffRows = kOffKs + 2 * 2 * kKeys * 4;           // [128][129] fp32 rows
-constexpr int kOffQinv = kOffRows + kRows * kPitch * 4;        // [128] fp32
-constexpr int kNumBars = 2 * kStages + 11;
+constexpr int kOffRows = kOffK;                                // [128][129] fp32 outputs over the K/V tiles
+constexpr int kOffQinv = kOffRed + 2 * 2 * kRows * 4;          // [128] fp32
+constexpr int kNumBars = 3 * kStages + 4 + 3 * kSP + 1;
+static_assert(kRows * kPitch * 4 <= kOffQ - kOffK, "output staging fits over the K/V tiles");
 constexpr int kOffBars = kOffQinv + kRows * 4;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;              // TMEM base, abort flag, masks
-constexpr int kSmem = kOffMisc + 16 + (kStages + 2) * 8;
+constexpr int kSmem = kOffMisc + 16 + 2 * kStages * 8;
 static_assert(kOffRaw % 16 == 0 && kRawBytes % 16 == 0 && kOffBars % 8 == 0, "alignment");
 static_assert(kSmem <= 227 * 1024, "shared memory");
 
@@ -124,6 +136,19 @@ __device__ __forceinline__ __half2 codes2(uint32_t w6) {
 }
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
+// Named barrier `id` of two warps (64 threads) that also returns the AND of
+// their flags; it orders their shared-memory accesses like bar.sync.
+__device__ __forceinline__ bool pair_and(int id, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n bar.red.and.pred po, %2, 64, pi;\n"
+      " selp.u32 %0, 1, 0, po;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id)
+      : "memory");
+  return r != 0;
+}
+
 template <int SCALE>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ TcParams p,
                                                                   const __grid_constant__ RotParams rp) {
@@ -133,20 +158,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
   uint64_t* raw_full = bars;                   // [kStages] bulk copies landed
-  uint64_t* raw_empty = bars + kStages;        // [kStages] dequantisation done with a stage
-  uint64_t* k_full = bars + 2 * kStages;       // [2] key tile and key scales ready
+  uint64_t* raw_empty = bars + kStages;        // [kStages] dequantisation and softmax done with a stage
+  uint64_t* ks_full = bars + 2 * kStages;      // [kStages] key scales and valid-key mask of a stage ready
+  uint64_t* k_full = bars + 3 * kStages;       // [2] key tile ready
   uint64_t* v_full = k_full + 2;               // [2] value tiles ready
-  uint64_t* s_full = v_full + 2;               // [2] S of the tile in TMEM
-  uint64_t* p_full = s_full + 2;               // [2] P of the tile in TMEM (and O rescaled)
-  uint64_t* pv_done = p_full + 2;              // [2] PV of the tile complete
-  uint64_t* drain = pv_done + 2;               // every MMA complete
+  uint64_t* s_full = v_full + 2;               // [kSP] S of the tile in TMEM
+  uint64_t* p_full = s_full + kSP;             // [kSP] P of the tile in TMEM (and O rescaled)
+  uint64_t* pv_done = p_full + kSP;            // [kSP] PV of the tile complete
+  uint64_t* drain = pv_done + kSP;             // every MMA complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   uint64_t* stage_mask = reinterpret_cast<uint64_t*>(smem + kOffMisc + 16);   // [kStages] valid keys
-  uint64_t* key_mask = stage_mask + kStages;                                  // [2]
+  uint64_t* key_mask = stage_mask + kStages;                                  // [kStages]
   float* rows = reinterpret_cast<float*>(smem + kOffRows);
   float* qinv_s = reinterpret_cast<float*>(smem + kOffQinv);
   float* ks_s = reinterpret_cast<float*>(smem + kOffKs);
+  float* red_s = reinterpret_cast<float*>(smem + kOffRed);
 
   const CacheGeom& g = p.g;
   const int kvh = blockIdx.y;
@@ -160,20 +187,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&raw_full[s], 1);
-      mbar_init(&raw_empty[s], 128);
+      mbar_init(&raw_empty[s], 128 + 256);
+      mbar_init(&ks_full[s], 128);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&k_full[b], 128);
       mbar_init(&v_full[b], 128);
-      mbar_init(&s_full[b], 1);
-      mbar_init(&p_full[b], 128);
-      mbar_init(&pv_done[b], 1);
+    }
+    for (int j = 0; j < kSP; ++j) {
+      mbar_init(&s_full[j], 1);
+      mbar_init(&p_full[j], 256);
+      mbar_init(&pv_done[j], 1);
     }
     mbar_init(drain, 1);
     *abort_flag = 0u;
     fence_mbar_init();
   }
-  if (warp == 8) tc::alloc(tmem_slot, kTmemCols);
+  if (warp == kMmaWarp) tc::alloc(tmem_slot, kTmemCols);
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
@@ -191,42 +221,48 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   };
 
   // bulk copies of tile t (16-key groups; a page holds whole groups since P
-  // is a multiple of 16) into its raw stage; called by dequant thread 0 only
+  // is a multiple of 16) into its raw stage; producer thread only.  Positions
+  // are below 2^31 (checked on the host): 32-bit page arithmetic.
   const int64_t pool_bytes = g.num_pages * g.page_bytes;
   (void)pool_bytes;   // read by the checked build only
   auto issue = [&](int t) {
     const int s = t % kStages;
     uint8_t* st = smem + kOffRaw + s * kRawBytes;
-    const int64_t k0 = (int64_t)t * kKeys;
-    int64_t gpage[4];
+    const uint32_t k0 = (uint32_t)t * kKeys, P = (uint32_t)g.page_size, last = (uint32_t)kmax;
+    int64_t pg[4];
+    uint32_t slot[4];
     uint64_t mask = 0;
     uint32_t bytes = 0;
 #pragma unroll
     for (int gi = 0; gi < 4; ++gi) {
-      const int64_t pos = k0 + 16 * gi;
-      gpage[gi] = -1;
-      if (pos > kmax) continue;
-      const int64_t pg = page_of(g, p.page_table, p.seq, pos / g.page_size);
-      if (pg < 0) {
+      const uint32_t pos = k0 + 16u * gi;
+      pg[gi] = -1;
+      slot[gi] = 0;
+      if (pos > last) continue;
+      const uint32_t lp = pos / P;
+      slot[gi] = pos - lp * P;
+      pg[gi] = page_of(g, p.page_table, p.seq, lp);
+      if (pg[gi] < 0) {
         set_status(p.status, KVQ3_DEV_BAD_PAGE);
         continue;
       }
-      gpage[gi] = pg;
       mask |= 0xFFFFull << (16 * gi);
       bytes += 16u * (2u * kCB + 2u * 2u * SB);
     }
-    if (kmax - k0 < kKeys - 1) mask &= (1ull << (kmax - k0 + 1)) - 1ull;   // keys past the last row
+    if (last - k0 < (uint32_t)kKeys - 1u) mask &= (1ull << (last - k0 + 1u)) - 1ull;   // keys past the last row
     stage_mask[s] = mask;
     mbar_expect_tx(&raw_full[s], bytes);
+#pragma unroll
     for (int gi = 0; gi < 4; ++gi) {
-      if (gpage[gi] < 0) continue;
-      int gj = gi;
-      while (gj + 1 < 4 && gpage[gj + 1] == gpage[gi]) ++gj;   // consecutive groups of one page
-      const uint32_t nk = 16u * (uint32_t)(gj - gi + 1);
-      const int64_t slot = (k0 + 16 * gi) % g.page_size;
-      const int64_t rk = record_offset(g, gpage[gi], kvh, 0), rv = record_offset(g, gpage[gi], kvh, 1);
-      const int64_t ck = rk + g.scale_hdr_bytes + slot * kCB, cv = rv + g.scale_hdr_bytes + slot * kCB;
-      const int64_t sk = rk + slot * 2 * SB, sv = rv + slot * 2 * SB;
+      if (pg[gi] < 0 || (gi > 0 && pg[gi - 1] == pg[gi])) continue;   // not the first group of a run
+      uint32_t nk = 16u;                                                // consecutive groups of one page
+#pragma unroll
+      for (int gj = gi + 1; gj < 4; ++gj)
+        if (pg[gj] == pg[gi] && nk == 16u * (uint32_t)(gj - gi)) nk += 16u;
+      const int64_t rk = record_offset(g, pg[gi], kvh, 0), rv = record_offset(g, pg[gi], kvh, 1);
+      const int64_t ck = rk + g.scale_hdr_bytes + (int64_t)slot[gi] * kCB;
+      const int64_t cv = rv + g.scale_hdr_bytes + (int64_t)slot[gi] * kCB;
+      const int64_t sk = rk + (int64_t)slot[gi] * 2 * SB, sv = rv + (int64_t)slot[gi] * 2 * SB;
       if (KVQ3_CHECK(p.status, in_range(ck, nk * kCB, pool_bytes) && in_range(cv, nk * kCB, pool_bytes) &&
                                    in_range(sk, nk * 2 * SB, pool_bytes) && in_range(sv, nk * 2 * SB, pool_bytes))) {
         bulk_copy(st + kRawK + 16 * gi * kCB, p.pool + ck, nk * kCB, &raw_full[s]);
@@ -240,14 +276,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                      "r"(nk * (2u * kCB + 2u * 2u * SB))
                      : "memory");
       }
-      gi = gj;
     }
   };
-  int issued = 0;   // tiles whose copies dequant thread 0 has issued
-  if (tid == 128)
-    for (; issued < min(kStages - 1, T); ++issued) issue(issued);
 
-  // ---- q1 = U q of the rows, scaled by qk_scale and a per-row power of two
+  // ---- q1 = U q of the rows, scaled by qk_scale and a per-row power of two,
+  // as hi + lo fp16 halves in the K-major A layout of QK^T: (row, d) at
+  // (row/8)*2048 + (d/8)*128 + (row%8)*16 + (d%8)*2, the lo halves 32 KB on
   {
     const uint32_t sgn = lane_signs<4>(rp, lane);
     float4 qt[1], qtr[1];
@@ -279,128 +313,135 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       if (amax > 0.0f) frexpf(amax, &ex);
       ex = max(-100, min(100, 8 - ex));                    // row maximum into (2^7, 2^8]
       const float sc = ldexpf(1.0f, ex);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) rows[row * kPitch + lane * 4 + e] = x[e] * sc;
+      const float2 y0 = make_float2(x[0] * sc, x[1] * sc), y1 = make_float2(x[2] * sc, x[3] * sc);
+      const __half2 h0 = __floats2half2_rn(y0.x, y0.y), h1 = __floats2half2_rn(y1.x, y1.y);
+      const float2 r0 = f2sub(y0, __half22float2(h0)), r1 = f2sub(y1, __half22float2(h1));
+      uint8_t* qa = smem + kOffQ + (row >> 3) * 2048 + (lane >> 1) * 128 + (row & 7) * 16 + (lane & 1) * 8;
+      *reinterpret_cast<uint2*>(qa) = make_uint2(h2u(h0), h2u(h1));
+      *reinterpret_cast<uint2*>(qa + 2 * kTile) =
+          make_uint2(h2u(__floats2half2_rn(r0.x, r0.y)), h2u(__floats2half2_rn(r1.x, r1.y)));
       if (lane == 0) qinv_s[row] = ldexpf(1.0f, -ex);
     }
   }
+  fence_proxy_async();   // generic stores read by the tensor cores
   __syncthreads();
-  if (warp < 4) {   // row = thread: hi and lo halves into TMEM (q1_hi cols 0-63, q1_lo 64-127)
-    const uint32_t lanes = (uint32_t)(32 * warp) << 16;
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      uint32_t hv[32], lv[32];
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float a = rows[tid * kPitch + 64 * hf + 2 * c], b = rows[tid * kPitch + 64 * hf + 2 * c + 1];
-        const __half2 hi = __floats2half2_rn(a, b);
-        const float2 f = __half22float2(hi);
-        hv[c] = h2u(hi);
-        lv[c] = h2u(__floats2half2_rn(a - f.x, b - f.y));
-      }
-      tc::st32(tmem + lanes + kColQ + 32 * hf, hv);
-      tc::st32(tmem + lanes + kColQ + 64 + 32 * hf, lv);
-    }
-    tc::wait_st();
-  }
-  tc::fence_before();
-  __syncthreads();
-  tc::fence_after();
 
-  if (warp < 4) {
+  if (warp >= kSoftmax0) {
     // ================================================================ softmax
-    const int row = tid;
-    const uint32_t lanes = (uint32_t)(32 * warp) << 16;
+    const int wq = warp & 3, kh = (warp - kSoftmax0) >> 2;   // lane quarter; key half (keys 32kh .. 32kh + 31)
+    const int row = 32 * wq + lane;
+    const uint32_t lanes = (uint32_t)(32 * wq) << 16;
     const float qinv = qinv_s[row];
+    const float2 qinv2 = make_float2(qinv, qinv);
     const int64_t lim = row < nrows ? p.pos0 + t0 + row / p.G : -1;
-    float m_used = -INFINITY, l = 0.0f;
-    bool ok = true;
-    for (int t = 0; t < T && ok; ++t) {
-      const int b = t & 1;
-      const uint32_t ph = (uint32_t)(t >> 1) & 1u;
-      ok = __all_sync(kFull, wait(&s_full[b], ph) && wait(&k_full[b], ph));
-      if (!ok) break;
-      tc::fence_after();
-      const uint32_t tS = tmem + lanes + kColSP + 128u * b;
-      const uint64_t km = key_mask[b];
-      const int64_t k0 = (int64_t)t * kKeys;
-      const bool full = km == ~0ull && k0 + kKeys - 1 <= lim;
-      float sv[kKeys];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {   // keys 32h .. 32h + 31
+    float m_used = -INFINITY;
+    float2 l2 = make_float2(0.0f, 0.0f);
+    bool okw = true;   // this warp's waits all succeeded (warp-uniform)
+    for (int t = 0; t < T; ++t) {
+      const int b = t & 1, s = t % kStages, j = t % kSP;
+      okw = okw && __all_sync(kFull, wait(&s_full[j], (uint32_t)(t / kSP) & 1u) &&
+                                         wait(&ks_full[s], (uint32_t)(t / kStages) & 1u));
+      const uint32_t tS = tmem + lanes + kColSP + 128u * j;
+      float2 sv[16];
+      float pmax = -INFINITY;
+      if (okw) {
+        tc::fence_after();
         uint32_t a[32], c[32];
-        tc::ld32(tS + 32 * h, a);         // block 0
-        tc::ld32(tS + 64 + 32 * h, c);    // block 1
+        tc::ld32(tS + 32 * kh, a);          // S, block 0, this half's keys
+        tc::ld32(tS + 64 + 32 * kh, c);     // S, block 1
+        const float4* ksr = reinterpret_cast<const float4*>(ks_s + (s * kKeys + 32 * kh) * 2);
+        const uint32_t km = (uint32_t)(key_mask[s] >> (32 * kh));
+        float4 kk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) kk[i] = ksr[i];   // (k0, k1) of keys 2i, 2i + 1
+        mbar_arrive(&raw_empty[s]);                   // done with the stage's scales and mask
         tc::wait_ld();
         tc::reg_fence(a);
         tc::reg_fence(c);
-        const float2* k0s = reinterpret_cast<const float2*>(ks_s + (b * 2 + 0) * kKeys + 32 * h);
-        const float2* k1s = reinterpret_cast<const float2*>(ks_s + (b * 2 + 1) * kKeys + 32 * h);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 x0 = k0s[i], x1 = k1s[i];
-          sv[32 * h + 2 * i] = fmaf(__uint_as_float(c[2 * i]), x1.x, __uint_as_float(a[2 * i]) * x0.x);
-          sv[32 * h + 2 * i + 1] = fmaf(__uint_as_float(c[2 * i + 1]), x1.y, __uint_as_float(a[2 * i + 1]) * x0.y);
+        for (int i = 0; i < 16; ++i)
+          sv[i] = f2fma(make_float2(__uint_as_float(c[2 * i]), __uint_as_float(c[2 * i + 1])),
+                        make_float2(kk[i].y, kk[i].w),
+                        f2mul(make_float2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1])),
+                              make_float2(kk[i].x, kk[i].z)));
+        const int64_t k0 = (int64_t)t * kKeys + 32 * kh;
+        if (!(km == 0xFFFFFFFFu && k0 + 31 <= lim)) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            if (!((km >> (2 * i)) & 1u) || k0 + 2 * i > lim) sv[i].x = -INFINITY;
+            if (!((km >> (2 * i + 1)) & 1u) || k0 + 2 * i + 1 > lim) sv[i].y = -INFINITY;
+          }
         }
-      }
-      if (!full) {
+        float m8[8];
 #pragma unroll
-        for (int k = 0; k < kKeys; ++k)
-          if (!((km >> k) & 1ull) || k0 + k > lim) sv[k] = -INFINITY;
-      }
-      float mx = sv[0];
+        for (int i = 0; i < 8; ++i) m8[i] = fmaxf(fmaxf(sv[2 * i].x, sv[2 * i].y), fmaxf(sv[2 * i + 1].x, sv[2 * i + 1].y));
 #pragma unroll
-      for (int k = 1; k < kKeys; ++k) mx = fmaxf(mx, sv[k]);
+        for (int i = 0; i < 4; ++i) m8[i] = fmaxf(m8[i], m8[i + 4]);
+        pmax = fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3]));
+        red_s[(b * 2 + kh) * kRows + row] = pmax;
+      }
+      if (!pair_and(1 + wq, okw)) break;                 // both warps of the rows go on, or neither
+      const float mx = fmaxf(pmax, red_s[(b * 2 + (kh ^ 1)) * kRows + row]);
       const float xm = mx * qinv;
       const bool need = xm > m_used + kRescale;
       if (__any_sync(kFull, need)) {
         const float m_new = need ? xm : m_used;
         const float alpha = need ? (m_used == -INFINITY ? 0.0f : ex2(m_used - m_new)) : 1.0f;
-        l *= alpha;
-        if (t > 0) {   // O holds PV up to tile t - 1: wait for it, then scale it in place
-          ok = __all_sync(kFull, wait(&pv_done[(t - 1) & 1], (uint32_t)((t - 1) >> 1) & 1u));
-          if (!ok) break;
-          tc::fence_after();
+        l2.x *= alpha;
+        l2.y *= alpha;
+        if (t > 0) {   // O holds PV up to tile t - 1: wait for it, then scale this warp's half in place
+          okw = __all_sync(kFull, wait(&pv_done[(t - 1) % kSP], (uint32_t)((t - 1) / kSP) & 1u));
+          if (okw) {
+            tc::fence_after();
 #pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) {
-            uint32_t o[32];
-            tc::ld32(tmem + lanes + kColO + 32 * c4, o);
-            tc::wait_ld();
-            tc::reg_fence(o);
+            for (int c4 = 0; c4 < 2; ++c4) {
+              uint32_t o[32];
+              const uint32_t ta = tmem + lanes + kColO + 64u * kh + 32u * c4;
+              tc::ld32(ta, o);
+              tc::wait_ld();
+              tc::reg_fence(o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tc::st32(tmem + lanes + kColO + 32 * c4, o);
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tc::st32(ta, o);
+            }
           }
         }
         m_used = m_new;
       }
+      if (!okw) continue;   // the partner learns of it at the next exchange
       const float moff = m_used == -INFINITY ? 0.0f : m_used;
-      uint32_t hv[32], lv[32];
-      float lsum = 0.0f;
+      const float2 moff2 = make_float2(-moff, -moff);
+      uint32_t hv[16], lv[16];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float p0 = ex2(fmaf(sv[2 * i], qinv, -moff)), p1 = ex2(fmaf(sv[2 * i + 1], qinv, -moff));
-        lsum += p0 + p1;
-        const __half2 hi = __floats2half2_rn(p0, p1);
-        const float2 f = __half22float2(hi);
+      for (int i = 0; i < 16; ++i) {
+        const float2 x = f2fma(sv[i], qinv2, moff2);
+        const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+        l2 = f2add(l2, pp);
+        const __half2 hi = __floats2half2_rn(pp.x, pp.y);
+        const float2 lo = f2sub(pp, __half22float2(hi));
         hv[i] = h2u(hi);
-        lv[i] = h2u(__floats2half2_rn(p0 - f.x, p1 - f.y));
+        lv[i] = h2u(__floats2half2_rn(lo.x, lo.y));
       }
-      l += lsum;
-      tc::st32(tS, hv);        // P hi over the first S columns (already read)
-      tc::st32(tS + 32, lv);   // P lo
+      tc::st16(tS + 16 * kh, hv);        // P hi (keys 32kh..) over S columns both warps have read
+      tc::st16(tS + 32 + 16 * kh, lv);   // P lo
       tc::wait_st();
       tc::fence_before();
-      mbar_arrive(&p_full[b]);
+      mbar_arrive(&p_full[j]);
     }
-    if (ok) ok = __all_sync(kFull, wait(&pv_done[(T - 1) & 1], (uint32_t)((T - 1) >> 1) & 1u));
+    // row sums of the two halves (in the slots of parity T & 1, which no one
+    // reads after the last tile's exchange); O of this warp's 64 columns
+    const int e = (T & 1) * 2;
+    red_s[(e + kh) * kRows + row] = l2.x + l2.y;
+    bool ok = pair_and(1 + wq, okw);
+    const float l = red_s[(e + kh) * kRows + row] + red_s[(e + (kh ^ 1)) * kRows + row];
+    if (ok) ok = __all_sync(kFull, wait(&pv_done[(T - 1) % kSP], (uint32_t)((T - 1) / kSP) & 1u));
     tc::fence_after();
     const float inv = (ok && l > 0.0f) ? 1.0f / l : 0.0f;
 #pragma unroll
-    for (int c4 = 0; c4 < 4; ++c4) {
+    for (int c4 = 0; c4 < 2; ++c4) {
       uint32_t o[32];
       if (ok) {
-        tc::ld32(tmem + lanes + kColO + 32 * c4, o);
+        tc::ld32(tmem + lanes + kColO + 64u * kh + 32u * c4, o);
         tc::wait_ld();
         tc::reg_fence(o);
       } else {
@@ -408,27 +449,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         for (int i = 0; i < 32; ++i) o[i] = 0u;
       }
 #pragma unroll
-      for (int i = 0; i < 32; ++i) rows[row * kPitch + 32 * c4 + i] = __uint_as_float(o[i]) * inv;
+      for (int i = 0; i < 32; ++i) rows[row * kPitch + 64 * kh + 32 * c4 + i] = __uint_as_float(o[i]) * inv;
     }
-  } else if (warp < 8) {
+  } else if (tid >= kDequant0) {
     // ================================================================ dequantisation
-    const int dt = tid - 128, key = dt >> 1, half = dt & 1;
-    int waited = 0;   // thread 0: tiles whose copies it has seen land
-    bool ok = true;
-    for (int t = 0; t < T && ok; ++t) {
+    // lane -> (key, half): 8 consecutive lanes hold 8 consecutive keys, so a
+    // 16-byte store of 8 lanes covers the 32 banks once
+    const int dt = tid - kDequant0, key = (dt >> 5) * 16 + (dt & 15), half = (dt >> 4) & 1;
+    for (int t = 0; t < T; ++t) {
       const int s = t % kStages, b = t & 1;
-      if (dt == 0 && issued < T) {   // refill the stage tile t - 1 used
-        if (t >= 1) ok = wait(&raw_empty[issued % kStages], (uint32_t)((issued / kStages) - 1) & 1u);
-        if (ok) issue(issued++);
-      }
-      ok = ok && wait(&raw_full[s], (uint32_t)(t / kStages) & 1u);
-      if (dt == 0 && ok) waited = t + 1;
+      // a failed wait leaves at once, arriving nowhere: a stage is released
+      // (raw_empty) only once its copies have landed
+      if (!wait(&raw_full[s], (uint32_t)(t / kStages) & 1u)) break;
       const uint8_t* st = smem + kOffRaw + s * kRawBytes;
-      const uint64_t vm = ok ? stage_mask[s] : 0ull;
+      const uint64_t vm = stage_mask[s];
       const bool kv = (vm >> key) & 1ull;
       // ---- keys: exact integer codes, K-major: (key, d) at (key/8)*2048 + (d/8)*128 + (key%8)*16 + (d%8)*2
-      if (t >= 2) ok = ok && wait(&p_full[b], (uint32_t)((t - 2) >> 1) & 1u);
-      if (ok) {
+      if (t >= 2 && !wait(&s_full[(t - 2) % kSP], (uint32_t)((t - 2) / kSP) & 1u)) break;   // QK(t - 2) read the buffer
+      {
         const uint2* src = reinterpret_cast<const uint2*>(st + kRawK + key * kCB + half * 24);
         uint32_t w[7];
 #pragma unroll
@@ -455,14 +493,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         if (SB == 4) bits = *reinterpret_cast<const uint32_t*>(sp);
         else if (SB == 2) bits = *reinterpret_cast<const uint16_t*>(sp);
         else bits = *sp;
-        ks_s[(b * 2 + half) * kKeys + key] = kv ? decode_scale(bits, SCALE) : 0.0f;
-        if (dt == 0) key_mask[b] = vm;
+        ks_s[(s * kKeys + key) * 2 + half] = kv ? decode_scale(bits, SCALE) : 0.0f;
+        if (dt == 0) key_mask[s] = vm;
       }
       fence_proxy_async();
       mbar_arrive(&k_full[b]);
+      mbar_arrive(&ks_full[s]);
       // ---- values c * s_hi, c * s_lo, MN-major: (key, d) at (d/8)*1024 + (key/8)*128 + (key%8)*16 + (d%8)*2
-      if (t >= 2) ok = ok && wait(&pv_done[b], (uint32_t)((t - 2) >> 1) & 1u);
-      if (ok) {
+      if (t >= 2 && !wait(&pv_done[(t - 2) % kSP], (uint32_t)((t - 2) / kSP) & 1u)) break;
+      {
         const uint2* src = reinterpret_cast<const uint2*>(st + kRawV + key * kCB + half * 24);
         uint32_t w[7];
 #pragma unroll
@@ -505,50 +544,70 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       mbar_arrive(&v_full[b]);
       mbar_arrive(&raw_empty[s]);
     }
-    if (dt == 0) {   // no bulk copy may still target this CTA's shared memory at exit
-      for (int t = waited; t < issued; ++t)
-        mbar_wait(&raw_full[t % kStages], (uint32_t)(t / kStages) & 1u, kDrainPolls);
+  } else if (tid == kProducer) {
+    // ================================================================ bulk copies
+    int issued = 0;
+    bool ok = true;
+    for (int t = 0; t < T && ok; ++t) {
+      if (t >= kStages) ok = wait(&raw_empty[t % kStages], (uint32_t)(t / kStages - 1) & 1u);   // tile t - kStages consumed
+      if (ok && *abort_flag) ok = false;
+      if (ok) issue(t), issued = t + 1;
     }
+    // no bulk copy may still target this CTA's shared memory at exit: the
+    // last kStages tiles issued are the only ones that can be in flight
+    for (int t = max(0, issued - kStages); t < issued; ++t)
+      mbar_wait(&raw_full[t % kStages], (uint32_t)(t / kStages) & 1u, kDrainPolls);
   } else if (tid == kMmaThread) {
     // ================================================================ MMA issue
     constexpr uint32_t kIdQK = tc::idesc_f16(128, kKeys, false);
     constexpr uint32_t kIdPV = tc::idesc_f16(128, kD, true);
+    // descriptors (start addresses in 16-byte units in the low half)
+    const uint64_t dq = tc::sdesc(smem_u32(smem + kOffQ), 128u, 2048u);
+    const uint64_t dk = tc::sdesc(smem_u32(smem + kOffK), 128u, 2048u);
+    const uint64_t dv = tc::sdesc(smem_u32(smem + kOffV), 128u, 1024u);
+    const uint32_t dq_lo = (uint32_t)dq, dq_hi = (uint32_t)(dq >> 32);
+    const uint32_t dk_lo = (uint32_t)dk, dk_hi = (uint32_t)(dk >> 32);
+    const uint32_t dv_lo = (uint32_t)dv, dv_hi = (uint32_t)(dv >> 32);
     bool ok = true;
     for (int t = 0; t <= T && ok; ++t) {
       if (t < T) {   // S_b(t) = q1[block b] . c_k[block b], hi and lo halves of q1
-        const int b = t & 1;
+        const int b = t & 1, j = t % kSP;
         ok = wait(&k_full[b], (uint32_t)(t >> 1) & 1u);
-        if (ok && t >= 2) ok = wait(&pv_done[b], (uint32_t)((t - 2) >> 1) & 1u);   // P(t-2) consumed
+        if (ok && t >= kSP) ok = wait(&pv_done[j], (uint32_t)(t / kSP - 1) & 1u);   // P(t - kSP) consumed
         if (!ok) break;
         tc::fence_after();
-        const uint32_t kb = smem_u32(smem + kOffK + b * kTile);
-        const uint32_t dS = tmem + kColSP + 128u * b;
+        const uint32_t kb = dk_lo + (uint32_t)b * (kTile >> 4);
+        const uint32_t dS = tmem + kColSP + 128u * j;
 #pragma unroll
         for (int blk = 0; blk < 2; ++blk)
 #pragma unroll
           for (int part = 0; part < 2; ++part)
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              tc::mma_ts(dS + 64u * blk, tmem + kColQ + 64u * part + 32u * blk + 8u * ks,
-                         tc::sdesc(kb + (uint32_t)(blk * 8 + ks * 2) * 128u, 128u, 2048u), kIdQK,
-                         (part | ks) != 0);
-        tc::commit(&s_full[b]);
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint32_t al = dq_lo + (uint32_t)((part * 2 * kTile + (blk * 8 + ks * 2) * 128) / 16);
+              const uint32_t bl = kb + (uint32_t)((blk * 8 + ks * 2) * 128 / 16);
+              if (part == 0 && ks == 0) tc::mma_ss_c<false>(dS + 64u * blk, al, dq_hi, bl, dk_hi, kIdQK);
+              else tc::mma_ss_c<true>(dS + 64u * blk, al, dq_hi, bl, dk_hi, kIdQK);
+            }
+        tc::commit(&s_full[j]);
       }
       if (t >= 1) {   // O += P(t-1) V(t-1)
-        const int tp = t - 1, b = tp & 1;
-        ok = wait(&p_full[b], (uint32_t)(tp >> 1) & 1u) && wait(&v_full[b], (uint32_t)(tp >> 1) & 1u);
+        const int tp = t - 1, b = tp & 1, j = tp % kSP;
+        ok = wait(&p_full[j], (uint32_t)(tp / kSP) & 1u) && wait(&v_full[b], (uint32_t)(tp >> 1) & 1u);
         if (!ok) break;
         tc::fence_after();
-        const uint32_t vb = smem_u32(smem + kOffV + b * 2 * kTile);
-        const uint32_t aP = tmem + kColSP + 128u * b;
+        const uint32_t vb = dv_lo + (uint32_t)b * (2 * kTile >> 4);
+        const uint32_t aP = tmem + kColSP + 128u * j;
 #pragma unroll
         for (int pr = 0; pr < (kLo ? 3 : 2); ++pr)   // (p_hi, v_hi), (p_lo, v_hi), (p_hi, v_lo)
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            tc::mma_ts(tmem + kColO, aP + (pr == 1 ? 32u : 0u) + 8u * ks,
-                       tc::sdesc(vb + (pr == 2 ? (uint32_t)kTile : 0u) + (uint32_t)ks * 256u, 128u, 1024u), kIdPV,
-                       !(tp == 0 && pr == 0 && ks == 0));
-        tc::commit(&pv_done[b]);
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint32_t a = aP + (pr == 1 ? 32u : 0u) + 8u * ks;
+            const uint32_t bl = vb + (uint32_t)(((pr == 2 ? kTile : 0) + ks * 256) / 16);
+            if (tp == 0 && pr == 0 && ks == 0) tc::mma_ts_c<false>(tmem + kColO, a, bl, dv_hi, kIdPV);
+            else tc::mma_ts_c<true>(tmem + kColO, a, bl, dv_hi, kIdPV);
+          }
+        tc::commit(&pv_done[j]);
       }
     }
     tc::commit(drain);   // whatever was issued completes before TMEM is freed
@@ -576,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
-  if (warp == 8) tc::dealloc(tmem, kTmemCols);
+  if (warp == kMmaWarp) tc::dealloc(tmem, kTmemCols);
 }
 
 template <int SCALE>

@@ -47,29 +47,6 @@ struct ChunkParams {
   float2 mat2[kChunkMaxD / 8][16];  // SO(4) block matrices of blocks (i, i + d/8), row-major
 };
 
-typedef unsigned long long u64;
-__device__ __forceinline__ float2 f2add(float2 a, float2 b) {
-  u64 d, x = *reinterpret_cast<u64*>(&a), y = *reinterpret_cast<u64*>(&b);
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(x), "l"(y));
-  return *reinterpret_cast<float2*>(&d);
-}
-__device__ __forceinline__ float2 f2sub(float2 a, float2 b) {
-  u64 d, x = *reinterpret_cast<u64*>(&a), y = *reinterpret_cast<u64*>(&b);
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(x), "l"(y));
-  return *reinterpret_cast<float2*>(&d);
-}
-__device__ __forceinline__ float2 f2mul(float2 a, float2 b) {
-  u64 d, x = *reinterpret_cast<u64*>(&a), y = *reinterpret_cast<u64*>(&b);
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(x), "l"(y));
-  return *reinterpret_cast<float2*>(&d);
-}
-__device__ __forceinline__ float2 f2fma(float2 a, float2 b, float2 c) {
-  u64 d, x = *reinterpret_cast<u64*>(&a), y = *reinterpret_cast<u64*>(&b),
-         z = *reinterpret_cast<u64*>(&c);
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(x), "l"(y), "l"(z));
-  return *reinterpret_cast<float2*>(&d);
-}
-
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
   const int n = valid ? 16 : 0;  // 0 source bytes: the 16 bytes are zero-filled
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n)
