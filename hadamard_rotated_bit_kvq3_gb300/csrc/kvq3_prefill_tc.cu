@@ -27,7 +27,7 @@
 // the product; E4M3 scales have s_lo = 0 and skip the third MMA).  Dequantised
 // values must lie in the fp16 range, as for every kernel of this library.
 //
-// Roles (14 warps):
+// Roles (15 warps):
 //  * warps 6-13, softmax: warps w and w + 4 share the 32 rows of TMEM lane
 //    quarter w % 4 (thread = row), each taking 32 of a tile's 64 keys; they trade
 //    row maxima through shared memory at a 64-thread named barrier that also
@@ -37,7 +37,8 @@
 //  * warps 2-5, dequantisation: thread = (key, half of the dimensions); a tile
 //    is unpacked into the MMA layouts in shared memory: integer key codes
 //    K-major, values c*s_hi and c*s_lo MN-major;
-//  * warp 0, lane 0: issues QK^T of tile t, then PV of tile t - 1;
+//  * warp 0, lane 0: issues QK^T; warp 14, lane 0: issues PV -- two streams,
+//    so that a wait of one never holds up the other's MMAs;
 //  * warp 1, lane 0: issues the bulk copies of packed codes and scales into a
 //    ring of raw stages, up to kStages tiles ahead.
 // TMEM: q1 hi / lo (128 columns), two S/P buffers (128 each), O (128).
@@ -58,12 +59,13 @@ constexpr int kKeys = 64;             // keys per tile
 constexpr int kD = 128;               // head dimension
 constexpr int kCB = 3 * kD / 8;       // code bytes per vector (48)
 constexpr int kStages = 4;            // raw stages in flight
-constexpr int kThreads = 14 * 32;
-constexpr int kMmaWarp = 0;           // the two one-thread roles take the lowest warps,
-constexpr int kMmaThread = 0;         // which the schedulers favour
-constexpr int kProducer = 32;
+constexpr int kThreads = 15 * 32;
+constexpr int kMmaWarp = 0;           // QK^T issue (lane 0) and the TMEM allocation
+constexpr int kMmaThread = 0;
+constexpr int kProducer = 32;         // warp 1, lane 0
 constexpr int kDequant0 = 2 * 32;     // warps 2-5
 constexpr int kSoftmax0 = 6;          // warps 6-13
+constexpr int kPvThread = 14 * 32;    // warp 14, lane 0: PV issue
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSP = 3;                // S/P buffers in TMEM
 constexpr uint32_t kColSP = 0, kColO = 384;   // TMEM: S/P buffer j at 128 j, O
@@ -83,7 +85,7 @@ constexpr int kOffRed = kOffKs + kStages * kKeys * 2 * 4;      // [2][2][128] fp
 constexpr int kPitch = kD + 1;                                 // row staging pitch (floats)
 constexpr int kOffRows = kOffK;                                // [128][129] fp32 outputs over the K/V tiles
 constexpr int kOffQinv = kOffRed + 2 * 2 * kRows * 4;          // [128] fp32
-constexpr int kNumBars = 3 * kStages + 4 + 3 * kSP + 1;
+constexpr int kNumBars = 3 * kStages + 4 + 3 * kSP + 2;
 static_assert(kRows * kPitch * 4 <= kOffQ - kOffK, "output staging fits over the K/V tiles");
 constexpr int kOffBars = kOffQinv + kRows * 4;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;              // TMEM base, abort flag, masks
@@ -165,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   uint64_t* s_full = v_full + 2;               // [kSP] S of the tile in TMEM
   uint64_t* p_full = s_full + kSP;             // [kSP] P of the tile in TMEM (and O rescaled)
   uint64_t* pv_done = p_full + kSP;            // [kSP] PV of the tile complete
-  uint64_t* drain = pv_done + kSP;             // every MMA complete
+  uint64_t* drain = pv_done + kSP;             // [2] every MMA of an issuer complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   uint64_t* stage_mask = reinterpret_cast<uint64_t*>(smem + kOffMisc + 16);   // [kStages] valid keys
@@ -199,7 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       mbar_init(&p_full[j], 256);
       mbar_init(&pv_done[j], 1);
     }
-    mbar_init(drain, 1);
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -221,11 +224,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   };
 
   // bulk copies of tile t (16-key groups; a page holds whole groups since P
-  // is a multiple of 16) into its raw stage; producer thread only.  Positions
-  // are below 2^31 (checked on the host): 32-bit page arithmetic.
+  // is a multiple of 16) into its raw stage; producer thread only.  Key 64 t
+  // sits at slot slot0 of logical page lp0 (tracked by the caller from tile
+  // to tile: no division); positions are below 2^31 (checked on the host).
   const int64_t pool_bytes = g.num_pages * g.page_bytes;
   (void)pool_bytes;   // read by the checked build only
-  auto issue = [&](int t) {
+  auto issue = [&](int t, uint32_t lp0, uint32_t slot0) {
     const int s = t % kStages;
     uint8_t* st = smem + kOffRaw + s * kRawBytes;
     const uint32_t k0 = (uint32_t)t * kKeys, P = (uint32_t)g.page_size, last = (uint32_t)kmax;
@@ -233,14 +237,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     uint32_t slot[4];
     uint64_t mask = 0;
     uint32_t bytes = 0;
+    uint32_t lp = lp0, sl = slot0;
 #pragma unroll
     for (int gi = 0; gi < 4; ++gi) {
+      if (gi > 0 && (sl += 16u) == P) {   // the next 16-key group starts a page
+        sl = 0u;
+        ++lp;
+      }
       const uint32_t pos = k0 + 16u * gi;
       pg[gi] = -1;
-      slot[gi] = 0;
+      slot[gi] = sl;
       if (pos > last) continue;
-      const uint32_t lp = pos / P;
-      slot[gi] = pos - lp * P;
       pg[gi] = page_of(g, p.page_table, p.seq, lp);
       if (pg[gi] < 0) {
         set_status(p.status, KVQ3_DEV_BAD_PAGE);
@@ -326,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   fence_proxy_async();   // generic stores read by the tensor cores
   __syncthreads();
 
-  if (warp >= kSoftmax0) {
+  if (warp >= kSoftmax0 && warp < kSoftmax0 + 8) {
     // ================================================================ softmax
     const int wq = warp & 3, kh = (warp - kSoftmax0) >> 2;   // lane quarter; key half (keys 32kh .. 32kh + 31)
     const int row = 32 * wq + lane;
@@ -451,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 #pragma unroll
       for (int i = 0; i < 32; ++i) rows[row * kPitch + 64 * kh + 32 * c4 + i] = __uint_as_float(o[i]) * inv;
     }
-  } else if (tid >= kDequant0) {
+  } else if (tid >= kDequant0 && tid < kDequant0 + 128) {
     // ================================================================ dequantisation
     // lane -> (key, half): 8 consecutive lanes hold 8 consecutive keys, so a
     // 16-byte store of 8 lanes covers the 32 banks once
@@ -548,70 +555,71 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     // ================================================================ bulk copies
     int issued = 0;
     bool ok = true;
+    uint32_t lp = 0, slot = 0;   // key 64 t = lp * P + slot
     for (int t = 0; t < T && ok; ++t) {
       if (t >= kStages) ok = wait(&raw_empty[t % kStages], (uint32_t)(t / kStages - 1) & 1u);   // tile t - kStages consumed
       if (ok && *abort_flag) ok = false;
-      if (ok) issue(t), issued = t + 1;
+      if (ok) issue(t, lp, slot), issued = t + 1;
+      for (slot += kKeys; slot >= (uint32_t)g.page_size; slot -= (uint32_t)g.page_size) ++lp;
     }
     // no bulk copy may still target this CTA's shared memory at exit: the
     // last kStages tiles issued are the only ones that can be in flight
     for (int t = max(0, issued - kStages); t < issued; ++t)
       mbar_wait(&raw_full[t % kStages], (uint32_t)(t / kStages) & 1u, kDrainPolls);
   } else if (tid == kMmaThread) {
-    // ================================================================ MMA issue
+    // ================================================================ QK^T issue
     constexpr uint32_t kIdQK = tc::idesc_f16(128, kKeys, false);
-    constexpr uint32_t kIdPV = tc::idesc_f16(128, kD, true);
     // descriptors (start addresses in 16-byte units in the low half)
     const uint64_t dq = tc::sdesc(smem_u32(smem + kOffQ), 128u, 2048u);
     const uint64_t dk = tc::sdesc(smem_u32(smem + kOffK), 128u, 2048u);
-    const uint64_t dv = tc::sdesc(smem_u32(smem + kOffV), 128u, 1024u);
     const uint32_t dq_lo = (uint32_t)dq, dq_hi = (uint32_t)(dq >> 32);
     const uint32_t dk_lo = (uint32_t)dk, dk_hi = (uint32_t)(dk >> 32);
-    const uint32_t dv_lo = (uint32_t)dv, dv_hi = (uint32_t)(dv >> 32);
-    bool ok = true;
-    for (int t = 0; t <= T && ok; ++t) {
-      if (t < T) {   // S_b(t) = q1[block b] . c_k[block b], hi and lo halves of q1
-        const int b = t & 1, j = t % kSP;
-        ok = wait(&k_full[b], (uint32_t)(t >> 1) & 1u);
-        if (ok && t >= kSP) ok = wait(&pv_done[j], (uint32_t)(t / kSP - 1) & 1u);   // P(t - kSP) consumed
-        if (!ok) break;
-        tc::fence_after();
-        const uint32_t kb = dk_lo + (uint32_t)b * (kTile >> 4);
-        const uint32_t dS = tmem + kColSP + 128u * j;
+    for (int t = 0; t < T; ++t) {   // S_b(t) = q1[block b] . c_k[block b], hi and lo halves of q1
+      const int b = t & 1, j = t % kSP;
+      if (!wait(&k_full[b], (uint32_t)(t >> 1) & 1u)) break;
+      if (t >= kSP && !wait(&pv_done[j], (uint32_t)(t / kSP - 1) & 1u)) break;   // P(t - kSP) consumed
+      tc::fence_after();
+      const uint32_t kb = dk_lo + (uint32_t)b * (kTile >> 4);
+      const uint32_t dS = tmem + kColSP + 128u * j;
 #pragma unroll
-        for (int blk = 0; blk < 2; ++blk)
+      for (int blk = 0; blk < 2; ++blk)
 #pragma unroll
-          for (int part = 0; part < 2; ++part)
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-              const uint32_t al = dq_lo + (uint32_t)((part * 2 * kTile + (blk * 8 + ks * 2) * 128) / 16);
-              const uint32_t bl = kb + (uint32_t)((blk * 8 + ks * 2) * 128 / 16);
-              if (part == 0 && ks == 0) tc::mma_ss_c<false>(dS + 64u * blk, al, dq_hi, bl, dk_hi, kIdQK);
-              else tc::mma_ss_c<true>(dS + 64u * blk, al, dq_hi, bl, dk_hi, kIdQK);
-            }
-        tc::commit(&s_full[j]);
-      }
-      if (t >= 1) {   // O += P(t-1) V(t-1)
-        const int tp = t - 1, b = tp & 1, j = tp % kSP;
-        ok = wait(&p_full[j], (uint32_t)(tp / kSP) & 1u) && wait(&v_full[b], (uint32_t)(tp >> 1) & 1u);
-        if (!ok) break;
-        tc::fence_after();
-        const uint32_t vb = dv_lo + (uint32_t)b * (2 * kTile >> 4);
-        const uint32_t aP = tmem + kColSP + 128u * j;
-#pragma unroll
-        for (int pr = 0; pr < (kLo ? 3 : 2); ++pr)   // (p_hi, v_hi), (p_lo, v_hi), (p_hi, v_lo)
+        for (int part = 0; part < 2; ++part)
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
-            const uint32_t a = aP + (pr == 1 ? 32u : 0u) + 8u * ks;
-            const uint32_t bl = vb + (uint32_t)(((pr == 2 ? kTile : 0) + ks * 256) / 16);
-            if (tp == 0 && pr == 0 && ks == 0) tc::mma_ts_c<false>(tmem + kColO, a, bl, dv_hi, kIdPV);
-            else tc::mma_ts_c<true>(tmem + kColO, a, bl, dv_hi, kIdPV);
+            const uint32_t al = dq_lo + (uint32_t)((part * 2 * kTile + (blk * 8 + ks * 2) * 128) / 16);
+            const uint32_t bl = kb + (uint32_t)((blk * 8 + ks * 2) * 128 / 16);
+            if (part == 0 && ks == 0) tc::mma_ss_c<false>(dS + 64u * blk, al, dq_hi, bl, dk_hi, kIdQK);
+            else tc::mma_ss_c<true>(dS + 64u * blk, al, dq_hi, bl, dk_hi, kIdQK);
           }
-        tc::commit(&pv_done[j]);
-      }
+      tc::commit(&s_full[j]);
     }
-    tc::commit(drain);   // whatever was issued completes before TMEM is freed
-    mbar_wait(drain, 0u, kDrainPolls);
+    tc::commit(&drain[0]);   // whatever was issued completes before TMEM is freed
+    mbar_wait(&drain[0], 0u, kDrainPolls);
+  } else if (tid == kPvThread) {
+    // ================================================================ PV issue
+    constexpr uint32_t kIdPV = tc::idesc_f16(128, kD, true);
+    const uint64_t dv = tc::sdesc(smem_u32(smem + kOffV), 128u, 1024u);
+    const uint32_t dv_lo = (uint32_t)dv, dv_hi = (uint32_t)(dv >> 32);
+    for (int t = 0; t < T; ++t) {   // O += P(t) V(t)
+      const int b = t & 1, j = t % kSP;
+      if (!wait(&p_full[j], (uint32_t)(t / kSP) & 1u) || !wait(&v_full[b], (uint32_t)(t >> 1) & 1u)) break;
+      tc::fence_after();
+      const uint32_t vb = dv_lo + (uint32_t)b * (2 * kTile >> 4);
+      const uint32_t aP = tmem + kColSP + 128u * j;
+#pragma unroll
+      for (int pr = 0; pr < (kLo ? 3 : 2); ++pr)   // (p_hi, v_hi), (p_lo, v_hi), (p_hi, v_lo)
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint32_t a = aP + (pr == 1 ? 32u : 0u) + 8u * ks;
+          const uint32_t bl = vb + (uint32_t)(((pr == 2 ? kTile : 0) + ks * 256) / 16);
+          if (t == 0 && pr == 0 && ks == 0) tc::mma_ts_c<false>(tmem + kColO, a, bl, dv_hi, kIdPV);
+          else tc::mma_ts_c<true>(tmem + kColO, a, bl, dv_hi, kIdPV);
+        }
+      tc::commit(&pv_done[j]);
+    }
+    tc::commit(&drain[1]);
+    mbar_wait(&drain[1], 0u, kDrainPolls);
   }
   __syncthreads();
 
