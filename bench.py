@@ -83,11 +83,25 @@ def workload_lens(w: I.Workload) -> np.ndarray:
     return np.full(w.batch, w.seq_len, np.int32)
 
 
-def source_hash() -> str:
+# the source files each profiled kernel is built from (headers included)
+KERNEL_SOURCES = {
+    "decode": ("kvq3_decode.cuh", "kvq3_decode.cu", "kvq3_decode_d*.cu"),
+    "write_chunk": ("kvq3_write_chunk.cu",),
+    "prefill_tc": ("kvq3_prefill_tc.cu", "kvq3_tc.cuh"),
+}
+
+
+def source_hash(kernel: str) -> str:
+    """Hash of the sources of `kernel`: its own files, the shared device and
+    internal headers and the public header."""
+    import fnmatch
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "hadamard_rotated_bit_kvq3_gb300", "csrc")
+    pats = KERNEL_SOURCES[kernel] + ("kvq3_common.cuh", "kvq3_internal.h")
     for f in sorted(os.listdir(csrc)):
-        h.update(open(os.path.join(csrc, f), "rb").read())
+        if any(fnmatch.fnmatch(f, pt) for pt in pats):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    h.update(open(os.path.join(ROOT, "include", "kvq3.h"), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -95,8 +109,8 @@ def load_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return dict(hbm=float(d["hbm_gbs"]), src="measured")
-    return dict(hbm=6800.0, src="fallback")
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d.get("bf16_tflops", 1900.0)), src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, src="fallback")
 
 
 class ClockSampler:
@@ -412,7 +426,7 @@ DECODE_METRIC = "decode tokens/s (one layer, all heads)"
 WRITE_METRIC = "write-path GB/s (fp16 in + packed out)"
 PREFILL_ATTN_METRIC = "prefill-attention query tokens/s (one layer, all heads)"
 PRIMARY = "ragged"                                 # the largest single-GPU decode workload
-EXTRAS = ("long70b", "llama8b", "prefill")         # measured in the same run, under "configs"
+EXTRAS = ("long70b", "llama8b", "prefill", "prefill_attn")   # measured in the same run, under "configs"
 NOMINAL_HBM_GBS = 8000.0                           # the HBM peak the method's target is quoted against
 
 
@@ -456,7 +470,8 @@ def recorded_traffic_of(kernel: str, name: str):
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
-    return d["dram_bytes_per_launch"] if d.get("source_hash") == source_hash() else None
+    fam = "decode" if kernel.startswith("decode") else kernel
+    return d["dram_bytes_per_launch"] if d.get("source_hash") == source_hash(fam) else None
 
 
 def _median(xs):
@@ -692,6 +707,8 @@ def run_suite(args, world, rank, dev):
         for name in names:
             if name == "prefill":
                 records[name] = prefill_record(args, world, rank, dev, peaks, False)
+            elif name == "prefill_attn":
+                records[name] = prefill_attn_record(args, world, rank, dev, peaks)
             else:
                 records[name] = decode_record(name, args, world, rank, dev, peaks, False)
             torch.cuda.synchronize()
@@ -708,6 +725,8 @@ def run_suite(args, world, rank, dev):
                     oracle_write_sample(w, n_tok), lambda per, nb=nb: nb / per / 1e9, "GB/s",
                     f"oracle write of {n_tok} tokens x {w.num_kv_heads} kv heads, K and V",
                     budget_s=10.0 if name != names[0] else 15.0)
+            elif name == "prefill_attn":
+                records[name]["cpu_baseline"] = prefill_attn_cpu_baseline(w, budget_s=10.0)
             else:
                 if args.batch:
                     import dataclasses
@@ -738,6 +757,12 @@ def profile_steps(name, args, rank, dev):
     import torch
     if name == "prefill":
         st = PrefillWorkload(dev, args.tokens)
+    elif name == "prefill_attn":
+        import dataclasses
+        w = workload(name)
+        if args.tokens:
+            w = dataclasses.replace(w, seq_len=args.tokens, chunk=min(w.chunk, max(1, args.tokens // 4)))
+        st = PrefillAttnWorkload(dev, w)
     else:
         st = GpuWorkload(name, dev, rank, args.batch)
     for _ in range(args.warmup + args.steps):
@@ -860,11 +885,14 @@ class PrefillAttnWorkload:
         return 4.0 * w.d * w.num_q_heads * keys
 
 
-def run_prefill_attn(args, world, rank, dev):
+def prefill_attn_record(args, world: int, rank: int, dev, peaks: dict) -> dict:
+    """The prefill-attention workload: device-timed steps (queries and cache
+    resident), then the same step with the fp16 queries copied from pinned
+    host memory and the fp32 outputs read back inside the timed region."""
     import dataclasses
 
     import torch
-    w = workload(args.workload)
+    w = workload("prefill_attn")
     if args.tokens:   # a shorter context (profiling): the chunk is at most a quarter of it
         w = dataclasses.replace(w, seq_len=args.tokens, chunk=min(w.chunk, max(1, args.tokens // 4)))
     st = PrefillAttnWorkload(dev, w)
@@ -873,52 +901,103 @@ def run_prefill_attn(args, world, rank, dev):
         st.step()
     torch.cuda.synchronize()
     assert int(st.status.item()) == 0
-    if args.profile:
-        for _ in range(args.steps):
-            st.step()
-        torch.cuda.synchronize()
-        print(json.dumps({"profile": w.name, "status": int(st.status.item())}))
-        return
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier(world)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(dev.index or 0) as clk:
-        a.record(stream)
-        for _ in range(args.steps):
-            st.step()
-        b.record(stream)
-        torch.cuda.synchronize()
-    ms = max_over_ranks(a.elapsed_time(b), world) / args.steps
+    a.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        st.step()
+        ev[i][1].record(stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
     assert int(st.status.item()) == 0
-    pk = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
-        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
-    peak = float(pk.get("bf16_tflops", 1900.0))
-    tflops = st.flops() / (ms * 1e-3) / 1e12
+    ms = max_over_ranks(a.elapsed_time(b), world) / args.steps
+    med = _median([x.elapsed_time(y) for x, y in ev])
+    tflops = st.flops() / (med * 1e-3) / 1e12
+    # end to end: queries from pinned host memory, outputs back
+    q_h = st.q.cpu().pin_memory()
+    out_h = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+
+    def e2e_step():
+        st.q.copy_(q_h, non_blocking=True)
+        st.step()
+        out_h.copy_(st.out, non_blocking=True)
+
+    for _ in range(min(args.warmup, 3)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    a.record(stream)
+    n_e2e = max(3, min(args.steps, 20))
+    for _ in range(n_e2e):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(a.elapsed_time(b), world) / n_e2e
     # d = 128 with 3-bit symmetric codes runs a tile kernel (one launch): the
     # tcgen05 one with blocks of 64, the mma.sync one with blocks of 32; the
     # other formats the decode kernel's prefill variant and the combine
     tile = w.d == 128 and w.bits == 3 and w.scale != "e4m3zp"
     tile_kernel = "prefill_tc_kernel" if w.block == 64 else "prefill_tile_kernel"
+    rec = {
+        "metric": PREFILL_ATTN_METRIC, "value": whole_job_rate(w.chunk, world, ms), "unit": "tokens/s",
+        "ms_per_step": ms, "ms_per_step_median": med,
+        "dtype": f"f16 mma / f32 accumulate ({w.bits}-bit packed cache)",
+        "config": workload_config(w, None, world),
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16"], "unit": "TFLOP/s",
+                     "frac": tflops / peaks["bf16"], "traffic": None,
+                     "flops": st.flops(),
+                     "kernel": "kvq3_prefill_attn (" + (tile_kernel if tile else
+                               "decode_split_kernel<..., prefill> + decode_combine_kernel") + ")",
+                     "timing": "median over steps of CUDA events around the kvq3_prefill_attn call",
+                     "peak_source": ("measured bf16 (fp16 MMAs have the same nominal rate)"
+                                     if peaks["src"] == "measured" else "fallback")},
+        "e2e": {"value": whole_job_rate(w.chunk, world, e2e_ms), "unit": "tokens/s",
+                "h2d_bytes_per_step": q_h.numel() * q_h.element_size(),
+                "d2h_bytes_per_step": out_h.numel() * out_h.element_size(), "steps": n_e2e},
+        "gpu_launches": (1 if tile else 2) * args.steps,
+    }
+    del st
+    torch.cuda.empty_cache()
+    return rec
+
+
+def prefill_attn_cpu_baseline(w: I.Workload, budget_s: float = 15.0) -> dict:
+    return timed_cpu_baseline(oracle_prefill_sample(w, 1), lambda per: 1.0 / per, "tokens/s",
+                              f"oracle prefill attention of the chunk's last query (all {w.num_q_heads} "
+                              f"heads) over the {w.seq_len}-token cache (cache written once, untimed)",
+                              budget_s=budget_s)
+
+
+def run_prefill_attn(args, world, rank, dev):
+    import torch
+    if args.profile:
+        import dataclasses
+        w = workload(args.workload)
+        if args.tokens:
+            w = dataclasses.replace(w, seq_len=args.tokens, chunk=min(w.chunk, max(1, args.tokens // 4)))
+        st = PrefillAttnWorkload(dev, w)
+        for _ in range(args.warmup + args.steps):
+            st.step()
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": w.name, "status": int(st.status.item())}))
+        return
+    peaks = load_peaks()
+    with ClockSampler(dev.index or 0) as clk:
+        rec = prefill_attn_record(args, world, rank, dev, peaks)
     if rank == 0:
-        cpu = None
+        line = {"metric": rec["metric"], "value": rec["value"], "unit": rec["unit"], "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": rec["ms_per_step"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": rec["dtype"],
+                "data": "synthetic", "config": rec["config"]}
+        for key in ("ms_per_step_median", "roofline", "e2e", "gpu_launches"):
+            line[key] = rec[key]
+        line["clocks"] = clk.summary()
         if not args.no_cpu_baseline and world == 1:
-            cpu = timed_cpu_baseline(oracle_prefill_sample(w, 1), lambda per: 1.0 / per, "tokens/s",
-                                     f"oracle prefill attention of the chunk's last query (all {w.num_q_heads} "
-                                     f"heads) over the {w.seq_len}-token cache (cache written once, untimed)")
-        print(json.dumps({
-            "metric": "prefill-attention query tokens/s (one layer, all heads)",
-            "value": whole_job_rate(w.chunk, world, ms), "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": f"f16 mma / f32 accumulate ({w.bits}-bit packed cache)",
-            "data": "synthetic",
-            "config": workload_config(w, None, world),
-            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
-                         "frac": tflops / peak, "traffic": None,
-                         "kernel": "kvq3_prefill_attn (" + (tile_kernel if tile else
-                                   "decode_split_kernel<..., prefill> + decode_combine_kernel") + ")",
-                         "peak_source": "measured bf16 (fp16 mma has the same nominal rate)"
-                         if pk else "fallback"},
-            "gpu_launches": (1 if tile else 2) * args.steps, "clocks": clk.summary(),
-            **({"cpu_baseline": cpu} if cpu else {})}))
+            line["cpu_baseline"] = prefill_attn_cpu_baseline(workload(args.workload))
+        print(json.dumps(line))
 
 
 def workload_desc(w: I.Workload) -> str:

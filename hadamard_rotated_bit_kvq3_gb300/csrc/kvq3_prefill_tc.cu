@@ -474,26 +474,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       // ---- keys: exact integer codes, K-major: (key, d) at (key/8)*2048 + (d/8)*128 + (key%8)*16 + (d%8)*2
       if (t >= 2 && !wait(&s_full[(t - 2) % kSP], (uint32_t)((t - 2) / kSP) & 1u)) break;   // QK(t - 2) read the buffer
       {
-        const uint2* src = reinterpret_cast<const uint2*>(st + kRawK + key * kCB + half * 24);
-        uint32_t w[7];
+        // the lane's 64 codes as two runs of 96 bits (32 codes, 4 groups of 8);
+        // the run loop is not unrolled, to keep the roles' code small
+        uint8_t* kt = smem + kOffK + b * kTile + (key >> 3) * 2048 + (key & 7) * 16 + 8 * half * 128;
+#pragma unroll 1
+        for (int r = 0; r < 2; ++r) {
+          const uint32_t* src = reinterpret_cast<const uint32_t*>(st + kRawK + key * kCB + half * 24 + 12 * r);
+          const uint32_t w[4] = {src[0], src[1], src[2], 0u};
 #pragma unroll
-        for (int i = 0; i < 3; ++i) {
-          const uint2 u = src[i];
-          w[2 * i] = u.x;
-          w[2 * i + 1] = u.y;
-        }
-        w[6] = 0u;
-        uint8_t* kt = smem + kOffK + b * kTile + (key >> 3) * 2048 + (key & 7) * 16;
-#pragma unroll
-        for (int gq = 0; gq < 8; ++gq) {
-          const int bit = 24 * gq;
-          const uint32_t w24 = __funnelshift_r(w[bit >> 5], w[(bit >> 5) + 1], bit & 31);
-          uint4 o;
-          o.x = h2u(codes2(w24));
-          o.y = h2u(codes2(w24 >> 6));
-          o.z = h2u(codes2(w24 >> 12));
-          o.w = h2u(codes2(w24 >> 18));
-          *reinterpret_cast<uint4*>(kt + (8 * half + gq) * 128) = o;
+          for (int gq = 0; gq < 4; ++gq) {
+            const int bit = 24 * gq;
+            const uint32_t w24 = __funnelshift_r(w[bit >> 5], w[(bit >> 5) + 1], bit & 31);
+            uint4 o;
+            o.x = h2u(codes2(w24));
+            o.y = h2u(codes2(w24 >> 6));
+            o.z = h2u(codes2(w24 >> 12));
+            o.w = h2u(codes2(w24 >> 18));
+            *reinterpret_cast<uint4*>(kt + (4 * r + gq) * 128) = o;
+          }
         }
         uint32_t bits;
         const uint8_t* sp = st + kRawKs + (key * 2 + half) * SB;
@@ -509,15 +507,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       // ---- values c * s_hi, c * s_lo, MN-major: (key, d) at (d/8)*1024 + (key/8)*128 + (key%8)*16 + (d%8)*2
       if (t >= 2 && !wait(&pv_done[(t - 2) % kSP], (uint32_t)((t - 2) / kSP) & 1u)) break;
       {
-        const uint2* src = reinterpret_cast<const uint2*>(st + kRawV + key * kCB + half * 24);
-        uint32_t w[7];
-#pragma unroll
-        for (int i = 0; i < 3; ++i) {
-          const uint2 u = src[i];
-          w[2 * i] = u.x;
-          w[2 * i + 1] = u.y;
-        }
-        w[6] = 0u;
         uint32_t bits;
         const uint8_t* sp = st + kRawVs + (key * 2 + half) * SB;
         if (SB == 4) bits = *reinterpret_cast<const uint32_t*>(sp);
@@ -526,24 +515,29 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         const float sv = kv ? decode_scale(bits, SCALE) : 0.0f;
         const float s_hi = __uint_as_float(__float_as_uint(sv) & 0xFFFF8000u);   // top 9 significant bits
         const __half2 hs = __float2half2_rn(s_hi), ls = __float2half2_rn(sv - s_hi);
-        uint8_t* vt = smem + kOffV + b * 2 * kTile + (key >> 3) * 128 + (key & 7) * 16;
+        uint8_t* vt = smem + kOffV + b * 2 * kTile + (key >> 3) * 128 + (key & 7) * 16 + 8 * half * 1024;
+#pragma unroll 1
+        for (int r = 0; r < 2; ++r) {
+          const uint32_t* src = reinterpret_cast<const uint32_t*>(st + kRawV + key * kCB + half * 24 + 12 * r);
+          const uint32_t w[4] = {src[0], src[1], src[2], 0u};
 #pragma unroll
-        for (int gq = 0; gq < 8; ++gq) {
-          const int bit = 24 * gq;
-          const uint32_t w24 = __funnelshift_r(w[bit >> 5], w[(bit >> 5) + 1], bit & 31);
-          const __half2 c0 = codes2(w24), c1 = codes2(w24 >> 6), c2 = codes2(w24 >> 12), c3 = codes2(w24 >> 18);
-          uint4 o;
-          o.x = h2u(__hmul2(c0, hs));
-          o.y = h2u(__hmul2(c1, hs));
-          o.z = h2u(__hmul2(c2, hs));
-          o.w = h2u(__hmul2(c3, hs));
-          *reinterpret_cast<uint4*>(vt + (8 * half + gq) * 1024) = o;
-          if (kLo) {
-            o.x = h2u(__hmul2(c0, ls));
-            o.y = h2u(__hmul2(c1, ls));
-            o.z = h2u(__hmul2(c2, ls));
-            o.w = h2u(__hmul2(c3, ls));
-            *reinterpret_cast<uint4*>(vt + kTile + (8 * half + gq) * 1024) = o;
+          for (int gq = 0; gq < 4; ++gq) {
+            const int bit = 24 * gq;
+            const uint32_t w24 = __funnelshift_r(w[bit >> 5], w[(bit >> 5) + 1], bit & 31);
+            const __half2 c0 = codes2(w24), c1 = codes2(w24 >> 6), c2 = codes2(w24 >> 12), c3 = codes2(w24 >> 18);
+            uint4 o;
+            o.x = h2u(__hmul2(c0, hs));
+            o.y = h2u(__hmul2(c1, hs));
+            o.z = h2u(__hmul2(c2, hs));
+            o.w = h2u(__hmul2(c3, hs));
+            *reinterpret_cast<uint4*>(vt + (4 * r + gq) * 1024) = o;
+            if (kLo) {
+              o.x = h2u(__hmul2(c0, ls));
+              o.y = h2u(__hmul2(c1, ls));
+              o.z = h2u(__hmul2(c2, ls));
+              o.w = h2u(__hmul2(c3, ls));
+              *reinterpret_cast<uint4*>(vt + kTile + (4 * r + gq) * 1024) = o;
+            }
           }
         }
       }

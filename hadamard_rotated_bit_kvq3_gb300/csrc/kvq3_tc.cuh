@@ -48,18 +48,10 @@ __device__ __forceinline__ void fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D (TMEM) = A (TMEM) x B (shared-memory descriptor) [+ D when acc].
-__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, bool acc) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
-      "r"(a), "l"(b), "r"(idesc), "r"((uint32_t)acc)
-      : "memory");
-}
-
-// As mma_ts with the accumulate flag fixed at compile time; the descriptor
-// comes as its two 32-bit halves (callers step the start address, bits 0-13
-// of the low half, by plain adds: shared-memory addresses stay below 2^18).
+// D (TMEM) = A (TMEM) x B (shared-memory descriptor) [+ D when ACC], the
+// accumulate flag fixed at compile time.  The descriptor comes as its two
+// 32-bit halves: callers step the start address (bits 0-13 of the low half)
+// by plain adds, as shared-memory addresses stay below 2^18.
 template <bool ACC>
 __device__ __forceinline__ void mma_ts_c(uint32_t d, uint32_t a, uint32_t b_lo, uint32_t b_hi, uint32_t idesc) {
   asm volatile(
