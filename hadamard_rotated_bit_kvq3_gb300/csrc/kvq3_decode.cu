@@ -2,6 +2,8 @@
 #include <math.h>
 #include <string.h>
 
+#include <algorithm>
+
 #include <mutex>
 
 #include "kvq3_decode.cuh"
@@ -143,6 +145,10 @@ kvq3_status kvq3_prefill_workspace_size(const kvq3_cache_desc* desc, int32_t num
   DecodePlan plan;
   if ((s = prefill_plan_for(vg, gcols, &plan)) != KVQ3_OK) return s;
   *bytes = plan.ws_bytes;
+  CacheGeom g;
+  make_geom(desc, &g);
+  if (prefill_tc_supported(g, num_q_heads))   // the tcgen05 path: split units' partials
+    *bytes = std::max(*bytes, prefill_tc_workspace(g, num_q_heads, n_q));
   return KVQ3_OK;
 }
 
@@ -178,8 +184,8 @@ static kvq3_status prefill_attn_impl(kvq3_rotation rot, const kvq3_cache_desc* d
     CacheGeom g;
     make_geom(desc, &g);
     if (prefill_tc_supported(g, num_q_heads))
-      return prefill_tc(g, cache, seq, pos0, n_q, q, num_q_heads, (float)qks, out, dev_status, rot->params,
-                        wait_limit, static_cast<cudaStream_t>(stream));
+      return prefill_tc(g, cache, seq, pos0, n_q, q, num_q_heads, (float)qks, out, workspace, ws_bytes,
+                        dev_status, rot->params, wait_limit, static_cast<cudaStream_t>(stream));
     return prefill_tiles(g, cache, seq, pos0, n_q, q, num_q_heads, (float)qks, out, dev_status,
                          rot->params, static_cast<cudaStream_t>(stream));
   }

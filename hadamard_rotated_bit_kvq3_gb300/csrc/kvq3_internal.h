@@ -35,9 +35,10 @@ constexpr uint32_t kWaitPolls = 1u << 22;
 // tcgen05 path of kvq3_prefill_attn: d = 128, 3-bit symmetric codes, blocks
 // of 64, at most 128 query heads per kv head (arguments already checked).
 bool prefill_tc_supported(const CacheGeom& g, int32_t hq);
+size_t prefill_tc_workspace(const CacheGeom& g, int32_t hq, int64_t n_q);
 kvq3_status prefill_tc(const CacheGeom& g, const kvq3_cache* cache, int32_t seq, int64_t pos0, int64_t n_q,
-                       const void* q, int32_t hq, float qk_scale, float* out, int32_t* dev_status,
-                       const RotParams& rp, uint32_t wait_limit, cudaStream_t st);
+                       const void* q, int32_t hq, float qk_scale, float* out, void* workspace, size_t ws_bytes,
+                       int32_t* dev_status, const RotParams& rp, uint32_t wait_limit, cudaStream_t st);
 
 // Tile-kernel path of kvq3_prefill_attn (d = 128; arguments already checked).
 kvq3_status prefill_tiles(const CacheGeom& g, const kvq3_cache* cache, int32_t seq, int64_t pos0,

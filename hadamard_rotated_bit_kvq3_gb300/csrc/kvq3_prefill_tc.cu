@@ -70,6 +70,8 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kSP = 3;                // S/P buffers in TMEM
 constexpr uint32_t kColSP = 0, kColO = 384;   // TMEM: S/P buffer j at 128 j, O
 constexpr float kRescale = 8.0f;      // log2 of the largest p between rescales
+constexpr int kMinSplit = 8;          // a unit of at least this many key tiles runs as two CTAs
+constexpr int kPartStride = 132;      // floats a row of a partial takes: O (128), m, l, padding
 
 // shared memory (bytes)
 constexpr int kTile = kKeys * kD * 2;                          // one fp16 tile (16 KB)
@@ -105,6 +107,9 @@ struct TcParams {
   float qk_scale;       // sm_scale * log2(e)
   float inv_sqrt_d;
   uint32_t wait_limit;
+  int32_t* counters;    // [units] halves of a split unit done (zeroed before the launch)
+  float* partial;       // [units][2][128 rows][kPartStride]: O (unnormalised), m, l of each half
+  int64_t ws_floats;    // floats of the partial area (bounds of the checked build)
 };
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
@@ -179,12 +184,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 
   const CacheGeom& g = p.g;
   const int kvh = blockIdx.y;
-  const int qblk = (int)gridDim.x - 1 - (int)blockIdx.x;   // longest query blocks first
+  const int nqb = (int)gridDim.x >> 1;
+  const int qblk = nqb - 1 - ((int)blockIdx.x >> 1);       // longest query blocks first
+  const int half = (int)blockIdx.x & 1;                    // which part of the unit's keys
+  const int unit = kvh * nqb + qblk;
   const int t0 = qblk * p.qb;
   const int ntok = min(p.qb, p.n - t0);
   const int nrows = ntok * p.G;
   const int64_t kmax = p.pos0 + t0 + ntok - 1;             // last position any row attends to
-  const int T = (int)(kmax / kKeys) + 1;                   // key tiles
+  const int T = (int)(kmax / kKeys) + 1;                   // key tiles of the unit
+  // a long unit runs as two CTAs, tiles [0, T/2) and [T/2, T), merged by the
+  // second to finish; a short one as one CTA (the other returns at once)
+  const bool split = T >= kMinSplit;
+  if (!split && half == 1) return;
+  const int tlo = split && half == 1 ? T / 2 : 0;
+  const int nt = split ? (half == 0 ? T / 2 : T - T / 2) : T;   // key tiles of this CTA
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -229,8 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   // to tile: no division); positions are below 2^31 (checked on the host).
   const int64_t pool_bytes = g.num_pages * g.page_bytes;
   (void)pool_bytes;   // read by the checked build only
-  auto issue = [&](int t, uint32_t lp0, uint32_t slot0) {
-    const int s = t % kStages;
+  auto issue = [&](int u, int t, uint32_t lp0, uint32_t slot0) {   // u: this CTA's tile count, t: the key tile
+    const int s = u % kStages;
     uint8_t* st = smem + kOffRaw + s * kRawBytes;
     const uint32_t k0 = (uint32_t)t * kKeys, P = (uint32_t)g.page_size, last = (uint32_t)kmax;
     int64_t pg[4];
@@ -344,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     float m_used = -INFINITY;
     float2 l2 = make_float2(0.0f, 0.0f);
     bool okw = true;   // this warp's waits all succeeded (warp-uniform)
-    for (int t = 0; t < T; ++t) {
+    for (int t = 0; t < nt; ++t) {   // t counts this CTA's tiles; key tile tlo + t
       const int b = t & 1, s = t % kStages, j = t % kSP;
       okw = okw && __all_sync(kFull, wait(&s_full[j], (uint32_t)(t / kSP) & 1u) &&
                                          wait(&ks_full[s], (uint32_t)(t / kStages) & 1u));
@@ -371,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                         make_float2(kk[i].y, kk[i].w),
                         f2mul(make_float2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1])),
                               make_float2(kk[i].x, kk[i].z)));
-        const int64_t k0 = (int64_t)t * kKeys + 32 * kh;
+        const int64_t k0 = (int64_t)(tlo + t) * kKeys + 32 * kh;
         if (!(km == 0xFFFFFFFFu && k0 + 31 <= lim)) {
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
@@ -435,15 +449,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       tc::fence_before();
       mbar_arrive(&p_full[j]);
     }
-    // row sums of the two halves (in the slots of parity T & 1, which no one
+    // row sums of the two halves (in the slots of parity nt & 1, which no one
     // reads after the last tile's exchange); O of this warp's 64 columns
-    const int e = (T & 1) * 2;
+    const int e = (nt & 1) * 2;
     red_s[(e + kh) * kRows + row] = l2.x + l2.y;
     bool ok = pair_and(1 + wq, okw);
     const float l = red_s[(e + kh) * kRows + row] + red_s[(e + (kh ^ 1)) * kRows + row];
-    if (ok) ok = __all_sync(kFull, wait(&pv_done[(T - 1) % kSP], (uint32_t)((T - 1) / kSP) & 1u));
+    if (ok) ok = __all_sync(kFull, wait(&pv_done[(nt - 1) % kSP], (uint32_t)((nt - 1) / kSP) & 1u));
     tc::fence_after();
-    const float inv = (ok && l > 0.0f) ? 1.0f / l : 0.0f;
+    // a whole unit: normalised rows into the staging; half of a split unit:
+    // O (unnormalised, relative to 2^m_used), m_used and l to its partial
+    const float inv = split ? 1.0f : (ok && l > 0.0f) ? 1.0f / l : 0.0f;
+    float* prow = p.partial + ((int64_t)(unit * 2 + half) * kRows + row) * kPartStride;
+    const bool pw = split && KVQ3_CHECK(p.status, in_range((prow - p.partial), kPartStride, p.ws_floats));
 #pragma unroll
     for (int c4 = 0; c4 < 2; ++c4) {
       uint32_t o[32];
@@ -455,15 +473,29 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[i] = 0u;
       }
+      if (split) {
+        if (pw) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) rows[row * kPitch + 64 * kh + 32 * c4 + i] = __uint_as_float(o[i]) * inv;
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(prow + 64 * kh + 32 * c4 + i) =
+                make_float4(__uint_as_float(o[i]), __uint_as_float(o[i + 1]), __uint_as_float(o[i + 2]),
+                            __uint_as_float(o[i + 3]));
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) rows[row * kPitch + 64 * kh + 32 * c4 + i] = __uint_as_float(o[i]) * inv;
+      }
+    }
+    if (pw && kh == 0) {
+      prow[kD] = ok ? m_used : -INFINITY;
+      prow[kD + 1] = ok ? l : 0.0f;
     }
   } else if (tid >= kDequant0 && tid < kDequant0 + 128) {
     // ================================================================ dequantisation
     // lane -> (key, half): 8 consecutive lanes hold 8 consecutive keys, so a
     // 16-byte store of 8 lanes covers the 32 banks once
-    const int dt = tid - kDequant0, key = (dt >> 5) * 16 + (dt & 15), half = (dt >> 4) & 1;
-    for (int t = 0; t < T; ++t) {
+    const int dt = tid - kDequant0, key = (dt >> 5) * 16 + (dt & 15), hd = (dt >> 4) & 1;   // key; half of the dimensions
+    for (int t = 0; t < nt; ++t) {   // this CTA's tiles
       const int s = t % kStages, b = t & 1;
       // a failed wait leaves at once, arriving nowhere: a stage is released
       // (raw_empty) only once its copies have landed
@@ -476,10 +508,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       {
         // the lane's 64 codes as two runs of 96 bits (32 codes, 4 groups of 8);
         // the run loop is not unrolled, to keep the roles' code small
-        uint8_t* kt = smem + kOffK + b * kTile + (key >> 3) * 2048 + (key & 7) * 16 + 8 * half * 128;
+        uint8_t* kt = smem + kOffK + b * kTile + (key >> 3) * 2048 + (key & 7) * 16 + 8 * hd * 128;
 #pragma unroll 1
         for (int r = 0; r < 2; ++r) {
-          const uint32_t* src = reinterpret_cast<const uint32_t*>(st + kRawK + key * kCB + half * 24 + 12 * r);
+          const uint32_t* src = reinterpret_cast<const uint32_t*>(st + kRawK + key * kCB + hd * 24 + 12 * r);
           const uint32_t w[4] = {src[0], src[1], src[2], 0u};
 #pragma unroll
           for (int gq = 0; gq < 4; ++gq) {
@@ -494,11 +526,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           }
         }
         uint32_t bits;
-        const uint8_t* sp = st + kRawKs + (key * 2 + half) * SB;
+        const uint8_t* sp = st + kRawKs + (key * 2 + hd) * SB;
         if (SB == 4) bits = *reinterpret_cast<const uint32_t*>(sp);
         else if (SB == 2) bits = *reinterpret_cast<const uint16_t*>(sp);
         else bits = *sp;
-        ks_s[(s * kKeys + key) * 2 + half] = kv ? decode_scale(bits, SCALE) : 0.0f;
+        ks_s[(s * kKeys + key) * 2 + hd] = kv ? decode_scale(bits, SCALE) : 0.0f;
         if (dt == 0) key_mask[s] = vm;
       }
       fence_proxy_async();
@@ -508,17 +540,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       if (t >= 2 && !wait(&pv_done[(t - 2) % kSP], (uint32_t)((t - 2) / kSP) & 1u)) break;
       {
         uint32_t bits;
-        const uint8_t* sp = st + kRawVs + (key * 2 + half) * SB;
+        const uint8_t* sp = st + kRawVs + (key * 2 + hd) * SB;
         if (SB == 4) bits = *reinterpret_cast<const uint32_t*>(sp);
         else if (SB == 2) bits = *reinterpret_cast<const uint16_t*>(sp);
         else bits = *sp;
         const float sv = kv ? decode_scale(bits, SCALE) : 0.0f;
         const float s_hi = __uint_as_float(__float_as_uint(sv) & 0xFFFF8000u);   // top 9 significant bits
         const __half2 hs = __float2half2_rn(s_hi), ls = __float2half2_rn(sv - s_hi);
-        uint8_t* vt = smem + kOffV + b * 2 * kTile + (key >> 3) * 128 + (key & 7) * 16 + 8 * half * 1024;
+        uint8_t* vt = smem + kOffV + b * 2 * kTile + (key >> 3) * 128 + (key & 7) * 16 + 8 * hd * 1024;
 #pragma unroll 1
         for (int r = 0; r < 2; ++r) {
-          const uint32_t* src = reinterpret_cast<const uint32_t*>(st + kRawV + key * kCB + half * 24 + 12 * r);
+          const uint32_t* src = reinterpret_cast<const uint32_t*>(st + kRawV + key * kCB + hd * 24 + 12 * r);
           const uint32_t w[4] = {src[0], src[1], src[2], 0u};
 #pragma unroll
           for (int gq = 0; gq < 4; ++gq) {
@@ -549,11 +581,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     // ================================================================ bulk copies
     int issued = 0;
     bool ok = true;
-    uint32_t lp = 0, slot = 0;   // key 64 t = lp * P + slot
-    for (int t = 0; t < T && ok; ++t) {
+    uint32_t lp = (uint32_t)(tlo * kKeys) / (uint32_t)g.page_size;   // key 64 (tlo + t) = lp * P + slot
+    uint32_t slot = (uint32_t)(tlo * kKeys) - lp * (uint32_t)g.page_size;
+    for (int t = 0; t < nt && ok; ++t) {
       if (t >= kStages) ok = wait(&raw_empty[t % kStages], (uint32_t)(t / kStages - 1) & 1u);   // tile t - kStages consumed
       if (ok && *abort_flag) ok = false;
-      if (ok) issue(t, lp, slot), issued = t + 1;
+      if (ok) issue(t, tlo + t, lp, slot), issued = t + 1;
       for (slot += kKeys; slot >= (uint32_t)g.page_size; slot -= (uint32_t)g.page_size) ++lp;
     }
     // no bulk copy may still target this CTA's shared memory at exit: the
@@ -568,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     const uint64_t dk = tc::sdesc(smem_u32(smem + kOffK), 128u, 2048u);
     const uint32_t dq_lo = (uint32_t)dq, dq_hi = (uint32_t)(dq >> 32);
     const uint32_t dk_lo = (uint32_t)dk, dk_hi = (uint32_t)(dk >> 32);
-    for (int t = 0; t < T; ++t) {   // S_b(t) = q1[block b] . c_k[block b], hi and lo halves of q1
+    for (int t = 0; t < nt; ++t) {   // S_b(t) = q1[block b] . c_k[block b], hi and lo halves of q1
       const int b = t & 1, j = t % kSP;
       if (!wait(&k_full[b], (uint32_t)(t >> 1) & 1u)) break;
       if (t >= kSP && !wait(&pv_done[j], (uint32_t)(t / kSP - 1) & 1u)) break;   // P(t - kSP) consumed
@@ -595,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     constexpr uint32_t kIdPV = tc::idesc_f16(128, kD, true);
     const uint64_t dv = tc::sdesc(smem_u32(smem + kOffV), 128u, 1024u);
     const uint32_t dv_lo = (uint32_t)dv, dv_hi = (uint32_t)(dv >> 32);
-    for (int t = 0; t < T; ++t) {   // O += P(t) V(t)
+    for (int t = 0; t < nt; ++t) {   // O += P(t) V(t)
       const int b = t & 1, j = t % kSP;
       if (!wait(&p_full[j], (uint32_t)(t / kSP) & 1u) || !wait(&v_full[b], (uint32_t)(t >> 1) & 1u)) break;
       tc::fence_after();
@@ -617,6 +650,38 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   }
   __syncthreads();
 
+  // ---- a split unit: the second half to finish merges the two partials
+  volatile int32_t* order = reinterpret_cast<volatile int32_t*>(tmem_slot + 2);
+  if (split) {
+    __threadfence();   // this half's partial before its count
+    __syncthreads();
+    if (tid == 0) *order = atomicAdd(p.counters + unit, 1);
+    __syncthreads();
+    if (*order == 1 && tid < 2 * kRows) {
+      __threadfence();
+      const int row = tid & (kRows - 1), ch = tid >> 7;   // 64 columns each
+      const float* pa = p.partial + ((int64_t)(unit * 2) * kRows + row) * kPartStride;
+      const float* pb = pa + (int64_t)kRows * kPartStride;
+      const float ma = __ldcg(pa + kD), la = __ldcg(pa + kD + 1), mb = __ldcg(pb + kD), lb = __ldcg(pb + kD + 1);
+      const float m = fmaxf(ma, mb);
+      const float fa = ma == -INFINITY ? 0.0f : ex2(ma - m), fb = mb == -INFINITY ? 0.0f : ex2(mb - m);
+      const float lt = la * fa + lb * fb;
+      const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
+#pragma unroll 4
+      for (int c = 0; c < 64; c += 4) {
+        const float4 a = __ldcg(reinterpret_cast<const float4*>(pa + 64 * ch + c));
+        const float4 b = __ldcg(reinterpret_cast<const float4*>(pb + 64 * ch + c));
+        float* r = rows + row * kPitch + 64 * ch + c;
+        r[0] = (a.x * fa + b.x * fb) * inv;
+        r[1] = (a.y * fa + b.y * fb) * inv;
+        r[2] = (a.z * fa + b.z * fb) * inv;
+        r[3] = (a.w * fa + b.w * fb) * inv;
+      }
+    }
+    __syncthreads();
+  }
+  const bool write_out = !split || *order == 1;
+
   // ---- outputs: rotate back with U^T (warp per row) and store
   {
     const uint32_t sgn = lane_signs<4>(rp, lane);
@@ -624,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     lane_quats<4>(rp, lane, qt);
     lane_quats_r<4>(rp, lane, qtr);
     const bool so4 = rot_so4(rp), pair = rot_pair(rp);
-    for (int row = warp; row < nrows; row += kThreads / 32) {
+    for (int row = warp; write_out && row < nrows; row += kThreads / 32) {
       float x[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) x[e] = rows[row * kPitch + lane * 4 + e];
@@ -645,7 +710,7 @@ kvq3_status launch_tc(const TcParams& p, const RotParams& rp, cudaStream_t st) {
   auto k = prefill_tc_kernel<SCALE>;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
     return KVQ3_ERR_CUDA;
-  const dim3 grid((unsigned)((p.n + p.qb - 1) / p.qb), (unsigned)p.g.hkv);
+  const dim3 grid((unsigned)(2 * ((p.n + p.qb - 1) / p.qb)), (unsigned)p.g.hkv);   // two CTAs a unit
   k<<<grid, kThreads, kSmem, st>>>(p, rp);
   return cudaGetLastError() == cudaSuccess ? KVQ3_OK : KVQ3_ERR_CUDA;
 }
@@ -658,11 +723,19 @@ bool prefill_tc_supported(const CacheGeom& g, int32_t hq) {
   return g.d == kD && g.bits == 3 && g.block == 64 && g.scale_type != KVQ3_SCALE_E4M3_ZP && hq / g.hkv <= kRows;
 }
 
+// Workspace of the tcgen05 path: one counter per unit (128 query rows of a kv
+// head), then per unit two partials of 128 rows x kPartStride floats.
+size_t prefill_tc_workspace(const CacheGeom& g, int32_t hq, int64_t n_q) {
+  const int64_t units = (n_q + kRows / (hq / g.hkv) - 1) / (kRows / (hq / g.hkv)) * g.hkv;
+  return (size_t)((units * 4 + 255) / 256 * 256) + (size_t)units * 2 * kRows * kPartStride * sizeof(float);
+}
+
 // tcgen05 path of kvq3_prefill_attn; arguments already checked.
 kvq3_status prefill_tc(const CacheGeom& g, const kvq3_cache* cache, int32_t seq, int64_t pos0, int64_t n_q,
-                       const void* q, int32_t hq, float qk_scale, float* out, int32_t* dev_status,
-                       const RotParams& rp, uint32_t wait_limit, cudaStream_t st) {
+                       const void* q, int32_t hq, float qk_scale, float* out, void* workspace, size_t ws_bytes,
+                       int32_t* dev_status, const RotParams& rp, uint32_t wait_limit, cudaStream_t st) {
   if (!prefill_tc_supported(g, hq)) return KVQ3_ERR_UNSUPPORTED;
+  if (!workspace || ws_bytes < prefill_tc_workspace(g, hq, n_q)) return KVQ3_ERR_WORKSPACE;
   TcParams p;
   memset(&p, 0, sizeof(p));
   p.g = g;
@@ -680,6 +753,12 @@ kvq3_status prefill_tc(const CacheGeom& g, const kvq3_cache* cache, int32_t seq,
   p.qk_scale = qk_scale;
   p.inv_sqrt_d = inv_sqrt(g.d);
   p.wait_limit = wait_limit;
+  const int64_t units = (n_q + p.qb - 1) / p.qb * g.hkv;
+  const size_t cbytes = (size_t)((units * 4 + 255) / 256 * 256);
+  p.counters = static_cast<int32_t*>(workspace);
+  p.partial = reinterpret_cast<float*>(static_cast<char*>(workspace) + cbytes);
+  p.ws_floats = (int64_t)((ws_bytes - cbytes) / sizeof(float));
+  if (cudaMemsetAsync(workspace, 0, (size_t)units * 4, st) != cudaSuccess) return KVQ3_ERR_CUDA;
   if (g.scale_type == KVQ3_SCALE_F32) return launch_tc<KVQ3_SCALE_F32>(p, rp, st);
   if (g.scale_type == KVQ3_SCALE_F16) return launch_tc<KVQ3_SCALE_F16>(p, rp, st);
   return launch_tc<KVQ3_SCALE_E4M3>(p, rp, st);
