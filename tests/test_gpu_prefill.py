@@ -141,3 +141,30 @@ def test_prefill_bad_page_flags_and_masks():
                 h = g * (c.hq // c.hkv) + gh
                 ref[i, h] = Ox.attention_rotated(U, q[i, h], kh[idx], vh[idx], 1.0 / np.sqrt(c.d))
     assert rel_err(got, ref) <= TOL_DECODE
+
+
+def test_prefill_workspace_covers_split_units():
+    import hadamard_rotated_bit_kvq3_gb300 as K
+    # d = 128, 3-bit symmetric codes, blocks of 64: the tcgen05 path, whose
+    # units (128 (token, head) rows of a kv head) may run as two CTAs that
+    # meet in the workspace: a counter per unit, then two partials of
+    # 128 rows x 132 floats per unit, after the 256-byte aligned counters
+    # (the size also covers the decode kernel's plan, which asks the device)
+    def desc(**kw):
+        base = dict(head_dim=128, num_kv_heads=8, block=64, bits=3, scale_type=1, eps=1e-6,
+                    page_size=128, batch=1, max_pages_per_seq=256, reserved=0, num_pages=256)
+        base.update(kw)
+        return K.CacheDesc(**base)
+    for hq, n in ((32, 2048), (32, 1), (24, 300), (8, 129), (128, 5)):
+        g = hq // 8
+        units = -(-n // (128 // g)) * 8
+        need = -(-units * 4 // 256) * 256 + units * 2 * 128 * 132 * 4
+        if g > 16:   # more than 16 query heads per kv head: refused
+            with pytest.raises(K.Kvq3Error):
+                K.kvq3_prefill_workspace_size(desc(), hq, n)
+            continue
+        assert K.kvq3_prefill_workspace_size(desc(), hq, n) >= need, (hq, n)
+    # other formats run on the decode kernel's prefill variant: no partials,
+    # far less than the tcgen05 path would ask for
+    small = K.kvq3_prefill_workspace_size(desc(block=32), 32, 2048)
+    assert small < 512 * 2 * 128 * 132 * 4

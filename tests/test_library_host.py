@@ -201,3 +201,4 @@ def test_calibration_arguments_checked_on_host(K):
         st = K.lib.kvq3_calib_sse_pair(rot, ctypes.byref(d), ctypes.c_void_p(quats), ctypes.c_void_p(quats_r), 1,
                                        ctypes.c_void_p(256), 16, sse, None)
         assert st == 1, (quats, quats_r)
+
