@@ -947,7 +947,9 @@ def prefill_attn_record(args, world: int, rank: int, dev, peaks: dict) -> dict:
         "dtype": f"f16 mma / f32 accumulate ({w.bits}-bit packed cache)",
         "config": workload_config(w, None, world),
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16"], "unit": "TFLOP/s",
-                     "frac": tflops / peaks["bf16"], "traffic": None,
+                     "frac": tflops / peaks["bf16"],
+                     "traffic": recorded_traffic_of("prefill_tc", "prefill_attn")
+                     if tile and w.block == 64 and not args.tokens else None,
                      "flops": st.flops(),
                      "kernel": "kvq3_prefill_attn (" + (tile_kernel if tile else
                                "decode_split_kernel<..., prefill> + decode_combine_kernel") + ")",
