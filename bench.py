@@ -936,10 +936,10 @@ def prefill_attn_record(args, world: int, rank: int, dev, peaks: dict) -> dict:
     b.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(a.elapsed_time(b), world) / n_e2e
-    # d = 128 with 3-bit symmetric codes runs a tile kernel (one launch): the
-    # tcgen05 one with blocks of 64, the mma.sync one with blocks of 32; the
-    # other formats the decode kernel's prefill variant and the combine
-    tile = w.d == 128 and w.bits == 3 and w.scale != "e4m3zp"
+    # d = 128 with symmetric codes runs a tile kernel (one launch): the tcgen05
+    # one with blocks of 64 (b = 2-4), the mma.sync one with blocks of 32
+    # (b = 3); the other formats the decode kernel's prefill variant and the combine
+    tile = w.d == 128 and w.scale != "e4m3zp" and (w.block == 64 or w.bits == 3)
     tile_kernel = "prefill_tc_kernel" if w.block == 64 else "prefill_tile_kernel"
     rec = {
         "metric": PREFILL_ATTN_METRIC, "value": whole_job_rate(w.chunk, world, ms), "unit": "tokens/s",

@@ -178,14 +178,19 @@ static kvq3_status prefill_attn_impl(kvq3_rotation rot, const kvq3_cache_desc* d
   if (!workspace || ws_bytes < plan.ws_bytes || reinterpret_cast<uintptr_t>(workspace) % 256)
     return KVQ3_ERR_WORKSPACE;
   const double qks = (sm_scale > 0.0f ? (double)sm_scale : 1.0 / sqrt((double)vg.d)) * 1.4426950408889634;
-  if (vg.d == 128 && vg.bits == 3 && vg.scale_type != KVQ3_SCALE_E4M3_ZP) {
+  {
     // shared dequantised tiles: each K/V tile is unpacked once for 128 query
-    // rows on the tcgen05 path (blocks of 64), for 64 on the mma.sync one
+    // rows on the tcgen05 path (d = 128, blocks of 64, b = 2-4), for 64 on
+    // the mma.sync one (d = 128, blocks of 32, b = 3)
     CacheGeom g;
     make_geom(desc, &g);
     if (prefill_tc_supported(g, num_q_heads))
       return prefill_tc(g, cache, seq, pos0, n_q, q, num_q_heads, (float)qks, out, workspace, ws_bytes,
                         dev_status, rot->params, wait_limit, static_cast<cudaStream_t>(stream));
+  }
+  if (vg.d == 128 && vg.bits == 3 && vg.scale_type != KVQ3_SCALE_E4M3_ZP) {
+    CacheGeom g;
+    make_geom(desc, &g);
     return prefill_tiles(g, cache, seq, pos0, n_q, q, num_q_heads, (float)qks, out, dev_status,
                          rot->params, static_cast<cudaStream_t>(stream));
   }

@@ -1,6 +1,6 @@
 // Chunked-prefill attention over the packed cache on the 5th-generation tensor
-// cores (tcgen05, accumulators in tensor memory): head dimension 128, 3-bit
-// symmetric codes, quantisation blocks of 64.
+// cores (tcgen05, accumulators in tensor memory): head dimension 128,
+// symmetric codes of b = 2, 3 or 4 bits, quantisation blocks of 64.
 //
 // "Orthogonally mixed 3-bit KV cache", Implementation notes (read path) and
 // Key formulas, with the causal mask of a prefill chunk: query token i sits at
@@ -20,8 +20,8 @@
 // The online softmax (base 2, lazy rescaling: the running maximum moves only
 // when a row's maximum grows by more than 2^8) gives p <= 2^8, kept as hi + lo
 // fp16 halves.  A value's scale is split as s_v = s_hi + s_lo with s_hi its
-// top 9 significant bits, so that c * s_hi and c * s_lo (|c| <= 4) are exact
-// fp16 numbers and
+// top 9 significant bits (8 at b = 4), so that c * s_hi and c * s_lo
+// (|c| <= 2^(b-1)) are exact fp16 numbers and
 //   O += p_hi . (c s_hi) + p_lo . (c s_hi) + p_hi . (c s_lo)
 // over full 128-dimension rows (the dropped p_lo . (c s_lo) is below 2^-20 of
 // the product; E4M3 scales have s_lo = 0 and skip the third MMA).  Dequantised
@@ -57,7 +57,6 @@ namespace {
 constexpr int kRows = 128;            // query rows per CTA = TMEM lanes
 constexpr int kKeys = 64;             // keys per tile
 constexpr int kD = 128;               // head dimension
-constexpr int kCB = 3 * kD / 8;       // code bytes per vector (48)
 constexpr int kStages = 4;            // raw stages in flight
 constexpr int kThreads = 15 * 32;
 constexpr int kMmaWarp = 0;           // QK^T issue (lane 0) and the TMEM allocation
@@ -77,9 +76,10 @@ constexpr int kPartStride = 132;      // floats a row of a partial takes: O (128
 constexpr int kTile = kKeys * kD * 2;                          // one fp16 tile (16 KB)
 constexpr int kOffK = 0;                                       // [2] key codes, K-major
 constexpr int kOffV = kOffK + 2 * kTile;                       // [2][hi, lo] values, MN-major
-constexpr int kRawK = 0, kRawV = kKeys * kCB;                  // raw stage: codes K, V
-constexpr int kRawKs = 2 * kKeys * kCB, kRawVs = kRawKs + kKeys * 2 * 4;   // scales K, V (<= 8 B a key)
-constexpr int kRawBytes = kRawVs + kKeys * 2 * 4;              // 7168
+constexpr int kMaxCB = 4 * kD / 8;                             // code bytes per vector at b = 4
+constexpr int kRawK = 0, kRawV = kKeys * kMaxCB;               // raw stage: codes K, V
+constexpr int kRawKs = 2 * kKeys * kMaxCB, kRawVs = kRawKs + kKeys * 2 * 4;   // scales K, V (<= 8 B a key)
+constexpr int kRawBytes = kRawVs + kKeys * 2 * 4;              // 9216
 constexpr int kOffQ = kOffV + 4 * kTile;                       // q1 hi, lo: K-major A of QK^T
 constexpr int kOffRaw = kOffQ + 4 * kTile;
 constexpr int kOffKs = kOffRaw + kStages * kRawBytes;          // [kStages][64 keys][2 blocks] fp32 key scales
@@ -135,11 +135,17 @@ __device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
-// two 3-bit two's-complement fields (bits 0-2 and 3-5 of w6) -> half2 of the
-// exact integers: (0x6400 | (c + 4)) - 1028
-__device__ __forceinline__ __half2 codes2(uint32_t w6) {
-  const uint32_t h = (((w6 & 63u) * 0x2001u) & 0x00070007u) ^ 0x64046404u;
-  return __hsub2(*reinterpret_cast<const __half2*>(&h), __halves2half2(__ushort_as_half(0x6404), __ushort_as_half(0x6404)));
+// two b-bit two's-complement fields (bits 0..b-1 and b..2b-1 of w) -> half2
+// of the exact integers: times 1 + 2^(16-b) puts the second field at bit
+// 16; flipping the sign bit gives c + 2^(b-1), and (0x6400 | (c + 2^(b-1)))
+// - (1024 + 2^(b-1)) = c
+template <int B>
+__device__ __forceinline__ __half2 codes2(uint32_t w) {
+  constexpr uint32_t f = (1u << B) - 1u, sgn = 1u << (B - 1);
+  const uint32_t h = (((w & ((1u << (2 * B)) - 1u)) * (1u + (1u << (16 - B)))) & (f | (f << 16))) ^
+                     ((0x6400u | sgn) * 0x10001u);
+  const __half off = __ushort_as_half((unsigned short)(0x6400u | sgn));
+  return __hsub2(*reinterpret_cast<const __half2*>(&h), __halves2half2(off, off));
 }
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
@@ -156,10 +162,11 @@ __device__ __forceinline__ bool pair_and(int id, bool v) {
   return r != 0;
 }
 
-template <int SCALE>
+template <int SCALE, int BITS>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ TcParams p,
                                                                   const __grid_constant__ RotParams rp) {
   constexpr int SB = SCALE == KVQ3_SCALE_F32 ? 4 : SCALE == KVQ3_SCALE_F16 ? 2 : 1;
+  constexpr int kCB = BITS * kD / 8;   // code bytes per vector
   constexpr bool kLo = SCALE != KVQ3_SCALE_E4M3;   // values carry a low part of the scale
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -510,18 +517,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         // the run loop is not unrolled, to keep the roles' code small
         uint8_t* kt = smem + kOffK + b * kTile + (key >> 3) * 2048 + (key & 7) * 16 + 8 * hd * 128;
 #pragma unroll 1
-        for (int r = 0; r < 2; ++r) {
-          const uint32_t* src = reinterpret_cast<const uint32_t*>(st + kRawK + key * kCB + hd * 24 + 12 * r);
-          const uint32_t w[4] = {src[0], src[1], src[2], 0u};
+        for (int r = 0; r < 2; ++r) {   // 32 codes: BITS words
+          const uint32_t* src = reinterpret_cast<const uint32_t*>(st + kRawK + key * kCB + hd * (kCB / 2) + r * (kCB / 4));
+          uint32_t w[BITS + 1];
 #pragma unroll
-          for (int gq = 0; gq < 4; ++gq) {
-            const int bit = 24 * gq;
-            const uint32_t w24 = __funnelshift_r(w[bit >> 5], w[(bit >> 5) + 1], bit & 31);
+          for (int i = 0; i < BITS; ++i) w[i] = src[i];
+          w[BITS] = 0u;
+#pragma unroll
+          for (int gq = 0; gq < 4; ++gq) {   // 8 codes at bit 8 BITS gq
+            const int bit = 8 * BITS * gq;
+            const uint32_t wg = (bit & 31) ? __funnelshift_r(w[bit >> 5], w[(bit >> 5) + 1], bit & 31) : w[bit >> 5];
             uint4 o;
-            o.x = h2u(codes2(w24));
-            o.y = h2u(codes2(w24 >> 6));
-            o.z = h2u(codes2(w24 >> 12));
-            o.w = h2u(codes2(w24 >> 18));
+            o.x = h2u(codes2<BITS>(wg));
+            o.y = h2u(codes2<BITS>(wg >> (2 * BITS)));
+            o.z = h2u(codes2<BITS>(wg >> (4 * BITS)));
+            o.w = h2u(codes2<BITS>(wg >> (6 * BITS)));
             *reinterpret_cast<uint4*>(kt + (4 * r + gq) * 128) = o;
           }
         }
@@ -545,18 +555,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         else if (SB == 2) bits = *reinterpret_cast<const uint16_t*>(sp);
         else bits = *sp;
         const float sv = kv ? decode_scale(bits, SCALE) : 0.0f;
-        const float s_hi = __uint_as_float(__float_as_uint(sv) & 0xFFFF8000u);   // top 9 significant bits
+        // top 9 significant bits (8 at b = 4): c s_hi stays within fp16's 11
+        const float s_hi = __uint_as_float(__float_as_uint(sv) & (BITS == 4 ? 0xFFFF0000u : 0xFFFF8000u));
         const __half2 hs = __float2half2_rn(s_hi), ls = __float2half2_rn(sv - s_hi);
         uint8_t* vt = smem + kOffV + b * 2 * kTile + (key >> 3) * 128 + (key & 7) * 16 + 8 * hd * 1024;
 #pragma unroll 1
         for (int r = 0; r < 2; ++r) {
-          const uint32_t* src = reinterpret_cast<const uint32_t*>(st + kRawV + key * kCB + hd * 24 + 12 * r);
-          const uint32_t w[4] = {src[0], src[1], src[2], 0u};
+          const uint32_t* src = reinterpret_cast<const uint32_t*>(st + kRawV + key * kCB + hd * (kCB / 2) + r * (kCB / 4));
+          uint32_t w[BITS + 1];
+#pragma unroll
+          for (int i = 0; i < BITS; ++i) w[i] = src[i];
+          w[BITS] = 0u;
 #pragma unroll
           for (int gq = 0; gq < 4; ++gq) {
-            const int bit = 24 * gq;
-            const uint32_t w24 = __funnelshift_r(w[bit >> 5], w[(bit >> 5) + 1], bit & 31);
-            const __half2 c0 = codes2(w24), c1 = codes2(w24 >> 6), c2 = codes2(w24 >> 12), c3 = codes2(w24 >> 18);
+            const int bit = 8 * BITS * gq;
+            const uint32_t wg = (bit & 31) ? __funnelshift_r(w[bit >> 5], w[(bit >> 5) + 1], bit & 31) : w[bit >> 5];
+            const __half2 c0 = codes2<BITS>(wg), c1 = codes2<BITS>(wg >> (2 * BITS)),
+                          c2 = codes2<BITS>(wg >> (4 * BITS)), c3 = codes2<BITS>(wg >> (6 * BITS));
             uint4 o;
             o.x = h2u(__hmul2(c0, hs));
             o.y = h2u(__hmul2(c1, hs));
@@ -705,9 +720,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   if (warp == kMmaWarp) tc::dealloc(tmem, kTmemCols);
 }
 
-template <int SCALE>
+template <int SCALE, int BITS>
 kvq3_status launch_tc(const TcParams& p, const RotParams& rp, cudaStream_t st) {
-  auto k = prefill_tc_kernel<SCALE>;
+  auto k = prefill_tc_kernel<SCALE, BITS>;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
     return KVQ3_ERR_CUDA;
   const dim3 grid((unsigned)(2 * ((p.n + p.qb - 1) / p.qb)), (unsigned)p.g.hkv);   // two CTAs a unit
@@ -715,12 +730,20 @@ kvq3_status launch_tc(const TcParams& p, const RotParams& rp, cudaStream_t st) {
   return cudaGetLastError() == cudaSuccess ? KVQ3_OK : KVQ3_ERR_CUDA;
 }
 
+template <int BITS>
+kvq3_status launch_bits(const CacheGeom& g, const TcParams& p, const RotParams& rp, cudaStream_t st) {
+  if (g.scale_type == KVQ3_SCALE_F32) return launch_tc<KVQ3_SCALE_F32, BITS>(p, rp, st);
+  if (g.scale_type == KVQ3_SCALE_F16) return launch_tc<KVQ3_SCALE_F16, BITS>(p, rp, st);
+  return launch_tc<KVQ3_SCALE_E4M3, BITS>(p, rp, st);
+}
+
 }  // namespace
 
 namespace kvq3 {
 
 bool prefill_tc_supported(const CacheGeom& g, int32_t hq) {
-  return g.d == kD && g.bits == 3 && g.block == 64 && g.scale_type != KVQ3_SCALE_E4M3_ZP && hq / g.hkv <= kRows;
+  return g.d == kD && g.bits >= 2 && g.bits <= 4 && g.block == 64 && g.scale_type != KVQ3_SCALE_E4M3_ZP &&
+         hq / g.hkv <= kRows;
 }
 
 // Workspace of the tcgen05 path: one counter per unit (128 query rows of a kv
@@ -759,9 +782,8 @@ kvq3_status prefill_tc(const CacheGeom& g, const kvq3_cache* cache, int32_t seq,
   p.partial = reinterpret_cast<float*>(static_cast<char*>(workspace) + cbytes);
   p.ws_floats = (int64_t)((ws_bytes - cbytes) / sizeof(float));
   if (cudaMemsetAsync(workspace, 0, (size_t)units * 4, st) != cudaSuccess) return KVQ3_ERR_CUDA;
-  if (g.scale_type == KVQ3_SCALE_F32) return launch_tc<KVQ3_SCALE_F32>(p, rp, st);
-  if (g.scale_type == KVQ3_SCALE_F16) return launch_tc<KVQ3_SCALE_F16>(p, rp, st);
-  return launch_tc<KVQ3_SCALE_E4M3>(p, rp, st);
+  return g.bits == 2 ? launch_bits<2>(g, p, rp, st) : g.bits == 4 ? launch_bits<4>(g, p, rp, st)
+                      : launch_bits<3>(g, p, rp, st);
 }
 
 }  // namespace kvq3

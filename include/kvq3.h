@@ -354,9 +354,9 @@ kvq3_status kvq3_decode_attn_noalloc(kvq3_rotation rot, const kvq3_cache_desc *d
  * q: device fp16 [n_q][Hq][d]; out: device fp32 [n_q][Hq][d]; sm_scale <= 0
  * means 1/sqrt(d); Hq a multiple of Hkv with Hq/Hkv <= 16.  Internally the
  * queries form tiles of up to 8 (query token, head) pairs per kv head; at
- * d = 128 with 3-bit symmetric codes and blocks of 64, units of 128 such
- * rows, a long unit's keys split in two ranges whose partial results meet in
- * the workspace.
+ * d = 128 with symmetric codes and blocks of 64, units of 128 such rows, a
+ * long unit's keys split in two ranges whose partial results meet in the
+ * workspace.
  * workspace:
  * device, ws_bytes >= kvq3_prefill_workspace_size(desc, Hq, n_q), 256-byte
  * aligned; calls sharing it must not overlap.  n_q = 0 is a no-op;

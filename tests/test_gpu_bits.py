@@ -167,6 +167,9 @@ PREFILL_CASES = [
     (dict(d=128, block=64, scale="f16", page=64, lens=(300,), hkv=2, hq=8), 0, 200, 100),
     (dict(d=128, block=32, scale="e4m3", page=16, lens=(90, 257), hkv=2, hq=16, paged=True), 1, 0, 257),
     (dict(d=64, block=32, scale="f32", page=16, lens=(150,), hkv=2, hq=12), 0, 60, 90),
+    # d = 128, blocks of 64: the tcgen05 kernel, here with units split in two key ranges
+    (dict(d=128, block=64, scale="e4m3", page=64, lens=(900,), hkv=2, hq=8), 0, 600, 300),
+    (dict(d=128, block=64, scale="f32", page=32, lens=(700,), hkv=1, hq=4, paged=True), 0, 500, 200),
     (dict(d=256, block=64, scale="f16", page=16, lens=(300, 180), hkv=2, hq=8, paged=True), 1, 100, 80),
 ]
 

@@ -33,6 +33,9 @@ PREFILL_CASES = [
     (dict(d=128, block=64, scale="e4m3", page=32, lens=(500,), hkv=4, hq=8, paged=True), 0, 499, 1),   # one query
     (dict(d=128, block=64, scale="f32", page=16, lens=(260,), hkv=1, hq=12), 0, 0, 260),      # G=12: 120-row CTAs, from 0
     (dict(d=128, block=64, scale="e4m3", page=64, lens=(1100,), hkv=2, hq=4, flags=7), 0, 1000, 100),  # SO(4) pairs
+    # units of eight or more key tiles run as two CTAs over the halves of their keys, merged in the workspace
+    (dict(d=128, block=64, scale="f16", page=16, lens=(40, 900), hkv=2, hq=8, paged=True), 1, 500, 300),  # 4 pages a tile
+    (dict(d=128, block=64, scale="f32", page=32, lens=(1300,), hkv=1, hq=16), 0, 1250, 50),    # G=16, 20 tiles
 ]
 
 
