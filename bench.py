@@ -936,11 +936,13 @@ def prefill_attn_record(args, world: int, rank: int, dev, peaks: dict) -> dict:
     b.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(a.elapsed_time(b), world) / n_e2e
-    # d = 128 with symmetric codes runs a tile kernel (one launch): the tcgen05
-    # one with blocks of 64 (b = 2-4), the mma.sync one with blocks of 32
-    # (b = 3); the other formats the decode kernel's prefill variant and the combine
-    tile = w.d == 128 and w.scale != "e4m3zp" and (w.block == 64 or w.bits == 3)
-    tile_kernel = "prefill_tc_kernel" if w.block == 64 else "prefill_tile_kernel"
+    # d = 128 runs a tile kernel (one launch): the tcgen05 one with blocks of
+    # 64 (symmetric codes of 2-4 bits, asymmetric 3-bit codes), the mma.sync
+    # one with blocks of 32 (symmetric 3-bit codes); the other formats the
+    # decode kernel's prefill variant and the combine
+    tc = w.d == 128 and w.block == 64 and (w.scale != "e4m3zp" or w.bits == 3)
+    tile = tc or (w.d == 128 and w.bits == 3 and w.scale != "e4m3zp")
+    tile_kernel = "prefill_tc_kernel" if tc else "prefill_tile_kernel"
     rec = {
         "metric": PREFILL_ATTN_METRIC, "value": whole_job_rate(w.chunk, world, ms), "unit": "tokens/s",
         "ms_per_step": ms, "ms_per_step_median": med,
@@ -949,7 +951,7 @@ def prefill_attn_record(args, world: int, rank: int, dev, peaks: dict) -> dict:
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16"], "unit": "TFLOP/s",
                      "frac": tflops / peaks["bf16"],
                      "traffic": recorded_traffic_of("prefill_tc", "prefill_attn")
-                     if tile and w.block == 64 and not args.tokens else None,
+                     if tc and w.bits == 3 and w.scale == "f16" and not args.tokens else None,
                      "flops": st.flops(),
                      "kernel": "kvq3_prefill_attn (" + (tile_kernel if tile else
                                "decode_split_kernel<..., prefill> + decode_combine_kernel") + ")",

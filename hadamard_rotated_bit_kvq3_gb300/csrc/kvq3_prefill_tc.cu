@@ -83,7 +83,11 @@ constexpr int kRawBytes = kRawVs + kKeys * 2 * 4;              // 9216
 constexpr int kOffQ = kOffV + 4 * kTile;                       // q1 hi, lo: K-major A of QK^T
 constexpr int kOffRaw = kOffQ + 4 * kTile;
 constexpr int kOffKs = kOffRaw + kStages * kRawBytes;          // [kStages][64 keys][2 blocks] fp32 key scales
-constexpr int kOffRed = kOffKs + kStages * kKeys * 2 * 4;      // [2][2][128] fp32 row maxima / sums traded
+constexpr int kOffZk = kOffKs + kStages * kKeys * 2 * 4;       // [kStages][64][2] key zero points (asymmetric codes)
+constexpr int kOffZv = kOffZk + kStages * kKeys * 2 * 4;       // [kStages][64][2] value zero points
+constexpr int kOffRsum = kOffZv + kStages * kKeys * 2 * 4;     // [128][2] per-row block sums of q1 (asymmetric codes)
+constexpr int kOffZred = kOffRsum + kRows * 2 * 4;             // [2][2][128] value zero-point sums traded
+constexpr int kOffRed = kOffZred + 2 * 2 * kRows * 4;          // [2][2][128] fp32 row maxima / sums traded
 constexpr int kPitch = kD + 1;                                 // row staging pitch (floats)
 constexpr int kOffRows = kOffK;                                // [128][129] fp32 outputs over the K/V tiles
 constexpr int kOffQinv = kOffRed + 2 * 2 * kRows * 4;          // [128] fp32
@@ -135,6 +139,13 @@ __device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// two b-bit unsigned fields -> half2 of the exact integers u: (0x6400 | u) - 1024
+template <int B>
+__device__ __forceinline__ __half2 ucodes2(uint32_t w) {
+  constexpr uint32_t f = (1u << B) - 1u;
+  const uint32_t h = (((w & ((1u << (2 * B)) - 1u)) * (1u + (1u << (16 - B)))) & (f | (f << 16))) ^ 0x64006400u;
+  return __hsub2(*reinterpret_cast<const __half2*>(&h), __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
+}
 // two b-bit two's-complement fields (bits 0..b-1 and b..2b-1 of w) -> half2
 // of the exact integers: times 1 + 2^(16-b) puts the second field at bit
 // 16; flipping the sign bit gives c + 2^(b-1), and (0x6400 | (c + 2^(b-1)))
@@ -165,9 +176,10 @@ __device__ __forceinline__ bool pair_and(int id, bool v) {
 template <int SCALE, int BITS>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ TcParams p,
                                                                   const __grid_constant__ RotParams rp) {
-  constexpr int SB = SCALE == KVQ3_SCALE_F32 ? 4 : SCALE == KVQ3_SCALE_F16 ? 2 : 1;
+  constexpr bool kAsym = SCALE == KVQ3_SCALE_E4M3_ZP;   // E4M3 scale and zero point, unsigned codes
+  constexpr int SB = SCALE == KVQ3_SCALE_F32 ? 4 : (SCALE == KVQ3_SCALE_F16 || kAsym) ? 2 : 1;
   constexpr int kCB = BITS * kD / 8;   // code bytes per vector
-  constexpr bool kLo = SCALE != KVQ3_SCALE_E4M3;   // values carry a low part of the scale
+  constexpr bool kLo = SCALE != KVQ3_SCALE_E4M3 && !kAsym;   // values carry a low part of the scale
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
@@ -188,6 +200,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   float* qinv_s = reinterpret_cast<float*>(smem + kOffQinv);
   float* ks_s = reinterpret_cast<float*>(smem + kOffKs);
   float* red_s = reinterpret_cast<float*>(smem + kOffRed);
+  float* zk_s = reinterpret_cast<float*>(smem + kOffZk);
+  float* zv_s = reinterpret_cast<float*>(smem + kOffZv);
+  float* rsum_s = reinterpret_cast<float*>(smem + kOffRsum);
+  float* zred_s = reinterpret_cast<float*>(smem + kOffZred);
 
   const CacheGeom& g = p.g;
   const int kvh = blockIdx.y;
@@ -349,6 +365,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       *reinterpret_cast<uint2*>(qa + 2 * kTile) =
           make_uint2(h2u(__floats2half2_rn(r0.x, r0.y)), h2u(__floats2half2_rn(r1.x, r1.y)));
       if (lane == 0) qinv_s[row] = ldexpf(1.0f, -ex);
+      if constexpr (kAsym) {   // sum of the q1 the MMAs see over each block (lanes 16b .. 16b + 15)
+        const float2 fh0 = __half22float2(h0), fh1 = __half22float2(h1);
+        const float2 fl0 = __half22float2(__floats2half2_rn(r0.x, r0.y));
+        const float2 fl1 = __half22float2(__floats2half2_rn(r1.x, r1.y));
+        float bs = ((fh0.x + fl0.x) + (fh0.y + fl0.y)) + ((fh1.x + fl1.x) + (fh1.y + fl1.y));
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) bs += __shfl_xor_sync(kFull, bs, o);
+        if ((lane & 15) == 0) rsum_s[row * 2 + (lane >> 4)] = bs;
+      }
     }
   }
   fence_proxy_async();   // generic stores read by the tensor cores
@@ -364,6 +389,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     const int64_t lim = row < nrows ? p.pos0 + t0 + row / p.G : -1;
     float m_used = -INFINITY;
     float2 l2 = make_float2(0.0f, 0.0f);
+    // asymmetric codes: per-row block sums of q1 (the keys' zero-point term)
+    // and this warp's share of sum_k p_k z_v(k, block) for blocks 0 and 1
+    const float2 rs0 = kAsym ? make_float2(rsum_s[row * 2], rsum_s[row * 2]) : make_float2(0.0f, 0.0f);
+    const float2 rs1 = kAsym ? make_float2(rsum_s[row * 2 + 1], rsum_s[row * 2 + 1]) : make_float2(0.0f, 0.0f);
+    float2 za0 = make_float2(0.0f, 0.0f), za1 = make_float2(0.0f, 0.0f);
     bool okw = true;   // this warp's waits all succeeded (warp-uniform)
     for (int t = 0; t < nt; ++t) {   // t counts this CTA's tiles; key tile tlo + t
       const int b = t & 1, s = t % kStages, j = t % kSP;
@@ -382,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         float4 kk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) kk[i] = ksr[i];   // (k0, k1) of keys 2i, 2i + 1
-        mbar_arrive(&raw_empty[s]);                   // done with the stage's scales and mask
+        if (!kAsym) mbar_arrive(&raw_empty[s]);       // done with the stage's scales and mask
         tc::wait_ld();
         tc::reg_fence(a);
         tc::reg_fence(c);
@@ -392,6 +422,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                         make_float2(kk[i].y, kk[i].w),
                         f2mul(make_float2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1])),
                               make_float2(kk[i].x, kk[i].z)));
+        if constexpr (kAsym) {   // + z_k(block) * sum_{d in block} q1_d
+          const float4* zkr = reinterpret_cast<const float4*>(zk_s + (s * kKeys + 32 * kh) * 2);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float4 z = zkr[i];
+            sv[i] = f2fma(make_float2(z.y, z.w), rs1, f2fma(make_float2(z.x, z.z), rs0, sv[i]));
+          }
+        }
         const int64_t k0 = (int64_t)(tlo + t) * kKeys + 32 * kh;
         if (!(km == 0xFFFFFFFFu && k0 + 31 <= lim)) {
 #pragma unroll
@@ -417,6 +455,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         const float alpha = need ? (m_used == -INFINITY ? 0.0f : ex2(m_used - m_new)) : 1.0f;
         l2.x *= alpha;
         l2.y *= alpha;
+        if constexpr (kAsym) {
+          za0 = f2mul(za0, make_float2(alpha, alpha));
+          za1 = f2mul(za1, make_float2(alpha, alpha));
+        }
         if (t > 0) {   // O holds PV up to tile t - 1: wait for it, then scale this warp's half in place
           okw = __all_sync(kFull, wait(&pv_done[(t - 1) % kSP], (uint32_t)((t - 1) / kSP) & 1u));
           if (okw) {
@@ -440,16 +482,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       const float moff = m_used == -INFINITY ? 0.0f : m_used;
       const float2 moff2 = make_float2(-moff, -moff);
       uint32_t hv[16], lv[16];
+      const float4* zvr = reinterpret_cast<const float4*>(zv_s + (s * kKeys + 32 * kh) * 2);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const float2 x = f2fma(sv[i], qinv2, moff2);
         const float2 pp = make_float2(ex2(x.x), ex2(x.y));
         l2 = f2add(l2, pp);
+        if constexpr (kAsym) {
+          const float4 z = zvr[i];
+          za0 = f2fma(pp, make_float2(z.x, z.z), za0);
+          za1 = f2fma(pp, make_float2(z.y, z.w), za1);
+        }
         const __half2 hi = __floats2half2_rn(pp.x, pp.y);
         const float2 lo = f2sub(pp, __half22float2(hi));
         hv[i] = h2u(hi);
         lv[i] = h2u(__floats2half2_rn(lo.x, lo.y));
       }
+      if (kAsym) mbar_arrive(&raw_empty[s]);   // done with the stage's zero points too
       tc::st16(tS + 16 * kh, hv);        // P hi (keys 32kh..) over S columns both warps have read
       tc::st16(tS + 32 + 16 * kh, lv);   // P lo
       tc::wait_st();
@@ -460,8 +509,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     // reads after the last tile's exchange); O of this warp's 64 columns
     const int e = (nt & 1) * 2;
     red_s[(e + kh) * kRows + row] = l2.x + l2.y;
+    if constexpr (kAsym) {
+      zred_s[(kh * 2 + 0) * kRows + row] = za0.x + za0.y;
+      zred_s[(kh * 2 + 1) * kRows + row] = za1.x + za1.y;
+    }
     bool ok = pair_and(1 + wq, okw);
     const float l = red_s[(e + kh) * kRows + row] + red_s[(e + (kh ^ 1)) * kRows + row];
+    // the zero-point share of O for this warp's columns (block kh)
+    const float zo = kAsym ? zred_s[(0 * 2 + kh) * kRows + row] + zred_s[(1 * 2 + kh) * kRows + row] : 0.0f;
     if (ok) ok = __all_sync(kFull, wait(&pv_done[(nt - 1) % kSP], (uint32_t)((nt - 1) / kSP) & 1u));
     tc::fence_after();
     // a whole unit: normalised rows into the staging; half of a split unit:
@@ -476,6 +531,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         tc::ld32(tmem + lanes + kColO + 64u * kh + 32u * c4, o);
         tc::wait_ld();
         tc::reg_fence(o);
+        if constexpr (kAsym) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) + zo);
+        }
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[i] = 0u;
@@ -528,10 +587,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             const int bit = 8 * BITS * gq;
             const uint32_t wg = (bit & 31) ? __funnelshift_r(w[bit >> 5], w[(bit >> 5) + 1], bit & 31) : w[bit >> 5];
             uint4 o;
-            o.x = h2u(codes2<BITS>(wg));
-            o.y = h2u(codes2<BITS>(wg >> (2 * BITS)));
-            o.z = h2u(codes2<BITS>(wg >> (4 * BITS)));
-            o.w = h2u(codes2<BITS>(wg >> (6 * BITS)));
+            if constexpr (kAsym) {
+              o.x = h2u(ucodes2<BITS>(wg));
+              o.y = h2u(ucodes2<BITS>(wg >> (2 * BITS)));
+              o.z = h2u(ucodes2<BITS>(wg >> (4 * BITS)));
+              o.w = h2u(ucodes2<BITS>(wg >> (6 * BITS)));
+            } else {
+              o.x = h2u(codes2<BITS>(wg));
+              o.y = h2u(codes2<BITS>(wg >> (2 * BITS)));
+              o.z = h2u(codes2<BITS>(wg >> (4 * BITS)));
+              o.w = h2u(codes2<BITS>(wg >> (6 * BITS)));
+            }
             *reinterpret_cast<uint4*>(kt + (4 * r + gq) * 128) = o;
           }
         }
@@ -540,7 +606,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         if (SB == 4) bits = *reinterpret_cast<const uint32_t*>(sp);
         else if (SB == 2) bits = *reinterpret_cast<const uint16_t*>(sp);
         else bits = *sp;
-        ks_s[(s * kKeys + key) * 2 + hd] = kv ? decode_scale(bits, SCALE) : 0.0f;
+        if constexpr (kAsym) {   // scale byte, then zero-point byte; the value's zero point as well
+          const uint32_t vbits = *reinterpret_cast<const uint16_t*>(st + kRawVs + (key * 2 + hd) * SB);
+          ks_s[(s * kKeys + key) * 2 + hd] = kv ? decode_scale(bits & 0xFFu, KVQ3_SCALE_E4M3) : 0.0f;
+          zk_s[(s * kKeys + key) * 2 + hd] = kv ? decode_scale(bits >> 8, KVQ3_SCALE_E4M3) : 0.0f;
+          zv_s[(s * kKeys + key) * 2 + hd] = kv ? decode_scale(vbits >> 8, KVQ3_SCALE_E4M3) : 0.0f;
+        } else {
+          ks_s[(s * kKeys + key) * 2 + hd] = kv ? decode_scale(bits, SCALE) : 0.0f;
+        }
         if (dt == 0) key_mask[s] = vm;
       }
       fence_proxy_async();
@@ -554,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         if (SB == 4) bits = *reinterpret_cast<const uint32_t*>(sp);
         else if (SB == 2) bits = *reinterpret_cast<const uint16_t*>(sp);
         else bits = *sp;
-        const float sv = kv ? decode_scale(bits, SCALE) : 0.0f;
+        const float sv = kv ? decode_scale(kAsym ? (bits & 0xFFu) : bits, kAsym ? KVQ3_SCALE_E4M3 : SCALE) : 0.0f;
         // top 9 significant bits (8 at b = 4): c s_hi stays within fp16's 11
         const float s_hi = __uint_as_float(__float_as_uint(sv) & (BITS == 4 ? 0xFFFF0000u : 0xFFFF8000u));
         const __half2 hs = __float2half2_rn(s_hi), ls = __float2half2_rn(sv - s_hi);
@@ -570,8 +643,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           for (int gq = 0; gq < 4; ++gq) {
             const int bit = 8 * BITS * gq;
             const uint32_t wg = (bit & 31) ? __funnelshift_r(w[bit >> 5], w[(bit >> 5) + 1], bit & 31) : w[bit >> 5];
-            const __half2 c0 = codes2<BITS>(wg), c1 = codes2<BITS>(wg >> (2 * BITS)),
-                          c2 = codes2<BITS>(wg >> (4 * BITS)), c3 = codes2<BITS>(wg >> (6 * BITS));
+            __half2 c0, c1, c2, c3;
+            if constexpr (kAsym) {   // u s: the zero point's share is summed by the softmax
+              c0 = ucodes2<BITS>(wg), c1 = ucodes2<BITS>(wg >> (2 * BITS));
+              c2 = ucodes2<BITS>(wg >> (4 * BITS)), c3 = ucodes2<BITS>(wg >> (6 * BITS));
+            } else {
+              c0 = codes2<BITS>(wg), c1 = codes2<BITS>(wg >> (2 * BITS));
+              c2 = codes2<BITS>(wg >> (4 * BITS)), c3 = codes2<BITS>(wg >> (6 * BITS));
+            }
             uint4 o;
             o.x = h2u(__hmul2(c0, hs));
             o.y = h2u(__hmul2(c1, hs));
@@ -732,6 +811,8 @@ kvq3_status launch_tc(const TcParams& p, const RotParams& rp, cudaStream_t st) {
 
 template <int BITS>
 kvq3_status launch_bits(const CacheGeom& g, const TcParams& p, const RotParams& rp, cudaStream_t st) {
+  if constexpr (BITS == 3)
+    if (g.scale_type == KVQ3_SCALE_E4M3_ZP) return launch_tc<KVQ3_SCALE_E4M3_ZP, 3>(p, rp, st);
   if (g.scale_type == KVQ3_SCALE_F32) return launch_tc<KVQ3_SCALE_F32, BITS>(p, rp, st);
   if (g.scale_type == KVQ3_SCALE_F16) return launch_tc<KVQ3_SCALE_F16, BITS>(p, rp, st);
   return launch_tc<KVQ3_SCALE_E4M3, BITS>(p, rp, st);
@@ -742,8 +823,8 @@ kvq3_status launch_bits(const CacheGeom& g, const TcParams& p, const RotParams& 
 namespace kvq3 {
 
 bool prefill_tc_supported(const CacheGeom& g, int32_t hq) {
-  return g.d == kD && g.bits >= 2 && g.bits <= 4 && g.block == 64 && g.scale_type != KVQ3_SCALE_E4M3_ZP &&
-         hq / g.hkv <= kRows;
+  return g.d == kD && g.bits >= 2 && g.bits <= 4 && g.block == 64 &&
+         (g.scale_type != KVQ3_SCALE_E4M3_ZP || g.bits == 3) && hq / g.hkv <= kRows;
 }
 
 // Workspace of the tcgen05 path: one counter per unit (128 query rows of a kv

@@ -122,7 +122,10 @@ def test_decode_isolated_matches_oracle_asym(cfg):
 
 
 @pytest.mark.parametrize("cfg", [(dict(d=128, block=64, page=64, lens=(300,), hkv=2, hq=8), 0, 200, 100),
-                                 (dict(d=256, block=64, page=16, lens=(300, 180), hkv=2, hq=8, paged=True), 1, 100, 80)],
+                                 (dict(d=256, block=64, page=16, lens=(300, 180), hkv=2, hq=8, paged=True), 1, 100, 80),
+                                 # the tcgen05 kernel with units split in two key ranges, and G = 16
+                                 (dict(d=128, block=64, page=32, lens=(900,), hkv=2, hq=8, paged=True), 0, 600, 300),
+                                 (dict(d=128, block=64, page=64, lens=(600,), hkv=1, hq=16), 0, 550, 50)],
                          ids=lambda c: _did(c[0]) + f"-pos{c[2]}-n{c[3]}")
 def test_prefill_matches_oracle_asym(cfg):
     import torch
