@@ -1,6 +1,7 @@
 // Chunked-prefill attention over the packed cache on the 5th-generation tensor
 // cores (tcgen05, accumulators in tensor memory): head dimension 128,
-// symmetric codes of b = 2, 3 or 4 bits, quantisation blocks of 64.
+// quantisation blocks of 64, symmetric codes of b = 2, 3 or 4 bits or the
+// asymmetric 3-bit codes (E4M3 scale and zero point).
 //
 // "Orthogonally mixed 3-bit KV cache", Implementation notes (read path) and
 // Key formulas, with the causal mask of a prefill chunk: query token i sits at
@@ -8,15 +9,20 @@
 // "Orthogonal Invariance in Activation Space", sections 4.1 and 4.3: the cache
 // is read with dequantisation fused into the attention products.
 //
-// One CTA = 128 query rows of one kv head (a row is a (query token, query
-// head) pair: 128 / G tokens x G heads), one row per TMEM lane.  It walks the
-// sequence in 64-key tiles up to its last row's position.
+// A unit = 128 query rows of one kv head (a row is a (query token, query
+// head) pair: 128 / G tokens x G heads), one row per TMEM lane.  Its keys are
+// walked in 64-key tiles up to its last row's position: by one CTA, or, for a
+// unit of at least kMinSplit tiles, by two CTAs over the two halves of the
+// tiles, each leaving O (unnormalised), its reference maximum and its row sum
+// in the workspace; the second to finish (a per-unit counter) merges them by
+// log-sum-exp.
 //
 // Arithmetic.  q1 = U q is scaled by sm_scale * log2(e) and a per-row power
 // of two and kept as hi + lo fp16 halves.  Key codes enter the products as
 // exact small fp16 integers, one accumulator per 64-dimension scale block:
 //   S_b = (q1_hi + q1_lo)[block b] . c_k[block b]       (two MMAs per k-step)
-// and the key scales are applied in fp32 afterwards: s = S_0 k_0 + S_1 k_1.
+// and the key scales are applied in fp32 afterwards: s = S_0 k_0 + S_1 k_1
+// (asymmetric codes: unsigned u, and s gains z_k(b) * sum_{d in b} q1_d).
 // The online softmax (base 2, lazy rescaling: the running maximum moves only
 // when a row's maximum grows by more than 2^8) gives p <= 2^8, kept as hi + lo
 // fp16 halves.  A value's scale is split as s_v = s_hi + s_lo with s_hi its
@@ -24,8 +30,10 @@
 // (|c| <= 2^(b-1)) are exact fp16 numbers and
 //   O += p_hi . (c s_hi) + p_lo . (c s_hi) + p_hi . (c s_lo)
 // over full 128-dimension rows (the dropped p_lo . (c s_lo) is below 2^-20 of
-// the product; E4M3 scales have s_lo = 0 and skip the third MMA).  Dequantised
-// values must lie in the fp16 range, as for every kernel of this library.
+// the product; E4M3 scales have s_lo = 0 and skip the third MMA; asymmetric
+// codes enter as u s, and each softmax thread adds sum_k p_k z_v(k, b) to its
+// row's block b).  Dequantised values must lie in the fp16 range, as for every
+// kernel of this library.
 //
 // Roles (15 warps):
 //  * warps 6-13, softmax: warps w and w + 4 share the 32 rows of TMEM lane
@@ -41,7 +49,8 @@
 //    so that a wait of one never holds up the other's MMAs;
 //  * warp 1, lane 0: issues the bulk copies of packed codes and scales into a
 //    ring of raw stages, up to kStages tiles ahead.
-// TMEM: q1 hi / lo (128 columns), two S/P buffers (128 each), O (128).
+// TMEM: three S/P buffers (128 columns each) and O (128); q1 hi / lo live in
+// shared memory as the A operand of QK^T.
 // Every hand-off is an mbarrier; every wait is bounded (a time-out sets
 // KVQ3_DEV_TIMEOUT and the CTA winds down: MMAs and copies in flight are
 // drained and TMEM freed before it exits).
