@@ -31,8 +31,11 @@
 //   O += p_hi . (c s_hi) + p_lo . (c s_hi) + p_hi . (c s_lo)
 // over full 128-dimension rows (the dropped p_lo . (c s_lo) is below 2^-20 of
 // the product; E4M3 scales have s_lo = 0 and skip the third MMA; asymmetric
-// codes enter as u s, and each softmax thread adds sum_k p_k z_v(k, b) to its
-// row's block b).  Dequantised values must lie in the fp16 range, as for every
+// codes enter centred, as (u - 2^(b-1)) s, and each softmax thread adds
+// sum_k p_k (z_v(k, b) + 2^(b-1) s_v(k, b)) to its row's block b: the
+// accumulator in tensor memory, which adds each tile's products to the sum of
+// the tiles before it, then holds sums of the size of the result rather than
+// of u s >= 0).  Dequantised values must lie in the fp16 range, as for every
 // kernel of this library.
 //
 // Roles (15 warps):
@@ -154,6 +157,14 @@ __device__ __forceinline__ __half2 ucodes2(uint32_t w) {
   constexpr uint32_t f = (1u << B) - 1u;
   const uint32_t h = (((w & ((1u << (2 * B)) - 1u)) * (1u + (1u << (16 - B)))) & (f | (f << 16))) ^ 0x64006400u;
   return __hsub2(*reinterpret_cast<const __half2*>(&h), __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
+}
+// two unsigned b-bit fields -> half2 of the centred integers u - 2^(b-1)
+template <int B>
+__device__ __forceinline__ __half2 ccodes2(uint32_t w) {
+  constexpr uint32_t f = (1u << B) - 1u;
+  const uint32_t h = (((w & ((1u << (2 * B)) - 1u)) * (1u + (1u << (16 - B)))) & (f | (f << 16))) ^ 0x64006400u;
+  const __half off = __ushort_as_half((unsigned short)(0x6400u | (1u << (B - 1))));
+  return __hsub2(*reinterpret_cast<const __half2*>(&h), __halves2half2(off, off));
 }
 // two b-bit two's-complement fields (bits 0..b-1 and b..2b-1 of w) -> half2
 // of the exact integers: times 1 + 2^(16-b) puts the second field at bit
@@ -619,7 +630,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           const uint32_t vbits = *reinterpret_cast<const uint16_t*>(st + kRawVs + (key * 2 + hd) * SB);
           ks_s[(s * kKeys + key) * 2 + hd] = kv ? decode_scale(bits & 0xFFu, KVQ3_SCALE_E4M3) : 0.0f;
           zk_s[(s * kKeys + key) * 2 + hd] = kv ? decode_scale(bits >> 8, KVQ3_SCALE_E4M3) : 0.0f;
-          zv_s[(s * kKeys + key) * 2 + hd] = kv ? decode_scale(vbits >> 8, KVQ3_SCALE_E4M3) : 0.0f;
+          // values enter the MMAs centred, (u - 2^(b-1)) s: their zero point
+          // gains 2^(b-1) s, so that the accumulator in tensor memory holds
+          // sums of the size of the result, not of u s >= 0
+          zv_s[(s * kKeys + key) * 2 + hd] =
+              kv ? decode_scale(vbits >> 8, KVQ3_SCALE_E4M3) +
+                       (float)(1 << (BITS - 1)) * decode_scale(vbits & 0xFFu, KVQ3_SCALE_E4M3)
+                 : 0.0f;
         } else {
           ks_s[(s * kKeys + key) * 2 + hd] = kv ? decode_scale(bits, SCALE) : 0.0f;
         }
@@ -653,9 +670,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             const int bit = 8 * BITS * gq;
             const uint32_t wg = (bit & 31) ? __funnelshift_r(w[bit >> 5], w[(bit >> 5) + 1], bit & 31) : w[bit >> 5];
             __half2 c0, c1, c2, c3;
-            if constexpr (kAsym) {   // u s: the zero point's share is summed by the softmax
-              c0 = ucodes2<BITS>(wg), c1 = ucodes2<BITS>(wg >> (2 * BITS));
-              c2 = ucodes2<BITS>(wg >> (4 * BITS)), c3 = ucodes2<BITS>(wg >> (6 * BITS));
+            if constexpr (kAsym) {   // (u - 2^(b-1)) s: the zero point's share is summed by the softmax
+              c0 = ccodes2<BITS>(wg), c1 = ccodes2<BITS>(wg >> (2 * BITS));
+              c2 = ccodes2<BITS>(wg >> (4 * BITS)), c3 = ccodes2<BITS>(wg >> (6 * BITS));
             } else {
               c0 = codes2<BITS>(wg), c1 = codes2<BITS>(wg >> (2 * BITS));
               c2 = codes2<BITS>(wg >> (4 * BITS)), c3 = codes2<BITS>(wg >> (6 * BITS));

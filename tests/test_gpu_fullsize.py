@@ -2,7 +2,8 @@
 times: the GPU writes and decodes the whole workload; the oracle recomputes
 sampled (sequence, kv head) units one by one from the same seeded inputs
 (codes of sampled positions bit-exact outside rounding boundaries; decode
-outputs of the sampled heads within 2e-3 * rms of those outputs)."""
+outputs of the sampled heads within 2e-3 * rms of those outputs; prefill
+attention of sampled query tokens within the same bar)."""
 import math
 
 import numpy as np
@@ -143,3 +144,38 @@ class _Shift:
 
     def __getitem__(self, sl):
         return self.rows[sl.start - self.t0:sl.stop - self.t0]
+
+
+@pytest.mark.parametrize("bits,scale", [(0, ""), (4, ""), (0, "e4m3zp")], ids=["default", "b4", "asym"])
+def test_fullsize_prefill_attention(oracle, bits, scale):
+    # the prefill-attention step bench.py times (2,048 queries at the end of a
+    # 32K-token cache, split units merged in the workspace); the oracle
+    # recomputes sampled query tokens -- the first and last rows of query
+    # blocks and of the chunk -- over its own cache of the same inputs
+    import bench
+    import torch
+    saved = bench.BITS_OVERRIDE, bench.SCALE_OVERRIDE
+    bench.BITS_OVERRIDE, bench.SCALE_OVERRIDE = bits, scale
+    try:
+        w = bench.workload("prefill_attn")
+    finally:
+        bench.BITS_OVERRIDE, bench.SCALE_OVERRIDE = saved
+    st = bench.PrefillAttnWorkload(torch.device("cuda:0"), w)
+    st.step()
+    torch.cuda.synchronize()
+    assert int(st.status.item()) == 0
+    out = st.out.cpu().numpy().astype(np.float64)
+    G = w.num_q_heads // w.num_kv_heads
+    q = I.q_np(w.data, w.chunk, w.num_q_heads, 0)
+    got, ref = [], []
+    for kvh in (0, 6):
+        lay, pool, U, _, _ = _oracle_unit(oracle, w, [w.seq_len], 0, kvh)
+        for i in (0, 31, 32, 1000, w.chunk - 32, w.chunk - 1):
+            qs = q[i:i + 1, kvh * G:(kvh + 1) * G]
+            ref.append(oracle.prefill(pool, lay, U, qs, 0, st.pos0 + i)[0])
+            got.append(out[i, kvh * G:(kvh + 1) * G])
+    got, ref = np.array(got), np.array(ref)
+    rms = math.sqrt(float(np.mean(ref ** 2)))
+    err = float(np.abs(got - ref).max())
+    print(f"prefill attention {w.bits}-bit {w.scale}: max|err|/rms = {err / rms:.3e}")
+    assert err <= TOL_DECODE * rms
