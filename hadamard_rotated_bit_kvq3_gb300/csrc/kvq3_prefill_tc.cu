@@ -12,10 +12,13 @@
 // A unit = 128 query rows of one kv head (a row is a (query token, query
 // head) pair: 128 / G tokens x G heads), one row per TMEM lane.  Its keys are
 // walked in 64-key tiles up to its last row's position: by one CTA, or, for a
-// unit of at least kMinSplit tiles, by two CTAs over the two halves of the
-// tiles, each leaving O (unnormalised), its reference maximum and its row sum
-// in the workspace; the second to finish (a per-unit counter) merges them by
-// log-sum-exp.
+// unit of at least kMinSplit tiles, by np CTAs over equal shares of the tiles
+// (two, or one per kChain tiles, at most kMaxParts), each leaving O
+// (unnormalised), its reference maximum and its row sum in the workspace; the
+// last to finish (a per-unit counter) merges them by log-sum-exp.  Bounding a
+// CTA's share also bounds how many tiles of products the accumulator in tensor
+// memory sums, and the error of that sum grows with the count (about linearly:
+// 3.8e-4 of rms(out) at 48-64 tiles, 1.8e-3 at 240, on 4-bit parity cases).
 //
 // Arithmetic.  q1 = U q is scaled by sm_scale * log2(e) and a per-row power
 // of two and kept as hi + lo fp16 halves.  Key codes enter the products as
@@ -59,6 +62,8 @@
 // drained and TMEM freed before it exits).
 #include <string.h>
 
+#include <algorithm>
+
 #include "kvq3_internal.h"
 #include "kvq3_tc.cuh"
 
@@ -81,7 +86,9 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kSP = 3;                // S/P buffers in TMEM
 constexpr uint32_t kColSP = 0, kColO = 384;   // TMEM: S/P buffer j at 128 j, O
 constexpr float kRescale = 8.0f;      // log2 of the largest p between rescales
-constexpr int kMinSplit = 8;          // a unit of at least this many key tiles runs as two CTAs
+constexpr int kMinSplit = 8;          // a unit of at least this many key tiles runs as several CTAs
+constexpr int kChain = 128;           // ... each over at most this many key tiles (while kMaxParts allow)
+constexpr int kMaxParts = 16;         // CTAs a unit can run as
 constexpr int kPartStride = 132;      // floats a row of a partial takes: O (128), m, l, padding
 
 // shared memory (bytes)
@@ -123,8 +130,9 @@ struct TcParams {
   float qk_scale;       // sm_scale * log2(e)
   float inv_sqrt_d;
   uint32_t wait_limit;
-  int32_t* counters;    // [units] halves of a split unit done (zeroed before the launch)
-  float* partial;       // [units][2][128 rows][kPartStride]: O (unnormalised), m, l of each half
+  int32_t parts;        // CTAs in the grid per unit (2 .. kMaxParts)
+  int32_t* counters;    // [units] parts of a split unit done (zeroed before the launch)
+  float* partial;       // [units][parts][128 rows][kPartStride]: O (unnormalised), m, l of each part
   int64_t ws_floats;    // floats of the partial area (bounds of the checked build)
 };
 
@@ -227,21 +235,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 
   const CacheGeom& g = p.g;
   const int kvh = blockIdx.y;
-  const int nqb = (int)gridDim.x >> 1;
-  const int qblk = nqb - 1 - ((int)blockIdx.x >> 1);       // longest query blocks first
-  const int half = (int)blockIdx.x & 1;                    // which part of the unit's keys
+  const int nqb = (int)gridDim.x / p.parts;
+  const int qblk = nqb - 1 - (int)blockIdx.x / p.parts;    // longest query blocks first
+  const int part = (int)blockIdx.x % p.parts;              // which part of the unit's keys
   const int unit = kvh * nqb + qblk;
   const int t0 = qblk * p.qb;
   const int ntok = min(p.qb, p.n - t0);
   const int nrows = ntok * p.G;
   const int64_t kmax = p.pos0 + t0 + ntok - 1;             // last position any row attends to
   const int T = (int)(kmax / kKeys) + 1;                   // key tiles of the unit
-  // a long unit runs as two CTAs, tiles [0, T/2) and [T/2, T), merged by the
-  // second to finish; a short one as one CTA (the other returns at once)
-  const bool split = T >= kMinSplit;
-  if (!split && half == 1) return;
-  const int tlo = split && half == 1 ? T / 2 : 0;
-  const int nt = split ? (half == 0 ? T / 2 : T - T / 2) : T;   // key tiles of this CTA
+  // a long unit runs as np CTAs over equal shares of its key tiles, at most
+  // kChain each (so that no accumulation in tensor memory runs longer), each
+  // leaving its partial in the workspace, merged by the last to finish; a
+  // short one as one CTA (the unit's other CTAs return at once)
+  const int np = T < kMinSplit ? 1 : min(p.parts, max(2, (T + kChain - 1) / kChain));
+  const bool split = np > 1;
+  if (part >= np) return;
+  const int tlo = (int)((int64_t)T * part / np);
+  const int nt = (int)((int64_t)T * (part + 1) / np) - tlo;   // key tiles of this CTA
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -539,10 +550,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     const float zo = kAsym ? zred_s[(0 * 2 + kh) * kRows + row] + zred_s[(1 * 2 + kh) * kRows + row] : 0.0f;
     if (ok) ok = __all_sync(kFull, wait(&pv_done[(nt - 1) % kSP], (uint32_t)((nt - 1) / kSP) & 1u));
     tc::fence_after();
-    // a whole unit: normalised rows into the staging; half of a split unit:
+    // a whole unit: normalised rows into the staging; part of a split unit:
     // O (unnormalised, relative to 2^m_used), m_used and l to its partial
     const float inv = split ? 1.0f : (ok && l > 0.0f) ? 1.0f / l : 0.0f;
-    float* prow = p.partial + ((int64_t)(unit * 2 + half) * kRows + row) * kPartStride;
+    float* prow = p.partial + ((int64_t)(unit * p.parts + part) * kRows + row) * kPartStride;
     const bool pw = split && KVQ3_CHECK(p.status, in_range((prow - p.partial), kPartStride, p.ws_floats));
 #pragma unroll
     for (int c4 = 0; c4 < 2; ++c4) {
@@ -770,37 +781,44 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   }
   __syncthreads();
 
-  // ---- a split unit: the second half to finish merges the two partials
+  // ---- a split unit: the last part to finish merges the partials
   volatile int32_t* order = reinterpret_cast<volatile int32_t*>(tmem_slot + 2);
   if (split) {
-    __threadfence();   // this half's partial before its count
+    __threadfence();   // this part's partial before its count
     __syncthreads();
     if (tid == 0) *order = atomicAdd(p.counters + unit, 1);
     __syncthreads();
-    if (*order == 1 && tid < 2 * kRows) {
+    if (*order == np - 1 && tid < 2 * kRows) {
       __threadfence();
       const int row = tid & (kRows - 1), ch = tid >> 7;   // 64 columns each
-      const float* pa = p.partial + ((int64_t)(unit * 2) * kRows + row) * kPartStride;
-      const float* pb = pa + (int64_t)kRows * kPartStride;
-      const float ma = __ldcg(pa + kD), la = __ldcg(pa + kD + 1), mb = __ldcg(pb + kD), lb = __ldcg(pb + kD + 1);
-      const float m = fmaxf(ma, mb);
-      const float fa = ma == -INFINITY ? 0.0f : ex2(ma - m), fb = mb == -INFINITY ? 0.0f : ex2(mb - m);
-      const float lt = la * fa + lb * fb;
+      const float* p0 = p.partial + ((int64_t)(unit * p.parts) * kRows + row) * kPartStride;
+      const int64_t ps = (int64_t)kRows * kPartStride;    // between parts
+      float m = -INFINITY;
+      for (int k = 0; k < np; ++k) m = fmaxf(m, __ldcg(p0 + k * ps + kD));
+      float* r = rows + row * kPitch + 64 * ch;
+#pragma unroll 4
+      for (int c = 0; c < 64; ++c) r[c] = 0.0f;
+      float lt = 0.0f;
+      for (int k = 0; k < np; ++k) {
+        const float* pk = p0 + k * ps;
+        const float mk = __ldcg(pk + kD), fk = mk == -INFINITY ? 0.0f : ex2(mk - m);
+        lt = fmaf(__ldcg(pk + kD + 1), fk, lt);
+#pragma unroll 4
+        for (int c = 0; c < 64; c += 4) {
+          const float4 a = __ldcg(reinterpret_cast<const float4*>(pk + 64 * ch + c));
+          r[c] = fmaf(a.x, fk, r[c]);
+          r[c + 1] = fmaf(a.y, fk, r[c + 1]);
+          r[c + 2] = fmaf(a.z, fk, r[c + 2]);
+          r[c + 3] = fmaf(a.w, fk, r[c + 3]);
+        }
+      }
       const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
 #pragma unroll 4
-      for (int c = 0; c < 64; c += 4) {
-        const float4 a = __ldcg(reinterpret_cast<const float4*>(pa + 64 * ch + c));
-        const float4 b = __ldcg(reinterpret_cast<const float4*>(pb + 64 * ch + c));
-        float* r = rows + row * kPitch + 64 * ch + c;
-        r[0] = (a.x * fa + b.x * fb) * inv;
-        r[1] = (a.y * fa + b.y * fb) * inv;
-        r[2] = (a.z * fa + b.z * fb) * inv;
-        r[3] = (a.w * fa + b.w * fb) * inv;
-      }
+      for (int c = 0; c < 64; ++c) r[c] *= inv;
     }
     __syncthreads();
   }
-  const bool write_out = !split || *order == 1;
+  const bool write_out = !split || *order == np - 1;
 
   // ---- outputs: rotate back with U^T (warp per row) and store
   {
@@ -830,7 +848,7 @@ kvq3_status launch_tc(const TcParams& p, const RotParams& rp, cudaStream_t st) {
   auto k = prefill_tc_kernel<SCALE, BITS>;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
     return KVQ3_ERR_CUDA;
-  const dim3 grid((unsigned)(2 * ((p.n + p.qb - 1) / p.qb)), (unsigned)p.g.hkv);   // two CTAs a unit
+  const dim3 grid((unsigned)(p.parts * ((p.n + p.qb - 1) / p.qb)), (unsigned)p.g.hkv);
   k<<<grid, kThreads, kSmem, st>>>(p, rp);
   return cudaGetLastError() == cudaSuccess ? KVQ3_OK : KVQ3_ERR_CUDA;
 }
@@ -854,10 +872,18 @@ bool prefill_tc_supported(const CacheGeom& g, int32_t hq) {
 }
 
 // Workspace of the tcgen05 path: one counter per unit (128 query rows of a kv
-// head), then per unit two partials of 128 rows x kPartStride floats.
+// head), then per unit one partial of 128 rows x kPartStride floats per CTA
+// the unit can run as (parts_for the longest context the cache holds).
+// CTAs per unit for units of up to `tiles` key tiles: enough for kChain
+// tiles each, at least 2, at most kMaxParts
+static int parts_for(int64_t tiles) {
+  return (int)std::min<int64_t>(kMaxParts, std::max<int64_t>(2, (tiles + kChain - 1) / kChain));
+}
+
 size_t prefill_tc_workspace(const CacheGeom& g, int32_t hq, int64_t n_q) {
   const int64_t units = (n_q + kRows / (hq / g.hkv) - 1) / (kRows / (hq / g.hkv)) * g.hkv;
-  return (size_t)((units * 4 + 255) / 256 * 256) + (size_t)units * 2 * kRows * kPartStride * sizeof(float);
+  const int parts = parts_for(((int64_t)g.max_pages * g.page_size + kKeys - 1) / kKeys);   // the longest context the cache holds
+  return (size_t)((units * 4 + 255) / 256 * 256) + (size_t)units * parts * kRows * kPartStride * sizeof(float);
 }
 
 // tcgen05 path of kvq3_prefill_attn; arguments already checked.
@@ -885,6 +911,10 @@ kvq3_status prefill_tc(const CacheGeom& g, const kvq3_cache* cache, int32_t seq,
   p.wait_limit = wait_limit;
   const int64_t units = (n_q + p.qb - 1) / p.qb * g.hkv;
   const size_t cbytes = (size_t)((units * 4 + 255) / 256 * 256);
+  // the longest unit (the last query block) attends to pos0 + n_q keys; the
+  // workspace holds parts_for() of the cache's capacity, which is not less
+  p.parts = std::min(parts_for((pos0 + n_q + kKeys - 1) / kKeys),
+                     parts_for(((int64_t)g.max_pages * g.page_size + kKeys - 1) / kKeys));
   p.counters = static_cast<int32_t*>(workspace);
   p.partial = reinterpret_cast<float*>(static_cast<char*>(workspace) + cbytes);
   p.ws_floats = (int64_t)((ws_bytes - cbytes) / sizeof(float));

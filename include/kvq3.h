@@ -355,8 +355,9 @@ kvq3_status kvq3_decode_attn_noalloc(kvq3_rotation rot, const kvq3_cache_desc *d
  * means 1/sqrt(d); Hq a multiple of Hkv with Hq/Hkv <= 16.  Internally the
  * queries form tiles of up to 8 (query token, head) pairs per kv head; at
  * d = 128 with symmetric codes and blocks of 64, units of 128 such rows, a
- * long unit's keys split in two ranges whose partial results meet in the
- * workspace.
+ * long unit's keys split in 2 to 16 ranges (one per 8,192 keys) whose
+ * partial results meet in the workspace, so the workspace grows with the
+ * longest context the cache holds, max_pages_per_seq * P.
  * workspace:
  * device, ws_bytes >= kvq3_prefill_workspace_size(desc, Hq, n_q), 256-byte
  * aligned; calls sharing it must not overlap.  n_q = 0 is a no-op;

@@ -33,9 +33,12 @@ PREFILL_CASES = [
     (dict(d=128, block=64, scale="e4m3", page=32, lens=(500,), hkv=4, hq=8, paged=True), 0, 499, 1),   # one query
     (dict(d=128, block=64, scale="f32", page=16, lens=(260,), hkv=1, hq=12), 0, 0, 260),      # G=12: 120-row CTAs, from 0
     (dict(d=128, block=64, scale="e4m3", page=64, lens=(1100,), hkv=2, hq=4, flags=7), 0, 1000, 100),  # SO(4) pairs
-    # units of eight or more key tiles run as two CTAs over the halves of their keys, merged in the workspace
+    # units of eight or more key tiles run as several CTAs over equal shares of their keys (two, or one
+    # per 128 tiles), merged in the workspace
     (dict(d=128, block=64, scale="f16", page=16, lens=(40, 900), hkv=2, hq=8, paged=True), 1, 500, 300),  # 4 pages a tile
     (dict(d=128, block=64, scale="f32", page=32, lens=(1300,), hkv=1, hq=16), 0, 1250, 50),    # G=16, 20 tiles
+    (dict(d=128, block=64, scale="f16", page=64, lens=(17000,), hkv=1, hq=4), 0, 16992, 8),    # 266 tiles: 3 parts
+    (dict(d=128, block=64, scale="e4m3", page=32, lens=(25000, 300), hkv=1, hq=8, paged=True), 0, 24990, 10),  # 4 parts
 ]
 
 
@@ -149,24 +152,28 @@ def test_prefill_bad_page_flags_and_masks():
 def test_prefill_workspace_covers_split_units():
     import hadamard_rotated_bit_kvq3_gb300 as K
     # d = 128, 3-bit symmetric codes, blocks of 64: the tcgen05 path, whose
-    # units (128 (token, head) rows of a kv head) may run as two CTAs that
-    # meet in the workspace: a counter per unit, then two partials of
-    # 128 rows x 132 floats per unit, after the 256-byte aligned counters
+    # units (128 (token, head) rows of a kv head) may run as several CTAs
+    # that meet in the workspace: a counter per unit, then one partial of
+    # 128 rows x 132 floats per CTA of the unit, after the 256-byte aligned
+    # counters; a unit runs as at most max(2, ceil(tiles / 128)) CTAs (16 at
+    # most), tiles = the 64-key tiles of the longest context the cache holds
     # (the size also covers the decode kernel's plan, which asks the device)
     def desc(**kw):
         base = dict(head_dim=128, num_kv_heads=8, block=64, bits=3, scale_type=1, eps=1e-6,
                     page_size=128, batch=1, max_pages_per_seq=256, reserved=0, num_pages=256)
         base.update(kw)
         return K.CacheDesc(**base)
-    for hq, n in ((32, 2048), (32, 1), (24, 300), (8, 129), (128, 5)):
-        g = hq // 8
-        units = -(-n // (128 // g)) * 8
-        need = -(-units * 4 // 256) * 256 + units * 2 * 128 * 132 * 4
-        if g > 16:   # more than 16 query heads per kv head: refused
-            with pytest.raises(K.Kvq3Error):
-                K.kvq3_prefill_workspace_size(desc(), hq, n)
-            continue
-        assert K.kvq3_prefill_workspace_size(desc(), hq, n) >= need, (hq, n)
+    for maxp, parts in ((256, 4), (4, 2), (65, 2), (129, 3), (4096, 16)):
+        for hq, n in ((32, 2048), (32, 1), (24, 300), (8, 129), (128, 5)):
+            g = hq // 8
+            units = -(-n // (128 // g)) * 8
+            need = -(-units * 4 // 256) * 256 + units * parts * 128 * 132 * 4
+            d = desc(max_pages_per_seq=maxp, num_pages=maxp)
+            if g > 16:   # more than 16 query heads per kv head: refused
+                with pytest.raises(K.Kvq3Error):
+                    K.kvq3_prefill_workspace_size(d, hq, n)
+                continue
+            assert K.kvq3_prefill_workspace_size(d, hq, n) >= need, (maxp, hq, n)
     # other formats run on the decode kernel's prefill variant: no partials,
     # far less than the tcgen05 path would ask for
     small = K.kvq3_prefill_workspace_size(desc(block=32), 32, 2048)
