@@ -166,7 +166,8 @@ static kvq3_status prefill_attn_impl(kvq3_rotation rot, const kvq3_cache_desc* d
       pos0 + n_q > (int64_t)vg.max_pages * vg.page_size || pos0 + n_q >= ((int64_t)1 << 31))
     return KVQ3_ERR_INVALID_ARG;
   if (n_q == 0) return KVQ3_OK;
-  if (!q || !out) return KVQ3_ERR_INVALID_ARG;
+  if (!q || !out || (reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) % 16 != 0)
+    return KVQ3_ERR_INVALID_ARG;   // 16-byte accesses to both
   {
     CacheGeom g;   // the real geometry for the cache checks (lengths unused)
     make_geom(desc, &g);

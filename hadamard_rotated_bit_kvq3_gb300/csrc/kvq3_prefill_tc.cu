@@ -354,6 +354,31 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     }
   };
 
+  // ---- the unit's fp16 query rows (row = token * G + head) staged in the
+  // key/value tile area, idle until the roles start: every thread's 16-byte
+  // loads in flight at once, rather than one row's latency after another
+  uint8_t* qrows = smem + kOffK;   // [128 rows][256 B]
+  static_assert(kRows * kD * 2 <= kOffQ - kOffK, "query staging fits the key/value tiles");
+  {
+    constexpr int kPieces = kRows * kD * 2 / 16, kPer = (kPieces + kThreads - 1) / kThreads;
+    uint4 v[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = tid + k * kThreads, row = i >> 4;
+      v[k] = make_uint4(0u, 0u, 0u, 0u);
+      if (i < kPieces && row < nrows) {
+        const int tok = t0 + row / p.G, h = kvh * p.G + row % p.G;
+        v[k] = *reinterpret_cast<const uint4*>(p.q + ((int64_t)tok * p.Hq + h) * kD + (i & 15) * 8);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = tid + k * kThreads;
+      if (i < kPieces) *reinterpret_cast<uint4*>(qrows + i * 16) = v[k];
+    }
+  }
+  __syncthreads();
+
   // ---- q1 = U q of the rows, scaled by qk_scale and a per-row power of two,
   // as hi + lo fp16 halves in the K-major A layout of QK^T: (row, d) at
   // (row/8)*2048 + (d/8)*128 + (row%8)*16 + (d%8)*2, the lo halves 32 KB on
@@ -364,10 +389,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     lane_quats_r<4>(rp, lane, qtr);
     const bool so4 = rot_so4(rp), pair = rot_pair(rp);
     for (int row = warp; row < kRows; row += kThreads / 32) {
-      float x[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      if (row < nrows) {
-        const int tok = t0 + row / p.G, h = kvh * p.G + row % p.G;
-        const uint2 raw = *reinterpret_cast<const uint2*>(p.q + ((int64_t)tok * p.Hq + h) * kD + lane * 4);
+      float x[4];
+      {   // zeros for the rows past the unit's (staged as zeros)
+        const uint2 raw = *reinterpret_cast<const uint2*>(qrows + row * 256 + lane * 8);
         const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
         const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
         x[0] = a.x;

@@ -351,8 +351,9 @@ kvq3_status kvq3_decode_attn_noalloc(kvq3_rotation rot, const kvq3_cache_desc *d
  * [0, pos0 + i] of that sequence -- one decode step of the sequence cut
  * after its own position.  The positions must already be in the cache (e.g.
  * written by kvq3_write_chunk); seq_lens is not read.
- * q: device fp16 [n_q][Hq][d]; out: device fp32 [n_q][Hq][d]; sm_scale <= 0
- * means 1/sqrt(d); Hq a multiple of Hkv with Hq/Hkv <= 16.  Internally the
+ * q: device fp16 [n_q][Hq][d]; out: device fp32 [n_q][Hq][d]; both 16-byte
+ * aligned (else KVQ3_ERR_INVALID_ARG); sm_scale <= 0 means 1/sqrt(d); Hq a
+ * multiple of Hkv with Hq/Hkv <= 16.  Internally the
  * queries form tiles of up to 8 (query token, head) pairs per kv head; at
  * d = 128 with symmetric codes and blocks of 64, units of 128 such rows, a
  * long unit's keys split in 2 to 16 ranges (one per 8,192 keys) whose

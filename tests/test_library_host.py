@@ -159,6 +159,21 @@ def test_invalid_descriptions_rejected_on_host(K):
     assert st == 1
 
 
+def test_prefill_arguments_checked_on_host(K):
+    # q and out are read and written 16 bytes at a time: a null or misaligned
+    # pointer is refused before any launch
+    d = K.CacheDesc(128, 2, 64, 3, 1, 1e-6, 16, 1, 4, 0, 4)
+    c = K.Cache(256, None, 256)
+    rot = K.kvq3_rotation_create(128, 1)
+    try:
+        for q, out in ((258, 256), (264, 256), (256, 260), (256, 264), (0, 256), (256, 0)):
+            st = K.lib.kvq3_prefill_attn(rot, ctypes.byref(d), ctypes.byref(c), 0, 0, 4, ctypes.c_void_p(q), 8,
+                                         0.0, ctypes.c_void_p(out), ctypes.c_void_p(256), 1 << 20, None, None)
+            assert st == 1, (q, out)
+    finally:
+        K.kvq3_rotation_destroy(rot)
+
+
 def test_calibration_arguments_checked_on_host(K):
     # workspace: candidate quaternions (rounded up to 256 bytes) + fp64 errors
     d = K.CacheDesc(128, 1, 64, 3, K.SCALE_TYPES["f16"], 1e-6, 16, 1, 1, 0, 1)
